@@ -1,0 +1,521 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each pin is a value the pages print, a closed form, a library routine that a
+special case reduces to, an invariant, or brute force on tiny inputs.  The
+planted-mistake tests at the end compile altered copies of the oracle and show
+that each plausible mistake fails at least one of these pins.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import qsa_inputs as qi
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def widen(h):
+    return qi.bf16_bits_to_f32(np.asarray(h, np.uint16))
+
+
+# --------------------------------------------------------------------------
+# bf16 narrowing: reduces to torch's round-to-nearest-even cast
+# --------------------------------------------------------------------------
+
+def test_bf16_narrowing_matches_torch_cast(orc):
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 2**32, size=20000, dtype=np.uint64).astype(np.uint32)
+    vals = bits.view(np.float32)
+    vals = vals[np.isfinite(vals)]
+    # exact ties: low half exactly 0x8000 with both parities of the kept lsb
+    ties = (np.arange(2000, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    specials = np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, 3.4028235e38, 1e-40, -1e-45],
+                        np.float32)
+    for v in np.concatenate([vals[:5000], ties, specials]):
+        want = torch.tensor([v], dtype=torch.float32).to(torch.bfloat16).view(torch.int16)
+        assert orc.f32_to_bf16(v) == (int(want.item()) & 0xFFFF), v
+
+
+def test_bf16_narrowing_keeps_nan(orc):
+    h = orc.f32_to_bf16(float("nan"))
+    assert (h & 0x7F80) == 0x7F80 and (h & 0x007F) != 0
+
+
+# --------------------------------------------------------------------------
+# RoPE tables
+# --------------------------------------------------------------------------
+
+def test_rope_position_zero_is_identity(orc):
+    c, s = orc.rope_table(4)
+    assert np.all(c[0] == 0x3F80) and np.all(s[0] == 0)
+
+
+def test_rope_closed_form_angles(orc):
+    theta = 10000.0
+    c, s = orc.rope_table(300, theta)
+    for p in (1, 2, 3, 7, 100, 299):
+        for j in (0, 1, 5, 16, 31):
+            ang = p * theta ** (-(2 * j) / 64.0)
+            for tab, fn in ((c, math.cos), (s, math.sin)):
+                got = float(widen(tab[p, j]))
+                # bf16 keeps 8 significant bits: half an ulp is <= 2^-9 relative
+                assert abs(got - fn(ang)) <= 2.0**-8 * max(abs(fn(ang)), 2.0**-8) + 1e-6, (p, j)
+                assert tab[p, j] == tab[p, j + 32]
+
+
+def test_rope_unit_circle(orc):
+    c, s = orc.rope_table(4096, 10000.0)
+    cf, sf = widen(c).astype(np.float64), widen(s).astype(np.float64)
+    assert np.max(np.abs(cf**2 + sf**2 - 1.0)) < 2 * 2.0**-8
+
+
+def test_rope_theta_matters(orc):
+    c1, _ = orc.rope_table(64, 10000.0)
+    c2, _ = orc.rope_table(64, 1e7)
+    assert np.array_equal(c1[:, 0], c2[:, 0])        # inv_freq[0] = 1 for every theta
+    assert not np.array_equal(c1[:, 16], c2[:, 16])
+
+
+# --------------------------------------------------------------------------
+# Pooling
+# --------------------------------------------------------------------------
+
+def const_keys(n_blocks, value, stride=128):
+    k = np.zeros((4 * n_blocks, stride), np.uint16)
+    k[:, :128] = qi.to_bf16_bits(np.full((4 * n_blocks, 128), value, np.float32))
+    return k
+
+
+def test_pool_constant_vector_closed_form(orc):
+    """All four tokens = all-ones vector, w = 0, eps = 0: the normed key is all
+    ones; block 0 is unrotated and block b is rotated at its first token 4b:
+    out_i = bf16(c_i - s_i), out_{i+32} = bf16(c_i + s_i), out_{64..} = 1."""
+    nb = 40
+    c, s = orc.rope_table(4 * nb)
+    w = np.zeros(128, np.uint16)
+    out = orc.pool_blocks(const_keys(nb, 1.0), 128, 0, nb, w, c, s, 0.0)
+    assert np.all(out[0] == 0x3F80)
+    for b in range(nb):
+        cf = widen(c[4 * b, :32]).astype(np.float32)
+        sf = widen(s[4 * b, :32]).astype(np.float32)
+        assert np.array_equal(out[b, :32], qi.to_bf16_bits(cf - sf)), b
+        assert np.array_equal(out[b, 32:64], qi.to_bf16_bits(cf + sf)), b
+        assert np.all(out[b, 64:] == 0x3F80)
+
+
+def test_pool_weight_enters_as_one_plus_w(orc):
+    rng = np.random.default_rng(3)
+    w = qi.normal_bf16(rng, (128,), 0.1)
+    c, s = orc.rope_table(4)
+    out = orc.pool_blocks(const_keys(1, 1.0), 128, 0, 1, w, c, s, 0.0)
+    want = qi.to_bf16_bits(np.float32(1.0) + widen(w))
+    assert np.array_equal(out[0], want)
+
+
+def test_pool_eps_and_mean_closed_form(orc):
+    """Tiny keys make eps visible: constant 2^-10 keys, eps = 1e-6.
+    mean = 2^-10, ms = 2^-20, y = 2^-10 / sqrt(2^-20 + 1e-6)."""
+    c, s = orc.rope_table(4)
+    w = np.zeros(128, np.uint16)
+    out = orc.pool_blocks(const_keys(1, 2.0**-10), 128, 0, 1, w, c, s, 1e-6)
+    y = 2.0**-10 / math.sqrt(2.0**-20 + 1e-6)
+    want = qi.to_bf16_bits(np.array([y], np.float32))[0]
+    assert np.all(out[0] == want), (hex(out[0, 0]), hex(want))
+
+
+def test_pool_mean_of_distinct_tokens(orc):
+    """Tokens 3, 1, 0, 0 average to 1 on dims 64..127 (unrotated) and tokens
+    2, 2, 2, 2 give 2 on dims 0..63: with eps = 0, w = 0 the rms is
+    sqrt((64*1 + 64*4)/128) = sqrt(2.5)."""
+    k = np.zeros((4, 128), np.float32)
+    k[:, :64] = 2.0
+    k[0, 64:], k[1, 64:] = 3.0, 1.0
+    c, s = orc.rope_table(4)
+    out = orc.pool_blocks(qi.to_bf16_bits(k), 128, 0, 1, np.zeros(128, np.uint16), c, s, 0.0)
+    r = 1.0 / math.sqrt(2.5)
+    assert np.all(out[0, 64:] == qi.to_bf16_bits(np.array([r], np.float32))[0])
+    assert np.all(out[0, :64] == qi.to_bf16_bits(np.array([2 * r], np.float32))[0])
+
+
+def test_pool_power_of_two_scale_invariance(orc):
+    rng = np.random.default_rng(11)
+    keys = qi.raw_keys(rng, 4 * 64)
+    w = qi.normal_bf16(rng, (128,), 0.1)
+    c, s = orc.rope_table(4 * 64)
+    a = orc.pool_blocks(keys, 128, 0, 64, w, c, s, 0.0)
+    for k in (-6, 3):
+        scaled = qi.to_bf16_bits(widen(keys) * np.float32(2.0**k))
+        b = orc.pool_blocks(scaled, 128, 0, 64, w, c, s, 0.0)
+        assert np.array_equal(a, b)
+
+
+def test_pool_unit_rms_and_rotation_preserves_pair_norms(orc):
+    rng = np.random.default_rng(12)
+    nb = 256
+    keys = qi.raw_keys(rng, 4 * nb, token_scale=True)
+    c, s = orc.rope_table(4 * nb)
+    out = widen(orc.pool_blocks(keys, 128, 0, nb, np.zeros(128, np.uint16), c, s, 1e-6))
+    out = out.astype(np.float64)
+    rms = np.sqrt(np.mean(out**2, axis=1))
+    assert np.all(np.abs(rms - 1.0) < 0.02)
+    # unrotated copy: block 0 of each key group pooled at position 0 has no rotation
+    pair_rot = out[:, :32] ** 2 + out[:, 32:64] ** 2
+    un = np.zeros_like(out)
+    for b in range(nb):
+        kb = keys[4 * b:4 * b + 4]
+        un[b] = widen(orc.pool_blocks(kb, 128, 0, 1, np.zeros(128, np.uint16), c, s, 1e-6)[0])
+    pair_un = un[:, :32] ** 2 + un[:, 32:64] ** 2
+    assert np.allclose(pair_rot, pair_un, rtol=0.03, atol=1e-3)
+    assert np.array_equal(out[:, 64:], un[:, 64:])
+
+
+def test_pool_stride_and_offset_indexing(orc):
+    """The fused q|k layout (stride 640, key at column 512) and a compact copy give
+    the same keys; pooling [f, f+n) from token 4f equals that slice of a full pool."""
+    rng = np.random.default_rng(13)
+    T = 4 * 48
+    fq = qi.fused_qk(rng, T)
+    kw = qi.normal_bf16(rng, (128,), 0.1)
+    c, s = orc.rope_table(T)
+    compact = np.ascontiguousarray(fq[:, 512:640])
+    full = orc.pool_blocks(compact, 128, 0, 48, kw, c, s, 1e-6)
+    fused = orc.pool_blocks(fq.reshape(-1)[512:], 640, 0, 48, kw, c, s, 1e-6)
+    assert np.array_equal(full, fused)
+    part = orc.pool_blocks(compact[4 * 17:], 128, 17, 9, kw, c, s, 1e-6, total_blocks=48)
+    assert np.array_equal(part[17:26], full[17:26])
+    assert np.all(part[:17] == 0) and np.all(part[26:] == 0)
+
+
+# --------------------------------------------------------------------------
+# Scoring
+# --------------------------------------------------------------------------
+
+def onehot_q(dims, signs=(1, 1, 1, 1)):
+    q = np.zeros((4, 128), np.float32)
+    for h, (d, sg) in enumerate(zip(dims, signs)):
+        q[h, d] = sg
+    return qi.to_bf16_bits(q)
+
+
+def test_score_onehot_closed_form(orc):
+    rng = np.random.default_rng(21)
+    keys = qi.normal_bf16(rng, (50, 128))
+    kf = widen(keys).astype(np.float64)
+    dims = (3, 77, 0, 127)
+    got = orc.score_row(onehot_q(dims), keys, 50)
+    want = sum(np.maximum(kf[:, d], 0.0) for d in dims) / math.sqrt(128.0)
+    assert np.allclose(got, want, rtol=1e-6, atol=0)
+
+
+def test_score_relu_is_per_head(orc):
+    """Head 1 is the negation of head 0: per-head relu gives |k_d|, a relu after
+    the head sum would give 0."""
+    rng = np.random.default_rng(22)
+    keys = qi.normal_bf16(rng, (64, 128))
+    kf = widen(keys).astype(np.float64)
+    q = onehot_q((5, 5, 9, 9), (1, -1, 1, -1))
+    got = orc.score_row(q, keys, 64)
+    want = (np.abs(kf[:, 5]) + np.abs(kf[:, 9])) / math.sqrt(128.0)
+    assert np.allclose(got, want, rtol=1e-6)
+    assert np.all(got > 0)
+
+
+def test_score_zero_query_and_power_of_two_linearity(orc):
+    rng = np.random.default_rng(23)
+    keys = qi.normal_bf16(rng, (80, 128))
+    q = qi.normal_bf16(rng, (4, 128))
+    assert np.all(orc.score_row(np.zeros((4, 128), np.uint16), keys, 80) == 0)
+    a = orc.score_row(q, keys, 80)
+    b = orc.score_row(qi.to_bf16_bits(widen(q) * 2), keys, 80)
+    assert np.array_equal(b, a * 2)
+
+
+def test_score_all_negative_heads_give_zero(orc):
+    rng = np.random.default_rng(24)
+    keys = np.abs(widen(qi.normal_bf16(rng, (30, 128)))) + 0.01
+    q = -np.abs(widen(qi.normal_bf16(rng, (4, 128)))) - 0.01
+    got = orc.score_row(qi.to_bf16_bits(q), qi.to_bf16_bits(keys), 30)
+    assert np.all(got == 0)
+
+
+def test_score_nan_propagates(orc):
+    rng = np.random.default_rng(25)
+    keys = qi.normal_bf16(rng, (10, 128))
+    keys[4, 17] = 0x7FC0
+    got = orc.score_row(qi.normal_bf16(rng, (4, 128)), keys, 10)
+    assert np.isnan(got[4]) and np.all(np.isfinite(np.delete(got, 4)))
+
+
+def test_score_rows_prefix_sentinel_and_key_base(orc):
+    rng = np.random.default_rng(26)
+    T = 64
+    fq = qi.fused_qk(rng, T)
+    qw, kw = qi.norm_weights(rng)
+    c, s = orc.rope_table(T)
+    keys = orc.pool_blocks(np.ascontiguousarray(fq[:, 512:]), 128, 0, T // 4, kw, c, s, 1e-6)
+    cols = 20
+    pos = np.array([0, 3, 4, 40, 63, 62], np.int32)
+    vis = np.array([1, 4, 2, 41, 60, 0], np.int32)
+    sc = np.full((len(pos), cols), -7.0, np.float32)
+    rc, _ = orc.score_rows(fq, 640, pos, len(pos), T, qw, c, s, 1e-6, keys, sc, cols,
+                           visible_len=vis)
+    assert rc == 0
+    for i, (p, v) in enumerate(zip(pos, vis)):
+        n = v // 4
+        assert np.all(sc[i, n:] == -7.0)
+        qp = orc.qprep(fq[i, :512], p, qw, c, s, 1e-6)
+        assert np.array_equal(sc[i, :n], orc.score_row(qp, keys, n))
+    # key_base: row i reads its own key set
+    keys2 = np.concatenate([np.zeros((5, 128), np.uint16), keys])
+    sc2 = np.full((len(pos), cols), -7.0, np.float32)
+    rc, _ = orc.score_rows(fq, 640, pos, len(pos), T, qw, c, s, 1e-6, keys2, sc2, cols,
+                           visible_len=vis, key_base=np.full(len(pos), 5, np.int64))
+    assert rc == 0 and np.array_equal(sc, sc2)
+
+
+def test_score_rows_range_errors(orc):
+    T = 16
+    c, s = orc.rope_table(T)
+    z = np.zeros(128, np.uint16)
+    fq = np.zeros((3, 640), np.uint16)
+    keys = np.zeros((4, 128), np.uint16)
+    sc = np.zeros((3, 4), np.float32)
+    for pos, vis, bad in (([0, 16, 1], None, 1), ([0, -1, 1], None, 1), ([0, 5, 1], [1, 7, 1], 1)):
+        rc, row = orc.score_rows(fq, 640, np.array(pos, np.int32), 3, T, z, c, s, 1e-6, keys, sc, 4,
+                                 visible_len=None if vis is None else np.array(vis, np.int32))
+        assert rc == 3 and row == bad
+
+
+# --------------------------------------------------------------------------
+# Selection: brute force, an independent radix select, closed forms, invariants
+# --------------------------------------------------------------------------
+
+def brute_force_mask(scores, p, tokens, budget):
+    """O(n^2): block b is kept iff fewer than K blocks precede it in the
+    canonical order (higher score, or equal score and lower index)."""
+    n, tail = (p + 1) // 4, (p + 1) % 4
+    K = min(budget // 4, n)
+    v = [0.0 if x == 0 else float(x) for x in scores[:n]]
+    m = np.zeros(tokens, np.uint8)
+    for b in range(n):
+        rank = sum(1 for c in range(n) if v[c] > v[b] or (v[c] == v[b] and c < b))
+        if rank < K:
+            m[4 * b:4 * b + 4] = 1
+    m[4 * n:p + 1] = 1
+    return m
+
+
+def radix_mask(scores, p, tokens, budget):
+    """Independent algorithm: 8-bit MSD radix select over order-preserving u32 keys."""
+    n = (p + 1) // 4
+    K = min(budget // 4, n)
+    s = np.asarray(scores[:n], np.float32).copy()
+    s[s == 0] = 0.0
+    u = s.view(np.uint32).astype(np.uint64)
+    key = np.where(u >> 31 == 1, (~u) & 0xFFFFFFFF, u | 0x80000000).astype(np.uint64)
+    prefix, need = 0, K
+    for shift in (24, 16, 8, 0):
+        hi = key >> (shift + 8)
+        cand = (hi == prefix) if shift < 24 else np.ones(n, bool)
+        digit = (key >> shift) & 0xFF
+        cnt = np.bincount(digit[cand].astype(np.int64), minlength=256)
+        above = 0
+        for d in range(255, -1, -1):
+            if above + cnt[d] >= need:
+                break
+            above += cnt[d]
+        need -= above
+        prefix = (prefix << 8) | d
+    kept = key > prefix
+    eq = np.nonzero(key == prefix)[0][:need]
+    kept[eq] = True
+    m = np.zeros(tokens, np.uint8)
+    for b in np.nonzero(kept)[0]:
+        m[4 * b:4 * b + 4] = 1
+    m[4 * n:p + 1] = 1
+    return m
+
+
+def test_select_exhaustive_tiny_rows(orc):
+    alphabet = [-0.0, 0.0, 1.0, 2.0, -1.0]
+    for n in range(1, 6):
+        for combo in itertools.product(alphabet, repeat=n):
+            s = np.array(combo, np.float32)
+            for tail in (0, 3):
+                p = 4 * n - 1 + tail
+                if tail == 3:
+                    p = 4 * n + 2
+                for budget in (4, 8, 12):
+                    got, rc = orc.select_row(s, p, p + 3, budget)
+                    assert rc == 0
+                    assert np.array_equal(got, brute_force_mask(s, p, p + 3, budget)), (combo, p, budget)
+
+
+def test_select_random_small_rows_vs_brute_force_and_radix(orc):
+    rng = np.random.default_rng(31)
+    for trial in range(300):
+        n = int(rng.integers(1, 13))
+        p = 4 * n - 1 + int(rng.integers(0, 4))
+        tokens = p + 1 + int(rng.integers(0, 9))
+        s = rng.choice(np.array([-0.0, 0.0, 0.5, 1.0, 1.0, 2.0, 3.5], np.float32), size=n)
+        s = s + (rng.random(n) < 0.3) * rng.standard_normal(n).astype(np.float32)
+        s = s.astype(np.float32)
+        budget = 4 * int(rng.integers(1, 15))
+        got, rc = orc.select_row(s, p, tokens, budget)
+        assert rc == 0
+        assert np.array_equal(got, brute_force_mask(s, p, tokens, budget))
+        if n > budget // 4:
+            assert np.array_equal(got, radix_mask(s, p, tokens, budget))
+
+
+def test_select_long_rows_vs_independent_radix(orc):
+    rng = np.random.default_rng(32)
+    for n, budget in ((513, 2048), (2048, 2048), (5000, 2044), (4000, 4), (3000, 512)):
+        s = qi.stress_scores(rng, 1, n)[0]
+        p = 4 * n - 1 + int(rng.integers(0, 4))
+        got, rc = orc.select_row(s, p, p + 1, budget)
+        assert rc == 0
+        assert np.array_equal(got, radix_mask(s, p, p + 1, budget))
+
+
+def test_select_invariants(orc):
+    rng = np.random.default_rng(33)
+    tokens = 9000
+    for trial in range(40):
+        p = int(rng.integers(0, tokens))
+        budget = 4 * int(rng.integers(1, 513))
+        n, tail = (p + 1) // 4, (p + 1) % 4
+        s = qi.stress_scores(rng, 1, max(n, 1), zero_frac=0.4, levels=16)[0]
+        m, rc = orc.select_row(s, p, tokens, budget)
+        assert rc == 0
+        K = min(budget // 4, n)
+        assert int(m.sum()) == 4 * K + tail                      # closed form
+        assert np.all(m[p + 1:] == 0)                             # causality
+        assert np.all(m[4 * n:p + 1] == 1)                        # the tail
+        blk = m[:4 * n].reshape(n, 4) if n else np.zeros((0, 4))
+        assert np.all((blk.min(1) == blk.max(1)))                  # whole blocks only
+        kept = blk[:, 0] == 1 if n else np.zeros(0, bool)
+        if n > budget // 4:
+            sv = np.where(s[:n] == 0, 0.0, s[:n])
+            assert sv[kept].min() >= sv[~kept].max()              # kept >= dropped
+            cut = sv[kept].min()
+            eqi = np.nonzero(sv == cut)[0]
+            k_eq = kept[eqi]
+            assert np.all(k_eq[:k_eq.sum()]) and not np.any(k_eq[k_eq.sum():])  # tie prefix
+        else:
+            assert np.all(m[:p + 1] == 1)                         # all-kept prefix
+
+
+def test_select_signed_zero_ties(orc):
+    # blocks: 5, -0, +0, -0, +0 ; keep 3 -> 5 and the two lowest-index zeros (1, 2)
+    s = np.array([5.0, -0.0, 0.0, -0.0, 0.0], np.float32)
+    m, rc = orc.select_row(s, 19, 20, 12)
+    assert rc == 0
+    assert list(m.reshape(5, 4)[:, 0]) == [1, 1, 1, 0, 0]
+    s = np.array([0.0, -0.0, 5.0, 0.0, -0.0], np.float32)
+    m, _ = orc.select_row(s, 19, 20, 12)
+    assert list(m.reshape(5, 4)[:, 0]) == [1, 1, 1, 0, 0]
+
+
+def test_select_nonfinite_and_range(orc):
+    s = np.array([1.0, np.nan, 2.0, 3.0], np.float32)
+    m, rc = orc.select_row(s, 15, 16, 4)
+    assert rc == 4 and np.all(m == 0xAB)                      # row untouched
+    m, rc = orc.select_row(s, 15, 16, 16)                     # all-kept: reads no score
+    assert rc == 0 and np.all(m == 1)
+    s = np.array([1.0, np.inf, 2.0, 3.0], np.float32)
+    assert orc.select_row(s, 15, 16, 8)[1] == 4
+    assert orc.select_row(s, 16, 16, 8)[1] == 3
+    assert orc.select_row(s, -1, 16, 8)[1] == 3
+    for bad in (0, -4, 6, 2052):
+        assert orc.select_row(s, 3, 16, bad)[1] == 1
+
+
+def test_select_golden_geometry(orc):
+    """Block counts, keep and mask length that the pages print (see the fixture)."""
+    rows = []
+    with open(os.path.join(GOLDEN, "select_geometry.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append([int(x) for x in line.split()[:6]])
+    assert len(rows) == 7
+    rng = np.random.default_rng(34)
+    for p, budget, blocks, tail, keep, ones in rows:
+        s = rng.standard_normal(blocks).astype(np.float32)
+        m, rc = orc.select_row(s, p, p + 1, budget)
+        assert rc == 0
+        assert (p + 1) // 4 == blocks and (p + 1) % 4 == tail
+        assert int(m.sum()) == ones == 4 * keep + tail
+        if blocks > keep:
+            kept = np.nonzero(m[:4 * blocks:4])[0]
+            top = np.argsort(-s, kind="stable")[:keep]
+            assert np.array_equal(np.sort(top), kept)
+
+
+# --------------------------------------------------------------------------
+# Planted mistakes: each altered copy of the oracle must fail a pin above
+# --------------------------------------------------------------------------
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "qsa_oracle.c")
+
+MUTANTS = {
+    "drop_tail": ("mask_row[t] = 1;", "(void)t;"),
+    "keep_one_fewer": ("for (int32_t i = 0; i < keep; ++i)", "for (int32_t i = 0; i < keep - 1; ++i)"),
+    "keep_one_more": ("for (int32_t i = 0; i < keep; ++i)", "for (int32_t i = 0; i <= keep && i < blocks; ++i)"),
+    "invert_order": ("if (a->v > b->v)\n        return -1;", "if (a->v < b->v)\n        return -2;"),
+    "ties_descending_index": ("return (a->b < b->b) ? -1 : (a->b > b->b);", "return (a->b > b->b) ? -1 : (a->b < b->b);"),
+    "ignore_causality": ("memset(mask_row, 1, (size_t)p + 1);", "memset(mask_row, 1, (size_t)tokens);"),
+    "relu_after_sum": [("float s = ((rl[0] + rl[1]) + rl[2]) + rl[3];",
+                        "float s = orc_relu(((rl[0] + rl[1]) + rl[2]) + rl[3]);"),
+                       ("rl[h] = orc_relu((float)acc);", "rl[h] = (float)acc;")],
+    "no_relu": ("rl[h] = orc_relu((float)acc);", "rl[h] = (float)acc;"),
+    "rope_at_block_end": ("(int64_t)ORC_RATIO * b, cos_t", "(int64_t)ORC_RATIO * b + 3, cos_t"),
+    "rope_sign_flip": ("out[i] = orc_narrow(a - b);", "out[i] = orc_narrow(a + b);"),
+    "rope_pairs_wrong": ("float x2 = n[i + ORC_HALF];", "float x2 = n[i + 64];"),
+    "weight_w_not_1pw": ("float gain = 1.0f + orc_widen(w[d]);", "float gain = orc_widen(w[d]);"),
+    "pool_by_sum": ("float mean = (float)acc * 0.25f;", "float mean = (float)acc;"),
+    "drop_eps": ("float r = 1.0f / sqrtf(ms + eps);", "float r = 1.0f / sqrtf(ms);"),
+    "no_scale": ("out[b] = (float)((double)s / root);", "out[b] = s;"),
+    "wrong_head_offset": ("orc_widen(q_prepped[h * ORC_HD + d])", "orc_widen(q_prepped[d])"),
+    "transposed_key": ("* (double)orc_widen(k[d]);", "* (double)orc_widen(block_keys[(int64_t)d * ORC_HD + b]);"),
+    "stride_ignored": ("acc += (double)orc_widen(k0[(int64_t)t * key_stride + d]);",
+                       "acc += (double)orc_widen(k0[(int64_t)t * ORC_HD + d]);"),
+    "cos_sin_swapped": ("float c = orc_widen(crow[i]);", "float c = orc_widen(srow[i]);"),
+}
+
+# the pins that must catch the mistakes (each mutant must fail at least one)
+PIN_TESTS = [
+    test_select_exhaustive_tiny_rows, test_select_invariants, test_select_signed_zero_ties,
+    test_select_golden_geometry, test_pool_constant_vector_closed_form,
+    test_pool_weight_enters_as_one_plus_w, test_pool_eps_and_mean_closed_form,
+    test_pool_mean_of_distinct_tokens, test_pool_stride_and_offset_indexing,
+    test_score_onehot_closed_form, test_score_relu_is_per_head,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    import oracle
+
+    edits = MUTANTS[name]
+    if isinstance(edits, tuple):
+        edits = [edits]
+    src = open(SRC).read()
+    for before, after in edits:
+        assert src.count(before) == 1, f"mutation anchor for {name} not unique"
+        src = src.replace(before, after)
+    path = tmp_path / f"mut_{name}.c"
+    path.write_text(src)
+    lib = oracle.load_from(oracle.compile_shared(str(path), str(tmp_path / f"mut_{name}.so")))
+    mutant = oracle.Oracle(lib)
+    caught = []
+    for pin in PIN_TESTS:
+        try:
+            pin(mutant)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"planted mistake {name} passed every pin"

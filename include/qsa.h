@@ -1,0 +1,203 @@
+/*
+ * qsa.h -- C ABI of libqsa.so, the GB300 (sm_103a) QSA token-indexer hot path.
+ *
+ * The QSA token indexer (pegainfer PR #1160 "score QSA token-indexer blocks in
+ * native CUDA" and PR #1178 "select QSA indexer blocks"; metrale layers/qsa.rs)
+ * turns a sequence's raw indexer keys and its query rows into a per-row u8
+ * visibility mask in three steps:
+ *
+ *   1. pool   -- each complete 4-token block of raw bf16 keys becomes one block
+ *                key: f32 mean -> bf16 -> (1 + w) RMSNorm -> bf16 -> partial
+ *                RoPE (first 64 of 128 dims) at the block's first token -> bf16;
+ *   2. score  -- S[r, b] = sum_h relu(q_h . k_b) / sqrt(128) over 4 query heads,
+ *                each head prepared like a key (norm with q_norm_w, RoPE at the
+ *                row's own position);
+ *   3. select -- per row at position p: blocks = (p+1)/4, tail = (p+1)%4,
+ *                keep = min(budget/4, blocks); the kept blocks are the `keep`
+ *                highest scores under the order (score descending, block index
+ *                ascending, -0.0 == +0.0); the mask is 1 on their 4 tokens each
+ *                and on the tail [4*blocks, p], 0 on every other byte of the row.
+ *
+ * Fixed geometry: 4 query heads, head dim 128, ratio 4, rotary dim 64.
+ *
+ * Conventions shared by every entry point
+ *  - bf16 values travel as uint16_t bit patterns (the upper half of an f32).
+ *  - Pointers marked DEVICE are CUDA device (or managed) pointers owned by the
+ *    caller; the library allocates nothing and frees nothing.  `stream` is a
+ *    cudaStream_t (NULL = the legacy default stream); every launch is
+ *    stream-ordered and asynchronous.
+ *  - Arguments are validated on the host before any launch.  A refusal returns
+ *    QSA_ERR_INVALID_VALUE and launches nothing.  Refused: negative extents,
+ *    NULL pointers with a non-empty extent, pointers or row strides not
+ *    16-byte aligned where the comment says so, a budget that is not a positive
+ *    multiple of 4 keeping at most 512 blocks, score_cols below tokens/4,
+ *    RoPE tables shorter than the positions a call can read, eps < 0 or NaN,
+ *    and size products that overflow.
+ *  - An empty launch (no rows, no tokens or no blocks) is a no-op returning
+ *    QSA_OK.
+ *  - Errors that only the device can see (a row position outside [0, tokens),
+ *    a visible length outside [0, p+1], a non-finite score inside a
+ *    truncating row's block prefix) do not trap: the kernel records the first
+ *    one in the caller's status word and leaves that row's output untouched.
+ *    dev_status is a DEVICE int32_t[2] = {code, row}; it must be zero before
+ *    the call (qsa_reset_status) and is read with qsa_read_status.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_VALUE = 1, /* refused on the host; nothing launched */
+    QSA_ERR_LAUNCH = 2,        /* the CUDA runtime refused a launch */
+    QSA_ERR_ROW_RANGE = 3,     /* device: pos or visible_len out of range */
+    QSA_ERR_NONFINITE = 4,     /* device: NaN/Inf score in a truncating row */
+    QSA_ERR_TIMEOUT = 5        /* device: a bounded wait gave up */
+} qsa_status;
+
+/* Which scorer qsa_score_rows_with runs. */
+typedef enum {
+    QSA_SCORE_AUTO = 0,   /* host picks: tensor cores for many rows sharing one key set */
+    QSA_SCORE_SIMT = 1,   /* bandwidth-bound warp-dot scorer (decode shape, any rows) */
+    QSA_SCORE_TCGEN05 = 2 /* tcgen05/TMEM/TMA tile scorer; needs key_base == NULL */
+} qsa_score_path;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t qsa_version(void);
+
+/* Short text for a status code (static storage). */
+const char *qsa_status_string(int32_t status);
+
+/*
+ * RoPE cos/sin tables, HOST memory, built on the CPU (no device work).
+ * Source: PR #1160 review ("read the cos and sin table that the rope module
+ * builds"): the indexer rotates with the same position embeddings as attention,
+ * so the tables are inputs of every rotating call.
+ * Row p (p < max_pos) of each table is 64 bf16 values [v_0..v_31, v_0..v_31]
+ * with v_j = bf16(f32(cos/sin(f32(p * f32(1 / theta^(2j/64)))))).
+ * cos_out, sin_out: HOST uint16_t[max_pos * 64], caller-owned.
+ * Refuses max_pos < 0, theta <= 0 or non-finite, NULL outputs with max_pos > 0.
+ */
+qsa_status qsa_rope_tables(int32_t max_pos, double theta, uint16_t *cos_out, uint16_t *sin_out);
+
+/*
+ * Pool blocks [first_block, first_block + n_blocks) into block keys.
+ * Source: PR #1160 description (block keys: raw keys averaged in float32, cast
+ * back to bf16, (1 + w) RMSNorm, partial RoPE at the block's first token);
+ * metrale layers/qsa.rs pool_new_blocks (only newly complete blocks).
+ *  keys        DEVICE bf16; the raw key of token 4*first_block + t is the 128
+ *              values at keys + t*key_stride, t < 4*n_blocks.  16-byte aligned;
+ *              key_stride >= 128 and a multiple of 8 (640 reads a fused q|k
+ *              row buffer offset to column 512; 128 reads a compact key cache).
+ *  k_norm_w    DEVICE bf16[128], 16-byte aligned; the norm weight is 1 + w.
+ *  cos_t/sin_t DEVICE bf16[table_rows * 64] from qsa_rope_tables, 16-byte
+ *              aligned; table_rows must exceed 4*(first_block + n_blocks - 1).
+ *  eps         RMSNorm epsilon (>= 0).
+ *  block_keys  DEVICE bf16 key cache; block b is written to block_keys + b*128.
+ *              16-byte aligned.  Nothing else is written.
+ */
+qsa_status qsa_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t first_block,
+                           int32_t n_blocks, const uint16_t *k_norm_w, const uint16_t *cos_t,
+                           const uint16_t *sin_t, int32_t table_rows, float eps,
+                           uint16_t *block_keys, void *stream);
+
+/*
+ * Score query rows against block keys.
+ * Source: PR #1160 description (sum_h relu(q_h . k_b) / sqrt(indexer_head_dim),
+ * relu per head before the head sum, written as a comparison so a NaN stays
+ * NaN; rows/visible_len as separate device arrays; only the visible prefix of
+ * each score row is written, the rest is left untouched).
+ *  q           DEVICE bf16; row i's four query heads are the 512 values at
+ *              q + i*q_stride (q_stride >= 512, multiple of 8; 640 for a fused
+ *              q|k buffer).  16-byte aligned.
+ *  pos         DEVICE int32[n_rows]: row i's position p (0 <= p < tokens).
+ *  visible_len DEVICE int32[n_rows] or NULL (= p + 1): the row sees its first
+ *              visible_len tokens, so blocks = visible_len / 4.
+ *  tokens      positions are < tokens.
+ *  q_norm_w    DEVICE bf16[128] query norm weight (used as 1 + w).
+ *  cos_t/sin_t DEVICE RoPE tables with table_rows >= tokens.
+ *  block_keys  DEVICE bf16 pooled keys; row i reads block b at
+ *              block_keys + (key_base[i] + b)*128.  16-byte aligned.
+ *  key_base    DEVICE int64[n_rows] or NULL (= 0): per-row block offset, so one
+ *              call can score rows of different sequences.
+ *  scores      DEVICE f32, row stride score_cols (>= tokens/4, multiple of 4;
+ *              spare capacity allowed), 16-byte aligned.  Row i gets entries
+ *              b < blocks; entries past that are not written.
+ *  dev_status  DEVICE int32[2] status word (see above).
+ * qsa_score_rows picks the scorer itself (QSA_SCORE_AUTO).
+ */
+qsa_status qsa_score_rows(const uint16_t *q, int64_t q_stride, const int32_t *pos,
+                          const int32_t *visible_len, int32_t n_rows, int32_t tokens,
+                          const uint16_t *q_norm_w, const uint16_t *cos_t, const uint16_t *sin_t,
+                          int32_t table_rows, float eps, const uint16_t *block_keys,
+                          const int64_t *key_base, float *scores, int64_t score_cols,
+                          int32_t *dev_status, void *stream);
+
+/* qsa_score_rows with an explicit scorer; QSA_SCORE_TCGEN05 refuses key_base != NULL. */
+qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_t *pos,
+                               const int32_t *visible_len, int32_t n_rows, int32_t tokens,
+                               const uint16_t *q_norm_w, const uint16_t *cos_t,
+                               const uint16_t *sin_t, int32_t table_rows, float eps,
+                               const uint16_t *block_keys, const int64_t *key_base,
+                               float *scores, int64_t score_cols, int32_t *dev_status,
+                               int32_t path, void *stream);
+
+/*
+ * Exact top-(budget/4) block selection into a u8 visibility mask.
+ * Source: PR #1178 "Exact semantics" (blocks, tail, keep; canonical order
+ * descending score then ascending block index; threshold-equal blocks fill the
+ * remaining slots in block order; -0.0 ties +0.0; the tail is always visible;
+ * a row with blocks <= budget/4 writes its whole visible prefix; a non-finite
+ * score in a truncating row's prefix is an error; explicit score_cols).
+ *  scores      DEVICE f32, row i at scores + i*score_cols, 16-byte aligned,
+ *              score_cols >= tokens/4 and a multiple of 4.  Only entries
+ *              b < (pos[i]+1)/4 are read, and none for rows under the budget.
+ *  pos         DEVICE int32[n_rows].
+ *  budget      positive multiple of 4, budget/4 <= 512.
+ *  mask        DEVICE u8[n_rows * tokens]; row i at mask + i*tokens (any
+ *              alignment).  Every byte of a valid row is written.
+ */
+qsa_status qsa_select_mask(const float *scores, int64_t score_cols, const int32_t *pos,
+                           int32_t n_rows, int32_t tokens, int32_t budget, uint8_t *mask,
+                           int32_t *dev_status, void *stream);
+
+/*
+ * The whole hot path on one stream: pool the newly complete blocks, score the
+ * rows, select.  Source: metrale layers/qsa.rs decode_select (ingest -> pool
+ * new blocks -> prepare q -> score -> top-k -> expand with the tail), with the
+ * host sort replaced by the on-device selection of PR #1178.
+ *  keys, key_stride, pool_first_block, pool_n_blocks, k_norm_w: as
+ *              qsa_pool_blocks (pool_n_blocks == 0 pools nothing);
+ *  q, q_stride, pos, n_rows, tokens, q_norm_w: as qsa_score_rows (every row
+ *              sees p + 1 tokens and reads block_keys from offset 0);
+ *  cos_t, sin_t, table_rows, eps: shared by pool and score;
+ *  budget, mask: as qsa_select_mask;
+ *  block_keys  DEVICE pooled-key cache (read and written);
+ *  scores      DEVICE f32 work buffer of n_rows * score_cols (its contents
+ *              afterwards are the rows' scores).
+ */
+qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t pool_first_block,
+                            int32_t pool_n_blocks, const uint16_t *k_norm_w, const uint16_t *q,
+                            int64_t q_stride, const int32_t *pos, int32_t n_rows, int32_t tokens,
+                            const uint16_t *q_norm_w, const uint16_t *cos_t,
+                            const uint16_t *sin_t, int32_t table_rows, float eps, int32_t budget,
+                            uint16_t *block_keys, float *scores, int64_t score_cols,
+                            uint8_t *mask, int32_t *dev_status, void *stream);
+
+/* Zero a DEVICE status word (stream-ordered). */
+qsa_status qsa_reset_status(int32_t *dev_status, void *stream);
+
+/* Copy a DEVICE status word to the host; synchronises `stream` first. */
+qsa_status qsa_read_status(const int32_t *dev_status, void *stream, int32_t *host_code,
+                           int32_t *host_row);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

@@ -1,0 +1,191 @@
+"""GB300-native QSA token indexer: pool -> score -> select, behind libqsa.so.
+
+This package is a thin ctypes binding over the C ABI declared in
+``include/qsa.h``.  Every function has the C entry point's name and argument
+order; device buffers are passed as CUDA torch tensors (their data pointers),
+``stream`` is a torch CUDA stream (default: the current stream).  The binding
+only marshals arguments: all work runs in the library's CUDA kernels.  There is
+no CPU fallback: importing the package fails loudly when libqsa.so is missing
+(build it with ``python -m sparse_attention_token_qsa_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqsa.so")
+
+QSA_OK = 0
+QSA_ERR_INVALID_VALUE = 1
+QSA_ERR_LAUNCH = 2
+QSA_ERR_ROW_RANGE = 3
+QSA_ERR_NONFINITE = 4
+QSA_ERR_TIMEOUT = 5
+
+QSA_SCORE_AUTO = 0
+QSA_SCORE_SIMT = 1
+QSA_SCORE_TCGEN05 = 2
+
+HEADS, HEAD_DIM, RATIO, ROT_DIM, FUSED_WIDTH = 4, 128, 4, 64, 640
+
+EXPORTED = ("qsa_version", "qsa_status_string", "qsa_rope_tables", "qsa_pool_blocks",
+            "qsa_score_rows", "qsa_score_rows_with", "qsa_select_mask", "qsa_index_select",
+            "qsa_reset_status", "qsa_read_status")
+
+
+class QsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: status {code} ({status_string(code)})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libqsa.so is not built ({LIB_PATH}); run "
+                          "`python -m sparse_attention_token_qsa_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, f64 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_double)
+    sig = {
+        "qsa_version": ([], i32),
+        "qsa_status_string": ([i32], ctypes.c_char_p),
+        "qsa_rope_tables": ([i32, f64, P, P], i32),
+        "qsa_pool_blocks": ([P, i64, i32, i32, P, P, P, i32, f32, P, P], i32),
+        "qsa_score_rows": ([P, i64, P, P, i32, i32, P, P, P, i32, f32, P, P, P, i64, P, P], i32),
+        "qsa_score_rows_with": ([P, i64, P, P, i32, i32, P, P, P, i32, f32, P, P, P, i64, P, i32, P],
+                                i32),
+        "qsa_select_mask": ([P, i64, P, i32, i32, i32, P, P, P], i32),
+        "qsa_index_select": ([P, i64, i32, i32, P, P, i64, P, i32, i32, P, P, P, i32, f32, i32, P, P,
+                              i64, P, P, P], i32),
+        "qsa_reset_status": ([P, P], i32),
+        "qsa_read_status": ([P, P, P, P], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return _lib.qsa_status_string(int(code)).decode()
+
+
+def _dev(t: torch.Tensor | None, name: str):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor: libqsa has no CPU path")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != QSA_OK:
+        raise QsaError(rc, where)
+
+
+def qsa_version() -> int:
+    return int(_lib.qsa_version())
+
+
+def qsa_rope_tables(max_pos: int, theta: float = 10000.0) -> tuple[np.ndarray, np.ndarray]:
+    """Host cos/sin tables [max_pos, 64] as uint16 bf16 bit patterns."""
+    cos_t = np.zeros((max_pos, ROT_DIM), np.uint16)
+    sin_t = np.zeros((max_pos, ROT_DIM), np.uint16)
+    _check(_lib.qsa_rope_tables(int(max_pos), float(theta),
+                                cos_t.ctypes.data_as(ctypes.c_void_p),
+                                sin_t.ctypes.data_as(ctypes.c_void_p)), "qsa_rope_tables")
+    return cos_t, sin_t
+
+
+def qsa_pool_blocks(keys, key_stride, first_block, n_blocks, k_norm_w, cos_t, sin_t, table_rows,
+                    eps, block_keys, stream=None) -> None:
+    _check(_lib.qsa_pool_blocks(_dev(keys, "keys"), int(key_stride), int(first_block),
+                                int(n_blocks), _dev(k_norm_w, "k_norm_w"), _dev(cos_t, "cos_t"),
+                                _dev(sin_t, "sin_t"), int(table_rows), float(eps),
+                                _dev(block_keys, "block_keys"), _stream(stream)),
+           "qsa_pool_blocks")
+
+
+def qsa_score_rows_with(q, q_stride, pos, visible_len, n_rows, tokens, q_norm_w, cos_t, sin_t,
+                        table_rows, eps, block_keys, key_base, scores, score_cols, dev_status,
+                        path=QSA_SCORE_AUTO, stream=None) -> None:
+    _check(_lib.qsa_score_rows_with(_dev(q, "q"), int(q_stride), _dev(pos, "pos"),
+                                    _dev(visible_len, "visible_len"), int(n_rows), int(tokens),
+                                    _dev(q_norm_w, "q_norm_w"), _dev(cos_t, "cos_t"),
+                                    _dev(sin_t, "sin_t"), int(table_rows), float(eps),
+                                    _dev(block_keys, "block_keys"), _dev(key_base, "key_base"),
+                                    _dev(scores, "scores"), int(score_cols),
+                                    _dev(dev_status, "dev_status"), int(path), _stream(stream)),
+           "qsa_score_rows_with")
+
+
+def qsa_score_rows(q, q_stride, pos, visible_len, n_rows, tokens, q_norm_w, cos_t, sin_t,
+                   table_rows, eps, block_keys, key_base, scores, score_cols, dev_status,
+                   stream=None) -> None:
+    _check(_lib.qsa_score_rows(_dev(q, "q"), int(q_stride), _dev(pos, "pos"),
+                               _dev(visible_len, "visible_len"), int(n_rows), int(tokens),
+                               _dev(q_norm_w, "q_norm_w"), _dev(cos_t, "cos_t"),
+                               _dev(sin_t, "sin_t"), int(table_rows), float(eps),
+                               _dev(block_keys, "block_keys"), _dev(key_base, "key_base"),
+                               _dev(scores, "scores"), int(score_cols),
+                               _dev(dev_status, "dev_status"), _stream(stream)),
+           "qsa_score_rows")
+
+
+def qsa_select_mask(scores, score_cols, pos, n_rows, tokens, budget, mask, dev_status,
+                    stream=None) -> None:
+    _check(_lib.qsa_select_mask(_dev(scores, "scores"), int(score_cols), _dev(pos, "pos"),
+                                int(n_rows), int(tokens), int(budget), _dev(mask, "mask"),
+                                _dev(dev_status, "dev_status"), _stream(stream)),
+           "qsa_select_mask")
+
+
+def qsa_index_select(keys, key_stride, pool_first_block, pool_n_blocks, k_norm_w, q, q_stride, pos,
+                     n_rows, tokens, q_norm_w, cos_t, sin_t, table_rows, eps, budget, block_keys,
+                     scores, score_cols, mask, dev_status, stream=None) -> None:
+    _check(_lib.qsa_index_select(_dev(keys, "keys"), int(key_stride), int(pool_first_block),
+                                 int(pool_n_blocks), _dev(k_norm_w, "k_norm_w"), _dev(q, "q"),
+                                 int(q_stride), _dev(pos, "pos"), int(n_rows), int(tokens),
+                                 _dev(q_norm_w, "q_norm_w"), _dev(cos_t, "cos_t"),
+                                 _dev(sin_t, "sin_t"), int(table_rows), float(eps), int(budget),
+                                 _dev(block_keys, "block_keys"), _dev(scores, "scores"),
+                                 int(score_cols), _dev(mask, "mask"),
+                                 _dev(dev_status, "dev_status"), _stream(stream)),
+           "qsa_index_select")
+
+
+def qsa_reset_status(dev_status, stream=None) -> None:
+    _check(_lib.qsa_reset_status(_dev(dev_status, "dev_status"), _stream(stream)),
+           "qsa_reset_status")
+
+
+def qsa_read_status(dev_status, stream=None) -> tuple[int, int]:
+    code, row = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(_lib.qsa_read_status(_dev(dev_status, "dev_status"), _stream(stream),
+                                ctypes.byref(code), ctypes.byref(row)), "qsa_read_status")
+    return int(code.value), int(row.value)
+
+
+def new_status(device="cuda") -> torch.Tensor:
+    """A zeroed device status word (int32[2])."""
+    return torch.zeros(2, dtype=torch.int32, device=device)

@@ -1,0 +1,142 @@
+// Device helpers for the QSA indexer kernels (sm_103a).
+//
+// Arithmetic conventions (PR #1160 "score QSA token-indexer blocks in native
+// CUDA": block keys are averaged in float32 and cast back to bf16, then (1 + w)
+// RMSNorm and partial RoPE, every bf16 rounding point of the reference kept;
+// its "Tolerance" section: the reference rounds float32 reductions):
+//  * the 4-token sum and the 128-term sum of squares are computed error-free
+//    (TwoSum cascades), so each equals the exact sum rounded once to f32;
+//  * every other step is one IEEE f32 operation (explicit _rn intrinsics, so
+//    no FMA contraction changes a rounding), then bf16 where the reference
+//    rounds to bf16.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qsa {
+
+constexpr int kHeads = 4;
+constexpr int kHeadDim = 128;
+constexpr int kRatio = 4;
+constexpr int kRot = 64;
+constexpr int kHalf = 32;
+constexpr int kMaxKeep = 512;  // budget / 4 <= 512
+
+enum : int32_t {
+  kOk = 0,
+  kErrRowRange = 3,
+  kErrNonFinite = 4,
+  kErrTimeout = 5,
+};
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
+
+__device__ __forceinline__ uint32_t f32_to_bf16(float f) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ float round_bf16(float f) { return bf16_to_f32(f32_to_bf16(f)); }
+
+// Low / high bf16 of a packed pair.
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) { return lo | (hi << 16); }
+
+// Error-free transformation: a + b = s + e exactly (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Record the first device-side error: {code, row}.  Never traps.
+__device__ __forceinline__ void report_error(int32_t *status, int32_t code, int32_t row) {
+  if (status == nullptr) return;
+  if (atomicCAS(status, 0, code) == 0) atomicExch(status + 1, row);
+}
+
+// (1 + w) RMSNorm then partial RoPE of one 128-vector held by a 16-lane group:
+// lane g (0..15 within the group) holds dims 8g..8g+7 in x[] (bf16 values as
+// f32).  Lanes 0-3 hold dims 0..31, lanes 4-7 dims 32..63 (the rotated half,
+// paired (i, i+32)), lanes 8-15 the unrotated dims.  `w8` holds the weight's
+// 8 bf16 for those dims, `c8`/`s8` the cos/sin row's entries 8g..8g+7 (lanes
+// 0..7 only).  Returns the 8 output bf16 packed in a uint4.  All 32 lanes of
+// the warp must call this (two groups per warp).
+__device__ __forceinline__ uint4 norm_rope_16(const float (&x)[8], const uint4 &w8, const uint4 &c8,
+                                              const uint4 &s8, float eps, int g) {
+  // sum of squares, error-free: squares of bf16 values are exact in f32
+  float hi = 0.f, lo = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float sq = __fmul_rn(x[e], x[e]);
+    float s, err;
+    two_sum(hi, sq, s, err);
+    hi = s;
+    lo = __fadd_rn(lo, err);
+  }
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) {
+    float ohi = __shfl_xor_sync(0xffffffffu, hi, off);
+    float olo = __shfl_xor_sync(0xffffffffu, lo, off);
+    float s, err;
+    two_sum(hi, ohi, s, err);
+    hi = s;
+    lo = __fadd_rn(__fadd_rn(lo, olo), err);
+  }
+  const float ms = __fmul_rn(__fadd_rn(hi, lo), 1.0f / 128.0f);
+  const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+
+  const uint32_t wv[4] = {w8.x, w8.y, w8.z, w8.w};
+  float n[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float w = (e & 1) ? hi_bf16(wv[e >> 1]) : lo_bf16(wv[e >> 1]);
+    n[e] = round_bf16(__fmul_rn(__fmul_rn(x[e], r), __fadd_rn(1.0f, w)));
+  }
+  // partner half of the rotary pair lives 4 lanes away
+  float part[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[e] = __shfl_xor_sync(0xffffffffu, n[e], 4);
+
+  const uint32_t cv[4] = {c8.x, c8.y, c8.z, c8.w};
+  const uint32_t sv[4] = {s8.x, s8.y, s8.z, s8.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float c = (e & 1) ? hi_bf16(cv[e >> 1]) : lo_bf16(cv[e >> 1]);
+    const float s = (e & 1) ? hi_bf16(sv[e >> 1]) : lo_bf16(sv[e >> 1]);
+    if (g < 4) {  // out_i = x_i c - x_{i+32} s
+      o[e] = f32_to_bf16(__fsub_rn(round_bf16(__fmul_rn(n[e], c)), round_bf16(__fmul_rn(part[e], s))));
+    } else if (g < 8) {  // out_{i+32} = x_{i+32} c + x_i s
+      o[e] = f32_to_bf16(__fadd_rn(round_bf16(__fmul_rn(n[e], c)), round_bf16(__fmul_rn(part[e], s))));
+    } else {
+      o[e] = f32_to_bf16(n[e]);
+    }
+  }
+  return make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
+                    pack_bf16(o[6], o[7]));
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&x)[8]) {
+  x[0] = lo_bf16(v.x); x[1] = hi_bf16(v.x);
+  x[2] = lo_bf16(v.y); x[3] = hi_bf16(v.y);
+  x[4] = lo_bf16(v.z); x[5] = hi_bf16(v.z);
+  x[6] = lo_bf16(v.w); x[7] = hi_bf16(v.w);
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldg_v4(const void *p) {
+  return *reinterpret_cast<const uint4 *>(p);
+}
+
+}  // namespace qsa

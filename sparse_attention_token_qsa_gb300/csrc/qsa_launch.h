@@ -1,0 +1,41 @@
+// Internal launchers of the QSA kernels (host side, one per kernel family).
+// Arguments are validated by the C ABI layer before these are called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qsa {
+
+cudaError_t launch_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t first_block,
+                               int32_t n_blocks, const uint16_t *k_norm_w, const uint16_t *cos_t,
+                               const uint16_t *sin_t, float eps, uint16_t *block_keys,
+                               cudaStream_t stream);
+
+struct ScoreArgs {
+  const uint16_t *q;
+  int64_t q_stride;
+  const int32_t *pos;
+  const int32_t *visible_len;
+  int32_t n_rows;
+  int32_t tokens;
+  const uint16_t *q_norm_w;
+  const uint16_t *cos_t;
+  const uint16_t *sin_t;
+  float eps;
+  const uint16_t *block_keys;
+  const int64_t *key_base;
+  float *scores;
+  int64_t score_cols;
+  int32_t *status;
+};
+
+cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream);
+cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream);
+extern const bool kTcScorerReady;
+
+cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t *pos,
+                          int32_t n_rows, int32_t tokens, int32_t budget, uint8_t *mask,
+                          int32_t *status, cudaStream_t stream);
+
+}  // namespace qsa

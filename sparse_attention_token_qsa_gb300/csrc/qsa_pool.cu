@@ -1,0 +1,77 @@
+// Block pooling kernel: one pooled bf16 key per complete 4-token block.
+//
+// PR #1160 "score QSA token-indexer blocks in native CUDA", description: every
+// complete micro-block of compress_ratio = 4 raw keys is averaged in float32,
+// cast back to bf16, (1 + w) RMSNorm'd and rotated (partial RoPE, 64 of 128
+// dims) at the block's FIRST token; one pass over the keys serves every row.
+// metrale layers/qsa.rs (pool_new_blocks) pools only newly complete blocks,
+// which is why the launch takes [first_block, first_block + n_blocks).
+//
+// Layout: a half-warp (16 lanes) owns one block; lane g loads the 16-byte
+// slice (dims 8g..8g+7) of each of the four token rows, so each token row is
+// one coalesced 256-byte read and the output row one 256-byte write.  HBM
+// traffic per block: 1024 B keys + 256 B out + 256 B cos/sin rows.
+#include "qsa_device.cuh"
+#include "qsa_launch.h"
+
+namespace qsa {
+
+constexpr int kPoolThreads = 256;               // 16 blocks per CTA
+constexpr int kPoolBlocksPerCta = kPoolThreads / 16;
+
+__global__ void __launch_bounds__(kPoolThreads)
+pool_blocks_kernel(const uint16_t *__restrict__ keys, int64_t key_stride, int32_t first_block,
+                   int32_t n_blocks, const uint16_t *__restrict__ k_norm_w,
+                   const uint16_t *__restrict__ cos_t, const uint16_t *__restrict__ sin_t,
+                   float eps, uint16_t *__restrict__ block_keys) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane & 15;
+  const int64_t i = (int64_t)blockIdx.x * kPoolBlocksPerCta + (threadIdx.x >> 4);
+  // Both half-warps must reach the shuffles in norm_rope_16: clamp the block
+  // index of an idle half-warp and drop its store instead of returning early.
+  const bool active = i < n_blocks;
+  const int64_t ii = active ? i : (int64_t)n_blocks - 1;
+  const int64_t b = (int64_t)first_block + ii;
+
+  const uint16_t *k0 = keys + (int64_t)kRatio * ii * key_stride + 8 * g;
+  uint4 t0 = ldg_nc_v4(k0);
+  uint4 t1 = ldg_nc_v4(k0 + key_stride);
+  uint4 t2 = ldg_nc_v4(k0 + 2 * key_stride);
+  uint4 t3 = ldg_nc_v4(k0 + 3 * key_stride);
+  const uint4 w8 = ldg_nc_v4(k_norm_w + 8 * g);
+  uint4 c8 = make_uint4(0, 0, 0, 0), s8 = make_uint4(0, 0, 0, 0);
+  if (g < 8) {
+    const int64_t P = (int64_t)kRatio * b;  // the block's first token
+    c8 = ldg_nc_v4(cos_t + P * kRot + 8 * g);
+    s8 = ldg_nc_v4(sin_t + P * kRot + 8 * g);
+  }
+  float a[8], bb[8], c[8], d[8], m[8];
+  unpack8(t0, a);
+  unpack8(t1, bb);
+  unpack8(t2, c);
+  unpack8(t3, d);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    // exact sum of the 4 bf16 values, rounded once to f32 (TwoSum cascade)
+    float s1, e1, s2, e2, s3, e3;
+    two_sum(a[e], bb[e], s1, e1);
+    two_sum(s1, c[e], s2, e2);
+    two_sum(s2, d[e], s3, e3);
+    const float sum = __fadd_rn(s3, __fadd_rn(__fadd_rn(e1, e2), e3));
+    m[e] = round_bf16(__fmul_rn(sum, 0.25f));  // f32 mean, cast back to bf16
+  }
+  const uint4 out = norm_rope_16(m, w8, c8, s8, eps, g);
+  if (active) *reinterpret_cast<uint4 *>(block_keys + b * kHeadDim + 8 * g) = out;
+}
+
+cudaError_t launch_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t first_block,
+                               int32_t n_blocks, const uint16_t *k_norm_w, const uint16_t *cos_t,
+                               const uint16_t *sin_t, float eps, uint16_t *block_keys,
+                               cudaStream_t stream) {
+  const int64_t grid = ((int64_t)n_blocks + kPoolBlocksPerCta - 1) / kPoolBlocksPerCta;
+  pool_blocks_kernel<<<(unsigned)grid, kPoolThreads, 0, stream>>>(
+      keys, key_stride, first_block, n_blocks, k_norm_w, cos_t, sin_t, eps, block_keys);
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

@@ -1,0 +1,143 @@
+// Bandwidth-bound block scorer (decode shape, and any row set).
+//
+// PR #1160 "score QSA token-indexer blocks in native CUDA", description: each
+// query row's four heads are normed with (1 + q_norm_w) and rotated at the
+// row's own position, then score(p, b) = sum_h relu(q_h . k_b) / sqrt(128), with
+// relu applied per head before the head sum and written as a comparison so a
+// NaN key keeps its NaN.  Only b < visible_len / 4 is written.
+// metrale layers/qsa.rs decode_select (qsa_qprep then qsa_score over the
+// complete blocks) is the decode use: one row streams every block key once.
+//
+// Design: every CTA prepares its row's four heads in shared memory (1 KiB read,
+// redundant across the row's CTAs but L2-resident), then 8-lane groups stream
+// block keys: lane g of a group owns dims {8(8j+g)+e : j<2, e<8}, so one
+// 16-byte load per lane per j makes each warp read 4 whole 256-byte keys per
+// pair of instructions.  The 4 head partial dots are reduce-scattered over
+// the 8 lanes (4 shuffles) and gathered to lane 0 (3 shuffles), which applies
+// relu, sums heads in order 0..3 and scales.  HBM traffic: 256 B of key read +
+// 4 B of score written per (row, block).
+#include "qsa_device.cuh"
+#include "qsa_launch.h"
+
+namespace qsa {
+
+constexpr int kSimtThreads = 256;
+constexpr int kSimtGroups = kSimtThreads / 8;  // 32 groups of 8 lanes
+constexpr int kSimtUnroll = 4;
+constexpr int kSimtBlocksPerIter = kSimtGroups * kSimtUnroll;  // 128
+
+__device__ __forceinline__ void prep_query_heads(const ScoreArgs &a, int row, int p,
+                                                 float (*q_s)[kHeadDim]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < 2) {  // 4 half-warps = 4 heads
+    const int h = warp * 2 + (lane >> 4);
+    const int g = lane & 15;
+    const uint4 v = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * g);
+    const uint4 w8 = ldg_nc_v4(a.q_norm_w + 8 * g);
+    uint4 c8 = make_uint4(0, 0, 0, 0), s8 = make_uint4(0, 0, 0, 0);
+    if (g < 8) {
+      c8 = ldg_nc_v4(a.cos_t + (int64_t)p * kRot + 8 * g);
+      s8 = ldg_nc_v4(a.sin_t + (int64_t)p * kRot + 8 * g);
+    }
+    float x[8];
+    unpack8(v, x);
+    const uint4 o = norm_rope_16(x, w8, c8, s8, a.eps, g);
+    float y[8];
+    unpack8(o, y);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q_s[h][8 * g + e] = y[e];
+  }
+}
+
+__global__ void __launch_bounds__(kSimtThreads)
+score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
+  __shared__ float q_s[kHeads][kHeadDim];
+  const int row = blockIdx.x;
+  const int p = a.pos[row];
+  const int vis = a.visible_len ? a.visible_len[row] : p + 1;
+  if (p < 0 || p >= a.tokens || vis < 0 || vis > p + 1) {
+    if (blockIdx.y == 0 && threadIdx.x == 0) report_error(a.status, kErrRowRange, row);
+    return;
+  }
+  const int n = vis >> 2;
+  const int c0 = blockIdx.y * blocks_per_cta;
+  if (c0 >= n) return;
+  const int c1 = min(n, c0 + blocks_per_cta);
+
+  prep_query_heads(a, row, p, q_s);
+  __syncthreads();
+
+  const int gi = threadIdx.x >> 3;
+  const int g = threadIdx.x & 7;
+  float qr[kHeads][2][8];
+#pragma unroll
+  for (int h = 0; h < kHeads; ++h)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qr[h][j][e] = q_s[h][8 * (8 * j + g) + e];
+
+  const uint16_t *kb = a.block_keys + (a.key_base ? a.key_base[row] : 0) * kHeadDim;
+  float *srow = a.scores + (int64_t)row * a.score_cols;
+  const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
+
+  for (int base = c0; base < c1; base += kSimtBlocksPerIter) {
+    uint4 kv[kSimtUnroll][2];
+#pragma unroll
+    for (int u = 0; u < kSimtUnroll; ++u) {
+      const int b = base + u * kSimtGroups + gi;
+      const int bc = b < c1 ? b : c0;
+      const uint16_t *kp = kb + (int64_t)bc * kHeadDim + 8 * g;
+      kv[u][0] = ldg_nc_v4(kp);
+      kv[u][1] = ldg_nc_v4(kp + 64);
+    }
+#pragma unroll
+    for (int u = 0; u < kSimtUnroll; ++u) {
+      float acc[kHeads] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float k[8];
+        unpack8(kv[u][j], k);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+#pragma unroll
+          for (int h = 0; h < kHeads; ++h) acc[h] = fmaf(qr[h][j][e], k[e], acc[h]);
+      }
+      // reduce-scatter the 4 head sums over the 8 lanes of the group
+      const bool up4 = g & 4;
+      float keep0 = up4 ? acc[2] : acc[0];
+      float keep1 = up4 ? acc[3] : acc[1];
+      const float send0 = up4 ? acc[0] : acc[2];
+      const float send1 = up4 ? acc[1] : acc[3];
+      keep0 += __shfl_xor_sync(0xffffffffu, send0, 4);
+      keep1 += __shfl_xor_sync(0xffffffffu, send1, 4);
+      const bool up2 = g & 2;
+      float d = up2 ? keep1 : keep0;
+      d += __shfl_xor_sync(0xffffffffu, up2 ? keep0 : keep1, 2);
+      d += __shfl_xor_sync(0xffffffffu, d, 1);
+      // lanes 0,2,4,6 of the group now hold heads 0,1,2,3
+      const float r = (d < 0.f) ? 0.f : d;  // relu as a comparison: NaN stays NaN
+      const float r1 = __shfl_down_sync(0xffffffffu, r, 2);
+      const float r2 = __shfl_down_sync(0xffffffffu, r, 4);
+      const float r3 = __shfl_down_sync(0xffffffffu, r, 6);
+      const int b = base + u * kSimtGroups + gi;
+      if (g == 0 && b < c1) srow[b] = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(r, r1), r2), r3), inv_sqrt_hd);
+    }
+  }
+}
+
+cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream) {
+  const int64_t n_max = (int64_t)a.tokens / kRatio;
+  if (n_max == 0) return cudaSuccess;
+  const int64_t iters = (n_max + kSimtBlocksPerIter - 1) / kSimtBlocksPerIter;
+  // enough CTAs to cover ~8 per SM, each streaming at least 128 blocks
+  int64_t k = ((int64_t)a.n_rows * iters) / (8 * 152);
+  k = k < 1 ? 1 : (k > 16 ? 16 : k);
+  while ((iters + k - 1) / k > 65535) ++k;
+  const int32_t bpc = (int32_t)(k * kSimtBlocksPerIter);
+  dim3 grid((unsigned)a.n_rows, (unsigned)((n_max + bpc - 1) / bpc));
+  score_simt_kernel<<<grid, kSimtThreads, 0, stream>>>(a, bpc);
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

@@ -1,0 +1,145 @@
+"""Host-only checks of the C ABI: no GPU, no launch.
+
+Every call here is refused (or is an empty launch) before the library forms a
+launch, so the dangling pointers below are never dereferenced.  Each refusal
+test first makes the same call with valid arguments and a zero extent, which
+must return QSA_OK: that positive control keeps the refusals from passing
+vacuously (the pattern of the refusal test in PR #1160's review).
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_attention_token_qsa_gb300 import build
+
+    build.build()
+    import sparse_attention_token_qsa_gb300 as qsa
+
+    return qsa.library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import sparse_attention_token_qsa_gb300 as qsa
+
+    names = header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(qsa.EXPORTED) == names
+
+
+def test_version_and_status_strings(lib):
+    assert lib.qsa_version() >= 100
+    for code in range(6):
+        assert lib.qsa_status_string(code)
+    assert b"unknown" in lib.qsa_status_string(99)
+
+
+A = 0x10000          # 16-byte aligned dangling pointer
+B = 0x20000
+U = 0x10002          # misaligned
+
+
+def P(x):
+    return ctypes.c_void_p(x)
+
+
+def select(lib, scores=A, score_cols=64, pos=B, n_rows=1, tokens=256, budget=2048, mask=A,
+           status=B):
+    return lib.qsa_select_mask(P(scores), score_cols, P(pos), n_rows, tokens, budget, P(mask),
+                               P(status), None)
+
+
+def test_select_refusals(lib):
+    assert select(lib, n_rows=0) == 0 and select(lib, tokens=0) == 0        # empty: no-op
+    for kw in (dict(budget=0), dict(budget=-4), dict(budget=6), dict(budget=2052),
+               dict(n_rows=-1), dict(tokens=-1), dict(score_cols=-4),
+               dict(score_cols=60), dict(score_cols=66), dict(scores=0), dict(pos=0),
+               dict(mask=0), dict(scores=U)):
+        assert select(lib, **kw) == 1, kw
+        assert select(lib, **{**kw, "n_rows": 0}) in (0, 1)
+    # budget and negative extents are refused even on an empty launch
+    assert select(lib, n_rows=0, budget=6) == 1
+    assert select(lib, n_rows=-1, tokens=0) == 1
+
+
+def pool(lib, keys=A, key_stride=640, first=0, n=0, w=A, cos=A, sin=A, rows=1 << 16, eps=1e-6,
+         out=A):
+    return lib.qsa_pool_blocks(P(keys), key_stride, first, n, P(w), P(cos), P(sin), rows, eps,
+                               P(out), None)
+
+
+def test_pool_refusals(lib):
+    assert pool(lib) == 0                                  # zero blocks: no-op
+    for kw in (dict(key_stride=120), dict(key_stride=644), dict(keys=U), dict(out=U), dict(w=U),
+               dict(cos=0), dict(sin=0), dict(keys=0), dict(out=0), dict(eps=-1.0),
+               dict(eps=float("nan")), dict(rows=4 * 9), dict(first=-1)):
+        assert pool(lib, n=10, **kw) == 1, kw
+    assert pool(lib, n=-1) == 1
+
+
+def score(lib, q=A, q_stride=640, pos=B, vis=None, n_rows=0, tokens=4096, w=A, cos=A, sin=A,
+          rows=4096, eps=1e-6, keys=A, base=None, scores=A, cols=1024, status=B, path=0):
+    return lib.qsa_score_rows_with(P(q), q_stride, P(pos), P(vis or 0), n_rows, tokens, P(w),
+                                   P(cos), P(sin), rows, eps, P(keys), P(base or 0), P(scores),
+                                   cols, P(status), path, None)
+
+
+def test_score_refusals(lib):
+    assert score(lib) == 0                                 # zero rows: no-op
+    for kw in (dict(q_stride=504), dict(q_stride=644), dict(q=U), dict(keys=U), dict(scores=U),
+               dict(cols=1020), dict(cols=1022), dict(rows=4095), dict(eps=-1e-6),
+               dict(q=0), dict(pos=0), dict(keys=0), dict(scores=0), dict(w=0), dict(cos=0),
+               dict(path=3), dict(path=2, base=B)):
+        assert score(lib, n_rows=3, **kw) == 1, kw
+    assert score(lib, n_rows=-3) == 1
+
+
+def test_index_select_refusals(lib):
+    def call(**kw):
+        a = dict(keys=A, ks=640, f=0, nb=0, kw=A, q=A, qs=640, pos=B, n=0, tokens=4096, qw=A,
+                 cos=A, sin=A, rows=4096, eps=1e-6, budget=2048, bk=A, sc=A, cols=1024, mask=A,
+                 st=B)
+        a.update(kw)
+        return lib.qsa_index_select(P(a["keys"]), a["ks"], a["f"], a["nb"], P(a["kw"]), P(a["q"]),
+                                    a["qs"], P(a["pos"]), a["n"], a["tokens"], P(a["qw"]),
+                                    P(a["cos"]), P(a["sin"]), a["rows"], a["eps"], a["budget"],
+                                    P(a["bk"]), P(a["sc"]), a["cols"], P(a["mask"]), P(a["st"]),
+                                    None)
+    assert call() == 0
+    assert call(budget=2047) == 1
+    assert call(nb=4, ks=100) == 1
+    assert call(n=2, qs=100) == 1
+    assert call(n=2, cols=100) == 1
+
+
+def test_status_calls_refuse_null(lib):
+    assert lib.qsa_reset_status(None, None) == 1
+    assert lib.qsa_read_status(None, None, None, None) == 1
+
+
+def test_rope_tables_match_oracle(lib, orc):
+    import sparse_attention_token_qsa_gb300 as qsa
+
+    for theta in (10000.0, 1e7):
+        c1, s1 = qsa.qsa_rope_tables(70000, theta)
+        c2, s2 = orc.rope_table(70000, theta)
+        assert np.array_equal(c1, c2) and np.array_equal(s1, s2)
+    assert lib.qsa_rope_tables(-1, 1e4, None, None) == 1
+    assert lib.qsa_rope_tables(4, 0.0, P(A), P(A)) == 1
+    assert lib.qsa_rope_tables(0, 1e4, None, None) == 0

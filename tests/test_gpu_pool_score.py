@@ -1,0 +1,205 @@
+"""GPU parity of qsa_pool_blocks and qsa_score_rows against the oracle.
+
+Pooled keys and scores must match within 5e-3 absolute + 1e-3 relative; the
+pooling is built to reproduce the oracle's rounding points, so the tests also
+report (and bound) how many pooled bf16 values differ at all.
+"""
+import numpy as np
+import pytest
+import torch
+
+import qsa_inputs as qi
+from qsa_cases import (EPS, THETA, assert_close, bf16_close, long_keys_case, oracle_scores,
+                       prefill_case)
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+def host16(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+@pytest.fixture(scope="module")
+def qsa():
+    import sparse_attention_token_qsa_gb300 as m
+
+    return m
+
+
+@pytest.fixture(scope="module")
+def tables(qsa):
+    c, s = qsa.qsa_rope_tables(262144 + 8, THETA)
+    return c, s, dev(c), dev(s)
+
+
+def gpu_pool(qsa, tables, keys_flat_dev, key_stride, first, n, k_norm_w, total_blocks):
+    c, s, cd, sd = tables
+    out = torch.full((total_blocks, 128), 0x7FAB, dtype=torch.int16, device="cuda")
+    qsa.qsa_pool_blocks(keys_flat_dev, key_stride, first, n, dev(k_norm_w), cd, sd, c.shape[0],
+                        EPS, out)
+    torch.cuda.synchronize()
+    return host16(out)
+
+
+def test_pool_fused_layout_prefill(qsa, orc, tables):
+    case = prefill_case()
+    T = case["T"]
+    c, s, _, _ = tables
+    nb = T // 4
+    fq_dev = dev(case["fq"])
+    got = gpu_pool(qsa, tables, fq_dev.view(-1)[512:], 640, 0, nb, case["k_norm_w"], nb)
+    want = orc.pool_blocks(case["fq"].reshape(-1)[512:], 640, 0, nb, case["k_norm_w"], c, s, EPS)
+    exact = bf16_close(got, want, "pooled keys (fused layout)")
+    assert exact == got.size, f"{got.size - exact} pooled values differ from the oracle"
+
+
+def test_pool_long_context_token_scaled(qsa, orc, tables):
+    case = long_keys_case()
+    keys = case["keys"]
+    nb = keys.shape[0] // 4
+    c, s, _, _ = tables
+    got = gpu_pool(qsa, tables, dev(keys).view(-1), 128, 0, nb, case["k_norm_w"], nb)
+    want = orc.pool_blocks(keys, 128, 0, nb, case["k_norm_w"], c, s, EPS)
+    exact = bf16_close(got, want, "pooled keys (64k, per-token scales)")
+    assert exact >= got.size - 2, f"{got.size - exact} pooled values differ from the oracle"
+
+
+@pytest.mark.parametrize("first,n", [(0, 1), (5, 17), (1000, 333), (16383, 1)])
+def test_pool_ranges_only_touch_their_blocks(qsa, orc, tables, first, n):
+    case = long_keys_case()
+    keys = case["keys"]
+    c, s, _, _ = tables
+    total = keys.shape[0] // 4
+    kd = dev(keys)
+    got = gpu_pool(qsa, tables, kd.view(-1)[4 * first * 128:], 128, first, n, case["k_norm_w"], total)
+    want = orc.pool_blocks(keys[4 * first:], 128, first, n, case["k_norm_w"], c, s, EPS,
+                           total_blocks=total)
+    assert np.array_equal(got[first:first + n], want[first:first + n])
+    untouched = np.ones(total, bool)
+    untouched[first:first + n] = False
+    assert np.all(got[untouched] == 0x7FAB)
+
+
+def pooled_prefill(orc, case, c, s):
+    nb = case["T"] // 4
+    return orc.pool_blocks(case["fq"].reshape(-1)[512:], 640, 0, nb, case["k_norm_w"], c, s, EPS)
+
+
+@pytest.mark.parametrize("path", [1])
+def test_score_prefill_all_rows(qsa, orc, tables, path):
+    """Every row of the 2304-token prefill, scored against the oracle's pooled keys;
+    entries past each row's prefix keep their sentinel."""
+    case = prefill_case()
+    T = case["T"]
+    c, s, cd, sd = tables
+    keys = pooled_prefill(orc, case, c, s)
+    cols = T // 4 + 4
+    sc = torch.full((T, cols), -7.0, dtype=torch.float32, device="cuda")
+    st = qsa.new_status()
+    qsa.qsa_score_rows_with(dev(case["fq"]), 640, dev(case["pos"]), None, T, T,
+                            dev(case["q_norm_w"]), cd, sd, c.shape[0], EPS, dev(keys), None, sc,
+                            cols, st, path=path)
+    assert qsa.qsa_read_status(st) == (0, 0)
+    got = sc.cpu().numpy()
+    want, res = oracle_scores(orc, case["fq"], 640, case["pos"], T, case["q_norm_w"], c, s, keys,
+                              cols)
+    assert all(rc == 0 for rc, _ in res)
+    worst = assert_close(got, want, "prefill scores")
+    assert worst < 5e-3
+
+
+def test_score_decode_rows_long_context(qsa, orc, tables):
+    """Decode rows at 64k (16384 blocks each), visible_len and key_base variants."""
+    case = long_keys_case()
+    keys_raw = case["keys"]
+    c, s, cd, sd = tables
+    nb = keys_raw.shape[0] // 4
+    keys = orc.pool_blocks(keys_raw, 128, 0, nb, case["k_norm_w"], c, s, EPS)
+    rows = 8
+    q = case["q"][:rows]
+    pos = np.array([65535, 65534, 65280, 40000, 4, 3, 70, 65535], np.int32)
+    vis = np.array([65536, 65533, 65281, 100, 5, 0, 71, 65532], np.int32)
+    base = np.array([0, 0, 0, 0, 0, 0, 0, 0], np.int64)
+    cols = 16384 + 12
+    for use_vis, use_base in ((False, False), (True, False), (True, True)):
+        sc = torch.full((rows, cols), -7.0, dtype=torch.float32, device="cuda")
+        st = qsa.new_status()
+        qsa.qsa_score_rows(dev(q), 512, dev(pos), dev(vis) if use_vis else None, rows, 65536,
+                           dev(case["q_norm_w"]), cd, sd, c.shape[0], EPS, dev(keys),
+                           dev(base) if use_base else None, sc, cols, st)
+        assert qsa.qsa_read_status(st) == (0, 0)
+        got = sc.cpu().numpy()
+        want, _ = oracle_scores(orc, q, 512, pos, 65536, case["q_norm_w"], c, s, keys, cols,
+                                visible_len=vis if use_vis else None,
+                                key_base=base if use_base else None)
+        assert_close(got, want, f"decode scores vis={use_vis} base={use_base}")
+
+
+def test_score_key_base_per_sequence(qsa, orc, tables):
+    """Rows of different sequences in one call: key_base selects each row's key set."""
+    rng = qi.rng_for(3, salt=1)
+    c, s, cd, sd = tables
+    lens = [4000, 9000, 6001]
+    kw = qi.normal_bf16(rng, (128,), 0.1)
+    qw = qi.normal_bf16(rng, (128,), 0.1)
+    pooled, base = [], []
+    off = 0
+    for L in lens:
+        raw = qi.raw_keys(rng, L)
+        pooled.append(orc.pool_blocks(raw, 128, 0, L // 4, kw, c, s, EPS))
+        base.append(off)
+        off += L // 4
+    keys = np.concatenate(pooled)
+    base = np.array(base, np.int64)
+    pos = np.array([L - 1 for L in lens], np.int32)
+    q = qi.fused_qk(rng, 3)[:, :512].copy()
+    cols = 2252
+    sc = torch.full((3, cols), -7.0, dtype=torch.float32, device="cuda")
+    st = qsa.new_status()
+    qsa.qsa_score_rows(dev(q), 512, dev(pos), None, 3, 9000, dev(qw), cd, sd, c.shape[0], EPS,
+                       dev(keys), dev(base), sc, cols, st)
+    assert qsa.qsa_read_status(st) == (0, 0)
+    want, _ = oracle_scores(orc, q, 512, pos, 9000, qw, c, s, keys, cols, key_base=base)
+    assert_close(sc.cpu().numpy(), want, "per-sequence scores")
+
+
+def test_score_nan_key_propagates(qsa, orc, tables):
+    case = prefill_case(T=512)
+    c, s, cd, sd = tables
+    keys = pooled_prefill(orc, case, c, s)
+    keys[37, 5] = 0x7FC0
+    T = 512
+    cols = 128
+    sc = torch.full((T, cols), -7.0, dtype=torch.float32, device="cuda")
+    st = qsa.new_status()
+    qsa.qsa_score_rows(dev(case["fq"]), 640, dev(case["pos"]), None, T, T, dev(case["q_norm_w"]),
+                       cd, sd, c.shape[0], EPS, dev(keys), None, sc, cols, st)
+    got = sc.cpu().numpy()
+    rows_seeing = np.arange(T)[(np.arange(T) + 1) // 4 > 37]
+    assert np.all(np.isnan(got[rows_seeing, 37]))
+    want, _ = oracle_scores(orc, case["fq"], 640, case["pos"], T, case["q_norm_w"], c, s, keys, cols)
+    assert_close(got, want, "scores with a NaN key")
+
+
+def test_score_row_range_errors(qsa, tables):
+    c, s, cd, sd = tables
+    q = torch.zeros((3, 640), dtype=torch.int16, device="cuda")
+    keys = torch.zeros((64, 128), dtype=torch.int16, device="cuda")
+    w = torch.zeros(128, dtype=torch.int16, device="cuda")
+    for pos, vis, bad in (([0, 256, 1], None, 1), ([0, -1, 1], None, 1),
+                          ([9, 9, 9], [10, 11, 4], 1)):
+        sc = torch.full((3, 64), -7.0, dtype=torch.float32, device="cuda")
+        st = qsa.new_status()
+        qsa.qsa_score_rows(q, 640, dev(np.array(pos, np.int32)),
+                           None if vis is None else dev(np.array(vis, np.int32)), 3, 256, w, cd, sd,
+                           c.shape[0], EPS, keys, None, sc, 64, st)
+        code, row = qsa.qsa_read_status(st)
+        assert (code, row) == (3, bad)
+        assert np.all(sc.cpu().numpy()[bad] == -7.0)

@@ -1,0 +1,175 @@
+"""GPU parity of qsa_select_mask against the oracle: bit-exact masks.
+
+The selection is integer work over the oracle's own f32 scores, so every case
+compares whole mask rows byte for byte.
+"""
+import numpy as np
+import pytest
+import torch
+
+import qsa_inputs as qi
+from qsa_cases import check_mask_structure, oracle_masks
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+@pytest.fixture(scope="module")
+def qsa():
+    import sparse_attention_token_qsa_gb300 as m
+
+    return m
+
+
+def gpu_select(qsa, scores, score_cols, pos, tokens, budget, mask_offset=0, expect=0):
+    n_rows = len(pos)
+    s = dev(scores)
+    p = dev(np.asarray(pos, np.int32))
+    buf = torch.full((n_rows * tokens + mask_offset + 16,), 0xAB, dtype=torch.uint8, device="cuda")
+    mask = buf[mask_offset:mask_offset + n_rows * tokens]
+    st = qsa.new_status()
+    qsa.qsa_select_mask(s, score_cols, p, n_rows, tokens, budget, mask, st)
+    code, row = qsa.qsa_read_status(st)
+    assert code == expect, (code, row)
+    out = mask.view(n_rows, tokens).cpu().numpy()
+    # guard bytes around the mask are untouched
+    g = buf.cpu().numpy()
+    assert np.all(g[:mask_offset] == 0xAB) and np.all(g[mask_offset + n_rows * tokens:] == 0xAB)
+    return out, row
+
+
+def test_select_stress_ties_all_budgets(qsa, orc):
+    """Selection-only stress at 256k: relu-sum-like scores, 70% exact zeros (half
+    -0.0), the rest on 64 levels; every budget the stress names."""
+    rng = qi.rng_for(4)
+    rows, tokens = 48, 262144
+    cols = tokens // 4
+    scores = qi.stress_scores(rng, rows, cols)
+    pos = np.full(rows, tokens - 1, np.int32)
+    pos[1::3] = tokens - 2          # 65535 blocks, tail 3
+    pos[2::3] = tokens - 7          # 65534 blocks, tail 2
+    for budget in (4, 512, 2048, 2044):
+        got, _ = gpu_select(qsa, scores, cols, pos, tokens, budget)
+        want, codes = oracle_masks(orc, scores, cols, pos, tokens, budget)
+        assert all(c == 0 for c in codes)
+        for r in range(rows):
+            assert np.array_equal(got[r], want[r]), (budget, r)
+
+
+def test_select_prefill_rows_with_injected_ties(qsa, orc):
+    """Single-sequence prefill geometry (T=2304): every row, all-kept rows below
+    the inert bound and truncating rows above it; 32 truncating rows get exact
+    ties at their cut and ~30% +-0.0 scores."""
+    rng = qi.rng_for(0, salt=7)
+    T = 2304
+    cols = T // 4
+    scores = rng.standard_normal((T, cols)).astype(np.float32) * 2.0
+    scores = np.maximum(scores, 0).astype(np.float32)
+    pos = np.arange(T, dtype=np.int32)
+    trunc = np.arange(2051, T)
+    for r in rng.choice(trunc, size=32, replace=False):
+        n = (r + 1) // 4
+        qi.sprinkle_signed_zeros(scores[r], rng, 0.3, n)
+        cut = np.sort(np.where(scores[r, :n] == 0, 0, scores[r, :n]))[::-1][511]
+        qi.set_blocks_to(scores[r], rng, np.float32(cut), int(rng.integers(8, 41)), n)
+    got, _ = gpu_select(qsa, scores, cols, pos, T, 2048)
+    want, codes = oracle_masks(orc, scores, cols, pos, T, 2048)
+    assert all(c == 0 for c in codes)
+    bad = [r for r in range(T) if not np.array_equal(got[r], want[r])]
+    assert not bad, bad[:10]
+    for r in (0, 1, 2, 3, 2046, 2047, 2050, 2051, 2054, T - 1):
+        check_mask_structure(got[r], r, T, 2048)
+
+
+def test_select_all_zero_rows_fill_in_index_order(qsa, orc):
+    tokens = 8192
+    cols = tokens // 4
+    scores = np.zeros((6, cols), np.float32)
+    scores[1, ::2] = -0.0
+    pos = np.array([8191, 8191, 4096, 2051, 3000, 8190], np.int32)
+    got, _ = gpu_select(qsa, scores, cols, pos, tokens, 2048)
+    want, _ = oracle_masks(orc, scores, cols, pos, tokens, 2048)
+    assert np.array_equal(got, want)
+    assert np.all(got[0, :2048] == 1) and np.all(got[0, 2048:] == 0)
+
+
+@pytest.mark.parametrize("tokens,offset", [(1000, 0), (1003, 1), (4099, 3), (65536, 5), (70001, 2)])
+def test_select_ragged_rows_and_unaligned_masks(qsa, orc, tokens, offset):
+    """Rows of every length in one launch, tokens not a multiple of 16, mask rows
+    at odd byte offsets, score_cols with spare capacity."""
+    rng = qi.rng_for(4, salt=tokens)
+    rows = 64
+    cols = ((tokens // 4 + 3) // 4) * 4 + 8
+    scores = qi.stress_scores(rng, rows, cols, zero_frac=0.3, levels=16)
+    pos = rng.integers(0, tokens, size=rows).astype(np.int32)
+    pos[:6] = [0, 1, 2, 3, tokens - 1, min(tokens - 1, 2050)]
+    for budget in (4, 64, 2048):
+        got, _ = gpu_select(qsa, scores, cols, pos, tokens, budget, mask_offset=offset)
+        want, codes = oracle_masks(orc, scores, cols, pos, tokens, budget)
+        assert all(c == 0 for c in codes)
+        for r in range(rows):
+            assert np.array_equal(got[r], want[r]), (budget, r, pos[r])
+
+
+@pytest.mark.parametrize("rows", [1, 2, 8, 40])
+def test_select_cluster_split_rows(qsa, orc, rows):
+    """Few long rows split over clusters of CTAs (decode shapes at 64k and 256k)."""
+    rng = qi.rng_for(3, salt=rows)
+    tokens = 262144 if rows <= 8 else 65536
+    cols = tokens // 4
+    scores = np.maximum(rng.standard_normal((rows, cols)).astype(np.float32), 0)
+    scores[:, rng.choice(cols, 50, replace=False)] = scores[0, 7]        # ties across slices
+    pos = rng.integers(tokens // 2, tokens, size=rows).astype(np.int32)
+    pos[0] = tokens - 1
+    got, _ = gpu_select(qsa, scores, cols, pos, tokens, 2048)
+    want, _ = oracle_masks(orc, scores, cols, pos, tokens, 2048)
+    for r in range(rows):
+        assert np.array_equal(got[r], want[r]), r
+
+
+def test_select_low_byte_differences_and_deep_truncation(qsa, orc):
+    """Keys that differ only in their lowest byte, and budget 4 at 256k."""
+    rng = qi.rng_for(4, salt=99)
+    tokens = 262144
+    cols = tokens // 4
+    base = np.float32(1.5).view(np.uint32)
+    bits = (base + rng.integers(0, 256, size=(2, cols)).astype(np.uint32)).astype(np.uint32)
+    scores = bits.view(np.float32)
+    pos = np.array([tokens - 1, tokens - 3], np.int32)
+    for budget in (4, 2048, 1028):
+        got, _ = gpu_select(qsa, scores, cols, pos, tokens, budget)
+        want, _ = oracle_masks(orc, scores, cols, pos, tokens, budget)
+        assert np.array_equal(got, want), budget
+
+
+def test_select_nonfinite_row_reported_and_untouched(qsa, orc):
+    tokens = 16384
+    cols = tokens // 4
+    rng = qi.rng_for(4, salt=5)
+    scores = rng.random((4, cols)).astype(np.float32)
+    scores[2, 1000] = np.nan
+    scores[0, 3] = np.inf     # row 0 is all-kept: its scores are not read
+    pos = np.array([1000, 16383, 16383, 9000], np.int32)
+    got, row = gpu_select(qsa, scores, cols, pos, tokens, 2048, expect=4)
+    assert row == 2
+    assert np.all(got[2] == 0xAB)
+    want, codes = oracle_masks(orc, scores, cols, pos, tokens, 2048)
+    assert codes == [0, 0, 4, 0]
+    for r in (0, 1, 3):
+        assert np.array_equal(got[r], want[r])
+
+
+def test_select_row_out_of_range_reported(qsa):
+    tokens = 4096
+    cols = tokens // 4
+    scores = np.ones((3, cols), np.float32)
+    pos = np.array([5, 4096, 7], np.int32)
+    got, row = gpu_select(qsa, scores, cols, pos, tokens, 2048, expect=3)
+    assert row == 1 and np.all(got[1] == 0xAB)
+    assert np.all(got[0, :6] == 1) and np.all(got[0, 6:] == 0)

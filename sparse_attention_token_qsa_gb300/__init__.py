@@ -6,7 +6,7 @@ order; device buffers are passed as CUDA torch tensors (their data pointers),
 ``stream`` is a torch CUDA stream (default: the current stream).  The binding
 only marshals arguments: all work runs in the library's CUDA kernels.  There is
 no CPU fallback: importing the package fails loudly when libqsa.so is missing
-(build it with ``python -m sparse_attention_token_qsa_gb300.build``).
+(build it with ``python sparse_attention_token_qsa_gb300/build.py``).
 """
 from __future__ import annotations
 
@@ -46,7 +46,7 @@ class QsaError(RuntimeError):
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libqsa.so is not built ({LIB_PATH}); run "
-                          "`python -m sparse_attention_token_qsa_gb300.build` (needs nvcc)")
+                          "`python sparse_attention_token_qsa_gb300/build.py` (needs nvcc)")
     lib = ctypes.CDLL(LIB_PATH)
     P, i32, i64, f32, f64 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                              ctypes.c_double)

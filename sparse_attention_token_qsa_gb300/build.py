@@ -4,7 +4,7 @@ Each translation unit under ``csrc/`` compiles in parallel to an object in
 ``_build/``; the objects link into ``libqsa.so`` beside this file.  Objects are
 reused while they are newer than every source and header.
 
-    python -m sparse_attention_token_qsa_gb300.build [--verbose-ptxas]
+    python sparse_attention_token_qsa_gb300/build.py [--verbose-ptxas]
 """
 from __future__ import annotations
 

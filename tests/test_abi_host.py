@@ -19,9 +19,9 @@ HEADER = os.path.join(ROOT, "include", "qsa.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from sparse_attention_token_qsa_gb300 import build
+    import __graft_entry__
 
-    build.build()
+    __graft_entry__.build()
     import sparse_attention_token_qsa_gb300 as qsa
 
     return qsa.library()

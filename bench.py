@@ -1,0 +1,552 @@
+#!/usr/bin/env python
+"""Benchmark of the QSA token-indexer hot path (pool -> score -> select) on GB300.
+
+Workload (one bench step = one decode step of one sequence): batch-1 decode at
+64k context -- one query row at positions 65280..65535 (16384 blocks), the
+pooled block keys cached, the block a token completes pooled on that step, then
+score and select with budget 2048.  To keep every step's inputs out of L2, the
+steps rotate over R independent sequences whose key caches together exceed the
+129 MB L2 (no flush is needed).  Steps are replayed from CUDA graphs, so the
+host does not pace the GPU.
+
+Printed: one JSON line (rank 0) with rows/s, per-kernel roofline of the
+dominant kernel (CUDA events, live), the oracle's CPU baseline, an end-to-end
+number through the public entry point with host buffers, clocks sampled during
+the timed region, and secondary measurements (selection at 256k).
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import qsa_inputs as qi  # noqa: E402
+
+METRIC = "indexer rows/s (pool+score+select) at 64k ctx; select µs/row at 256k; % roofline"
+WORKLOAD = "decode batch 1, pos 65280..65535 of a 64k-token context (16384 blocks), budget 2048"
+TOKENS = 65536
+N_BLOCKS = TOKENS // 4
+FIRST_POS = TOKENS - 256
+BUDGET = 2048
+EPS = 1e-6
+THETA = 10000.0
+L2_BYTES = 129 * 1024 * 1024
+
+# algorithmic bytes per unit (measurement)
+POOL_BYTES_PER_BLOCK = 1024 + 256 + 256
+SCORE_BYTES_PER_BLOCK = 256 + 4
+SELECT_BYTES_PER_BLOCK = 4          # + 1 byte per mask token written
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=16384)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=1024)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ncu-case", default=None,
+                    help="run one small case of a kernel for an ncu capture and exit")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def source_digest(name: str) -> str:
+    with open(os.path.join(ROOT, "sparse_attention_token_qsa_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:12]
+
+
+def recorded_traffic(kernel: str, workload: str, src: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is
+    unchanged since that capture (profiles/dram_traffic.txt)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest(src)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload and parts[3] == digest:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples while the timed region runs (host wall clock stamps)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            time.sleep(0.2)
+            if self.proc.poll() not in (None, 0) and gpu_id:   # id not accepted: all GPUs
+                self.proc = subprocess.Popen(cmd[:-2] + ["-i", "0"], stdout=subprocess.PIPE,
+                                             stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        inside = [s for t, s in self.samples if t0 <= t <= t1 + 0.15]
+        if not inside:  # region shorter than the sampling period: nearest samples
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[1]]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        smax = [num(s[1]) for s in inside if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4)
+                          if len(s) > 4 + i and s[4 + i].lower().startswith("active")})
+        power = [num(s[2]) for s in inside if num(s[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "power_w_max": max(power) if power else None, "samples": len(inside)}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return None
+
+
+def dev_tensor(torch, a, device):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(device)
+
+
+# ------------------------------------------------------------ the workload
+
+class DecodeWorkload:
+    """R independent 64k-token sequences, each with a raw-key cache, a pooled
+    block-key cache, 256 decode query rows, and its own score and mask rows."""
+
+    def __init__(self, torch, qsa, device, n_seq: int):
+        self.torch, self.qsa, self.device = torch, qsa, device
+        self.R = n_seq
+        rng = qi.rng_for(1)
+        self.q_norm_w, self.k_norm_w = qi.norm_weights(rng)
+        c, s = qsa.qsa_rope_tables(TOKENS, THETA)
+        self.cos_h, self.sin_h = c, s
+        self.cos, self.sin = dev_tensor(torch, c, device), dev_tensor(torch, s, device)
+        self.qw = dev_tensor(torch, self.q_norm_w, device)
+        self.kw = dev_tensor(torch, self.k_norm_w, device)
+        self.keys, self.cache, self.q, self.scores, self.mask = [], [], [], [], []
+        self.keys_host0 = None
+        self.q_host0 = None
+        for r in range(n_seq):
+            rr = qi.rng_for(1, salt=r + 1)
+            k = qi.raw_keys(rr, TOKENS, token_scale=True)
+            q = np.ascontiguousarray(qi.fused_qk(rr, 256)[:, :512])
+            if r == 0:
+                self.keys_host0, self.q_host0 = k, q
+            self.keys.append(dev_tensor(torch, k, device))
+            self.q.append(dev_tensor(torch, q, device))
+            self.cache.append(torch.zeros((N_BLOCKS, 128), dtype=torch.int16, device=device))
+            self.scores.append(torch.zeros((1, N_BLOCKS), dtype=torch.float32, device=device))
+            self.mask.append(torch.zeros((1, TOKENS), dtype=torch.uint8, device=device))
+        self.status = qsa.new_status(device)
+        # the cache holds every block completed before the decode window
+        for r in range(n_seq):
+            qsa.qsa_pool_blocks(self.keys[r], 128, 0, FIRST_POS // 4, self.kw, self.cos, self.sin,
+                                TOKENS, EPS, self.cache[r])
+        self.positions = dev_tensor(torch, np.arange(FIRST_POS, TOKENS, dtype=np.int32), device)
+        torch.cuda.synchronize(device)
+
+    def step_params(self, k: int):
+        seq = k % self.R
+        j = (k // self.R) % 256
+        return seq, j, FIRST_POS + j
+
+    def pool(self, k):
+        seq, j, p = self.step_params(k)
+        if (p + 1) % 4 == 0:
+            b = (p + 1) // 4 - 1
+            self.qsa.qsa_pool_blocks(self.keys[seq][4 * b:], 128, b, 1, self.kw, self.cos,
+                                     self.sin, TOKENS, EPS, self.cache[seq])
+
+    def score(self, k):
+        seq, j, p = self.step_params(k)
+        self.qsa.qsa_score_rows(self.q[seq][j:j + 1], 512, self.positions[j:j + 1], None, 1,
+                                TOKENS, self.qw, self.cos, self.sin, TOKENS, EPS, self.cache[seq],
+                                None, self.scores[seq], N_BLOCKS, self.status)
+
+    def select(self, k):
+        seq, j, p = self.step_params(k)
+        self.qsa.qsa_select_mask(self.scores[seq], N_BLOCKS, self.positions[j:j + 1], 1, TOKENS,
+                                 BUDGET, self.mask[seq], self.status)
+
+    def step(self, k):
+        self.pool(k)
+        self.score(k)
+        self.select(k)
+
+    def fused_step(self, k, q_src=None, pos_src=None):
+        """The public entry point for one step (qsa_index_select)."""
+        seq, j, p = self.step_params(k)
+        completes = (p + 1) % 4 == 0
+        b = (p + 1) // 4 - 1
+        self.qsa.qsa_index_select(self.keys[seq][4 * b:] if completes else self.keys[seq], 128,
+                                  b if completes else 0, 1 if completes else 0, self.kw,
+                                  self.q[seq][j:j + 1] if q_src is None else q_src, 512,
+                                  self.positions[j:j + 1] if pos_src is None else pos_src, 1,
+                                  TOKENS, self.qw, self.cos, self.sin, TOKENS, EPS, BUDGET,
+                                  self.cache[seq], self.scores[seq], N_BLOCKS, self.mask[seq],
+                                  self.status)
+
+
+def capture_graphs(torch, fn, steps, chunk=256):
+    """CUDA graphs replaying fn(k) for k in steps, chunk steps per graph."""
+    graphs = []
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    for i in range(0, len(steps), chunk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for k in steps[i:i + chunk]:
+                fn(k)
+        graphs.append(g)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return graphs
+
+
+def time_graphs(torch, graphs):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record()
+    for g in graphs:
+        g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def oracle_decode_rate(seconds: float, max_rows: int | None = None):
+    """The oracle on the host cores: decode steps at 64k on one sequence,
+    row-parallel over threads (each thread runs whole steps)."""
+    import oracle
+
+    orc = oracle.Oracle()
+    rng = qi.rng_for(1)
+    qw, kw = qi.norm_weights(rng)
+    rr = qi.rng_for(1, salt=1)
+    keys = qi.raw_keys(rr, TOKENS, token_scale=True)
+    q = np.ascontiguousarray(qi.fused_qk(rr, 256)[:, :512])
+    c, s = orc.rope_table(TOKENS, THETA)
+    cache = orc.pool_blocks(keys, 128, 0, FIRST_POS // 4, kw, c, s, EPS, total_blocks=N_BLOCKS)
+    cores = max(1, min(os.cpu_count() or 1, 64))
+    caches = [cache.copy() for _ in range(cores)]
+    stop = time.time() + seconds
+    counts = [0] * cores
+
+    def worker(t):
+        sc = np.zeros((1, N_BLOCKS), np.float32)
+        j = t
+        while time.time() < stop and (max_rows is None or j < max_rows):
+            p = FIRST_POS + (j % 256)
+            if (p + 1) % 4 == 0:      # pool the block this token completes (own copy)
+                b = (p + 1) // 4 - 1
+                orc.pool_blocks(keys[4 * b:], 128, b, 1, kw, c, s, EPS, block_keys=caches[t])
+            orc.score_rows(q[j % 256:j % 256 + 1], 512, np.array([p], np.int32), 1, TOKENS, qw, c,
+                           s, EPS, caches[t], sc, N_BLOCKS)
+            orc.select_row(sc[0, :(p + 1) // 4], p, TOKENS, BUDGET)
+            counts[t] += 1
+            j += cores
+
+    t0 = time.time()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        list(ex.map(worker, range(cores)))
+    dt = time.time() - t0
+    rows = sum(counts)
+    return rows / dt, cores, rows, dt
+
+
+# ------------------------------------------------------------ main arms
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    # K steps of one decode row each, row-parallel over the host cores, bounded
+    # at 240 s of wall time (the line reports how many rows ran)
+    rate, cores, rows, dt = oracle_decode_rate(seconds=240.0, max_rows=max(args.steps, 1))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": rows, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * dt / max(rows, 1) * cores, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "budget": BUDGET, "rows_per_step": 1,
+                   "parallelism": "host threads"},
+        "cpu_baseline": {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} decode rows in {dt:.1f} s on {cores} threads"},
+        "e2e": {"value": rate, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, device):
+    import torch
+
+    import sparse_attention_token_qsa_gb300 as qsa
+
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = load_peaks()
+    per_seq_bytes = N_BLOCKS * 256 + TOKENS * 256 + N_BLOCKS * 4 + TOKENS
+    R = max(8, int(np.ceil(1.5 * L2_BYTES / (N_BLOCKS * 256))))
+    wl = DecodeWorkload(torch, qsa, device, R)
+
+    # warm-up (eager): first calls also set kernel attributes outside any capture
+    for k in range(max(args.warmup, 3)):
+        wl.step(k)
+    torch.cuda.synchronize()
+    code, row = qsa.qsa_read_status(wl.status)
+    assert code == 0, f"device status {code} row {row}"
+
+    K = args.steps
+    steps = list(range(args.warmup, args.warmup + K))
+    graphs = capture_graphs(torch, wl.step, steps)
+    for g in graphs[:2]:
+        g.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(gpu_uuid(torch, device))
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ms = time_graphs(torch, graphs)
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.summary(t0, t1)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    ms_per_step = ms / K
+    value = world * K / (ms / 1000.0)
+    code, row = qsa.qsa_read_status(wl.status)
+    assert code == 0, f"device status {code} row {row}"
+
+    # per-kernel durations: the same launches, one kernel at a time, CUDA events
+    kern = {}
+    for name, fn, bytes_per_launch, src in (
+            ("score", wl.score, SCORE_BYTES_PER_BLOCK * N_BLOCKS, "qsa_score_simt.cu"),
+            ("select", wl.select, SELECT_BYTES_PER_BLOCK * N_BLOCKS + TOKENS, "qsa_select.cu")):
+        gk = capture_graphs(torch, fn, steps[:min(K, 4096)])
+        t_ms = time_graphs(torch, gk) / min(K, 4096)
+        kern[name] = {"us": t_ms * 1000.0, "bytes": bytes_per_launch, "src": src}
+    pool_steps = [k for k in steps[:4096] if (wl.step_params(k)[2] + 1) % 4 == 0]
+    gk = capture_graphs(torch, wl.pool, pool_steps)
+    kern["pool"] = {"us": time_graphs(torch, gk) / max(1, len(pool_steps)) * 1000.0,
+                    "bytes": POOL_BYTES_PER_BLOCK, "src": "qsa_pool.cu"}
+    dom = max(("score", "select"), key=lambda n: kern[n]["us"])
+    d = kern[dom]
+    achieved = d["bytes"] / (d["us"] * 1e-6) / 1e9
+    traffic = recorded_traffic(f"{dom}", "decode64k", d["src"])
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_gbs,
+                "unit": "GB/s", "frac": achieved / hbm_gbs, "traffic": traffic,
+                "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes": d["bytes"],
+                "avg_launch_us": d["us"]}
+    kernels = {n: {"avg_launch_us": round(v["us"], 3), "algorithmic_bytes": v["bytes"],
+                   "achieved_gbs": round(v["bytes"] / (v["us"] * 1e-6) / 1e9, 1),
+                   "frac_of_measured_hbm": round(v["bytes"] / (v["us"] * 1e-6) / 1e9 / hbm_gbs, 4)}
+               for n, v in kern.items()}
+
+    # end to end through qsa_index_select with host buffers (eager)
+    E = min(args.e2e_steps, K)
+    q_host = torch.from_numpy(np.ascontiguousarray(wl.q_host0.view(np.int16))).pin_memory()
+    k_host = torch.from_numpy(np.ascontiguousarray(wl.keys_host0.view(np.int16))).pin_memory()
+    pos_host = torch.arange(FIRST_POS, TOKENS, dtype=torch.int32).pin_memory()
+    mask_host = torch.empty((2, TOKENS), dtype=torch.uint8).pin_memory()
+    stat_host = torch.empty(2, dtype=torch.int32).pin_memory()
+    q_step = torch.empty((1, 512), dtype=torch.int16, device=device)
+    pos_step = torch.empty(1, dtype=torch.int32, device=device)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e_start.record()
+    for i in range(E):
+        k = steps[i]
+        seq, j, p = wl.step_params(k)
+        q_step.copy_(q_host[j:j + 1], non_blocking=True)
+        wl.keys[seq][p:p + 1].copy_(k_host[p:p + 1], non_blocking=True)
+        pos_step.copy_(pos_host[j:j + 1], non_blocking=True)
+        wl.fused_step(k, q_src=q_step, pos_src=pos_step)
+        mask_host[i & 1].copy_(wl.mask[seq][0], non_blocking=True)
+        stat_host.copy_(wl.status, non_blocking=True)
+    e_end.record()
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_end)
+    e2e = {"value": world * E / (e2e_ms / 1000.0), "unit": "rows/s",
+           "h2d_bytes_per_step": 512 * 2 + 128 * 2 + 4, "d2h_bytes_per_step": TOKENS + 8,
+           "steps": E, "path": "qsa_index_select, pinned host buffers, eager launches"}
+    assert int(stat_host[0]) == 0
+
+    secondary = {}
+    if not args.no_secondary:
+        secondary["select_256k"] = select_256k(torch, qsa, device, hbm_gbs)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 math, u8 mask",
+        "data": "synthetic (seeded N(0,1) bf16 keys and queries, per-token log-uniform key scale)",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "budget": BUDGET, "rows_per_step": 1,
+                   "sequences_rotated": R, "bytes_per_sequence": per_seq_bytes,
+                   "l2": "inputs larger than L2 (steps rotate over the sequences)",
+                   "launch": "CUDA graphs of 256 steps; pool+score+select per step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "kernels": kernels, "clocks": clk, "e2e": e2e,
+        "gpu_launches": int(K * 2 + sum(1 for k in steps if (wl.step_params(k)[2] + 1) % 4 == 0)),
+        "secondary": secondary,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, rows, dt = oracle_decode_rate(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{rows} decode rows (pos 65280.., 64k ctx) in "
+                                          f"{dt:.1f} s on {cores} host threads"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def select_256k(torch, qsa, device, hbm_gbs):
+    """Selection at 256k: 1024 rows at p = 262143 (65536 blocks) with relu-sum-like
+    scores (70% zeros, 64 levels), budget 2048; amortised over the rows, and one
+    row at a time (rotating over the 1024 rows so inputs stay larger than L2)."""
+    tokens, rows = 262144, 1024
+    cols = tokens // 4
+    rng = qi.rng_for(4)
+    sc = torch.from_numpy(qi.stress_scores(rng, rows, cols)).to(device)
+    pos = torch.full((rows,), tokens - 1, dtype=torch.int32, device=device)
+    mask = torch.empty((rows, tokens), dtype=torch.uint8, device=device)
+    st = qsa.new_status(device)
+    for _ in range(3):
+        qsa.qsa_select_mask(sc, cols, pos, rows, tokens, BUDGET, mask, st)
+    torch.cuda.synchronize()
+    g = capture_graphs(torch, lambda k: qsa.qsa_select_mask(sc, cols, pos, rows, tokens, BUDGET,
+                                                            mask, st), list(range(10)), chunk=10)
+    ms = time_graphs(torch, g) / 10
+    byts = rows * (cols * 4 + tokens)
+    one = capture_graphs(torch, lambda k: qsa.qsa_select_mask(sc[k % rows:k % rows + 1], cols,
+                                                              pos[:1], 1, tokens, BUDGET,
+                                                              mask[k % rows:k % rows + 1], st),
+                         list(range(512)), chunk=256)
+    ms1 = time_graphs(torch, one) / 512
+    code, _ = qsa.qsa_read_status(st)
+    assert code == 0
+    return {"rows": rows, "us_per_row_amortised": ms * 1000.0 / rows, "launch_us": ms * 1000.0,
+            "achieved_gbs": byts / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": byts / (ms * 1e-3) / 1e9 / hbm_gbs,
+            "us_single_row": ms1 * 1000.0, "budget": BUDGET,
+            "context": "pages' L20 radix select: 298 us/row at 256k (context only)"}
+
+
+# ------------------------------------------------------------ ncu cases
+
+def ncu_case(name: str):
+    """Small cases for ncu captures (a few launches of one kernel)."""
+    import torch
+
+    import sparse_attention_token_qsa_gb300 as qsa
+
+    dev = torch.device("cuda:0")
+    if name in ("decode", "score", "select", "pool"):
+        wl = DecodeWorkload(torch, qsa, dev, 4)
+        for k in range(8):
+            wl.step(k)
+    elif name == "select256k":
+        select_256k(torch, qsa, dev, 6800.0)
+    torch.cuda.synchronize()
+    print("ncu case done:", name)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group("gloo")
+        run_reference(args, rank, world)
+        return
+    import torch
+
+    if args.ncu_case:
+        ncu_case(args.ncu_case)
+        return
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    run_ours(args, rank, world, device)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -122,7 +122,10 @@ qsa_status qsa_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t fir
  *  q_norm_w    DEVICE bf16[128] query norm weight (used as 1 + w).
  *  cos_t/sin_t DEVICE RoPE tables with table_rows >= tokens.
  *  block_keys  DEVICE bf16 pooled keys; row i reads block b at
- *              block_keys + (key_base[i] + b)*128.  16-byte aligned.
+ *              block_keys + (key_base[i] + b)*128.  16-byte aligned.  With
+ *              key_base == NULL the buffer must be readable for tokens/4
+ *              blocks (the tensor-core scorer fetches whole 128-block tiles;
+ *              blocks past a row's prefix are read but never used).
  *  key_base    DEVICE int64[n_rows] or NULL (= 0): per-row block offset, so one
  *              call can score rows of different sequences.
  *  scores      DEVICE f32, row stride score_cols (>= tokens/4, multiple of 4;

@@ -92,7 +92,7 @@ def pooled_prefill(orc, case, c, s):
     return orc.pool_blocks(case["fq"].reshape(-1)[512:], 640, 0, nb, case["k_norm_w"], c, s, EPS)
 
 
-@pytest.mark.parametrize("path", [1])
+@pytest.mark.parametrize("path", [1, 2])
 def test_score_prefill_all_rows(qsa, orc, tables, path):
     """Every row of the 2304-token prefill, scored against the oracle's pooled keys;
     entries past each row's prefix keep their sentinel."""
@@ -170,7 +170,8 @@ def test_score_key_base_per_sequence(qsa, orc, tables):
     assert_close(sc.cpu().numpy(), want, "per-sequence scores")
 
 
-def test_score_nan_key_propagates(qsa, orc, tables):
+@pytest.mark.parametrize("path", [1, 2])
+def test_score_nan_key_propagates(qsa, orc, tables, path):
     case = prefill_case(T=512)
     c, s, cd, sd = tables
     keys = pooled_prefill(orc, case, c, s)
@@ -179,8 +180,10 @@ def test_score_nan_key_propagates(qsa, orc, tables):
     cols = 128
     sc = torch.full((T, cols), -7.0, dtype=torch.float32, device="cuda")
     st = qsa.new_status()
-    qsa.qsa_score_rows(dev(case["fq"]), 640, dev(case["pos"]), None, T, T, dev(case["q_norm_w"]),
-                       cd, sd, c.shape[0], EPS, dev(keys), None, sc, cols, st)
+    qsa.qsa_score_rows_with(dev(case["fq"]), 640, dev(case["pos"]), None, T, T,
+                            dev(case["q_norm_w"]), cd, sd, c.shape[0], EPS, dev(keys), None, sc,
+                            cols, st, path=path)
+    assert qsa.qsa_read_status(st) == (0, 0)
     got = sc.cpu().numpy()
     rows_seeing = np.arange(T)[(np.arange(T) + 1) // 4 > 37]
     assert np.all(np.isnan(got[rows_seeing, 37]))
@@ -203,3 +206,76 @@ def test_score_row_range_errors(qsa, tables):
         code, row = qsa.qsa_read_status(st)
         assert (code, row) == (3, bad)
         assert np.all(sc.cpu().numpy()[bad] == -7.0)
+
+
+@pytest.mark.parametrize("n_rows,tokens,seed", [(100, 3000, 1), (64, 520, 2), (1, 9000, 3),
+                                                (257, 4100, 4)])
+def test_score_tc_ragged_tiles(qsa, orc, tables, n_rows, tokens, seed):
+    """Tensor-core scorer on ragged shapes: rows not a multiple of the 64-row tile,
+    block counts not a multiple of the 128-block tile, arbitrary positions and
+    visible lengths (including empty prefixes), one invalid row."""
+    rng = qi.rng_for(2, salt=seed)
+    c, s, cd, sd = tables
+    raw = qi.raw_keys(rng, tokens)
+    qw, kw = qi.norm_weights(rng)
+    nb = tokens // 4
+    keys = orc.pool_blocks(raw, 128, 0, nb, kw, c, s, EPS)
+    q = qi.fused_qk(rng, n_rows)
+    pos = rng.integers(0, tokens, size=n_rows).astype(np.int32)
+    pos[: min(4, n_rows)] = np.arange(min(4, n_rows))
+    vis = (pos + 1).astype(np.int32)
+    cut = rng.random(n_rows) < 0.3
+    vis[cut] = rng.integers(0, pos[cut] + 2).astype(np.int32)
+    cols = nb + 4 - nb % 4 + 4
+    sc = torch.full((n_rows, cols), -7.0, dtype=torch.float32, device="cuda")
+    st = qsa.new_status()
+    qsa.qsa_score_rows_with(dev(q), 640, dev(pos), dev(vis), n_rows, tokens, dev(qw), cd, sd,
+                            c.shape[0], EPS, dev(keys), None, sc, cols, st, path=2)
+    assert qsa.qsa_read_status(st) == (0, 0)
+    want, _ = oracle_scores(orc, q, 640, pos, tokens, qw, c, s, keys, cols, visible_len=vis)
+    assert_close(sc.cpu().numpy(), want, f"tcgen05 scores {n_rows}x{tokens}")
+    if n_rows >= 3:   # an out-of-range row is reported and left untouched
+        pos_bad = pos.copy()
+        pos_bad[2] = tokens
+        sc.fill_(-7.0)
+        st = qsa.new_status()
+        qsa.qsa_score_rows_with(dev(q), 640, dev(pos_bad), None, n_rows, tokens, dev(qw), cd, sd,
+                                c.shape[0], EPS, dev(keys), None, sc, cols, st, path=2)
+        assert qsa.qsa_read_status(st) == (3, 2)
+        got = sc.cpu().numpy()
+        assert np.all(got[2] == -7.0)
+        want2, _ = oracle_scores(orc, q, 640, pos, tokens, qw, c, s, keys, cols)
+        keep = np.ones(n_rows, bool)
+        keep[2] = False
+        assert_close(got[keep], want2[keep], "tcgen05 scores beside a bad row")
+
+
+def test_score_tc_chunk_64k_sampled(qsa, orc, tables):
+    """Chunked prefill: 4096 rows at positions 61440..65535 of a 64k sequence,
+    the [16384, 128] x [128, 16384] contraction; sampled rows against the oracle,
+    the sentinel on every row past its prefix."""
+    rng = qi.rng_for(2)
+    c, s, cd, sd = tables
+    tokens, first, rows = 65536, 61440, 4096
+    raw = qi.raw_keys(rng, tokens)
+    qw, kw = qi.norm_weights(rng)
+    keys_d = torch.zeros((tokens // 4, 128), dtype=torch.int16, device="cuda")
+    qsa.qsa_pool_blocks(dev(raw).view(-1), 128, 0, tokens // 4, dev(kw), cd, sd, c.shape[0], EPS,
+                        keys_d)
+    keys = keys_d.cpu().numpy().view(np.uint16)
+    q = qi.fused_qk(rng, rows)
+    pos = np.arange(first, first + rows, dtype=np.int32)
+    cols = tokens // 4
+    sc = torch.full((rows, cols), -7.0, dtype=torch.float32, device="cuda")
+    st = qsa.new_status()
+    qsa.qsa_score_rows(dev(q), 640, dev(pos), None, rows, tokens, dev(qw), cd, sd, c.shape[0], EPS,
+                       keys_d, None, sc, cols, st)
+    assert qsa.qsa_read_status(st) == (0, 0)
+    got = sc.cpu().numpy()
+    n = (pos + 1) // 4
+    for i in range(rows):
+        assert np.all(got[i, n[i]:] == -7.0)
+    sample = np.unique(np.concatenate([np.arange(0, 4), np.arange(60, 68), np.arange(rows - 4, rows),
+                                       rng.choice(rows, 40, replace=False)]))
+    want, _ = oracle_scores(orc, q[sample], 640, pos[sample], tokens, qw, c, s, keys, cols)
+    assert_close(got[sample], want, "64k chunk scores (sampled rows)")

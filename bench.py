@@ -448,6 +448,8 @@ def run_ours(args, rank, world, device):
     secondary = {}
     if not args.no_secondary:
         secondary["select_256k"] = select_256k(torch, qsa, device, hbm_gbs)
+        secondary["prefill_chunk_64k"] = prefill_chunk(torch, qsa, device, hbm_gbs, bf16_tf)
+        secondary["decode_long_32seq"] = decode_long(torch, qsa, device, hbm_gbs)
 
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
@@ -472,7 +474,7 @@ def run_ours(args, rank, world, device):
         print(json.dumps(line), flush=True)
 
 
-def select_256k(torch, qsa, device, hbm_gbs):
+def select_256k(torch, qsa, device, hbm_gbs, ncu=False):
     """Selection at 256k: 1024 rows at p = 262143 (65536 blocks) with relu-sum-like
     scores (70% zeros, 64 levels), budget 2048; amortised over the rows, and one
     row at a time (rotating over the 1024 rows so inputs stay larger than L2)."""
@@ -483,9 +485,11 @@ def select_256k(torch, qsa, device, hbm_gbs):
     pos = torch.full((rows,), tokens - 1, dtype=torch.int32, device=device)
     mask = torch.empty((rows, tokens), dtype=torch.uint8, device=device)
     st = qsa.new_status(device)
-    for _ in range(3):
+    for _ in range(2 if ncu else 3):
         qsa.qsa_select_mask(sc, cols, pos, rows, tokens, BUDGET, mask, st)
     torch.cuda.synchronize()
+    if ncu:
+        return None
     g = capture_graphs(torch, lambda k: qsa.qsa_select_mask(sc, cols, pos, rows, tokens, BUDGET,
                                                             mask, st), list(range(10)), chunk=10)
     ms = time_graphs(torch, g) / 10
@@ -503,21 +507,167 @@ def select_256k(torch, qsa, device, hbm_gbs):
             "context": "pages' L20 radix select: 298 us/row at 256k (context only)"}
 
 
+def time_fn(torch, fn, iters):
+    g = capture_graphs(torch, lambda k: fn(), list(range(iters)), chunk=iters)
+    return time_graphs(torch, g) / iters
+
+
+def prefill_chunk(torch, qsa, device, hbm_gbs, bf16_tf, ncu=False):
+    """Chunked prefill: a 4096-row chunk at positions 61440..65535 of a 64k
+    sequence.  Pool the chunk's 1024 new blocks, score 4096 rows on the tensor
+    cores ([16384, 128] x [128, 16384] with the relu / head-sum epilogue), select."""
+    tokens, first, rows = 65536, 61440, 4096
+    nb = tokens // 4
+    c, s = qsa.qsa_rope_tables(tokens, THETA)
+    cd, sd = dev_tensor(torch, c, device), dev_tensor(torch, s, device)
+    rng = qi.rng_for(2)
+    qw, kw = qi.norm_weights(rng)
+    qw, kw = dev_tensor(torch, qw, device), dev_tensor(torch, kw, device)
+    raw = qi.torch_normal_bf16(torch, (tokens, 128), qi.seed_for(2, 1), device)
+    fq = qi.torch_normal_bf16(torch, (rows, 640), qi.seed_for(2, 2), device)
+    cache = torch.zeros((nb, 128), dtype=torch.int16, device=device)
+    qsa.qsa_pool_blocks(raw.view(-1), 128, 0, first // 4, kw, cd, sd, tokens, EPS, cache)
+    pos = torch.arange(first, tokens, dtype=torch.int32, device=device)
+    sc = torch.empty((rows, nb), dtype=torch.float32, device=device)
+    mask = torch.empty((rows, tokens), dtype=torch.uint8, device=device)
+    st = qsa.new_status(device)
+
+    def pool():
+        qsa.qsa_pool_blocks(raw[first:].reshape(-1), 128, first // 4, 1024, kw, cd, sd, tokens,
+                            EPS, cache)
+
+    def score():
+        qsa.qsa_score_rows(fq, 640, pos, None, rows, tokens, qw, cd, sd, tokens, EPS, cache, None,
+                           sc, nb, st)
+
+    def select():
+        qsa.qsa_select_mask(sc, nb, pos, rows, tokens, BUDGET, mask, st)
+
+    def step():
+        pool()
+        score()
+        select()
+
+    for _ in range(2 if ncu else 3):
+        step()
+    torch.cuda.synchronize()
+    if ncu:
+        return None
+    it = 10
+    t_step = time_fn(torch, step, it)
+    t_pool = time_fn(torch, pool, it)
+    t_score = time_fn(torch, score, it)
+    t_sel = time_fn(torch, select, it)
+    code, row = qsa.qsa_read_status(st)
+    assert code == 0, (code, row)
+    live = int(sum((p + 1) // 4 for p in range(first, tokens)))
+    flops = 1024.0 * live
+    score_bytes = 4.0 * live + nb * 256 + rows * 512 * 2
+    sel_bytes = 4.0 * live + rows * tokens
+    pool_bytes = 1024 * POOL_BYTES_PER_BLOCK
+    return {
+        "rows": rows, "rows_per_s": rows / (t_step * 1e-3), "step_us": t_step * 1000.0,
+        "pool": {"us": t_pool * 1000.0, "blocks": 1024,
+                 "frac_of_measured_hbm": pool_bytes / (t_pool * 1e-3) / 1e9 / hbm_gbs},
+        "score_tcgen05": {"us": t_score * 1000.0, "live_scores": live,
+                          "achieved_tflops": flops / (t_score * 1e-3) / 1e12,
+                          "frac_of_measured_bf16": flops / (t_score * 1e-3) / 1e12 / bf16_tf,
+                          "achieved_gbs": score_bytes / (t_score * 1e-3) / 1e9,
+                          "frac_of_measured_hbm": score_bytes / (t_score * 1e-3) / 1e9 / hbm_gbs},
+        "select": {"us": t_sel * 1000.0, "achieved_gbs": sel_bytes / (t_sel * 1e-3) / 1e9,
+                   "frac_of_measured_hbm": sel_bytes / (t_sel * 1e-3) / 1e9 / hbm_gbs},
+    }
+
+
+def decode_long(torch, qsa, device, hbm_gbs, ncu=False):
+    """Decode at long context: 32 sequences, one row each, lengths U[131072, 262144],
+    per-sequence key caches addressed by key_base, score_cols 65536, tokens 262144.
+    Also times pooling every complete block of all 32 sequences (the pool
+    throughput case)."""
+    n_seq, tokens = 32, 262144
+    rng = qi.rng_for(3)
+    lens = qi.long_context_lengths(rng, n_seq)
+    nbs = lens // 4
+    c, s = qsa.qsa_rope_tables(tokens, THETA)
+    cd, sd = dev_tensor(torch, c, device), dev_tensor(torch, s, device)
+    qw, kw = qi.norm_weights(rng)
+    qw, kw = dev_tensor(torch, qw, device), dev_tensor(torch, kw, device)
+    tok_off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    blk_off = np.concatenate([[0], np.cumsum(nbs)]).astype(np.int64)
+    raw = qi.torch_normal_bf16(torch, (int(tok_off[-1]), 128), qi.seed_for(3, 1), device)
+    cache = torch.zeros((int(blk_off[-1]) + 8, 128), dtype=torch.int16, device=device)
+
+    def pool_all():
+        for i in range(n_seq):
+            qsa.qsa_pool_blocks(raw[tok_off[i]:tok_off[i + 1]].reshape(-1), 128, 0, int(nbs[i]),
+                                kw, cd, sd, tokens, EPS, cache[blk_off[i]:])
+
+    pool_all()
+    q = qi.torch_normal_bf16(torch, (n_seq, 512), qi.seed_for(3, 2), device)
+    pos = torch.from_numpy((lens - 1).astype(np.int32)).to(device)
+    base = torch.from_numpy(blk_off[:-1].copy()).to(device)
+    cols = 65536
+    sc = torch.empty((n_seq, cols), dtype=torch.float32, device=device)
+    mask = torch.empty((n_seq, tokens), dtype=torch.uint8, device=device)
+    st = qsa.new_status(device)
+
+    def score():
+        qsa.qsa_score_rows(q, 512, pos, None, n_seq, tokens, qw, cd, sd, tokens, EPS, cache, base,
+                           sc, cols, st)
+
+    def select():
+        qsa.qsa_select_mask(sc, cols, pos, n_seq, tokens, BUDGET, mask, st)
+
+    for _ in range(2 if ncu else 3):
+        score()
+        select()
+    torch.cuda.synchronize()
+    if ncu:
+        return None
+    t_pool = time_fn(torch, pool_all, 3)
+    t_score = time_fn(torch, score, 10)
+    t_sel = time_fn(torch, select, 10)
+    code, row = qsa.qsa_read_status(st)
+    assert code == 0, (code, row)
+    blocks = int(nbs.sum())
+    sb = SCORE_BYTES_PER_BLOCK * blocks
+    selb = 4 * blocks + n_seq * tokens
+    pb = POOL_BYTES_PER_BLOCK * blocks
+    return {
+        "sequences": n_seq, "blocks": blocks, "rows_per_s": n_seq / ((t_score + t_sel) * 1e-3),
+        "score": {"us": t_score * 1000.0, "achieved_gbs": sb / (t_score * 1e-3) / 1e9,
+                  "frac_of_measured_hbm": sb / (t_score * 1e-3) / 1e9 / hbm_gbs},
+        "select": {"us": t_sel * 1000.0, "achieved_gbs": selb / (t_sel * 1e-3) / 1e9,
+                   "frac_of_measured_hbm": selb / (t_sel * 1e-3) / 1e9 / hbm_gbs},
+        "pool_all_blocks": {"us": t_pool * 1000.0, "launches": n_seq,
+                            "achieved_gbs": pb / (t_pool * 1e-3) / 1e9,
+                            "frac_of_measured_hbm": pb / (t_pool * 1e-3) / 1e9 / hbm_gbs},
+    }
+
+
 # ------------------------------------------------------------ ncu cases
 
 def ncu_case(name: str):
-    """Small cases for ncu captures (a few launches of one kernel)."""
+    """Small eager cases for ncu captures: a few launches of each kernel, no
+    timing, no graphs."""
     import torch
 
     import sparse_attention_token_qsa_gb300 as qsa
 
     dev = torch.device("cuda:0")
-    if name in ("decode", "score", "select", "pool"):
+    torch.cuda.set_device(dev)
+    if name == "decode":
         wl = DecodeWorkload(torch, qsa, dev, 4)
         for k in range(8):
             wl.step(k)
+    elif name == "prefill":
+        prefill_chunk(torch, qsa, dev, 6800.0, 1900.0, ncu=True)
     elif name == "select256k":
-        select_256k(torch, qsa, dev, 6800.0)
+        select_256k(torch, qsa, dev, 6800.0, ncu=True)
+    elif name == "decode_long":
+        decode_long(torch, qsa, dev, 6800.0, ncu=True)
+    else:
+        raise SystemExit(f"unknown ncu case {name}")
     torch.cuda.synchronize()
     print("ncu case done:", name)
 

@@ -114,3 +114,15 @@ def long_context_lengths(rng: np.random.Generator, n_seq: int, lo: int = 131072,
                          hi: int = 262144) -> np.ndarray:
     """Sequence lengths drawn uniformly from [lo, hi] (inclusive)."""
     return rng.integers(lo, hi + 1, size=n_seq).astype(np.int64)
+
+
+def torch_normal_bf16(torch, shape, seed: int, device, std: float = 1.0, token_scale: bool = False):
+    """Large N(0,1) bf16 draws made on the device by torch's seeded generator
+    (for benchmark-sized buffers; the oracle never sees these)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std
+    if token_scale:
+        u = torch.rand((shape[0], 1), generator=g, device=device, dtype=torch.float32)
+        x = x * torch.exp(np.log(0.25) + u * (np.log(4.0) - np.log(0.25)))
+    return x.to(torch.bfloat16).view(torch.int16)

@@ -12,19 +12,23 @@
 //     D[rows*4, blocks] = Q[rows*4, 128] x K[blocks, 128]^T
 // is a dense bf16 GEMM with K = 128, so it runs as tcgen05.mma.
 //
-// CTA tile: 64 query rows (two M = 128 halves, M index = 4 * row + head) x
-// 128 blocks (N) per step, K = 128 in 8 MMAs of K = 16.
+// CTA tile: 128 blocks (M, the TMEM lanes) x 64 query rows * 4 heads (N = 256,
+// column = 4 * row + head), K = 128 in 8 MMAs of K = 16.  With the heads on N,
+// one TMEM lane (one thread of the epilogue) holds a block's dot with all four
+// heads of a row in four adjacent columns, so the relu and the head sum are
+// register-local and each warp store writes 32 consecutive blocks of one row.
 //  * the CTA prepares its 64 rows' heads itself (norm + RoPE, exact sums like
 //    the pooling kernel) and writes them into shared memory in the 128-byte
-//    swizzled K-major layout the MMA descriptors expect;
-//  * warp 0 (one lane) streams block-key tiles with TMA (128B swizzle) into a
-//    4-stage ring guarded by mbarriers;
+//    swizzled K-major layout the MMA descriptors expect (the B operand);
+//  * warp 0 (one lane) streams block-key tiles (the A operand) with TMA
+//    (128B swizzle) into a 4-stage ring guarded by mbarriers;
 //  * warp 1 (one lane) issues the MMAs into one of two TMEM accumulators
-//    (2 halves x 128 columns each, 512 columns in all) and commits to
-//    mbarriers that free the key stage and publish the accumulator;
-//  * warps 4..11 drain the accumulator: tcgen05.ld 32 columns, relu, a
-//    4-lane reduce-scatter sums the heads (each lane ends with 8 contiguous
-//    columns of one row), scale, and 2 x 16-byte stores per lane;
+//    (256 columns each, 512 in all) and commits to mbarriers that free the key
+//    stage and publish the accumulator;
+//  * warps 4..11 drain the accumulator: warp w reads TMEM lane quarter w % 4
+//    (32 blocks) and one half of the columns (32 rows), 32 columns per
+//    tcgen05.ld, relu per head, ((h0 + h1) + h2) + h3, scale, coalesced stores
+//    of the blocks each row can see;
 //  * every mbarrier wait is bounded: on timeout the kernel records
 //    QSA_ERR_TIMEOUT, lets the other roles drop out, drains its own MMAs and
 //    frees its TMEM.
@@ -45,13 +49,14 @@ constexpr int kStages = 4;
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 8;
-constexpr uint32_t kAHalf = 128 * 128 * 2;   // one M-half: 128 rows x 128 dims bf16 (32 KiB)
-constexpr uint32_t kAChunk = 128 * 128;      // 64 dims x 128 rows (16 KiB)
-constexpr uint32_t kBStage = kBN * 128 * 2;  // 32 KiB
-constexpr uint32_t kBChunk = kBN * 128;      // 16 KiB
-constexpr uint32_t kAOff = 0;
-constexpr uint32_t kBOff = 2 * kAHalf;
-constexpr uint32_t kCtrlOff = kBOff + kStages * kBStage;
+constexpr int kQCols = kRowsPerCta * 4;       // N = 256 query-head rows
+constexpr uint32_t kQChunk = kQCols * 128;     // 64 dims x 256 rows (32 KiB)
+constexpr uint32_t kQBytes = 2 * kQChunk;      // the whole query tile (64 KiB)
+constexpr uint32_t kKStage = kBN * 128 * 2;    // one key tile: 128 blocks x 128 dims (32 KiB)
+constexpr uint32_t kKChunk = kBN * 128;        // 64 dims x 128 blocks (16 KiB)
+constexpr uint32_t kQOff = 0;
+constexpr uint32_t kKOff = kQBytes;
+constexpr uint32_t kCtrlOff = kKOff + kStages * kKStage;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kSpinLimit = 4000000000LL;  // ~2 s of SM clock
 
@@ -140,9 +145,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: D f32, A/B bf16, both K-major, M = 128, N = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(128 >> 4) << 24);
+// Instruction descriptor, kind::f16: D f32, A/B bf16, both K-major, M = 128, N = 256.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kQCols >> 3) << 17) |
+                            ((uint32_t)(kBN >> 4) << 24);
 
 __device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t accumulate) {
@@ -189,8 +194,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl &C = *reinterpret_cast<Ctrl *>(smem + kCtrlOff);
-  const uint32_t sA = smem_u32(smem + kAOff);
-  const uint32_t sB = smem_u32(smem + kBOff);
+  const uint32_t sQ = smem_u32(smem + kQOff);
+  const uint32_t sK = smem_u32(smem + kKOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = blockIdx.x * kRowsPerCta;
@@ -237,7 +242,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
   __syncthreads();
   tc_fence_after();
 
-  // ---- query heads of the 64 rows into the swizzled A tile
+  // ---- query heads of the 64 rows into the swizzled B (N-side) tile
   for (int pair = warp; pair < kRowsPerCta * kHeads / 2; pair += kThreads / 32) {
     const int vec = pair * 2 + (lane >> 4);
     const int rl = vec >> 2, h = vec & 3, g = lane & 15;
@@ -256,13 +261,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
     unpack8(v, x);
     uint4 o = norm_rope_16(x, w8, c8, s8, a.eps, g);
     if (!valid) o = make_uint4(0, 0, 0, 0);
-    const int half = rl >> 5;
-    const int m = 4 * (rl & 31) + h;
+    const int n = 4 * rl + h;
     const int chunk = g >> 3, unit = g & 7;
-    uint8_t *dst = smem + kAOff + half * kAHalf + chunk * kAChunk + m * 128 + ((unit ^ (m & 7)) << 4);
+    uint8_t *dst = smem + kQOff + chunk * kQChunk + n * 128 + ((unit ^ (n & 7)) << 4);
     *reinterpret_cast<uint4 *>(dst) = o;
   }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // A is read by the tensor core
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by the tensor core
   __syncthreads();
 
   const int32_t max_n = C.max_n;
@@ -284,10 +288,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
         const uint32_t it = (uint32_t)(i / kStages);
         if (!mbar_wait(smem_u32(&C.empty[s]), (it & 1u) ^ 1u, abort_flag)) break;
         const uint32_t fb = smem_u32(&C.full[s]);
-        mbar_expect_tx(fb, kBStage);
+        mbar_expect_tx(fb, kKStage);
         const int n0 = (t_begin + i) * kBN;
-        tma_load_2d(sB + s * kBStage, &kmap, 0, n0, fb);
-        tma_load_2d(sB + s * kBStage + kBChunk, &kmap, 64, n0, fb);
+        tma_load_2d(sK + s * kKStage, &kmap, 0, n0, fb);
+        tma_load_2d(sK + s * kKStage + kKChunk, &kmap, 64, n0, fb);
         issued = i + 1;
       }
       if (*abort_flag) {  // let our own copies land before the CTA leaves
@@ -308,14 +312,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
         if (!mbar_wait(smem_u32(&C.full[s]), it & 1u, abort_flag)) break;
         tc_fence_after();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t koff = (uint32_t)(kk >> 2) * kAChunk + (uint32_t)(kk & 3) * 32u;
-            const uint64_t ad = sw128_desc(sA + half * kAHalf + koff);
-            const uint64_t bd = sw128_desc(sB + s * kBStage + koff);
-            mma_bf16(tmem + (uint32_t)(buf * 256 + half * 128), ad, bd, kk > 0 ? 1u : 0u);
-          }
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t kin = (uint32_t)(kk & 3) * 32u;  // K step inside the 128-byte swizzle row
+          const uint64_t ad = sw128_desc(sK + s * kKStage + (uint32_t)(kk >> 2) * kKChunk + kin);
+          const uint64_t bd = sw128_desc(sQ + (uint32_t)(kk >> 2) * kQChunk + kin);
+          mma_bf16(tmem + (uint32_t)(buf * kQCols), ad, bd, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&C.empty[s]));
         mma_commit(smem_u32(&C.tfull[buf]));
@@ -328,59 +329,33 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
     }
   } else if (warp >= kEpiWarp0) {
     // ---- epilogue: TMEM -> relu -> head sum -> scale -> scores
-    const int e = warp - kEpiWarp0;
-    const int half = e >> 2;
-    const int quarter = warp & 3;  // the TMEM lane quarter this warp may read
-    const int rl = half * 32 + quarter * 8 + (lane >> 2);
-    const int h = lane & 3;
-    const int row = row0 + rl;
-    const int32_t n_r = C.row_n[rl];
-    float *srow = a.scores + (int64_t)row * a.score_cols;
+    const int quarter = warp & 3;               // the TMEM lane quarter this warp may read
+    const int chalf = (warp - kEpiWarp0) >> 2;  // which 32 rows (128 columns) it drains
     const float inv_sqrt_hd = 0.08838834764831845f;
     for (int i = 0; i < ntiles; ++i) {
       const int buf = i & 1;
       const uint32_t ja = (uint32_t)(i >> 1);
       if (!warp_wait(smem_u32(&C.tfull[buf]), ja & 1u, abort_flag)) break;
       tc_fence_after();
-      const int n0 = (t_begin + i) * kBN;
+      const int b = (t_begin + i) * kBN + quarter * 32 + lane;  // this thread's block
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * 256 + half * 128 + c * 32), v);
-        float r[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float d = __uint_as_float(v[j]);
-          r[j] = (d < 0.f) ? 0.f : d;  // relu per head; NaN stays NaN
-        }
-        // 4-lane reduce-scatter over the heads: lane h keeps columns 8h..8h+7
-        const bool hi2 = (h & 2) != 0;
-        float w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float keep = hi2 ? r[16 + j] : r[j];
-          const float send = hi2 ? r[j] : r[16 + j];
-          w[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        }
-        const bool hi1 = (h & 1) != 0;
-        float o[8];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) +
+                      (uint32_t)(buf * kQCols + chalf * 128 + c * 32),
+                  v);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float keep = hi1 ? w[8 + j] : w[j];
-          const float send = hi1 ? w[j] : w[8 + j];
-          o[j] = __fmul_rn(keep + __shfl_xor_sync(0xffffffffu, send, 1), inv_sqrt_hd);
-        }
-        const int col = n0 + c * 32 + 8 * h;
-        if (n_r > 0 && col < n_r) {
-          if (col + 8 <= n_r) {
-            float4 *dst = reinterpret_cast<float4 *>(srow + col);
-            dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-            dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-          } else {
+          const int rl = chalf * 32 + c * 8 + j;
+          float hs[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (col + j < n_r) srow[col + j] = o[j];
+          for (int hh = 0; hh < 4; ++hh) {
+            const float d = __uint_as_float(v[4 * j + hh]);
+            hs[hh] = (d < 0.f) ? 0.f : d;  // relu per head; NaN stays NaN
           }
+          const float sum = __fadd_rn(__fadd_rn(__fadd_rn(hs[0], hs[1]), hs[2]), hs[3]);
+          if (b < C.row_n[rl])
+            a.scores[(int64_t)(row0 + rl) * a.score_cols + b] = __fmul_rn(sum, inv_sqrt_hd);
         }
       }
       tc_fence_before();
@@ -456,10 +431,20 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream) {
   }
   const int32_t row_tiles = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
   const int32_t tiles_total = (int32_t)((n_cap + kBN - 1) / kBN);
-  int32_t splits = (sm_count() + row_tiles - 1) / row_tiles;
-  if (splits < 1) splits = 1;
-  if (splits > tiles_total) splits = tiles_total;
-  if (splits > 65535) splits = 65535;
+  // one CTA per SM: pick the split of the N tiles that minimises
+  // waves x tiles-per-CTA (the critical path), fewer CTAs on a tie
+  const int64_t sms = sm_count();
+  int32_t splits = 1;
+  int64_t best = -1;
+  for (int32_t sp = 1; sp <= tiles_total && sp <= 65535; ++sp) {
+    const int64_t waves = ((int64_t)row_tiles * sp + sms - 1) / sms;
+    const int64_t cost = waves * ((tiles_total + sp - 1) / sp);
+    if (best < 0 || cost < best) {
+      best = cost;
+      splits = sp;
+    }
+    if ((int64_t)row_tiles * sp > 64 * sms) break;
+  }
   const int32_t per_split = (tiles_total + splits - 1) / splits;
   dim3 grid((unsigned)row_tiles, (unsigned)splits);
   score_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map, a, tiles_total, per_split);

@@ -332,6 +332,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
     const int quarter = warp & 3;               // the TMEM lane quarter this warp may read
     const int chalf = (warp - kEpiWarp0) >> 2;  // which 32 rows (128 columns) it drains
     const float inv_sqrt_hd = 0.08838834764831845f;
+    float *const srow0 = a.scores + (int64_t)(row0 + chalf * 32) * a.score_cols;
+    const int64_t ld = a.score_cols;
     for (int i = 0; i < ntiles; ++i) {
       const int buf = i & 1;
       const uint32_t ja = (uint32_t)(i >> 1);
@@ -340,23 +342,30 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
       const int b = (t_begin + i) * kBN + quarter * 32 + lane;  // this thread's block
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
+        // the 8 rows' visible block counts, read before any store of this chunk
+        // so the stores below never force a reload
+        int32_t lim[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) lim[j] = C.row_n[chalf * 32 + c * 8 + j];
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) +
                       (uint32_t)(buf * kQCols + chalf * 128 + c * 32),
                   v);
+        float out[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int rl = chalf * 32 + c * 8 + j;
           float hs[4];
 #pragma unroll
           for (int hh = 0; hh < 4; ++hh) {
             const float d = __uint_as_float(v[4 * j + hh]);
             hs[hh] = (d < 0.f) ? 0.f : d;  // relu per head; NaN stays NaN
           }
-          const float sum = __fadd_rn(__fadd_rn(__fadd_rn(hs[0], hs[1]), hs[2]), hs[3]);
-          if (b < C.row_n[rl])
-            a.scores[(int64_t)(row0 + rl) * a.score_cols + b] = __fmul_rn(sum, inv_sqrt_hd);
+          out[j] = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(hs[0], hs[1]), hs[2]), hs[3]), inv_sqrt_hd);
         }
+        float *dst = srow0 + (int64_t)(c * 8) * ld + b;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (b < lim[j]) dst[(int64_t)j * ld] = out[j];
       }
       tc_fence_before();
       __syncwarp();

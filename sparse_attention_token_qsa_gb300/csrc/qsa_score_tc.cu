@@ -440,14 +440,16 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream) {
   }
   const int32_t row_tiles = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
   const int32_t tiles_total = (int32_t)((n_cap + kBN - 1) / kBN);
-  // one CTA per SM: pick the split of the N tiles that minimises
-  // waves x tiles-per-CTA (the critical path), fewer CTAs on a tie
+  // one CTA per SM: pick the split of the N tiles that minimises the critical
+  // path, waves x (tiles per CTA + the CTA's fixed cost: query prep, TMEM
+  // allocation, pipeline fill ~ 3 tiles), fewer CTAs on a tie
   const int64_t sms = sm_count();
+  constexpr int64_t kCtaOverheadTiles = 3;
   int32_t splits = 1;
   int64_t best = -1;
   for (int32_t sp = 1; sp <= tiles_total && sp <= 65535; ++sp) {
     const int64_t waves = ((int64_t)row_tiles * sp + sms - 1) / sms;
-    const int64_t cost = waves * ((tiles_total + sp - 1) / sp);
+    const int64_t cost = waves * ((tiles_total + sp - 1) / sp + kCtaOverheadTiles);
     if (best < 0 || cost < best) {
       best = cost;
       splits = sp;

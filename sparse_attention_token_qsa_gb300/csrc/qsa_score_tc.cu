@@ -187,6 +187,58 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+        "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// relu that keeps NaN (max.NaN returns NaN when either input is NaN)
+__device__ __forceinline__ float relu_nan(float d) {
+  float r;
+  asm("max.NaN.f32 %0, %1, 0f00000000;" : "=f"(r) : "f"(d));
+  return r;
+}
+
+// Reduce one 32-column chunk (8 rows x 4 heads) held in `cur` to 8 scores and
+// store the ones inside each row's visible prefix; before that, start the TMEM
+// load of the next chunk into `nxt` (when `prefetch`), and wait for it after.
+__device__ __forceinline__ void drain_chunk(const uint32_t (&cur)[32], int c, uint32_t tbase,
+                                            uint32_t (&nxt)[32], bool prefetch,
+                                            const int32_t *row_n, float *srow0, int64_t ld, int b,
+                                            float inv_sqrt_hd) {
+  int32_t lim[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) lim[j] = row_n[c * 8 + j];
+  if (prefetch) tmem_ld32_async(tbase + (uint32_t)((c + 1) * 32), nxt);
+  float out[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float h0 = relu_nan(__uint_as_float(cur[4 * j + 0]));
+    const float h1 = relu_nan(__uint_as_float(cur[4 * j + 1]));
+    const float h2 = relu_nan(__uint_as_float(cur[4 * j + 2]));
+    const float h3 = relu_nan(__uint_as_float(cur[4 * j + 3]));
+    out[j] = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(h0, h1), h2), h3), inv_sqrt_hd);
+  }
+  float *dst = srow0 + (int64_t)(c * 8) * ld + b;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (b < lim[j]) dst[(int64_t)j * ld] = out[j];
+  if (prefetch) tmem_wait_ld();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int32_t tiles_total,
                 int32_t tiles_per_split) {
@@ -340,33 +392,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
       if (!warp_wait(smem_u32(&C.tfull[buf]), ja & 1u, abort_flag)) break;
       tc_fence_after();
       const int b = (t_begin + i) * kBN + quarter * 32 + lane;  // this thread's block
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        // the 8 rows' visible block counts, read before any store of this chunk
-        // so the stores below never force a reload
-        int32_t lim[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) lim[j] = C.row_n[chalf * 32 + c * 8 + j];
-        uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) +
-                      (uint32_t)(buf * kQCols + chalf * 128 + c * 32),
-                  v);
-        float out[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float hs[4];
-#pragma unroll
-          for (int hh = 0; hh < 4; ++hh) {
-            const float d = __uint_as_float(v[4 * j + hh]);
-            hs[hh] = (d < 0.f) ? 0.f : d;  // relu per head; NaN stays NaN
-          }
-          out[j] = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(hs[0], hs[1]), hs[2]), hs[3]), inv_sqrt_hd);
-        }
-        float *dst = srow0 + (int64_t)(c * 8) * ld + b;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (b < lim[j]) dst[(int64_t)j * ld] = out[j];
-      }
+      const uint32_t tbase =
+          tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kQCols + chalf * 128);
+      // TMEM loads are pipelined: chunk c+1 is in flight while chunk c is reduced
+      uint32_t va[32], vb[32];
+      tmem_ld32_async(tbase, va);
+      tmem_wait_ld();
+      drain_chunk(va, 0, tbase, vb, true, C.row_n + chalf * 32, srow0, ld, b, inv_sqrt_hd);
+      drain_chunk(vb, 1, tbase, va, true, C.row_n + chalf * 32, srow0, ld, b, inv_sqrt_hd);
+      drain_chunk(va, 2, tbase, vb, true, C.row_n + chalf * 32, srow0, ld, b, inv_sqrt_hd);
+      drain_chunk(vb, 3, tbase, va, false, C.row_n + chalf * 32, srow0, ld, b, inv_sqrt_hd);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&C.tempty[buf]));

@@ -60,16 +60,24 @@ constexpr uint32_t kCtrlOff = kKOff + kStages * kKStage;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kSpinLimit = 4000000000LL;  // ~2 s of SM clock
 
+constexpr int kPrepWarps = 10;              // warps 2..11 prepare the query tile
+constexpr int kPairs = kRowsPerCta * kHeads / 2;  // (row, head) vectors, two per warp step
+constexpr int kMaxRowTiles = 1024;           // per-row-tile balancing up to 65536 rows
+
 struct Ctrl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t qfree;
+  uint64_t qready;
   uint32_t tmem_base;
   int32_t abort;
-  int32_t max_n;
-  int32_t row_n[kRowsPerCta];
+  int32_t row_n[2][kRowsPerCta];  // by row-tile switch parity
+  int32_t row_p[2][kRowsPerCta];
+  int32_t need[kMaxRowTiles];
+  int32_t start[kMaxRowTiles + 2];
 };
 
 constexpr size_t kSmemBytes = kCtrlOff + sizeof(Ctrl) + 1024;  // + alignment slack
@@ -239,20 +247,120 @@ __device__ __forceinline__ void drain_chunk(const uint32_t (&cur)[32], int c, ui
   if (prefetch) tmem_wait_ld();
 }
 
+// Query prep for row tile `rt` by warps 2..11: the rows' visible block counts
+// and positions into row_n/row_p (read by the epilogue after the q_ready
+// barrier), and every (row, head) vector normed, rotated and written to the
+// swizzled B tile.  No intra-group barrier: each vector reads its row's
+// position itself; loads are batched four vectors deep per half-warp.
+__device__ __forceinline__ void prep_row_tile(const ScoreArgs &a, uint8_t *smem, int32_t *row_p,
+                                              int32_t *row_n, int rt, int warp, int lane) {
+  const int qt = (warp - 2) * 32 + lane;  // 0..319
+  if (qt < kRowsPerCta) {
+    const int row = rt * kRowsPerCta + qt;
+    int32_t n = 0, p = 0;
+    if (row < a.n_rows) {
+      p = a.pos[row];
+      const int32_t vis = a.visible_len ? a.visible_len[row] : p + 1;
+      if (p < 0 || p >= a.tokens || vis < 0 || vis > p + 1) {
+        n = -1;
+        p = 0;
+      } else {
+        n = vis >> 2;
+      }
+    }
+    row_n[qt] = n;
+    row_p[qt] = p;
+  }
+  const int qw = warp - 2;
+  const int g = lane & 15;
+  const uint4 w8 = ldg_nc_v4(a.q_norm_w + 8 * g);
+  for (int base = qw; base < kPairs; base += kPrepWarps * 4) {
+    int32_t pv[4];
+    bool ok[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // positions first (one round trip for all four)
+      const int pair = base + kPrepWarps * u;
+      const int row = rt * kRowsPerCta + ((pair * 2 + (lane >> 4)) >> 2);
+      pv[u] = 0;
+      ok[u] = false;
+      if (pair < kPairs && row < a.n_rows) {
+        const int32_t p = a.pos[row];
+        const int32_t vis = a.visible_len ? a.visible_len[row] : p + 1;
+        ok[u] = !(p < 0 || p >= a.tokens || vis < 0 || vis > p + 1);
+        pv[u] = ok[u] ? p : 0;
+      }
+    }
+    uint4 qv[4], c8[4], s8[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int pair = base + kPrepWarps * u;
+      qv[u] = c8[u] = s8[u] = make_uint4(0, 0, 0, 0);
+      if (pair < kPairs) {
+        const int vec = pair * 2 + (lane >> 4);
+        const int row = rt * kRowsPerCta + (vec >> 2);
+        if (ok[u]) qv[u] = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + (vec & 3) * kHeadDim + 8 * g);
+        if (g < 8) {
+          c8[u] = ldg_nc_v4(a.cos_t + (int64_t)pv[u] * kRot + 8 * g);
+          s8[u] = ldg_nc_v4(a.sin_t + (int64_t)pv[u] * kRot + 8 * g);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int pair = base + kPrepWarps * u;
+      if (pair < kPairs) {  // warp-uniform
+        const int vec = pair * 2 + (lane >> 4);
+        float x[8];
+        unpack8(qv[u], x);
+        uint4 o = norm_rope_16(x, w8, c8[u], s8[u], a.eps, g);
+        if (!ok[u]) o = make_uint4(0, 0, 0, 0);
+        const int n = vec;  // 4 * row + head
+        uint8_t *dst = smem + kQOff + (g >> 3) * kQChunk + n * 128 + (((g & 7) ^ (n & 7)) << 4);
+        *reinterpret_cast<uint4 *>(dst) = o;
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by the tensor core
+}
+
+// Walks a CTA's contiguous range of (row tile, block tile) work units in
+// row-tile-major order; `k` counts row-tile switches (the first unit is one).
+struct UnitCursor {
+  const int32_t *start;  // exclusive prefix of block tiles per row tile
+  int32_t rt, nt, k;
+  __device__ void init(const int32_t *st, int32_t w) {
+    start = st;
+    rt = 0;
+    while (start[rt + 1] <= w) ++rt;
+    nt = w - start[rt];
+    k = 0;
+  }
+  // advance to w + 1; returns true when the row tile changed
+  __device__ bool next() {
+    ++nt;
+    if (start[rt] + nt < start[rt + 1]) return false;
+    do {
+      ++rt;
+    } while (start[rt + 1] == start[rt]);
+    nt = 0;
+    ++k;
+    return true;
+  }
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int32_t tiles_total,
-                int32_t tiles_per_split) {
+                int32_t row_base) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl &C = *reinterpret_cast<Ctrl *>(smem + kCtrlOff);
   const uint32_t sQ = smem_u32(smem + kQOff);
   const uint32_t sK = smem_u32(smem + kKOff);
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row0 = blockIdx.x * kRowsPerCta;
+  const int32_t row_tiles = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
 
-  // ---- set-up: barriers, TMEM, per-row visible blocks
+  // ---- set-up: barriers, TMEM, and the work each row tile needs
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&C.full[s]), 1);
@@ -263,8 +371,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
       mbar_init(smem_u32(&C.tempty[b]), kEpiWarps);
     }
     mbar_init(smem_u32(&C.drain), 1);
+    mbar_init(smem_u32(&C.qfree), 1);
+    mbar_init(smem_u32(&C.qready), kPrepWarps);
     C.abort = 0;
-    C.max_n = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 2) {
@@ -274,74 +383,53 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid < kRowsPerCta) {
-    const int row = row0 + tid;
-    int32_t n = 0;
-    if (row < a.n_rows) {
-      const int32_t p = a.pos[row];
-      const int32_t vis = a.visible_len ? a.visible_len[row] : p + 1;
-      if (p < 0 || p >= a.tokens || vis < 0 || vis > p + 1) {
-        if (blockIdx.y == 0) report_error(a.status, kErrRowRange, row);
-        n = -1;  // invalid row: no query, no writes
-      } else {
-        n = vis >> 2;
-      }
+  for (int t = tid; t < row_tiles; t += kThreads) C.need[t] = 0;  // row_tiles <= kMaxRowTiles
+  __syncthreads();
+  // block tiles each row tile needs: its longest visible prefix
+  for (int r = tid; r < a.n_rows; r += kThreads) {
+    const int32_t p = a.pos[r];
+    const int32_t vis = a.visible_len ? a.visible_len[r] : p + 1;
+    if (p < 0 || p >= a.tokens || vis < 0 || vis > p + 1) {
+      if (blockIdx.x == 0) report_error(a.status, kErrRowRange, row_base + r);
+    } else if (vis >= 4) {
+      atomicMax(&C.need[r / kRowsPerCta], ((vis >> 2) + kBN - 1) / kBN);
     }
-    C.row_n[tid] = n;
-    if (n > 0) atomicMax(&C.max_n, n);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int32_t acc = 0;
+    for (int t = 0; t < row_tiles; ++t) {
+      C.start[t] = acc;
+      acc += C.need[t];
+    }
+    C.start[row_tiles] = acc;
+    C.start[row_tiles + 1] = 0x7fffffff;  // sentinel for the cursor
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  // ---- query heads of the 64 rows into the swizzled B (N-side) tile
-  for (int pair = warp; pair < kRowsPerCta * kHeads / 2; pair += kThreads / 32) {
-    const int vec = pair * 2 + (lane >> 4);
-    const int rl = vec >> 2, h = vec & 3, g = lane & 15;
-    const int row = row0 + rl;
-    const bool valid = C.row_n[rl] >= 0 && row < a.n_rows;
-    const int32_t p = valid ? a.pos[row] : 0;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (valid) v = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * g);
-    const uint4 w8 = ldg_nc_v4(a.q_norm_w + 8 * g);
-    uint4 c8 = make_uint4(0, 0, 0, 0), s8 = make_uint4(0, 0, 0, 0);
-    if (g < 8) {
-      c8 = ldg_nc_v4(a.cos_t + (int64_t)p * kRot + 8 * g);
-      s8 = ldg_nc_v4(a.sin_t + (int64_t)p * kRot + 8 * g);
-    }
-    float x[8];
-    unpack8(v, x);
-    uint4 o = norm_rope_16(x, w8, c8, s8, a.eps, g);
-    if (!valid) o = make_uint4(0, 0, 0, 0);
-    const int n = 4 * rl + h;
-    const int chunk = g >> 3, unit = g & 7;
-    uint8_t *dst = smem + kQOff + chunk * kQChunk + n * 128 + ((unit ^ (n & 7)) << 4);
-    *reinterpret_cast<uint4 *>(dst) = o;
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by the tensor core
-  __syncthreads();
-
-  const int32_t max_n = C.max_n;
-  const int32_t t_begin = blockIdx.y * tiles_per_split;
-  int32_t t_end = t_begin + tiles_per_split;
-  if (t_end > tiles_total) t_end = tiles_total;
-  const int32_t need = (max_n + kBN - 1) / kBN;
-  if (t_end > need) t_end = need;
-  const int ntiles = t_end > t_begin ? t_end - t_begin : 0;
+  const int64_t W = C.start[row_tiles];
+  const int32_t w0 = (int32_t)(W * blockIdx.x / gridDim.x);
+  const int32_t w1 = (int32_t)(W * (blockIdx.x + 1) / gridDim.x);
+  const int nunits = w1 - w0;
   const uint32_t tmem = C.tmem_base;
   volatile int32_t *abort_flag = &C.abort;
 
   if (warp == 0) {
-    // ---- TMA producer
-    if (lane == 0) {
+    // ---- TMA producer: key tiles, independent of the row tile
+    if (lane == 0 && nunits > 0) {
+      UnitCursor cur;
+      cur.init(C.start, w0);
       int issued = 0;
-      for (int i = 0; i < ntiles; ++i) {
+      for (int i = 0; i < nunits; ++i) {
+        if (i > 0) cur.next();
         const int s = i % kStages;
         const uint32_t it = (uint32_t)(i / kStages);
         if (!mbar_wait(smem_u32(&C.empty[s]), (it & 1u) ^ 1u, abort_flag)) break;
         const uint32_t fb = smem_u32(&C.full[s]);
         mbar_expect_tx(fb, kKStage);
-        const int n0 = (t_begin + i) * kBN;
+        const int n0 = cur.nt * kBN;
         tma_load_2d(sK + s * kKStage, &kmap, 0, n0, fb);
         tma_load_2d(sK + s * kKStage + kKChunk, &kmap, 64, n0, fb);
         issued = i + 1;
@@ -353,9 +441,24 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
     }
   } else if (warp == 1) {
     // ---- MMA issuer
-    if (lane == 0) {
-      bool any = false;
-      for (int i = 0; i < ntiles; ++i) {
+    if (lane == 0 && nunits > 0) {
+      UnitCursor cur;
+      cur.init(C.start, w0);
+      int drains = 0;
+      bool ok = true;
+      for (int i = 0; i < nunits && ok; ++i) {
+        const bool sw = (i == 0) || cur.next();
+        if (sw) {  // the query tile is rebuilt: every MMA reading it must be done
+          if (i > 0) {
+            mma_commit(smem_u32(&C.drain));
+            ok = mbar_wait(smem_u32(&C.drain), (uint32_t)(drains & 1), abort_flag);
+            ++drains;
+            if (!ok) break;
+          }
+          mbar_arrive(smem_u32(&C.qfree));
+          if (!mbar_wait(smem_u32(&C.qready), (uint32_t)(cur.k & 1), abort_flag)) break;
+          tc_fence_after();
+        }
         const int s = i % kStages;
         const uint32_t it = (uint32_t)(i / kStages);
         const int buf = i & 1;
@@ -372,36 +475,49 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
         }
         mma_commit(smem_u32(&C.empty[s]));
         mma_commit(smem_u32(&C.tfull[buf]));
-        any = true;
       }
-      if (any) {  // every MMA this thread issued has finished before TMEM is freed
-        mma_commit(smem_u32(&C.drain));
-        mbar_wait(smem_u32(&C.drain), 0u, nullptr);
-      }
+      // every MMA this thread issued has finished before TMEM is freed
+      mma_commit(smem_u32(&C.drain));
+      mbar_wait(smem_u32(&C.drain), (uint32_t)(drains & 1), nullptr);
     }
-  } else if (warp >= kEpiWarp0) {
-    // ---- epilogue: TMEM -> relu -> head sum -> scale -> scores
+  } else if (nunits > 0) {
+    // ---- warps 2..11: query prep at every row-tile switch; 4..11 also drain TMEM
+    const bool epi = warp >= kEpiWarp0;
     const int quarter = warp & 3;               // the TMEM lane quarter this warp may read
     const int chalf = (warp - kEpiWarp0) >> 2;  // which 32 rows (128 columns) it drains
     const float inv_sqrt_hd = 0.08838834764831845f;
-    float *const srow0 = a.scores + (int64_t)(row0 + chalf * 32) * a.score_cols;
     const int64_t ld = a.score_cols;
-    for (int i = 0; i < ntiles; ++i) {
+    UnitCursor cur;
+    cur.init(C.start, w0);
+    for (int i = 0; i < nunits; ++i) {
+      const bool sw = (i == 0) || cur.next();
+      const int par = cur.k & 1;
+      if (sw) {
+        if (!warp_wait(smem_u32(&C.qfree), (uint32_t)(cur.k & 1), abort_flag)) break;
+        prep_row_tile(a, smem, C.row_p[par], C.row_n[par], cur.rt, warp, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&C.qready));
+      }
+      if (!epi) continue;
+      // the row limits of this row tile were written by all prep warps
+      if (sw && !warp_wait(smem_u32(&C.qready), (uint32_t)(cur.k & 1), abort_flag)) break;
       const int buf = i & 1;
       const uint32_t ja = (uint32_t)(i >> 1);
       if (!warp_wait(smem_u32(&C.tfull[buf]), ja & 1u, abort_flag)) break;
       tc_fence_after();
-      const int b = (t_begin + i) * kBN + quarter * 32 + lane;  // this thread's block
+      const int b = cur.nt * kBN + quarter * 32 + lane;  // this thread's block
+      float *const srow0 = a.scores + (int64_t)(cur.rt * kRowsPerCta + chalf * 32) * ld;
+      const int32_t *rn = C.row_n[par] + chalf * 32;
       const uint32_t tbase =
           tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kQCols + chalf * 128);
       // TMEM loads are pipelined: chunk c+1 is in flight while chunk c is reduced
       uint32_t va[32], vb[32];
       tmem_ld32_async(tbase, va);
       tmem_wait_ld();
-      drain_chunk(va, 0, tbase, vb, true, C.row_n + chalf * 32, srow0, ld, b, inv_sqrt_hd);
-      drain_chunk(vb, 1, tbase, va, true, C.row_n + chalf * 32, srow0, ld, b, inv_sqrt_hd);
-      drain_chunk(va, 2, tbase, vb, true, C.row_n + chalf * 32, srow0, ld, b, inv_sqrt_hd);
-      drain_chunk(vb, 3, tbase, va, false, C.row_n + chalf * 32, srow0, ld, b, inv_sqrt_hd);
+      drain_chunk(va, 0, tbase, vb, true, rn, srow0, ld, b, inv_sqrt_hd);
+      drain_chunk(vb, 1, tbase, va, true, rn, srow0, ld, b, inv_sqrt_hd);
+      drain_chunk(va, 2, tbase, vb, true, rn, srow0, ld, b, inv_sqrt_hd);
+      drain_chunk(vb, 3, tbase, va, false, rn, srow0, ld, b, inv_sqrt_hd);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&C.tempty[buf]));
@@ -409,7 +525,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
   }
 
   __syncthreads();
-  if (C.abort && tid == 0) report_error(a.status, kErrTimeout, row0);
+  if (C.abort && tid == 0) report_error(a.status, kErrTimeout, (int32_t)blockIdx.x);
   if (warp == 2) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -473,28 +589,28 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int32_t row_tiles = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
+  // persistent: one CTA per SM, each taking a balanced contiguous range of
+  // (row tile, block tile) units; more than kMaxRowTiles row tiles go in slabs
   const int32_t tiles_total = (int32_t)((n_cap + kBN - 1) / kBN);
-  // one CTA per SM: pick the split of the N tiles that minimises the critical
-  // path, waves x (tiles per CTA + the CTA's fixed cost: query prep, TMEM
-  // allocation, pipeline fill ~ 3 tiles), fewer CTAs on a tie
-  const int64_t sms = sm_count();
-  constexpr int64_t kCtaOverheadTiles = 3;
-  int32_t splits = 1;
-  int64_t best = -1;
-  for (int32_t sp = 1; sp <= tiles_total && sp <= 65535; ++sp) {
-    const int64_t waves = ((int64_t)row_tiles * sp + sms - 1) / sms;
-    const int64_t cost = waves * ((tiles_total + sp - 1) / sp + kCtaOverheadTiles);
-    if (best < 0 || cost < best) {
-      best = cost;
-      splits = sp;
-    }
-    if ((int64_t)row_tiles * sp > 64 * sms) break;
+  // per slab: at most kMaxRowTiles row tiles, and row tiles x block tiles in int32
+  int64_t slab_tiles = (int64_t)INT32_MAX / tiles_total;
+  if (slab_tiles > kMaxRowTiles) slab_tiles = kMaxRowTiles;
+  const int32_t slab = (int32_t)slab_tiles * kRowsPerCta;
+  for (int32_t r0 = 0; r0 < a.n_rows; r0 += slab) {
+    ScoreArgs b = a;
+    b.n_rows = a.n_rows - r0 < slab ? a.n_rows - r0 : slab;
+    b.q = a.q + (int64_t)r0 * a.q_stride;
+    b.pos = a.pos + r0;
+    b.visible_len = a.visible_len ? a.visible_len + r0 : nullptr;
+    b.scores = a.scores + (int64_t)r0 * a.score_cols;
+    const int64_t row_tiles = (b.n_rows + kRowsPerCta - 1) / kRowsPerCta;
+    int64_t ctas = sm_count();
+    if (ctas > row_tiles * tiles_total) ctas = row_tiles * tiles_total;
+    score_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(map, b, tiles_total, r0);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  const int32_t per_split = (tiles_total + splits - 1) / splits;
-  dim3 grid((unsigned)row_tiles, (unsigned)splits);
-  score_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map, a, tiles_total, per_split);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace qsa

@@ -46,9 +46,9 @@ namespace {
 constexpr int kRowsPerCta = 64;
 constexpr int kBN = 128;
 constexpr int kStages = 4;
-constexpr int kThreads = 384;
+constexpr int kThreads = 640;   // 20 warps
 constexpr int kEpiWarp0 = 4;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;   // 4 per TMEM lane quarter
 constexpr int kQCols = kRowsPerCta * 4;       // N = 256 query-head rows
 constexpr uint32_t kQChunk = kQCols * 128;     // 64 dims x 256 rows (32 KiB)
 constexpr uint32_t kQBytes = 2 * kQChunk;      // the whole query tile (64 KiB)
@@ -60,7 +60,7 @@ constexpr uint32_t kCtrlOff = kKOff + kStages * kKStage;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kSpinLimit = 4000000000LL;  // ~2 s of SM clock
 
-constexpr int kPrepWarps = 10;              // warps 2..11 prepare the query tile
+constexpr int kPrepWarps = 18;              // warps 2..19 prepare the query tile
 constexpr int kPairs = kRowsPerCta * kHeads / 2;  // (row, head) vectors, two per warp step
 constexpr int kMaxRowTiles = 1024;           // per-row-tile balancing up to 65536 rows
 
@@ -72,6 +72,7 @@ struct Ctrl {
   uint64_t drain;
   uint64_t qfree;
   uint64_t qready;
+  uint64_t rowinfo;
   uint32_t tmem_base;
   int32_t abort;
   int32_t row_n[2][kRowsPerCta];  // by row-tile switch parity
@@ -209,42 +210,17 @@ __device__ __forceinline__ float relu_nan(float d) {
   return r;
 }
 
-// Reduce one 32-column chunk (8 rows x 4 heads) held in `cur` to 8 scores and
-// store the ones inside each row's visible prefix; before that, start the TMEM
-// load of the next chunk into `nxt` (when `prefetch`), and wait for it after.
-__device__ __forceinline__ void drain_chunk(const uint32_t (&cur)[32], int c, uint32_t tbase,
-                                            uint32_t (&nxt)[32], bool prefetch,
-                                            const int32_t *row_n, float *srow0, int64_t ld, int b,
-                                            float inv_sqrt_hd) {
-  int32_t lim[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) lim[j] = row_n[c * 8 + j];
-  if (prefetch) tmem_ld32_async(tbase + (uint32_t)((c + 1) * 32), nxt);
-  float out[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float h0 = relu_nan(__uint_as_float(cur[4 * j + 0]));
-    const float h1 = relu_nan(__uint_as_float(cur[4 * j + 1]));
-    const float h2 = relu_nan(__uint_as_float(cur[4 * j + 2]));
-    const float h3 = relu_nan(__uint_as_float(cur[4 * j + 3]));
-    out[j] = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(h0, h1), h2), h3), inv_sqrt_hd);
-  }
-  float *dst = srow0 + (int64_t)(c * 8) * ld + b;
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (b < lim[j]) dst[(int64_t)j * ld] = out[j];
-  if (prefetch) tmem_wait_ld();
-}
-
-// Query prep for row tile `rt` by warps 2..11: the rows' visible block counts
-// and positions into row_n/row_p (read by the epilogue after the q_ready
-// barrier), and every (row, head) vector normed, rotated and written to the
-// swizzled B tile.  No intra-group barrier: each vector reads its row's
-// position itself; loads are batched four vectors deep per half-warp.
-__device__ __forceinline__ void prep_row_tile(const ScoreArgs &a, uint8_t *smem, int32_t *row_p,
-                                              int32_t *row_n, int rt, int warp, int lane) {
-  const int qt = (warp - 2) * 32 + lane;  // 0..319
-  if (qt < kRowsPerCta) {
+// Query prep for row tile `rt` by warps 2..19.  Warps 2 and 3 publish the rows'
+// positions and visible block counts (row_p/row_n) through the rowinfo
+// barrier; then every (row, head) vector is normed, rotated and written to
+// the swizzled B tile, loads batched four vectors deep per half-warp.
+// Returns false if a bounded wait gave up.
+__device__ __forceinline__ bool prep_row_tile(const ScoreArgs &a, uint8_t *smem, int32_t *row_p,
+                                              int32_t *row_n, uint32_t rowinfo, uint32_t parity,
+                                              int rt, int warp, int lane,
+                                              volatile int32_t *abort_flag) {
+  if (warp < 4) {
+    const int qt = (warp - 2) * 32 + lane;  // 0..63
     const int row = rt * kRowsPerCta + qt;
     int32_t n = 0, p = 0;
     if (row < a.n_rows) {
@@ -259,26 +235,14 @@ __device__ __forceinline__ void prep_row_tile(const ScoreArgs &a, uint8_t *smem,
     }
     row_n[qt] = n;
     row_p[qt] = p;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(rowinfo);
   }
-  const int qw = warp - 2;
   const int g = lane & 15;
   const uint4 w8 = ldg_nc_v4(a.q_norm_w + 8 * g);
+  if (!warp_wait(rowinfo, parity, abort_flag)) return false;
+  const int qw = warp - 2;
   for (int base = qw; base < kPairs; base += kPrepWarps * 4) {
-    int32_t pv[4];
-    bool ok[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {  // positions first (one round trip for all four)
-      const int pair = base + kPrepWarps * u;
-      const int row = rt * kRowsPerCta + ((pair * 2 + (lane >> 4)) >> 2);
-      pv[u] = 0;
-      ok[u] = false;
-      if (pair < kPairs && row < a.n_rows) {
-        const int32_t p = a.pos[row];
-        const int32_t vis = a.visible_len ? a.visible_len[row] : p + 1;
-        ok[u] = !(p < 0 || p >= a.tokens || vis < 0 || vis > p + 1);
-        pv[u] = ok[u] ? p : 0;
-      }
-    }
     uint4 qv[4], c8[4], s8[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -286,11 +250,13 @@ __device__ __forceinline__ void prep_row_tile(const ScoreArgs &a, uint8_t *smem,
       qv[u] = c8[u] = s8[u] = make_uint4(0, 0, 0, 0);
       if (pair < kPairs) {
         const int vec = pair * 2 + (lane >> 4);
-        const int row = rt * kRowsPerCta + (vec >> 2);
-        if (ok[u]) qv[u] = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + (vec & 3) * kHeadDim + 8 * g);
+        const int rl = vec >> 2;
+        if (row_n[rl] >= 0 && rt * kRowsPerCta + rl < a.n_rows)
+          qv[u] = ldg_nc_v4(a.q + (int64_t)(rt * kRowsPerCta + rl) * a.q_stride +
+                            (vec & 3) * kHeadDim + 8 * g);
         if (g < 8) {
-          c8[u] = ldg_nc_v4(a.cos_t + (int64_t)pv[u] * kRot + 8 * g);
-          s8[u] = ldg_nc_v4(a.sin_t + (int64_t)pv[u] * kRot + 8 * g);
+          c8[u] = ldg_nc_v4(a.cos_t + (int64_t)row_p[rl] * kRot + 8 * g);
+          s8[u] = ldg_nc_v4(a.sin_t + (int64_t)row_p[rl] * kRot + 8 * g);
         }
       }
     }
@@ -298,18 +264,19 @@ __device__ __forceinline__ void prep_row_tile(const ScoreArgs &a, uint8_t *smem,
     for (int u = 0; u < 4; ++u) {
       const int pair = base + kPrepWarps * u;
       if (pair < kPairs) {  // warp-uniform
-        const int vec = pair * 2 + (lane >> 4);
+        const int vec = pair * 2 + (lane >> 4);  // = 4 * row + head
+        const int rl = vec >> 2;
         float x[8];
         unpack8(qv[u], x);
         uint4 o = norm_rope_16(x, w8, c8[u], s8[u], a.eps, g);
-        if (!ok[u]) o = make_uint4(0, 0, 0, 0);
-        const int n = vec;  // 4 * row + head
-        uint8_t *dst = smem + kQOff + (g >> 3) * kQChunk + n * 128 + (((g & 7) ^ (n & 7)) << 4);
+        if (row_n[rl] < 0 || rt * kRowsPerCta + rl >= a.n_rows) o = make_uint4(0, 0, 0, 0);
+        uint8_t *dst = smem + kQOff + (g >> 3) * kQChunk + vec * 128 + (((g & 7) ^ (vec & 7)) << 4);
         *reinterpret_cast<uint4 *>(dst) = o;
       }
     }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by the tensor core
+  return true;
 }
 
 // Walks a CTA's contiguous range of (row tile, block tile) work units in
@@ -362,6 +329,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
     mbar_init(smem_u32(&C.drain), 1);
     mbar_init(smem_u32(&C.qfree), 1);
     mbar_init(smem_u32(&C.qready), kPrepWarps);
+    mbar_init(smem_u32(&C.rowinfo), 2);
     C.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -470,10 +438,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
       mbar_wait(smem_u32(&C.drain), (uint32_t)(drains & 1), nullptr);
     }
   } else if (nunits > 0) {
-    // ---- warps 2..11: query prep at every row-tile switch; 4..11 also drain TMEM
+    // ---- warps 2..19: query prep at every row-tile switch; 4..19 also drain TMEM
     const bool epi = warp >= kEpiWarp0;
-    const int quarter = warp & 3;               // the TMEM lane quarter this warp may read
-    const int chalf = (warp - kEpiWarp0) >> 2;  // which 32 rows (128 columns) it drains
+    const int quarter = warp & 3;             // the TMEM lane quarter this warp may read
+    const int cq = (warp - kEpiWarp0) >> 2;   // which 16 rows (64 columns) it drains
     const float inv_sqrt_hd = 0.08838834764831845f;
     const int64_t ld = a.score_cols;
     UnitCursor cur;
@@ -483,30 +451,41 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
       const int par = cur.k & 1;
       if (sw) {
         if (!warp_wait(smem_u32(&C.qfree), (uint32_t)(cur.k & 1), abort_flag)) break;
-        prep_row_tile(a, smem, C.row_p[par], C.row_n[par], cur.rt, warp, lane);
+        if (!prep_row_tile(a, smem, C.row_p[par], C.row_n[par], smem_u32(&C.rowinfo),
+                           (uint32_t)(cur.k & 1), cur.rt, warp, lane, abort_flag))
+          break;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&C.qready));
       }
       if (!epi) continue;
-      // the row limits of this row tile were written by all prep warps
-      if (sw && !warp_wait(smem_u32(&C.qready), (uint32_t)(cur.k & 1), abort_flag)) break;
       const int buf = i & 1;
       const uint32_t ja = (uint32_t)(i >> 1);
       if (!warp_wait(smem_u32(&C.tfull[buf]), ja & 1u, abort_flag)) break;
       tc_fence_after();
       const int b = cur.nt * kBN + quarter * 32 + lane;  // this thread's block
-      float *const srow0 = a.scores + (int64_t)(cur.rt * kRowsPerCta + chalf * 32) * ld;
-      const int32_t *rn = C.row_n[par] + chalf * 32;
-      const uint32_t tbase =
-          tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kQCols + chalf * 128);
-      // TMEM loads are pipelined: chunk c+1 is in flight while chunk c is reduced
-      uint32_t va[32], vb[32];
-      tmem_ld32_async(tbase, va);
-      tmem_wait_ld();
-      drain_chunk(va, 0, tbase, vb, true, rn, srow0, ld, b, inv_sqrt_hd);
-      drain_chunk(vb, 1, tbase, va, true, rn, srow0, ld, b, inv_sqrt_hd);
-      drain_chunk(va, 2, tbase, vb, true, rn, srow0, ld, b, inv_sqrt_hd);
-      drain_chunk(vb, 3, tbase, va, false, rn, srow0, ld, b, inv_sqrt_hd);
+      float *const srow0 = a.scores + (int64_t)(cur.rt * kRowsPerCta + cq * 16) * ld;
+      const int32_t *rn = C.row_n[par] + cq * 16;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        int32_t lim[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) lim[j] = rn[c * 8 + j];
+        uint32_t v[32];
+        tmem_ld32_async(tmem + ((uint32_t)(quarter * 32) << 16) +
+                            (uint32_t)(buf * kQCols + cq * 64 + c * 32),
+                        v);
+        tmem_wait_ld();
+        float *dst = srow0 + (int64_t)(c * 8) * ld + b;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float h0 = relu_nan(__uint_as_float(v[4 * j + 0]));
+          const float h1 = relu_nan(__uint_as_float(v[4 * j + 1]));
+          const float h2 = relu_nan(__uint_as_float(v[4 * j + 2]));
+          const float h3 = relu_nan(__uint_as_float(v[4 * j + 3]));
+          const float sc = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(h0, h1), h2), h3), inv_sqrt_hd);
+          if (b < lim[j]) dst[(int64_t)j * ld] = sc;
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&C.tempty[buf]));

@@ -536,9 +536,11 @@ def prefill_chunk(torch, qsa, device, hbm_gbs, bf16_tf, ncu=False):
         qsa.qsa_pool_blocks(raw[first:].reshape(-1), 128, first // 4, 1024, kw, cd, sd, tokens,
                             EPS, cache)
 
+    ws = qsa.new_workspace(rows, device)
+
     def score():
         qsa.qsa_score_rows(fq, 640, pos, None, rows, tokens, qw, cd, sd, tokens, EPS, cache, None,
-                           sc, nb, st)
+                           sc, nb, st, workspace=ws)
 
     def select():
         qsa.qsa_select_mask(sc, nb, pos, rows, tokens, BUDGET, mask, st)

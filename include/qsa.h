@@ -132,23 +132,36 @@ qsa_status qsa_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t fir
  *              spare capacity allowed), 16-byte aligned.  Row i gets entries
  *              b < blocks; entries past that are not written.
  *  dev_status  DEVICE int32[2] status word (see above).
- * qsa_score_rows picks the scorer itself (QSA_SCORE_AUTO).
+ *  workspace   DEVICE scratch owned by the caller, or NULL; 16-byte aligned.
+ *              The tensor-core scorer needs qsa_score_workspace_bytes(n_rows)
+ *              bytes for the prepared query heads; its contents on entry do
+ *              not matter and are overwritten.  The SIMT scorer uses none.
+ * qsa_score_rows picks the scorer itself (QSA_SCORE_AUTO): the tensor-core
+ * scorer for 64 or more rows sharing one key set (key_base == NULL) when the
+ * workspace is large enough, the SIMT scorer otherwise.
  */
 qsa_status qsa_score_rows(const uint16_t *q, int64_t q_stride, const int32_t *pos,
                           const int32_t *visible_len, int32_t n_rows, int32_t tokens,
                           const uint16_t *q_norm_w, const uint16_t *cos_t, const uint16_t *sin_t,
                           int32_t table_rows, float eps, const uint16_t *block_keys,
                           const int64_t *key_base, float *scores, int64_t score_cols,
-                          int32_t *dev_status, void *stream);
+                          int32_t *dev_status, void *workspace, int64_t workspace_bytes,
+                          void *stream);
 
-/* qsa_score_rows with an explicit scorer; QSA_SCORE_TCGEN05 refuses key_base != NULL. */
+/* Workspace bytes the tensor-core scorer needs for n_rows query rows
+ * (1024 per row: 4 prepared heads x 128 bf16); -1 for n_rows < 0. */
+int64_t qsa_score_workspace_bytes(int32_t n_rows);
+
+/* qsa_score_rows with an explicit scorer; QSA_SCORE_TCGEN05 refuses key_base != NULL
+ * and a workspace smaller than qsa_score_workspace_bytes(n_rows). */
 qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_t *pos,
                                const int32_t *visible_len, int32_t n_rows, int32_t tokens,
                                const uint16_t *q_norm_w, const uint16_t *cos_t,
                                const uint16_t *sin_t, int32_t table_rows, float eps,
                                const uint16_t *block_keys, const int64_t *key_base,
                                float *scores, int64_t score_cols, int32_t *dev_status,
-                               int32_t path, void *stream);
+                               int32_t path, void *workspace, int64_t workspace_bytes,
+                               void *stream);
 
 /*
  * Exact top-(budget/4) block selection into a u8 visibility mask.
@@ -182,7 +195,8 @@ qsa_status qsa_select_mask(const float *scores, int64_t score_cols, const int32_
  *  budget, mask: as qsa_select_mask;
  *  block_keys  DEVICE pooled-key cache (read and written);
  *  scores      DEVICE f32 work buffer of n_rows * score_cols (its contents
- *              afterwards are the rows' scores).
+ *              afterwards are the rows' scores);
+ *  workspace, workspace_bytes: as qsa_score_rows (NULL selects the SIMT scorer).
  */
 qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t pool_first_block,
                             int32_t pool_n_blocks, const uint16_t *k_norm_w, const uint16_t *q,
@@ -190,7 +204,8 @@ qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t po
                             const uint16_t *q_norm_w, const uint16_t *cos_t,
                             const uint16_t *sin_t, int32_t table_rows, float eps, int32_t budget,
                             uint16_t *block_keys, float *scores, int64_t score_cols,
-                            uint8_t *mask, int32_t *dev_status, void *stream);
+                            uint8_t *mask, int32_t *dev_status, void *workspace,
+                            int64_t workspace_bytes, void *stream);
 
 /* Zero a DEVICE status word (stream-ordered). */
 qsa_status qsa_reset_status(int32_t *dev_status, void *stream);

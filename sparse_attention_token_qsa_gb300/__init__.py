@@ -33,8 +33,8 @@ QSA_SCORE_TCGEN05 = 2
 HEADS, HEAD_DIM, RATIO, ROT_DIM, FUSED_WIDTH = 4, 128, 4, 64, 640
 
 EXPORTED = ("qsa_version", "qsa_status_string", "qsa_rope_tables", "qsa_pool_blocks",
-            "qsa_score_rows", "qsa_score_rows_with", "qsa_select_mask", "qsa_index_select",
-            "qsa_reset_status", "qsa_read_status")
+            "qsa_score_rows", "qsa_score_rows_with", "qsa_score_workspace_bytes",
+            "qsa_select_mask", "qsa_index_select", "qsa_reset_status", "qsa_read_status")
 
 
 class QsaError(RuntimeError):
@@ -55,12 +55,14 @@ def _load() -> ctypes.CDLL:
         "qsa_status_string": ([i32], ctypes.c_char_p),
         "qsa_rope_tables": ([i32, f64, P, P], i32),
         "qsa_pool_blocks": ([P, i64, i32, i32, P, P, P, i32, f32, P, P], i32),
-        "qsa_score_rows": ([P, i64, P, P, i32, i32, P, P, P, i32, f32, P, P, P, i64, P, P], i32),
-        "qsa_score_rows_with": ([P, i64, P, P, i32, i32, P, P, P, i32, f32, P, P, P, i64, P, i32, P],
-                                i32),
+        "qsa_score_rows": ([P, i64, P, P, i32, i32, P, P, P, i32, f32, P, P, P, i64, P, P, i64, P],
+                           i32),
+        "qsa_score_rows_with": ([P, i64, P, P, i32, i32, P, P, P, i32, f32, P, P, P, i64, P, i32, P,
+                                 i64, P], i32),
+        "qsa_score_workspace_bytes": ([i32], i64),
         "qsa_select_mask": ([P, i64, P, i32, i32, i32, P, P, P], i32),
         "qsa_index_select": ([P, i64, i32, i32, P, P, i64, P, i32, i32, P, P, P, i32, f32, i32, P, P,
-                              i64, P, P, P], i32),
+                              i64, P, P, P, i64, P], i32),
         "qsa_reset_status": ([P, P], i32),
         "qsa_read_status": ([P, P, P, P], i32),
     }
@@ -126,29 +128,47 @@ def qsa_pool_blocks(keys, key_stride, first_block, n_blocks, k_norm_w, cos_t, si
            "qsa_pool_blocks")
 
 
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+
+
+def qsa_score_workspace_bytes(n_rows: int) -> int:
+    return int(_lib.qsa_score_workspace_bytes(int(n_rows)))
+
+
+def new_workspace(n_rows: int, device="cuda") -> torch.Tensor:
+    """A device workspace large enough for the tensor-core scorer."""
+    return torch.empty(max(1, qsa_score_workspace_bytes(n_rows)), dtype=torch.uint8, device=device)
+
+
 def qsa_score_rows_with(q, q_stride, pos, visible_len, n_rows, tokens, q_norm_w, cos_t, sin_t,
                         table_rows, eps, block_keys, key_base, scores, score_cols, dev_status,
-                        path=QSA_SCORE_AUTO, stream=None) -> None:
+                        path=QSA_SCORE_AUTO, workspace=None, stream=None) -> None:
+    ws, wsb = _ws(workspace)
     _check(_lib.qsa_score_rows_with(_dev(q, "q"), int(q_stride), _dev(pos, "pos"),
                                     _dev(visible_len, "visible_len"), int(n_rows), int(tokens),
                                     _dev(q_norm_w, "q_norm_w"), _dev(cos_t, "cos_t"),
                                     _dev(sin_t, "sin_t"), int(table_rows), float(eps),
                                     _dev(block_keys, "block_keys"), _dev(key_base, "key_base"),
                                     _dev(scores, "scores"), int(score_cols),
-                                    _dev(dev_status, "dev_status"), int(path), _stream(stream)),
+                                    _dev(dev_status, "dev_status"), int(path), ws, int(wsb),
+                                    _stream(stream)),
            "qsa_score_rows_with")
 
 
 def qsa_score_rows(q, q_stride, pos, visible_len, n_rows, tokens, q_norm_w, cos_t, sin_t,
                    table_rows, eps, block_keys, key_base, scores, score_cols, dev_status,
-                   stream=None) -> None:
+                   workspace=None, stream=None) -> None:
+    ws, wsb = _ws(workspace)
     _check(_lib.qsa_score_rows(_dev(q, "q"), int(q_stride), _dev(pos, "pos"),
                                _dev(visible_len, "visible_len"), int(n_rows), int(tokens),
                                _dev(q_norm_w, "q_norm_w"), _dev(cos_t, "cos_t"),
                                _dev(sin_t, "sin_t"), int(table_rows), float(eps),
                                _dev(block_keys, "block_keys"), _dev(key_base, "key_base"),
                                _dev(scores, "scores"), int(score_cols),
-                               _dev(dev_status, "dev_status"), _stream(stream)),
+                               _dev(dev_status, "dev_status"), ws, int(wsb), _stream(stream)),
            "qsa_score_rows")
 
 
@@ -162,7 +182,8 @@ def qsa_select_mask(scores, score_cols, pos, n_rows, tokens, budget, mask, dev_s
 
 def qsa_index_select(keys, key_stride, pool_first_block, pool_n_blocks, k_norm_w, q, q_stride, pos,
                      n_rows, tokens, q_norm_w, cos_t, sin_t, table_rows, eps, budget, block_keys,
-                     scores, score_cols, mask, dev_status, stream=None) -> None:
+                     scores, score_cols, mask, dev_status, workspace=None, stream=None) -> None:
+    ws, wsb = _ws(workspace)
     _check(_lib.qsa_index_select(_dev(keys, "keys"), int(key_stride), int(pool_first_block),
                                  int(pool_n_blocks), _dev(k_norm_w, "k_norm_w"), _dev(q, "q"),
                                  int(q_stride), _dev(pos, "pos"), int(n_rows), int(tokens),
@@ -170,7 +191,7 @@ def qsa_index_select(keys, key_stride, pool_first_block, pool_n_blocks, k_norm_w
                                  _dev(sin_t, "sin_t"), int(table_rows), float(eps), int(budget),
                                  _dev(block_keys, "block_keys"), _dev(scores, "scores"),
                                  int(score_cols), _dev(mask, "mask"),
-                                 _dev(dev_status, "dev_status"), _stream(stream)),
+                                 _dev(dev_status, "dev_status"), ws, int(wsb), _stream(stream)),
            "qsa_index_select")
 
 

@@ -141,27 +141,37 @@ qsa_status qsa_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t fir
                                            (cudaStream_t)stream));
 }
 
+int64_t qsa_score_workspace_bytes(int32_t n_rows) {
+  return n_rows < 0 ? -1 : (int64_t)n_rows * 4 * kHeadDim * 2;
+}
+
 qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_t *pos,
                                const int32_t *visible_len, int32_t n_rows, int32_t tokens,
                                const uint16_t *q_norm_w, const uint16_t *cos_t,
                                const uint16_t *sin_t, int32_t table_rows, float eps,
                                const uint16_t *block_keys, const int64_t *key_base,
                                float *scores, int64_t score_cols, int32_t *dev_status,
-                               int32_t path, void *stream) {
+                               int32_t path, void *workspace, int64_t workspace_bytes,
+                               void *stream) {
   if (path != QSA_SCORE_AUTO && path != QSA_SCORE_SIMT && path != QSA_SCORE_TCGEN05)
     return QSA_ERR_INVALID_VALUE;
+  if (workspace_bytes < 0) return QSA_ERR_INVALID_VALUE;
   qsa_status st = check_score_args(q, q_stride, pos, n_rows, tokens, q_norm_w, cos_t, sin_t,
                                    table_rows, eps, block_keys, scores, score_cols);
   if (st != QSA_OK || n_rows == 0 || tokens == 0) return st;
-  if (path == QSA_SCORE_TCGEN05 && key_base != nullptr) return QSA_ERR_INVALID_VALUE;
+  const bool ws_ok = workspace != nullptr && aligned16(workspace) &&
+                     workspace_bytes >= qsa_score_workspace_bytes(n_rows) &&
+                     (int64_t)n_rows * 4 <= INT32_MAX;
+  if (path == QSA_SCORE_TCGEN05 && (key_base != nullptr || !ws_ok)) return QSA_ERR_INVALID_VALUE;
   qsa::ScoreArgs a{q,          q_stride, pos,   visible_len, n_rows,     tokens,
                    q_norm_w,   cos_t,    sin_t, eps,         block_keys, key_base,
                    scores,     score_cols, dev_status};
   if (path == QSA_SCORE_AUTO)
-    path = (qsa::kTcScorerReady && key_base == nullptr && n_rows >= 64 && tokens >= 2048)
+    path = (qsa::kTcScorerReady && key_base == nullptr && ws_ok && n_rows >= 64 && tokens >= 2048)
                ? QSA_SCORE_TCGEN05
                : QSA_SCORE_SIMT;
-  if (path == QSA_SCORE_TCGEN05) return from_cuda(qsa::launch_score_tc(a, (cudaStream_t)stream));
+  if (path == QSA_SCORE_TCGEN05)
+    return from_cuda(qsa::launch_score_tc(a, static_cast<uint16_t *>(workspace), (cudaStream_t)stream));
   return from_cuda(qsa::launch_score_simt(a, (cudaStream_t)stream));
 }
 
@@ -170,10 +180,11 @@ qsa_status qsa_score_rows(const uint16_t *q, int64_t q_stride, const int32_t *po
                           const uint16_t *q_norm_w, const uint16_t *cos_t, const uint16_t *sin_t,
                           int32_t table_rows, float eps, const uint16_t *block_keys,
                           const int64_t *key_base, float *scores, int64_t score_cols,
-                          int32_t *dev_status, void *stream) {
+                          int32_t *dev_status, void *workspace, int64_t workspace_bytes,
+                          void *stream) {
   return qsa_score_rows_with(q, q_stride, pos, visible_len, n_rows, tokens, q_norm_w, cos_t, sin_t,
                              table_rows, eps, block_keys, key_base, scores, score_cols, dev_status,
-                             QSA_SCORE_AUTO, stream);
+                             QSA_SCORE_AUTO, workspace, workspace_bytes, stream);
 }
 
 qsa_status qsa_select_mask(const float *scores, int64_t score_cols, const int32_t *pos,
@@ -191,7 +202,8 @@ qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t po
                             const uint16_t *q_norm_w, const uint16_t *cos_t,
                             const uint16_t *sin_t, int32_t table_rows, float eps, int32_t budget,
                             uint16_t *block_keys, float *scores, int64_t score_cols,
-                            uint8_t *mask, int32_t *dev_status, void *stream) {
+                            uint8_t *mask, int32_t *dev_status, void *workspace,
+                            int64_t workspace_bytes, void *stream) {
   // validate all three stages before launching any of them
   qsa_status st = check_pool_args(keys, key_stride, pool_first_block, pool_n_blocks, k_norm_w,
                                   cos_t, sin_t, table_rows, eps, block_keys);
@@ -201,6 +213,7 @@ qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t po
   if (st != QSA_OK) return st;
   st = check_select_args(scores, score_cols, pos, n_rows, tokens, budget, mask);
   if (st != QSA_OK) return st;
+  if (workspace_bytes < 0) return QSA_ERR_INVALID_VALUE;
   cudaStream_t s = (cudaStream_t)stream;
   if (pool_n_blocks > 0) {
     st = from_cuda(qsa::launch_pool_blocks(keys, key_stride, pool_first_block, pool_n_blocks,
@@ -210,7 +223,7 @@ qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t po
   if (n_rows == 0 || tokens == 0) return QSA_OK;
   st = qsa_score_rows_with(q, q_stride, pos, nullptr, n_rows, tokens, q_norm_w, cos_t, sin_t,
                            table_rows, eps, block_keys, nullptr, scores, score_cols, dev_status,
-                           QSA_SCORE_AUTO, stream);
+                           QSA_SCORE_AUTO, workspace, workspace_bytes, stream);
   if (st != QSA_OK) return st;
   return from_cuda(qsa::launch_select(scores, score_cols, pos, n_rows, tokens, budget, mask,
                                       dev_status, s));

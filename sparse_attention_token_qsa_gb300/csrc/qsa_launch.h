@@ -31,7 +31,10 @@ struct ScoreArgs {
 };
 
 cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream);
-cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream);
+// Prepared query heads, [n_rows * 4, 128] bf16, into a workspace.
+cudaError_t launch_qprep(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream);
+// Tensor-core scorer; qws is a workspace of n_rows * 1024 bytes (16-byte aligned).
+cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream);
 extern const bool kTcScorerReady;
 
 cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t *pos,

@@ -17,16 +17,17 @@
 // one TMEM lane (one thread of the epilogue) holds a block's dot with all four
 // heads of a row in four adjacent columns, so the relu and the head sum are
 // register-local and each warp store writes 32 consecutive blocks of one row.
-//  * the CTA prepares its 64 rows' heads itself (norm + RoPE, exact sums like
-//    the pooling kernel) and writes them into shared memory in the 128-byte
-//    swizzled K-major layout the MMA descriptors expect (the B operand);
+//  * the rows' heads are prepared once per launch by qprep_kernel into a
+//    workspace laid out [rows * 4, 128] (the B operand, K-major);
 //  * warp 0 (one lane) streams block-key tiles (the A operand) with TMA
-//    (128B swizzle) into a 4-stage ring guarded by mbarriers;
+//    (128B swizzle) into a 4-stage ring guarded by mbarriers, and at every
+//    row-tile switch, once the MMAs reading the old query tile are done, loads
+//    the new 64-row query tile (2 x 32 KiB) with TMA;
 //  * warp 1 (one lane) issues the MMAs into one of two TMEM accumulators
 //    (256 columns each, 512 in all) and commits to mbarriers that free the key
 //    stage and publish the accumulator;
-//  * warps 4..11 drain the accumulator: warp w reads TMEM lane quarter w % 4
-//    (32 blocks) and one half of the columns (32 rows), 32 columns per
+//  * warps 4..19 drain the accumulator: warp w reads TMEM lane quarter w % 4
+//    (32 blocks) and a quarter of the columns (16 rows), 32 columns per
 //    tcgen05.ld, relu per head, ((h0 + h1) + h2) + h3, scale, coalesced stores
 //    of the blocks each row can see;
 //  * every mbarrier wait is bounded: on timeout the kernel records
@@ -60,8 +61,6 @@ constexpr uint32_t kCtrlOff = kKOff + kStages * kKStage;
 constexpr uint32_t kTmemCols = 512;
 constexpr long long kSpinLimit = 4000000000LL;  // ~2 s of SM clock
 
-constexpr int kPrepWarps = 18;              // warps 2..19 prepare the query tile
-constexpr int kPairs = kRowsPerCta * kHeads / 2;  // (row, head) vectors, two per warp step
 constexpr int kMaxRowTiles = 1024;           // per-row-tile balancing up to 65536 rows
 
 struct Ctrl {
@@ -72,11 +71,8 @@ struct Ctrl {
   uint64_t drain;
   uint64_t qfree;
   uint64_t qready;
-  uint64_t rowinfo;
   uint32_t tmem_base;
   int32_t abort;
-  int32_t row_n[2][kRowsPerCta];  // by row-tile switch parity
-  int32_t row_p[2][kRowsPerCta];
   int32_t need[kMaxRowTiles];
   int32_t start[kMaxRowTiles + 2];
 };
@@ -210,75 +206,6 @@ __device__ __forceinline__ float relu_nan(float d) {
   return r;
 }
 
-// Query prep for row tile `rt` by warps 2..19.  Warps 2 and 3 publish the rows'
-// positions and visible block counts (row_p/row_n) through the rowinfo
-// barrier; then every (row, head) vector is normed, rotated and written to
-// the swizzled B tile, loads batched four vectors deep per half-warp.
-// Returns false if a bounded wait gave up.
-__device__ __forceinline__ bool prep_row_tile(const ScoreArgs &a, uint8_t *smem, int32_t *row_p,
-                                              int32_t *row_n, uint32_t rowinfo, uint32_t parity,
-                                              int rt, int warp, int lane,
-                                              volatile int32_t *abort_flag) {
-  if (warp < 4) {
-    const int qt = (warp - 2) * 32 + lane;  // 0..63
-    const int row = rt * kRowsPerCta + qt;
-    int32_t n = 0, p = 0;
-    if (row < a.n_rows) {
-      p = a.pos[row];
-      const int32_t vis = a.visible_len ? a.visible_len[row] : p + 1;
-      if (p < 0 || p >= a.tokens || vis < 0 || vis > p + 1) {
-        n = -1;
-        p = 0;
-      } else {
-        n = vis >> 2;
-      }
-    }
-    row_n[qt] = n;
-    row_p[qt] = p;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(rowinfo);
-  }
-  const int g = lane & 15;
-  const uint4 w8 = ldg_nc_v4(a.q_norm_w + 8 * g);
-  if (!warp_wait(rowinfo, parity, abort_flag)) return false;
-  const int qw = warp - 2;
-  for (int base = qw; base < kPairs; base += kPrepWarps * 4) {
-    uint4 qv[4], c8[4], s8[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int pair = base + kPrepWarps * u;
-      qv[u] = c8[u] = s8[u] = make_uint4(0, 0, 0, 0);
-      if (pair < kPairs) {
-        const int vec = pair * 2 + (lane >> 4);
-        const int rl = vec >> 2;
-        if (row_n[rl] >= 0 && rt * kRowsPerCta + rl < a.n_rows)
-          qv[u] = ldg_nc_v4(a.q + (int64_t)(rt * kRowsPerCta + rl) * a.q_stride +
-                            (vec & 3) * kHeadDim + 8 * g);
-        if (g < 8) {
-          c8[u] = ldg_nc_v4(a.cos_t + (int64_t)row_p[rl] * kRot + 8 * g);
-          s8[u] = ldg_nc_v4(a.sin_t + (int64_t)row_p[rl] * kRot + 8 * g);
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int pair = base + kPrepWarps * u;
-      if (pair < kPairs) {  // warp-uniform
-        const int vec = pair * 2 + (lane >> 4);  // = 4 * row + head
-        const int rl = vec >> 2;
-        float x[8];
-        unpack8(qv[u], x);
-        uint4 o = norm_rope_16(x, w8, c8[u], s8[u], a.eps, g);
-        if (row_n[rl] < 0 || rt * kRowsPerCta + rl >= a.n_rows) o = make_uint4(0, 0, 0, 0);
-        uint8_t *dst = smem + kQOff + (g >> 3) * kQChunk + vec * 128 + (((g & 7) ^ (vec & 7)) << 4);
-        *reinterpret_cast<uint4 *>(dst) = o;
-      }
-    }
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by the tensor core
-  return true;
-}
-
 // Walks a CTA's contiguous range of (row tile, block tile) work units in
 // row-tile-major order; `k` counts row-tile switches (the first unit is one).
 struct UnitCursor {
@@ -305,8 +232,8 @@ struct UnitCursor {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int32_t tiles_total,
-                int32_t row_base) {
+score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                const ScoreArgs a, int32_t tiles_total, int32_t row_base) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -328,8 +255,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
     }
     mbar_init(smem_u32(&C.drain), 1);
     mbar_init(smem_u32(&C.qfree), 1);
-    mbar_init(smem_u32(&C.qready), kPrepWarps);
-    mbar_init(smem_u32(&C.rowinfo), 2);
+    mbar_init(smem_u32(&C.qready), 1);
     C.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -374,13 +300,13 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
   volatile int32_t *abort_flag = &C.abort;
 
   if (warp == 0) {
-    // ---- TMA producer: key tiles, independent of the row tile
+    // ---- TMA producer: key tiles, and the query tile at every row-tile switch
     if (lane == 0 && nunits > 0) {
       UnitCursor cur;
       cur.init(C.start, w0);
       int issued = 0;
       for (int i = 0; i < nunits; ++i) {
-        if (i > 0) cur.next();
+        const bool sw = (i == 0) || cur.next();
         const int s = i % kStages;
         const uint32_t it = (uint32_t)(i / kStages);
         if (!mbar_wait(smem_u32(&C.empty[s]), (it & 1u) ^ 1u, abort_flag)) break;
@@ -390,10 +316,19 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
         tma_load_2d(sK + s * kKStage, &kmap, 0, n0, fb);
         tma_load_2d(sK + s * kKStage + kKChunk, &kmap, 64, n0, fb);
         issued = i + 1;
+        if (sw) {  // the MMAs reading the previous query tile have drained
+          if (!mbar_wait(smem_u32(&C.qfree), (uint32_t)(cur.k & 1), abort_flag)) break;
+          const uint32_t qb = smem_u32(&C.qready);
+          mbar_expect_tx(qb, kQBytes);
+          const int qy = (row_base + cur.rt * kRowsPerCta) * kHeads;
+          tma_load_2d(sQ, &qmap, 0, qy, qb);
+          tma_load_2d(sQ + kQChunk, &qmap, 64, qy, qb);
+        }
       }
       if (*abort_flag) {  // let our own copies land before the CTA leaves
         for (int i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i)
           mbar_wait(smem_u32(&C.full[i % kStages]), (uint32_t)(i / kStages) & 1u, nullptr);
+        mbar_wait(smem_u32(&C.qready), (uint32_t)(cur.k & 1), nullptr);
       }
     }
   } else if (warp == 1) {
@@ -438,7 +373,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
       mbar_wait(smem_u32(&C.drain), (uint32_t)(drains & 1), nullptr);
     }
   } else if (nunits > 0) {
-    // ---- warps 2..19: query prep at every row-tile switch; 4..19 also drain TMEM
+    // ---- warps 4..19: drain TMEM (warps 2 and 3 have no role)
     const bool epi = warp >= kEpiWarp0;
     const int quarter = warp & 3;             // the TMEM lane quarter this warp may read
     const int cq = (warp - kEpiWarp0) >> 2;   // which 16 rows (64 columns) it drains
@@ -446,30 +381,29 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int
     const int64_t ld = a.score_cols;
     UnitCursor cur;
     cur.init(C.start, w0);
-    for (int i = 0; i < nunits; ++i) {
+    int32_t my_n = 0;  // lane j < 16: visible blocks of this warp's row j
+    for (int i = 0; i < nunits && epi; ++i) {
       const bool sw = (i == 0) || cur.next();
-      const int par = cur.k & 1;
       if (sw) {
-        if (!warp_wait(smem_u32(&C.qfree), (uint32_t)(cur.k & 1), abort_flag)) break;
-        if (!prep_row_tile(a, smem, C.row_p[par], C.row_n[par], smem_u32(&C.rowinfo),
-                           (uint32_t)(cur.k & 1), cur.rt, warp, lane, abort_flag))
-          break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&C.qready));
+        const int r = cur.rt * kRowsPerCta + cq * 16 + (lane & 15);
+        my_n = 0;
+        if (lane < 16 && r < a.n_rows) {
+          const int32_t p = a.pos[r];
+          const int32_t vis = a.visible_len ? a.visible_len[r] : p + 1;
+          if (!(p < 0 || p >= a.tokens || vis < 0 || vis > p + 1)) my_n = vis >> 2;
+        }
       }
-      if (!epi) continue;
       const int buf = i & 1;
       const uint32_t ja = (uint32_t)(i >> 1);
       if (!warp_wait(smem_u32(&C.tfull[buf]), ja & 1u, abort_flag)) break;
       tc_fence_after();
       const int b = cur.nt * kBN + quarter * 32 + lane;  // this thread's block
       float *const srow0 = a.scores + (int64_t)(cur.rt * kRowsPerCta + cq * 16) * ld;
-      const int32_t *rn = C.row_n[par] + cq * 16;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         int32_t lim[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) lim[j] = rn[c * 8 + j];
+        for (int j = 0; j < 8; ++j) lim[j] = __shfl_sync(0xffffffffu, my_n, c * 8 + j);
         uint32_t v[32];
         tmem_ld32_async(tmem + ((uint32_t)(quarter * 32) << 16) +
                             (uint32_t)(buf * kQCols + cq * 64 + c * 32),
@@ -533,23 +467,35 @@ int sm_count() {
 
 }  // namespace
 
-cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream) {
+cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream) {
   const int64_t n_cap = (int64_t)a.tokens / kRatio;  // no row sees more blocks than this
-  if (n_cap == 0) return cudaSuccess;
+  if (n_cap == 0 || a.n_rows == 0) return cudaSuccess;
+  if ((int64_t)a.n_rows * kHeads > INT32_MAX) return cudaErrorInvalidValue;
   EncodeTiledFn enc = encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
-  // block keys: 2D [n_cap rows, 128 bf16], rows 256 B apart; boxes of 128 rows x 64 dims
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)n_cap};
-  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)kBN};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.block_keys),
-                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-
+  // block keys: 2D [n_cap rows, 128 bf16], rows 256 B apart; boxes of 128 rows x 64 dims
+  CUtensorMap kmap;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)n_cap};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kBN};
+    if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(a.block_keys),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  // prepared queries: 2D [n_rows * 4, 128 bf16]; boxes of 256 rows (64 query rows) x 64 dims
+  CUtensorMap qmap;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)a.n_rows * kHeads};
+    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kQCols};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qws, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -557,10 +503,12 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  cudaError_t e = launch_qprep(a, qws, stream);
+  if (e != cudaSuccess) return e;
   // persistent: one CTA per SM, each taking a balanced contiguous range of
-  // (row tile, block tile) units; more than kMaxRowTiles row tiles go in slabs
+  // (row tile, block tile) units; more than kMaxRowTiles row tiles go in slabs,
+  // and row tiles x block tiles stays in int32 per slab
   const int32_t tiles_total = (int32_t)((n_cap + kBN - 1) / kBN);
-  // per slab: at most kMaxRowTiles row tiles, and row tiles x block tiles in int32
   int64_t slab_tiles = (int64_t)INT32_MAX / tiles_total;
   if (slab_tiles > kMaxRowTiles) slab_tiles = kMaxRowTiles;
   const int32_t slab = (int32_t)slab_tiles * kRowsPerCta;
@@ -574,8 +522,9 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream) {
     const int64_t row_tiles = (b.n_rows + kRowsPerCta - 1) / kRowsPerCta;
     int64_t ctas = sm_count();
     if (ctas > row_tiles * tiles_total) ctas = row_tiles * tiles_total;
-    score_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(map, b, tiles_total, r0);
-    cudaError_t e = cudaGetLastError();
+    score_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(kmap, qmap, b, tiles_total,
+                                                                      r0);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -94,10 +94,11 @@ def test_pool_refusals(lib):
 
 
 def score(lib, q=A, q_stride=640, pos=B, vis=None, n_rows=0, tokens=4096, w=A, cos=A, sin=A,
-          rows=4096, eps=1e-6, keys=A, base=None, scores=A, cols=1024, status=B, path=0):
+          rows=4096, eps=1e-6, keys=A, base=None, scores=A, cols=1024, status=B, path=0, ws=None,
+          wsb=0):
     return lib.qsa_score_rows_with(P(q), q_stride, P(pos), P(vis or 0), n_rows, tokens, P(w),
                                    P(cos), P(sin), rows, eps, P(keys), P(base or 0), P(scores),
-                                   cols, P(status), path, None)
+                                   cols, P(status), path, P(ws or 0), wsb, None)
 
 
 def test_score_refusals(lib):
@@ -105,27 +106,32 @@ def test_score_refusals(lib):
     for kw in (dict(q_stride=504), dict(q_stride=644), dict(q=U), dict(keys=U), dict(scores=U),
                dict(cols=1020), dict(cols=1022), dict(rows=4095), dict(eps=-1e-6),
                dict(q=0), dict(pos=0), dict(keys=0), dict(scores=0), dict(w=0), dict(cos=0),
-               dict(path=3), dict(path=2, base=B)):
+               dict(path=3), dict(path=2, base=B, ws=A, wsb=1 << 20), dict(path=2),
+               dict(path=2, ws=A, wsb=3 * 1024 - 1), dict(path=2, ws=U, wsb=1 << 20),
+               dict(wsb=-1)):
         assert score(lib, n_rows=3, **kw) == 1, kw
     assert score(lib, n_rows=-3) == 1
+    assert lib.qsa_score_workspace_bytes(3) == 3 * 1024
+    assert lib.qsa_score_workspace_bytes(0) == 0 and lib.qsa_score_workspace_bytes(-1) == -1
 
 
 def test_index_select_refusals(lib):
     def call(**kw):
         a = dict(keys=A, ks=640, f=0, nb=0, kw=A, q=A, qs=640, pos=B, n=0, tokens=4096, qw=A,
                  cos=A, sin=A, rows=4096, eps=1e-6, budget=2048, bk=A, sc=A, cols=1024, mask=A,
-                 st=B)
+                 st=B, ws=0, wsb=0)
         a.update(kw)
         return lib.qsa_index_select(P(a["keys"]), a["ks"], a["f"], a["nb"], P(a["kw"]), P(a["q"]),
                                     a["qs"], P(a["pos"]), a["n"], a["tokens"], P(a["qw"]),
                                     P(a["cos"]), P(a["sin"]), a["rows"], a["eps"], a["budget"],
                                     P(a["bk"]), P(a["sc"]), a["cols"], P(a["mask"]), P(a["st"]),
-                                    None)
+                                    P(a["ws"]), a["wsb"], None)
     assert call() == 0
     assert call(budget=2047) == 1
     assert call(nb=4, ks=100) == 1
     assert call(n=2, qs=100) == 1
     assert call(n=2, cols=100) == 1
+    assert call(wsb=-5) == 1
 
 
 def test_status_calls_refuse_null(lib):

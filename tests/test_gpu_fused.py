@@ -53,7 +53,7 @@ def test_prefill_end_to_end(qsa, orc, tables):
     st = qsa.new_status()
     qsa.qsa_index_select(fq_d.view(-1)[512:], 640, 0, nb, dev(case["k_norm_w"]), fq_d, 640,
                          dev(case["pos"]), T, T, dev(case["q_norm_w"]), cd, sd, c.shape[0], EPS,
-                         BUDGET, bk, sc, cols, mask, st)
+                         BUDGET, bk, sc, cols, mask, st, workspace=qsa.new_workspace(T))
     assert qsa.qsa_read_status(st) == (0, 0)
     keys_o = orc.pool_blocks(fq.reshape(-1)[512:], 640, 0, nb, case["k_norm_w"], c, s, EPS)
     assert np.array_equal(bk.cpu().numpy().view(np.uint16), keys_o)

@@ -105,7 +105,7 @@ def test_score_prefill_all_rows(qsa, orc, tables, path):
     st = qsa.new_status()
     qsa.qsa_score_rows_with(dev(case["fq"]), 640, dev(case["pos"]), None, T, T,
                             dev(case["q_norm_w"]), cd, sd, c.shape[0], EPS, dev(keys), None, sc,
-                            cols, st, path=path)
+                            cols, st, path=path, workspace=qsa.new_workspace(T))
     assert qsa.qsa_read_status(st) == (0, 0)
     got = sc.cpu().numpy()
     want, res = oracle_scores(orc, case["fq"], 640, case["pos"], T, case["q_norm_w"], c, s, keys,
@@ -182,7 +182,7 @@ def test_score_nan_key_propagates(qsa, orc, tables, path):
     st = qsa.new_status()
     qsa.qsa_score_rows_with(dev(case["fq"]), 640, dev(case["pos"]), None, T, T,
                             dev(case["q_norm_w"]), cd, sd, c.shape[0], EPS, dev(keys), None, sc,
-                            cols, st, path=path)
+                            cols, st, path=path, workspace=qsa.new_workspace(T))
     assert qsa.qsa_read_status(st) == (0, 0)
     got = sc.cpu().numpy()
     rows_seeing = np.arange(T)[(np.arange(T) + 1) // 4 > 37]
@@ -229,8 +229,9 @@ def test_score_tc_ragged_tiles(qsa, orc, tables, n_rows, tokens, seed):
     cols = nb + 4 - nb % 4 + 4
     sc = torch.full((n_rows, cols), -7.0, dtype=torch.float32, device="cuda")
     st = qsa.new_status()
+    ws = qsa.new_workspace(n_rows)
     qsa.qsa_score_rows_with(dev(q), 640, dev(pos), dev(vis), n_rows, tokens, dev(qw), cd, sd,
-                            c.shape[0], EPS, dev(keys), None, sc, cols, st, path=2)
+                            c.shape[0], EPS, dev(keys), None, sc, cols, st, path=2, workspace=ws)
     assert qsa.qsa_read_status(st) == (0, 0)
     want, _ = oracle_scores(orc, q, 640, pos, tokens, qw, c, s, keys, cols, visible_len=vis)
     assert_close(sc.cpu().numpy(), want, f"tcgen05 scores {n_rows}x{tokens}")
@@ -240,7 +241,8 @@ def test_score_tc_ragged_tiles(qsa, orc, tables, n_rows, tokens, seed):
         sc.fill_(-7.0)
         st = qsa.new_status()
         qsa.qsa_score_rows_with(dev(q), 640, dev(pos_bad), None, n_rows, tokens, dev(qw), cd, sd,
-                                c.shape[0], EPS, dev(keys), None, sc, cols, st, path=2)
+                                c.shape[0], EPS, dev(keys), None, sc, cols, st, path=2,
+                                workspace=ws)
         assert qsa.qsa_read_status(st) == (3, 2)
         got = sc.cpu().numpy()
         assert np.all(got[2] == -7.0)
@@ -269,7 +271,7 @@ def test_score_tc_chunk_64k_sampled(qsa, orc, tables):
     sc = torch.full((rows, cols), -7.0, dtype=torch.float32, device="cuda")
     st = qsa.new_status()
     qsa.qsa_score_rows(dev(q), 640, dev(pos), None, rows, tokens, dev(qw), cd, sd, c.shape[0], EPS,
-                       keys_d, None, sc, cols, st)
+                       keys_d, None, sc, cols, st, workspace=qsa.new_workspace(rows))
     assert qsa.qsa_read_status(st) == (0, 0)
     got = sc.cpu().numpy()
     n = (pos + 1) // 4

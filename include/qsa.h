@@ -164,6 +164,36 @@ qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_
                                void *stream);
 
 /*
+ * qsa_score_rows_noalloc -- the tensor-core scorer without a caller workspace.
+ * The pages have no counterpart to this entry point.  It serves callers that
+ * cannot allocate device memory when they score: engines that reserve all free
+ * HBM up front (for their KV cache) and forbid allocation afterwards, code
+ * running where the CUDA allocator may not be called (a host callback), and
+ * real-time loops that cannot take an allocation's latency or failure
+ * mid-step.  Arguments are those of qsa_score_rows with key_base == NULL and
+ * no workspace; the library allocates nothing here either: the query-prep
+ * workspace is a file-scope device array of QSA_NOALLOC_MAX_ROWS * 1024 bytes
+ * (8 MiB) that every GPU loading the library holds until exit.
+ *  - n_rows > QSA_NOALLOC_MAX_ROWS is refused with QSA_ERR_INVALID_VALUE before
+ *    any launch; other refusals are qsa_score_rows_with's (QSA_SCORE_TCGEN05).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; QSA_ERR_LAUNCH if the
+ *    lookup fails.  Make the first call on each device before any stream
+ *    capture.
+ *  - Every call shares the one array and it keeps the last call's contents;
+ *    each call overwrites all of it that it reads, so nothing must start at
+ *    zero.  Calls that overlap on the GPU (unordered streams or host threads
+ *    on one device) race on it: order them.
+ */
+#define QSA_NOALLOC_MAX_ROWS 8192
+qsa_status qsa_score_rows_noalloc(const uint16_t *q, int64_t q_stride, const int32_t *pos,
+                                  const int32_t *visible_len, int32_t n_rows, int32_t tokens,
+                                  const uint16_t *q_norm_w, const uint16_t *cos_t,
+                                  const uint16_t *sin_t, int32_t table_rows, float eps,
+                                  const uint16_t *block_keys, float *scores, int64_t score_cols,
+                                  int32_t *dev_status, void *stream);
+
+/*
  * Exact top-(budget/4) block selection into a u8 visibility mask.
  * Source: PR #1178 "Exact semantics" (blocks, tail, keep; canonical order
  * descending score then ascending block index; threshold-equal blocks fill the

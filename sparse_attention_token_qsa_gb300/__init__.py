@@ -34,7 +34,8 @@ HEADS, HEAD_DIM, RATIO, ROT_DIM, FUSED_WIDTH = 4, 128, 4, 64, 640
 
 EXPORTED = ("qsa_version", "qsa_status_string", "qsa_rope_tables", "qsa_pool_blocks",
             "qsa_score_rows", "qsa_score_rows_with", "qsa_score_workspace_bytes",
-            "qsa_select_mask", "qsa_index_select", "qsa_reset_status", "qsa_read_status")
+            "qsa_score_rows_noalloc", "qsa_select_mask", "qsa_index_select", "qsa_reset_status",
+            "qsa_read_status")
 
 
 class QsaError(RuntimeError):
@@ -60,6 +61,7 @@ def _load() -> ctypes.CDLL:
         "qsa_score_rows_with": ([P, i64, P, P, i32, i32, P, P, P, i32, f32, P, P, P, i64, P, i32, P,
                                  i64, P], i32),
         "qsa_score_workspace_bytes": ([i32], i64),
+        "qsa_score_rows_noalloc": ([P, i64, P, P, i32, i32, P, P, P, i32, f32, P, P, i64, P, P], i32),
         "qsa_select_mask": ([P, i64, P, i32, i32, i32, P, P, P], i32),
         "qsa_index_select": ([P, i64, i32, i32, P, P, i64, P, i32, i32, P, P, P, i32, f32, i32, P, P,
                               i64, P, P, P, i64, P], i32),
@@ -170,6 +172,24 @@ def qsa_score_rows(q, q_stride, pos, visible_len, n_rows, tokens, q_norm_w, cos_
                                _dev(scores, "scores"), int(score_cols),
                                _dev(dev_status, "dev_status"), ws, int(wsb), _stream(stream)),
            "qsa_score_rows")
+
+
+QSA_NOALLOC_MAX_ROWS = 8192
+
+
+def qsa_score_rows_noalloc(q, q_stride, pos, visible_len, n_rows, tokens, q_norm_w, cos_t, sin_t,
+                           table_rows, eps, block_keys, scores, score_cols, dev_status,
+                           stream=None) -> None:
+    """Tensor-core scoring with the library's built-in workspace (no allocation
+    by anyone); at most QSA_NOALLOC_MAX_ROWS rows, calls must not overlap."""
+    _check(_lib.qsa_score_rows_noalloc(_dev(q, "q"), int(q_stride), _dev(pos, "pos"),
+                                       _dev(visible_len, "visible_len"), int(n_rows), int(tokens),
+                                       _dev(q_norm_w, "q_norm_w"), _dev(cos_t, "cos_t"),
+                                       _dev(sin_t, "sin_t"), int(table_rows), float(eps),
+                                       _dev(block_keys, "block_keys"), _dev(scores, "scores"),
+                                       int(score_cols), _dev(dev_status, "dev_status"),
+                                       _stream(stream)),
+           "qsa_score_rows_noalloc")
 
 
 def qsa_select_mask(scores, score_cols, pos, n_rows, tokens, budget, mask, dev_status,

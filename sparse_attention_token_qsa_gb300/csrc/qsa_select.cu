@@ -32,16 +32,30 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelMaxCluster = 16;
 constexpr int kSelCapMax = 16384;  // keys cached per CTA (64 KiB)
 
+// Radix rounds over the 32-bit order key: round 0 takes the top 12 bits
+// (4096 bins: sign, exponent and 3 mantissa bits, so one round already splits
+// a binade eight ways), rounds 1..3 take 8, 8 and 4 bits.
+constexpr int kRounds = 4;
+__host__ __device__ constexpr int round_bins(int r) { return r == 0 ? 4096 : (r == 3 ? 16 : 256); }
+// key >> round_shift(r) = the prefix known after round r
+__host__ __device__ constexpr int round_shift(int r) { return r == 0 ? 20 : (r == 1 ? 12 : (r == 2 ? 4 : 0)); }
+constexpr int kCandCap = 4096;                    // keys of round 0's bin kept for rounds 1..3
+constexpr uint32_t kZeroKey = 0x80000000u;        // order key of +0.0 (and folded -0.0)
+
 struct SelectSmem {
-  uint32_t hist[2][257];  // [buffer][bin], slot 256 = non-finite count
-  uint32_t merged[256];
+  uint32_t hist0[4096];  // per-round histograms; in a cluster round 0's is merged in place
+  uint32_t hist1[256];
+  uint32_t hist2[256];
+  uint32_t hist3[16];
   uint32_t warp_tot[kSelWarps];
-  uint32_t scan_tot[kSelWarps];
+  uint32_t msmall[256];  // rounds 1..3 merged over a cluster
+  uint32_t nonfinite;
+  uint32_t nonfinite_all;
+  uint32_t ncand;
   int32_t sel_bin;
   uint32_t sel_above;
   uint32_t eq_base;
-  uint32_t nonfinite;
-  // keys[] follows (dynamic)
+  // cand[kCandCap] and keys[] follow (dynamic)
 };
 
 __device__ __forceinline__ uint32_t order_key(float s) {
@@ -148,13 +162,49 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
   return before + incl - v;
 }
 
+// Find the bin of histogram M[nb] (shared memory) that holds the need-th
+// largest key, scanning bins from the top: S.sel_bin gets the bin, S.sel_above
+// the number of keys in higher bins.  Every thread of the CTA calls it.
+__device__ __forceinline__ void find_bin(const uint32_t *M, int nb, uint32_t need, SelectSmem &S) {
+  const int tid = threadIdx.x;
+  const int per = (nb + kSelThreads - 1) / kSelThreads;
+  const int hi = nb - 1 - tid * per;  // this thread's bins: hi, hi-1, ..., hi-per+1
+  uint32_t sum = 0;
+  for (int j = 0; j < per; ++j)
+    if (hi - j >= 0) sum += M[hi - j];
+  uint32_t total;
+  const uint32_t before = block_excl_scan(sum, S.warp_tot, total);
+  if (before < need && need <= before + sum) {
+    uint32_t acc = before;
+    for (int j = 0; j < per; ++j) {
+      const uint32_t c = M[hi - j];
+      if (acc + c >= need) {
+        S.sel_bin = hi - j;
+        S.sel_above = acc;
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
+
+// Lanes below this one in the warp.
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
 __global__ void __launch_bounds__(kSelThreads)
 select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_t *__restrict__ pos,
               int32_t tokens, int32_t keep_max, uint8_t *__restrict__ mask, int32_t *status,
               int32_t C, int32_t cap) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectSmem &S = *reinterpret_cast<SelectSmem *>(smem_raw);
-  uint32_t *keys_s = reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(SelectSmem) + 15) & ~size_t(15)));
+  uint32_t *cand_s =
+      reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(SelectSmem) + 15) & ~size_t(15)));
+  uint32_t *keys_s = cand_s + kCandCap;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t row = blockIdx.x / C;
@@ -183,11 +233,16 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   const float *srow = scores + (int64_t)row * score_cols + b0;
   const int32_t cached = min(cnt, cap);
 
-  for (int i = tid; i < 2 * 257; i += kSelThreads) (&S.hist[0][0])[i] = 0u;
-  if (tid == 0) S.eq_base = 0u;
+  for (int i = tid; i < 4096 + 256 + 256 + 16; i += kSelThreads) (&S.hist0[0])[i] = 0u;
+  if (tid == 0) {
+    S.nonfinite = 0u;
+    S.ncand = 0u;
+    S.eq_base = 0u;
+  }
   __syncthreads();
 
-  // ---- pass 0: load, check, key, histogram of the top byte
+  // ---- round 0 while loading: key cache, finiteness, top-12-bit histogram.
+  // Exact zeros (relu outputs) share one bin: counted by ballot, not match.any.
   {
     const int32_t nq = (cnt + 3) >> 2;
     uint32_t nonfinite = 0;
@@ -207,86 +262,123 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
           key = order_key(sv[e]);
           if (i < cached) keys_s[i] = key;
         }
-        hist_add(S.hist[0], key >> 24, valid);
+        const bool zero = valid && key == kZeroKey;
+        const uint32_t zb = __ballot_sync(0xffffffffu, zero);
+        if (lane == 0 && zb) atomicAdd(&S.hist0[kZeroKey >> 20], (uint32_t)__popc(zb));
+        hist_add(S.hist0, key >> 20, valid && !zero);
       }
     }
-    if (nonfinite) atomicAdd(&S.hist[0][256], 1u);
+    if (nonfinite) atomicOr(&S.nonfinite, 1u);
   }
 
-  uint32_t prefix = 0;   // digits found so far
-  int bits = 0;          // how many of the key's top bits `prefix` holds
+  uint32_t prefix = 0;   // the threshold's top bits found so far
+  int shift = 32;        // prefix = threshold >> shift
   uint32_t need = (uint32_t)min(keep_max, n);  // keys still to keep at/below the prefix
   bool done = false;     // every key matching the prefix is kept
   bool bad = false;      // a non-finite score somewhere in the row
+  bool use_cand = false; // rounds 1..3 run on the compacted candidates
 
-  for (int pass = 0; pass < 4; ++pass) {
-    const int buf = pass & 1;
-    const int shift = 24 - 8 * pass;
-    if (pass > 0) {  // histogram the next digit of the candidates
-      for (int32_t ib = warp * 32; ib < cnt; ib += kSelThreads) {
+  for (int r = 0; r < kRounds; ++r) {
+    uint32_t *H = r == 0 ? S.hist0 : (r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3));
+    const int nb = round_bins(r);
+    const int sh = round_shift(r);
+    if (r > 0) {  // histogram this round's digit of the keys matching the prefix
+      const int32_t n_src = use_cand ? (int32_t)S.ncand : cnt;
+      for (int32_t ib = warp * 32; ib < n_src; ib += kSelThreads) {
         const int32_t i = ib + lane;
-        const bool in = i < cnt;
+        const bool in = i < n_src;
         uint32_t key = 0;
-        if (in) key = (i < cached) ? keys_s[i] : order_key(__ldg(srow + i));
-        const bool cand = in && ((key >> (shift + 8)) == prefix);
-        hist_add(S.hist[buf], (key >> shift) & 0xffu, cand);
+        if (in) key = use_cand ? cand_s[i] : (i < cached ? keys_s[i] : order_key(__ldg(srow + i)));
+        const bool match = in && (key >> shift) == prefix;
+        hist_add(H, (key >> sh) & (uint32_t)(nb - 1), match);
       }
     }
-    // publish this CTA's histogram to the cluster, then merge all of them
+    // make the local histogram visible, then merge over the cluster
     if (C > 1) cluster_sync_all(); else __syncthreads();
-    if (tid < 256) {
-      uint32_t t = 0;
-      for (int r = 0; r < C; ++r)
-        t += (C > 1) ? ld_dsmem(&S.hist[buf][tid], (uint32_t)r) : S.hist[buf][tid];
-      S.merged[tid] = t;
-    } else if (pass == 0 && tid == 256) {
-      uint32_t nf = 0;
-      for (int r = 0; r < C; ++r)
-        nf += (C > 1) ? ld_dsmem(&S.hist[0][256], (uint32_t)r) : S.hist[0][256];
-      S.nonfinite = nf;
-    }
-    // the next pass fills the other buffer; every peer finished reading it
-    // (previous pass's merge) before arriving at the barrier above
-    if (tid < 257) S.hist[buf ^ 1][tid] = 0u;
-    __syncthreads();
-    if (pass == 0 && S.nonfinite != 0) {
-      bad = true;
-      break;
-    }
-    // find the digit holding the need-th largest key: inclusive scan of the
-    // merged histogram from the top bin down (threads 0..255 = bins 255..0)
-    uint32_t c = 0, incl = 0;
-    if (tid < 256) {
-      c = S.merged[255 - tid];
-      incl = c;
+    const uint32_t *M = H;
+    if (r == 0) {
+      if (C > 1) {
+        if (tid == 0) {
+          uint32_t nf = 0;
+          for (int q = 0; q < C; ++q) nf |= ld_dsmem(&S.nonfinite, (uint32_t)q);
+          S.nonfinite_all = nf;
+        }
+      } else if (tid == 0) {
+        S.nonfinite_all = S.nonfinite;
+      }
+      __syncthreads();
+      if (S.nonfinite_all != 0u) {  // the same verdict in every CTA of the cluster
+        bad = true;
+        break;
+      }
+      if (C > 1) {
+        // reduce-scatter: this CTA sums its slice of bins over the cluster, in place
+        const int slice = nb / C;
+        for (int b = (int)rank * slice + tid; b < ((int)rank + 1) * slice; b += kSelThreads) {
+          uint32_t v[kSelMaxCluster];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+          for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&H[b], (uint32_t)q) : 0u;
+          uint32_t t = 0;
+#pragma unroll
+          for (int q = 0; q < kSelMaxCluster; ++q) t += v[q];
+          H[b] = t;
+        }
+        cluster_sync_all();
+        // gather the other slices' merged bins (their owners no longer change them)
+        uint32_t g[4096 / kSelThreads];
+#pragma unroll
+        for (int j = 0; j < 4096 / kSelThreads; ++j) {
+          const int b = tid + j * kSelThreads;
+          const int owner = b / slice;
+          g[j] = owner != (int)rank ? ld_dsmem(&H[b], (uint32_t)owner) : H[b];
+        }
+#pragma unroll
+        for (int j = 0; j < 4096 / kSelThreads; ++j) H[tid + j * kSelThreads] = g[j];
+        __syncthreads();
       }
-      if (lane == 31) S.scan_tot[warp] = incl;
-    }
-    __syncthreads();
-    if (tid < 256) {
-      uint32_t before = 0;
-      for (int w = 0; w < warp; ++w) before += S.scan_tot[w];
-      const uint32_t hi_incl = before + incl, hi_excl = hi_incl - c;
-      if (hi_excl < need && need <= hi_incl) {
-        S.sel_bin = 255 - tid;
-        S.sel_above = hi_excl;
+    } else if (C > 1) {
+      for (int b = tid; b < nb; b += kSelThreads) {
+        uint32_t v[kSelMaxCluster];
+#pragma unroll
+        for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&H[b], (uint32_t)q) : 0u;
+        uint32_t t = 0;
+#pragma unroll
+        for (int q = 0; q < kSelMaxCluster; ++q) t += v[q];
+        S.msmall[b] = t;
       }
+      __syncthreads();
+      M = S.msmall;
     }
-    __syncthreads();
+    find_bin(M, nb, need, S);
     const uint32_t B = (uint32_t)S.sel_bin;
+    const uint32_t cntB = M[B];
     need -= S.sel_above;
-    prefix = (prefix << 8) | B;
-    bits += 8;
-    if (S.merged[B] == need) {
+    prefix = (r == 0) ? B : ((prefix << (shift - sh)) | B);
+    shift = sh;
+    if (cntB == need) {
       done = true;  // the whole bin is kept: no tie to rank
-    } else if (pass == 3 && tid == 0) {
+    } else if (r == 0) {
+      use_cand = cntB <= (uint32_t)kCandCap;  // the merged count bounds every CTA's share
+      if (use_cand) {  // compact this CTA's keys of the bin
+        for (int32_t ib = warp * 32; ib < cnt; ib += kSelThreads) {
+          const int32_t i = ib + lane;
+          const bool in = i < cnt;
+          uint32_t key = 0;
+          if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
+          const bool c = in && (key >> 20) == prefix;
+          const uint32_t m = __ballot_sync(0xffffffffu, c);
+          if (m) {
+            uint32_t base = 0;
+            if (lane == 0) base = atomicAdd(&S.ncand, (uint32_t)__popc(m));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (c) cand_s[base + __popc(m & lanemask_lt())] = key;
+          }
+        }
+      }
+    } else if (r == kRounds - 1 && tid == 0) {
       // keys equal to the threshold in lower-ranked CTAs precede ours in block order
       uint32_t e = 0;
-      for (uint32_t r = 0; r < rank; ++r) e += ld_dsmem(&S.hist[buf][B], r);
+      for (uint32_t q = 0; q < rank; ++q) e += ld_dsmem(&S.hist3[B], q);
       S.eq_base = e;
     }
     __syncthreads();
@@ -296,8 +388,6 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   if (!bad) {
     const uintptr_t rb = reinterpret_cast<uintptr_t>(mrow);
     const bool al16 = (rb & 15u) == 0, al4 = (rb & 3u) == 0;
-    const uint32_t thresh = prefix;
-    const int tshift = 32 - bits;
     uint32_t running = done ? 0u : S.eq_base;
     for (int32_t tb = 0; tb < cnt; tb += 4 * kSelThreads) {
       const int32_t i = tb + 4 * tid;
@@ -312,21 +402,21 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       if (done) {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (e < m && (k[e] >> tshift) >= thresh) kept |= 1u << e;
-      } else {
+          if (e < m && (k[e] >> shift) >= prefix) kept |= 1u << e;
+      } else {  // the threshold key itself: ties filled in block order
         uint32_t eqc = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) eqc += (e < m && k[e] == thresh) ? 1u : 0u;
+        for (int e = 0; e < 4; ++e) eqc += (e < m && k[e] == prefix) ? 1u : 0u;
         uint32_t total;
-        uint32_t r = running + block_excl_scan(eqc, S.warp_tot, total);
+        uint32_t rk = running + block_excl_scan(eqc, S.warp_tot, total);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (e >= m) continue;
-          if (k[e] > thresh) {
+          if (k[e] > prefix) {
             kept |= 1u << e;
-          } else if (k[e] == thresh) {
-            if (r < need) kept |= 1u << e;
-            ++r;
+          } else if (k[e] == prefix) {
+            if (rk < need) kept |= 1u << e;
+            ++rk;
           }
         }
         running += total;
@@ -342,14 +432,15 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   } else if (rank == 0 && tid == 0) {
     report_error(status, kErrNonFinite, row);
   }
-  // no CTA may leave while a peer can still read its histograms
+  // no CTA may leave while a peer can still read its shared memory
   if (C > 1) cluster_sync_all();
 }
 
 static int g_max_cluster = -1;
 
 static size_t select_smem_bytes(int32_t cap) {
-  return ((sizeof(SelectSmem) + 15) & ~size_t(15)) + 4 * (size_t)(cap > 0 ? cap : 1);
+  return ((sizeof(SelectSmem) + 15) & ~size_t(15)) + 4 * (size_t)kCandCap +
+         4 * (size_t)(cap > 0 ? cap : 1);
 }
 
 // Largest cluster the select kernel can be co-scheduled with (16 needs the

@@ -244,28 +244,37 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   // ---- round 0 while loading: key cache, finiteness, top-12-bit histogram.
   // Exact zeros (relu outputs) share one bin: counted by ballot, not match.any.
   {
+    constexpr int kLoadsInFlight = 4;  // float4 loads issued per thread before use
     const int32_t nq = (cnt + 3) >> 2;
     uint32_t nonfinite = 0;
-    for (int32_t qb = warp * 32; qb < nq; qb += kSelThreads) {
-      const int32_t qd = qb + lane;
-      const bool qv = qd < nq;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (qv) v = __ldg(reinterpret_cast<const float4 *>(srow) + qd);
-      const float sv[4] = {v.x, v.y, v.z, v.w};
+    for (int32_t qb = warp * 32; qb < nq; qb += kSelThreads * kLoadsInFlight) {
+      float4 v[kLoadsInFlight];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int32_t i = 4 * qd + e;
-        const bool valid = qv && i < cnt;
-        uint32_t key = 0;
-        if (valid) {
-          if (!isfinite(sv[e])) nonfinite = 1;
-          key = order_key(sv[e]);
-          if (i < cached) keys_s[i] = key;
+      for (int u = 0; u < kLoadsInFlight; ++u) {
+        const int32_t qd = qb + u * kSelThreads + lane;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (qd < nq) v[u] = __ldg(reinterpret_cast<const float4 *>(srow) + qd);
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadsInFlight; ++u) {
+        const int32_t qd = qb + u * kSelThreads + lane;
+        const bool qv = qd < nq;
+        const float sv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int32_t i = 4 * qd + e;
+          const bool valid = qv && i < cnt;
+          uint32_t key = 0;
+          if (valid) {
+            if (!isfinite(sv[e])) nonfinite = 1;
+            key = order_key(sv[e]);
+            if (i < cached) keys_s[i] = key;
+          }
+          const bool zero = valid && key == kZeroKey;
+          const uint32_t zb = __ballot_sync(0xffffffffu, zero);
+          if (lane == 0 && zb) atomicAdd(&S.hist0[kZeroKey >> 20], (uint32_t)__popc(zb));
+          hist_add(S.hist0, key >> 20, valid && !zero);
         }
-        const bool zero = valid && key == kZeroKey;
-        const uint32_t zb = __ballot_sync(0xffffffffu, zero);
-        if (lane == 0 && zb) atomicAdd(&S.hist0[kZeroKey >> 20], (uint32_t)__popc(zb));
-        hist_add(S.hist0, key >> 20, valid && !zero);
       }
     }
     if (nonfinite) atomicOr(&S.nonfinite, 1u);

@@ -15,9 +15,11 @@
 //  * a row is split over a cluster of C CTAs (C = 1..16): each CTA owns a
 //    contiguous, 4-aligned slice of the row's blocks and keeps its keys in
 //    shared memory, so HBM sees each score once;
-//  * per pass every CTA builds a 256-bin histogram of its candidates
-//    (warp-aggregated with match.any), the cluster merges the C histograms
-//    through distributed shared memory, and every CTA derives the same digit;
+//  * the first round histograms the top 12 bits of every key as it is loaded
+//    (exact zeros counted by ballot, a warp-uniform bin added once); the keys
+//    of the selected bin are compacted and rounds of 8, 8 and 4 bits run on
+//    them only; each round's histograms are merged over the cluster through
+//    distributed shared memory and every CTA derives the same digit;
 //  * ties at the final key are ranked in index order by the count of equal
 //    keys in lower-ranked CTAs (read from their last histogram) plus an
 //    in-CTA block scan;
@@ -82,12 +84,19 @@ __device__ __forceinline__ uint32_t ld_dsmem(const uint32_t *local, uint32_t ran
   return v;
 }
 
-// Warp-aggregated histogram increment; every lane of the warp must call it.
+// Histogram increment for one key per lane; every lane of the warp calls it.
+// A warp whose active lanes all share one bin adds once; otherwise each lane
+// adds its own (exact zeros, the common heavy bin, are peeled off beforehand
+// by the caller, so the remaining lanes rarely collide).
 __device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, bool valid) {
   const unsigned act = __ballot_sync(0xffffffffu, valid);
-  if (valid) {
-    const unsigned peers = __match_any_sync(act, bin);
-    if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+  if (act == 0u) return;
+  const int leader = __ffs(act) - 1;
+  const uint32_t b0 = __shfl_sync(0xffffffffu, bin, leader);
+  if (__all_sync(0xffffffffu, !valid || bin == b0)) {
+    if ((int)(threadIdx.x & 31) == leader) atomicAdd(&h[b0], (uint32_t)__popc(act));
+  } else if (valid) {
+    atomicAdd(&h[bin], 1u);
   }
 }
 

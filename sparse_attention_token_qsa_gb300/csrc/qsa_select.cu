@@ -50,6 +50,7 @@ struct SelectSmem {
   uint32_t hist2[256];
   uint32_t hist3[16];
   uint32_t warp_tot[kSelWarps];
+  uint32_t wcount[kSelWarps];
   uint32_t msmall[256];  // rounds 1..3 merged over a cluster
   uint32_t nonfinite;
   uint32_t nonfinite_all;
@@ -84,20 +85,11 @@ __device__ __forceinline__ uint32_t ld_dsmem(const uint32_t *local, uint32_t ran
   return v;
 }
 
-// Histogram increment for one key per lane; every lane of the warp calls it.
-// A warp whose active lanes all share one bin adds once; otherwise each lane
-// adds its own (exact zeros, the common heavy bin, are peeled off beforehand
-// by the caller, so the remaining lanes rarely collide).
+// Histogram increment for one key per lane (exact zeros, the one heavy bin of
+// relu scores, are counted separately by the caller with a ballot, so the
+// remaining lanes of a warp rarely hit the same bin).
 __device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, bool valid) {
-  const unsigned act = __ballot_sync(0xffffffffu, valid);
-  if (act == 0u) return;
-  const int leader = __ffs(act) - 1;
-  const uint32_t b0 = __shfl_sync(0xffffffffu, bin, leader);
-  if (__all_sync(0xffffffffu, !valid || bin == b0)) {
-    if ((int)(threadIdx.x & 31) == leader) atomicAdd(&h[b0], (uint32_t)__popc(act));
-  } else if (valid) {
-    atomicAdd(&h[bin], 1u);
-  }
+  if (valid) atomicAdd(&h[bin], 1u);
 }
 
 // Write bytes [a, b) of a mask row: byte t = (t <= p).
@@ -269,16 +261,24 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         const int32_t qd = qb + u * kSelThreads + lane;
         const bool qv = qd < nq;
         const float sv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t kq[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kq[e] = order_key(sv[e]);
+          if (qv && 4 * qd + e < cnt && !isfinite(sv[e])) nonfinite = 1;
+        }
+        if (qv && 4 * qd + 3 < cached) {  // one 16-byte store per quad
+          *reinterpret_cast<uint4 *>(keys_s + 4 * qd) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+        } else if (qv) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int32_t i = 4 * qd + e;
           const bool valid = qv && i < cnt;
-          uint32_t key = 0;
-          if (valid) {
-            if (!isfinite(sv[e])) nonfinite = 1;
-            key = order_key(sv[e]);
-            if (i < cached) keys_s[i] = key;
-          }
+          const uint32_t key = kq[e];
           const bool zero = valid && key == kZeroKey;
           const uint32_t zb = __ballot_sync(0xffffffffu, zero);
           if (lane == 0 && zb) atomicAdd(&S.hist0[kZeroKey >> 20], (uint32_t)__popc(zb));
@@ -377,21 +377,41 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       done = true;  // the whole bin is kept: no tie to rank
     } else if (r == 0) {
       use_cand = cntB <= (uint32_t)kCandCap;  // the merged count bounds every CTA's share
-      if (use_cand) {  // compact this CTA's keys of the bin
-        for (int32_t ib = warp * 32; ib < cnt; ib += kSelThreads) {
-          const int32_t i = ib + lane;
-          const bool in = i < cnt;
+      if (use_cand) {
+        // compact this CTA's keys of the bin, in block order and without
+        // atomics: each warp counts the matches in its own contiguous range,
+        // a scan of the warp counts gives each warp its offset, then each warp
+        // writes its matches with a ballot prefix
+        const int32_t wlen = (cnt + kSelWarps - 1) / kSelWarps;
+        const int32_t w_lo = min(cnt, warp * wlen);
+        const int32_t w_hi = min(cnt, w_lo + wlen);
+        uint32_t wc = 0;
+        for (int32_t i0 = w_lo; i0 < w_hi; i0 += 32) {
+          const int32_t i = i0 + lane;
+          const bool in = i < w_hi;
+          uint32_t key = 0;
+          if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
+          wc += (uint32_t)__popc(__ballot_sync(0xffffffffu, in && (key >> 20) == prefix));
+        }
+        if (lane == 0) S.wcount[warp] = wc;
+        __syncthreads();
+        uint32_t base = 0, total = 0;
+        for (int w = 0; w < kSelWarps; ++w) {
+          const uint32_t c = S.wcount[w];
+          base += (w < warp) ? c : 0u;
+          total += c;
+        }
+        for (int32_t i0 = w_lo; i0 < w_hi; i0 += 32) {
+          const int32_t i = i0 + lane;
+          const bool in = i < w_hi;
           uint32_t key = 0;
           if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
           const bool c = in && (key >> 20) == prefix;
           const uint32_t m = __ballot_sync(0xffffffffu, c);
-          if (m) {
-            uint32_t base = 0;
-            if (lane == 0) base = atomicAdd(&S.ncand, (uint32_t)__popc(m));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (c) cand_s[base + __popc(m & lanemask_lt())] = key;
-          }
+          if (c) cand_s[base + __popc(m & lanemask_lt())] = key;
+          base += (uint32_t)__popc(m);
         }
+        if (tid == 0) S.ncand = total;
       }
     } else if (r == kRounds - 1 && tid == 0) {
       // keys equal to the threshold in lower-ranked CTAs precede ours in block order
@@ -411,10 +431,18 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       const int32_t i = tb + 4 * tid;
       const int m = max(0, min(4, cnt - i));
       uint32_t k[4];
+      if (m == 4 && i + 3 < cached) {  // one 16-byte load per thread
+        const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
+        k[0] = kv.x;
+        k[1] = kv.y;
+        k[2] = kv.z;
+        k[3] = kv.w;
+      } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int32_t ie = i + e;
-        k[e] = (e < m) ? ((ie < cached) ? keys_s[ie] : order_key(__ldg(srow + ie))) : 0u;
+        for (int e = 0; e < 4; ++e) {
+          const int32_t ie = i + e;
+          k[e] = (e < m) ? ((ie < cached) ? keys_s[ie] : order_key(__ldg(srow + ie))) : 0u;
+        }
       }
       uint32_t kept = 0;
       if (done) {

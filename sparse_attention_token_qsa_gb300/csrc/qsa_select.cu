@@ -51,14 +51,18 @@ struct SelectSmem {
   uint32_t hist3[16];
   uint32_t warp_tot[kSelWarps];
   uint32_t wcount[kSelWarps];
-  uint32_t msmall[256];  // rounds 1..3 merged over a cluster
+  uint32_t msmall[256];  // rounds 1..3 merged over a cluster (fallback path)
+  uint32_t roff[kSelMaxCluster + 1];  // rank 0: where each rank's candidates start
+  uint32_t rule_prefix;  // the kept set: (key >> rule_shift) > rule_prefix, or equal
+  uint32_t rule_shift;   //   to it at a block index <= rule_cut
+  int32_t rule_cut;
   uint32_t nonfinite;
   uint32_t nonfinite_all;
   uint32_t ncand;
   int32_t sel_bin;
   uint32_t sel_above;
   uint32_t eq_base;
-  // cand[kCandCap] and keys[] follow (dynamic)
+  // cand keys [kCandCap] u32, cand local indices [kCandCap] u16, keys[] follow (dynamic)
 };
 
 __device__ __forceinline__ uint32_t order_key(float s) {
@@ -82,6 +86,15 @@ __device__ __forceinline__ uint32_t ld_dsmem(const uint32_t *local, uint32_t ran
   uint32_t raddr, v;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(rank));
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(raddr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ld_dsmem_u16(const uint16_t *local, uint32_t rank) {
+  uint32_t laddr = (uint32_t)__cvta_generic_to_shared(local);
+  uint32_t raddr;
+  uint16_t v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(rank));
+  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(raddr) : "memory");
   return v;
 }
 
@@ -205,7 +218,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   SelectSmem &S = *reinterpret_cast<SelectSmem *>(smem_raw);
   uint32_t *cand_s =
       reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(SelectSmem) + 15) & ~size_t(15)));
-  uint32_t *keys_s = cand_s + kCandCap;
+  uint16_t *cand_li = reinterpret_cast<uint16_t *>(cand_s + kCandCap);
+  uint32_t *keys_s = reinterpret_cast<uint32_t *>(cand_li + kCandCap);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t row = blockIdx.x / C;
@@ -289,144 +303,253 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     if (nonfinite) atomicOr(&S.nonfinite, 1u);
   }
 
-  uint32_t prefix = 0;   // the threshold's top bits found so far
-  int shift = 32;        // prefix = threshold >> shift
   uint32_t need = (uint32_t)min(keep_max, n);  // keys still to keep at/below the prefix
-  bool done = false;     // every key matching the prefix is kept
-  bool bad = false;      // a non-finite score somewhere in the row
-  bool use_cand = false; // rounds 1..3 run on the compacted candidates
+  bool bad = false;        // a non-finite score somewhere in the row
+  bool scan_ties = false;  // fallback: ties ranked by a block scan in the mask pass
+  uint32_t prefix = 0;     // fallback state: the threshold's top bits so far ...
+  int shift = 32;          // ... prefix = threshold >> shift
 
-  for (int r = 0; r < kRounds; ++r) {
-    uint32_t *H = r == 0 ? S.hist0 : (r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3));
-    const int nb = round_bins(r);
-    const int sh = round_shift(r);
-    if (r > 0) {  // histogram this round's digit of the keys matching the prefix
-      const int32_t n_src = use_cand ? (int32_t)S.ncand : cnt;
-      for (int32_t ib = warp * 32; ib < n_src; ib += kSelThreads) {
-        const int32_t i = ib + lane;
-        const bool in = i < n_src;
-        uint32_t key = 0;
-        if (in) key = use_cand ? cand_s[i] : (i < cached ? keys_s[i] : order_key(__ldg(srow + i)));
-        const bool match = in && (key >> shift) == prefix;
-        hist_add(H, (key >> sh) & (uint32_t)(nb - 1), match);
-      }
+  // ---- round 0: merge the top-12-bit histograms over the cluster
+  if (C > 1) cluster_sync_all(); else __syncthreads();
+  if (tid == 0) {
+    uint32_t nf = 0;
+    if (C > 1) {
+      for (int q = 0; q < C; ++q) nf |= ld_dsmem(&S.nonfinite, (uint32_t)q);
+    } else {
+      nf = S.nonfinite;
     }
-    // make the local histogram visible, then merge over the cluster
-    if (C > 1) cluster_sync_all(); else __syncthreads();
-    const uint32_t *M = H;
-    if (r == 0) {
-      if (C > 1) {
-        if (tid == 0) {
-          uint32_t nf = 0;
-          for (int q = 0; q < C; ++q) nf |= ld_dsmem(&S.nonfinite, (uint32_t)q);
-          S.nonfinite_all = nf;
-        }
-      } else if (tid == 0) {
-        S.nonfinite_all = S.nonfinite;
+    S.nonfinite_all = nf;
+  }
+  __syncthreads();
+  bad = S.nonfinite_all != 0u;  // the same verdict in every CTA of the cluster
+  if (!bad && C > 1) {
+    // reduce-scatter: this CTA sums its slice of bins over the cluster, in place
+    const int slice = 4096 / C;
+    for (int b = (int)rank * slice + tid; b < ((int)rank + 1) * slice; b += kSelThreads) {
+      uint32_t v[kSelMaxCluster];
+#pragma unroll
+      for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&S.hist0[b], (uint32_t)q) : 0u;
+      uint32_t t = 0;
+#pragma unroll
+      for (int q = 0; q < kSelMaxCluster; ++q) t += v[q];
+      S.hist0[b] = t;
+    }
+    cluster_sync_all();
+    // gather the other slices' merged bins (their owners no longer change them)
+    uint32_t g[4096 / kSelThreads];
+#pragma unroll
+    for (int j = 0; j < 4096 / kSelThreads; ++j) {
+      const int b = tid + j * kSelThreads;
+      const int owner = b / slice;
+      g[j] = owner != (int)rank ? ld_dsmem(&S.hist0[b], (uint32_t)owner) : S.hist0[b];
+    }
+#pragma unroll
+    for (int j = 0; j < 4096 / kSelThreads; ++j) S.hist0[tid + j * kSelThreads] = g[j];
+    __syncthreads();
+  }
+
+  if (!bad) {
+    find_bin(S.hist0, 4096, need, S);
+    const uint32_t B0 = (uint32_t)S.sel_bin;
+    const uint32_t cnt0 = S.hist0[B0];
+    need -= S.sel_above;
+    prefix = B0;
+    shift = 20;
+    if (cnt0 == need) {  // the whole bin is kept
+      if (tid == 0) {
+        S.rule_prefix = B0;
+        S.rule_shift = 20;
+        S.rule_cut = INT32_MAX;
       }
       __syncthreads();
-      if (S.nonfinite_all != 0u) {  // the same verdict in every CTA of the cluster
-        bad = true;
-        break;
+    } else if (cnt0 <= (uint32_t)kCandCap && per <= 65536) {
+      // ---- candidate path.  Compact this CTA's keys of the bin in block
+      // order, with local indices, and without atomics: each warp counts its
+      // matches in its own contiguous range, a scan of the counts gives each
+      // warp its offset, then each warp writes with a ballot prefix.
+      const int32_t wlen = (cnt + kSelWarps - 1) / kSelWarps;
+      const int32_t w_lo = min(cnt, warp * wlen);
+      const int32_t w_hi = min(cnt, w_lo + wlen);
+      uint32_t wc = 0;
+      for (int32_t i0 = w_lo; i0 < w_hi; i0 += 32) {
+        const int32_t i = i0 + lane;
+        const bool in = i < w_hi;
+        uint32_t key = 0;
+        if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
+        wc += (uint32_t)__popc(__ballot_sync(0xffffffffu, in && (key >> 20) == B0));
       }
+      if (lane == 0) S.wcount[warp] = wc;
+      __syncthreads();
+      uint32_t base = 0, total = 0;
+      for (int w = 0; w < kSelWarps; ++w) {
+        const uint32_t c = S.wcount[w];
+        base += (w < warp) ? c : 0u;
+        total += c;
+      }
+      for (int32_t i0 = w_lo; i0 < w_hi; i0 += 32) {
+        const int32_t i = i0 + lane;
+        const bool in = i < w_hi;
+        uint32_t key = 0;
+        if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
+        const bool c = in && (key >> 20) == B0;
+        const uint32_t m = __ballot_sync(0xffffffffu, c);
+        if (c) {
+          const uint32_t at = base + __popc(m & lanemask_lt());
+          cand_s[at] = key;
+          cand_li[at] = (uint16_t)i;
+        }
+        base += (uint32_t)__popc(m);
+      }
+      if (tid == 0) S.ncand = total;
+      if (C > 1) cluster_sync_all(); else __syncthreads();
+      if (rank == 0) {
+        // rank 0 gathers every CTA's candidates after its own: the list stays
+        // in block order because slices are in rank order
+        if (tid == 0) {
+          uint32_t o = 0;
+          for (int q = 0; q < C; ++q) {
+            S.roff[q] = o;
+            o += (q == 0) ? S.ncand : ld_dsmem(&S.ncand, (uint32_t)q);
+          }
+          S.roff[C] = o;
+        }
+        __syncthreads();
+        for (int q = 1; q < C; ++q) {
+          const uint32_t o = S.roff[q], cq = S.roff[q + 1] - o;
+          for (uint32_t j = tid; j < cq; j += kSelThreads) {
+            cand_s[o + j] = ld_dsmem(&cand_s[j], (uint32_t)q);
+            cand_li[o + j] = ld_dsmem_u16(&cand_li[j], (uint32_t)q);
+          }
+        }
+        __syncthreads();
+        const int32_t nl = (int32_t)S.roff[C];
+        // rounds 1..3 on the candidates, all local
+        bool done = false;
+        for (int r = 1; r < kRounds && !done; ++r) {
+          uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
+          const int nb = round_bins(r), sh = round_shift(r);
+          for (int32_t j = tid; j < nl; j += kSelThreads) {
+            const uint32_t key = cand_s[j];
+            if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+          }
+          __syncthreads();
+          find_bin(H, nb, need, S);
+          const uint32_t B = (uint32_t)S.sel_bin;
+          const uint32_t cB = H[B];
+          need -= S.sel_above;
+          prefix = (prefix << (shift - sh)) | B;
+          shift = sh;
+          done = cB == need;
+          __syncthreads();
+        }
+        if (done) {
+          if (tid == 0) {
+            S.rule_prefix = prefix;
+            S.rule_shift = (uint32_t)shift;
+            S.rule_cut = INT32_MAX;
+          }
+        } else {
+          // ties at the full key: keep the first `need` equal keys in block
+          // order; the list is in block order, so find the need-th equal entry
+          constexpr int kPerThread = kCandCap / kSelThreads;
+          const int32_t j0 = tid * kPerThread;
+          uint32_t eq = 0;
+#pragma unroll
+          for (int e = 0; e < kPerThread; ++e)
+            eq += (j0 + e < nl && cand_s[j0 + e] == prefix) ? 1u : 0u;
+          uint32_t tot;
+          const uint32_t before = block_excl_scan(eq, S.warp_tot, tot);
+          if (before < need && need <= before + eq) {
+            uint32_t acc = before;
+            for (int e = 0; e < kPerThread; ++e) {
+              const int32_t j = j0 + e;
+              if (j < nl && cand_s[j] == prefix && ++acc == need) {
+                int q = 0;
+                while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
+                S.rule_prefix = prefix;
+                S.rule_shift = 0;
+                S.rule_cut = q * per + (int32_t)cand_li[j];
+                break;
+              }
+            }
+          }
+        }
+        __syncthreads();
+      }
+      // every CTA takes rank 0's rule
+      if (C > 1) cluster_sync_all();
+      if (rank != 0 && tid == 0) {
+        S.rule_prefix = ld_dsmem(&S.rule_prefix, 0u);
+        S.rule_shift = ld_dsmem(&S.rule_shift, 0u);
+        S.rule_cut = (int32_t)ld_dsmem(reinterpret_cast<const uint32_t *>(&S.rule_cut), 0u);
+      }
+      __syncthreads();
+    } else {
+      scan_ties = true;  // ---- fallback: rounds over every key (part B)
+    }
+  }
+
+  if (scan_ties) {
+    // ---- fallback (round 0's bin holds more than kCandCap keys): rounds 1..3
+    // over every key, each histogram merged over the cluster
+    bool done = false;
+    for (int r = 1; r < kRounds && !done; ++r) {
+      uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
+      const int nb = round_bins(r), sh = round_shift(r);
+      for (int32_t ib = warp * 32; ib < cnt; ib += kSelThreads) {
+        const int32_t i = ib + lane;
+        const bool in = i < cnt;
+        uint32_t key = 0;
+        if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
+        hist_add(H, (key >> sh) & (uint32_t)(nb - 1), in && (key >> shift) == prefix);
+      }
+      if (C > 1) cluster_sync_all(); else __syncthreads();
+      const uint32_t *M = H;
       if (C > 1) {
-        // reduce-scatter: this CTA sums its slice of bins over the cluster, in place
-        const int slice = nb / C;
-        for (int b = (int)rank * slice + tid; b < ((int)rank + 1) * slice; b += kSelThreads) {
+        for (int b = tid; b < nb; b += kSelThreads) {
           uint32_t v[kSelMaxCluster];
 #pragma unroll
           for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&H[b], (uint32_t)q) : 0u;
           uint32_t t = 0;
 #pragma unroll
           for (int q = 0; q < kSelMaxCluster; ++q) t += v[q];
-          H[b] = t;
+          S.msmall[b] = t;
         }
-        cluster_sync_all();
-        // gather the other slices' merged bins (their owners no longer change them)
-        uint32_t g[4096 / kSelThreads];
-#pragma unroll
-        for (int j = 0; j < 4096 / kSelThreads; ++j) {
-          const int b = tid + j * kSelThreads;
-          const int owner = b / slice;
-          g[j] = owner != (int)rank ? ld_dsmem(&H[b], (uint32_t)owner) : H[b];
-        }
-#pragma unroll
-        for (int j = 0; j < 4096 / kSelThreads; ++j) H[tid + j * kSelThreads] = g[j];
         __syncthreads();
+        M = S.msmall;
       }
-    } else if (C > 1) {
-      for (int b = tid; b < nb; b += kSelThreads) {
-        uint32_t v[kSelMaxCluster];
-#pragma unroll
-        for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&H[b], (uint32_t)q) : 0u;
-        uint32_t t = 0;
-#pragma unroll
-        for (int q = 0; q < kSelMaxCluster; ++q) t += v[q];
-        S.msmall[b] = t;
+      find_bin(M, nb, need, S);
+      const uint32_t B = (uint32_t)S.sel_bin;
+      const uint32_t cB = M[B];
+      need -= S.sel_above;
+      prefix = (prefix << (shift - sh)) | B;
+      shift = sh;
+      done = cB == need;
+      if (!done && r == kRounds - 1 && tid == 0) {
+        // keys equal to the threshold in lower-ranked CTAs precede ours in block order
+        uint32_t e = 0;
+        for (uint32_t q = 0; q < rank; ++q) e += ld_dsmem(&S.hist3[B], q);
+        S.eq_base = e;
       }
       __syncthreads();
-      M = S.msmall;
     }
-    find_bin(M, nb, need, S);
-    const uint32_t B = (uint32_t)S.sel_bin;
-    const uint32_t cntB = M[B];
-    need -= S.sel_above;
-    prefix = (r == 0) ? B : ((prefix << (shift - sh)) | B);
-    shift = sh;
-    if (cntB == need) {
-      done = true;  // the whole bin is kept: no tie to rank
-    } else if (r == 0) {
-      use_cand = cntB <= (uint32_t)kCandCap;  // the merged count bounds every CTA's share
-      if (use_cand) {
-        // compact this CTA's keys of the bin, in block order and without
-        // atomics: each warp counts the matches in its own contiguous range,
-        // a scan of the warp counts gives each warp its offset, then each warp
-        // writes its matches with a ballot prefix
-        const int32_t wlen = (cnt + kSelWarps - 1) / kSelWarps;
-        const int32_t w_lo = min(cnt, warp * wlen);
-        const int32_t w_hi = min(cnt, w_lo + wlen);
-        uint32_t wc = 0;
-        for (int32_t i0 = w_lo; i0 < w_hi; i0 += 32) {
-          const int32_t i = i0 + lane;
-          const bool in = i < w_hi;
-          uint32_t key = 0;
-          if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
-          wc += (uint32_t)__popc(__ballot_sync(0xffffffffu, in && (key >> 20) == prefix));
-        }
-        if (lane == 0) S.wcount[warp] = wc;
-        __syncthreads();
-        uint32_t base = 0, total = 0;
-        for (int w = 0; w < kSelWarps; ++w) {
-          const uint32_t c = S.wcount[w];
-          base += (w < warp) ? c : 0u;
-          total += c;
-        }
-        for (int32_t i0 = w_lo; i0 < w_hi; i0 += 32) {
-          const int32_t i = i0 + lane;
-          const bool in = i < w_hi;
-          uint32_t key = 0;
-          if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
-          const bool c = in && (key >> 20) == prefix;
-          const uint32_t m = __ballot_sync(0xffffffffu, c);
-          if (c) cand_s[base + __popc(m & lanemask_lt())] = key;
-          base += (uint32_t)__popc(m);
-        }
-        if (tid == 0) S.ncand = total;
+    if (done) {
+      scan_ties = false;
+      if (tid == 0) {
+        S.rule_prefix = prefix;
+        S.rule_shift = (uint32_t)shift;
+        S.rule_cut = INT32_MAX;
       }
-    } else if (r == kRounds - 1 && tid == 0) {
-      // keys equal to the threshold in lower-ranked CTAs precede ours in block order
-      uint32_t e = 0;
-      for (uint32_t q = 0; q < rank; ++q) e += ld_dsmem(&S.hist3[B], q);
-      S.eq_base = e;
+      __syncthreads();
     }
-    __syncthreads();
-    if (done) break;
   }
 
   if (!bad) {
     const uintptr_t rb = reinterpret_cast<uintptr_t>(mrow);
     const bool al16 = (rb & 15u) == 0, al4 = (rb & 3u) == 0;
-    uint32_t running = done ? 0u : S.eq_base;
+    const uint32_t rp = S.rule_prefix, rs = S.rule_shift;
+    const int32_t rc = S.rule_cut;
+    uint32_t running = S.eq_base;
     for (int32_t tb = 0; tb < cnt; tb += 4 * kSelThreads) {
       const int32_t i = tb + 4 * tid;
       const int m = max(0, min(4, cnt - i));
@@ -445,11 +568,13 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         }
       }
       uint32_t kept = 0;
-      if (done) {
+      if (!scan_ties) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (e < m && (k[e] >> shift) >= prefix) kept |= 1u << e;
-      } else {  // the threshold key itself: ties filled in block order
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t kk = k[e] >> rs;
+          if (e < m && (kk > rp || (kk == rp && b0 + i + e <= rc))) kept |= 1u << e;
+        }
+      } else {  // the threshold key itself: ties filled in block order by a scan
         uint32_t eqc = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e) eqc += (e < m && k[e] == prefix) ? 1u : 0u;
@@ -485,7 +610,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 static int g_max_cluster = -1;
 
 static size_t select_smem_bytes(int32_t cap) {
-  return ((sizeof(SelectSmem) + 15) & ~size_t(15)) + 4 * (size_t)kCandCap +
+  return ((sizeof(SelectSmem) + 15) & ~size_t(15)) + 6 * (size_t)kCandCap +
          4 * (size_t)(cap > 0 ? cap : 1);
 }
 

@@ -405,21 +405,27 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       if (rank == 0) {
         // rank 0 gathers every CTA's candidates after its own: the list stays
         // in block order because slices are in rank order
-        if (tid == 0) {
-          uint32_t o = 0;
-          for (int q = 0; q < C; ++q) {
-            S.roff[q] = o;
-            o += (q == 0) ? S.ncand : ld_dsmem(&S.ncand, (uint32_t)q);
+        if (warp == 0) {  // every rank's count at once, then a warp prefix sum
+          uint32_t c = 0;
+          if (lane < C) c = lane == 0 ? S.ncand : ld_dsmem(&S.ncand, (uint32_t)lane);
+          uint32_t incl = c;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
           }
-          S.roff[C] = o;
+          if (lane < C) S.roff[lane] = incl - c;
+          if (lane == C - 1) S.roff[C] = incl;
         }
         __syncthreads();
-        for (int q = 1; q < C; ++q) {
-          const uint32_t o = S.roff[q], cq = S.roff[q + 1] - o;
-          for (uint32_t j = tid; j < cq; j += kSelThreads) {
-            cand_s[o + j] = ld_dsmem(&cand_s[j], (uint32_t)q);
-            cand_li[o + j] = ld_dsmem_u16(&cand_li[j], (uint32_t)q);
-          }
+        // one thread per remote entry across all ranks, loads independent
+        const uint32_t own = S.roff[1], all = S.roff[C];
+        for (uint32_t j = own + tid; j < all; j += kSelThreads) {
+          int q = 1;
+          while (q + 1 < C && S.roff[q + 1] <= j) ++q;
+          const uint32_t jj = j - S.roff[q];
+          cand_s[j] = ld_dsmem(&cand_s[jj], (uint32_t)q);
+          cand_li[j] = ld_dsmem_u16(&cand_li[jj], (uint32_t)q);
         }
         __syncthreads();
         const int32_t nl = (int32_t)S.roff[C];

@@ -29,7 +29,7 @@
 
 namespace qsa {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 768;  // 24 warps; two CTAs share an SM
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelMaxCluster = 16;
 constexpr int kSelCapMax = 16384;  // keys cached per CTA (64 KiB)
@@ -210,7 +210,7 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-__global__ void __launch_bounds__(kSelThreads)
+__global__ void __launch_bounds__(kSelThreads, 2)
 select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_t *__restrict__ pos,
               int32_t tokens, int32_t keep_max, uint8_t *__restrict__ mask, int32_t *status,
               int32_t C, int32_t cap) {
@@ -336,15 +336,20 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     }
     cluster_sync_all();
     // gather the other slices' merged bins (their owners no longer change them)
-    uint32_t g[4096 / kSelThreads];
+    constexpr int kGather = (4096 + kSelThreads - 1) / kSelThreads;
+    uint32_t g[kGather];
 #pragma unroll
-    for (int j = 0; j < 4096 / kSelThreads; ++j) {
+    for (int j = 0; j < kGather; ++j) {
       const int b = tid + j * kSelThreads;
-      const int owner = b / slice;
-      g[j] = owner != (int)rank ? ld_dsmem(&S.hist0[b], (uint32_t)owner) : S.hist0[b];
+      g[j] = 0u;
+      if (b < 4096) {
+        const int owner = b / slice;
+        g[j] = owner != (int)rank ? ld_dsmem(&S.hist0[b], (uint32_t)owner) : S.hist0[b];
+      }
     }
 #pragma unroll
-    for (int j = 0; j < 4096 / kSelThreads; ++j) S.hist0[tid + j * kSelThreads] = g[j];
+    for (int j = 0; j < kGather; ++j)
+      if (tid + j * kSelThreads < 4096) S.hist0[tid + j * kSelThreads] = g[j];
     __syncthreads();
   }
 
@@ -457,7 +462,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         } else {
           // ties at the full key: keep the first `need` equal keys in block
           // order; the list is in block order, so find the need-th equal entry
-          constexpr int kPerThread = kCandCap / kSelThreads;
+          constexpr int kPerThread = (kCandCap + kSelThreads - 1) / kSelThreads;
           const int32_t j0 = tid * kPerThread;
           uint32_t eq = 0;
 #pragma unroll
@@ -651,14 +656,16 @@ static int max_cluster_size() {
   return best;
 }
 
-// Cluster size for a launch: split rows whose slice would overflow the key
-// cache, then keep splitting while the grid cannot fill the GPU.
+// Cluster size for a launch: split a row over a cluster only when its blocks
+// overflow one CTA's key cache.  (Splitting further to fill the GPU costs more
+// in cluster barriers and remote reads than it gains: a 16384-block row is
+// faster on one CTA than on sixteen.)
 int select_cluster_size(int64_t n_rows, int64_t tokens) {
+  (void)n_rows;
   const int64_t n_max = tokens / kRatio;
   const int cmax = max_cluster_size();
   int C = 1;
   while (C < cmax && (n_max + C - 1) / C > kSelCapMax) C <<= 1;
-  while (C < cmax && n_rows * C < 2 * 152 && n_max / (2 * C) >= 1024) C <<= 1;
   return C;
 }
 

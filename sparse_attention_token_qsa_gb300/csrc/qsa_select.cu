@@ -29,7 +29,7 @@
 
 namespace qsa {
 
-constexpr int kSelThreads = 768;  // 24 warps; two CTAs share an SM
+constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelMaxCluster = 16;
 constexpr int kSelCapMax = 16384;  // keys cached per CTA (64 KiB)
@@ -261,7 +261,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   {
     constexpr int kLoadsInFlight = 4;  // float4 loads issued per thread before use
     const int32_t nq = (cnt + 3) >> 2;
-    uint32_t nonfinite = 0;
+    uint32_t nonfinite = 0, zeros = 0;
     for (int32_t qb = warp * 32; qb < nq; qb += kSelThreads * kLoadsInFlight) {
       float4 v[kLoadsInFlight];
 #pragma unroll
@@ -273,33 +273,34 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 #pragma unroll
       for (int u = 0; u < kLoadsInFlight; ++u) {
         const int32_t qd = qb + u * kSelThreads + lane;
-        const bool qv = qd < nq;
-        const float sv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        uint32_t kq[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          kq[e] = order_key(sv[e]);
-          if (qv && 4 * qd + e < cnt && !isfinite(sv[e])) nonfinite = 1;
-        }
-        if (qv && 4 * qd + 3 < cached) {  // one 16-byte store per quad
+        if (qd >= nq) continue;  // per lane: nothing below needs the whole warp
+        const uint32_t kq[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z),
+                                order_key(v[u].w)};
+        if (4 * qd + 3 < cached) {  // one 16-byte store per quad
           *reinterpret_cast<uint4 *>(keys_s + 4 * qd) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-        } else if (qv) {
+        } else {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int32_t i = 4 * qd + e;
-          const bool valid = qv && i < cnt;
+          if (4 * qd + e >= cnt) continue;
           const uint32_t key = kq[e];
-          const bool zero = valid && key == kZeroKey;
-          const uint32_t zb = __ballot_sync(0xffffffffu, zero);
-          if (lane == 0 && zb) atomicAdd(&S.hist0[kZeroKey >> 20], (uint32_t)__popc(zb));
-          hist_add(S.hist0, key >> 20, valid && !zero);
+          const float sf = e == 0 ? v[u].x : (e == 1 ? v[u].y : (e == 2 ? v[u].z : v[u].w));
+          nonfinite |= isfinite(sf) ? 0u : 1u;
+          if (key == kZeroKey) {
+            ++zeros;  // exact zeros, the one heavy bin of relu scores
+          } else {
+            atomicAdd(&S.hist0[key >> 20], 1u);
+          }
         }
       }
     }
+    // one add per warp for the zeros
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) zeros += __shfl_xor_sync(0xffffffffu, zeros, off);
+    if (lane == 0 && zeros) atomicAdd(&S.hist0[kZeroKey >> 20], zeros);
     if (nonfinite) atomicOr(&S.nonfinite, 1u);
   }
 

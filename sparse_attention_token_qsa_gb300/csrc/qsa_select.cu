@@ -203,6 +203,42 @@ __device__ __forceinline__ void find_bin(const uint32_t *M, int nb, uint32_t nee
   __syncthreads();
 }
 
+// One warp's version of find_bin for the small rounds (nb <= 256): the bin
+// of H holding the need-th largest key and the count above it, returned to
+// every lane.  Warp-synchronous: no block barrier.
+__device__ __forceinline__ void warp_find_bin(const uint32_t *H, int nb, uint32_t need, int lane,
+                                              uint32_t &bin, uint32_t &above) {
+  const int per = (nb + 31) / 32;
+  const int hi = nb - 1 - lane * per;  // this lane's bins, from the top
+  uint32_t sum = 0;
+  for (int j = 0; j < per; ++j)
+    if (hi - j >= 0) sum += H[hi - j];
+  uint32_t incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  const uint32_t before = incl - sum;
+  const bool mine = before < need && need <= incl;
+  uint32_t mb = 0, ma = 0;
+  if (mine) {
+    uint32_t acc = before;
+    for (int j = 0; j < per; ++j) {
+      const uint32_t c = H[hi - j];
+      if (acc + c >= need) {
+        mb = (uint32_t)(hi - j);
+        ma = acc;
+        break;
+      }
+      acc += c;
+    }
+  }
+  const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+  bin = __shfl_sync(0xffffffffu, mb, src);
+  above = __shfl_sync(0xffffffffu, ma, src);
+}
+
 // Lanes below this one in the warp.
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -373,17 +409,37 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       // order, with local indices, and without atomics: each warp counts its
       // matches in its own contiguous range, a scan of the counts gives each
       // warp its offset, then each warp writes with a ballot prefix.
-      const int32_t wlen = (cnt + kSelWarps - 1) / kSelWarps;
+      // each warp owns a contiguous range of whole 128-key chunks; a lane
+      // takes 4 consecutive keys of a chunk (one 16-byte shared load)
+      const int32_t wlen = (((cnt + kSelWarps - 1) / kSelWarps) + 127) & ~127;
       const int32_t w_lo = min(cnt, warp * wlen);
       const int32_t w_hi = min(cnt, w_lo + wlen);
+      auto quad_matches = [&](int32_t i, uint32_t (&k)[4]) -> uint32_t {
+        if (i + 3 < cached && i + 3 < w_hi) {
+          const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
+          k[0] = kv.x;
+          k[1] = kv.y;
+          k[2] = kv.z;
+          k[3] = kv.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            k[e] = (i + e < w_hi) ? (i + e < cached ? keys_s[i + e] : order_key(__ldg(srow + i + e)))
+                                  : ~0u;  // never in a bin: (~0u >> 20) != B0 for B0 < 4095
+        }
+        uint32_t bits = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i + e < w_hi && (k[e] >> 20) == B0) bits |= 1u << e;
+        return bits;
+      };
       uint32_t wc = 0;
-      for (int32_t i0 = w_lo; i0 < w_hi; i0 += 32) {
-        const int32_t i = i0 + lane;
-        const bool in = i < w_hi;
-        uint32_t key = 0;
-        if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
-        wc += (uint32_t)__popc(__ballot_sync(0xffffffffu, in && (key >> 20) == B0));
+      for (int32_t i0 = w_lo; i0 < w_hi; i0 += 128) {
+        uint32_t k[4];
+        wc += (uint32_t)__popc(quad_matches(i0 + 4 * lane, k));
       }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) wc += __shfl_xor_sync(0xffffffffu, wc, off);
       if (lane == 0) S.wcount[warp] = wc;
       __syncthreads();
       uint32_t base = 0, total = 0;
@@ -392,19 +448,27 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         base += (w < warp) ? c : 0u;
         total += c;
       }
-      for (int32_t i0 = w_lo; i0 < w_hi; i0 += 32) {
-        const int32_t i = i0 + lane;
-        const bool in = i < w_hi;
-        uint32_t key = 0;
-        if (in) key = i < cached ? keys_s[i] : order_key(__ldg(srow + i));
-        const bool c = in && (key >> 20) == B0;
-        const uint32_t m = __ballot_sync(0xffffffffu, c);
-        if (c) {
-          const uint32_t at = base + __popc(m & lanemask_lt());
-          cand_s[at] = key;
-          cand_li[at] = (uint16_t)i;
+      for (int32_t i0 = w_lo; i0 < w_hi; i0 += 128) {
+        const int32_t i = i0 + 4 * lane;
+        uint32_t k[4];
+        const uint32_t bits = quad_matches(i, k);
+        const uint32_t c = (uint32_t)__popc(bits);
+        uint32_t incl = c;  // warp inclusive scan of the lanes' match counts
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
         }
-        base += (uint32_t)__popc(m);
+        uint32_t at = base + incl - c;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (bits & (1u << e)) {
+            cand_s[at] = k[e];
+            cand_li[at] = (uint16_t)(i + e);
+            ++at;
+          }
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (tid == 0) S.ncand = total;
       if (C > 1) cluster_sync_all(); else __syncthreads();
@@ -435,53 +499,56 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         }
         __syncthreads();
         const int32_t nl = (int32_t)S.roff[C];
-        // rounds 1..3 on the candidates, all local
-        bool done = false;
-        for (int r = 1; r < kRounds && !done; ++r) {
-          uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
-          const int nb = round_bins(r), sh = round_shift(r);
-          for (int32_t j = tid; j < nl; j += kSelThreads) {
-            const uint32_t key = cand_s[j];
-            if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+        // rounds 1..3 on the candidates and the tie cutoff, by one warp
+        if (warp == 0) {
+          bool done = false;
+          for (int r = 1; r < kRounds && !done; ++r) {
+            uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
+            const int nb = round_bins(r), sh = round_shift(r);
+            for (int32_t j = lane; j < nl; j += 32) {
+              const uint32_t key = cand_s[j];
+              if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+            }
+            __syncwarp();
+            uint32_t B, above;
+            warp_find_bin(H, nb, need, lane, B, above);
+            const uint32_t cB = H[B];
+            need -= above;
+            prefix = (prefix << (shift - sh)) | B;
+            shift = sh;
+            done = cB == need;
           }
-          __syncthreads();
-          find_bin(H, nb, need, S);
-          const uint32_t B = (uint32_t)S.sel_bin;
-          const uint32_t cB = H[B];
-          need -= S.sel_above;
-          prefix = (prefix << (shift - sh)) | B;
-          shift = sh;
-          done = cB == need;
-          __syncthreads();
-        }
-        if (done) {
-          if (tid == 0) {
-            S.rule_prefix = prefix;
-            S.rule_shift = (uint32_t)shift;
-            S.rule_cut = INT32_MAX;
-          }
-        } else {
-          // ties at the full key: keep the first `need` equal keys in block
-          // order; the list is in block order, so find the need-th equal entry
-          constexpr int kPerThread = (kCandCap + kSelThreads - 1) / kSelThreads;
-          const int32_t j0 = tid * kPerThread;
-          uint32_t eq = 0;
+          if (done) {
+            if (lane == 0) {
+              S.rule_prefix = prefix;
+              S.rule_shift = (uint32_t)shift;
+              S.rule_cut = INT32_MAX;
+            }
+          } else {
+            // ties at the full key: keep the first `need` equal keys in block
+            // order; the list is in block order, so find the need-th equal entry
+            const int32_t chunk = (nl + 31) / 32;
+            const int32_t j0 = lane * chunk, j1 = min(nl, j0 + chunk);
+            uint32_t eq = 0;
+            for (int32_t j = j0; j < j1; ++j) eq += cand_s[j] == prefix ? 1u : 0u;
+            uint32_t incl = eq;
 #pragma unroll
-          for (int e = 0; e < kPerThread; ++e)
-            eq += (j0 + e < nl && cand_s[j0 + e] == prefix) ? 1u : 0u;
-          uint32_t tot;
-          const uint32_t before = block_excl_scan(eq, S.warp_tot, tot);
-          if (before < need && need <= before + eq) {
-            uint32_t acc = before;
-            for (int e = 0; e < kPerThread; ++e) {
-              const int32_t j = j0 + e;
-              if (j < nl && cand_s[j] == prefix && ++acc == need) {
-                int q = 0;
-                while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
-                S.rule_prefix = prefix;
-                S.rule_shift = 0;
-                S.rule_cut = q * per + (int32_t)cand_li[j];
-                break;
+            for (int off = 1; off < 32; off <<= 1) {
+              const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+              if (lane >= off) incl += o;
+            }
+            const uint32_t before = incl - eq;
+            if (before < need && need <= incl) {
+              uint32_t acc = before;
+              for (int32_t j = j0; j < j1; ++j) {
+                if (cand_s[j] == prefix && ++acc == need) {
+                  int q = 0;
+                  while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
+                  S.rule_prefix = prefix;
+                  S.rule_shift = 0;
+                  S.rule_cut = q * per + (int32_t)cand_li[j];
+                  break;
+                }
               }
             }
           }

@@ -343,6 +343,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   uint32_t need = (uint32_t)min(keep_max, n);  // keys still to keep at/below the prefix
   bool bad = false;        // a non-finite score somewhere in the row
   bool scan_ties = false;  // fallback: ties ranked by a block scan in the mask pass
+  bool cand_path = false;  // mask written during compaction; candidates patched after
+  uint32_t own_n = 0;      // this CTA's own candidates (at the start of its list)
   uint32_t prefix = 0;     // fallback state: the threshold's top bits so far ...
   int shift = 32;          // ... prefix = threshold >> shift
 
@@ -448,10 +450,21 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         base += (w < warp) ? c : 0u;
         total += c;
       }
+      const uintptr_t rbm = reinterpret_cast<uintptr_t>(mrow);
+      const bool m16 = (rbm & 15u) == 0, m4 = (rbm & 3u) == 0;
       for (int32_t i0 = w_lo; i0 < w_hi; i0 += 128) {
         const int32_t i = i0 + 4 * lane;
         uint32_t k[4];
         const uint32_t bits = quad_matches(i, k);
+        // keys above the bin are kept, below it dropped: their mask bytes are
+        // final now; the bin's own keys are written as dropped and patched
+        // once the threshold inside the bin is known
+        const int mq = max(0, min(4, w_hi - i));
+        uint32_t kept = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e < mq && (k[e] >> 20) > B0) kept |= 1u << e;
+        if (mq > 0) store_blocks(mrow, (int64_t)b0 + i, mq, kept, m16, m4);
         const uint32_t c = (uint32_t)__popc(bits);
         uint32_t incl = c;  // warp inclusive scan of the lanes' match counts
 #pragma unroll
@@ -471,6 +484,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         base += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (tid == 0) S.ncand = total;
+      own_n = total;
+      cand_path = true;
       if (C > 1) cluster_sync_all(); else __syncthreads();
       if (rank == 0) {
         // rank 0 gathers every CTA's candidates after its own: the list stays
@@ -499,56 +514,62 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         }
         __syncthreads();
         const int32_t nl = (int32_t)S.roff[C];
-        // rounds 1..3 on the candidates and the tie cutoff, by one warp
-        if (warp == 0) {
-          bool done = false;
-          for (int r = 1; r < kRounds && !done; ++r) {
-            uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
-            const int nb = round_bins(r), sh = round_shift(r);
-            for (int32_t j = lane; j < nl; j += 32) {
-              const uint32_t key = cand_s[j];
-              if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
-            }
-            __syncwarp();
+        // rounds 1..3 on the candidates: every thread histograms, one warp
+        // finds the bin (two barriers a round); then the tie cutoff
+        bool done = false;
+        for (int r = 1; r < kRounds && !done; ++r) {
+          uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
+          const int nb = round_bins(r), sh = round_shift(r);
+          for (int32_t j = tid; j < nl; j += kSelThreads) {
+            const uint32_t key = cand_s[j];
+            if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+          }
+          __syncthreads();
+          if (warp == 0) {
             uint32_t B, above;
             warp_find_bin(H, nb, need, lane, B, above);
-            const uint32_t cB = H[B];
-            need -= above;
-            prefix = (prefix << (shift - sh)) | B;
-            shift = sh;
-            done = cB == need;
-          }
-          if (done) {
             if (lane == 0) {
-              S.rule_prefix = prefix;
-              S.rule_shift = (uint32_t)shift;
-              S.rule_cut = INT32_MAX;
+              S.sel_bin = (int32_t)B;
+              S.sel_above = above;
             }
-          } else {
-            // ties at the full key: keep the first `need` equal keys in block
-            // order; the list is in block order, so find the need-th equal entry
-            const int32_t chunk = (nl + 31) / 32;
-            const int32_t j0 = lane * chunk, j1 = min(nl, j0 + chunk);
-            uint32_t eq = 0;
-            for (int32_t j = j0; j < j1; ++j) eq += cand_s[j] == prefix ? 1u : 0u;
-            uint32_t incl = eq;
+          }
+          __syncthreads();
+          const uint32_t B = (uint32_t)S.sel_bin;
+          const uint32_t cB = H[B];
+          need -= S.sel_above;
+          prefix = (prefix << (shift - sh)) | B;
+          shift = sh;
+          done = cB == need;
+          __syncthreads();  // sel_bin is rewritten next round
+        }
+        if (done) {
+          if (tid == 0) {
+            S.rule_prefix = prefix;
+            S.rule_shift = (uint32_t)shift;
+            S.rule_cut = INT32_MAX;
+          }
+        } else {
+          // ties at the full key: keep the first `need` equal keys in block
+          // order; the list is in block order, so find the need-th equal entry
+          constexpr int kPerThread = (kCandCap + kSelThreads - 1) / kSelThreads;
+          const int32_t j0 = tid * kPerThread;
+          uint32_t eq = 0;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-              const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-              if (lane >= off) incl += o;
-            }
-            const uint32_t before = incl - eq;
-            if (before < need && need <= incl) {
-              uint32_t acc = before;
-              for (int32_t j = j0; j < j1; ++j) {
-                if (cand_s[j] == prefix && ++acc == need) {
-                  int q = 0;
-                  while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
-                  S.rule_prefix = prefix;
-                  S.rule_shift = 0;
-                  S.rule_cut = q * per + (int32_t)cand_li[j];
-                  break;
-                }
+          for (int e = 0; e < kPerThread; ++e)
+            eq += (j0 + e < nl && cand_s[j0 + e] == prefix) ? 1u : 0u;
+          uint32_t tot;
+          const uint32_t before = block_excl_scan(eq, S.warp_tot, tot);
+          if (before < need && need <= before + eq) {
+            uint32_t acc = before;
+            for (int e = 0; e < kPerThread; ++e) {
+              const int32_t j = j0 + e;
+              if (j < nl && cand_s[j] == prefix && ++acc == need) {
+                int q = 0;
+                while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
+                S.rule_prefix = prefix;
+                S.rule_shift = 0;
+                S.rule_cut = q * per + (int32_t)cand_li[j];
+                break;
               }
             }
           }
@@ -629,7 +650,14 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     const uint32_t rp = S.rule_prefix, rs = S.rule_shift;
     const int32_t rc = S.rule_cut;
     uint32_t running = S.eq_base;
-    for (int32_t tb = 0; tb < cnt; tb += 4 * kSelThreads) {
+    if (cand_path) {  // the mask is written but for this CTA's candidates
+      for (uint32_t j = tid; j < own_n; j += kSelThreads) {
+        const uint32_t kk = cand_s[j] >> rs;
+        const int32_t li = (int32_t)cand_li[j];
+        if (kk > rp || (kk == rp && b0 + li <= rc)) store_blocks(mrow, (int64_t)b0 + li, 1, 1u, false, al4);
+      }
+    }
+    for (int32_t tb = 0; tb < (cand_path ? 0 : cnt); tb += 4 * kSelThreads) {
       const int32_t i = tb + 4 * tid;
       const int m = max(0, min(4, cnt - i));
       uint32_t k[4];

@@ -64,25 +64,11 @@ score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
   if (c0 >= n) return;
   const int c1 = min(n, c0 + blocks_per_cta);
 
-  prep_query_heads(a, row, p, q_s);
-  __syncthreads();
-
   const int gi = threadIdx.x >> 3;
   const int g = threadIdx.x & 7;
-  float qr[kHeads][2][8];
-#pragma unroll
-  for (int h = 0; h < kHeads; ++h)
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qr[h][j][e] = q_s[h][8 * (8 * j + g) + e];
-
   const uint16_t *kb = a.block_keys + (a.key_base ? a.key_base[row] : 0) * kHeadDim;
-  float *srow = a.scores + (int64_t)row * a.score_cols;
-  const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
-
-  for (int base = c0; base < c1; base += kSimtBlocksPerIter) {
-    uint4 kv[kSimtUnroll][2];
+  uint4 kv[kSimtUnroll][2];
+  auto load_keys = [&](int base) {
 #pragma unroll
     for (int u = 0; u < kSimtUnroll; ++u) {
       const int b = base + u * kSimtGroups + gi;
@@ -91,6 +77,25 @@ score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
       kv[u][0] = ldg_nc_v4(kp);
       kv[u][1] = ldg_nc_v4(kp + 64);
     }
+  };
+  // the first keys are in flight while the query heads are prepared
+  load_keys(c0);
+  prep_query_heads(a, row, p, q_s);
+  __syncthreads();
+
+  float qr[kHeads][2][8];
+#pragma unroll
+  for (int h = 0; h < kHeads; ++h)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qr[h][j][e] = q_s[h][8 * (8 * j + g) + e];
+
+  float *srow = a.scores + (int64_t)row * a.score_cols;
+  const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
+
+  for (int base = c0; base < c1; base += kSimtBlocksPerIter) {
+    if (base != c0) load_keys(base);
 #pragma unroll
     for (int u = 0; u < kSimtUnroll; ++u) {
       float acc[kHeads] = {0.f, 0.f, 0.f, 0.f};

@@ -12,18 +12,23 @@
 // status word, the row left untouched; no trap).
 //
 // GB300 design:
-//  * a row is split over a cluster of C CTAs (C = 1..16): each CTA owns a
-//    contiguous, 4-aligned slice of the row's blocks and keeps its keys in
-//    shared memory, so HBM sees each score once;
+//  * a row is split over a cluster of C CTAs (C = 1..16) only when its blocks
+//    overflow one CTA's key cache: each CTA owns a contiguous, 4-aligned slice
+//    of the row's blocks and keeps its keys in shared memory, so HBM sees
+//    each score once;
 //  * the first round histograms the top 12 bits of every key as it is loaded
-//    (exact zeros counted by ballot, a warp-uniform bin added once); the keys
-//    of the selected bin are compacted and rounds of 8, 8 and 4 bits run on
-//    them only; each round's histograms are merged over the cluster through
-//    distributed shared memory and every CTA derives the same digit;
-//  * ties at the final key are ranked in index order by the count of equal
-//    keys in lower-ranked CTAs (read from their last histogram) plus an
-//    in-CTA block scan;
-//  * the mask row is written with 16-byte stores where the row is aligned.
+//    (exact zeros, the heavy bin of relu scores, counted in registers and
+//    added once per warp); the histograms merge over the cluster through
+//    distributed shared memory; a non-finite score shows up as a count in one
+//    of the 16 outer bins, so no per-key check is needed;
+//  * one pass over the cached keys then writes the final mask bytes of every
+//    key outside the selected bin and compacts the bin's keys (with their
+//    block indices) into a candidate list, which rank 0 gathers; rounds of
+//    8, 8 and 4 bits run on the candidates only, and exact ties at the final
+//    key are cut by radix rounds on the block index (lowest indices kept);
+//  * every CTA then patches the mask bytes of its own candidates.  A bin too
+//    large for the candidate list falls back to rounds over every key, with
+//    ties ranked by a block scan in the mask pass.
 #include "qsa_device.cuh"
 #include "qsa_launch.h"
 
@@ -50,14 +55,11 @@ struct SelectSmem {
   uint32_t hist2[256];
   uint32_t hist3[16];
   uint32_t warp_tot[kSelWarps];
-  uint32_t wcount[kSelWarps];
   uint32_t msmall[256];  // rounds 1..3 merged over a cluster (fallback path)
   uint32_t roff[kSelMaxCluster + 1];  // rank 0: where each rank's candidates start
   uint32_t rule_prefix;  // the kept set: (key >> rule_shift) > rule_prefix, or equal
   uint32_t rule_shift;   //   to it at a block index <= rule_cut
   int32_t rule_cut;
-  uint32_t nonfinite;
-  uint32_t nonfinite_all;
   uint32_t ncand;
   int32_t sel_bin;
   uint32_t sel_above;
@@ -65,8 +67,12 @@ struct SelectSmem {
   // cand keys [kCandCap] u32, cand local indices [kCandCap] u16, keys[] follow (dynamic)
 };
 
+// Monotonic u32 key of a score.  -0.0 folds into +0.0 on the bit pattern: a
+// float select (s == 0 ? 0 : s) may be rewritten by the compiler in ways that
+// do not keep a NaN's bits, and NaNs must land in the outer bins.
 __device__ __forceinline__ uint32_t order_key(float s) {
-  const uint32_t u = __float_as_uint(s == 0.0f ? 0.0f : s);  // fold -0.0 into +0.0
+  uint32_t u = __float_as_uint(s);
+  u = (u << 1) ? u : 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
@@ -239,13 +245,6 @@ __device__ __forceinline__ void warp_find_bin(const uint32_t *H, int nb, uint32_
   above = __shfl_sync(0xffffffffu, ma, src);
 }
 
-// Lanes below this one in the warp.
-__device__ __forceinline__ uint32_t lanemask_lt() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
 __global__ void __launch_bounds__(kSelThreads, 2)
 select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_t *__restrict__ pos,
               int32_t tokens, int32_t keep_max, uint8_t *__restrict__ mask, int32_t *status,
@@ -286,7 +285,6 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 
   for (int i = tid; i < 4096 + 256 + 256 + 16; i += kSelThreads) (&S.hist0[0])[i] = 0u;
   if (tid == 0) {
-    S.nonfinite = 0u;
     S.ncand = 0u;
     S.eq_base = 0u;
   }
@@ -297,7 +295,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   {
     constexpr int kLoadsInFlight = 4;  // float4 loads issued per thread before use
     const int32_t nq = (cnt + 3) >> 2;
-    uint32_t nonfinite = 0, zeros = 0;
+    uint32_t zeros = 0;
     for (int32_t qb = warp * 32; qb < nq; qb += kSelThreads * kLoadsInFlight) {
       float4 v[kLoadsInFlight];
 #pragma unroll
@@ -323,8 +321,6 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         for (int e = 0; e < 4; ++e) {
           if (4 * qd + e >= cnt) continue;
           const uint32_t key = kq[e];
-          const float sf = e == 0 ? v[u].x : (e == 1 ? v[u].y : (e == 2 ? v[u].z : v[u].w));
-          nonfinite |= isfinite(sf) ? 0u : 1u;
           if (key == kZeroKey) {
             ++zeros;  // exact zeros, the one heavy bin of relu scores
           } else {
@@ -337,7 +333,6 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) zeros += __shfl_xor_sync(0xffffffffu, zeros, off);
     if (lane == 0 && zeros) atomicAdd(&S.hist0[kZeroKey >> 20], zeros);
-    if (nonfinite) atomicOr(&S.nonfinite, 1u);
   }
 
   uint32_t need = (uint32_t)min(keep_max, n);  // keys still to keep at/below the prefix
@@ -349,19 +344,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   int shift = 32;          // ... prefix = threshold >> shift
 
   // ---- round 0: merge the top-12-bit histograms over the cluster
-  if (C > 1) cluster_sync_all(); else __syncthreads();
-  if (tid == 0) {
-    uint32_t nf = 0;
-    if (C > 1) {
-      for (int q = 0; q < C; ++q) nf |= ld_dsmem(&S.nonfinite, (uint32_t)q);
-    } else {
-      nf = S.nonfinite;
-    }
-    S.nonfinite_all = nf;
-  }
-  __syncthreads();
-  bad = S.nonfinite_all != 0u;  // the same verdict in every CTA of the cluster
-  if (!bad && C > 1) {
+  if (C > 1) {
+    cluster_sync_all();
     // reduce-scatter: this CTA sums its slice of bins over the cluster, in place
     const int slice = 4096 / C;
     for (int b = (int)rank * slice + tid; b < ((int)rank + 1) * slice; b += kSelThreads) {
@@ -389,7 +373,15 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 #pragma unroll
     for (int j = 0; j < kGather; ++j)
       if (tid + j * kSelThreads < 4096) S.hist0[tid + j * kSelThreads] = g[j];
-    __syncthreads();
+  }
+  // A score is non-finite exactly when its key lands in one of the 16 outer
+  // bins: keys of -inf and negative NaNs are below 0x00800000 (bins 0..7),
+  // keys of +inf and positive NaNs at or above 0xFF800000 (bins 0xFF8..0xFFF),
+  // and every finite score's key lies between.
+  __syncthreads();
+  {
+    const bool nf = tid < 16 && S.hist0[tid < 8 ? tid : 0xFF0 + tid] != 0u;
+    bad = __syncthreads_or(nf) != 0;  // the same verdict in every CTA of the cluster
   }
 
   if (!bad) {
@@ -407,89 +399,59 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       }
       __syncthreads();
     } else if (cnt0 <= (uint32_t)kCandCap && per <= 65536) {
-      // ---- candidate path.  Compact this CTA's keys of the bin in block
-      // order, with local indices, and without atomics: each warp counts its
-      // matches in its own contiguous range, a scan of the counts gives each
-      // warp its offset, then each warp writes with a ballot prefix.
-      // each warp owns a contiguous range of whole 128-key chunks; a lane
-      // takes 4 consecutive keys of a chunk (one 16-byte shared load)
-      const int32_t wlen = (((cnt + kSelWarps - 1) / kSelWarps) + 127) & ~127;
-      const int32_t w_lo = min(cnt, warp * wlen);
-      const int32_t w_hi = min(cnt, w_lo + wlen);
-      auto quad_matches = [&](int32_t i, uint32_t (&k)[4]) -> uint32_t {
-        if (i + 3 < cached && i + 3 < w_hi) {
-          const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
-          k[0] = kv.x;
-          k[1] = kv.y;
-          k[2] = kv.z;
-          k[3] = kv.w;
-        } else {
+      // ---- candidate path.  One pass over this CTA's keys: the mask bytes of
+      // keys above the bin (kept) and below it (dropped) are final; the bin's
+      // own keys are written as dropped, appended with their local block
+      // index to the candidate list (slots from a shared counter, so the list
+      // is unordered) and patched once the threshold inside the bin is known.
+      {
+        const uintptr_t rbm = reinterpret_cast<uintptr_t>(mrow);
+        const bool m16 = (rbm & 15u) == 0, m4 = (rbm & 3u) == 0;
+        for (int32_t i = 4 * tid; i < cnt; i += 4 * kSelThreads) {
+          uint32_t k[4];
+          if (i + 3 < cached) {  // one 16-byte shared load
+            const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
+            k[0] = kv.x;
+            k[1] = kv.y;
+            k[2] = kv.z;
+            k[3] = kv.w;
+          } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            k[e] = (i + e < w_hi) ? (i + e < cached ? keys_s[i + e] : order_key(__ldg(srow + i + e)))
-                                  : ~0u;  // never in a bin: (~0u >> 20) != B0 for B0 < 4095
-        }
-        uint32_t bits = 0;
+            for (int e = 0; e < 4; ++e)
+              k[e] = (i + e < cnt) ? (i + e < cached ? keys_s[i + e] : order_key(__ldg(srow + i + e)))
+                                   : 0u;
+          }
+          const int mq = min(4, cnt - i);
+          uint32_t bits = 0, kept = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (i + e < w_hi && (k[e] >> 20) == B0) bits |= 1u << e;
-        return bits;
-      };
-      uint32_t wc = 0;
-      for (int32_t i0 = w_lo; i0 < w_hi; i0 += 128) {
-        uint32_t k[4];
-        wc += (uint32_t)__popc(quad_matches(i0 + 4 * lane, k));
-      }
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t d = k[e] >> 20;
+            if (e < mq) {
+              bits |= (d == B0 ? 1u : 0u) << e;
+              kept |= (d > B0 ? 1u : 0u) << e;
+            }
+          }
+          store_blocks(mrow, (int64_t)b0 + i, mq, kept, m16, m4);
+          if (bits) {
+            uint32_t at = atomicAdd(&S.ncand, (uint32_t)__popc(bits));
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) wc += __shfl_xor_sync(0xffffffffu, wc, off);
-      if (lane == 0) S.wcount[warp] = wc;
-      __syncthreads();
-      uint32_t base = 0, total = 0;
-      for (int w = 0; w < kSelWarps; ++w) {
-        const uint32_t c = S.wcount[w];
-        base += (w < warp) ? c : 0u;
-        total += c;
-      }
-      const uintptr_t rbm = reinterpret_cast<uintptr_t>(mrow);
-      const bool m16 = (rbm & 15u) == 0, m4 = (rbm & 3u) == 0;
-      for (int32_t i0 = w_lo; i0 < w_hi; i0 += 128) {
-        const int32_t i = i0 + 4 * lane;
-        uint32_t k[4];
-        const uint32_t bits = quad_matches(i, k);
-        // keys above the bin are kept, below it dropped: their mask bytes are
-        // final now; the bin's own keys are written as dropped and patched
-        // once the threshold inside the bin is known
-        const int mq = max(0, min(4, w_hi - i));
-        uint32_t kept = 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (e < mq && (k[e] >> 20) > B0) kept |= 1u << e;
-        if (mq > 0) store_blocks(mrow, (int64_t)b0 + i, mq, kept, m16, m4);
-        const uint32_t c = (uint32_t)__popc(bits);
-        uint32_t incl = c;  // warp inclusive scan of the lanes' match counts
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += o;
-        }
-        uint32_t at = base + incl - c;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (bits & (1u << e)) {
-            cand_s[at] = k[e];
-            cand_li[at] = (uint16_t)(i + e);
-            ++at;
+            for (int e = 0; e < 4; ++e) {
+              if (bits & (1u << e)) {
+                cand_s[at] = k[e];
+                cand_li[at] = (uint16_t)(i + e);
+                ++at;
+              }
+            }
           }
         }
-        base += __shfl_sync(0xffffffffu, incl, 31);
       }
-      if (tid == 0) S.ncand = total;
-      own_n = total;
       cand_path = true;
       if (C > 1) cluster_sync_all(); else __syncthreads();
+      own_n = S.ncand;
       if (rank == 0) {
-        // rank 0 gathers every CTA's candidates after its own: the list stays
-        // in block order because slices are in rank order
+        // rank 0 gathers every CTA's candidates after its own, rank by rank,
+        // so an entry's rank (and with it its global block index) follows
+        // from where it sits in the list
         if (warp == 0) {  // every rank's count at once, then a warp prefix sum
           uint32_t c = 0;
           if (lane < C) c = lane == 0 ? S.ncand : ld_dsmem(&S.ncand, (uint32_t)lane);
@@ -515,7 +477,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         __syncthreads();
         const int32_t nl = (int32_t)S.roff[C];
         // rounds 1..3 on the candidates: every thread histograms, one warp
-        // finds the bin (two barriers a round); then the tie cutoff
+        // finds the bin (two barriers a round)
         bool done = false;
         for (int r = 1; r < kRounds && !done; ++r) {
           uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
@@ -549,29 +511,47 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
             S.rule_cut = INT32_MAX;
           }
         } else {
-          // ties at the full key: keep the first `need` equal keys in block
-          // order; the list is in block order, so find the need-th equal entry
-          constexpr int kPerThread = (kCandCap + kSelThreads - 1) / kSelThreads;
-          const int32_t j0 = tid * kPerThread;
-          uint32_t eq = 0;
-#pragma unroll
-          for (int e = 0; e < kPerThread; ++e)
-            eq += (j0 + e < nl && cand_s[j0 + e] == prefix) ? 1u : 0u;
-          uint32_t tot;
-          const uint32_t before = block_excl_scan(eq, S.warp_tot, tot);
-          if (before < need && need <= before + eq) {
-            uint32_t acc = before;
-            for (int e = 0; e < kPerThread; ++e) {
-              const int32_t j = j0 + e;
-              if (j < nl && cand_s[j] == prefix && ++acc == need) {
-                int q = 0;
-                while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
-                S.rule_prefix = prefix;
-                S.rule_shift = 0;
-                S.rule_cut = q * per + (int32_t)cand_li[j];
-                break;
+          // ties at the full key: of the keys equal to `prefix`, the `need`
+          // with the lowest block indices are kept.  Radix rounds over the
+          // equal candidates' block indices, 8 bits at a time from the
+          // highest bit an index < n can have, find the cut index.
+          const uint32_t top = (uint32_t)n - 1u;
+          int ish = top ? ((32 - __clz((int)top) + 7) & ~7) : 8;  // index bits, rounded up
+          uint32_t iprefix = 0;  // the cut index's bits above ish
+          uint32_t *H = S.hist0;  // round 0's histogram is no longer read
+          for (int ir = 0; ir < 4; ++ir) {
+            const int sh = ish - 8;
+            if (tid < 256) H[tid] = 0u;
+            __syncthreads();
+            for (int32_t j = tid; j < nl; j += kSelThreads) {
+              if (cand_s[j] != prefix) continue;
+              int q = 0;
+              while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
+              const uint32_t gi = (uint32_t)(q * per) + (uint32_t)cand_li[j];
+              if (ish >= 32 || (gi >> ish) == iprefix)  // ascending: digit d counts in bin 255-d
+                atomicAdd(&H[255u - ((gi >> sh) & 255u)], 1u);
+            }
+            __syncthreads();
+            if (warp == 0) {
+              uint32_t B, above;
+              warp_find_bin(H, 256, need, lane, B, above);
+              if (lane == 0) {
+                S.sel_bin = (int32_t)B;
+                S.sel_above = above;
               }
             }
+            __syncthreads();
+            const uint32_t cB = H[S.sel_bin];
+            need -= S.sel_above;
+            iprefix = (iprefix << 8) | (255u - (uint32_t)S.sel_bin);
+            ish = sh;
+            __syncthreads();  // sel_bin and H are rewritten next round
+            if (cB == need || ish == 0) break;  // at ish == 0 a bin holds one index
+          }
+          if (tid == 0) {
+            S.rule_prefix = prefix;
+            S.rule_shift = 0;
+            S.rule_cut = (int32_t)((((uint64_t)iprefix + 1u) << ish) - 1u);
           }
         }
         __syncthreads();

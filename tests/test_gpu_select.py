@@ -165,6 +165,29 @@ def test_select_nonfinite_row_reported_and_untouched(qsa, orc):
         assert np.array_equal(got[r], want[r])
 
 
+@pytest.mark.parametrize("bits", [0x7F800000, 0xFF800000, 0x7FC00001, 0xFFC00000, 0xFF800001])
+def test_select_each_nonfinite_kind_reported(qsa, orc, bits):
+    """+inf, -inf, a positive and two negative NaNs: each one, anywhere in a
+    truncating row's prefix, is an error for that row alone; the same value
+    past the row's prefix, or in an all-kept row, is never read."""
+    tokens = 65536
+    cols = tokens // 4
+    rng = qi.rng_for(4, salt=bits & 0xFFFF)
+    scores = rng.random((4, cols)).astype(np.float32)
+    bad = np.array([bits], np.uint32).view(np.float32)[0]
+    scores[1, 12345] = bad     # inside row 1's prefix
+    scores[2, 15000] = bad     # past row 2's prefix (pos 40000 -> 10000 blocks)
+    scores[3, 100] = bad       # row 3 keeps every block: its scores are not read
+    pos = np.array([65535, 65535, 40000, 2000], np.int32)
+    got, row = gpu_select(qsa, scores, cols, pos, tokens, 2048, expect=4)
+    assert row == 1
+    assert np.all(got[1] == 0xAB)
+    want, codes = oracle_masks(orc, scores, cols, pos, tokens, 2048)
+    assert codes == [0, 4, 0, 0]
+    for r in (0, 2, 3):
+        assert np.array_equal(got[r], want[r])
+
+
 def test_select_row_out_of_range_reported(qsa):
     tokens = 4096
     cols = tokens // 4

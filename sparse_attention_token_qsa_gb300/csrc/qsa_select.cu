@@ -34,8 +34,11 @@
 
 namespace qsa {
 
-constexpr int kSelThreads = 512;
-constexpr int kSelWarps = kSelThreads / 32;
+// Two block shapes: 512 threads with the row's keys cached in shared memory
+// (two CTAs per SM) for launches with few rows, where latency matters; 256
+// threads that re-read keys from L2 instead (four smaller CTAs per SM hide
+// each other's barrier phases) for launches with many rows.
+constexpr int kSelMaxWarps = 16;
 constexpr int kSelMaxCluster = 16;
 constexpr int kSelCapMax = 16384;  // keys cached per CTA (64 KiB)
 
@@ -54,7 +57,7 @@ struct SelectSmem {
   uint32_t hist1[256];
   uint32_t hist2[256];
   uint32_t hist3[16];
-  uint32_t warp_tot[kSelWarps];
+  uint32_t warp_tot[kSelMaxWarps];
   uint32_t msmall[256];  // rounds 1..3 merged over a cluster (fallback path)
   uint32_t roff[kSelMaxCluster + 1];  // rank 0: where each rank's candidates start
   uint32_t rule_prefix;  // the kept set: (key >> rule_shift) > rule_prefix, or equal
@@ -73,7 +76,8 @@ struct SelectSmem {
 __device__ __forceinline__ uint32_t order_key(float s) {
   uint32_t u = __float_as_uint(s);
   u = (u << 1) ? u : 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  // negative: all bits flipped; non-negative: the sign bit set
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -160,6 +164,7 @@ __device__ __forceinline__ void store_blocks(uint8_t *mrow, int64_t blk, int cnt
 
 // Exclusive block-wide scan of v (all threads call); returns the exclusive
 // prefix and writes the block total to *total.
+template <int NT>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_tot, uint32_t &total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = v;
@@ -172,7 +177,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
   __syncthreads();
   uint32_t before = 0, tot = 0;
 #pragma unroll
-  for (int w = 0; w < kSelWarps; ++w) {
+  for (int w = 0; w < NT / 32; ++w) {
     const uint32_t t = warp_tot[w];
     before += (w < warp) ? t : 0u;
     tot += t;
@@ -185,15 +190,16 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
 // Find the bin of histogram M[nb] (shared memory) that holds the need-th
 // largest key, scanning bins from the top: S.sel_bin gets the bin, S.sel_above
 // the number of keys in higher bins.  Every thread of the CTA calls it.
+template <int NT>
 __device__ __forceinline__ void find_bin(const uint32_t *M, int nb, uint32_t need, SelectSmem &S) {
   const int tid = threadIdx.x;
-  const int per = (nb + kSelThreads - 1) / kSelThreads;
+  const int per = (nb + NT - 1) / NT;
   const int hi = nb - 1 - tid * per;  // this thread's bins: hi, hi-1, ..., hi-per+1
   uint32_t sum = 0;
   for (int j = 0; j < per; ++j)
     if (hi - j >= 0) sum += M[hi - j];
   uint32_t total;
-  const uint32_t before = block_excl_scan(sum, S.warp_tot, total);
+  const uint32_t before = block_excl_scan<NT>(sum, S.warp_tot, total);
   if (before < need && need <= before + sum) {
     uint32_t acc = before;
     for (int j = 0; j < per; ++j) {
@@ -245,7 +251,8 @@ __device__ __forceinline__ void warp_find_bin(const uint32_t *H, int nb, uint32_
   above = __shfl_sync(0xffffffffu, ma, src);
 }
 
-__global__ void __launch_bounds__(kSelThreads, 2)
+template <int NT>
+__global__ void __launch_bounds__(NT, NT == 256 ? 5 : 2)
 select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_t *__restrict__ pos,
               int32_t tokens, int32_t keep_max, uint8_t *__restrict__ mask, int32_t *status,
               int32_t C, int32_t cap) {
@@ -283,30 +290,30 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   const float *srow = scores + (int64_t)row * score_cols + b0;
   const int32_t cached = min(cnt, cap);
 
-  for (int i = tid; i < 4096 + 256 + 256 + 16; i += kSelThreads) (&S.hist0[0])[i] = 0u;
+  for (int i = tid; i < 4096 + 256 + 256 + 16; i += NT) (&S.hist0[0])[i] = 0u;
   if (tid == 0) {
     S.ncand = 0u;
     S.eq_base = 0u;
   }
   __syncthreads();
 
-  // ---- round 0 while loading: key cache, finiteness, top-12-bit histogram.
-  // Exact zeros (relu outputs) share one bin: counted by ballot, not match.any.
+  // ---- round 0 while loading: key cache and top-12-bit histogram.  Exact
+  // zeros (relu outputs) share one bin: counted in registers, added per warp.
   {
     constexpr int kLoadsInFlight = 4;  // float4 loads issued per thread before use
     const int32_t nq = (cnt + 3) >> 2;
     uint32_t zeros = 0;
-    for (int32_t qb = warp * 32; qb < nq; qb += kSelThreads * kLoadsInFlight) {
+    for (int32_t qb = warp * 32; qb < nq; qb += NT * kLoadsInFlight) {
       float4 v[kLoadsInFlight];
 #pragma unroll
       for (int u = 0; u < kLoadsInFlight; ++u) {
-        const int32_t qd = qb + u * kSelThreads + lane;
+        const int32_t qd = qb + u * NT + lane;
         v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (qd < nq) v[u] = __ldg(reinterpret_cast<const float4 *>(srow) + qd);
       }
 #pragma unroll
       for (int u = 0; u < kLoadsInFlight; ++u) {
-        const int32_t qd = qb + u * kSelThreads + lane;
+        const int32_t qd = qb + u * NT + lane;
         if (qd >= nq) continue;  // per lane: nothing below needs the whole warp
         const uint32_t kq[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z),
                                 order_key(v[u].w)};
@@ -317,14 +324,12 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
           for (int e = 0; e < 4; ++e)
             if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
         }
+        const int ne = min(4, cnt - 4 * qd);  // keys of this quad in the slice
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          if (4 * qd + e >= cnt) continue;
-          const uint32_t key = kq[e];
-          if (key == kZeroKey) {
-            ++zeros;  // exact zeros, the one heavy bin of relu scores
-          } else {
-            atomicAdd(&S.hist0[key >> 20], 1u);
+          if (ne == 4 || e < ne) {  // whole quads need no per-key test
+            zeros += kq[e] == kZeroKey ? 1u : 0u;
+            if (kq[e] != kZeroKey) atomicAdd(&S.hist0[kq[e] >> 20], 1u);
           }
         }
       }
@@ -348,7 +353,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     cluster_sync_all();
     // reduce-scatter: this CTA sums its slice of bins over the cluster, in place
     const int slice = 4096 / C;
-    for (int b = (int)rank * slice + tid; b < ((int)rank + 1) * slice; b += kSelThreads) {
+    for (int b = (int)rank * slice + tid; b < ((int)rank + 1) * slice; b += NT) {
       uint32_t v[kSelMaxCluster];
 #pragma unroll
       for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&S.hist0[b], (uint32_t)q) : 0u;
@@ -359,11 +364,11 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     }
     cluster_sync_all();
     // gather the other slices' merged bins (their owners no longer change them)
-    constexpr int kGather = (4096 + kSelThreads - 1) / kSelThreads;
+    constexpr int kGather = (4096 + NT - 1) / NT;
     uint32_t g[kGather];
 #pragma unroll
     for (int j = 0; j < kGather; ++j) {
-      const int b = tid + j * kSelThreads;
+      const int b = tid + j * NT;
       g[j] = 0u;
       if (b < 4096) {
         const int owner = b / slice;
@@ -372,7 +377,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     }
 #pragma unroll
     for (int j = 0; j < kGather; ++j)
-      if (tid + j * kSelThreads < 4096) S.hist0[tid + j * kSelThreads] = g[j];
+      if (tid + j * NT < 4096) S.hist0[tid + j * NT] = g[j];
   }
   // A score is non-finite exactly when its key lands in one of the 16 outer
   // bins: keys of -inf and negative NaNs are below 0x00800000 (bins 0..7),
@@ -385,7 +390,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   }
 
   if (!bad) {
-    find_bin(S.hist0, 4096, need, S);
+    find_bin<NT>(S.hist0, 4096, need, S);
     const uint32_t B0 = (uint32_t)S.sel_bin;
     const uint32_t cnt0 = S.hist0[B0];
     need -= S.sel_above;
@@ -407,7 +412,9 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       {
         const uintptr_t rbm = reinterpret_cast<uintptr_t>(mrow);
         const bool m16 = (rbm & 15u) == 0, m4 = (rbm & 3u) == 0;
-        for (int32_t i = 4 * tid; i < cnt; i += 4 * kSelThreads) {
+        // B0 < 0xFF8 (a finite key's bin), so the upper edge does not wrap
+        const uint32_t bin_lo = B0 << 20, bin_hi = (B0 + 1u) << 20;
+        for (int32_t i = 4 * tid; i < cnt; i += 4 * NT) {
           uint32_t k[4];
           if (i + 3 < cached) {  // one 16-byte shared load
             const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
@@ -415,6 +422,12 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
             k[1] = kv.y;
             k[2] = kv.z;
             k[3] = kv.w;
+          } else if (i >= cached && i + 3 < cnt) {  // not cached: one 16-byte load (L2)
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + i));
+            k[0] = order_key(f.x);
+            k[1] = order_key(f.y);
+            k[2] = order_key(f.z);
+            k[3] = order_key(f.w);
           } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -422,16 +435,22 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
                                    : 0u;
           }
           const int mq = min(4, cnt - i);
-          uint32_t bits = 0, kept = 0;
+          // whole keys against the bin's edges: >= hi kept, [lo, hi) candidates
+          uint32_t bits = 0, w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const uint32_t d = k[e] >> 20;
-            if (e < mq) {
-              bits |= (d == B0 ? 1u : 0u) << e;
-              kept |= (d > B0 ? 1u : 0u) << e;
-            }
+            const bool in = mq == 4 || e < mq;
+            const bool kp = k[e] >= bin_hi;
+            w[e] = (in && kp) ? 0x01010101u : 0u;
+            bits |= (in && !kp && k[e] >= bin_lo) ? (1u << e) : 0u;
           }
-          store_blocks(mrow, (int64_t)b0 + i, mq, kept, m16, m4);
+          if (mq == 4 && m16) {
+            *reinterpret_cast<uint4 *>(mrow + 4 * ((int64_t)b0 + i)) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+            store_blocks(mrow, (int64_t)b0 + i, mq,
+                         (w[0] & 1u) | ((w[1] & 1u) << 1) | ((w[2] & 1u) << 2) | ((w[3] & 1u) << 3),
+                         m16, m4);
+          }
           if (bits) {
             uint32_t at = atomicAdd(&S.ncand, (uint32_t)__popc(bits));
 #pragma unroll
@@ -467,7 +486,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         __syncthreads();
         // one thread per remote entry across all ranks, loads independent
         const uint32_t own = S.roff[1], all = S.roff[C];
-        for (uint32_t j = own + tid; j < all; j += kSelThreads) {
+        for (uint32_t j = own + tid; j < all; j += NT) {
           int q = 1;
           while (q + 1 < C && S.roff[q + 1] <= j) ++q;
           const uint32_t jj = j - S.roff[q];
@@ -482,7 +501,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         for (int r = 1; r < kRounds && !done; ++r) {
           uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
           const int nb = round_bins(r), sh = round_shift(r);
-          for (int32_t j = tid; j < nl; j += kSelThreads) {
+          for (int32_t j = tid; j < nl; j += NT) {
             const uint32_t key = cand_s[j];
             if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
           }
@@ -523,7 +542,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
             const int sh = ish - 8;
             if (tid < 256) H[tid] = 0u;
             __syncthreads();
-            for (int32_t j = tid; j < nl; j += kSelThreads) {
+            for (int32_t j = tid; j < nl; j += NT) {
               if (cand_s[j] != prefix) continue;
               int q = 0;
               while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
@@ -576,7 +595,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     for (int r = 1; r < kRounds && !done; ++r) {
       uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
       const int nb = round_bins(r), sh = round_shift(r);
-      for (int32_t ib = warp * 32; ib < cnt; ib += kSelThreads) {
+      for (int32_t ib = warp * 32; ib < cnt; ib += NT) {
         const int32_t i = ib + lane;
         const bool in = i < cnt;
         uint32_t key = 0;
@@ -586,7 +605,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       if (C > 1) cluster_sync_all(); else __syncthreads();
       const uint32_t *M = H;
       if (C > 1) {
-        for (int b = tid; b < nb; b += kSelThreads) {
+        for (int b = tid; b < nb; b += NT) {
           uint32_t v[kSelMaxCluster];
 #pragma unroll
           for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&H[b], (uint32_t)q) : 0u;
@@ -598,7 +617,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         __syncthreads();
         M = S.msmall;
       }
-      find_bin(M, nb, need, S);
+      find_bin<NT>(M, nb, need, S);
       const uint32_t B = (uint32_t)S.sel_bin;
       const uint32_t cB = M[B];
       need -= S.sel_above;
@@ -631,13 +650,13 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     const int32_t rc = S.rule_cut;
     uint32_t running = S.eq_base;
     if (cand_path) {  // the mask is written but for this CTA's candidates
-      for (uint32_t j = tid; j < own_n; j += kSelThreads) {
+      for (uint32_t j = tid; j < own_n; j += NT) {
         const uint32_t kk = cand_s[j] >> rs;
         const int32_t li = (int32_t)cand_li[j];
         if (kk > rp || (kk == rp && b0 + li <= rc)) store_blocks(mrow, (int64_t)b0 + li, 1, 1u, false, al4);
       }
     }
-    for (int32_t tb = 0; tb < (cand_path ? 0 : cnt); tb += 4 * kSelThreads) {
+    for (int32_t tb = 0; tb < (cand_path ? 0 : cnt); tb += 4 * NT) {
       const int32_t i = tb + 4 * tid;
       const int m = max(0, min(4, cnt - i));
       uint32_t k[4];
@@ -666,7 +685,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 #pragma unroll
         for (int e = 0; e < 4; ++e) eqc += (e < m && k[e] == prefix) ? 1u : 0u;
         uint32_t total;
-        uint32_t rk = running + block_excl_scan(eqc, S.warp_tot, total);
+        uint32_t rk = running + block_excl_scan<NT>(eqc, S.warp_tot, total);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (e >= m) continue;
@@ -702,13 +721,16 @@ static size_t select_smem_bytes(int32_t cap) {
 }
 
 // Largest cluster the select kernel can be co-scheduled with (16 needs the
-// non-portable opt-in; fall back to 8, 4, 2 if the GPU refuses).
+// non-portable opt-in; fall back to 8, 4, 2 if the GPU refuses).  Both block
+// shapes get their attributes here, once.
 static int max_cluster_size() {
   if (g_max_cluster >= 0) return g_max_cluster;
   int best = 1;
-  cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)select_smem_bytes(kSelCapMax));
+  for (auto fn : {select_kernel<512>, select_kernel<256>}) {
+    cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)select_smem_bytes(kSelCapMax));
+  }
   for (int c = kSelMaxCluster; c >= 2; c >>= 1) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -717,12 +739,12 @@ static int max_cluster_size() {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(c);
-    cfg.blockDim = dim3(kSelThreads);
+    cfg.blockDim = dim3(512);
     cfg.dynamicSmemBytes = select_smem_bytes(kSelCapMax);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, select_kernel, &cfg) == cudaSuccess && n > 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, select_kernel<512>, &cfg) == cudaSuccess && n > 0) {
       best = c;
       break;
     }
@@ -730,6 +752,20 @@ static int max_cluster_size() {
   cudaGetLastError();  // a refused query leaves no sticky error
   g_max_cluster = best;
   return best;
+}
+
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      n = 1;
+    cudaGetLastError();
+  }
+  return n;
 }
 
 // Cluster size for a launch: split a row over a cluster only when its blocks
@@ -752,7 +788,10 @@ cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t
   const int64_t n_max = (int64_t)tokens / kRatio;
   const int C = select_cluster_size(n_rows, tokens);
   const int64_t per = (((n_max + C - 1) / C) + 3) & ~int64_t(3);
-  const int32_t cap = (int32_t)(per < kSelCapMax ? per : kSelCapMax);
+  const int64_t ctas = (int64_t)n_rows * C;
+  // more CTAs than two waves of the wide shape: small CTAs, keys re-read from L2
+  const bool narrow = ctas > 2 * (int64_t)sm_count();
+  const int32_t cap = narrow ? 0 : (int32_t)(per < kSelCapMax ? per : kSelCapMax);
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -760,14 +799,17 @@ cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)((int64_t)n_rows * C));
-  cfg.blockDim = dim3(kSelThreads);
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(narrow ? 256 : 512);
   cfg.dynamicSmemBytes = select_smem_bytes(cap);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = C > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, select_kernel, scores, score_cols, pos, tokens, keep_max, mask,
-                            status, (int32_t)C, cap);
+  if (narrow)
+    return cudaLaunchKernelEx(&cfg, select_kernel<256>, scores, score_cols, pos, tokens, keep_max,
+                              mask, status, (int32_t)C, cap);
+  return cudaLaunchKernelEx(&cfg, select_kernel<512>, scores, score_cols, pos, tokens, keep_max,
+                            mask, status, (int32_t)C, cap);
 }
 
 }  // namespace qsa

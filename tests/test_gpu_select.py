@@ -46,9 +46,10 @@ def gpu_select(qsa, scores, score_cols, pos, tokens, budget, mask_offset=0, expe
 
 def test_select_stress_ties_all_budgets(qsa, orc):
     """Selection-only stress at 256k: relu-sum-like scores, 70% exact zeros (half
-    -0.0), the rest on 64 levels; every budget the stress names."""
+    -0.0), the rest on 64 levels; every budget the stress names.  96 rows split
+    over clusters of 4 are enough CTAs for the many-row block shape."""
     rng = qi.rng_for(4)
-    rows, tokens = 48, 262144
+    rows, tokens = 96, 262144
     cols = tokens // 4
     scores = qi.stress_scores(rng, rows, cols)
     pos = np.full(rows, tokens - 1, np.int32)

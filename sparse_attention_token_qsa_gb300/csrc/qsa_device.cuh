@@ -52,6 +52,17 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched so
+// that it may start while the previous kernel in its stream is finishing;
+// this call, made by every thread before its first global memory access and
+// before any early return, waits until that kernel has completed and its
+// writes are visible, then lets the next kernel in the stream begin to
+// launch.  A launch without the programmatic attribute passes both at once.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Record the first device-side error: {code, row}.  Never traps.
 __device__ __forceinline__ void report_error(int32_t *status, int32_t code, int32_t row) {
   if (status == nullptr) return;

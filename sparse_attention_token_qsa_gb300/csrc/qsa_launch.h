@@ -7,6 +7,35 @@
 
 namespace qsa {
 
+// Launch `kernel` so that it may begin while the previous kernel in `stream`
+// finishes (programmatic stream serialization).  The kernel must call
+// grid_dependency_sync() before it touches global memory; an optional cluster
+// shape is passed through.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, unsigned cluster_x, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster_x > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster_x;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 cudaError_t launch_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t first_block,
                                int32_t n_blocks, const uint16_t *k_norm_w, const uint16_t *cos_t,
                                const uint16_t *sin_t, float eps, uint16_t *block_keys,

@@ -24,6 +24,7 @@ pool_blocks_kernel(const uint16_t *__restrict__ keys, int64_t key_stride, int32_
                    int32_t n_blocks, const uint16_t *__restrict__ k_norm_w,
                    const uint16_t *__restrict__ cos_t, const uint16_t *__restrict__ sin_t,
                    float eps, uint16_t *__restrict__ block_keys) {
+  grid_dependency_sync();
   const int lane = threadIdx.x & 31;
   const int g = lane & 15;
   const int64_t i = (int64_t)blockIdx.x * kPoolBlocksPerCta + (threadIdx.x >> 4);
@@ -69,9 +70,9 @@ cudaError_t launch_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t
                                const uint16_t *sin_t, float eps, uint16_t *block_keys,
                                cudaStream_t stream) {
   const int64_t grid = ((int64_t)n_blocks + kPoolBlocksPerCta - 1) / kPoolBlocksPerCta;
-  pool_blocks_kernel<<<(unsigned)grid, kPoolThreads, 0, stream>>>(
-      keys, key_stride, first_block, n_blocks, k_norm_w, cos_t, sin_t, eps, block_keys);
-  return cudaGetLastError();
+  return launch_dependent(pool_blocks_kernel, dim3((unsigned)grid), dim3(kPoolThreads), 0, stream,
+                          1u, keys, key_stride, first_block, n_blocks, k_norm_w, cos_t, sin_t,
+                          eps, block_keys);
 }
 
 }  // namespace qsa

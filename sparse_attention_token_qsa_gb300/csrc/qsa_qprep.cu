@@ -20,6 +20,7 @@ constexpr int kPrepVecsPerCta = kPrepThreads / 16;
 
 __global__ void __launch_bounds__(kPrepThreads)
 qprep_kernel(const ScoreArgs a, uint16_t *__restrict__ qws) {
+  grid_dependency_sync();
   const int lane = threadIdx.x & 31;
   const int g = lane & 15;
   const int64_t nvec = (int64_t)a.n_rows * kHeads;
@@ -51,8 +52,8 @@ qprep_kernel(const ScoreArgs a, uint16_t *__restrict__ qws) {
 cudaError_t launch_qprep(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream) {
   const int64_t nvec = (int64_t)a.n_rows * kHeads;
   const int64_t grid = (nvec + kPrepVecsPerCta - 1) / kPrepVecsPerCta;
-  qprep_kernel<<<(unsigned)grid, kPrepThreads, 0, stream>>>(a, qws);
-  return cudaGetLastError();
+  return launch_dependent(qprep_kernel, dim3((unsigned)grid), dim3(kPrepThreads), 0, stream, 1u, a,
+                          qws);
 }
 
 }  // namespace qsa

@@ -52,6 +52,7 @@ __device__ __forceinline__ void prep_query_heads(const ScoreArgs &a, int row, in
 __global__ void __launch_bounds__(kSimtThreads)
 score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
   __shared__ float q_s[kHeads][kHeadDim];
+  grid_dependency_sync();
   const int row = blockIdx.x;
   const int p = a.pos[row];
   const int vis = a.visible_len ? a.visible_len[row] : p + 1;
@@ -141,8 +142,7 @@ cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream) {
   while ((iters + k - 1) / k > 65535) ++k;
   const int32_t bpc = (int32_t)(k * kSimtBlocksPerIter);
   dim3 grid((unsigned)a.n_rows, (unsigned)((n_max + bpc - 1) / bpc));
-  score_simt_kernel<<<grid, kSimtThreads, 0, stream>>>(a, bpc);
-  return cudaGetLastError();
+  return launch_dependent(score_simt_kernel, grid, dim3(kSimtThreads), 0, stream, 1u, a, bpc);
 }
 
 }  // namespace qsa

@@ -242,6 +242,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   const uint32_t sK = smem_u32(smem + kKOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t row_tiles = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
+  grid_dependency_sync();  // before TMEM too: an earlier launch may hold it
 
   // ---- set-up: barriers, TMEM, and the work each row tile needs
   if (tid == 0) {
@@ -522,9 +523,8 @@ cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stre
     const int64_t row_tiles = (b.n_rows + kRowsPerCta - 1) / kRowsPerCta;
     int64_t ctas = sm_count();
     if (ctas > row_tiles * tiles_total) ctas = row_tiles * tiles_total;
-    score_tc_kernel<<<(unsigned)ctas, kThreads, kSmemBytes, stream>>>(kmap, qmap, b, tiles_total,
-                                                                      r0);
-    e = cudaGetLastError();
+    e = launch_dependent(score_tc_kernel, dim3((unsigned)ctas), dim3(kThreads), kSmemBytes, stream,
+                         1u, kmap, qmap, b, tiles_total, r0);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

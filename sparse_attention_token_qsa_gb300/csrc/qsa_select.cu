@@ -263,6 +263,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   uint16_t *cand_li = reinterpret_cast<uint16_t *>(cand_s + kCandCap);
   uint32_t *keys_s = reinterpret_cast<uint32_t *>(cand_li + kCandCap);
 
+  grid_dependency_sync();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t row = blockIdx.x / C;
   const uint32_t rank = (C > 1) ? cluster_rank() : 0u;
@@ -793,23 +794,14 @@ cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t
   const bool narrow = ctas > 2 * (int64_t)sm_count();
   const int32_t cap = narrow ? 0 : (int32_t)(per < kSelCapMax ? per : kSelCapMax);
 
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)ctas);
-  cfg.blockDim = dim3(narrow ? 256 : 512);
-  cfg.dynamicSmemBytes = select_smem_bytes(cap);
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = C > 1 ? 1 : 0;
+  const size_t smem = select_smem_bytes(cap);
   if (narrow)
-    return cudaLaunchKernelEx(&cfg, select_kernel<256>, scores, score_cols, pos, tokens, keep_max,
-                              mask, status, (int32_t)C, cap);
-  return cudaLaunchKernelEx(&cfg, select_kernel<512>, scores, score_cols, pos, tokens, keep_max,
-                            mask, status, (int32_t)C, cap);
+    return launch_dependent(select_kernel<256>, dim3((unsigned)ctas), dim3(256), smem, stream,
+                            (unsigned)C, scores, score_cols, pos, tokens, keep_max, mask, status,
+                            (int32_t)C, cap);
+  return launch_dependent(select_kernel<512>, dim3((unsigned)ctas), dim3(512), smem, stream,
+                          (unsigned)C, scores, score_cols, pos, tokens, keep_max, mask, status,
+                          (int32_t)C, cap);
 }
 
 }  // namespace qsa

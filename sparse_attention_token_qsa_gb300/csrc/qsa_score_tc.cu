@@ -26,10 +26,14 @@
 //  * warp 1 (one lane) issues the MMAs into one of two TMEM accumulators
 //    (256 columns each, 512 in all) and commits to mbarriers that free the key
 //    stage and publish the accumulator;
-//  * warps 4..19 drain the accumulator: warp w reads TMEM lane quarter w % 4
-//    (32 blocks) and a quarter of the columns (16 rows), 32 columns per
-//    tcgen05.ld, relu per head, ((h0 + h1) + h2) + h3, scale, coalesced stores
-//    of the blocks each row can see;
+//  * warps 4..19 drain the accumulators in two groups of eight, group g
+//    taking accumulator g (every other unit), so each SM sub-partition holds
+//    warps of two units in different phases: warp w reads TMEM lane quarter
+//    w % 4 (32 blocks) and half of the columns (32 rows) in chunks of 16
+//    columns, the next chunk loading while the current one is reduced (relu
+//    per head, ((h0 + h1) + h2) + h3, scale) and stored with coalesced
+//    128-byte stores; units off the causal diagonal store without per-row
+//    tests;
 //  * every mbarrier wait is bounded: on timeout the kernel records
 //    QSA_ERR_TIMEOUT, lets the other roles drop out, drains its own MMAs and
 //    frees its TMEM.
@@ -181,22 +185,25 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&v)[32]) {
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-        "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-        "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-        "=r"(v[31])
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// Wait for this thread's TMEM loads.  The loaded registers pass through the
+// statement, so no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&v)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15])
+               :
+               : "memory");
 }
 
 // relu that keeps NaN (max.NaN returns NaN when either input is NaN)
@@ -252,7 +259,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&C.tfull[b]), 1);
-      mbar_init(smem_u32(&C.tempty[b]), kEpiWarps);
+      mbar_init(smem_u32(&C.tempty[b]), kEpiWarps / 2);  // one group per accumulator
     }
     mbar_init(smem_u32(&C.drain), 1);
     mbar_init(smem_u32(&C.qfree), 1);
@@ -374,52 +381,79 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
       mbar_wait(smem_u32(&C.drain), (uint32_t)(drains & 1), nullptr);
     }
   } else if (nunits > 0) {
-    // ---- warps 4..19: drain TMEM (warps 2 and 3 have no role)
+    // ---- warps 4..19: drain TMEM (warps 2 and 3 have no role).  Two groups of
+    // eight warps, one per accumulator: group g drains the units i with
+    // i % 2 == g, so each SM sub-partition holds warps of two units at once.
     const bool epi = warp >= kEpiWarp0;
-    const int quarter = warp & 3;             // the TMEM lane quarter this warp may read
-    const int cq = (warp - kEpiWarp0) >> 2;   // which 16 rows (64 columns) it drains
+    const int grp = (warp - kEpiWarp0) >> 3;       // accumulator / unit parity
+    const int quarter = warp & 3;                  // the TMEM lane quarter this warp may read
+    const int half = ((warp - kEpiWarp0) >> 2) & 1;  // which 32 rows (128 columns) it drains
     const float inv_sqrt_hd = 0.08838834764831845f;
     const int64_t ld = a.score_cols;
     UnitCursor cur;
     cur.init(C.start, w0);
-    int32_t my_n = 0;  // lane j < 16: visible blocks of this warp's row j
+    int32_t my_n = 0;     // lane j: visible blocks of this warp's row j
+    int32_t lim_min = 0;  // the smallest over the warp's 32 rows
     for (int i = 0; i < nunits && epi; ++i) {
       const bool sw = (i == 0) || cur.next();
-      if (sw) {
-        const int r = cur.rt * kRowsPerCta + cq * 16 + (lane & 15);
+      if (sw) {  // new row tile: this warp's rows and how far each may be written
+        const int r = cur.rt * kRowsPerCta + half * 32 + lane;
         my_n = 0;
-        if (lane < 16 && r < a.n_rows) {
+        if (r < a.n_rows) {
           const int32_t p = a.pos[r];
           const int32_t vis = a.visible_len ? a.visible_len[r] : p + 1;
           if (!(p < 0 || p >= a.tokens || vis < 0 || vis > p + 1)) my_n = vis >> 2;
         }
+        lim_min = my_n;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+          lim_min = min(lim_min, __shfl_xor_sync(0xffffffffu, lim_min, off));
       }
-      const int buf = i & 1;
+      if ((i & 1) != grp) continue;
+      const int buf = grp;
       const uint32_t ja = (uint32_t)(i >> 1);
       if (!warp_wait(smem_u32(&C.tfull[buf]), ja & 1u, abort_flag)) break;
       tc_fence_after();
       const int b = cur.nt * kBN + quarter * 32 + lane;  // this thread's block
-      float *const srow0 = a.scores + (int64_t)(cur.rt * kRowsPerCta + cq * 16) * ld;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        int32_t lim[8];
+      // warp-uniform: all 32 blocks visible to all 32 rows (every unit off the
+      // causal diagonal), so the stores need no per-row test
+      const bool whole = cur.nt * kBN + quarter * 32 + 32 <= lim_min;
+      float *dst = a.scores + (int64_t)(cur.rt * kRowsPerCta + half * 32) * ld + b;
+      // eight chunks of 16 columns (4 rows x 4 heads); chunk c + 1 loads while
+      // chunk c is reduced and stored
+      const uint32_t taddr =
+          tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kQCols + half * 128);
+      uint32_t va[16], vb[16];
+      tmem_ld16_async(taddr, va);
+      tmem_wait_ld(va);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) lim[j] = __shfl_sync(0xffffffffu, my_n, c * 8 + j);
-        uint32_t v[32];
-        tmem_ld32_async(tmem + ((uint32_t)(quarter * 32) << 16) +
-                            (uint32_t)(buf * kQCols + cq * 64 + c * 32),
-                        v);
-        tmem_wait_ld();
-        float *dst = srow0 + (int64_t)(c * 8) * ld + b;
+      for (int c = 0; c < 8; ++c) {
+        uint32_t(&v)[16] = (c & 1) ? vb : va;
+        uint32_t(&vn)[16] = (c & 1) ? va : vb;
+        if (c < 7) tmem_ld16_async(taddr + (uint32_t)(c + 1) * 16u, vn);
+        float sc[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
           const float h0 = relu_nan(__uint_as_float(v[4 * j + 0]));
           const float h1 = relu_nan(__uint_as_float(v[4 * j + 1]));
           const float h2 = relu_nan(__uint_as_float(v[4 * j + 2]));
           const float h3 = relu_nan(__uint_as_float(v[4 * j + 3]));
-          const float sc = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(h0, h1), h2), h3), inv_sqrt_hd);
-          if (b < lim[j]) dst[(int64_t)j * ld] = sc;
+          sc[j] = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(h0, h1), h2), h3), inv_sqrt_hd);
         }
+        if (whole) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            *dst = sc[j];
+            dst += ld;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (b < __shfl_sync(0xffffffffu, my_n, c * 4 + j)) *dst = sc[j];
+            dst += ld;
+          }
+        }
+        if (c < 7) tmem_wait_ld(vn);
       }
       tc_fence_before();
       __syncwarp();

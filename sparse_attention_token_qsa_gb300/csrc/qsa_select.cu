@@ -80,6 +80,13 @@ __device__ __forceinline__ uint32_t order_key(float s) {
   return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
+// The float whose order key is k (for finite keys): key >= k exactly when the
+// score >= key_to_float(k), since the key is monotone in the score and -0.0
+// compares equal to +0.0 on both sides.
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -251,7 +258,7 @@ __device__ __forceinline__ void warp_find_bin(const uint32_t *H, int nb, uint32_
   above = __shfl_sync(0xffffffffu, ma, src);
 }
 
-template <int NT>
+template <int NT, bool CACHE>
 __global__ void __launch_bounds__(NT, NT == 256 ? 5 : 2)
 select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_t *__restrict__ pos,
               int32_t tokens, int32_t keep_max, uint8_t *__restrict__ mask, int32_t *status,
@@ -289,7 +296,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   const int32_t b1 = min(n, b0 + per);
   const int32_t cnt = b1 - b0;
   const float *srow = scores + (int64_t)row * score_cols + b0;
-  const int32_t cached = min(cnt, cap);
+  const int32_t cached = CACHE ? min(cnt, cap) : 0;
 
   for (int i = tid; i < 4096 + 256 + 256 + 16; i += NT) (&S.hist0[0])[i] = 0u;
   if (tid == 0) {
@@ -316,21 +323,37 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       for (int u = 0; u < kLoadsInFlight; ++u) {
         const int32_t qd = qb + u * NT + lane;
         if (qd >= nq) continue;  // per lane: nothing below needs the whole warp
-        const uint32_t kq[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z),
-                                order_key(v[u].w)};
-        if (4 * qd + 3 < cached) {  // one 16-byte store per quad
-          *reinterpret_cast<uint4 *>(keys_s + 4 * qd) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
-        }
         const int ne = min(4, cnt - 4 * qd);  // keys of this quad in the slice
+        if constexpr (CACHE) {
+          const uint32_t kq[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z),
+                                  order_key(v[u].w)};
+          if (4 * qd + 3 < cached) {  // one 16-byte store per quad
+            *reinterpret_cast<uint4 *>(keys_s + 4 * qd) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+          } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (ne == 4 || e < ne) {  // whole quads need no per-key test
-            zeros += kq[e] == kZeroKey ? 1u : 0u;
-            if (kq[e] != kZeroKey) atomicAdd(&S.hist0[kq[e] >> 20], 1u);
+            for (int e = 0; e < 4; ++e)
+              if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (ne == 4 || e < ne) {  // whole quads need no per-key test
+              zeros += kq[e] == kZeroKey ? 1u : 0u;
+              if (kq[e] != kZeroKey) atomicAdd(&S.hist0[kq[e] >> 20], 1u);
+            }
+          }
+        } else {
+          // no copy to keep: zeros of either sign are found on the raw bits,
+          // and no other key needs the -0.0 fold
+          const uint32_t uq[4] = {__float_as_uint(v[u].x), __float_as_uint(v[u].y),
+                                  __float_as_uint(v[u].z), __float_as_uint(v[u].w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (ne == 4 || e < ne) {
+              const bool z = (uq[e] << 1) == 0u;
+              zeros += z ? 1u : 0u;
+              const uint32_t key = uq[e] ^ ((uint32_t)((int32_t)uq[e] >> 31) | 0x80000000u);
+              if (!z) atomicAdd(&S.hist0[key >> 20], 1u);
+            }
           }
         }
       }
@@ -415,35 +438,51 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         const bool m16 = (rbm & 15u) == 0, m4 = (rbm & 3u) == 0;
         // B0 < 0xFF8 (a finite key's bin), so the upper edge does not wrap
         const uint32_t bin_lo = B0 << 20, bin_hi = (B0 + 1u) << 20;
+        const float t_lo = key_to_float(bin_lo), t_hi = key_to_float(bin_hi);
         for (int32_t i = 4 * tid; i < cnt; i += 4 * NT) {
-          uint32_t k[4];
-          if (i + 3 < cached) {  // one 16-byte shared load
-            const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
-            k[0] = kv.x;
-            k[1] = kv.y;
-            k[2] = kv.z;
-            k[3] = kv.w;
-          } else if (i >= cached && i + 3 < cnt) {  // not cached: one 16-byte load (L2)
-            const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + i));
-            k[0] = order_key(f.x);
-            k[1] = order_key(f.y);
-            k[2] = order_key(f.z);
-            k[3] = order_key(f.w);
-          } else {
+          uint32_t k[4];  // order keys (cached), else raw score bits
+          if constexpr (CACHE) {
+            if (i + 3 < cached) {  // one 16-byte shared load
+              const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
+              k[0] = kv.x;
+              k[1] = kv.y;
+              k[2] = kv.z;
+              k[3] = kv.w;
+            } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              k[e] = (i + e < cnt) ? (i + e < cached ? keys_s[i + e] : order_key(__ldg(srow + i + e)))
-                                   : 0u;
+              for (int e = 0; e < 4; ++e)
+                k[e] = (i + e < cnt) ? (i + e < cached ? keys_s[i + e] : order_key(__ldg(srow + i + e)))
+                                     : 0u;
+            }
+          } else {
+            if (i + 3 < cnt) {  // one 16-byte load (L2)
+              const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + i));
+              k[0] = __float_as_uint(f.x);
+              k[1] = __float_as_uint(f.y);
+              k[2] = __float_as_uint(f.z);
+              k[3] = __float_as_uint(f.w);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) k[e] = (i + e < cnt) ? __float_as_uint(__ldg(srow + i + e)) : 0u;
+            }
           }
           const int mq = min(4, cnt - i);
-          // whole keys against the bin's edges: >= hi kept, [lo, hi) candidates
+          // against the bin's edges (keys, or raw scores against the edges'
+          // floats): >= hi kept, [lo, hi) candidates
           uint32_t bits = 0, w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const bool in = mq == 4 || e < mq;
-            const bool kp = k[e] >= bin_hi;
+            bool kp, lo;
+            if constexpr (CACHE) {
+              kp = k[e] >= bin_hi;
+              lo = k[e] >= bin_lo;
+            } else {
+              kp = __uint_as_float(k[e]) >= t_hi;
+              lo = __uint_as_float(k[e]) >= t_lo;
+            }
             w[e] = (in && kp) ? 0x01010101u : 0u;
-            bits |= (in && !kp && k[e] >= bin_lo) ? (1u << e) : 0u;
+            bits |= (in && !kp && lo) ? (1u << e) : 0u;
           }
           if (mq == 4 && m16) {
             *reinterpret_cast<uint4 *>(mrow + 4 * ((int64_t)b0 + i)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -457,7 +496,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               if (bits & (1u << e)) {
-                cand_s[at] = k[e];
+                cand_s[at] = CACHE ? k[e] : order_key(__uint_as_float(k[e]));
                 cand_li[at] = (uint16_t)(i + e);
                 ++at;
               }
@@ -727,7 +766,7 @@ static size_t select_smem_bytes(int32_t cap) {
 static int max_cluster_size() {
   if (g_max_cluster >= 0) return g_max_cluster;
   int best = 1;
-  for (auto fn : {select_kernel<512>, select_kernel<256>}) {
+  for (auto fn : {select_kernel<512, true>, select_kernel<256, false>}) {
     cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)select_smem_bytes(kSelCapMax));
@@ -745,7 +784,7 @@ static int max_cluster_size() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, select_kernel<512>, &cfg) == cudaSuccess && n > 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, select_kernel<512, true>, &cfg) == cudaSuccess && n > 0) {
       best = c;
       break;
     }
@@ -796,10 +835,10 @@ cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t
 
   const size_t smem = select_smem_bytes(cap);
   if (narrow)
-    return launch_dependent(select_kernel<256>, dim3((unsigned)ctas), dim3(256), smem, stream,
+    return launch_dependent(select_kernel<256, false>, dim3((unsigned)ctas), dim3(256), smem, stream,
                             (unsigned)C, scores, score_cols, pos, tokens, keep_max, mask, status,
                             (int32_t)C, cap);
-  return launch_dependent(select_kernel<512>, dim3((unsigned)ctas), dim3(512), smem, stream,
+  return launch_dependent(select_kernel<512, true>, dim3((unsigned)ctas), dim3(512), smem, stream,
                           (unsigned)C, scores, score_cols, pos, tokens, keep_max, mask, status,
                           (int32_t)C, cap);
 }

@@ -8,14 +8,19 @@
 // metrale layers/qsa.rs decode_select (qsa_qprep then qsa_score over the
 // complete blocks) is the decode use: one row streams every block key once.
 //
-// Design: every CTA prepares its row's four heads in shared memory (1 KiB read,
-// redundant across the row's CTAs but L2-resident), then 8-lane groups stream
-// block keys: lane g of a group owns dims {8(8j+g)+e : j<2, e<8}, so one
-// 16-byte load per lane per j makes each warp read 4 whole 256-byte keys per
-// pair of instructions.  The 4 head partial dots are reduce-scattered over
-// the 8 lanes (4 shuffles) and gathered to lane 0 (3 shuffles), which applies
-// relu, sums heads in order 0..3 and scales.  HBM traffic: 256 B of key read +
-// 4 B of score written per (row, block).
+// Design: a CTA owns a contiguous range of one row's blocks, whose keys are
+// contiguous in memory.  One thread streams them into shared memory with the
+// bulk-copy engine (cp.async.bulk, 1-D TMA), 128 keys (32 KiB) per stage in a
+// ring of three, each stage completing an mbarrier; the first copies are in
+// flight while the CTA prepares the row's four heads (1 KiB read, redundant
+// across the row's CTAs but L2-resident).  8-lane groups then reduce keys
+// from shared memory: lane g of a group owns dims {8(8j+g)+e : j<2, e<8}, so
+// a quarter-warp's 16-byte loads cover one 128-byte run of a key (no bank
+// conflicts).  The 4 head partial dots are reduce-scattered over the 8 lanes
+// (4 shuffles) and gathered to lane 0 (3 shuffles), which applies relu, sums
+// heads in order 0..3 and scales.  HBM traffic: 256 B of key read + 4 B of
+// score written per (row, block).  Every wait is bounded: on timeout the CTA
+// records QSA_ERR_TIMEOUT, lets its own copies land, and returns.
 #include "qsa_device.cuh"
 #include "qsa_launch.h"
 
@@ -24,7 +29,39 @@ namespace qsa {
 constexpr int kSimtThreads = 256;
 constexpr int kSimtGroups = kSimtThreads / 8;  // 32 groups of 8 lanes
 constexpr int kSimtUnroll = 4;
-constexpr int kSimtBlocksPerIter = kSimtGroups * kSimtUnroll;  // 128
+constexpr int kSimtBlocksPerIter = kSimtGroups * kSimtUnroll;  // 128 keys: one stage
+constexpr int kSimtStages = 3;
+constexpr uint32_t kSimtStageBytes = kSimtBlocksPerIter * kHeadDim * 2;  // 32 KiB
+constexpr long long kSimtSpinLimit = 4000000000LL;                      // ~2 s of SM clock
+
+struct SimtSmem {
+  float q_s[kHeads][kHeadDim];
+  uint64_t full[kSimtStages];
+};
+constexpr size_t kSimtStageOff = (sizeof(SimtSmem) + 127) & ~size_t(127);
+constexpr size_t kSimtSmemBytes = kSimtStageOff + kSimtStages * (size_t)kSimtStageBytes;
+
+__device__ __forceinline__ uint32_t simt_smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Bounded wait on an mbarrier phase (the thread sleeps in hardware between
+// tests).  Returns false once the limit is reached.
+__device__ __forceinline__ bool simt_wait(uint32_t mbar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(mbar), "r"(parity), "r"(20000u)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > kSimtSpinLimit) return false;
+  }
+}
 
 __device__ __forceinline__ void prep_query_heads(const ScoreArgs &a, int row, int p,
                                                  float (*q_s)[kHeadDim]) {
@@ -51,7 +88,9 @@ __device__ __forceinline__ void prep_query_heads(const ScoreArgs &a, int row, in
 
 __global__ void __launch_bounds__(kSimtThreads)
 score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
-  __shared__ float q_s[kHeads][kHeadDim];
+  extern __shared__ __align__(128) uint8_t simt_smem_raw[];
+  SimtSmem &S = *reinterpret_cast<SimtSmem *>(simt_smem_raw);
+  uint8_t *stages = simt_smem_raw + kSimtStageOff;
   grid_dependency_sync();
   const int row = blockIdx.x;
   const int p = a.pos[row];
@@ -64,39 +103,66 @@ score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
   const int c0 = blockIdx.y * blocks_per_cta;
   if (c0 >= n) return;
   const int c1 = min(n, c0 + blocks_per_cta);
-
-  const int gi = threadIdx.x >> 3;
-  const int g = threadIdx.x & 7;
+  const int n_it = (c1 - c0 + kSimtBlocksPerIter - 1) / kSimtBlocksPerIter;
   const uint16_t *kb = a.block_keys + (a.key_base ? a.key_base[row] : 0) * kHeadDim;
-  uint4 kv[kSimtUnroll][2];
-  auto load_keys = [&](int base) {
-#pragma unroll
-    for (int u = 0; u < kSimtUnroll; ++u) {
-      const int b = base + u * kSimtGroups + gi;
-      const int bc = b < c1 ? b : c0;
-      const uint16_t *kp = kb + (int64_t)bc * kHeadDim + 8 * g;
-      kv[u][0] = ldg_nc_v4(kp);
-      kv[u][1] = ldg_nc_v4(kp + 64);
-    }
+  const int tid = threadIdx.x;
+
+  // stage `it` of this CTA's range: keys [c0 + 128 it, ...) into ring slot it % 3
+  auto issue = [&](int it) {
+    const int base = c0 + it * kSimtBlocksPerIter;
+    const uint32_t bytes = (uint32_t)min(kSimtBlocksPerIter, c1 - base) * (kHeadDim * 2);
+    const uint32_t mb = simt_smem_u32(&S.full[it % kSimtStages]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(simt_smem_u32(stages + (size_t)(it % kSimtStages) * kSimtStageBytes)),
+        "l"(kb + (int64_t)base * kHeadDim), "r"(bytes), "r"(mb)
+        : "memory");
   };
-  // the first keys are in flight while the query heads are prepared
-  load_keys(c0);
-  prep_query_heads(a, row, p, q_s);
+  if (tid == 0) {
+    for (int s = 0; s < kSimtStages; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(simt_smem_u32(&S.full[s]))
+                   : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int it = 0; it < min(kSimtStages, n_it); ++it) issue(it);
+  }
+  // the first stages are in flight while the query heads are prepared
+  prep_query_heads(a, row, p, S.q_s);
   __syncthreads();
 
+  const int gi = tid >> 3;
+  const int g = tid & 7;
   float qr[kHeads][2][8];
 #pragma unroll
   for (int h = 0; h < kHeads; ++h)
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) qr[h][j][e] = q_s[h][8 * (8 * j + g) + e];
+      for (int e = 0; e < 8; ++e) qr[h][j][e] = S.q_s[h][8 * (8 * j + g) + e];
 
   float *srow = a.scores + (int64_t)row * a.score_cols;
   const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
 
-  for (int base = c0; base < c1; base += kSimtBlocksPerIter) {
-    if (base != c0) load_keys(base);
+  int it = 0;
+  bool failed = false;
+  for (; it < n_it; ++it) {
+    const int s = it % kSimtStages;
+    const bool ok = simt_wait(simt_smem_u32(&S.full[s]), (uint32_t)(it / kSimtStages) & 1u);
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    const int base = c0 + it * kSimtBlocksPerIter;
+    const uint8_t *st = stages + (size_t)s * kSimtStageBytes;
+    uint4 kv[kSimtUnroll][2];
+#pragma unroll
+    for (int u = 0; u < kSimtUnroll; ++u) {
+      const int lb = u * kSimtGroups + gi;  // key within the stage
+      const uint8_t *kp = st + (size_t)(base + lb < c1 ? lb : 0) * (kHeadDim * 2) + 16 * g;
+      kv[u][0] = *reinterpret_cast<const uint4 *>(kp);
+      kv[u][1] = *reinterpret_cast<const uint4 *>(kp + 128);
+    }
 #pragma unroll
     for (int u = 0; u < kSimtUnroll; ++u) {
       float acc[kHeads] = {0.f, 0.f, 0.f, 0.f};
@@ -129,12 +195,28 @@ score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
       const int b = base + u * kSimtGroups + gi;
       if (g == 0 && b < c1) srow[b] = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(r, r1), r2), r3), inv_sqrt_hd);
     }
+    __syncthreads();  // every warp is done with slot s
+    if (tid == 0 && it + kSimtStages < n_it) issue(it + kSimtStages);
+  }
+  if (failed && tid == 0) {
+    report_error(a.status, kErrTimeout, row);
+    // let this CTA's own copies land before its shared memory is released
+    for (int k = it; k < min(n_it, it + kSimtStages); ++k)
+      simt_wait(simt_smem_u32(&S.full[k % kSimtStages]), (uint32_t)(k / kSimtStages) & 1u);
   }
 }
 
 cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream) {
   const int64_t n_max = (int64_t)a.tokens / kRatio;
   if (n_max == 0) return cudaSuccess;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(score_simt_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSimtSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   const int64_t iters = (n_max + kSimtBlocksPerIter - 1) / kSimtBlocksPerIter;
   // enough CTAs to cover ~8 per SM, each streaming at least 128 blocks
   int64_t k = ((int64_t)a.n_rows * iters) / (8 * 152);
@@ -142,7 +224,8 @@ cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream) {
   while ((iters + k - 1) / k > 65535) ++k;
   const int32_t bpc = (int32_t)(k * kSimtBlocksPerIter);
   dim3 grid((unsigned)a.n_rows, (unsigned)((n_max + bpc - 1) / bpc));
-  return launch_dependent(score_simt_kernel, grid, dim3(kSimtThreads), 0, stream, 1u, a, bpc);
+  return launch_dependent(score_simt_kernel, grid, dim3(kSimtThreads), kSimtSmemBytes, stream, 1u,
+                          a, bpc);
 }
 
 }  // namespace qsa

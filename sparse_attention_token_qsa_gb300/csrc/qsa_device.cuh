@@ -114,18 +114,19 @@ __device__ __forceinline__ uint4 norm_rope_16(const float (&x)[8], const uint4 &
 
   const uint32_t cv[4] = {c8.x, c8.y, c8.z, c8.w};
   const uint32_t sv[4] = {s8.x, s8.y, s8.z, s8.w};
+  // out_i = x_i c - x_{i+32} s (lanes 0-3), out_{i+32} = x_{i+32} c + x_i s
+  // (lanes 4-7), unrotated dims pass (lanes 8-15); branch-free, with a - b
+  // taken as a + (-b), which IEEE defines to be the same operation
+  const bool rot = g < 8, neg = g < 4;
   uint32_t o[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const float c = (e & 1) ? hi_bf16(cv[e >> 1]) : lo_bf16(cv[e >> 1]);
     const float s = (e & 1) ? hi_bf16(sv[e >> 1]) : lo_bf16(sv[e >> 1]);
-    if (g < 4) {  // out_i = x_i c - x_{i+32} s
-      o[e] = f32_to_bf16(__fsub_rn(round_bf16(__fmul_rn(n[e], c)), round_bf16(__fmul_rn(part[e], s))));
-    } else if (g < 8) {  // out_{i+32} = x_{i+32} c + x_i s
-      o[e] = f32_to_bf16(__fadd_rn(round_bf16(__fmul_rn(n[e], c)), round_bf16(__fmul_rn(part[e], s))));
-    } else {
-      o[e] = f32_to_bf16(n[e]);
-    }
+    const float t1 = round_bf16(__fmul_rn(n[e], c));
+    const float t2 = round_bf16(__fmul_rn(part[e], s));
+    const float r = __fadd_rn(t1, neg ? -t2 : t2);
+    o[e] = f32_to_bf16(rot ? r : n[e]);
   }
   return make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
                     pack_bf16(o[6], o[7]));

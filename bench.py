@@ -205,6 +205,8 @@ class DecodeWorkload:
             self.scores.append(torch.zeros((1, N_BLOCKS), dtype=torch.float32, device=device))
             self.mask.append(torch.zeros((1, TOKENS), dtype=torch.uint8, device=device))
         self.status = qsa.new_status(device)
+        # zeroed workspace of the fused decode entry (every call leaves it zero)
+        self.dws = qsa.new_decode_workspace(1, TOKENS, device)
         # the cache holds every block completed before the decode window
         for r in range(n_seq):
             qsa.qsa_pool_blocks(self.keys[r], 128, 0, FIRST_POS // 4, self.kw, self.cos, self.sin,
@@ -235,23 +237,27 @@ class DecodeWorkload:
         self.qsa.qsa_select_mask(self.scores[seq], N_BLOCKS, self.positions[j:j + 1], 1, TOKENS,
                                  BUDGET, self.mask[seq], self.status)
 
-    def step(self, k):
+    def step_three(self, k):
+        """One step through the three single-stage entry points."""
         self.pool(k)
         self.score(k)
         self.select(k)
 
-    def fused_step(self, k, q_src=None, pos_src=None):
-        """The public entry point for one step (qsa_index_select)."""
+    def step(self, k, q_src=None, pos_src=None, pool=True):
+        """One decode step through its public entry point (qsa_decode_index_select):
+        pool the block the token completes, then score and select in one launch."""
         seq, j, p = self.step_params(k)
-        completes = (p + 1) % 4 == 0
+        completes = pool and (p + 1) % 4 == 0
         b = (p + 1) // 4 - 1
-        self.qsa.qsa_index_select(self.keys[seq][4 * b:] if completes else self.keys[seq], 128,
-                                  b if completes else 0, 1 if completes else 0, self.kw,
-                                  self.q[seq][j:j + 1] if q_src is None else q_src, 512,
-                                  self.positions[j:j + 1] if pos_src is None else pos_src, 1,
-                                  TOKENS, self.qw, self.cos, self.sin, TOKENS, EPS, BUDGET,
-                                  self.cache[seq], self.scores[seq], N_BLOCKS, self.mask[seq],
-                                  self.status)
+        self.qsa.qsa_decode_index_select(
+            self.keys[seq][4 * b:] if completes else self.keys[seq], 128, b if completes else 0,
+            1 if completes else 0, self.kw, self.q[seq][j:j + 1] if q_src is None else q_src, 512,
+            self.positions[j:j + 1] if pos_src is None else pos_src, 1, TOKENS, self.qw, self.cos,
+            self.sin, TOKENS, EPS, BUDGET, self.cache[seq], self.scores[seq], N_BLOCKS,
+            self.mask[seq], self.status, self.dws)
+
+    def fused_only(self, k):
+        self.step(k, pool=False)
 
 
 def capture_graphs(torch, fn, steps, chunk=256):
@@ -359,6 +365,7 @@ def run_ours(args, rank, world, device):
     # warm-up (eager): first calls also set kernel attributes outside any capture
     for k in range(max(args.warmup, 3)):
         wl.step(k)
+        wl.step_three(k)
     torch.cuda.synchronize()
     code, row = qsa.qsa_read_status(wl.status)
     assert code == 0, f"device status {code} row {row}"
@@ -390,9 +397,15 @@ def run_ours(args, rank, world, device):
     code, row = qsa.qsa_read_status(wl.status)
     assert code == 0, f"device status {code} row {row}"
 
+    # the same steps through the three single-stage entry points
+    g3 = capture_graphs(torch, wl.step_three, steps[:min(K, 4096)])
+    three_us = time_graphs(torch, g3) / min(K, 4096) * 1000.0
+
     # per-kernel durations: the same launches, one kernel at a time, CUDA events
     kern = {}
     for name, fn, bytes_per_launch, src in (
+            ("decode_fused", wl.fused_only, SCORE_BYTES_PER_BLOCK * N_BLOCKS + TOKENS,
+             "qsa_decode.cu"),
             ("score", wl.score, SCORE_BYTES_PER_BLOCK * N_BLOCKS, "qsa_score_simt.cu"),
             ("select", wl.select, SELECT_BYTES_PER_BLOCK * N_BLOCKS + TOKENS, "qsa_select.cu")):
         gk = capture_graphs(torch, fn, steps[:min(K, 4096)])
@@ -402,7 +415,7 @@ def run_ours(args, rank, world, device):
     gk = capture_graphs(torch, wl.pool, pool_steps)
     kern["pool"] = {"us": time_graphs(torch, gk) / max(1, len(pool_steps)) * 1000.0,
                     "bytes": POOL_BYTES_PER_BLOCK, "src": "qsa_pool.cu"}
-    dom = max(("score", "select"), key=lambda n: kern[n]["us"])
+    dom = "decode_fused"
     d = kern[dom]
     achieved = d["bytes"] / (d["us"] * 1e-6) / 1e9
     traffic = recorded_traffic(f"{dom}", "decode64k", d["src"])
@@ -435,7 +448,7 @@ def run_ours(args, rank, world, device):
         q_step.copy_(q_host[j:j + 1], non_blocking=True)
         wl.keys[seq][p:p + 1].copy_(k_host[p:p + 1], non_blocking=True)
         pos_step.copy_(pos_host[j:j + 1], non_blocking=True)
-        wl.fused_step(k, q_src=q_step, pos_src=pos_step)
+        wl.step(k, q_src=q_step, pos_src=pos_step)
         mask_host[i & 1].copy_(wl.mask[seq][0], non_blocking=True)
         stat_host.copy_(wl.status, non_blocking=True)
 
@@ -454,7 +467,8 @@ def run_ours(args, rank, world, device):
     assert int(stat_host[0]) == 0
     e2e = {"value": world * E / (e2e_ms / 1000.0), "unit": "rows/s",
            "h2d_bytes_per_step": 512 * 2 + 128 * 2 + 4, "d2h_bytes_per_step": TOKENS + 8,
-           "steps": E, "path": "qsa_index_select with pinned host buffers, replayed from CUDA graphs",
+           "steps": E,
+           "path": "qsa_decode_index_select with pinned host buffers, replayed from CUDA graphs",
            "eager_value": world * E / (eager_ms / 1000.0)}
 
     secondary = {}
@@ -471,10 +485,13 @@ def run_ours(args, rank, world, device):
         "config": {"workload": WORKLOAD, "tokens": TOKENS, "budget": BUDGET, "rows_per_step": 1,
                    "sequences_rotated": R, "bytes_per_sequence": per_seq_bytes,
                    "l2": "inputs larger than L2 (steps rotate over the sequences)",
-                   "launch": "CUDA graphs of 256 steps; pool+score+select per step",
+                   "launch": "CUDA graphs of 256 steps; per step qsa_decode_index_select: "
+                             "the pool launch when a block completes, then one fused "
+                             "score+select launch",
+                   "three_entry_points_us_per_step": three_us,
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "kernels": kernels, "clocks": clk, "e2e": e2e,
-        "gpu_launches": int(K * 2 + sum(1 for k in steps if (wl.step_params(k)[2] + 1) % 4 == 0)),
+        "gpu_launches": int(K + sum(1 for k in steps if (wl.step_params(k)[2] + 1) % 4 == 0)),
         "secondary": secondary,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -237,6 +237,45 @@ qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t po
                             uint8_t *mask, int32_t *dev_status, void *workspace,
                             int64_t workspace_bytes, void *stream);
 
+/*
+ * Bytes of the workspace qsa_decode_index_select needs: per row, a 4096-bin
+ * histogram, three counters and room for tokens/4 candidates.  -1 for
+ * negative arguments.
+ */
+int64_t qsa_decode_workspace_bytes(int32_t n_rows, int32_t tokens);
+
+/*
+ * The same operation as qsa_index_select (pool the newly complete blocks,
+ * score every row with the streaming scorer, select), for decode-sized row
+ * counts: after the pooling launch, scoring and selection run as ONE
+ * cooperative launch in which each row's scoring CTAs also build the row's
+ * histogram, meet at a bounded grid barrier, write their own blocks' mask
+ * bytes, and the row's last CTA resolves the threshold bin.  Source: metrale
+ * layers/qsa.rs decode_select (score then top-k each decode step), PR #1160
+ * (scores), PR #1178 "Exact semantics" (selection).  Results equal those of
+ * qsa_index_select with the SIMT scorer.  When the rows' CTAs cannot all be
+ * resident at once, the call falls back to the scorer and the selector as two
+ * launches (same results; the workspace is not used).
+ *  arguments   as qsa_index_select, except:
+ *  decode_ws   DEVICE workspace of at least qsa_decode_workspace_bytes(n_rows,
+ *              tokens) bytes, 16-byte aligned, ZERO before the first call.
+ *              Each call that completes leaves it zero again; after a call
+ *              that reported an error on the device it may be left dirty and
+ *              must be zeroed before the next call.  Calls sharing one
+ *              workspace must be stream-ordered.
+ *  Returns QSA_ERR_INVALID_VALUE for a missing, small or unaligned workspace
+ *  (rows and tokens non-zero), or any argument qsa_index_select refuses.
+ */
+qsa_status qsa_decode_index_select(const uint16_t *keys, int64_t key_stride,
+                                   int32_t pool_first_block, int32_t pool_n_blocks,
+                                   const uint16_t *k_norm_w, const uint16_t *q, int64_t q_stride,
+                                   const int32_t *pos, int32_t n_rows, int32_t tokens,
+                                   const uint16_t *q_norm_w, const uint16_t *cos_t,
+                                   const uint16_t *sin_t, int32_t table_rows, float eps,
+                                   int32_t budget, uint16_t *block_keys, float *scores,
+                                   int64_t score_cols, uint8_t *mask, int32_t *dev_status,
+                                   void *decode_ws, int64_t decode_ws_bytes, void *stream);
+
 /* Zero a DEVICE status word (stream-ordered). */
 qsa_status qsa_reset_status(int32_t *dev_status, void *stream);
 

@@ -34,7 +34,8 @@ HEADS, HEAD_DIM, RATIO, ROT_DIM, FUSED_WIDTH = 4, 128, 4, 64, 640
 
 EXPORTED = ("qsa_version", "qsa_status_string", "qsa_rope_tables", "qsa_pool_blocks",
             "qsa_score_rows", "qsa_score_rows_with", "qsa_score_workspace_bytes",
-            "qsa_score_rows_noalloc", "qsa_select_mask", "qsa_index_select", "qsa_reset_status",
+            "qsa_score_rows_noalloc", "qsa_select_mask", "qsa_index_select",
+            "qsa_decode_workspace_bytes", "qsa_decode_index_select", "qsa_reset_status",
             "qsa_read_status")
 
 
@@ -65,6 +66,9 @@ def _load() -> ctypes.CDLL:
         "qsa_select_mask": ([P, i64, P, i32, i32, i32, P, P, P], i32),
         "qsa_index_select": ([P, i64, i32, i32, P, P, i64, P, i32, i32, P, P, P, i32, f32, i32, P, P,
                               i64, P, P, P, i64, P], i32),
+        "qsa_decode_workspace_bytes": ([i32, i32], i64),
+        "qsa_decode_index_select": ([P, i64, i32, i32, P, P, i64, P, i32, i32, P, P, P, i32, f32, i32,
+                                     P, P, i64, P, P, P, i64, P], i32),
         "qsa_reset_status": ([P, P], i32),
         "qsa_read_status": ([P, P, P, P], i32),
     }
@@ -213,6 +217,35 @@ def qsa_index_select(keys, key_stride, pool_first_block, pool_n_blocks, k_norm_w
                                  int(score_cols), _dev(mask, "mask"),
                                  _dev(dev_status, "dev_status"), ws, int(wsb), _stream(stream)),
            "qsa_index_select")
+
+
+def qsa_decode_workspace_bytes(n_rows: int, tokens: int) -> int:
+    return int(_lib.qsa_decode_workspace_bytes(int(n_rows), int(tokens)))
+
+
+def new_decode_workspace(n_rows: int, tokens: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for qsa_decode_index_select (each completed call
+    leaves it zero again)."""
+    n = max(16, qsa_decode_workspace_bytes(n_rows, tokens))
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def qsa_decode_index_select(keys, key_stride, pool_first_block, pool_n_blocks, k_norm_w, q, q_stride,
+                            pos, n_rows, tokens, q_norm_w, cos_t, sin_t, table_rows, eps, budget,
+                            block_keys, scores, score_cols, mask, dev_status, decode_ws,
+                            stream=None) -> None:
+    ws, wsb = _ws(decode_ws)
+    _check(_lib.qsa_decode_index_select(_dev(keys, "keys"), int(key_stride), int(pool_first_block),
+                                        int(pool_n_blocks), _dev(k_norm_w, "k_norm_w"),
+                                        _dev(q, "q"), int(q_stride), _dev(pos, "pos"), int(n_rows),
+                                        int(tokens), _dev(q_norm_w, "q_norm_w"),
+                                        _dev(cos_t, "cos_t"), _dev(sin_t, "sin_t"),
+                                        int(table_rows), float(eps), int(budget),
+                                        _dev(block_keys, "block_keys"), _dev(scores, "scores"),
+                                        int(score_cols), _dev(mask, "mask"),
+                                        _dev(dev_status, "dev_status"), ws, int(wsb),
+                                        _stream(stream)),
+           "qsa_decode_index_select")
 
 
 def qsa_reset_status(dev_status, stream=None) -> None:

@@ -229,6 +229,53 @@ qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t po
                                       dev_status, s));
 }
 
+int64_t qsa_decode_workspace_bytes(int32_t n_rows, int32_t tokens) {
+  if (n_rows < 0 || tokens < 0) return -1;
+  return (int64_t)n_rows * qsa::decode_row_ws_bytes(tokens);
+}
+
+qsa_status qsa_decode_index_select(const uint16_t *keys, int64_t key_stride,
+                                   int32_t pool_first_block, int32_t pool_n_blocks,
+                                   const uint16_t *k_norm_w, const uint16_t *q, int64_t q_stride,
+                                   const int32_t *pos, int32_t n_rows, int32_t tokens,
+                                   const uint16_t *q_norm_w, const uint16_t *cos_t,
+                                   const uint16_t *sin_t, int32_t table_rows, float eps,
+                                   int32_t budget, uint16_t *block_keys, float *scores,
+                                   int64_t score_cols, uint8_t *mask, int32_t *dev_status,
+                                   void *decode_ws, int64_t decode_ws_bytes, void *stream) {
+  qsa_status st = check_pool_args(keys, key_stride, pool_first_block, pool_n_blocks, k_norm_w,
+                                  cos_t, sin_t, table_rows, eps, block_keys);
+  if (st != QSA_OK) return st;
+  st = check_score_args(q, q_stride, pos, n_rows, tokens, q_norm_w, cos_t, sin_t, table_rows, eps,
+                        block_keys, scores, score_cols);
+  if (st != QSA_OK) return st;
+  st = check_select_args(scores, score_cols, pos, n_rows, tokens, budget, mask);
+  if (st != QSA_OK) return st;
+  const int64_t need = qsa_decode_workspace_bytes(n_rows, tokens);
+  if (n_rows > 0 && tokens > 0 &&
+      (decode_ws == nullptr || decode_ws_bytes < need ||
+       (reinterpret_cast<uintptr_t>(decode_ws) & 15u) != 0))
+    return QSA_ERR_INVALID_VALUE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (pool_n_blocks > 0) {
+    st = from_cuda(qsa::launch_pool_blocks(keys, key_stride, pool_first_block, pool_n_blocks,
+                                           k_norm_w, cos_t, sin_t, eps, block_keys, s));
+    if (st != QSA_OK) return st;
+  }
+  if (n_rows == 0 || tokens == 0) return QSA_OK;
+  qsa::ScoreArgs a = {q,        q_stride, pos,        nullptr,    n_rows, tokens, q_norm_w,
+                      cos_t,    sin_t,    eps,        block_keys, nullptr, scores, score_cols,
+                      dev_status};
+  bool launched = false;
+  st = from_cuda(qsa::launch_decode_fused(a, budget, mask, decode_ws, s, &launched));
+  if (st != QSA_OK || launched) return st;
+  // more rows than can be co-resident: the scorer and the selector, in turn
+  st = from_cuda(qsa::launch_score_simt(a, s));
+  if (st != QSA_OK) return st;
+  return from_cuda(qsa::launch_select(scores, score_cols, pos, n_rows, tokens, budget, mask,
+                                      dev_status, s));
+}
+
 qsa_status qsa_reset_status(int32_t *dev_status, void *stream) {
   if (!dev_status) return QSA_ERR_INVALID_VALUE;
   return from_cuda(cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), (cudaStream_t)stream));

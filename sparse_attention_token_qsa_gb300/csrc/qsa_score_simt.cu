@@ -8,83 +8,16 @@
 // metrale layers/qsa.rs decode_select (qsa_qprep then qsa_score over the
 // complete blocks) is the decode use: one row streams every block key once.
 //
-// Design: a CTA owns a contiguous range of one row's blocks, whose keys are
-// contiguous in memory.  One thread streams them into shared memory with the
-// bulk-copy engine (cp.async.bulk, 1-D TMA), 128 keys (32 KiB) per stage in a
-// ring of three, each stage completing an mbarrier; the first copies are in
-// flight while the CTA prepares the row's four heads (1 KiB read, redundant
-// across the row's CTAs but L2-resident).  8-lane groups then reduce keys
-// from shared memory: lane g of a group owns dims {8(8j+g)+e : j<2, e<8}, so
-// a quarter-warp's 16-byte loads cover one 128-byte run of a key (no bank
-// conflicts).  The 4 head partial dots are reduce-scattered over the 8 lanes
-// (4 shuffles) and gathered to lane 0 (3 shuffles), which applies relu, sums
-// heads in order 0..3 and scales.  HBM traffic: 256 B of key read + 4 B of
-// score written per (row, block).  Every wait is bounded: on timeout the CTA
-// records QSA_ERR_TIMEOUT, lets its own copies land, and returns.
-#include "qsa_device.cuh"
-#include "qsa_launch.h"
+// The kernel splits each row's visible blocks into contiguous ranges, one per
+// CTA, and streams them through the shared core (bulk copies into a shared
+// memory ring, 8-lane dot products, relu and head sum).  HBM traffic: 256 B of
+// key read + 4 B of score written per (row, block).  On a timed-out wait the
+// CTA records QSA_ERR_TIMEOUT once its own copies have landed.
+#include "qsa_score_simt.cuh"
 
 namespace qsa {
 
-constexpr int kSimtThreads = 256;
-constexpr int kSimtGroups = kSimtThreads / 8;  // 32 groups of 8 lanes
-constexpr int kSimtUnroll = 4;
-constexpr int kSimtBlocksPerIter = kSimtGroups * kSimtUnroll;  // 128 keys: one stage
-constexpr int kSimtStages = 3;
-constexpr uint32_t kSimtStageBytes = kSimtBlocksPerIter * kHeadDim * 2;  // 32 KiB
-constexpr long long kSimtSpinLimit = 4000000000LL;                      // ~2 s of SM clock
-
-struct SimtSmem {
-  float q_s[kHeads][kHeadDim];
-  uint64_t full[kSimtStages];
-};
-constexpr size_t kSimtStageOff = (sizeof(SimtSmem) + 127) & ~size_t(127);
-constexpr size_t kSimtSmemBytes = kSimtStageOff + kSimtStages * (size_t)kSimtStageBytes;
-
-__device__ __forceinline__ uint32_t simt_smem_u32(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-// Bounded wait on an mbarrier phase (the thread sleeps in hardware between
-// tests).  Returns false once the limit is reached.
-__device__ __forceinline__ bool simt_wait(uint32_t mbar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (true) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(mbar), "r"(parity), "r"(20000u)
-        : "memory");
-    if (ok) return true;
-    if (clock64() - t0 > kSimtSpinLimit) return false;
-  }
-}
-
-__device__ __forceinline__ void prep_query_heads(const ScoreArgs &a, int row, int p,
-                                                 float (*q_s)[kHeadDim]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < 2) {  // 4 half-warps = 4 heads
-    const int h = warp * 2 + (lane >> 4);
-    const int g = lane & 15;
-    const uint4 v = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * g);
-    const uint4 w8 = ldg_nc_v4(a.q_norm_w + 8 * g);
-    uint4 c8 = make_uint4(0, 0, 0, 0), s8 = make_uint4(0, 0, 0, 0);
-    if (g < 8) {
-      c8 = ldg_nc_v4(a.cos_t + (int64_t)p * kRot + 8 * g);
-      s8 = ldg_nc_v4(a.sin_t + (int64_t)p * kRot + 8 * g);
-    }
-    float x[8];
-    unpack8(v, x);
-    const uint4 o = norm_rope_16(x, w8, c8, s8, a.eps, g);
-    float y[8];
-    unpack8(o, y);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) q_s[h][8 * g + e] = y[e];
-  }
-}
+constexpr size_t kSimtSmemBytes = kSimtStageOff + kSimtRingBytes;
 
 __global__ void __launch_bounds__(kSimtThreads)
 score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
@@ -103,107 +36,8 @@ score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
   const int c0 = blockIdx.y * blocks_per_cta;
   if (c0 >= n) return;
   const int c1 = min(n, c0 + blocks_per_cta);
-  const int n_it = (c1 - c0 + kSimtBlocksPerIter - 1) / kSimtBlocksPerIter;
-  const uint16_t *kb = a.block_keys + (a.key_base ? a.key_base[row] : 0) * kHeadDim;
-  const int tid = threadIdx.x;
-
-  // stage `it` of this CTA's range: keys [c0 + 128 it, ...) into ring slot it % 3
-  auto issue = [&](int it) {
-    const int base = c0 + it * kSimtBlocksPerIter;
-    const uint32_t bytes = (uint32_t)min(kSimtBlocksPerIter, c1 - base) * (kHeadDim * 2);
-    const uint32_t mb = simt_smem_u32(&S.full[it % kSimtStages]);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(bytes)
-                 : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(simt_smem_u32(stages + (size_t)(it % kSimtStages) * kSimtStageBytes)),
-        "l"(kb + (int64_t)base * kHeadDim), "r"(bytes), "r"(mb)
-        : "memory");
-  };
-  if (tid == 0) {
-    for (int s = 0; s < kSimtStages; ++s)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(simt_smem_u32(&S.full[s]))
-                   : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    for (int it = 0; it < min(kSimtStages, n_it); ++it) issue(it);
-  }
-  // the first stages are in flight while the query heads are prepared
-  prep_query_heads(a, row, p, S.q_s);
-  __syncthreads();
-
-  const int gi = tid >> 3;
-  const int g = tid & 7;
-  float qr[kHeads][2][8];
-#pragma unroll
-  for (int h = 0; h < kHeads; ++h)
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qr[h][j][e] = S.q_s[h][8 * (8 * j + g) + e];
-
-  float *srow = a.scores + (int64_t)row * a.score_cols;
-  const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
-
-  int it = 0;
-  bool failed = false;
-  for (; it < n_it; ++it) {
-    const int s = it % kSimtStages;
-    const bool ok = simt_wait(simt_smem_u32(&S.full[s]), (uint32_t)(it / kSimtStages) & 1u);
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    const int base = c0 + it * kSimtBlocksPerIter;
-    const uint8_t *st = stages + (size_t)s * kSimtStageBytes;
-    uint4 kv[kSimtUnroll][2];
-#pragma unroll
-    for (int u = 0; u < kSimtUnroll; ++u) {
-      const int lb = u * kSimtGroups + gi;  // key within the stage
-      const uint8_t *kp = st + (size_t)(base + lb < c1 ? lb : 0) * (kHeadDim * 2) + 16 * g;
-      kv[u][0] = *reinterpret_cast<const uint4 *>(kp);
-      kv[u][1] = *reinterpret_cast<const uint4 *>(kp + 128);
-    }
-#pragma unroll
-    for (int u = 0; u < kSimtUnroll; ++u) {
-      float acc[kHeads] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float k[8];
-        unpack8(kv[u][j], k);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-#pragma unroll
-          for (int h = 0; h < kHeads; ++h) acc[h] = fmaf(qr[h][j][e], k[e], acc[h]);
-      }
-      // reduce-scatter the 4 head sums over the 8 lanes of the group
-      const bool up4 = g & 4;
-      float keep0 = up4 ? acc[2] : acc[0];
-      float keep1 = up4 ? acc[3] : acc[1];
-      const float send0 = up4 ? acc[0] : acc[2];
-      const float send1 = up4 ? acc[1] : acc[3];
-      keep0 += __shfl_xor_sync(0xffffffffu, send0, 4);
-      keep1 += __shfl_xor_sync(0xffffffffu, send1, 4);
-      const bool up2 = g & 2;
-      float d = up2 ? keep1 : keep0;
-      d += __shfl_xor_sync(0xffffffffu, up2 ? keep0 : keep1, 2);
-      d += __shfl_xor_sync(0xffffffffu, d, 1);
-      // lanes 0,2,4,6 of the group now hold heads 0,1,2,3
-      const float r = (d < 0.f) ? 0.f : d;  // relu as a comparison: NaN stays NaN
-      const float r1 = __shfl_down_sync(0xffffffffu, r, 2);
-      const float r2 = __shfl_down_sync(0xffffffffu, r, 4);
-      const float r3 = __shfl_down_sync(0xffffffffu, r, 6);
-      const int b = base + u * kSimtGroups + gi;
-      if (g == 0 && b < c1) srow[b] = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(r, r1), r2), r3), inv_sqrt_hd);
-    }
-    __syncthreads();  // every warp is done with slot s
-    if (tid == 0 && it + kSimtStages < n_it) issue(it + kSimtStages);
-  }
-  if (failed && tid == 0) {
+  if (!simt_score_blocks(a, row, p, c0, c1, S, stages, [](int, float) {}) && threadIdx.x == 0)
     report_error(a.status, kErrTimeout, row);
-    // let this CTA's own copies land before its shared memory is released
-    for (int k = it; k < min(n_it, it + kSimtStages); ++k)
-      simt_wait(simt_smem_u32(&S.full[k % kSimtStages]), (uint32_t)(k / kSimtStages) & 1u);
-  }
 }
 
 cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream) {

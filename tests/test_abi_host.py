@@ -134,6 +134,37 @@ def test_index_select_refusals(lib):
     assert call(wsb=-5) == 1
 
 
+def test_decode_workspace_bytes(lib):
+    row = 16640 + 8 * (65536 // 4)          # histogram + counters, then the candidates
+    assert lib.qsa_decode_workspace_bytes(1, 65536) == (row + 255) // 256 * 256
+    assert lib.qsa_decode_workspace_bytes(3, 65536) == 3 * ((row + 255) // 256 * 256)
+    assert lib.qsa_decode_workspace_bytes(2, 4099) % 256 == 0
+    assert lib.qsa_decode_workspace_bytes(0, 65536) == 0
+    assert lib.qsa_decode_workspace_bytes(-1, 65536) == -1
+
+
+def test_decode_index_select_refusals(lib):
+    """Decided on the host before any launch: the pointers are never read."""
+    def call(**kw):
+        a = dict(keys=A, ks=640, f=0, nb=0, kw=A, q=A, qs=640, pos=B, n=2, tokens=4096, qw=A,
+                 cos=A, sin=A, rows=4096, eps=1e-6, budget=2048, bk=A, sc=A, cols=1024, mask=A,
+                 st=B, ws=0, wsb=0)
+        a.update(kw)
+        return lib.qsa_decode_index_select(P(a["keys"]), a["ks"], a["f"], a["nb"], P(a["kw"]),
+                                           P(a["q"]), a["qs"], P(a["pos"]), a["n"], a["tokens"],
+                                           P(a["qw"]), P(a["cos"]), P(a["sin"]), a["rows"],
+                                           a["eps"], a["budget"], P(a["bk"]), P(a["sc"]),
+                                           a["cols"], P(a["mask"]), P(a["st"]), P(a["ws"]),
+                                           a["wsb"], None)
+    need = lib.qsa_decode_workspace_bytes(2, 4096)
+    assert call() == 1                               # no workspace
+    assert call(ws=A, wsb=need - 1) == 1             # too small
+    assert call(ws=A + 8, wsb=need) == 1             # not 16-byte aligned
+    assert call(ws=A, wsb=need, budget=2047) == 1    # what qsa_index_select refuses
+    assert call(ws=A, wsb=need, n=2, cols=100) == 1
+    assert call(n=0) == 0                            # nothing to do: no workspace needed
+
+
 def test_status_calls_refuse_null(lib):
     assert lib.qsa_reset_status(None, None) == 1
     assert lib.qsa_read_status(None, None, None, None) == 1

@@ -50,6 +50,8 @@ L2_BYTES = 129 * 1024 * 1024
 POOL_BYTES_PER_BLOCK = 1024 + 256 + 256
 SCORE_BYTES_PER_BLOCK = 256 + 4
 SELECT_BYTES_PER_BLOCK = 4          # + 1 byte per mask token written
+DECODE_FUSED_SOURCES = ("qsa_decode.cu", "qsa_score_simt.cuh", "qsa_select_util.cuh",
+                        "qsa_device.cuh")
 
 
 def parse_args():
@@ -79,9 +81,13 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def source_digest(name: str) -> str:
-    with open(os.path.join(ROOT, "sparse_attention_token_qsa_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:12]
+def source_digest(names) -> str:
+    """sha256 (12 hex) over a kernel's source files, concatenated in order."""
+    h = hashlib.sha256()
+    for name in ([names] if isinstance(names, str) else names):
+        with open(os.path.join(ROOT, "sparse_attention_token_qsa_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
 
 
 def recorded_traffic(kernel: str, workload: str, src: str):
@@ -405,7 +411,7 @@ def run_ours(args, rank, world, device):
     kern = {}
     for name, fn, bytes_per_launch, src in (
             ("decode_fused", wl.fused_only, SCORE_BYTES_PER_BLOCK * N_BLOCKS + TOKENS,
-             "qsa_decode.cu"),
+             DECODE_FUSED_SOURCES),
             ("score", wl.score, SCORE_BYTES_PER_BLOCK * N_BLOCKS, "qsa_score_simt.cu"),
             ("select", wl.select, SELECT_BYTES_PER_BLOCK * N_BLOCKS + TOKENS, "qsa_select.cu")):
         gk = capture_graphs(torch, fn, steps[:min(K, 4096)])

@@ -22,9 +22,14 @@
  *
  * Conventions shared by every entry point
  *  - bf16 values travel as uint16_t bit patterns (the upper half of an f32).
- *  - Pointers marked DEVICE are CUDA device (or managed) pointers owned by the
- *    caller; the library allocates nothing and frees nothing.  `stream` is a
- *    cudaStream_t (NULL = the legacy default stream); every launch is
+ *  - Pointers marked DEVICE are pointers the GPU can address, owned by the
+ *    caller: CUDA device or managed memory, or page-locked host memory (it is
+ *    mapped into the unified address space, and the kernels read and write it
+ *    in place over the CPU-GPU link, e.g. a decode step's query row, position
+ *    and mask row).  Keep the large arrays (block keys, scores) and every
+ *    workspace and status word in device memory: atomics and bulk copies
+ *    target them.  The library allocates nothing and frees nothing.  `stream`
+ *    is a cudaStream_t (NULL = the legacy default stream); every launch is
  *    stream-ordered and asynchronous.
  *  - Arguments are validated on the host before any launch.  A refusal returns
  *    QSA_ERR_INVALID_VALUE and launches nothing.  Refused: negative extents,

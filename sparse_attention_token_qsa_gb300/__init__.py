@@ -91,12 +91,17 @@ def status_string(code: int) -> str:
 
 
 def _dev(t: torch.Tensor | None, name: str):
+    """The device-addressable pointer of a CUDA tensor, or of a pinned host tensor
+    (page-locked host memory is mapped into the unified address space, so the
+    kernels read and write it directly over the CPU-GPU link).  Anything else is
+    refused: every computation runs in the library's kernels."""
     if t is None:
         return None
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor: libqsa has no CPU path")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory: libqsa has no "
+                         "CPU path")
     return ctypes.c_void_p(t.data_ptr())
 
 

@@ -252,3 +252,44 @@ def test_decode_workspace_reused_across_shapes(qsa, orc, tables):
                                                             tokens, nb, qw, ws=ws)
         assert dst == (0, 0) and int(ws.count_nonzero()) == 0
         assert np.array_equal(dmask, pmask), (n_rows, tokens)
+
+
+def test_decode_with_inputs_and_mask_in_pinned_host_memory(qsa, orc, tables):
+    """A decode step whose query rows, positions, raw keys (pooled this call) and
+    mask live in pinned host memory, read and written in place by the kernels,
+    gives exactly the results of the same call on device buffers."""
+    rng = qi.rng_for(1, salt=82)
+    c, s, cd, sd = tables
+    tokens = 65536
+    nb = tokens // 4
+    raw = qi.normal_bf16(rng, (tokens, 128))
+    qw_h, kw_h = qi.norm_weights(rng)
+    cache_np = orc.pool_blocks(raw, 128, 0, nb - 1, kw_h, c, s, EPS, total_blocks=nb)
+    q_np = qi.normal_bf16(rng, (2, 512))
+    pos_np = np.array([tokens - 1, 50001], np.int32)     # row 0 completes block nb - 1
+    outs = []
+    for where in ("device", "host"):
+        cache = dev(cache_np.copy())
+        sc = torch.full((2, nb), -7.0, dtype=torch.float32, device="cuda")
+        st = qsa.new_status()
+        ws = qsa.new_decode_workspace(2, tokens)
+        if where == "device":
+            keys, q, pos = dev(raw), dev(q_np), dev(pos_np)
+            mask = torch.full((2, tokens), 0xAB, dtype=torch.uint8, device="cuda")
+        else:
+            keys = torch.from_numpy(raw.view(np.int16)).pin_memory()
+            q = torch.from_numpy(q_np.view(np.int16)).pin_memory()
+            pos = torch.from_numpy(pos_np).pin_memory()
+            mask = torch.full((2, tokens), 0xAB, dtype=torch.uint8).pin_memory()
+        qsa.qsa_decode_index_select(keys.view(-1)[4 * (nb - 1) * 128:], 128, nb - 1, 1, dev(kw_h), q,
+                                    512, pos, 2, tokens, dev(qw_h), cd, sd, c.shape[0], EPS, BUDGET,
+                                    cache, sc, nb, mask, st, ws)
+        assert qsa.qsa_read_status(st) == (0, 0)
+        torch.cuda.synchronize()
+        outs.append((cache.cpu().numpy(), sc.cpu().numpy(), mask.cpu().numpy().copy()))
+        assert int(ws.count_nonzero()) == 0
+    assert np.array_equal(outs[0][0], outs[1][0]), "pooled keys differ"
+    assert np.array_equal(outs[0][1], outs[1][1]), "scores differ"
+    assert np.array_equal(outs[0][2], outs[1][2]), "masks differ"
+    want, _ = oracle_masks(orc, outs[1][1], nb, pos_np, tokens, BUDGET)
+    assert np.array_equal(outs[1][2], want)

@@ -655,16 +655,20 @@ static int sm_count() {
   return n;
 }
 
-// Cluster size for a launch: split a row over a cluster only when its blocks
-// overflow one CTA's key cache.  (Splitting further to fill the GPU costs more
-// in cluster barriers and remote reads than it gains: a 16384-block row is
-// faster on one CTA than on sixteen.)
+// Cluster size for a launch: split a row over a cluster when its blocks
+// overflow one CTA's key cache, and then, for launches of a few such rows,
+// further while the whole launch stays within half the GPU and every CTA keeps
+// at least 4096 keys (one 65536-block row: 13.7 us on 4 CTAs, 11.3 us on 16; 32
+// such rows are fastest on 4 each: more CTAs than one wave cost more in
+// cluster barriers and remote reads than they gain).
 int select_cluster_size(int64_t n_rows, int64_t tokens) {
-  (void)n_rows;
   const int64_t n_max = tokens / kRatio;
   const int cmax = max_cluster_size();
   int C = 1;
   while (C < cmax && (n_max + C - 1) / C > kSelCapMax) C <<= 1;
+  // (a row that fits one CTA stays on one: its cluster barriers would cost more)
+  while (C > 1 && 2 * C <= cmax && n_rows * 2 * C <= sm_count() / 2 && n_max / (2 * C) >= 4096)
+    C <<= 1;
   return C;
 }
 

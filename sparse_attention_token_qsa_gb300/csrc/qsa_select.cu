@@ -158,51 +158,65 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     constexpr int kLoadsInFlight = 4;  // float4 loads issued per thread before use
     const int32_t nq = (cnt + 3) >> 2;
     uint32_t zeros = 0;
-    for (int32_t qb = warp * 32; qb < nq; qb += NT * kLoadsInFlight) {
+    // one quad's keys into the histogram (and the key cache); ne = its keys in
+    // the slice, a constant 4 on the fast path below
+    auto take = [&](const float4 &f, int32_t qd, int ne) {
+      if constexpr (CACHE) {
+        const uint32_t kq[4] = {order_key(f.x), order_key(f.y), order_key(f.z), order_key(f.w)};
+        if (4 * qd + 3 < cached) {  // one 16-byte store per quad
+          *reinterpret_cast<uint4 *>(keys_s + 4 * qd) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e < ne) {
+            zeros += kq[e] == kZeroKey ? 1u : 0u;
+            if (kq[e] != kZeroKey) atomicAdd(&S.hist0[kq[e] >> 20], 1u);
+          }
+        }
+      } else {
+        // no copy to keep: zeros of either sign are found on the raw bits,
+        // and no other key needs the -0.0 fold
+        const uint32_t uq[4] = {__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z),
+                                __float_as_uint(f.w)};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e < ne) {
+            const bool z = (uq[e] << 1) == 0u;
+            zeros += z ? 1u : 0u;
+            const uint32_t key = uq[e] ^ ((uint32_t)((int32_t)uq[e] >> 31) | 0x80000000u);
+            if (!z) atomicAdd(&S.hist0[key >> 20], 1u);
+          }
+        }
+      }
+    };
+    const float4 *srow4 = reinterpret_cast<const float4 *>(srow);
+    const int32_t nq_full = cnt >> 2;  // quads whose four keys all lie in the slice
+    int32_t qb = warp * 32;
+    // whole batches first: every lane's quads are full, no per-quad tests
+    for (; qb + (kLoadsInFlight - 1) * NT + 32 <= nq_full; qb += NT * kLoadsInFlight) {
+      float4 v[kLoadsInFlight];
+#pragma unroll
+      for (int u = 0; u < kLoadsInFlight; ++u) v[u] = __ldg(srow4 + qb + u * NT + lane);
+#pragma unroll
+      for (int u = 0; u < kLoadsInFlight; ++u) take(v[u], qb + u * NT + lane, 4);
+    }
+    // the rest of the slice, quad by quad
+    for (; qb < nq; qb += NT * kLoadsInFlight) {
       float4 v[kLoadsInFlight];
 #pragma unroll
       for (int u = 0; u < kLoadsInFlight; ++u) {
         const int32_t qd = qb + u * NT + lane;
         v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (qd < nq) v[u] = __ldg(reinterpret_cast<const float4 *>(srow) + qd);
+        if (qd < nq) v[u] = __ldg(srow4 + qd);
       }
 #pragma unroll
       for (int u = 0; u < kLoadsInFlight; ++u) {
         const int32_t qd = qb + u * NT + lane;
-        if (qd >= nq) continue;  // per lane: nothing below needs the whole warp
-        const int ne = min(4, cnt - 4 * qd);  // keys of this quad in the slice
-        if constexpr (CACHE) {
-          const uint32_t kq[4] = {order_key(v[u].x), order_key(v[u].y), order_key(v[u].z),
-                                  order_key(v[u].w)};
-          if (4 * qd + 3 < cached) {  // one 16-byte store per quad
-            *reinterpret_cast<uint4 *>(keys_s + 4 * qd) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (ne == 4 || e < ne) {  // whole quads need no per-key test
-              zeros += kq[e] == kZeroKey ? 1u : 0u;
-              if (kq[e] != kZeroKey) atomicAdd(&S.hist0[kq[e] >> 20], 1u);
-            }
-          }
-        } else {
-          // no copy to keep: zeros of either sign are found on the raw bits,
-          // and no other key needs the -0.0 fold
-          const uint32_t uq[4] = {__float_as_uint(v[u].x), __float_as_uint(v[u].y),
-                                  __float_as_uint(v[u].z), __float_as_uint(v[u].w)};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (ne == 4 || e < ne) {
-              const bool z = (uq[e] << 1) == 0u;
-              zeros += z ? 1u : 0u;
-              const uint32_t key = uq[e] ^ ((uint32_t)((int32_t)uq[e] >> 31) | 0x80000000u);
-              if (!z) atomicAdd(&S.hist0[key >> 20], 1u);
-            }
-          }
-        }
+        if (qd < nq) take(v[u], qd, min(4, cnt - 4 * qd));
       }
     }
     // one add per warp for the zeros
@@ -286,40 +300,15 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         // B0 < 0xFF8 (a finite key's bin), so the upper edge does not wrap
         const uint32_t bin_lo = B0 << 20, bin_hi = (B0 + 1u) << 20;
         const float t_lo = key_to_float(bin_lo), t_hi = key_to_float(bin_hi);
-        for (int32_t i = 4 * tid; i < cnt; i += 4 * NT) {
-          uint32_t k[4];  // order keys (cached), else raw score bits
-          if constexpr (CACHE) {
-            if (i + 3 < cached) {  // one 16-byte shared load
-              const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
-              k[0] = kv.x;
-              k[1] = kv.y;
-              k[2] = kv.z;
-              k[3] = kv.w;
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                k[e] = (i + e < cnt) ? (i + e < cached ? keys_s[i + e] : order_key(__ldg(srow + i + e)))
-                                     : 0u;
-            }
-          } else {
-            if (i + 3 < cnt) {  // one 16-byte load (L2)
-              const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + i));
-              k[0] = __float_as_uint(f.x);
-              k[1] = __float_as_uint(f.y);
-              k[2] = __float_as_uint(f.z);
-              k[3] = __float_as_uint(f.w);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) k[e] = (i + e < cnt) ? __float_as_uint(__ldg(srow + i + e)) : 0u;
-            }
-          }
-          const int mq = min(4, cnt - i);
+        // one quad: its mask word(s) and its candidates; mq = its keys in the
+        // slice, a constant 4 on the fast path
+        auto place = [&](int32_t i, const uint32_t (&k)[4], int mq) {
           // against the bin's edges (keys, or raw scores against the edges'
           // floats): >= hi kept, [lo, hi) candidates
           uint32_t bits = 0, w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const bool in = mq == 4 || e < mq;
+            const bool in = e < mq;
             bool kp, lo;
             if constexpr (CACHE) {
               kp = k[e] >= bin_hi;
@@ -348,6 +337,35 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
                 ++at;
               }
             }
+          }
+        };
+        for (int32_t i = 4 * tid; i < cnt; i += 4 * NT) {
+          uint32_t k[4];  // order keys (cached), else raw score bits
+          if (i + 3 < cnt && (!CACHE || i + 3 < cached)) {  // a whole quad, one 16-byte load
+            if constexpr (CACHE) {
+              const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
+              k[0] = kv.x;
+              k[1] = kv.y;
+              k[2] = kv.z;
+              k[3] = kv.w;
+            } else {
+              const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + i));
+              k[0] = __float_as_uint(f.x);
+              k[1] = __float_as_uint(f.y);
+              k[2] = __float_as_uint(f.z);
+              k[3] = __float_as_uint(f.w);
+            }
+            place(i, k, 4);
+          } else {  // the slice's last quad, or past the key cache
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if constexpr (CACHE)
+                k[e] = (i + e < cnt) ? (i + e < cached ? keys_s[i + e] : order_key(__ldg(srow + i + e)))
+                                     : 0u;
+              else
+                k[e] = (i + e < cnt) ? __float_as_uint(__ldg(srow + i + e)) : 0u;
+            }
+            place(i, k, min(4, cnt - i));
           }
         }
       }

@@ -683,6 +683,13 @@ int select_cluster_size(int64_t n_rows, int64_t tokens) {
   const int64_t n_max = tokens / kRatio;
   const int cmax = max_cluster_size();
   int C = 1;
+  if (n_rows > 2 * (int64_t)sm_count()) {
+    // many rows take the shape without a key cache: a row needs a cluster only
+    // past 65536 blocks (16-bit local indices); 1024 rows x 65536 blocks run
+    // in 206 us on one CTA each, 224 us on clusters of 4
+    while (C < cmax && (n_max + C - 1) / C > 65536) C <<= 1;
+    return C;
+  }
   while (C < cmax && (n_max + C - 1) / C > kSelCapMax) C <<= 1;
   // (a row that fits one CTA stays on one: its cluster barriers would cost more)
   while (C > 1 && 2 * C <= cmax && n_rows * 2 * C <= sm_count() / 2 && n_max / (2 * C) >= 4096)

@@ -63,6 +63,26 @@ def test_select_stress_ties_all_budgets(qsa, orc):
             assert np.array_equal(got[r], want[r]), (budget, r)
 
 
+def test_select_many_long_rows_one_cta_each(qsa, orc):
+    """More rows than two waves of CTAs at 256k: each 65536-block row runs on one
+    CTA of the shape without a key cache (no cluster), stress scores with massive
+    ties, and rows of every tail."""
+    rng = qi.rng_for(4, salt=320)
+    rows, tokens = 320, 262144
+    cols = tokens // 4
+    scores = qi.stress_scores(rng, rows, cols, zero_frac=0.5, levels=256)
+    pos = np.full(rows, tokens - 1, np.int32)
+    pos[1::4] = tokens - 2
+    pos[2::4] = tokens - 3
+    pos[3::4] = rng.integers(2051, tokens, size=len(pos[3::4]))
+    for budget in (2048, 4):
+        got, _ = gpu_select(qsa, scores, cols, pos, tokens, budget)
+        want, codes = oracle_masks(orc, scores, cols, pos, tokens, budget)
+        assert all(c == 0 for c in codes)
+        bad = [r for r in range(rows) if not np.array_equal(got[r], want[r])]
+        assert not bad, (budget, bad[:8])
+
+
 def test_select_prefill_rows_with_injected_ties(qsa, orc):
     """Single-sequence prefill geometry (T=2304): every row, all-kept rows below
     the inert bound and truncating rows above it; 32 truncating rows get exact

@@ -518,12 +518,11 @@ def run_ours(args, rank, world, device):
                    "sequences_rotated": R, "bytes_per_sequence": per_seq_bytes,
                    "l2": "inputs larger than L2 (steps rotate over the sequences)",
                    "launch": "CUDA graphs of 256 steps; per step qsa_decode_index_select: "
-                             "the pool launch when a block completes, then one fused "
-                             "score+select launch",
+                             "one fused launch (pool the completed block, score, select)",
                    "three_entry_points_us_per_step": three_us,
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "kernels": kernels, "clocks": clk, "e2e": e2e,
-        "gpu_launches": int(K + sum(1 for k in steps if (wl.step_params(k)[2] + 1) % 4 == 0)),
+        "gpu_launches": int(K),  # one fused launch per step (it pools the new block itself)
         "secondary": secondary,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

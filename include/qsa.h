@@ -252,10 +252,11 @@ int64_t qsa_decode_workspace_bytes(int32_t n_rows, int32_t tokens);
 /*
  * The same operation as qsa_index_select (pool the newly complete blocks,
  * score every row with the streaming scorer, select), for decode-sized row
- * counts: after the pooling launch, scoring and selection run as ONE
- * cooperative launch in which each row's scoring CTAs also build the row's
- * histogram, meet at a bounded grid barrier, write their own blocks' mask
- * bytes, and the row's last CTA resolves the threshold bin.  Source: metrale
+ * counts, as ONE cooperative launch: the CTAs whose block ranges hold new
+ * blocks pool them while their keys stream in, each row's scoring CTAs build
+ * the row's histogram, meet at a bounded grid barrier and write their own
+ * blocks' mask bytes, and the row's last CTA resolves the threshold bin.
+ * (New blocks at or past tokens/4 are pooled by a separate launch first.)  Source: metrale
  * layers/qsa.rs decode_select (score then top-k each decode step), PR #1160
  * (scores), PR #1178 "Exact semantics" (selection).  Results equal those of
  * qsa_index_select with the SIMT scorer.  When the rows' CTAs cannot all be

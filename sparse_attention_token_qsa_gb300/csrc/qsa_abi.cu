@@ -257,19 +257,26 @@ qsa_status qsa_decode_index_select(const uint16_t *keys, int64_t key_stride,
        (reinterpret_cast<uintptr_t>(decode_ws) & 15u) != 0))
     return QSA_ERR_INVALID_VALUE;
   cudaStream_t s = (cudaStream_t)stream;
-  if (pool_n_blocks > 0) {
-    st = from_cuda(qsa::launch_pool_blocks(keys, key_stride, pool_first_block, pool_n_blocks,
-                                           k_norm_w, cos_t, sin_t, eps, block_keys, s));
-    if (st != QSA_OK) return st;
-  }
-  if (n_rows == 0 || tokens == 0) return QSA_OK;
+  auto pool_launch = [&]() -> qsa_status {
+    if (pool_n_blocks == 0) return QSA_OK;
+    return from_cuda(qsa::launch_pool_blocks(keys, key_stride, pool_first_block, pool_n_blocks,
+                                             k_norm_w, cos_t, sin_t, eps, block_keys, s));
+  };
+  if (n_rows == 0 || tokens == 0) return pool_launch();
+  // new blocks inside the token range are pooled by the fused launch itself
+  const bool pool_inside =
+      (int64_t)pool_first_block + pool_n_blocks <= (int64_t)(tokens / 4);
+  if (!pool_inside && (st = pool_launch()) != QSA_OK) return st;
   qsa::ScoreArgs a = {q,        q_stride, pos,        nullptr,    n_rows, tokens, q_norm_w,
                       cos_t,    sin_t,    eps,        block_keys, nullptr, scores, score_cols,
                       dev_status};
   bool launched = false;
-  st = from_cuda(qsa::launch_decode_fused(a, budget, mask, decode_ws, s, &launched));
+  st = from_cuda(qsa::launch_decode_fused(a, budget, mask, decode_ws, keys, key_stride,
+                                          pool_first_block, pool_inside ? pool_n_blocks : 0,
+                                          k_norm_w, block_keys, s, &launched));
   if (st != QSA_OK || launched) return st;
-  // more rows than can be co-resident: the scorer and the selector, in turn
+  // more rows than can be co-resident: pool, score and select in turn
+  if (pool_inside && (st = pool_launch()) != QSA_OK) return st;
   st = from_cuda(qsa::launch_score_simt(a, s));
   if (st != QSA_OK) return st;
   return from_cuda(qsa::launch_select(scores, score_cols, pos, n_rows, tokens, budget, mask,

@@ -78,9 +78,20 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
   return v;
 }
 
+struct PoolArgs {         // newly complete blocks to pool in the same launch
+  const uint16_t *keys;  // token 4 * first's raw key
+  int64_t key_stride;
+  int32_t first, n;      // blocks [first, first + n); n = 0: none
+  const uint16_t *k_norm_w;
+  uint16_t *block_keys;  // the scorer's block-key cache, written here
+};
+
+constexpr int kDecPoolOverlap = 12;  // blocks a scoring CTA pools in its copy window (warps 2..7)
+
 __global__ void __launch_bounds__(kDecThreads)
 decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ mask,
-                    uint8_t *__restrict__ ws, int64_t row_ws_bytes, int32_t bpc) {
+                    uint8_t *__restrict__ ws, int64_t row_ws_bytes, int32_t bpc,
+                    const PoolArgs pa) {
   extern __shared__ __align__(128) uint8_t dec_smem[];
   SimtSmem &S = *reinterpret_cast<SimtSmem *>(dec_smem);
   uint8_t *ring = dec_smem + kSimtStageOff;
@@ -92,11 +103,39 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x, y = blockIdx.y, ny = gridDim.y;
   const int32_t p = a.pos[row];
-  if (p < 0 || p >= a.tokens) {  // uniform over the row's CTAs: nobody waits for them
+  const bool valid = p >= 0 && p < a.tokens;
+  const int32_t n = valid ? (p + 1) >> 2 : 0;
+
+  // ---- 0. the newly complete blocks in this CTA's range are pooled here
+  // (every row's CTAs pool them, writing identical keys, so the range is
+  // covered whatever each row sees).  A CTA that scores them does it in its
+  // copy window and patches its landed stage; any other CTA, or one with more
+  // than kDecPoolOverlap of them, pools before it scores.
+  const int pr0 = max(pa.first, y * bpc);
+  const int pr1 = min(pa.first + pa.n, min(y * bpc + bpc, a.tokens >> 2));
+  const int npool = max(0, pr1 - pr0);
+  const int c0_ = y * bpc;
+  const int cnt_ = max(0, min(n, c0_ + bpc) - c0_);
+  const bool overlap = npool > 0 && cnt_ > 0 && npool <= kDecPoolOverlap;
+  auto pool_one = [&](int b) {  // both half-warps of the calling warp call it
+    return pool_block_16(pa.keys + (int64_t)(b - pa.first) * kRatio * pa.key_stride,
+                         pa.key_stride, b, pa.k_norm_w, a.cos_t, a.sin_t, a.eps, lane & 15);
+  };
+  if (npool > 0 && !overlap) {
+    for (int j0 = 0; j0 < npool; j0 += kDecThreads / 16) {
+      const int j = j0 + (tid >> 4);
+      const uint4 key = pool_one(pr0 + min(j, npool - 1));
+      if (j < npool)
+        *reinterpret_cast<uint4 *>(pa.block_keys + (int64_t)(pr0 + j) * kHeadDim + 8 * (lane & 15)) = key;
+    }
+    __syncthreads();
+    // the bulk copies below read these keys through the async proxy
+    if (tid == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
+  if (!valid) {  // uniform over the row's CTAs: nobody waits for them
     if (y == 0 && tid == 0) report_error(a.status, kErrRowRange, row);
     return;
   }
-  const int32_t n = (p + 1) >> 2;
   uint8_t *mrow = mask + (int64_t)row * a.tokens;
   uint8_t *wrow = ws + (int64_t)row * row_ws_bytes;
   RowHdr &W = *reinterpret_cast<RowHdr *>(wrow);
@@ -107,8 +146,27 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   const int cnt = max(0, c1 - c0);
 
   // ---- 1. scores of this CTA's blocks
-  if (cnt > 0 &&
-      !simt_score_blocks(a, row, p, c0, c1, S, ring, [&](int b, float sc) { sc_s[b - c0] = sc; })) {
+  const int pj = (warp - 2) * 2 + (lane >> 4);  // warps 2..7: pooled block pr0 + pj
+  uint4 pooled = make_uint4(0u, 0u, 0u, 0u);
+  auto prologue = [&]() {
+    if (overlap && warp >= 2) {
+      pooled = pool_one(pr0 + min(pj, npool - 1));
+      if (pj < npool)
+        *reinterpret_cast<uint4 *>(pa.block_keys + (int64_t)(pr0 + pj) * kHeadDim + 8 * (lane & 15)) =
+            pooled;
+    }
+  };
+  auto patch = [&](int base, uint8_t *st) {  // the stage read the keys before pooling
+    if (overlap && pr0 < base + kSimtBlocksPerIter && pr1 > base) {
+      const int b = pr0 + pj;
+      if (warp >= 2 && pj < npool && b >= base && b < base + kSimtBlocksPerIter)
+        *reinterpret_cast<uint4 *>(st + (size_t)(b - base) * (kHeadDim * 2) + 16 * (lane & 15)) =
+            pooled;
+      __syncthreads();
+    }
+  };
+  if (cnt > 0 && !simt_score_blocks(a, row, p, c0, c1, S, ring,
+                                    [&](int b, float sc) { sc_s[b - c0] = sc; }, prologue, patch)) {
     if (tid == 0) report_error(a.status, kErrTimeout, row);
     return;  // the row's other CTAs time out at the barrier below
   }
@@ -379,7 +437,9 @@ int64_t decode_row_ws_bytes(int32_t tokens) {
 }
 
 cudaError_t launch_decode_fused(const ScoreArgs &a, int32_t budget, uint8_t *mask, void *ws,
-                                cudaStream_t stream, bool *launched) {
+                                const uint16_t *pool_keys, int64_t pool_key_stride,
+                                int32_t pool_first, int32_t pool_n, const uint16_t *k_norm_w,
+                                uint16_t *block_keys, cudaStream_t stream, bool *launched) {
   *launched = false;
   const int64_t n_max = (int64_t)a.tokens / kRatio;
   const int cap = dec_capacity();
@@ -405,9 +465,10 @@ cudaError_t launch_decode_fused(const ScoreArgs &a, int32_t budget, uint8_t *mas
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  const PoolArgs pa{pool_keys, pool_key_stride, pool_first, pool_n, k_norm_w, block_keys};
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, decode_fused_kernel, a, budget / kRatio, mask,
-                         static_cast<uint8_t *>(ws), decode_row_ws_bytes(a.tokens), bpc);
+                         static_cast<uint8_t *>(ws), decode_row_ws_bytes(a.tokens), bpc, pa);
   if (e == cudaSuccess) *launched = true;
   return e;
 }

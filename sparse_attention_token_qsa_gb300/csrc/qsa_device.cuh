@@ -147,6 +147,45 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
   return v;
 }
 
+// The pooled key of block b, computed by a 16-lane group (every lane calls
+// it; lane g returns dims 8g..8g+7): tok0 points at the block's first raw key,
+// the next three follow key_stride apart.  PR #1160 "score QSA token-indexer
+// blocks in native CUDA", description: the four keys averaged in float32 (the
+// exact sum rounded once, then x 1/4), cast back to bf16, (1 + w) RMSNorm, and
+// partial RoPE at the block's first token, 4b.
+__device__ __forceinline__ uint4 pool_block_16(const uint16_t *tok0, int64_t key_stride, int64_t b,
+                                               const uint16_t *k_norm_w, const uint16_t *cos_t,
+                                               const uint16_t *sin_t, float eps, int g) {
+  const uint16_t *k0 = tok0 + 8 * g;
+  uint4 t0 = ldg_nc_v4(k0);
+  uint4 t1 = ldg_nc_v4(k0 + key_stride);
+  uint4 t2 = ldg_nc_v4(k0 + 2 * key_stride);
+  uint4 t3 = ldg_nc_v4(k0 + 3 * key_stride);
+  const uint4 w8 = ldg_nc_v4(k_norm_w + 8 * g);
+  uint4 c8 = make_uint4(0, 0, 0, 0), s8 = make_uint4(0, 0, 0, 0);
+  if (g < 8) {
+    const int64_t P = (int64_t)kRatio * b;  // the block's first token
+    c8 = ldg_nc_v4(cos_t + P * kRot + 8 * g);
+    s8 = ldg_nc_v4(sin_t + P * kRot + 8 * g);
+  }
+  float a[8], bb[8], c[8], d[8], m[8];
+  unpack8(t0, a);
+  unpack8(t1, bb);
+  unpack8(t2, c);
+  unpack8(t3, d);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    // exact sum of the 4 bf16 values, rounded once to f32 (TwoSum cascade)
+    float s1, e1, s2, e2, s3, e3;
+    two_sum(a[e], bb[e], s1, e1);
+    two_sum(s1, c[e], s2, e2);
+    two_sum(s2, d[e], s3, e3);
+    const float sum = __fadd_rn(s3, __fadd_rn(__fadd_rn(e1, e2), e3));
+    m[e] = round_bf16(__fmul_rn(sum, 0.25f));  // f32 mean, cast back to bf16
+  }
+  return norm_rope_16(m, w8, c8, s8, eps, g);
+}
+
 __device__ __forceinline__ uint4 ldg_v4(const void *p) {
   return *reinterpret_cast<const uint4 *>(p);
 }

@@ -66,12 +66,16 @@ cudaError_t launch_qprep(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream)
 cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream);
 extern const bool kTcScorerReady;
 
-// Fused decode step (score + select in one cooperative launch).  Sets
-// *launched; returns cudaSuccess with *launched false when the rows' CTAs
-// cannot all be co-resident (the caller then takes the two-kernel path).
+// Fused decode step (pool the given new blocks, score, select: one
+// cooperative launch; pool_n = 0 pools nothing, and the blocks must lie below
+// tokens / 4).  Sets *launched; returns cudaSuccess with *launched false when
+// the rows' CTAs cannot all be co-resident (the caller then launches the pool,
+// score and select kernels itself).
 int64_t decode_row_ws_bytes(int32_t tokens);
 cudaError_t launch_decode_fused(const ScoreArgs &a, int32_t budget, uint8_t *mask, void *ws,
-                                cudaStream_t stream, bool *launched);
+                                const uint16_t *pool_keys, int64_t pool_key_stride,
+                                int32_t pool_first, int32_t pool_n, const uint16_t *k_norm_w,
+                                uint16_t *block_keys, cudaStream_t stream, bool *launched);
 
 cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t *pos,
                           int32_t n_rows, int32_t tokens, int32_t budget, uint8_t *mask,

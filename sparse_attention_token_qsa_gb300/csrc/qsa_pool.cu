@@ -34,34 +34,8 @@ pool_blocks_kernel(const uint16_t *__restrict__ keys, int64_t key_stride, int32_
   const int64_t ii = active ? i : (int64_t)n_blocks - 1;
   const int64_t b = (int64_t)first_block + ii;
 
-  const uint16_t *k0 = keys + (int64_t)kRatio * ii * key_stride + 8 * g;
-  uint4 t0 = ldg_nc_v4(k0);
-  uint4 t1 = ldg_nc_v4(k0 + key_stride);
-  uint4 t2 = ldg_nc_v4(k0 + 2 * key_stride);
-  uint4 t3 = ldg_nc_v4(k0 + 3 * key_stride);
-  const uint4 w8 = ldg_nc_v4(k_norm_w + 8 * g);
-  uint4 c8 = make_uint4(0, 0, 0, 0), s8 = make_uint4(0, 0, 0, 0);
-  if (g < 8) {
-    const int64_t P = (int64_t)kRatio * b;  // the block's first token
-    c8 = ldg_nc_v4(cos_t + P * kRot + 8 * g);
-    s8 = ldg_nc_v4(sin_t + P * kRot + 8 * g);
-  }
-  float a[8], bb[8], c[8], d[8], m[8];
-  unpack8(t0, a);
-  unpack8(t1, bb);
-  unpack8(t2, c);
-  unpack8(t3, d);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    // exact sum of the 4 bf16 values, rounded once to f32 (TwoSum cascade)
-    float s1, e1, s2, e2, s3, e3;
-    two_sum(a[e], bb[e], s1, e1);
-    two_sum(s1, c[e], s2, e2);
-    two_sum(s2, d[e], s3, e3);
-    const float sum = __fadd_rn(s3, __fadd_rn(__fadd_rn(e1, e2), e3));
-    m[e] = round_bf16(__fmul_rn(sum, 0.25f));  // f32 mean, cast back to bf16
-  }
-  const uint4 out = norm_rope_16(m, w8, c8, s8, eps, g);
+  const uint4 out = pool_block_16(keys + (int64_t)kRatio * ii * key_stride, key_stride, b, k_norm_w,
+                                  cos_t, sin_t, eps, g);
   if (active) *reinterpret_cast<uint4 *>(block_keys + b * kHeadDim + 8 * g) = out;
 }
 

@@ -85,13 +85,26 @@ __device__ __forceinline__ void prep_query_heads(const ScoreArgs &a, int row, in
   }
 }
 
+// Hooks that do nothing (the plain scorer's).
+struct SimtNoHook {
+  __device__ void operator()() const {}
+  __device__ void operator()(int, uint8_t *) const {}
+};
+
 // Score blocks [c0, c1) of `row` (c0 < c1), writing scores[row, b] and calling
 // emit(b, score) from the one lane that holds each score.  All kSimtThreads
-// threads call it.  Returns false if a wait timed out (the CTA's own copies
-// have then landed, and the caller reports the error).
-template <typename Emit>
+// threads call it.  Two hooks let a caller work in the copy window: prologue()
+// runs on every thread once the first copies are in flight (warps 0 and 1 are
+// busy with the query heads meanwhile), and patch(base, stage) runs on every
+// thread when the stage of keys [base, base + 128) has landed, before it is
+// read (a patch that writes the stage ends with a CTA barrier).  Returns false
+// if a wait timed out (the CTA's own copies have then landed, and the caller
+// reports the error).
+template <typename Emit, typename Prologue = SimtNoHook, typename Patch = SimtNoHook>
 __device__ __forceinline__ bool simt_score_blocks(const ScoreArgs &a, int row, int p, int c0, int c1,
-                                                  SimtSmem &S, uint8_t *stages, Emit emit) {
+                                                  SimtSmem &S, uint8_t *stages, Emit emit,
+                                                  Prologue prologue = SimtNoHook(),
+                                                  Patch patch = SimtNoHook()) {
   const int n_it = (c1 - c0 + kSimtBlocksPerIter - 1) / kSimtBlocksPerIter;
   const uint16_t *kb = a.block_keys + (a.key_base ? a.key_base[row] : 0) * kHeadDim;
   const int tid = threadIdx.x;
@@ -118,6 +131,7 @@ __device__ __forceinline__ bool simt_score_blocks(const ScoreArgs &a, int row, i
   }
   // the first stages are in flight while the query heads are prepared
   prep_query_heads(a, row, p, S.q_s);
+  prologue();
   __syncthreads();
 
   const int gi = tid >> 3;
@@ -143,7 +157,8 @@ __device__ __forceinline__ bool simt_score_blocks(const ScoreArgs &a, int row, i
       break;
     }
     const int base = c0 + it * kSimtBlocksPerIter;
-    const uint8_t *st = stages + (size_t)s * kSimtStageBytes;
+    uint8_t *st = stages + (size_t)s * kSimtStageBytes;
+    patch(base, st);
     uint4 kv[kSimtUnroll][2];
 #pragma unroll
     for (int u = 0; u < kSimtUnroll; ++u) {

@@ -293,3 +293,50 @@ def test_decode_with_inputs_and_mask_in_pinned_host_memory(qsa, orc, tables):
     assert np.array_equal(outs[0][2], outs[1][2]), "masks differ"
     want, _ = oracle_masks(orc, outs[1][1], nb, pos_np, tokens, BUDGET)
     assert np.array_equal(outs[1][2], want)
+
+
+@pytest.mark.parametrize("first,count", [(16255, 2), (16300, 84), (16383, 1)])
+def test_decode_pools_new_blocks_in_the_same_launch(qsa, orc, tables, first, count):
+    """The fused launch pools the new blocks itself: a range straddling two CTAs
+    (each pools its share while its keys stream in), a range too long for that
+    (pooled before scoring), rows that see none of the new blocks; the cache,
+    scores and masks equal those of the separate pool kernel and the oracle."""
+    rng = qi.rng_for(1, salt=first)
+    c, s, cd, sd = tables
+    tokens = 65536
+    nb = tokens // 4
+    raw = qi.normal_bf16(rng, (tokens, 128))
+    qw_h, kw_h = qi.norm_weights(rng)
+    keys_o = orc.pool_blocks(raw, 128, 0, nb, kw_h, c, s, EPS)
+    cache_np = keys_o.copy()
+    cache_np[first:] = 0x7FAB                          # not pooled yet (NaN pattern)
+    # the newest token completes block first + count - 1: no row sees further
+    last = 4 * (first + count) - 1
+    pos = np.array([last, 4 * first + 2, last - 1], np.int32)
+    q_np = qi.normal_bf16(rng, (3, 512))
+    outs = []
+    for entry in ("decode", "plain"):
+        cache = dev(cache_np)
+        sc = torch.full((3, nb), -7.0, dtype=torch.float32, device="cuda")
+        mask = torch.full((3, tokens), 0xAB, dtype=torch.uint8, device="cuda")
+        st = qsa.new_status()
+        args = (dev(raw).view(-1)[4 * first * 128:], 128, first, count, dev(kw_h), dev(q_np), 512,
+                dev(pos), 3, tokens, dev(qw_h), cd, sd, c.shape[0], EPS, BUDGET, cache, sc, nb, mask,
+                st)
+        if entry == "decode":
+            ws = qsa.new_decode_workspace(3, tokens)
+            qsa.qsa_decode_index_select(*args, ws)
+            torch.cuda.synchronize()
+            assert int(ws.count_nonzero()) == 0
+        else:
+            qsa.qsa_index_select(*args)
+        assert qsa.qsa_read_status(st) == (0, 0)
+        outs.append((cache.cpu().numpy().view(np.uint16), sc.cpu().numpy(), mask.cpu().numpy()))
+    top = first + count
+    assert np.array_equal(outs[0][0][:top], keys_o[:top]), "pooled cache differs from the oracle"
+    assert np.all(outs[0][0][top:] == 0x7FAB), "blocks past the new range were written"
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1]), "scores differ"
+    assert np.array_equal(outs[0][2], outs[1][2]), "masks differ"
+    want, _ = oracle_masks(orc, outs[0][1], nb, pos, tokens, BUDGET)
+    assert np.array_equal(outs[0][2], want)

@@ -69,6 +69,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_select_row.restype = ctypes.c_int
     lib.orc_select_rows.argtypes = [P, i64, P, i32, i32, i32, P, P]
     lib.orc_select_rows.restype = ctypes.c_int
+    lib.orc_mask_tokens.argtypes = [P, i32, P, i32]
+    lib.orc_mask_tokens.restype = i32
+    lib.orc_gather.argtypes = [P, P, i32, i32, i32, P, i32, P]
+    lib.orc_gather.restype = i32
     return lib
 
 
@@ -172,3 +176,21 @@ class Oracle:
                                     _p(_c(pos, np.int32)), int(n_rows), int(tokens), int(budget),
                                     _p(mask), _p(err))
         return mask, rc, int(err[0])
+
+    def mask_tokens(self, mask_row, cap: int | None = None) -> np.ndarray:
+        """The tokens whose mask byte is set, ascending (all of them if cap is None)."""
+        m = _c(mask_row, np.uint8)
+        cap = int(m.size) if cap is None else int(cap)
+        out = np.zeros(max(cap, 1), np.int32)
+        n = int(self.L.orc_mask_tokens(_p(m), int(m.size), _p(out), cap))
+        return out[:min(n, cap)].copy(), n
+
+    def gather(self, pool, table, page_size: int, width: int, sel) -> tuple[np.ndarray, int]:
+        """Rows of a paged pool [pages * page_size, width] for the tokens in sel."""
+        pool = _c(pool, np.uint16)
+        table = _c(table, np.int32)
+        sel = _c(sel, np.int32)
+        out = np.zeros((max(len(sel), 1), width), np.uint16)
+        rc = self.L.orc_gather(_p(pool), _p(table), int(table.size), int(page_size), int(width),
+                               _p(sel), int(sel.size), _p(out))
+        return out[:len(sel)], int(rc)

@@ -18,7 +18,9 @@
  *           (blocks/tail/keep arithmetic, canonical tie order, mask contents,
  *           +-0 tie, non-finite is an error, empty launch is a no-op).
  *  [LAYER]  metrale layers/qsa.rs: module doc (mean-pool, norm, rope at the
- *           block's first position), decode_select (host sort by (-score, idx)).
+ *           block's first position), decode_select (host sort by (-score, idx);
+ *           the selected token list and the gather of its K/V rows from the
+ *           paged cache into a contiguous scratch).
  *
  * Readings taken where the pages are silent (each also listed in the design doc):
  *  R1  bf16 <-> f32: widening is exact; narrowing is round-to-nearest-even,
@@ -314,4 +316,46 @@ int orc_select_rows(const float *scores, int64_t score_cols, const int32_t *pos,
         }
     }
     return first;
+}
+
+/*
+ * [LAYER] metrale layers/qsa.rs decode_select, after the top-k: the selected
+ * token list is every kept block's `ratio` tokens, blocks ascending, then the
+ * tail tokens -- i.e. every token whose mask byte is 1, in ascending order.
+ * Here: the tokens t < tokens with mask_row[t] != 0, ascending; at most `cap`
+ * are written to out; the return value is how many there are.
+ */
+int32_t orc_mask_tokens(const uint8_t *mask_row, int32_t tokens, int32_t *out, int32_t cap)
+{
+    int32_t n = 0;
+    for (int32_t t = 0; t < tokens; ++t) {
+        if (mask_row[t] != 0) {
+            if (n < cap)
+                out[n] = t;
+            ++n;
+        }
+    }
+    return n;
+}
+
+/*
+ * [LAYER] metrale layers/qsa.rs decode_select's gather (QsaSelection: a
+ * contiguous NHD k/v scratch read as a paged cache through an identity table).
+ * The paged pool holds `width` = kv_heads * head_dim bf16 values per token,
+ * pages of page_size tokens: token t of the sequence lives in physical page
+ * table[t / page_size], slot t % page_size.  Output row i is the pool row of
+ * token sel[i], for i < n_sel.  Returns ORC_ERR_INVALID_VALUE (and copies
+ * nothing more) at the first token outside [0, table_len * page_size).
+ */
+int orc_gather(const uint16_t *pool, const int32_t *table, int32_t table_len, int32_t page_size,
+               int32_t width, const int32_t *sel, int32_t n_sel, uint16_t *out)
+{
+    for (int32_t i = 0; i < n_sel; ++i) {
+        const int32_t t = sel[i];
+        if (t < 0 || t / page_size >= table_len)
+            return ORC_ERR_INVALID_VALUE;
+        const int64_t slot = (int64_t)table[t / page_size] * page_size + t % page_size;
+        memcpy(out + (int64_t)i * width, pool + slot * width, (size_t)width * sizeof(uint16_t));
+    }
+    return ORC_OK;
 }

@@ -462,7 +462,69 @@ def test_select_golden_geometry(orc):
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "qsa_oracle.c")
 
+
+# ---- token list and paged gather (metrale layers/qsa.rs decode_select)
+
+def test_mask_tokens_equals_nonzero(orc):
+    """The token list is every set mask byte, ascending: numpy's nonzero on random
+    masks; the count is reported even when the list is capped."""
+    rng = np.random.default_rng(11)
+    for tokens in (1, 7, 64, 1000):
+        m = (rng.random(tokens) < 0.3).astype(np.uint8)
+        got, n = orc.mask_tokens(m)
+        assert n == int(m.sum()) and np.array_equal(got, np.nonzero(m)[0])
+        cap = max(1, n // 2)
+        got_c, n_c = orc.mask_tokens(m, cap)
+        assert n_c == n and np.array_equal(got_c, np.nonzero(m)[0][:cap])
+
+
+def test_mask_tokens_of_a_selection_is_the_pages_list(orc):
+    """decode_select's list: the kept blocks (top keep by (-score, index), then
+    sorted ascending) expanded to their 4 tokens each, then the tail tokens --
+    built here from a numpy sort, compared with the oracle's select + list."""
+    rng = np.random.default_rng(12)
+    for p, budget in ((2052, 2048), (4099, 64), (30001, 2048), (9, 4)):
+        n = (p + 1) // 4
+        sc = (rng.integers(0, 40, size=n) / 8.0).astype(np.float32)   # ties at the cut
+        mask, rc = orc.select_row(sc, p, p + 7, budget)
+        assert rc == 0
+        keep = min(budget // 4, n)
+        order = np.lexsort((np.arange(n), -sc.astype(np.float64)))[:keep]
+        blocks = np.sort(order)
+        want = np.concatenate([(4 * blocks[:, None] + np.arange(4)).reshape(-1),
+                               np.arange(4 * n, p + 1)]).astype(np.int32)
+        got, cnt = orc.mask_tokens(mask)
+        assert cnt == 4 * keep + (p + 1) % 4
+        assert np.array_equal(got, want)
+
+
+def test_gather_equals_fancy_indexing(orc):
+    """Output row i is the pool row of token sel[i]: page table[t // page_size],
+    slot t % page_size -- numpy fancy indexing on a shuffled page table."""
+    rng = np.random.default_rng(13)
+    page_size, width, pages = 16, 96, 40
+    pool = rng.integers(0, 65535, size=(pages * page_size, width)).astype(np.uint16)
+    table = rng.permutation(pages).astype(np.int32)[:30]
+    sel = np.sort(rng.choice(30 * page_size, size=100, replace=False)).astype(np.int32)
+    got, rc = orc.gather(pool, table, page_size, width, sel)
+    assert rc == 0
+    want = pool.reshape(pages, page_size, width)[table[sel // page_size], sel % page_size]
+    assert np.array_equal(got, want)
+
+
+def test_gather_refuses_tokens_past_the_table(orc):
+    pool = np.zeros((32, 8), np.uint16)
+    table = np.array([1, 0], np.int32)
+    assert orc.gather(pool, table, 16, 8, np.array([31], np.int32))[1] == 0
+    assert orc.gather(pool, table, 16, 8, np.array([32], np.int32))[1] == 1
+    assert orc.gather(pool, table, 16, 8, np.array([-1], np.int32))[1] == 1
+
 MUTANTS = {
+    "tokens_count_capped": ("    return n;\n}\n\n/*\n * [LAYER] metrale layers/qsa.rs decode_select's gather",
+                            "    return n < cap ? n : cap;\n}\n\n/*\n * [LAYER] metrale layers/qsa.rs decode_select's gather"),
+    "gather_page_slot_swapped": ("table[t / page_size] * page_size + t % page_size",
+                                 "table[t % page_size] * page_size + t / page_size"),
+    "gather_ignores_table": ("(int64_t)table[t / page_size] * page_size", "(int64_t)(t / page_size) * page_size"),
     "drop_tail": ("mask_row[t] = 1;", "(void)t;"),
     "keep_one_fewer": ("for (int32_t i = 0; i < keep; ++i)", "for (int32_t i = 0; i < keep - 1; ++i)"),
     "keep_one_more": ("for (int32_t i = 0; i < keep; ++i)", "for (int32_t i = 0; i <= keep && i < blocks; ++i)"),
@@ -494,6 +556,8 @@ PIN_TESTS = [
     test_pool_weight_enters_as_one_plus_w, test_pool_eps_and_mean_closed_form,
     test_pool_mean_of_distinct_tokens, test_pool_stride_and_offset_indexing,
     test_score_onehot_closed_form, test_score_relu_is_per_head,
+    test_mask_tokens_equals_nonzero, test_mask_tokens_of_a_selection_is_the_pages_list,
+    test_gather_equals_fancy_indexing, test_gather_refuses_tokens_past_the_table,
 ]
 
 

@@ -50,6 +50,9 @@ L2_BYTES = 129 * 1024 * 1024
 POOL_BYTES_PER_BLOCK = 1024 + 256 + 256
 SCORE_BYTES_PER_BLOCK = 256 + 4
 SELECT_BYTES_PER_BLOCK = 4          # + 1 byte per mask token written
+GATHER_WIDTH = 512                  # 2 KV heads x head dim 256, bf16
+GATHER_PAGE = 16                    # tokens per cache page
+GATHER_BYTES_PER_TOKEN = 8 * GATHER_WIDTH + 8   # K, V read and written; index and page entry
 DECODE_FUSED_SOURCES = ("qsa_decode.cu", "qsa_score_simt.cuh", "qsa_select_util.cuh",
                         "qsa_device.cuh")
 
@@ -508,6 +511,7 @@ def run_ours(args, rank, world, device):
         secondary["select_256k"] = select_256k(torch, qsa, device, hbm_gbs)
         secondary["prefill_chunk_64k"] = prefill_chunk(torch, qsa, device, hbm_gbs, bf16_tf)
         secondary["decode_long_32seq"] = decode_long(torch, qsa, device, hbm_gbs)
+        secondary["decode_gather_64k"] = decode_gather(torch, qsa, device, hbm_gbs)
 
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
@@ -707,6 +711,77 @@ def decode_long(torch, qsa, device, hbm_gbs, ncu=False):
     }
 
 
+def decode_gather(torch, qsa, device, hbm_gbs, ncu=False):
+    """The decode chain after selection at 64k: 64 sequences, one row each at
+    p = 65534 (2051 selected tokens: 512 kept blocks and the 3-token tail),
+    each with its own paged K/V cache (pages of 16 tokens, 2 KV heads x 256
+    bf16, the pages of a sequence shuffled over the pool).  Times the token
+    lists of all 64 mask rows, the gather of their K/V rows, and one row's
+    list + gather (rotating over the 64 rows so each call reads cold data)."""
+    rows, tokens = 64, TOKENS
+    cols = tokens // 4
+    g = torch.Generator(device=device)
+    g.manual_seed(qi.seed_for(5))
+    sc = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32)
+    pos = torch.full((rows,), tokens - 2, dtype=torch.int32, device=device)
+    mask = torch.empty((rows, tokens), dtype=torch.uint8, device=device)
+    st = qsa.new_status(device)
+    qsa.qsa_select_mask(sc, cols, pos, rows, tokens, BUDGET, mask, st)
+    table_len = tokens // GATHER_PAGE
+    pages = rows * table_len
+    k_pool = torch.randint(-32768, 32767, (pages * GATHER_PAGE, GATHER_WIDTH), generator=g,
+                           device=device, dtype=torch.int16)
+    v_pool = torch.randint(-32768, 32767, (pages * GATHER_PAGE, GATHER_WIDTH), generator=g,
+                           device=device, dtype=torch.int16)
+    perm = torch.stack([torch.randperm(table_len, generator=g, device=device)
+                        for _ in range(rows)])
+    table = (perm + torch.arange(rows, device=device)[:, None] * table_len).to(torch.int32)
+    sel_cols = BUDGET + 3
+    sel = torch.empty((rows, sel_cols), dtype=torch.int32, device=device)
+    n_sel = torch.zeros(rows, dtype=torch.int32, device=device)
+    k_out = torch.empty((rows * sel_cols, GATHER_WIDTH), dtype=torch.int16, device=device)
+    v_out = torch.empty_like(k_out)
+
+    def tokens_all():
+        qsa.qsa_mask_tokens(mask, rows, tokens, sel, sel_cols, n_sel)
+
+    def gather_all():
+        qsa.qsa_gather_kv(k_pool, v_pool, GATHER_WIDTH, pages, table, table_len, table_len,
+                          GATHER_PAGE, sel, sel_cols, n_sel, rows, sel_cols, k_out, v_out,
+                          sel_cols, st)
+
+    def one_row(k):
+        r = k % rows
+        qsa.qsa_mask_tokens(mask[r], 1, tokens, sel[r], sel_cols, n_sel[r:r + 1])
+        qsa.qsa_gather_kv(k_pool, v_pool, GATHER_WIDTH, pages, table[r], table_len, table_len,
+                          GATHER_PAGE, sel[r], sel_cols, n_sel[r:r + 1], 1, sel_cols,
+                          k_out[r * sel_cols:], v_out[r * sel_cols:], sel_cols, st)
+
+    for _ in range(2 if ncu else 3):
+        tokens_all()
+        gather_all()
+    torch.cuda.synchronize()
+    if ncu:
+        return None
+    t_tok = time_fn(torch, tokens_all, 10)
+    t_gat = time_fn(torch, gather_all, 10)
+    gr = capture_graphs(torch, one_row, list(range(256)), chunk=256)
+    t_one = time_graphs(torch, gr) / 256
+    code, row = qsa.qsa_read_status(st)
+    assert code == 0, (code, row)
+    n = int(n_sel.sum())
+    tb = rows * tokens + 4 * n + 4 * rows
+    gb = GATHER_BYTES_PER_TOKEN * n
+    return {
+        "rows": rows, "selected_tokens": n, "width": GATHER_WIDTH, "page_size": GATHER_PAGE,
+        "mask_tokens": {"us": t_tok * 1000.0, "achieved_gbs": tb / (t_tok * 1e-3) / 1e9,
+                        "frac_of_measured_hbm": tb / (t_tok * 1e-3) / 1e9 / hbm_gbs},
+        "gather_kv": {"us": t_gat * 1000.0, "achieved_gbs": gb / (t_gat * 1e-3) / 1e9,
+                      "frac_of_measured_hbm": gb / (t_gat * 1e-3) / 1e9 / hbm_gbs},
+        "one_row_list_and_gather_us": t_one * 1000.0,
+    }
+
+
 # ------------------------------------------------------------ ncu cases
 
 def ncu_case(name: str):
@@ -728,6 +803,8 @@ def ncu_case(name: str):
         select_256k(torch, qsa, dev, 6800.0, ncu=True)
     elif name == "decode_long":
         decode_long(torch, qsa, dev, 6800.0, ncu=True)
+    elif name == "gather":
+        decode_gather(torch, qsa, dev, 6800.0, ncu=True)
     else:
         raise SystemExit(f"unknown ncu case {name}")
     torch.cuda.synchronize()

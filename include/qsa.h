@@ -62,7 +62,9 @@ typedef enum {
     QSA_ERR_LAUNCH = 2,        /* the CUDA runtime refused a launch */
     QSA_ERR_ROW_RANGE = 3,     /* device: pos or visible_len out of range */
     QSA_ERR_NONFINITE = 4,     /* device: NaN/Inf score in a truncating row */
-    QSA_ERR_TIMEOUT = 5        /* device: a bounded wait gave up */
+    QSA_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up */
+    QSA_ERR_TOKEN_RANGE = 6    /* device: a gathered token or its page lies outside
+                                  the page table or the pool */
 } qsa_status;
 
 /* Which scorer qsa_score_rows_with runs. */
@@ -281,6 +283,46 @@ qsa_status qsa_decode_index_select(const uint16_t *keys, int64_t key_stride,
                                    int32_t budget, uint16_t *block_keys, float *scores,
                                    int64_t score_cols, uint8_t *mask, int32_t *dev_status,
                                    void *decode_ws, int64_t decode_ws_bytes, void *stream);
+
+/*
+ * The selected token list of each mask row: the tokens t < tokens whose mask
+ * byte is non-zero, ascending.  Source: metrale layers/qsa.rs decode_select,
+ * after its top-k (every kept block's four tokens, blocks ascending, then the
+ * tail -- exactly the set bytes of the mask qsa_select_mask writes).
+ *  mask     DEVICE u8 [n_rows * tokens], row i at mask + i*tokens (any alignment).
+ *  sel      DEVICE int32, row i at sel + i*sel_cols; the first
+ *           min(count, sel_cols) tokens are written, the rest of the row is
+ *           left alone.  For a selection mask, budget + 3 columns always suffice.
+ *  n_sel    DEVICE int32 [n_rows]: each row's count of set bytes (a count above
+ *           sel_cols means the list was cut).
+ */
+qsa_status qsa_mask_tokens(const uint8_t *mask, int32_t n_rows, int32_t tokens, int32_t *sel,
+                           int64_t sel_cols, int32_t *n_sel, void *stream);
+
+/*
+ * Gather the K and V rows of each row's selected tokens from a paged cache into
+ * a contiguous scratch.  Source: metrale layers/qsa.rs decode_select and its
+ * QsaSelection (a contiguous NHD k/v scratch that the paged decode attention
+ * reads through an identity block table).
+ *  k_pool, v_pool  DEVICE bf16 [pool_pages * page_size, width], 16-byte aligned;
+ *           width = kv_heads * head_dim values per token, a multiple of 8.
+ *  table    DEVICE int32: row i's page table at table + i*table_cols
+ *           (table_cols = 0: one table shared by every row), table_len entries;
+ *           token t of the row is in physical page table[t / page_size], slot
+ *           t % page_size.
+ *  sel, sel_cols, n_sel: as qsa_mask_tokens writes them; row i gathers its
+ *           first min(n_sel[i], max_sel) tokens (max_sel <= sel_cols, out_rows).
+ *  k_out, v_out  DEVICE bf16 [n_rows * out_rows, width], 16-byte aligned: row i's
+ *           j-th token at (i*out_rows + j).
+ *  A token outside [0, table_len * page_size), or a table entry outside
+ *  [0, pool_pages), is recorded as QSA_ERR_TOKEN_RANGE and not read.
+ */
+qsa_status qsa_gather_kv(const uint16_t *k_pool, const uint16_t *v_pool, int32_t width,
+                         int32_t pool_pages, const int32_t *table, int32_t table_len,
+                         int64_t table_cols, int32_t page_size, const int32_t *sel,
+                         int64_t sel_cols, const int32_t *n_sel, int32_t n_rows, int32_t max_sel,
+                         uint16_t *k_out, uint16_t *v_out, int64_t out_rows, int32_t *dev_status,
+                         void *stream);
 
 /* Zero a DEVICE status word (stream-ordered). */
 qsa_status qsa_reset_status(int32_t *dev_status, void *stream);

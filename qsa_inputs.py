@@ -126,3 +126,15 @@ def torch_normal_bf16(torch, shape, seed: int, device, std: float = 1.0, token_s
         u = torch.rand((shape[0], 1), generator=g, device=device, dtype=torch.float32)
         x = x * torch.exp(np.log(0.25) + u * (np.log(4.0) - np.log(0.25)))
     return x.to(torch.bfloat16).view(torch.int16)
+
+
+def paged_kv_pool(rng: np.random.Generator, pages: int, page_size: int, width: int) -> np.ndarray:
+    """[pages * page_size, width] bf16 bit patterns, every 16-bit pattern
+    possible (NaNs and infinities included: a gather copies bits)."""
+    return rng.integers(0, 1 << 16, size=(pages * page_size, width), dtype=np.uint16)
+
+
+def page_tables(rng: np.random.Generator, n_rows: int, table_len: int, pages: int) -> np.ndarray:
+    """[n_rows, table_len] int32: each row's pages drawn without repeats from
+    [0, pages), in shuffled order."""
+    return np.stack([rng.permutation(pages)[:table_len] for _ in range(n_rows)]).astype(np.int32)

@@ -25,6 +25,7 @@ QSA_ERR_LAUNCH = 2
 QSA_ERR_ROW_RANGE = 3
 QSA_ERR_NONFINITE = 4
 QSA_ERR_TIMEOUT = 5
+QSA_ERR_TOKEN_RANGE = 6
 
 QSA_SCORE_AUTO = 0
 QSA_SCORE_SIMT = 1
@@ -35,8 +36,8 @@ HEADS, HEAD_DIM, RATIO, ROT_DIM, FUSED_WIDTH = 4, 128, 4, 64, 640
 EXPORTED = ("qsa_version", "qsa_status_string", "qsa_rope_tables", "qsa_pool_blocks",
             "qsa_score_rows", "qsa_score_rows_with", "qsa_score_workspace_bytes",
             "qsa_score_rows_noalloc", "qsa_select_mask", "qsa_index_select",
-            "qsa_decode_workspace_bytes", "qsa_decode_index_select", "qsa_reset_status",
-            "qsa_read_status")
+            "qsa_decode_workspace_bytes", "qsa_decode_index_select", "qsa_mask_tokens",
+            "qsa_gather_kv", "qsa_reset_status", "qsa_read_status")
 
 
 class QsaError(RuntimeError):
@@ -69,6 +70,9 @@ def _load() -> ctypes.CDLL:
         "qsa_decode_workspace_bytes": ([i32, i32], i64),
         "qsa_decode_index_select": ([P, i64, i32, i32, P, P, i64, P, i32, i32, P, P, P, i32, f32, i32,
                                      P, P, i64, P, P, P, i64, P], i32),
+        "qsa_mask_tokens": ([P, i32, i32, P, i64, P, P], i32),
+        "qsa_gather_kv": ([P, P, i32, i32, P, i32, i64, i32, P, i64, P, i32, i32, P, P, i64, P, P],
+                          i32),
         "qsa_reset_status": ([P, P], i32),
         "qsa_read_status": ([P, P, P, P], i32),
     }
@@ -251,6 +255,24 @@ def qsa_decode_index_select(keys, key_stride, pool_first_block, pool_n_blocks, k
                                         _dev(dev_status, "dev_status"), ws, int(wsb),
                                         _stream(stream)),
            "qsa_decode_index_select")
+
+
+def qsa_mask_tokens(mask, n_rows, tokens, sel, sel_cols, n_sel, stream=None) -> None:
+    _check(_lib.qsa_mask_tokens(_dev(mask, "mask"), int(n_rows), int(tokens), _dev(sel, "sel"),
+                                int(sel_cols), _dev(n_sel, "n_sel"), _stream(stream)),
+           "qsa_mask_tokens")
+
+
+def qsa_gather_kv(k_pool, v_pool, width, pool_pages, table, table_len, table_cols, page_size, sel,
+                  sel_cols, n_sel, n_rows, max_sel, k_out, v_out, out_rows, dev_status,
+                  stream=None) -> None:
+    _check(_lib.qsa_gather_kv(_dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), int(width),
+                              int(pool_pages), _dev(table, "table"), int(table_len),
+                              int(table_cols), int(page_size), _dev(sel, "sel"), int(sel_cols),
+                              _dev(n_sel, "n_sel"), int(n_rows), int(max_sel),
+                              _dev(k_out, "k_out"), _dev(v_out, "v_out"), int(out_rows),
+                              _dev(dev_status, "dev_status"), _stream(stream)),
+           "qsa_gather_kv")
 
 
 def qsa_reset_status(dev_status, stream=None) -> None:

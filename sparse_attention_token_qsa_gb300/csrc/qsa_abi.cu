@@ -100,6 +100,7 @@ const char *qsa_status_string(int32_t status) {
     case QSA_ERR_ROW_RANGE: return "row position or visible length out of range";
     case QSA_ERR_NONFINITE: return "non-finite score in a truncating row";
     case QSA_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case QSA_ERR_TOKEN_RANGE: return "a selected token or its page lies outside the page table or the pool";
     default: return "unknown status";
   }
 }
@@ -281,6 +282,45 @@ qsa_status qsa_decode_index_select(const uint16_t *keys, int64_t key_stride,
   if (st != QSA_OK) return st;
   return from_cuda(qsa::launch_select(scores, score_cols, pos, n_rows, tokens, budget, mask,
                                       dev_status, s));
+}
+
+qsa_status qsa_mask_tokens(const uint8_t *mask, int32_t n_rows, int32_t tokens, int32_t *sel,
+                           int64_t sel_cols, int32_t *n_sel, void *stream) {
+  if (n_rows < 0 || tokens < 0 || sel_cols < 0) return QSA_ERR_INVALID_VALUE;
+  if (n_rows == 0) return QSA_OK;
+  if (!n_sel || (tokens > 0 && !mask) || (sel_cols > 0 && !sel)) return QSA_ERR_INVALID_VALUE;
+  if ((int64_t)n_rows * tokens > ((int64_t)1 << 46) || (int64_t)n_rows * sel_cols > ((int64_t)1 << 46))
+    return QSA_ERR_INVALID_VALUE;
+  return from_cuda(qsa::launch_mask_tokens(mask, n_rows, tokens, sel, sel_cols, n_sel,
+                                           (cudaStream_t)stream));
+}
+
+qsa_status qsa_gather_kv(const uint16_t *k_pool, const uint16_t *v_pool, int32_t width,
+                         int32_t pool_pages, const int32_t *table, int32_t table_len,
+                         int64_t table_cols, int32_t page_size, const int32_t *sel,
+                         int64_t sel_cols, const int32_t *n_sel, int32_t n_rows, int32_t max_sel,
+                         uint16_t *k_out, uint16_t *v_out, int64_t out_rows, int32_t *dev_status,
+                         void *stream) {
+  if (n_rows < 0 || max_sel < 0 || width < 0 || pool_pages < 0 || table_len < 0 ||
+      table_cols < 0 || sel_cols < 0 || out_rows < 0)
+    return QSA_ERR_INVALID_VALUE;
+  if (n_rows == 0 || max_sel == 0 || width == 0) return QSA_OK;
+  if (width % 8 != 0 || page_size <= 0 || max_sel > sel_cols || max_sel > out_rows)
+    return QSA_ERR_INVALID_VALUE;
+  if (table_cols != 0 && table_cols < table_len) return QSA_ERR_INVALID_VALUE;
+  if (!k_pool || !v_pool || !table || !sel || !n_sel || !k_out || !v_out || !dev_status)
+    return QSA_ERR_INVALID_VALUE;
+  if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_out) || !aligned16(v_out))
+    return QSA_ERR_INVALID_VALUE;
+  if ((int64_t)pool_pages * page_size * width > ((int64_t)1 << 46) ||
+      (int64_t)n_rows * out_rows * width > ((int64_t)1 << 46) ||
+      (int64_t)n_rows * sel_cols > ((int64_t)1 << 46) ||
+      (int64_t)table_len * page_size > INT32_MAX)
+    return QSA_ERR_INVALID_VALUE;
+  return from_cuda(qsa::launch_gather_kv(k_pool, v_pool, width, pool_pages, table, table_len,
+                                         table_cols, page_size, sel, sel_cols, n_sel, n_rows,
+                                         max_sel, k_out, v_out, out_rows, dev_status,
+                                         (cudaStream_t)stream));
 }
 
 qsa_status qsa_reset_status(int32_t *dev_status, void *stream) {

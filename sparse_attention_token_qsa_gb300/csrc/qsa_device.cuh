@@ -29,6 +29,7 @@ enum : int32_t {
   kErrRowRange = 3,
   kErrNonFinite = 4,
   kErrTimeout = 5,
+  kErrTokenRange = 6,
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }

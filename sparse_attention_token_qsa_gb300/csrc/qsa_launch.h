@@ -77,6 +77,17 @@ cudaError_t launch_decode_fused(const ScoreArgs &a, int32_t budget, uint8_t *mas
                                 int32_t pool_first, int32_t pool_n, const uint16_t *k_norm_w,
                                 uint16_t *block_keys, cudaStream_t stream, bool *launched);
 
+// Selected token lists of mask rows, and the gather of their K/V rows.
+cudaError_t launch_mask_tokens(const uint8_t *mask, int32_t n_rows, int32_t tokens, int32_t *sel,
+                               int64_t sel_cols, int32_t *n_sel, cudaStream_t stream);
+cudaError_t launch_gather_kv(const uint16_t *k_pool, const uint16_t *v_pool, int32_t width,
+                             int32_t pool_pages, const int32_t *table, int32_t table_len,
+                             int64_t table_cols,
+                             int32_t page_size, const int32_t *sel, int64_t sel_cols,
+                             const int32_t *n_sel, int32_t n_rows, int32_t max_sel,
+                             uint16_t *k_out, uint16_t *v_out, int64_t out_rows, int32_t *status,
+                             cudaStream_t stream);
+
 cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t *pos,
                           int32_t n_rows, int32_t tokens, int32_t budget, uint8_t *mask,
                           int32_t *status, cudaStream_t stream);

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.qsa_version() >= 100
-    for code in range(6):
+    for code in range(7):
         assert lib.qsa_status_string(code)
     assert b"unknown" in lib.qsa_status_string(99)
 
@@ -163,6 +163,31 @@ def test_decode_index_select_refusals(lib):
     assert call(ws=A, wsb=need, budget=2047) == 1    # what qsa_index_select refuses
     assert call(ws=A, wsb=need, n=2, cols=100) == 1
     assert call(n=0) == 0                            # nothing to do: no workspace needed
+
+
+def test_mask_tokens_refusals(lib):
+    def call(mask=A, n=2, tokens=4096, sel=A, cols=2051, n_sel=B):
+        return lib.qsa_mask_tokens(P(mask), n, tokens, P(sel), cols, P(n_sel), None)
+    assert call(n=0) == 0                            # nothing to do
+    assert call(n=-1) == 1 and call(tokens=-1) == 1 and call(cols=-1) == 1
+    assert call(n_sel=0) == 1 and call(mask=0) == 1 and call(sel=0) == 1
+    assert call(n=1 << 30, tokens=1 << 20) == 1      # extent past the library's bound
+
+
+def test_gather_kv_refusals(lib):
+    def call(**kw):
+        a = dict(k=A, v=B, width=512, pages=4096, table=A, tlen=4096, tcols=4096, psz=16, sel=A,
+                 scols=2051, n_sel=B, n=2, max_sel=2051, ko=A, vo=B, orows=2051, st=B)
+        a.update(kw)
+        return lib.qsa_gather_kv(P(a["k"]), P(a["v"]), a["width"], a["pages"], P(a["table"]),
+                                 a["tlen"], a["tcols"], a["psz"], P(a["sel"]), a["scols"],
+                                 P(a["n_sel"]), a["n"], a["max_sel"], P(a["ko"]), P(a["vo"]),
+                                 a["orows"], P(a["st"]), None)
+    assert call(n=0) == 0 and call(max_sel=0) == 0 and call(width=0) == 0   # nothing to do
+    for kw in (dict(width=12), dict(width=-8), dict(psz=0), dict(max_sel=2052),
+               dict(orows=2050), dict(tcols=4095), dict(pages=-1), dict(k=U), dict(vo=U),
+               dict(table=0), dict(st=0), dict(n_sel=0), dict(tlen=1 << 28, tcols=0)):
+        assert call(**kw) == 1, kw
 
 
 def test_status_calls_refuse_null(lib):

@@ -67,6 +67,8 @@ struct SelectSmem {
   int32_t sel_bin;
   uint32_t sel_above;
   uint32_t eq_base;
+  uint32_t band_hi;  // sampled band: keys at or above its upper edge
+  int32_t band_bin[2];  // sampled band: its top and bottom bins
   // cand keys [kCandCap] u32, cand local indices [kCandCap] u16, keys[] follow (dynamic)
 };
 
@@ -149,81 +151,9 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   if (tid == 0) {
     S.ncand = 0u;
     S.eq_base = 0u;
+    S.band_hi = 0u;
   }
   __syncthreads();
-
-  // ---- round 0 while loading: key cache and top-12-bit histogram.  Exact
-  // zeros (relu outputs) share one bin: counted in registers, added per warp.
-  {
-    constexpr int kLoadsInFlight = 4;  // float4 loads issued per thread before use
-    const int32_t nq = (cnt + 3) >> 2;
-    uint32_t zeros = 0;
-    // one quad's keys into the histogram (and the key cache); ne = its keys in
-    // the slice, a constant 4 on the fast path below
-    auto take = [&](const float4 &f, int32_t qd, int ne) {
-      if constexpr (CACHE) {
-        const uint32_t kq[4] = {order_key(f.x), order_key(f.y), order_key(f.z), order_key(f.w)};
-        if (4 * qd + 3 < cached) {  // one 16-byte store per quad
-          *reinterpret_cast<uint4 *>(keys_s + 4 * qd) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (e < ne) {
-            zeros += kq[e] == kZeroKey ? 1u : 0u;
-            if (kq[e] != kZeroKey) atomicAdd(&S.hist0[kq[e] >> 20], 1u);
-          }
-        }
-      } else {
-        // no copy to keep: zeros of either sign are found on the raw bits,
-        // and no other key needs the -0.0 fold
-        const uint32_t uq[4] = {__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z),
-                                __float_as_uint(f.w)};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (e < ne) {
-            const bool z = (uq[e] << 1) == 0u;
-            zeros += z ? 1u : 0u;
-            const uint32_t key = uq[e] ^ ((uint32_t)((int32_t)uq[e] >> 31) | 0x80000000u);
-            if (!z) atomicAdd(&S.hist0[key >> 20], 1u);
-          }
-        }
-      }
-    };
-    const float4 *srow4 = reinterpret_cast<const float4 *>(srow);
-    const int32_t nq_full = cnt >> 2;  // quads whose four keys all lie in the slice
-    int32_t qb = warp * 32;
-    // whole batches first: every lane's quads are full, no per-quad tests
-    for (; qb + (kLoadsInFlight - 1) * NT + 32 <= nq_full; qb += NT * kLoadsInFlight) {
-      float4 v[kLoadsInFlight];
-#pragma unroll
-      for (int u = 0; u < kLoadsInFlight; ++u) v[u] = __ldg(srow4 + qb + u * NT + lane);
-#pragma unroll
-      for (int u = 0; u < kLoadsInFlight; ++u) take(v[u], qb + u * NT + lane, 4);
-    }
-    // the rest of the slice, quad by quad
-    for (; qb < nq; qb += NT * kLoadsInFlight) {
-      float4 v[kLoadsInFlight];
-#pragma unroll
-      for (int u = 0; u < kLoadsInFlight; ++u) {
-        const int32_t qd = qb + u * NT + lane;
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (qd < nq) v[u] = __ldg(srow4 + qd);
-      }
-#pragma unroll
-      for (int u = 0; u < kLoadsInFlight; ++u) {
-        const int32_t qd = qb + u * NT + lane;
-        if (qd < nq) take(v[u], qd, min(4, cnt - 4 * qd));
-      }
-    }
-    // one add per warp for the zeros
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) zeros += __shfl_xor_sync(0xffffffffu, zeros, off);
-    if (lane == 0 && zeros) atomicAdd(&S.hist0[kZeroKey >> 20], zeros);
-  }
 
   uint32_t need = (uint32_t)min(keep_max, n);  // keys still to keep at/below the prefix
   bool bad = false;        // a non-finite score somewhere in the row
@@ -232,98 +162,87 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   uint32_t own_n = 0;      // this CTA's own candidates (at the start of its list)
   uint32_t prefix = 0;     // fallback state: the threshold's top bits so far ...
   int shift = 32;          // ... prefix = threshold >> shift
+  bool rule_ready = false;  // the kept set is known: no candidate rounds
 
-  // ---- round 0: merge the top-12-bit histograms over the cluster
-  if (C > 1) {
-    cluster_sync_all();
-    // reduce-scatter: this CTA sums its slice of bins over the cluster, in place
-    const int slice = 4096 / C;
-    for (int b = (int)rank * slice + tid; b < ((int)rank + 1) * slice; b += NT) {
-      uint32_t v[kSelMaxCluster];
-#pragma unroll
-      for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&S.hist0[b], (uint32_t)q) : 0u;
-      uint32_t t = 0;
-#pragma unroll
-      for (int q = 0; q < kSelMaxCluster; ++q) t += v[q];
-      S.hist0[b] = t;
-    }
-    cluster_sync_all();
-    // gather the other slices' merged bins (their owners no longer change them)
-    constexpr int kGather = (4096 + NT - 1) / NT;
-    uint32_t g[kGather];
-#pragma unroll
-    for (int j = 0; j < kGather; ++j) {
-      const int b = tid + j * NT;
-      g[j] = 0u;
-      if (b < 4096) {
-        const int owner = b / slice;
-        g[j] = owner != (int)rank ? ld_dsmem(&S.hist0[b], (uint32_t)owner) : S.hist0[b];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kGather; ++j)
-      if (tid + j * NT < 4096) S.hist0[tid + j * NT] = g[j];
-  }
-  // A score is non-finite exactly when its key lands in one of the 16 outer
-  // bins: keys of -inf and negative NaNs are below 0x00800000 (bins 0..7),
-  // keys of +inf and positive NaNs at or above 0xFF800000 (bins 0xFF8..0xFFF),
-  // and every finite score's key lies between.
-  __syncthreads();
+  // ---- sampled band (a row on one CTA, long enough for a sample).  8 * NT
+  // scores in runs of 8, spread evenly over the row, are histogrammed on the
+  // top 12 key bits.  With r = need * samples / n, the bins holding the
+  // sample's (r - d)-th and (r + d)-th largest keys (d = 3 sqrt(r) + 2) bound
+  // a band [t_lo, t_hi) that holds the row's keep-th key unless the sample is
+  // far off.  One pass over the row then writes every key's mask bytes (kept
+  // at or above t_hi, dropped below t_lo, dropped for now inside the band),
+  // counts the kept keys and lists the band's keys as candidates.  If the
+  // counts put the keep-th key in the band and the list fits, the candidate
+  // rounds finish the selection; otherwise (or on a non-finite score) the row
+  // is selected again by the full-histogram path, which rewrites every byte.
+  bool sampled = false;
   {
-    const bool nf = tid < 16 && S.hist0[tid < 8 ? tid : 0xFF0 + tid] != 0u;
-    bad = __syncthreads_or(nf) != 0;  // the same verdict in every CTA of the cluster
-  }
-
-  if (!bad) {
-    find_bin<NT>(S.hist0, 4096, need, S.warp_tot, &S.sel_bin, &S.sel_above);
-    const uint32_t B0 = (uint32_t)S.sel_bin;
-    const uint32_t cnt0 = S.hist0[B0];
-    need -= S.sel_above;
-    prefix = B0;
-    shift = 20;
-    if (cnt0 == need) {  // the whole bin is kept
-      if (tid == 0) {
-        S.rule_prefix = B0;
-        S.rule_shift = 20;
-        S.rule_cut = INT32_MAX;
-      }
-      __syncthreads();
-    } else if (cnt0 <= (uint32_t)kCandCap && per <= 65536) {
-      // ---- candidate path.  One pass over this CTA's keys: the mask bytes of
-      // keys above the bin (kept) and below it (dropped) are final; the bin's
-      // own keys are written as dropped, appended with their local block
-      // index to the candidate list (slots from a shared counter, so the list
-      // is unordered) and patched once the threshold inside the bin is known.
+    constexpr int kSamp = 8 * NT;
+    // (rows whose keys a second pass would still find in L2 are faster on the
+    // full-histogram path, and the cached shape never reads a key twice)
+    const bool try_sample = !CACHE && C == 1 && cnt > 32768 && cnt <= 65536 &&
+                            need * (uint32_t)kSamp >= 16u * (uint32_t)cnt;
+    if (try_sample) {
+      const float r = (float)need * (float)kSamp / (float)cnt;
+      const float d = ceilf(3.f * sqrtf(r)) + 2.f;
+      const uint32_t r_hi = (uint32_t)fmaxf(1.f, floorf(r - d));
+      const uint32_t r_lo = (uint32_t)ceilf(r + d);
+      bool ok;
       {
+        // the pass's first two batches head for L2 while the sample is read
+        for (int u = 0; u < 8; ++u) {
+          const int32_t qd = warp * 32 + (u >> 2) * 4 * NT + (u & 3) * NT + lane;
+          if (4 * qd < cnt)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(srow + 4 * (int64_t)qd));
+        }
+        // run `tid` starts at a multiple of 8 at most cnt - 8 (rows are 16-byte aligned)
+        const int32_t at = (int32_t)((((int64_t)tid * (cnt - 8)) / (NT - 1)) & ~int64_t(7));
+        const float4 f0 = __ldg(reinterpret_cast<const float4 *>(srow + at));
+        const float4 f1 = __ldg(reinterpret_cast<const float4 *>(srow + at + 4));
+        const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+        bool nf = false;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          nf |= (__float_as_uint(v[e]) & 0x7F800000u) == 0x7F800000u;
+          atomicAdd(&S.hist0[order_key(v[e]) >> 20], 1u);
+        }
+        ok = __syncthreads_or(nf) == 0;
+      }
+      int32_t bhi = 0, blo = 0;
+      if (ok) {
+        find_two_bins<NT>(S.hist0, 4096, r_hi, r_lo, S.warp_tot, S.band_bin);
+        bhi = S.band_bin[0];
+        blo = S.band_bin[1];
+        // finite edges, and a band the 256-bin histogram below can hold
+        ok = blo >= 8 && bhi <= 0xFF6 && bhi - blo < 256;
+      }
+      if (ok) {
+        const float t_lo = key_to_float((uint32_t)blo << 20);
+        const float t_hi = key_to_float((uint32_t)(bhi + 1) << 20);
         const uintptr_t rbm = reinterpret_cast<uintptr_t>(mrow);
         const bool m16 = (rbm & 15u) == 0, m4 = (rbm & 3u) == 0;
-        // B0 < 0xFF8 (a finite key's bin), so the upper edge does not wrap
-        const uint32_t bin_lo = B0 << 20, bin_hi = (B0 + 1u) << 20;
-        const float t_lo = key_to_float(bin_lo), t_hi = key_to_float(bin_hi);
-        // one quad: its mask word(s) and its candidates; mq = its keys in the
-        // slice, a constant 4 on the fast path
-        auto place = [&](int32_t i, const uint32_t (&k)[4], int mq) {
-          // against the bin's edges (keys, or raw scores against the edges'
-          // floats): >= hi kept, [lo, hi) candidates
-          uint32_t bits = 0, w[4];
+        uint32_t kept_n = 0;
+        float chk = 0.f;  // stays +0 unless a score is non-finite (or a quad's sum overflows)
+        // one quad of scores (mq of them in the row): its mask bytes, kept
+        // count and candidates
+        auto band_quad = [&](int32_t i, const float4 &f, int mq) {
+          const float x[4] = {f.x, f.y, f.z, f.w};
+          uint32_t w[4], bits = 0;
+          float s = 0.f;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const bool in = e < mq;
-            bool kp, lo;
-            if constexpr (CACHE) {
-              kp = k[e] >= bin_hi;
-              lo = k[e] >= bin_lo;
-            } else {
-              kp = __uint_as_float(k[e]) >= t_hi;
-              lo = __uint_as_float(k[e]) >= t_lo;
-            }
-            w[e] = (in && kp) ? 0x01010101u : 0u;
-            bits |= (in && !kp && lo) ? (1u << e) : 0u;
+            const bool kp = in && x[e] >= t_hi;
+            w[e] = kp ? 0x01010101u : 0u;
+            kept_n += kp ? 1u : 0u;
+            bits |= (in && !kp && x[e] >= t_lo) ? (1u << e) : 0u;
+            s += in ? x[e] : 0.f;
           }
+          chk = fmaf(s, 0.f, chk);  // inf * 0 and NaN * 0 are NaN
           if (mq == 4 && m16) {
-            *reinterpret_cast<uint4 *>(mrow + 4 * ((int64_t)b0 + i)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(mrow + 4 * (int64_t)i) = make_uint4(w[0], w[1], w[2], w[3]);
           } else {
-            store_blocks(mrow, (int64_t)b0 + i, mq,
+            store_blocks(mrow, (int64_t)i, mq,
                          (w[0] & 1u) | ((w[1] & 1u) << 1) | ((w[2] & 1u) << 2) | ((w[3] & 1u) << 3),
                          m16, m4);
           }
@@ -332,165 +251,424 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               if (bits & (1u << e)) {
-                cand_s[at] = CACHE ? k[e] : order_key(__uint_as_float(k[e]));
-                cand_li[at] = (uint16_t)(i + e);
+                if (at < (uint32_t)kCandCap) {
+                  cand_s[at] = order_key(x[e]);
+                  cand_li[at] = (uint16_t)(i + e);
+                }
                 ++at;
               }
             }
           }
         };
-        for (int32_t i = 4 * tid; i < cnt; i += 4 * NT) {
-          uint32_t k[4];  // order keys (cached), else raw score bits
-          if (i + 3 < cnt && (!CACHE || i + 3 < cached)) {  // a whole quad, one 16-byte load
-            if constexpr (CACHE) {
-              const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
-              k[0] = kv.x;
-              k[1] = kv.y;
-              k[2] = kv.z;
-              k[3] = kv.w;
-            } else {
-              const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + i));
-              k[0] = __float_as_uint(f.x);
-              k[1] = __float_as_uint(f.y);
-              k[2] = __float_as_uint(f.z);
-              k[3] = __float_as_uint(f.w);
-            }
-            place(i, k, 4);
-          } else {  // the slice's last quad, or past the key cache
+        constexpr int kLoadsInFlight = 4;  // float4 loads issued per thread before use
+        const float4 *srow4 = reinterpret_cast<const float4 *>(srow);
+        const int32_t nq = (cnt + 3) >> 2, nq_full = cnt >> 2;
+        int32_t qb = warp * 32;
+        for (; qb + (kLoadsInFlight - 1) * NT + 32 <= nq_full; qb += NT * kLoadsInFlight) {
+          float4 v[kLoadsInFlight];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if constexpr (CACHE)
-                k[e] = (i + e < cnt) ? (i + e < cached ? keys_s[i + e] : order_key(__ldg(srow + i + e)))
-                                     : 0u;
-              else
-                k[e] = (i + e < cnt) ? __float_as_uint(__ldg(srow + i + e)) : 0u;
-            }
-            place(i, k, min(4, cnt - i));
-          }
-        }
-      }
-      cand_path = true;
-      if (C > 1) cluster_sync_all(); else __syncthreads();
-      own_n = S.ncand;
-      if (rank == 0) {
-        // rank 0 gathers every CTA's candidates after its own, rank by rank,
-        // so an entry's rank (and with it its global block index) follows
-        // from where it sits in the list
-        if (warp == 0) {  // every rank's count at once, then a warp prefix sum
-          uint32_t c = 0;
-          if (lane < C) c = lane == 0 ? S.ncand : ld_dsmem(&S.ncand, (uint32_t)lane);
-          uint32_t incl = c;
+          for (int u = 0; u < kLoadsInFlight; ++u) v[u] = __ldg(srow4 + qb + u * NT + lane);
 #pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-          }
-          if (lane < C) S.roff[lane] = incl - c;
-          if (lane == C - 1) S.roff[C] = incl;
+          for (int u = 0; u < kLoadsInFlight; ++u) band_quad(4 * (qb + u * NT + lane), v[u], 4);
         }
-        __syncthreads();
-        // one thread per remote entry across all ranks, loads independent
-        const uint32_t own = S.roff[1], all = S.roff[C];
-        for (uint32_t j = own + tid; j < all; j += NT) {
-          int q = 1;
-          while (q + 1 < C && S.roff[q + 1] <= j) ++q;
-          const uint32_t jj = j - S.roff[q];
-          cand_s[j] = ld_dsmem(&cand_s[jj], (uint32_t)q);
-          cand_li[j] = ld_dsmem_u16(&cand_li[jj], (uint32_t)q);
-        }
-        __syncthreads();
-        const int32_t nl = (int32_t)S.roff[C];
-        // rounds 1..3 on the candidates: every thread histograms, one warp
-        // finds the bin (two barriers a round)
-        bool done = false;
-        for (int r = 1; r < kRounds && !done; ++r) {
-          uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
-          const int nb = round_bins(r), sh = round_shift(r);
-          for (int32_t j = tid; j < nl; j += NT) {
-            const uint32_t key = cand_s[j];
-            if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+        for (; qb < nq; qb += NT * kLoadsInFlight) {
+          float4 v[kLoadsInFlight];
+#pragma unroll
+          for (int u = 0; u < kLoadsInFlight; ++u) {
+            const int32_t qd = qb + u * NT + lane;
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (qd < nq) v[u] = __ldg(srow4 + qd);
           }
-          __syncthreads();
-          if (warp == 0) {
-            uint32_t B, above;
-            warp_find_bin(H, nb, need, lane, B, above);
-            if (lane == 0) {
-              S.sel_bin = (int32_t)B;
-              S.sel_above = above;
+#pragma unroll
+          for (int u = 0; u < kLoadsInFlight; ++u) {
+            const int32_t qd = qb + u * NT + lane;
+            if (qd < nq) band_quad(4 * qd, v[u], min(4, cnt - 4 * qd));
+          }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) kept_n += __shfl_xor_sync(0xffffffffu, kept_n, off);
+        if (lane == 0 && kept_n) atomicAdd(&S.band_hi, kept_n);
+        const bool nf = !(chk == 0.f);
+        ok = __syncthreads_or(nf) == 0;  // (also the barrier before the totals are read)
+        const uint32_t hi_n = S.band_hi, nc = S.ncand;
+        ok = ok && hi_n <= need && hi_n + nc >= need && nc <= (uint32_t)kCandCap;
+        if (ok) {
+          sampled = true;
+          cand_path = true;
+          need -= hi_n;
+          if (need == 0) {  // exactly the keys at or above t_hi: no candidate is kept
+            rule_ready = true;
+            if (tid == 0) {
+              S.rule_prefix = (uint32_t)bhi;
+              S.rule_shift = 20;
+              S.rule_cut = -1;
             }
-          }
-          __syncthreads();
-          const uint32_t B = (uint32_t)S.sel_bin;
-          const uint32_t cB = H[B];
-          need -= S.sel_above;
-          prefix = (prefix << (shift - sh)) | B;
-          shift = sh;
-          done = cB == need;
-          __syncthreads();  // sel_bin is rewritten next round
-        }
-        if (done) {
-          if (tid == 0) {
-            S.rule_prefix = prefix;
-            S.rule_shift = (uint32_t)shift;
-            S.rule_cut = INT32_MAX;
-          }
-        } else {
-          // ties at the full key: of the keys equal to `prefix`, the `need`
-          // with the lowest block indices are kept.  Radix rounds over the
-          // equal candidates' block indices, 8 bits at a time from the
-          // highest bit an index < n can have, find the cut index.
-          const uint32_t top = (uint32_t)n - 1u;
-          int ish = top ? ((32 - __clz((int)top) + 7) & ~7) : 8;  // index bits, rounded up
-          uint32_t iprefix = 0;  // the cut index's bits above ish
-          uint32_t *H = S.hist0;  // round 0's histogram is no longer read
-          for (int ir = 0; ir < 4; ++ir) {
-            const int sh = ish - 8;
-            if (tid < 256) H[tid] = 0u;
-            __syncthreads();
-            for (int32_t j = tid; j < nl; j += NT) {
-              if (cand_s[j] != prefix) continue;
-              int q = 0;
-              while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
-              const uint32_t gi = (uint32_t)(q * per) + (uint32_t)cand_li[j];
-              if (ish >= 32 || (gi >> ish) == iprefix)  // ascending: digit d counts in bin 255-d
-                atomicAdd(&H[255u - ((gi >> sh) & 255u)], 1u);
-            }
+          } else {
+            // the candidates' bins within the band: the one holding the need-th
+            for (uint32_t j = tid; j < nc; j += NT)
+              atomicAdd(&S.hist1[(cand_s[j] >> 20) - (uint32_t)blo], 1u);
             __syncthreads();
             if (warp == 0) {
               uint32_t B, above;
-              warp_find_bin(H, 256, need, lane, B, above);
+              warp_find_bin(S.hist1, bhi - blo + 1, need, lane, B, above);
               if (lane == 0) {
                 S.sel_bin = (int32_t)B;
                 S.sel_above = above;
               }
             }
             __syncthreads();
-            const uint32_t cB = H[S.sel_bin];
             need -= S.sel_above;
-            iprefix = (iprefix << 8) | (255u - (uint32_t)S.sel_bin);
-            ish = sh;
-            __syncthreads();  // sel_bin and H are rewritten next round
-            if (cB == need || ish == 0) break;  // at ish == 0 a bin holds one index
+            prefix = (uint32_t)blo + (uint32_t)S.sel_bin;
+            shift = 20;
+            if (tid < 256) S.hist1[tid] = 0u;  // round 1 histograms here again
           }
-          if (tid == 0) {
-            S.rule_prefix = prefix;
-            S.rule_shift = 0;
-            S.rule_cut = (int32_t)((((uint64_t)iprefix + 1u) << ish) - 1u);
+        }
+      }
+      if (!sampled) {  // start over on the full histogram
+        __syncthreads();
+        for (int i = tid; i < 4096; i += NT) S.hist0[i] = 0u;
+        if (tid == 0) S.ncand = 0u;
+        __syncthreads();
+      }
+    }
+  }
+
+  if (!sampled) {
+    // ---- round 0 while loading: key cache and top-12-bit histogram.  Exact
+    // zeros (relu outputs) share one bin: counted in registers, added per warp.
+    {
+      constexpr int kLoadsInFlight = 4;  // float4 loads issued per thread before use
+      const int32_t nq = (cnt + 3) >> 2;
+      uint32_t zeros = 0;
+      // one quad's keys into the histogram (and the key cache); ne = its keys in
+      // the slice, a constant 4 on the fast path below
+      auto take = [&](const float4 &f, int32_t qd, int ne) {
+        if constexpr (CACHE) {
+          const uint32_t kq[4] = {order_key(f.x), order_key(f.y), order_key(f.z), order_key(f.w)};
+          if (4 * qd + 3 < cached) {  // one 16-byte store per quad
+            *reinterpret_cast<uint4 *>(keys_s + 4 * qd) = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (e < ne) {
+              zeros += kq[e] == kZeroKey ? 1u : 0u;
+              if (kq[e] != kZeroKey) atomicAdd(&S.hist0[kq[e] >> 20], 1u);
+            }
+          }
+        } else {
+          // no copy to keep: zeros of either sign are found on the raw bits,
+          // and no other key needs the -0.0 fold
+          const uint32_t uq[4] = {__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z),
+                                  __float_as_uint(f.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (e < ne) {
+              const bool z = (uq[e] << 1) == 0u;
+              zeros += z ? 1u : 0u;
+              const uint32_t key = uq[e] ^ ((uint32_t)((int32_t)uq[e] >> 31) | 0x80000000u);
+              if (!z) atomicAdd(&S.hist0[key >> 20], 1u);
+            }
+          }
+        }
+      };
+      const float4 *srow4 = reinterpret_cast<const float4 *>(srow);
+      const int32_t nq_full = cnt >> 2;  // quads whose four keys all lie in the slice
+      int32_t qb = warp * 32;
+      // whole batches first: every lane's quads are full, no per-quad tests
+      for (; qb + (kLoadsInFlight - 1) * NT + 32 <= nq_full; qb += NT * kLoadsInFlight) {
+        float4 v[kLoadsInFlight];
+#pragma unroll
+        for (int u = 0; u < kLoadsInFlight; ++u) v[u] = __ldg(srow4 + qb + u * NT + lane);
+#pragma unroll
+        for (int u = 0; u < kLoadsInFlight; ++u) take(v[u], qb + u * NT + lane, 4);
+      }
+      // the rest of the slice, quad by quad
+      for (; qb < nq; qb += NT * kLoadsInFlight) {
+        float4 v[kLoadsInFlight];
+#pragma unroll
+        for (int u = 0; u < kLoadsInFlight; ++u) {
+          const int32_t qd = qb + u * NT + lane;
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (qd < nq) v[u] = __ldg(srow4 + qd);
+        }
+#pragma unroll
+        for (int u = 0; u < kLoadsInFlight; ++u) {
+          const int32_t qd = qb + u * NT + lane;
+          if (qd < nq) take(v[u], qd, min(4, cnt - 4 * qd));
+        }
+      }
+      // one add per warp for the zeros
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) zeros += __shfl_xor_sync(0xffffffffu, zeros, off);
+      if (lane == 0 && zeros) atomicAdd(&S.hist0[kZeroKey >> 20], zeros);
+    }
+
+    // ---- round 0: merge the top-12-bit histograms over the cluster
+    if (C > 1) {
+      cluster_sync_all();
+      // reduce-scatter: this CTA sums its slice of bins over the cluster, in place
+      const int slice = 4096 / C;
+      for (int b = (int)rank * slice + tid; b < ((int)rank + 1) * slice; b += NT) {
+        uint32_t v[kSelMaxCluster];
+#pragma unroll
+        for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&S.hist0[b], (uint32_t)q) : 0u;
+        uint32_t t = 0;
+#pragma unroll
+        for (int q = 0; q < kSelMaxCluster; ++q) t += v[q];
+        S.hist0[b] = t;
+      }
+      cluster_sync_all();
+      // gather the other slices' merged bins (their owners no longer change them)
+      constexpr int kGather = (4096 + NT - 1) / NT;
+      uint32_t g[kGather];
+#pragma unroll
+      for (int j = 0; j < kGather; ++j) {
+        const int b = tid + j * NT;
+        g[j] = 0u;
+        if (b < 4096) {
+          const int owner = b / slice;
+          g[j] = owner != (int)rank ? ld_dsmem(&S.hist0[b], (uint32_t)owner) : S.hist0[b];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kGather; ++j)
+        if (tid + j * NT < 4096) S.hist0[tid + j * NT] = g[j];
+    }
+    // A score is non-finite exactly when its key lands in one of the 16 outer
+    // bins: keys of -inf and negative NaNs are below 0x00800000 (bins 0..7),
+    // keys of +inf and positive NaNs at or above 0xFF800000 (bins 0xFF8..0xFFF),
+    // and every finite score's key lies between.
+    __syncthreads();
+    {
+      const bool nf = tid < 16 && S.hist0[tid < 8 ? tid : 0xFF0 + tid] != 0u;
+      bad = __syncthreads_or(nf) != 0;  // the same verdict in every CTA of the cluster
+    }
+
+    if (!bad) {
+      find_bin<NT>(S.hist0, 4096, need, S.warp_tot, &S.sel_bin, &S.sel_above);
+      const uint32_t B0 = (uint32_t)S.sel_bin;
+      const uint32_t cnt0 = S.hist0[B0];
+      need -= S.sel_above;
+      prefix = B0;
+      shift = 20;
+      if (cnt0 == need) {  // the whole bin is kept
+        if (tid == 0) {
+          S.rule_prefix = B0;
+          S.rule_shift = 20;
+          S.rule_cut = INT32_MAX;
+        }
+        __syncthreads();
+      } else if (cnt0 <= (uint32_t)kCandCap && per <= 65536) {
+        // ---- candidate path.  One pass over this CTA's keys: the mask bytes of
+        // keys above the bin (kept) and below it (dropped) are final; the bin's
+        // own keys are written as dropped, appended with their local block
+        // index to the candidate list (slots from a shared counter, so the list
+        // is unordered) and patched once the threshold inside the bin is known.
+        {
+          const uintptr_t rbm = reinterpret_cast<uintptr_t>(mrow);
+          const bool m16 = (rbm & 15u) == 0, m4 = (rbm & 3u) == 0;
+          // B0 < 0xFF8 (a finite key's bin), so the upper edge does not wrap
+          const uint32_t bin_lo = B0 << 20, bin_hi = (B0 + 1u) << 20;
+          const float t_lo = key_to_float(bin_lo), t_hi = key_to_float(bin_hi);
+          // one quad: its mask word(s) and its candidates; mq = its keys in the
+          // slice, a constant 4 on the fast path
+          auto place = [&](int32_t i, const uint32_t (&k)[4], int mq) {
+            // against the bin's edges (keys, or raw scores against the edges'
+            // floats): >= hi kept, [lo, hi) candidates
+            uint32_t bits = 0, w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const bool in = e < mq;
+              bool kp, lo;
+              if constexpr (CACHE) {
+                kp = k[e] >= bin_hi;
+                lo = k[e] >= bin_lo;
+              } else {
+                kp = __uint_as_float(k[e]) >= t_hi;
+                lo = __uint_as_float(k[e]) >= t_lo;
+              }
+              w[e] = (in && kp) ? 0x01010101u : 0u;
+              bits |= (in && !kp && lo) ? (1u << e) : 0u;
+            }
+            if (mq == 4 && m16) {
+              *reinterpret_cast<uint4 *>(mrow + 4 * ((int64_t)b0 + i)) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+              store_blocks(mrow, (int64_t)b0 + i, mq,
+                           (w[0] & 1u) | ((w[1] & 1u) << 1) | ((w[2] & 1u) << 2) | ((w[3] & 1u) << 3),
+                           m16, m4);
+            }
+            if (bits) {
+              uint32_t at = atomicAdd(&S.ncand, (uint32_t)__popc(bits));
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if (bits & (1u << e)) {
+                  cand_s[at] = CACHE ? k[e] : order_key(__uint_as_float(k[e]));
+                  cand_li[at] = (uint16_t)(i + e);
+                  ++at;
+                }
+              }
+            }
+          };
+          for (int32_t i = 4 * tid; i < cnt; i += 4 * NT) {
+            uint32_t k[4];  // order keys (cached), else raw score bits
+            if (i + 3 < cnt && (!CACHE || i + 3 < cached)) {  // a whole quad, one 16-byte load
+              if constexpr (CACHE) {
+                const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
+                k[0] = kv.x;
+                k[1] = kv.y;
+                k[2] = kv.z;
+                k[3] = kv.w;
+              } else {
+                const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + i));
+                k[0] = __float_as_uint(f.x);
+                k[1] = __float_as_uint(f.y);
+                k[2] = __float_as_uint(f.z);
+                k[3] = __float_as_uint(f.w);
+              }
+              place(i, k, 4);
+            } else {  // the slice's last quad, or past the key cache
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if constexpr (CACHE)
+                  k[e] = (i + e < cnt) ? (i + e < cached ? keys_s[i + e] : order_key(__ldg(srow + i + e)))
+                                       : 0u;
+                else
+                  k[e] = (i + e < cnt) ? __float_as_uint(__ldg(srow + i + e)) : 0u;
+              }
+              place(i, k, min(4, cnt - i));
+            }
+          }
+        }
+        cand_path = true;
+      } else {
+        scan_ties = true;  // ---- fallback: rounds over every key (part B)
+      }
+    }
+  }
+
+  if (cand_path) {
+    if (C > 1) cluster_sync_all(); else __syncthreads();
+    own_n = S.ncand;
+    if (rank == 0 && !rule_ready) {
+      // rank 0 gathers every CTA's candidates after its own, rank by rank,
+      // so an entry's rank (and with it its global block index) follows
+      // from where it sits in the list
+      if (warp == 0) {  // every rank's count at once, then a warp prefix sum
+        uint32_t c = 0;
+        if (lane < C) c = lane == 0 ? S.ncand : ld_dsmem(&S.ncand, (uint32_t)lane);
+        uint32_t incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (lane < C) S.roff[lane] = incl - c;
+        if (lane == C - 1) S.roff[C] = incl;
+      }
+      __syncthreads();
+      // one thread per remote entry across all ranks, loads independent
+      const uint32_t own = S.roff[1], all = S.roff[C];
+      for (uint32_t j = own + tid; j < all; j += NT) {
+        int q = 1;
+        while (q + 1 < C && S.roff[q + 1] <= j) ++q;
+        const uint32_t jj = j - S.roff[q];
+        cand_s[j] = ld_dsmem(&cand_s[jj], (uint32_t)q);
+        cand_li[j] = ld_dsmem_u16(&cand_li[jj], (uint32_t)q);
+      }
+      __syncthreads();
+      const int32_t nl = (int32_t)S.roff[C];
+      // rounds 1..3 on the candidates: every thread histograms, one warp
+      // finds the bin (two barriers a round)
+      bool done = false;
+      for (int r = 1; r < kRounds && !done; ++r) {
+        uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
+        const int nb = round_bins(r), sh = round_shift(r);
+        for (int32_t j = tid; j < nl; j += NT) {
+          const uint32_t key = cand_s[j];
+          if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+          uint32_t B, above;
+          warp_find_bin(H, nb, need, lane, B, above);
+          if (lane == 0) {
+            S.sel_bin = (int32_t)B;
+            S.sel_above = above;
           }
         }
         __syncthreads();
+        const uint32_t B = (uint32_t)S.sel_bin;
+        const uint32_t cB = H[B];
+        need -= S.sel_above;
+        prefix = (prefix << (shift - sh)) | B;
+        shift = sh;
+        done = cB == need;
+        __syncthreads();  // sel_bin is rewritten next round
       }
-      // every CTA takes rank 0's rule
-      if (C > 1) cluster_sync_all();
-      if (rank != 0 && tid == 0) {
-        S.rule_prefix = ld_dsmem(&S.rule_prefix, 0u);
-        S.rule_shift = ld_dsmem(&S.rule_shift, 0u);
-        S.rule_cut = (int32_t)ld_dsmem(reinterpret_cast<const uint32_t *>(&S.rule_cut), 0u);
+      if (done) {
+        if (tid == 0) {
+          S.rule_prefix = prefix;
+          S.rule_shift = (uint32_t)shift;
+          S.rule_cut = INT32_MAX;
+        }
+      } else {
+        // ties at the full key: of the keys equal to `prefix`, the `need`
+        // with the lowest block indices are kept.  Radix rounds over the
+        // equal candidates' block indices, 8 bits at a time from the
+        // highest bit an index < n can have, find the cut index.
+        const uint32_t top = (uint32_t)n - 1u;
+        int ish = top ? ((32 - __clz((int)top) + 7) & ~7) : 8;  // index bits, rounded up
+        uint32_t iprefix = 0;  // the cut index's bits above ish
+        uint32_t *H = S.hist0;  // round 0's histogram is no longer read
+        for (int ir = 0; ir < 4; ++ir) {
+          const int sh = ish - 8;
+          if (tid < 256) H[tid] = 0u;
+          __syncthreads();
+          for (int32_t j = tid; j < nl; j += NT) {
+            if (cand_s[j] != prefix) continue;
+            int q = 0;
+            while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
+            const uint32_t gi = (uint32_t)(q * per) + (uint32_t)cand_li[j];
+            if (ish >= 32 || (gi >> ish) == iprefix)  // ascending: digit d counts in bin 255-d
+              atomicAdd(&H[255u - ((gi >> sh) & 255u)], 1u);
+          }
+          __syncthreads();
+          if (warp == 0) {
+            uint32_t B, above;
+            warp_find_bin(H, 256, need, lane, B, above);
+            if (lane == 0) {
+              S.sel_bin = (int32_t)B;
+              S.sel_above = above;
+            }
+          }
+          __syncthreads();
+          const uint32_t cB = H[S.sel_bin];
+          need -= S.sel_above;
+          iprefix = (iprefix << 8) | (255u - (uint32_t)S.sel_bin);
+          ish = sh;
+          __syncthreads();  // sel_bin and H are rewritten next round
+          if (cB == need || ish == 0) break;  // at ish == 0 a bin holds one index
+        }
+        if (tid == 0) {
+          S.rule_prefix = prefix;
+          S.rule_shift = 0;
+          S.rule_cut = (int32_t)((((uint64_t)iprefix + 1u) << ish) - 1u);
+        }
       }
       __syncthreads();
-    } else {
-      scan_ties = true;  // ---- fallback: rounds over every key (part B)
     }
+    // every CTA takes rank 0's rule
+    if (C > 1) cluster_sync_all();
+    if (rank != 0 && tid == 0) {
+      S.rule_prefix = ld_dsmem(&S.rule_prefix, 0u);
+      S.rule_shift = ld_dsmem(&S.rule_shift, 0u);
+      S.rule_cut = (int32_t)ld_dsmem(reinterpret_cast<const uint32_t *>(&S.rule_cut), 0u);
+    }
+    __syncthreads();
   }
 
   if (scan_ties) {

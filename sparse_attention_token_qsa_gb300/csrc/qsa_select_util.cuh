@@ -134,6 +134,37 @@ __device__ __forceinline__ void find_bin(const uint32_t *M, int nb, uint32_t nee
   __syncthreads();
 }
 
+// find_bin for two ranks at once (one scan): the bins holding the need_a-th
+// and the need_b-th largest keys (1 <= need_a, need_b <= the histogram's
+// total), written to bins[0] and bins[1] (shared memory, read after the call).
+template <int NT>
+__device__ __forceinline__ void find_two_bins(const uint32_t *M, int nb, uint32_t need_a,
+                                              uint32_t need_b, uint32_t *warp_tot, int32_t *bins) {
+  const int tid = threadIdx.x;
+  const int per = (nb + NT - 1) / NT;
+  const int hi = nb - 1 - tid * per;  // this thread's bins: hi, hi-1, ..., hi-per+1
+  uint32_t sum = 0;
+  for (int j = 0; j < per; ++j)
+    if (hi - j >= 0) sum += M[hi - j];
+  uint32_t total;
+  const uint32_t before = block_excl_scan<NT>(sum, warp_tot, total);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint32_t need = k == 0 ? need_a : need_b;
+    if (before < need && need <= before + sum) {
+      uint32_t acc = before;
+      for (int j = 0; j < per; ++j) {
+        acc += M[hi - j];
+        if (acc >= need) {
+          bins[k] = hi - j;
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
 // One warp's version of find_bin for the small rounds (nb <= 256): the bin
 // of H holding the need-th largest key and the count above it, returned to
 // every lane.  Warp-synchronous: no block barrier.

@@ -711,14 +711,14 @@ def decode_long(torch, qsa, device, hbm_gbs, ncu=False):
     }
 
 
-def decode_gather(torch, qsa, device, hbm_gbs, ncu=False):
+def decode_gather(torch, qsa, device, hbm_gbs, ncu=False, rows=64):
     """The decode chain after selection at 64k: 64 sequences, one row each at
     p = 65534 (2051 selected tokens: 512 kept blocks and the 3-token tail),
     each with its own paged K/V cache (pages of 16 tokens, 2 KV heads x 256
     bf16, the pages of a sequence shuffled over the pool).  Times the token
     lists of all 64 mask rows, the gather of their K/V rows, and one row's
     list + gather (rotating over the 64 rows so each call reads cold data)."""
-    rows, tokens = 64, TOKENS
+    tokens = TOKENS
     cols = tokens // 4
     g = torch.Generator(device=device)
     g.manual_seed(qi.seed_for(5))
@@ -805,6 +805,8 @@ def ncu_case(name: str):
         decode_long(torch, qsa, dev, 6800.0, ncu=True)
     elif name == "gather":
         decode_gather(torch, qsa, dev, 6800.0, ncu=True)
+    elif name == "gather_small":      # 8 rows: 1.1 GB of K/V pools
+        decode_gather(torch, qsa, dev, 6800.0, ncu=True, rows=8)
     else:
         raise SystemExit(f"unknown ncu case {name}")
     torch.cuda.synchronize()

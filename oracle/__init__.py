@@ -73,6 +73,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_mask_tokens.restype = i32
     lib.orc_gather.argtypes = [P, P, i32, i32, i32, P, i32, P]
     lib.orc_gather.restype = i32
+    lib.orc_sparse_attn.argtypes = [P, i32, i32, i32, P, P, P, i32, i32, P, i32, f64, P]
+    lib.orc_sparse_attn.restype = ctypes.c_int
     return lib
 
 
@@ -194,3 +196,18 @@ class Oracle:
         rc = self.L.orc_gather(_p(pool), _p(table), int(table.size), int(page_size), int(width),
                                _p(sel), int(sel.size), _p(out))
         return out[:len(sel)], int(rc)
+
+    def sparse_attn(self, q_row, nq: int, nkv: int, hd: int, k_pool, v_pool, table,
+                    page_size: int, sel, scale: float) -> tuple[np.ndarray, int]:
+        """One row's attention over its selected tokens: bf16 [nq * hd] and the
+        return code.  Pools are [slots, nkv, hd] bf16 bit patterns."""
+        q = _c(q_row, np.uint16)
+        kp, vp = _c(k_pool, np.uint16), _c(v_pool, np.uint16)
+        table = _c(table, np.int32)
+        sel = _c(sel, np.int32)
+        out = np.zeros(nq * hd, np.uint16)
+        rc = self.L.orc_sparse_attn(_p(q), int(nq), int(nkv), int(hd), _p(kp), _p(vp), _p(table),
+                                    int(table.size), int(page_size), _p(sel), int(sel.size),
+                                    float(scale), _p(out))
+        return out, int(rc)
+

@@ -21,6 +21,11 @@
  *           block's first position), decode_select (host sort by (-score, idx);
  *           the selected token list and the gather of its K/V rows from the
  *           paged cache into a contiguous scratch).
+ *  [PREFILL] atlas layers/qsa_select.rs prefill_select: rows at or past the
+ *           inert bound get their attention context replaced by attention
+ *           over exactly their selected set (kept blocks' tokens and the tail),
+ *           read from the paged K/V cache through the sequence's block table,
+ *           with nq query heads over nkv KV heads and a 1/sqrt(d) scale.
  *
  * Readings taken where the pages are silent (each also listed in the design doc):
  *  R1  bf16 <-> f32: widening is exact; narrowing is round-to-nearest-even,
@@ -43,6 +48,12 @@
  *      ((r0 + r1) + r2) + r3 in f32; score = f32(sum / sqrt(128)).
  *  R7  Selection compares real values, with -0.0 equal to +0.0; the canonical
  *      order is descending score then ascending block index.
+ *  R8  Sparse attention is softmax attention restricted to the selected
+ *      tokens: query head h reads KV head h / (nq / nkv) (consecutive query
+ *      heads share a KV head); logits s_j = (q_h . k_j) * scale with the dot
+ *      exact in double; weights exp(s_j - max s) in double; output
+ *      sum_j w_j v_j / sum_j w_j in double, rounded to f32 and then to bf16
+ *      (the attention output's dtype).  A row with no selected token gets zeros.
  *
  * Build: plain C11, no fast-math, no FMA contraction (-ffp-contract=off).
  */
@@ -359,3 +370,69 @@ int orc_gather(const uint16_t *pool, const int32_t *table, int32_t table_len, in
     }
     return ORC_OK;
 }
+
+/* The pool slot of token t: its page's physical index, then its place in the page. */
+static int64_t orc_attn_slot(const int32_t *table, int32_t page_size, int32_t t)
+{
+    const int32_t page = t / page_size;
+    return (int64_t)table[page] * page_size + (t - page * page_size);
+}
+
+/*
+ * [PREFILL] + R8: one query row's sparse attention.  q holds nq heads of hd
+ * bf16 values; the pools hold [slots, nkv, hd] bf16 (slot = page * page_size +
+ * t % page_size, page = table[t / page_size]); out receives nq * hd bf16.
+ * Returns ORC_ERR_INVALID_VALUE (out unspecified) at a token outside
+ * [0, table_len * page_size).
+ */
+int orc_sparse_attn(const uint16_t *q, int32_t nq, int32_t nkv, int32_t hd, const uint16_t *k_pool,
+                    const uint16_t *v_pool, const int32_t *table, int32_t table_len,
+                    int32_t page_size, const int32_t *sel, int32_t n_sel, double scale,
+                    uint16_t *out)
+{
+    if (nq <= 0 || nkv <= 0 || nq % nkv != 0 || hd <= 0)
+        return ORC_ERR_INVALID_VALUE;
+    for (int32_t j = 0; j < n_sel; ++j)
+        if (sel[j] < 0 || sel[j] / page_size >= table_len)
+            return ORC_ERR_INVALID_VALUE;
+    const int32_t group = nq / nkv;
+    double *w = (double *)malloc(sizeof(double) * (n_sel > 0 ? n_sel : 1));
+    double *acc = (double *)malloc(sizeof(double) * hd);
+    if (!w || !acc) {
+        free(w);
+        free(acc);
+        return ORC_ERR_INVALID_VALUE;
+    }
+    for (int32_t h = 0; h < nq; ++h) {
+        const int32_t g = h / group;
+        const uint16_t *qh = q + (int64_t)h * hd;
+        double mx = -INFINITY;
+        for (int32_t j = 0; j < n_sel; ++j) {
+            const int32_t t = sel[j];
+            const uint16_t *k = k_pool + (orc_attn_slot(table, page_size, t) * nkv + g) * hd;
+            double d = 0.0;
+            for (int32_t e = 0; e < hd; ++e)
+                d += (double)orc_widen(qh[e]) * (double)orc_widen(k[e]);
+            w[j] = d * scale;
+            if (w[j] > mx)
+                mx = w[j];
+        }
+        double den = 0.0;
+        for (int32_t e = 0; e < hd; ++e)
+            acc[e] = 0.0;
+        for (int32_t j = 0; j < n_sel; ++j) {
+            const int32_t t = sel[j];
+            const uint16_t *v = v_pool + (orc_attn_slot(table, page_size, t) * nkv + g) * hd;
+            const double wj = exp(w[j] - mx);
+            den += wj;
+            for (int32_t e = 0; e < hd; ++e)
+                acc[e] += wj * (double)orc_widen(v[e]);
+        }
+        for (int32_t e = 0; e < hd; ++e)
+            out[(int64_t)h * hd + e] = n_sel > 0 ? orc_narrow((float)(acc[e] / den)) : 0;
+    }
+    free(w);
+    free(acc);
+    return ORC_OK;
+}
+

@@ -519,12 +519,139 @@ def test_gather_refuses_tokens_past_the_table(orc):
     assert orc.gather(pool, table, 16, 8, np.array([32], np.int32))[1] == 1
     assert orc.gather(pool, table, 16, 8, np.array([-1], np.int32))[1] == 1
 
+# --------------------------------------------------------------------------
+# sparse attention over the selected tokens (atlas qsa_select.rs prefill_select)
+# --------------------------------------------------------------------------
+
+def bf16_ulp_close(got, want, ulps=1):
+    """bf16 bit patterns within `ulps` units in the last place (same sign)."""
+    g = np.asarray(got, np.uint16).astype(np.int32)
+    w = np.asarray(want, np.uint16).astype(np.int32)
+    return bool(np.all(np.abs(g - w) <= ulps))
+
+
+def attn_case(rng, nq=4, nkv=2, hd=16, page_size=4, pages=12, table_len=10):
+    k = qi.normal_bf16(rng, (pages * page_size, nkv * hd))
+    v = qi.normal_bf16(rng, (pages * page_size, nkv * hd))
+    table = rng.permutation(pages)[:table_len].astype(np.int32)
+    q = qi.normal_bf16(rng, (nq * hd,))
+    return q, k, v, table
+
+
+def test_sparse_attn_one_token_is_its_value_row(orc):
+    """One selected token: every head's output is that token's V row of the
+    head's KV group (heads 0..G-1 read KV head 0, the next G KV head 1...)."""
+    rng = np.random.default_rng(21)
+    for nq, nkv in ((4, 2), (6, 3), (4, 1), (2, 2)):
+        hd = 16
+        q, k, v, table = attn_case(rng, nq, nkv, hd)
+        t = 17
+        out, rc = orc.sparse_attn(q, nq, nkv, hd, k, v, table, 4, np.array([t], np.int32), 0.25)
+        assert rc == 0
+        slot = table[t // 4] * 4 + t % 4
+        vrow = v[slot].reshape(nkv, hd)
+        for h in range(nq):
+            assert np.array_equal(out.reshape(nq, hd)[h], vrow[h // (nq // nkv)]), (nq, nkv, h)
+
+
+def test_sparse_attn_equal_logits_give_the_mean(orc):
+    """q = 0 makes every logit equal: the output is the plain mean of the
+    selected V rows (rounded to f32, then bf16)."""
+    rng = np.random.default_rng(22)
+    nq, nkv, hd, ps = 4, 2, 16, 4
+    _, k, v, table = attn_case(rng, nq, nkv, hd, ps)
+    q = np.zeros(nq * hd, np.uint16)
+    sel = np.array([0, 3, 9, 21, 30, 39], np.int32)
+    out, rc = orc.sparse_attn(q, nq, nkv, hd, k, v, table, ps, sel, 0.7)
+    assert rc == 0
+    slots = table[sel // ps] * ps + sel % ps
+    vv = widen(v[slots]).astype(np.float64).reshape(len(sel), nkv, hd)
+    for h in range(nq):
+        mean = vv[:, h // 2, :].mean(axis=0).astype(np.float32)
+        want = qi.to_bf16_bits(mean)
+        assert bf16_ulp_close(out.reshape(nq, hd)[h], want), h
+
+
+def test_sparse_attn_two_tokens_logistic_weights(orc):
+    """Two tokens whose logits differ by D: weights sigmoid(D) and 1 - sigmoid(D)
+    (the closed form of a two-way softmax), with D = scale * (q . (k1 - k2))."""
+    nq, nkv, hd, ps = 2, 1, 8, 4
+    table = np.arange(4, dtype=np.int32)
+    k = np.zeros((16, hd), np.float32)
+    v = np.zeros((16, hd), np.float32)
+    k[5, 0], k[9, 0] = 1.5, -0.5
+    v[5] = np.linspace(-1, 1, hd)
+    v[9] = np.linspace(2, -3, hd)
+    q = np.zeros((nq, hd), np.float32)
+    q[0, 0], q[1, 0] = 2.0, -1.0
+    scale = 0.375
+    out, rc = orc.sparse_attn(qi.to_bf16_bits(q.ravel()), nq, nkv, hd, qi.to_bf16_bits(k),
+                              qi.to_bf16_bits(v), table, ps, np.array([5, 9], np.int32), scale)
+    assert rc == 0
+    for h in range(nq):
+        d = scale * q[h, 0] * (k[5, 0] - k[9, 0])
+        w = 1.0 / (1.0 + math.exp(-d))
+        want = qi.to_bf16_bits((w * v[5] + (1 - w) * v[9]).astype(np.float32))
+        assert bf16_ulp_close(out.reshape(nq, hd)[h], want), h
+
+
+def test_sparse_attn_scale_multiplies_the_logits(orc):
+    """scale s with q equals scale 1 with s*q when s is a power of two (s*q is
+    exact in bf16)."""
+    rng = np.random.default_rng(23)
+    nq, nkv, hd, ps = 4, 2, 16, 4
+    q, k, v, table = attn_case(rng, nq, nkv, hd, ps)
+    sel = np.array([1, 2, 6, 11, 25, 38], np.int32)
+    a, _ = orc.sparse_attn(q, nq, nkv, hd, k, v, table, ps, sel, 0.25)
+    q4 = qi.to_bf16_bits(widen(q) * np.float32(0.25))
+    b, _ = orc.sparse_attn(q4, nq, nkv, hd, k, v, table, ps, sel, 1.0)
+    assert np.array_equal(a, b)
+    c, _ = orc.sparse_attn(q, nq, nkv, hd, k, v, table, ps, sel, 1.0)
+    assert not np.array_equal(a, c)
+
+
+def test_sparse_attn_reads_through_the_page_table(orc):
+    """The same row through a shuffled page table and through the identity
+    table over a pool whose pages numpy rearranged: identical outputs; and a
+    permuted token list gives the same output up to summation order."""
+    rng = np.random.default_rng(24)
+    nq, nkv, hd, ps = 4, 2, 16, 4
+    q, k, v, table = attn_case(rng, nq, nkv, hd, ps)
+    sel = np.array([0, 5, 6, 7, 13, 22, 31, 39], np.int32)
+    a, rc = orc.sparse_attn(q, nq, nkv, hd, k, v, table, ps, sel, 0.3)
+    assert rc == 0
+    kc = k.reshape(-1, ps, nkv * hd)[table].reshape(-1, nkv * hd)
+    vc = v.reshape(-1, ps, nkv * hd)[table].reshape(-1, nkv * hd)
+    b, _ = orc.sparse_attn(q, nq, nkv, hd, kc, vc, np.arange(len(table), dtype=np.int32), ps, sel,
+                           0.3)
+    assert np.array_equal(a, b)
+    c, _ = orc.sparse_attn(q, nq, nkv, hd, k, v, table, ps, sel[::-1].copy(), 0.3)
+    assert bf16_ulp_close(a, c)
+
+
+def test_sparse_attn_refuses_tokens_past_the_table(orc):
+    rng = np.random.default_rng(25)
+    q, k, v, table = attn_case(rng)
+    assert orc.sparse_attn(q, 4, 2, 16, k, v, table, 4, np.array([39], np.int32), 1.0)[1] == 0
+    assert orc.sparse_attn(q, 4, 2, 16, k, v, table, 4, np.array([40], np.int32), 1.0)[1] == 1
+    assert orc.sparse_attn(q, 4, 2, 16, k, v, table, 4, np.array([-2], np.int32), 1.0)[1] == 1
+    out, rc = orc.sparse_attn(q, 4, 2, 16, k, v, table, 4, np.zeros(0, np.int32), 1.0)
+    assert rc == 0 and not out.any()          # no selected token: zeros
+
 MUTANTS = {
     "tokens_count_capped": ("    return n;\n}\n\n/*\n * [LAYER] metrale layers/qsa.rs decode_select's gather",
                             "    return n < cap ? n : cap;\n}\n\n/*\n * [LAYER] metrale layers/qsa.rs decode_select's gather"),
     "gather_page_slot_swapped": ("table[t / page_size] * page_size + t % page_size",
                                  "table[t % page_size] * page_size + t / page_size"),
     "gather_ignores_table": ("(int64_t)table[t / page_size] * page_size", "(int64_t)(t / page_size) * page_size"),
+    "attn_heads_interleaved": ("const int32_t g = h / group;", "const int32_t g = h % nkv;"),
+    "attn_no_scale": ("w[j] = d * scale;", "w[j] = d;"),
+    "attn_slot_ignores_table": ("return (int64_t)table[page] * page_size + (t - page * page_size);",
+                                "return (int64_t)page * page_size + (t - page * page_size);"),
+    "attn_drops_last_token": ("for (int32_t j = 0; j < n_sel; ++j) {\n            const int32_t t = sel[j];\n            const uint16_t *v",
+                              "for (int32_t j = 0; j + 1 < n_sel; ++j) {\n            const int32_t t = sel[j];\n            const uint16_t *v"),
+    "attn_values_from_keys": ("const uint16_t *v = v_pool + (", "const uint16_t *v = k_pool + ("),
+    "attn_no_normalisation": ("orc_narrow((float)(acc[e] / den))", "orc_narrow((float)acc[e])"),
     "drop_tail": ("mask_row[t] = 1;", "(void)t;"),
     "keep_one_fewer": ("for (int32_t i = 0; i < keep; ++i)", "for (int32_t i = 0; i < keep - 1; ++i)"),
     "keep_one_more": ("for (int32_t i = 0; i < keep; ++i)", "for (int32_t i = 0; i <= keep && i < blocks; ++i)"),
@@ -558,6 +685,9 @@ PIN_TESTS = [
     test_score_onehot_closed_form, test_score_relu_is_per_head,
     test_mask_tokens_equals_nonzero, test_mask_tokens_of_a_selection_is_the_pages_list,
     test_gather_equals_fancy_indexing, test_gather_refuses_tokens_past_the_table,
+    test_sparse_attn_one_token_is_its_value_row, test_sparse_attn_equal_logits_give_the_mean,
+    test_sparse_attn_two_tokens_logistic_weights, test_sparse_attn_scale_multiplies_the_logits,
+    test_sparse_attn_reads_through_the_page_table, test_sparse_attn_refuses_tokens_past_the_table,
 ]
 
 

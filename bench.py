@@ -512,6 +512,7 @@ def run_ours(args, rank, world, device):
         secondary["prefill_chunk_64k"] = prefill_chunk(torch, qsa, device, hbm_gbs, bf16_tf)
         secondary["decode_long_32seq"] = decode_long(torch, qsa, device, hbm_gbs)
         secondary["decode_gather_64k"] = decode_gather(torch, qsa, device, hbm_gbs)
+        secondary["prefill_attn_64k"] = prefill_attn(torch, qsa, device, hbm_gbs, bf16_tf)
 
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
@@ -782,6 +783,61 @@ def decode_gather(torch, qsa, device, hbm_gbs, ncu=False, rows=64):
     }
 
 
+def prefill_attn(torch, qsa, device, hbm_gbs, bf16_tf, ncu=False, rows=4096):
+    """Sparse prefill attention on the chunked-prefill shape: rows at positions
+    65536 - rows .. 65535 of one 64k sequence, each attending its 2048 selected
+    tokens plus tail (lists from the device selection of random scores), 16
+    query heads over 2 KV heads of 256, pages of 16 shuffled over the pool."""
+    tokens, first = TOKENS, TOKENS - rows
+    nq, nkv, hd, page = 16, 2, 256, 16
+    cols = tokens // 4
+    g = torch.Generator(device=device)
+    g.manual_seed(qi.seed_for(7))
+    sc = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32)
+    pos = torch.arange(first, tokens, dtype=torch.int32, device=device)
+    mask = torch.empty((rows, tokens), dtype=torch.uint8, device=device)
+    st = qsa.new_status(device)
+    qsa.qsa_select_mask(sc, cols, pos, rows, tokens, BUDGET, mask, st)
+    sel_cols = BUDGET + 3
+    sel = torch.empty((rows, sel_cols), dtype=torch.int32, device=device)
+    n_sel = torch.zeros(rows, dtype=torch.int32, device=device)
+    qsa.qsa_mask_tokens(mask, rows, tokens, sel, sel_cols, n_sel)
+    del sc, mask
+    table_len = tokens // page
+    kv_shape = (table_len * page, nkv * hd)
+    k_pool = (torch.randn(kv_shape, generator=g, device=device) * 1.0).to(torch.bfloat16).view(torch.int16)
+    v_pool = (torch.randn(kv_shape, generator=g, device=device) * 1.0).to(torch.bfloat16).view(torch.int16)
+    table = torch.randperm(table_len, generator=g, device=device).to(torch.int32)
+    q = (torch.randn((rows, nq * hd), generator=g, device=device) * 2.0).to(torch.bfloat16).view(torch.int16)
+    out = torch.empty((rows, nq * hd), dtype=torch.int16, device=device)
+
+    def attn():
+        qsa.qsa_sparse_attn(q, nq * hd, nq, nkv, hd, k_pool, v_pool, table_len, page, table,
+                            table_len, 0, sel, sel_cols, n_sel, rows, sel_cols, 1.0 / 16.0, out,
+                            nq * hd, st)
+
+    for _ in range(2 if ncu else 3):
+        attn()
+    torch.cuda.synchronize()
+    if ncu:
+        return None
+    t = time_fn(torch, attn, 10)
+    code, row = qsa.qsa_read_status(st)
+    assert code == 0, (code, row)
+    n = int(n_sel.sum())
+    gathered = n * nkv * hd * 2 * 2 + rows * nq * hd * 2 * 2 + n * 4
+    unique = 2 * kv_shape[0] * kv_shape[1] * 2 + rows * nq * hd * 2 * 2 + n * 4
+    flops = 4.0 * nq * hd * n
+    return {
+        "rows": rows, "selected_tokens": n, "heads": f"{nq}q/{nkv}kv x {hd}", "page_size": page,
+        "us": t * 1000.0, "rows_per_s": rows / (t * 1e-3),
+        "gathered_gbs": gathered / (t * 1e-3) / 1e9,
+        "unique_bytes": unique, "unique_frac_of_measured_hbm": unique / (t * 1e-3) / 1e9 / hbm_gbs,
+        "achieved_tflops": flops / (t * 1e-3) / 1e12,
+        "frac_of_measured_bf16": flops / (t * 1e-3) / 1e12 / bf16_tf,
+    }
+
+
 # ------------------------------------------------------------ ncu cases
 
 def ncu_case(name: str):
@@ -805,6 +861,8 @@ def ncu_case(name: str):
         decode_long(torch, qsa, dev, 6800.0, ncu=True)
     elif name == "gather":
         decode_gather(torch, qsa, dev, 6800.0, ncu=True)
+    elif name == "attn":
+        prefill_attn(torch, qsa, dev, 6800.0, 1900.0, ncu=True, rows=512)
     elif name == "gather_small":      # 8 rows: 1.1 GB of K/V pools
         decode_gather(torch, qsa, dev, 6800.0, ncu=True, rows=8)
     else:

@@ -327,6 +327,42 @@ qsa_status qsa_gather_kv(const uint16_t *k_pool, const uint16_t *v_pool, int32_t
                          uint16_t *k_out, uint16_t *v_out, int64_t out_rows, int32_t *dev_status,
                          void *stream);
 
+/*
+ * Attention of each query row over its selected tokens only.  Source: atlas
+ * layers/qsa_select.rs prefill_select (a row past the inert bound gets its
+ * attention context replaced by attention over exactly its selected set --
+ * kept blocks' tokens and the tail -- read from the paged K/V cache through
+ * the sequence's block table, nq query heads over nkv KV heads, a 1/sqrt(d)
+ * scale); metrale layers/qsa.rs module comment (the top budget/ratio blocks
+ * plus the incomplete tail).
+ *  q        DEVICE bf16, row i at q + i*q_stride: nq heads of head_dim values
+ *           (already rotated), 16-byte aligned, q_stride a multiple of 8 and
+ *           >= nq*head_dim.  Query head h reads KV head h / (nq / nkv).
+ *  k_pool, v_pool  DEVICE bf16 [pool_pages * page_size, nkv, head_dim],
+ *           16-byte aligned; head_dim is 128 or 256.
+ *  table, table_len, table_cols, page_size: as in qsa_gather_kv (token t of
+ *           row i is in page table[i*table_cols + t / page_size], slot
+ *           t % page_size; table_cols = 0 shares one table).
+ *  sel, sel_cols, n_sel: the selected tokens as qsa_mask_tokens writes them;
+ *           row i attends its first min(n_sel[i], max_sel) tokens
+ *           (max_sel <= sel_cols).  A row with none gets zeros.
+ *  scale    multiplies every logit q_h . k (finite; typically 1/sqrt(head_dim)).
+ *  out      DEVICE bf16, row i at out + i*out_stride (nq*head_dim values),
+ *           16-byte aligned, out_stride a multiple of 8 and >= nq*head_dim.
+ *  Softmax and accumulation run in f32 with the weights rounded to bf16 for
+ *  the weighted sum of V (its normaliser uses the same rounded weights).  A
+ *  token outside the table, or a table entry outside the pool, is recorded
+ *  as QSA_ERR_TOKEN_RANGE and left out; a row that reports it has an
+ *  unspecified output.
+ */
+qsa_status qsa_sparse_attn(const uint16_t *q, int64_t q_stride, int32_t nq, int32_t nkv,
+                           int32_t head_dim, const uint16_t *k_pool, const uint16_t *v_pool,
+                           int32_t pool_pages, int32_t page_size, const int32_t *table,
+                           int32_t table_len, int64_t table_cols, const int32_t *sel,
+                           int64_t sel_cols, const int32_t *n_sel, int32_t n_rows, int32_t max_sel,
+                           float scale, uint16_t *out, int64_t out_stride, int32_t *dev_status,
+                           void *stream);
+
 /* Zero a DEVICE status word (stream-ordered). */
 qsa_status qsa_reset_status(int32_t *dev_status, void *stream);
 

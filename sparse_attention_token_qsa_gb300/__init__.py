@@ -37,7 +37,7 @@ EXPORTED = ("qsa_version", "qsa_status_string", "qsa_rope_tables", "qsa_pool_blo
             "qsa_score_rows", "qsa_score_rows_with", "qsa_score_workspace_bytes",
             "qsa_score_rows_noalloc", "qsa_select_mask", "qsa_index_select",
             "qsa_decode_workspace_bytes", "qsa_decode_index_select", "qsa_mask_tokens",
-            "qsa_gather_kv", "qsa_reset_status", "qsa_read_status")
+            "qsa_gather_kv", "qsa_sparse_attn", "qsa_reset_status", "qsa_read_status")
 
 
 class QsaError(RuntimeError):
@@ -73,6 +73,8 @@ def _load() -> ctypes.CDLL:
         "qsa_mask_tokens": ([P, i32, i32, P, i64, P, P], i32),
         "qsa_gather_kv": ([P, P, i32, i32, P, i32, i64, i32, P, i64, P, i32, i32, P, P, i64, P, P],
                           i32),
+        "qsa_sparse_attn": ([P, i64, i32, i32, i32, P, P, i32, i32, P, i32, i64, P, i64, P, i32,
+                             i32, f32, P, i64, P, P], i32),
         "qsa_reset_status": ([P, P], i32),
         "qsa_read_status": ([P, P, P, P], i32),
     }
@@ -273,6 +275,19 @@ def qsa_gather_kv(k_pool, v_pool, width, pool_pages, table, table_len, table_col
                               _dev(k_out, "k_out"), _dev(v_out, "v_out"), int(out_rows),
                               _dev(dev_status, "dev_status"), _stream(stream)),
            "qsa_gather_kv")
+
+
+def qsa_sparse_attn(q, q_stride, nq, nkv, head_dim, k_pool, v_pool, pool_pages, page_size, table,
+                    table_len, table_cols, sel, sel_cols, n_sel, n_rows, max_sel, scale, out,
+                    out_stride, dev_status, stream=None) -> None:
+    _check(_lib.qsa_sparse_attn(_dev(q, "q"), int(q_stride), int(nq), int(nkv), int(head_dim),
+                                _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"), int(pool_pages),
+                                int(page_size), _dev(table, "table"), int(table_len),
+                                int(table_cols), _dev(sel, "sel"), int(sel_cols),
+                                _dev(n_sel, "n_sel"), int(n_rows), int(max_sel), float(scale),
+                                _dev(out, "out"), int(out_stride), _dev(dev_status, "dev_status"),
+                                _stream(stream)),
+           "qsa_sparse_attn")
 
 
 def qsa_reset_status(dev_status, stream=None) -> None:

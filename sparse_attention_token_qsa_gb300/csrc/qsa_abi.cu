@@ -8,6 +8,7 @@
 // pointer is formed) and PR #1160 "score QSA token-indexer blocks in native
 // CUDA" (rows and visible_len as separate device arrays; the RoPE tables are
 // inputs; only rms_eps is a run-time scalar).
+#include <cmath>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -321,6 +322,41 @@ qsa_status qsa_gather_kv(const uint16_t *k_pool, const uint16_t *v_pool, int32_t
                                          table_cols, page_size, sel, sel_cols, n_sel, n_rows,
                                          max_sel, k_out, v_out, out_rows, dev_status,
                                          (cudaStream_t)stream));
+}
+
+qsa_status qsa_sparse_attn(const uint16_t *q, int64_t q_stride, int32_t nq, int32_t nkv,
+                           int32_t head_dim, const uint16_t *k_pool, const uint16_t *v_pool,
+                           int32_t pool_pages, int32_t page_size, const int32_t *table,
+                           int32_t table_len, int64_t table_cols, const int32_t *sel,
+                           int64_t sel_cols, const int32_t *n_sel, int32_t n_rows, int32_t max_sel,
+                           float scale, uint16_t *out, int64_t out_stride, int32_t *dev_status,
+                           void *stream) {
+  if (n_rows < 0 || max_sel < 0 || pool_pages < 0 || table_len < 0 || table_cols < 0 ||
+      sel_cols < 0 || q_stride < 0 || out_stride < 0)
+    return QSA_ERR_INVALID_VALUE;
+  if (n_rows == 0) return QSA_OK;
+  if (nq <= 0 || nkv <= 0 || nq % nkv != 0 || (head_dim != 128 && head_dim != 256) ||
+      page_size <= 0 || max_sel > sel_cols || !std::isfinite(scale))
+    return QSA_ERR_INVALID_VALUE;
+  if (table_cols != 0 && table_cols < table_len) return QSA_ERR_INVALID_VALUE;
+  const int64_t row_len = (int64_t)nq * head_dim;
+  if (q_stride < row_len || out_stride < row_len || (q_stride & 7) != 0 || (out_stride & 7) != 0)
+    return QSA_ERR_INVALID_VALUE;
+  if (!q || !k_pool || !v_pool || !out || !n_sel || !dev_status ||
+      (max_sel > 0 && (!sel || !table)))
+    return QSA_ERR_INVALID_VALUE;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return QSA_ERR_INVALID_VALUE;
+  const int64_t chunks = (nq / nkv + 7) / 8;
+  if ((int64_t)n_rows * nkv * chunks > INT32_MAX || (int64_t)table_len * page_size > INT32_MAX ||
+      (int64_t)pool_pages * page_size * nkv * head_dim > ((int64_t)1 << 46) ||
+      (int64_t)n_rows * (q_stride > out_stride ? q_stride : out_stride) > ((int64_t)1 << 46) ||
+      (int64_t)n_rows * sel_cols > ((int64_t)1 << 46))
+    return QSA_ERR_INVALID_VALUE;
+  return from_cuda(qsa::launch_sparse_attn(q, q_stride, nq, nkv, head_dim, k_pool, v_pool,
+                                           pool_pages, page_size, table, table_len, table_cols,
+                                           sel, sel_cols, n_sel, n_rows, max_sel, scale, out,
+                                           out_stride, dev_status, (cudaStream_t)stream));
 }
 
 qsa_status qsa_reset_status(int32_t *dev_status, void *stream) {

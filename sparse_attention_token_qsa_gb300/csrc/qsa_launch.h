@@ -92,4 +92,14 @@ cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t
                           int32_t n_rows, int32_t tokens, int32_t budget, uint8_t *mask,
                           int32_t *status, cudaStream_t stream);
 
+// Sparse attention of each row over its selected tokens (qsa_attn.cu);
+// head_dim is 128 or 256, nq a multiple of nkv.
+cudaError_t launch_sparse_attn(const uint16_t *q, int64_t q_stride, int32_t nq, int32_t nkv,
+                               int32_t head_dim, const uint16_t *k_pool, const uint16_t *v_pool,
+                               int32_t pool_pages, int32_t page_size, const int32_t *table,
+                               int32_t table_len, int64_t table_cols, const int32_t *sel,
+                               int64_t sel_cols, const int32_t *n_sel, int32_t n_rows,
+                               int32_t max_sel, float scale, uint16_t *out, int64_t out_stride,
+                               int32_t *status, cudaStream_t stream);
+
 }  // namespace qsa

@@ -75,6 +75,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_gather.restype = i32
     lib.orc_sparse_attn.argtypes = [P, i32, i32, i32, P, P, P, i32, i32, P, i32, f64, P]
     lib.orc_sparse_attn.restype = ctypes.c_int
+    lib.orc_proj.argtypes = [P, i64, P, i32, i32, i32, P, i64]
+    lib.orc_proj.restype = ctypes.c_int
     return lib
 
 
@@ -210,4 +212,15 @@ class Oracle:
                                     int(table.size), int(page_size), _p(sel), int(sel.size),
                                     float(scale), _p(out))
         return out, int(rc)
+
+    def proj(self, x, w) -> tuple[np.ndarray, int]:
+        """y = x W^T for bf16 x [rows, hidden] and W [out, hidden]: bf16 [rows, out]."""
+        x = _c(x, np.uint16)
+        w = _c(w, np.uint16)
+        rows, hidden = x.shape
+        out_cols = w.shape[0]
+        y = np.zeros((max(rows, 1), out_cols), np.uint16)
+        rc = self.L.orc_proj(_p(x), int(hidden), _p(w), int(rows), int(hidden), int(out_cols),
+                             _p(y), int(out_cols))
+        return y[:rows], int(rc)
 

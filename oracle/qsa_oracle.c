@@ -25,7 +25,10 @@
  *           inert bound get their attention context replaced by attention
  *           over exactly their selected set (kept blocks' tokens and the tail),
  *           read from the paged K/V cache through the sequence's block table,
- *           with nq query heads over nkv KV heads and a 1/sqrt(d) scale.
+ *           with nq query heads over nkv KV heads and a 1/sqrt(d) scale;
+ *           before scoring, the indexer's fused q|k row comes from a dense bf16
+ *           projection of the normed hidden states (hidden -> 640) in slabs of
+ *           2048 rows.
  *
  * Readings taken where the pages are silent (each also listed in the design doc):
  *  R1  bf16 <-> f32: widening is exact; narrowing is round-to-nearest-even,
@@ -54,6 +57,9 @@
  *      exact in double; weights exp(s_j - max s) in double; output
  *      sum_j w_j v_j / sum_j w_j in double, rounded to f32 and then to bf16
  *      (the attention output's dtype).  A row with no selected token gets zeros.
+ *  R9  The projection y = x W^T (W stored [out, in], as a linear layer keeps
+ *      it) sums the exact bf16 x bf16 products in double, rounds to f32, then
+ *      to bf16 (the output dtype; the pages call it a bf16 dense projection).
  *
  * Build: plain C11, no fast-math, no FMA contraction (-ffp-contract=off).
  */
@@ -433,6 +439,30 @@ int orc_sparse_attn(const uint16_t *q, int32_t nq, int32_t nkv, int32_t hd, cons
     }
     free(w);
     free(acc);
+    return ORC_OK;
+}
+
+/*
+ * [PREFILL] + R9: the index_qk_proj projection of one slab.  x holds n_rows
+ * rows of `hidden` bf16 at row stride x_stride; w holds out_cols rows of
+ * `hidden` bf16 (a linear layer's [out, in] weight); y receives n_rows rows of
+ * out_cols bf16 at row stride y_stride.
+ */
+int orc_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, int32_t n_rows,
+             int32_t hidden, int32_t out_cols, uint16_t *y, int64_t y_stride)
+{
+    if (n_rows < 0 || hidden <= 0 || out_cols <= 0)
+        return ORC_ERR_INVALID_VALUE;
+    for (int32_t r = 0; r < n_rows; ++r) {
+        const uint16_t *xr = x + (int64_t)r * x_stride;
+        for (int32_t n = 0; n < out_cols; ++n) {
+            const uint16_t *wn = w + (int64_t)n * hidden;
+            double acc = 0.0;
+            for (int32_t k = 0; k < hidden; ++k)
+                acc += (double)orc_widen(xr[k]) * (double)orc_widen(wn[k]);
+            y[(int64_t)r * y_stride + n] = orc_narrow((float)acc);
+        }
+    }
     return ORC_OK;
 }
 

@@ -638,11 +638,54 @@ def test_sparse_attn_refuses_tokens_past_the_table(orc):
     out, rc = orc.sparse_attn(q, 4, 2, 16, k, v, table, 4, np.zeros(0, np.int32), 1.0)
     assert rc == 0 and not out.any()          # no selected token: zeros
 
+# --------------------------------------------------------------------------
+# the index_qk_proj projection y = x W^T (a dense bf16 linear layer)
+# --------------------------------------------------------------------------
+
+def test_proj_selecting_weights_copy_columns(orc):
+    """W whose row n is the unit vector e_{perm(n)}: y[:, n] = x[:, perm(n)]
+    exactly (a single exact product per output)."""
+    rng = np.random.default_rng(31)
+    hidden, out = 48, 16
+    x = qi.normal_bf16(rng, (7, hidden))
+    perm = rng.permutation(hidden)[:out]
+    w = np.zeros((out, hidden), np.float32)
+    w[np.arange(out), perm] = 1.0
+    y, rc = orc.proj(x, qi.to_bf16_bits(w))
+    assert rc == 0
+    assert np.array_equal(y, x[:, perm])
+
+
+def test_proj_matches_numpy_matmul(orc):
+    """Against numpy's float64 matmul of the widened operands, rounded to f32
+    then bf16 (equal up to the double summation order: at most one bf16 step)."""
+    rng = np.random.default_rng(32)
+    x = qi.normal_bf16(rng, (9, 200))
+    w = qi.normal_bf16(rng, (24, 200), std=0.05)
+    y, rc = orc.proj(x, w)
+    assert rc == 0
+    ref = (widen(x).astype(np.float64) @ widen(w).astype(np.float64).T).astype(np.float32)
+    want = qi.to_bf16_bits(ref)
+    assert np.all(np.abs(y.astype(np.int32) - want.astype(np.int32)) <= 1)
+    assert np.mean(y == want) > 0.99
+
+
+def test_proj_is_linear_in_powers_of_two(orc):
+    """y(2x) = 2 y(x) and y(x, -W) = -y(x, W), bit for bit."""
+    rng = np.random.default_rng(33)
+    x = qi.normal_bf16(rng, (4, 64))
+    w = qi.normal_bf16(rng, (8, 64))
+    y, _ = orc.proj(x, w)
+    y2, _ = orc.proj(qi.to_bf16_bits(widen(x) * 2), w)
+    assert np.array_equal(widen(y2), widen(y) * 2)
+    yn, _ = orc.proj(x, w ^ np.uint16(0x8000))
+    assert np.array_equal(widen(yn), -widen(y))
+
 MUTANTS = {
     "tokens_count_capped": ("    return n;\n}\n\n/*\n * [LAYER] metrale layers/qsa.rs decode_select's gather",
                             "    return n < cap ? n : cap;\n}\n\n/*\n * [LAYER] metrale layers/qsa.rs decode_select's gather"),
-    "gather_page_slot_swapped": ("table[t / page_size] * page_size + t % page_size",
-                                 "table[t % page_size] * page_size + t / page_size"),
+    "gather_page_not_scaled": ("(int64_t)table[t / page_size] * page_size + t % page_size",
+                               "(int64_t)table[t / page_size] + t % page_size"),
     "gather_ignores_table": ("(int64_t)table[t / page_size] * page_size", "(int64_t)(t / page_size) * page_size"),
     "attn_heads_interleaved": ("const int32_t g = h / group;", "const int32_t g = h % nkv;"),
     "attn_no_scale": ("w[j] = d * scale;", "w[j] = d;"),
@@ -652,6 +695,12 @@ MUTANTS = {
                               "for (int32_t j = 0; j + 1 < n_sel; ++j) {\n            const int32_t t = sel[j];\n            const uint16_t *v"),
     "attn_values_from_keys": ("const uint16_t *v = v_pool + (", "const uint16_t *v = k_pool + ("),
     "attn_no_normalisation": ("orc_narrow((float)(acc[e] / den))", "orc_narrow((float)acc[e])"),
+    "proj_weight_transposed": ("const uint16_t *wn = w + (int64_t)n * hidden;",
+                               "const uint16_t *wn = w + n;"),
+    "proj_drops_last_k": ("for (int32_t k = 0; k < hidden; ++k)\n                acc +=",
+                          "for (int32_t k = 0; k + 1 < hidden; ++k)\n                acc +="),
+    "proj_rounds_through_bf16_early": ("acc += (double)orc_widen(xr[k]) * (double)orc_widen(wn[k]);",
+                                       "acc = orc_round_bf16((float)(acc + (double)orc_widen(xr[k]) * (double)orc_widen(wn[k])));"),
     "drop_tail": ("mask_row[t] = 1;", "(void)t;"),
     "keep_one_fewer": ("for (int32_t i = 0; i < keep; ++i)", "for (int32_t i = 0; i < keep - 1; ++i)"),
     "keep_one_more": ("for (int32_t i = 0; i < keep; ++i)", "for (int32_t i = 0; i <= keep && i < blocks; ++i)"),
@@ -688,6 +737,8 @@ PIN_TESTS = [
     test_sparse_attn_one_token_is_its_value_row, test_sparse_attn_equal_logits_give_the_mean,
     test_sparse_attn_two_tokens_logistic_weights, test_sparse_attn_scale_multiplies_the_logits,
     test_sparse_attn_reads_through_the_page_table, test_sparse_attn_refuses_tokens_past_the_table,
+    test_proj_selecting_weights_copy_columns, test_proj_matches_numpy_matmul,
+    test_proj_is_linear_in_powers_of_two,
 ]
 
 

@@ -513,6 +513,7 @@ def run_ours(args, rank, world, device):
         secondary["decode_long_32seq"] = decode_long(torch, qsa, device, hbm_gbs)
         secondary["decode_gather_64k"] = decode_gather(torch, qsa, device, hbm_gbs)
         secondary["prefill_attn_64k"] = prefill_attn(torch, qsa, device, hbm_gbs, bf16_tf)
+        secondary["qk_proj"] = qk_proj(torch, qsa, device, bf16_tf)
 
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": K,
@@ -838,6 +839,36 @@ def prefill_attn(torch, qsa, device, hbm_gbs, bf16_tf, ncu=False, rows=4096):
     }
 
 
+def qk_proj(torch, qsa, device, bf16_tf, ncu=False):
+    """The indexer's qk projection on tcgen05: one 2048-row slab (the pages'
+    slab) and a 4096-row prefill chunk, hidden 2560 -> 640, bf16."""
+    hidden, out_cols = 2560, 640
+    g = torch.Generator(device=device)
+    g.manual_seed(qi.seed_for(9))
+    w = (torch.randn((out_cols, hidden), generator=g, device=device) * 0.02).to(torch.bfloat16).view(torch.int16)
+    st = qsa.new_status(device)
+    res = {"hidden": hidden, "out_cols": out_cols}
+    for rows in (2048, 4096):
+        x = torch.randn((rows, hidden), generator=g, device=device).to(torch.bfloat16).view(torch.int16)
+        y = torch.empty((rows, out_cols), dtype=torch.int16, device=device)
+
+        def proj():
+            qsa.qsa_qk_proj(x, hidden, w, rows, hidden, out_cols, y, out_cols, st)
+
+        for _ in range(2 if ncu else 3):
+            proj()
+        torch.cuda.synchronize()
+        if ncu:
+            continue
+        t = time_fn(torch, proj, 20)
+        flops = 2.0 * rows * hidden * out_cols
+        res[f"rows_{rows}"] = {"us": t * 1000.0, "achieved_tflops": flops / (t * 1e-3) / 1e12,
+                               "frac_of_measured_bf16": flops / (t * 1e-3) / 1e12 / bf16_tf}
+    code, row = qsa.qsa_read_status(st)
+    assert code == 0, (code, row)
+    return None if ncu else res
+
+
 # ------------------------------------------------------------ ncu cases
 
 def ncu_case(name: str):
@@ -861,6 +892,8 @@ def ncu_case(name: str):
         decode_long(torch, qsa, dev, 6800.0, ncu=True)
     elif name == "gather":
         decode_gather(torch, qsa, dev, 6800.0, ncu=True)
+    elif name == "proj":
+        qk_proj(torch, qsa, dev, 1900.0, ncu=True)
     elif name == "attn":
         prefill_attn(torch, qsa, dev, 6800.0, 1900.0, ncu=True, rows=512)
     elif name == "gather_small":      # 8 rows: 1.1 GB of K/V pools

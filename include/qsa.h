@@ -363,6 +363,23 @@ qsa_status qsa_sparse_attn(const uint16_t *q, int64_t q_stride, int32_t nq, int3
                            float scale, uint16_t *out, int64_t out_stride, int32_t *dev_status,
                            void *stream);
 
+/*
+ * The indexer's qk projection of normed hidden states: y = x W^T in bf16 with
+ * f32 accumulation, rounded once to bf16.  Source: atlas layers/qsa_select.rs
+ * prefill_select (each 2048-row slab of the normed hidden states is projected
+ * hidden -> 640, the fused q|k row that q-prep, pooling and scoring read).
+ *  x        DEVICE bf16 [n_rows, hidden], row stride x_stride (a multiple of 8,
+ *           >= hidden), 16-byte aligned; hidden a positive multiple of 8.
+ *  w        DEVICE bf16 [out_cols, hidden] (a linear layer's [out, in]
+ *           weight), contiguous, 16-byte aligned; out_cols a multiple of 16.
+ *  y        DEVICE bf16 [n_rows, out_cols], row stride y_stride (a multiple
+ *           of 8, >= out_cols), 16-byte aligned.
+ *  n_rows <= 65535 * 128.  A bounded wait that gives up is QSA_ERR_TIMEOUT.
+ */
+qsa_status qsa_qk_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, int32_t n_rows,
+                       int32_t hidden, int32_t out_cols, uint16_t *y, int64_t y_stride,
+                       int32_t *dev_status, void *stream);
+
 /* Zero a DEVICE status word (stream-ordered). */
 qsa_status qsa_reset_status(int32_t *dev_status, void *stream);
 

@@ -37,7 +37,8 @@ EXPORTED = ("qsa_version", "qsa_status_string", "qsa_rope_tables", "qsa_pool_blo
             "qsa_score_rows", "qsa_score_rows_with", "qsa_score_workspace_bytes",
             "qsa_score_rows_noalloc", "qsa_select_mask", "qsa_index_select",
             "qsa_decode_workspace_bytes", "qsa_decode_index_select", "qsa_mask_tokens",
-            "qsa_gather_kv", "qsa_sparse_attn", "qsa_reset_status", "qsa_read_status")
+            "qsa_gather_kv", "qsa_sparse_attn", "qsa_qk_proj", "qsa_reset_status",
+            "qsa_read_status")
 
 
 class QsaError(RuntimeError):
@@ -75,6 +76,7 @@ def _load() -> ctypes.CDLL:
                           i32),
         "qsa_sparse_attn": ([P, i64, i32, i32, i32, P, P, i32, i32, P, i32, i64, P, i64, P, i32,
                              i32, f32, P, i64, P, P], i32),
+        "qsa_qk_proj": ([P, i64, P, i32, i32, i32, P, i64, P, P], i32),
         "qsa_reset_status": ([P, P], i32),
         "qsa_read_status": ([P, P, P, P], i32),
     }
@@ -288,6 +290,14 @@ def qsa_sparse_attn(q, q_stride, nq, nkv, head_dim, k_pool, v_pool, pool_pages, 
                                 _dev(out, "out"), int(out_stride), _dev(dev_status, "dev_status"),
                                 _stream(stream)),
            "qsa_sparse_attn")
+
+
+def qsa_qk_proj(x, x_stride, w, n_rows, hidden, out_cols, y, y_stride, dev_status,
+                stream=None) -> None:
+    _check(_lib.qsa_qk_proj(_dev(x, "x"), int(x_stride), _dev(w, "w"), int(n_rows), int(hidden),
+                            int(out_cols), _dev(y, "y"), int(y_stride),
+                            _dev(dev_status, "dev_status"), _stream(stream)),
+           "qsa_qk_proj")
 
 
 def qsa_reset_status(dev_status, stream=None) -> None:

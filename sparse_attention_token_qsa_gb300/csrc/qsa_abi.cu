@@ -359,6 +359,26 @@ qsa_status qsa_sparse_attn(const uint16_t *q, int64_t q_stride, int32_t nq, int3
                                            out_stride, dev_status, (cudaStream_t)stream));
 }
 
+qsa_status qsa_qk_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, int32_t n_rows,
+                       int32_t hidden, int32_t out_cols, uint16_t *y, int64_t y_stride,
+                       int32_t *dev_status, void *stream) {
+  if (n_rows < 0 || hidden < 0 || out_cols < 0 || x_stride < 0 || y_stride < 0)
+    return QSA_ERR_INVALID_VALUE;
+  if (n_rows == 0) return QSA_OK;
+  if (hidden == 0 || hidden % 8 != 0 || out_cols == 0 || out_cols % 16 != 0)
+    return QSA_ERR_INVALID_VALUE;
+  if (x_stride < hidden || x_stride % 8 != 0 || y_stride < out_cols || y_stride % 8 != 0)
+    return QSA_ERR_INVALID_VALUE;
+  if (!x || !w || !y || !dev_status) return QSA_ERR_INVALID_VALUE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return QSA_ERR_INVALID_VALUE;
+  if ((int64_t)n_rows > (int64_t)65535 * 128 ||
+      (int64_t)n_rows * (x_stride > y_stride ? x_stride : y_stride) > ((int64_t)1 << 46) ||
+      (int64_t)hidden * out_cols > ((int64_t)1 << 46))
+    return QSA_ERR_INVALID_VALUE;
+  return from_cuda(qsa::launch_proj(x, x_stride, w, n_rows, hidden, out_cols, y, y_stride,
+                                    dev_status, (cudaStream_t)stream));
+}
+
 qsa_status qsa_reset_status(int32_t *dev_status, void *stream) {
   if (!dev_status) return QSA_ERR_INVALID_VALUE;
   return from_cuda(cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), (cudaStream_t)stream));

@@ -102,4 +102,9 @@ cudaError_t launch_sparse_attn(const uint16_t *q, int64_t q_stride, int32_t nq, 
                                int32_t max_sel, float scale, uint16_t *out, int64_t out_stride,
                                int32_t *status, cudaStream_t stream);
 
+// The indexer's qk projection y = x W^T on tcgen05 (qsa_proj.cu).
+cudaError_t launch_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, int32_t n_rows,
+                        int32_t hidden, int32_t out_cols, uint16_t *y, int64_t y_stride,
+                        int32_t *status, cudaStream_t stream);
+
 }  // namespace qsa

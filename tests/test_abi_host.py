@@ -190,6 +190,37 @@ def test_gather_kv_refusals(lib):
         assert call(**kw) == 1, kw
 
 
+def test_sparse_attn_refusals(lib):
+    def call(**kw):
+        a = dict(q=A, qs=4096, nq=16, nkv=2, hd=256, k=A, v=B, pages=64, psz=16, table=A, tlen=64,
+                 tcols=64, sel=A, scols=2051, n_sel=B, n=2, max_sel=2051, scale=0.0625, out=B,
+                 os=4096, st=B)
+        a.update(kw)
+        return lib.qsa_sparse_attn(P(a["q"]), a["qs"], a["nq"], a["nkv"], a["hd"], P(a["k"]),
+                                   P(a["v"]), a["pages"], a["psz"], P(a["table"]), a["tlen"],
+                                   a["tcols"], P(a["sel"]), a["scols"], P(a["n_sel"]), a["n"],
+                                   a["max_sel"], a["scale"], P(a["out"]), a["os"], P(a["st"]), None)
+    assert call(n=0) == 0                             # nothing to do
+    for kw in (dict(nq=15), dict(nkv=0), dict(hd=64), dict(psz=0), dict(max_sel=2052),
+               dict(tcols=63), dict(qs=4095), dict(qs=4100), dict(os=4000), dict(q=U),
+               dict(out=U), dict(k=0), dict(sel=0), dict(table=0), dict(n_sel=0),
+               dict(scale=float("nan")), dict(scale=float("inf")), dict(n=-1)):
+        assert call(**kw) == 1, kw
+
+
+def test_qk_proj_refusals(lib):
+    def call(**kw):
+        a = dict(x=A, xs=2560, w=B, n=2048, hid=2560, out=640, y=A, ys=640, st=B)
+        a.update(kw)
+        return lib.qsa_qk_proj(P(a["x"]), a["xs"], P(a["w"]), a["n"], a["hid"], a["out"],
+                               P(a["y"]), a["ys"], P(a["st"]), None)
+    assert call(n=0) == 0                             # nothing to do
+    for kw in (dict(hid=0), dict(hid=2564), dict(out=648), dict(out=0), dict(xs=2552),
+               dict(xs=2561), dict(ys=636), dict(x=U), dict(y=U), dict(w=0), dict(st=0),
+               dict(n=-1), dict(n=65535 * 128 + 1)):
+        assert call(**kw) == 1, kw
+
+
 def test_status_calls_refuse_null(lib):
     assert lib.qsa_reset_status(None, None) == 1
     assert lib.qsa_read_status(None, None, None, None) == 1

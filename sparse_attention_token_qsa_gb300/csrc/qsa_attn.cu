@@ -9,13 +9,17 @@
 // attends the top budget/ratio blocks plus the incomplete tail).  Here the
 // selected set comes as the token lists qsa_mask_tokens writes.
 //
-// Per (row, KV head, chunk of 8 query heads) one CTA of 4 warps; the warps
-// split the row's tokens into 16-token tiles, round robin, and run an online
-// softmax each, combined at the end through shared memory.  A tile's K and V
-// rows (one 16-byte aligned run of head_dim bf16 per token and KV head) are
-// brought by the bulk-copy engine into a per-warp ring of three stages, row
-// stride head_dim * 2 + 16 bytes so that the fragment loads below hit 32
-// distinct banks.
+// Per (row, KV head, chunk of 8 query heads) one CTA of 4 warps, the grid
+// ordered KV head first.  The CTA walks the row's tokens in 16-token tiles:
+// warp 0's lanes bring each token's K and V rows (one 16-byte aligned run of
+// head_dim bf16 per token and KV head) with the bulk-copy engine into a
+// three-stage ring shared by the CTA (row stride head_dim * 2 + 16 bytes, so
+// the fragment loads below hit 32 distinct banks); the four warps split the
+// head dims, each computing its part of the logits and of the output.  The
+// partial logits meet once per tile in shared memory and every warp sums them
+// in the same order, so every warp holds the same softmax state and no final
+// combine is needed.  About 55 KiB of shared memory per CTA: four CTAs (16
+// warps) per SM.
 //
 // The contraction per (row, KV head) has only 8 query heads, so it runs on
 // warp-level mma.sync m16n8k16 (bf16 in, f32 accumulate):
@@ -45,25 +49,32 @@ constexpr int kAttnStages = 3;
 constexpr int kAttnTile = 16;  // tokens per tile
 constexpr long long kAttnSpinLimit = 4000000000LL;
 
+// Control block at the start of shared memory (one per CTA).
+struct AttnCtrl {
+  uint64_t full[kAttnStages];               // a tile's K and V rows have landed
+  uint32_t vmask[kAttnStages][kAttnWarps];  // which of each warp's 4 tokens are in the list
+  int32_t abort;
+  alignas(16) float xbuf[2][kAttnWarps * 32 * 4];  // partial logits, double-buffered by tile
+};
+
 template <int HD>
 struct AttnGeom {
-  static constexpr int kRowBytes = HD * 2;                        // one token's K (or V) row
-  static constexpr int kStride = kRowBytes + 16;                  // in shared memory
-  static constexpr int kStageBytes = 2 * kAttnTile * kStride;     // K rows then V rows
-  static constexpr int kWarpBytes = kAttnStages * kStageBytes;
-  static constexpr int kSteps = HD / 16;                          // k-steps of S = Q K^T
-  static constexpr int kChunksPerLane = HD / 32;                  // 16-byte K/Q chunks per lane
-  static constexpr int kMTiles = HD / 16;                         // m-tiles of O^T
-  static constexpr int kVChunks = HD / 64;                        // 16-byte V chunks per lane and token
-  static constexpr size_t kSmem = 128 + (size_t)kAttnWarps * kWarpBytes;
+  static constexpr int kRowBytes = HD * 2;                     // one token's K (or V) row
+  static constexpr int kStride = kRowBytes + 16;               // in shared memory
+  static constexpr int kStageBytes = 2 * kAttnTile * kStride;  // K rows then V rows
+  static constexpr int kJ = HD / 128;  // 16-byte K chunks per lane per warp (S, its head dims)
+  static constexpr int kMT = HD / 64;  // m-tiles of O^T per warp (its head dims)
+  static constexpr size_t kRingOff = (sizeof(AttnCtrl) + 127) & ~size_t(127);
+  static constexpr size_t kSmem = kRingOff + (size_t)kAttnStages * kStageBytes;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Bounded wait on an mbarrier phase; false once the limit is reached.
-__device__ __forceinline__ bool attn_wait(uint32_t mbar, uint32_t parity) {
+// Bounded wait on an mbarrier phase.  Returns false at once when the CTA has
+// aborted, and raises the abort flag when the limit is reached.
+__device__ bool attn_wait(uint32_t mbar, uint32_t parity, volatile int32_t *abort_flag) {
   const long long t0 = clock64();
   while (true) {
     uint32_t ok;
@@ -75,7 +86,11 @@ __device__ __forceinline__ bool attn_wait(uint32_t mbar, uint32_t parity) {
         : "r"(mbar), "r"(parity), "r"(20000u)
         : "memory");
     if (ok) return true;
-    if (clock64() - t0 > kAttnSpinLimit) return false;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (clock64() - t0 > kAttnSpinLimit) {
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
   }
 }
 
@@ -131,12 +146,12 @@ struct AttnArgs {
 };
 
 template <int HD>
-__global__ void __launch_bounds__(32 * kAttnWarps, 1)
+__global__ void __launch_bounds__(32 * kAttnWarps, 4)
 sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
   using Geo = AttnGeom<HD>;
   extern __shared__ __align__(128) uint8_t attn_smem[];
-  uint64_t *bars = reinterpret_cast<uint64_t *>(attn_smem);  // [warp][stage]
-  uint8_t *rings = attn_smem + 128;
+  AttnCtrl &C = *reinterpret_cast<AttnCtrl *>(attn_smem);
+  uint8_t *ring = attn_smem + Geo::kRingOff;
   grid_dependency_sync();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
@@ -150,128 +165,156 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
   const int32_t *srow = a.sel + (int64_t)row * a.sel_cols;
   const int32_t *trow = a.table + (int64_t)row * a.table_cols;
   const int heads_here = min(8, a.group - hc * 8);
-  uint8_t *ring = rings + (size_t)warp * Geo::kWarpBytes;
-  uint64_t *wbar = bars + warp * kAttnStages;
+  volatile int32_t *abort_flag = &C.abort;
 
-  // query head g of this chunk (zero rows past the group), in k_chunk order
-  uint32_t qa[Geo::kSteps][2];
+  // query head g of this chunk (zero rows past the group): this warp's head
+  // dims only, in k_chunk order (j = warp * kJ + jj)
+  uint32_t qa[2 * Geo::kJ][2];
   {
     const bool hv = g < heads_here;
     const uint16_t *qh =
         a.q + (int64_t)row * a.q_stride + (int64_t)(kvh * a.group + hc * 8 + (hv ? g : 0)) * HD;
 #pragma unroll
-    for (int j = 0; j < Geo::kChunksPerLane; ++j) {
+    for (int jj = 0; jj < Geo::kJ; ++jj) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (hv) v = ldg_nc_v4(qh + 8 * k_chunk(q, j));
-      qa[2 * j][0] = v.x;
-      qa[2 * j][1] = v.y;
-      qa[2 * j + 1][0] = v.z;
-      qa[2 * j + 1][1] = v.w;
+      if (hv) v = ldg_nc_v4(qh + 8 * k_chunk(q, warp * Geo::kJ + jj));
+      qa[2 * jj][0] = v.x;
+      qa[2 * jj][1] = v.y;
+      qa[2 * jj + 1][0] = v.z;
+      qa[2 * jj + 1][1] = v.w;
     }
   }
-  if (lane == 0) {
-    for (int s = 0; s < kAttnStages; ++s)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&wbar[s])) : "memory");
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAttnStages; ++s)  // one expect_tx arrival per warp
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&C.full[s])),
+                   "r"(kAttnWarps)
+                   : "memory");
+    C.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncwarp();
+  __syncthreads();
 
-  // this warp's tiles are warp, warp + 4, ...: local tile i is row tokens
-  // [16 (warp + 4 i), +16).  Lane x and lane x + 16 handle token x of a tile
-  // (its K row and its V row).  The two lookups before a tile's copies (its
-  // token, then that token's page entry) are loads whose results the next
-  // tile's issue consumes, so their latency overlaps a tile of work.
+  // ---- producers: warp w brings tokens 4w .. 4w+3 of each tile, lanes 0..3
+  // their K rows and lanes 4..7 their V rows, into the stage tile i % S.  The
+  // two lookups before a tile's copies (its token, then that token's page
+  // entry) run ahead in queues: tokens 2L tiles ahead, pages L tiles ahead.
   const int n_tiles = (n + kAttnTile - 1) / kAttnTile;
-  const int my_tiles = n_tiles > warp ? (n_tiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
+  const int tok_in_tile = 4 * warp + (lane & 3);  // lanes 0..7 (the rest mirror them)
   constexpr int32_t kNoToken = INT32_MIN;
   auto fetch_tok = [&](int i) -> int32_t {
-    const int32_t j = (warp + kAttnWarps * i) * kAttnTile + (lane & 15);
-    return (i < my_tiles && j < n) ? srow[j] : kNoToken;
+    const int32_t j = i * kAttnTile + tok_in_tile;
+    return (i < n_tiles && j < n) ? srow[j] : kNoToken;
   };
   auto fetch_page = [&](int32_t t) -> int32_t {  // -1: outside the table
     if (t == kNoToken) return kNoToken;
     const int32_t pg = t >= 0 ? t / a.page_size : -1;
     return (t >= 0 && pg < a.table_len) ? trow[pg] : -1;
   };
-  uint64_t vbits = 0;  // valid-token bits of the tile in each stage (16 per stage)
-  auto start = [&](int i, int32_t t, int32_t phys) {
+  auto start = [&](int i, int32_t t, int32_t phys) {  // this warp's part of tile i
     const int s = i % kAttnStages;
-    const bool ok = t != kNoToken && phys >= 0 && phys < a.pool_pages;
-    if (t != kNoToken && !ok && lane < 16) report_error(a.status, kErrTokenRange, row);
+    const bool ok = lane < 8 && t != kNoToken && phys >= 0 && phys < a.pool_pages;
+    if (lane < 4 && t != kNoToken && !ok) report_error(a.status, kErrTokenRange, row);
     const uint32_t bal = __ballot_sync(0xffffffffu, ok);
-    vbits = (vbits & ~(0xFFFFull << (16 * s))) | ((uint64_t)(bal & 0xFFFFu) << (16 * s));
-    const uint32_t mb = smem_u32(&wbar[s]);
-    if (lane == 0)
+    const uint32_t mb = smem_u32(&C.full[s]);
+    if (lane == 0) {
+      C.vmask[s][warp] = (bal & 0xFu) << (4 * warp);
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb),
                    "r"((uint32_t)__popc(bal) * (uint32_t)Geo::kRowBytes)
                    : "memory");
+    }
     __syncwarp();
     if (ok) {
       const int32_t pg = t / a.page_size;
       const int64_t src_row = ((int64_t)phys * a.page_size + (t - pg * a.page_size)) * a.nkv + kvh;
-      const uint16_t *src = (lane < 16 ? a.k_pool : a.v_pool) + src_row * HD;
+      const uint16_t *src = (lane < 4 ? a.k_pool : a.v_pool) + src_row * HD;
       const uint8_t *dst = ring + (size_t)s * Geo::kStageBytes +
-                           (lane < 16 ? 0 : kAttnTile * Geo::kStride) + (lane & 15) * Geo::kStride;
+                           (lane < 4 ? 0 : kAttnTile * Geo::kStride) + tok_in_tile * Geo::kStride;
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
               "r"(smem_u32(dst)), "l"(src), "r"((uint32_t)Geo::kRowBytes), "r"(mb)
           : "memory");
     }
   };
-  // prologue: the first kAttnStages tiles, their lookups issued side by side
-  int32_t tok_pre[kAttnStages + 1], page_pre[kAttnStages];
-#pragma unroll
-  for (int k = 0; k <= kAttnStages; ++k) tok_pre[k] = fetch_tok(k);
-#pragma unroll
-  for (int k = 0; k < kAttnStages; ++k) page_pre[k] = fetch_page(tok_pre[k]);
+  constexpr int kLook = 3, kLook2 = 2 * kLook;
   int issued = 0;
+  int32_t tokq[kLook2], pageq[kLook];
+  {
+    int32_t tok_pre[kAttnStages + kLook2], page_pre[kAttnStages + kLook];
 #pragma unroll
-  for (int k = 0; k < kAttnStages; ++k)
-    if (k < my_tiles) {
-      start(k, tok_pre[k], page_pre[k]);
-      ++issued;
-    }
-  int32_t tok_next = tok_pre[kAttnStages];            // tile `issued`
-  int32_t page_next = fetch_page(tok_next);           // in flight
-  int32_t tok_after = fetch_tok(kAttnStages + 1);     // tile `issued + 1`, in flight
+    for (int k = 0; k < kAttnStages + kLook2; ++k) tok_pre[k] = fetch_tok(k);
+#pragma unroll
+    for (int k = 0; k < kAttnStages + kLook; ++k) page_pre[k] = fetch_page(tok_pre[k]);
+#pragma unroll
+    for (int k = 0; k < kAttnStages; ++k)
+      if (k < n_tiles) {
+        start(k, tok_pre[k], page_pre[k]);
+        ++issued;
+      }
+#pragma unroll
+    for (int k = 0; k < kLook2; ++k) tokq[k] = tok_pre[kAttnStages + k];  // tiles S .. S + 2L - 1
+#pragma unroll
+    for (int k = 0; k < kLook; ++k) pageq[k] = page_pre[kAttnStages + k];  // tiles S .. S + L - 1
+  }
 
-  float m_run = -INFINITY;  // running max of head g's logits (log2 units)
+  float m_run = -INFINITY;  // running max of head g's logits (log2 units), same in every warp
   float l_run = 0.f;        // this lane's part of head g's weight sum
-  float acc[Geo::kMTiles][4];
+  float acc[Geo::kMT][4];
 #pragma unroll
-  for (int t = 0; t < Geo::kMTiles; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-  bool failed = false;
-  int i = 0;
-  for (; i < my_tiles; ++i) {
+  for (int t = 0; t < Geo::kMT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  for (int i = 0; i < n_tiles; ++i) {
     const int s = i % kAttnStages;
-    const bool okw = attn_wait(smem_u32(&wbar[s]), (uint32_t)(i / kAttnStages) & 1u);
-    if (!__all_sync(0xffffffffu, okw)) {
-      failed = true;
-      break;
-    }
+    // every warp runs every iteration and every barrier; after an abort the
+    // waits return at once and the results are discarded
+    // (every lane waits: each acquires the bulk copies' writes for itself)
+    const bool okw = __all_sync(
+        0xffffffffu, attn_wait(smem_u32(&C.full[s]), (uint32_t)(i / kAttnStages) & 1u, abort_flag));
     const uint8_t *kt = ring + (size_t)s * Geo::kStageBytes;
     const uint8_t *vt = kt + kAttnTile * Geo::kStride;
-    const uint32_t vb = (uint32_t)(vbits >> (16 * s)) & 0xFFFFu;
+    uint32_t vb = 0;
+    if (okw) {
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) vb |= C.vmask[s][w];
+    }
 
-    // ---- S = Q K^T over the tile's two 8-token halves (two chains each)
-    float sc[2][2][4];
+    // ---- this warp's part of S = Q K^T: its head dims, both 8-token halves
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int x = 0; x < 2; ++x)
-#pragma unroll
-      for (int y = 0; y < 2; ++y) sc[x][y][0] = sc[x][y][1] = sc[x][y][2] = sc[x][y][3] = 0.f;
-#pragma unroll
-    for (int j = 0; j < Geo::kChunksPerLane; ++j) {
-      const int c = k_chunk(q, j);
+    for (int jj = 0; jj < Geo::kJ; ++jj) {
+      const int c = k_chunk(q, warp * Geo::kJ + jj);
       const uint4 k0 = *reinterpret_cast<const uint4 *>(kt + g * Geo::kStride + 16 * c);
       const uint4 k1 = *reinterpret_cast<const uint4 *>(kt + (g + 8) * Geo::kStride + 16 * c);
-      mma_bf16(sc[0][j & 1], qa[2 * j][0], 0u, qa[2 * j][1], 0u, k0.x, k0.y);
-      mma_bf16(sc[1][j & 1], qa[2 * j][0], 0u, qa[2 * j][1], 0u, k1.x, k1.y);
-      mma_bf16(sc[0][j & 1], qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, k0.z, k0.w);
-      mma_bf16(sc[1][j & 1], qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, k1.z, k1.w);
+      mma_bf16(sc[0], qa[2 * jj][0], 0u, qa[2 * jj][1], 0u, k0.x, k0.y);
+      mma_bf16(sc[1], qa[2 * jj][0], 0u, qa[2 * jj][1], 0u, k1.x, k1.y);
+      mma_bf16(sc[0], qa[2 * jj + 1][0], 0u, qa[2 * jj + 1][1], 0u, k0.z, k0.w);
+      mma_bf16(sc[1], qa[2 * jj + 1][0], 0u, qa[2 * jj + 1][1], 0u, k1.z, k1.w);
     }
-    // this lane's logits: head g at tile tokens 2q, 2q+1, 2q+8, 2q+9
-    float sv[4] = {sc[0][0][0] + sc[0][1][0], sc[0][0][1] + sc[0][1][1], sc[1][0][0] + sc[1][1][0],
-                   sc[1][0][1] + sc[1][1][1]};
+    // partial logits of head g at tile tokens 2q, 2q+1, 2q+8, 2q+9, summed over
+    // the warps in a fixed order so every warp holds the same values
+    float4 *xb = reinterpret_cast<float4 *>(C.xbuf[i & 1]);
+    xb[warp * 32 + lane] = make_float4(sc[0][0], sc[0][1], sc[1][0], sc[1][1]);
+    __syncthreads();
+    // every warp is past tile i - 1: its stage takes tile i - 1 + S
+    const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;  // one verdict per warp
+    if (i >= 1 && issued < n_tiles && !aborted) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      start(issued, tokq[0], pageq[0]);  // the queues' head is tile `issued`
+      ++issued;
+#pragma unroll
+      for (int k = 0; k + 1 < kLook; ++k) pageq[k] = pageq[k + 1];
+      pageq[kLook - 1] = fetch_page(tokq[kLook]);  // token loaded kLook tiles ago
+#pragma unroll
+      for (int k = 0; k + 1 < kLook2; ++k) tokq[k] = tokq[k + 1];
+      tokq[kLook2 - 1] = fetch_tok(issued + kLook2 - 1);
+    }
+    float sv[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float4 p = xb[w * 32 + lane];
+      sv[0] += p.x;
+      sv[1] += p.y;
+      sv[2] += p.z;
+      sv[3] += p.w;
+    }
     float tmax = -INFINITY;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -289,12 +332,12 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
     const uint32_t pb1 = pack_bf16x2(exp2f(sv[2] - m_use), exp2f(sv[3] - m_use));
     // the weights the product uses are the rounded ones: so is their sum
     l_run = l_run * alpha + ((bf16_lo(pb0) + bf16_hi(pb0)) + (bf16_lo(pb1) + bf16_hi(pb1)));
-    // O^T's columns are heads 2q, 2q+1, whose factors lanes 8q and 8q+4 hold
     if (__any_sync(0xffffffffu, alpha != 1.f)) {  // some head's maximum moved
+      // O^T's columns are heads 2q, 2q+1, whose factors lanes 8q and 8q+4 hold
       const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * q);
       const float al1 = __shfl_sync(0xffffffffu, alpha, 8 * q + 4);
 #pragma unroll
-      for (int t = 0; t < Geo::kMTiles; ++t) {
+      for (int t = 0; t < Geo::kMT; ++t) {
         acc[t][0] *= al0;
         acc[t][2] *= al0;
         acc[t][1] *= al1;
@@ -302,104 +345,82 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
       }
     }
 
-    // ---- O^T += V^T P^T: V rows of tokens 2q, 2q+1, 2q+8, 2q+9 at chunks g + 8c
+    // ---- O^T += V^T P^T for this warp's m-tiles T = warp * kMT + t: rows g,
+    // g+8 of m-tile T are dims 8(g + 8c) + 2e, +1 with c = T / 4, e = T % 4
     // (in a partial tile a token outside the list contributes zeros: its stage
     // row may hold anything)
     auto pv = [&](const uint32_t z0, const uint32_t z1, const uint32_t z2, const uint32_t z3) {
+      const int c = (warp * Geo::kMT) / 4;
+      const int off = 16 * (g + 8 * c);
+      const uint4 v0 = *reinterpret_cast<const uint4 *>(vt + (2 * q) * Geo::kStride + off);
+      const uint4 v1 = *reinterpret_cast<const uint4 *>(vt + (2 * q + 1) * Geo::kStride + off);
+      const uint4 v2 = *reinterpret_cast<const uint4 *>(vt + (2 * q + 8) * Geo::kStride + off);
+      const uint4 v3 = *reinterpret_cast<const uint4 *>(vt + (2 * q + 9) * Geo::kStride + off);
+      // words e = (warp * kMT) % 4 + t of the chunk: dims 8(g + 8c) + 2e, +1
+      uint32_t w0[Geo::kMT], w1[Geo::kMT], w2[Geo::kMT], w3[Geo::kMT];
+      if constexpr (Geo::kMT == 4) {
+        w0[0] = v0.x; w0[1] = v0.y; w0[2] = v0.z; w0[3] = v0.w;
+        w1[0] = v1.x; w1[1] = v1.y; w1[2] = v1.z; w1[3] = v1.w;
+        w2[0] = v2.x; w2[1] = v2.y; w2[2] = v2.z; w2[3] = v2.w;
+        w3[0] = v3.x; w3[1] = v3.y; w3[2] = v3.z; w3[3] = v3.w;
+      } else {  // two m-tiles: the low or the high half of the chunk
+        const bool hi = (warp & 1) != 0;
+        w0[0] = hi ? v0.z : v0.x; w0[1] = hi ? v0.w : v0.y;
+        w1[0] = hi ? v1.z : v1.x; w1[1] = hi ? v1.w : v1.y;
+        w2[0] = hi ? v2.z : v2.x; w2[1] = hi ? v2.w : v2.y;
+        w3[0] = hi ? v3.z : v3.x; w3[1] = hi ? v3.w : v3.y;
+      }
 #pragma unroll
-      for (int c = 0; c < Geo::kVChunks; ++c) {
-        const int off = 16 * (g + 8 * c);
-        const uint4 v0 = *reinterpret_cast<const uint4 *>(vt + (2 * q) * Geo::kStride + off);
-        const uint4 v1 = *reinterpret_cast<const uint4 *>(vt + (2 * q + 1) * Geo::kStride + off);
-        const uint4 v2 = *reinterpret_cast<const uint4 *>(vt + (2 * q + 8) * Geo::kStride + off);
-        const uint4 v3 = *reinterpret_cast<const uint4 *>(vt + (2 * q + 9) * Geo::kStride + off);
-        const uint32_t w0[4] = {v0.x & z0, v0.y & z0, v0.z & z0, v0.w & z0};
-        const uint32_t w1[4] = {v1.x & z1, v1.y & z1, v1.z & z1, v1.w & z1};
-        const uint32_t w2[4] = {v2.x & z2, v2.y & z2, v2.z & z2, v2.w & z2};
-        const uint32_t w3[4] = {v3.x & z3, v3.y & z3, v3.z & z3, v3.w & z3};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          // m-tile 4c + e: rows g, g+8 are dims 8(g + 8c) + 2e, +1
-          mma_bf16(acc[4 * c + e], prmt(w0[e], w1[e], 0x5410u), prmt(w0[e], w1[e], 0x7632u),
-                   prmt(w2[e], w3[e], 0x5410u), prmt(w2[e], w3[e], 0x7632u), pb0, pb1);
-        }
+      for (int t = 0; t < Geo::kMT; ++t) {
+        const uint32_t x0 = w0[t] & z0, x1 = w1[t] & z1, x2 = w2[t] & z2, x3 = w3[t] & z3;
+        mma_bf16(acc[t], prmt(x0, x1, 0x5410u), prmt(x0, x1, 0x7632u), prmt(x2, x3, 0x5410u),
+                 prmt(x2, x3, 0x7632u), pb0, pb1);
       }
     };
-    if (vb == 0xFFFFu) {  // a whole tile (uniform over the warp): constant masks fold away
+    if (vb == 0xFFFFu) {  // a whole tile (uniform over the CTA): constant masks fold away
       pv(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
     } else {
       pv((vb >> (2 * q)) & 1u ? 0xFFFFFFFFu : 0u, (vb >> (2 * q + 1)) & 1u ? 0xFFFFFFFFu : 0u,
          (vb >> (2 * q + 8)) & 1u ? 0xFFFFFFFFu : 0u, (vb >> (2 * q + 9)) & 1u ? 0xFFFFFFFFu : 0u);
     }
-    if (issued < my_tiles) {  // refill this stage once every lane is done reading it
-      __syncwarp();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      start(issued, tok_next, page_next);
-      ++issued;
-      tok_next = tok_after;
-      page_next = fetch_page(tok_next);
-      tok_after = fetch_tok(issued + 1);
-    }
-  }
-  if (failed) {
-    if (lane == 0) report_error(a.status, kErrTimeout, row);
-    // let this warp's own copies land before the ring is reused below
-    for (int k = i; k < issued; ++k)
-      attn_wait(smem_u32(&wbar[k % kAttnStages]), (uint32_t)(k / kAttnStages) & 1u);
   }
 
-  // ---- combine the warps: head h's output is sum_w 2^(m_w - M) O_w / sum_w 2^(m_w - M) l_w
+  // ---- output: head h = 2q, 2q+1 of this warp's dims, normalised by the
+  // head's weight sum (every warp holds the same one)
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  __syncthreads();  // every warp's copies have landed: the rings are free
-  float *mw = reinterpret_cast<float *>(rings);  // [warp][8] running maxima
-  float *lw = mw + kAttnWarps * 8;               // [warp][8] weight sums
-  float *ow = lw + kAttnWarps * 8;               // [warp][8 heads][HD] unnormalised outputs
-  if (q == 0) {
-    mw[warp * 8 + g] = m_run;
-    lw[warp * 8 + g] = l_run;
-  }
+  const float l0 = __shfl_sync(0xffffffffu, l_run, 8 * q);
+  const float l1 = __shfl_sync(0xffffffffu, l_run, 8 * q + 4);
+  const float inv0 = l0 == 0.f ? 0.f : 1.f / l0;  // no selected token: zeros
+  const float inv1 = l1 == 0.f ? 0.f : 1.f / l1;
+  uint16_t *orow = a.out + (int64_t)row * a.out_stride + (int64_t)(kvh * a.group + hc * 8) * HD;
+  {
+    const int c = (warp * Geo::kMT) / 4;
+    const int d0 = 8 * (g + 8 * c) + 2 * ((warp * Geo::kMT) % 4);  // this warp's first dim here
+    uint32_t h0[Geo::kMT], h1[Geo::kMT];
 #pragma unroll
-  for (int t = 0; t < Geo::kMTiles; ++t) {
-    const int d0 = 8 * (g + 8 * (t >> 2)) + 2 * (t & 3);
-    float *o0 = ow + (size_t)(warp * 8 + 2 * q) * HD + d0;
-    float *o1 = ow + (size_t)(warp * 8 + 2 * q + 1) * HD + d0;
-    o0[0] = acc[t][0];
-    o0[1] = acc[t][2];
-    o1[0] = acc[t][1];
-    o1[1] = acc[t][3];
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < heads_here * (HD / 8); idx += 32 * kAttnWarps) {
-    const int h = idx / (HD / 8), d0 = 8 * (idx % (HD / 8));
-    float mx = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) mx = fmaxf(mx, mw[w * 8 + h]);
-    float f[kAttnWarps], den = 0.f;
-#pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
-      f[w] = mx == -INFINITY ? 0.f : exp2f(mw[w * 8 + h] - mx);
-      den += f[w] * lw[w * 8 + h];
+    for (int t = 0; t < Geo::kMT; ++t) {
+      h0[t] = pack_bf16x2(acc[t][0] * inv0, acc[t][2] * inv0);
+      h1[t] = pack_bf16x2(acc[t][1] * inv1, acc[t][3] * inv1);
     }
-    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
-      const float4 x0 = *reinterpret_cast<const float4 *>(ow + (size_t)(w * 8 + h) * HD + d0);
-      const float4 x1 = *reinterpret_cast<const float4 *>(ow + (size_t)(w * 8 + h) * HD + d0 + 4);
-      o[0] += f[w] * x0.x;
-      o[1] += f[w] * x0.y;
-      o[2] += f[w] * x0.z;
-      o[3] += f[w] * x0.w;
-      o[4] += f[w] * x1.x;
-      o[5] += f[w] * x1.y;
-      o[6] += f[w] * x1.z;
-      o[7] += f[w] * x1.w;
+    if constexpr (Geo::kMT == 4) {
+      if (2 * q < heads_here)
+        *reinterpret_cast<uint4 *>(orow + (int64_t)(2 * q) * HD + d0) = make_uint4(h0[0], h0[1], h0[2], h0[3]);
+      if (2 * q + 1 < heads_here)
+        *reinterpret_cast<uint4 *>(orow + (int64_t)(2 * q + 1) * HD + d0) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+    } else {
+      if (2 * q < heads_here)
+        *reinterpret_cast<uint2 *>(orow + (int64_t)(2 * q) * HD + d0) = make_uint2(h0[0], h0[1]);
+      if (2 * q + 1 < heads_here)
+        *reinterpret_cast<uint2 *>(orow + (int64_t)(2 * q + 1) * HD + d0) = make_uint2(h1[0], h1[1]);
     }
-    const float inv = den == 0.f ? 0.f : 1.f / den;  // no selected token: zeros
-    const uint4 r = make_uint4(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv),
-                               pack_bf16x2(o[4] * inv, o[5] * inv), pack_bf16x2(o[6] * inv, o[7] * inv));
-    *reinterpret_cast<uint4 *>(a.out + (int64_t)row * a.out_stride +
-                               (int64_t)(kvh * a.group + hc * 8 + h) * HD + d0) = r;
+  }
+  if (*abort_flag && threadIdx.x == 0) report_error(a.status, kErrTimeout, row);
+  // the copies issued land before the CTA's shared memory is released (in a
+  // run that completed, every tile was waited for already)
+  if (lane == 0) {
+    for (int k = max(0, issued - kAttnStages); k < issued; ++k)
+      attn_wait(smem_u32(&C.full[k % kAttnStages]), (uint32_t)(k / kAttnStages) & 1u, nullptr);
   }
 }
 

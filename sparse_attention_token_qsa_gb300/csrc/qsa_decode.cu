@@ -48,8 +48,16 @@ struct RowHdr {  // per row, at the start of the row's workspace
   uint32_t arrive;  // CTAs whose histogram is in
   uint32_t ticket;  // CTAs done writing their blocks
   uint32_t ncand;   // candidates listed
-  uint32_t pad[61];
+  uint32_t maxbin[8];  // the highest bin any key landed in (CTA y adds to slot y % 8)
+  uint32_t lowbad;     // a key landed below bin 8 (a negative non-finite score)
+  uint32_t pad[52];
 };
+static_assert(sizeof(RowHdr) == 16640, "the workspace layout is part of the ABI");
+
+// Keys of the keep-th largest score and everything above it sit in the top few
+// dozen bins of a row's histogram, so each CTA first reads only this many bins
+// below the row's highest one (and the whole histogram if they fall short).
+constexpr int kDecWindow = 256;
 
 struct DecSmem {  // selection scratch, laid over the key ring once scoring is done
   uint32_t hist0[4096];
@@ -93,6 +101,7 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
                     uint8_t *__restrict__ ws, int64_t row_ws_bytes, int32_t bpc,
                     const PoolArgs pa) {
   extern __shared__ __align__(128) uint8_t dec_smem[];
+  __shared__ uint32_t s_maxbin, s_low;  // this CTA's highest bin, any bin below 8
   SimtSmem &S = *reinterpret_cast<SimtSmem *>(dec_smem);
   uint8_t *ring = dec_smem + kSimtStageOff;
   float *sc_s = reinterpret_cast<float *>(ring + kSimtRingBytes);
@@ -102,6 +111,10 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   grid_dependency_sync();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x, y = blockIdx.y, ny = gridDim.y;
+  if (tid == 0) {
+    s_maxbin = 0u;
+    s_low = 0u;
+  }
   const int32_t p = a.pos[row];
   const bool valid = p >= 0 && p < a.tokens;
   const int32_t n = valid ? (p + 1) >> 2 : 0;
@@ -179,17 +192,30 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   __syncthreads();  // sc_s complete; the ring is free
   // one add per distinct bin per warp: a row's keys crowd into a few hundred
   // bins, and every CTA of the row adds into the same workspace counters
+  uint32_t my_max = 0u, my_low = 0u;
   for (int i0 = warp * 32; i0 < cnt; i0 += kDecThreads) {
     const int i = i0 + lane;
     const uint32_t bin = i < cnt ? order_key(sc_s[i]) >> 20 : 0xFFFFFFFFu;
     const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-    if (bin != 0xFFFFFFFFu && lane == __ffs(peers) - 1)
-      atomicAdd(&W.hist0[bin], (uint32_t)__popc(peers));
+    if (bin != 0xFFFFFFFFu) {
+      if (lane == __ffs(peers) - 1) atomicAdd(&W.hist0[bin], (uint32_t)__popc(peers));
+      my_max = max(my_max, bin);
+      my_low |= bin < 8u ? 1u : 0u;
+    }
+  }
+  my_max = __reduce_max_sync(0xffffffffu, my_max);
+  my_low = __reduce_or_sync(0xffffffffu, my_low);
+  if (lane == 0) {
+    atomicMax(&s_maxbin, my_max);
+    if (my_low) s_low = 1u;
   }
 
   // ---- 2. grid barrier over the row's CTAs
   __syncthreads();
   if (tid == 0) {
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(&W.maxbin[y & 7]), "r"(s_maxbin)
+                 : "memory");
+    if (s_low) asm volatile("red.relaxed.gpu.global.or.b32 [%0], 1;" ::"l"(&W.lowbad) : "memory");
     // release: the CTA's histogram adds (ordered before it by the barrier
     // above) are visible to whoever sees the count
     red_add_release_gpu(&W.arrive, 1u);
@@ -210,39 +236,72 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   }
 
   // ---- 3. the threshold bin, this CTA's mask bytes and candidates
-  // the row's histogram into shared memory: one 16 KiB bulk copy (the copy
-  // engine reads global memory through the async proxy, so that proxy is
-  // fenced after the acquire that made the other CTAs' adds visible)
+  // A non-finite score lands above bin 0xFF7 (positive) or below bin 8
+  // (negative); every finite one between.  The row's histogram comes into
+  // shared memory by bulk copies (the copy engine reads global memory through
+  // the async proxy, so that proxy is fenced after the acquire that made the
+  // other CTAs' adds visible): first the kDecWindow bins ending at the row's
+  // highest one, then, only if they hold fewer than keep keys, all 4096.
   if (tid == 0) {
-    const uint32_t mb = simt_smem_u32(&S.full[0]);  // the ring's barriers are free again
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mb) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(16384u)
-                 : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(simt_smem_u32(D.hist0)),
-        "l"(W.hist0), "r"(16384u), "r"(mb)
-        : "memory");
-    D.flag = simt_wait(mb, 0u) ? 1 : 0;
+    uint32_t mx = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx = max(mx, __ldcg(&W.maxbin[k]));
+    const bool nf = __ldcg(&W.lowbad) != 0u || mx >= 0xFF8u;
+    D.rule_prefix = nf ? 1u : 0u;  // (scratch: the non-finite verdict)
+    // window start: 16-byte aligned, rounded up so the highest bin stays inside
+    // (mx <= 0xFF7 for a finite row, so the window ends inside the histogram)
+    D.rule_shift = ((uint32_t)max(0, (int)mx + 1 - kDecWindow) + 3u) & ~3u;
   }
   __syncthreads();
-  if (!D.flag) {
-    if (tid == 0) report_error(a.status, kErrTimeout, row);
-    return;
-  }
-  const bool bad = __syncthreads_or(tid < 16 && D.hist0[tid < 8 ? tid : 0xFF0 + tid] != 0u) != 0;
+  const bool bad = D.rule_prefix != 0u;
+  const uint32_t wlo = D.rule_shift;
+  auto fetch_hist = [&](uint32_t first, uint32_t nbins, uint32_t parity) {
+    if (tid == 0) {
+      const uint32_t mb = simt_smem_u32(&S.full[0]);  // the ring's barriers are free again
+      if (parity == 0u) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mb) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(4u * nbins)
+                   : "memory");
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+              "r"(simt_smem_u32(D.hist0)),
+          "l"(W.hist0 + first), "r"(4u * nbins), "r"(mb)
+          : "memory");
+      D.flag = simt_wait(mb, parity) ? 1 : 0;
+      D.sel_bin = -1;
+    }
+    __syncthreads();
+    return D.flag != 0;
+  };
   uint32_t need = (uint32_t)min(keep_max, n);
+  uint32_t hbase = wlo;  // D.hist0[i] holds bin hbase + i
+  if (!bad) {
+    if (!fetch_hist(wlo, kDecWindow, 0u)) {
+      if (tid == 0) report_error(a.status, kErrTimeout, row);
+      return;
+    }
+    find_bin<kDecThreads>(D.hist0, kDecWindow, need, D.warp_tot, &D.sel_bin, &D.sel_above);
+    if (D.sel_bin < 0) {  // the keep-th key lies below the window
+      __syncthreads();    // every thread has read sel_bin
+      hbase = 0u;
+      if (!fetch_hist(0u, 4096u, 1u)) {
+        if (tid == 0) report_error(a.status, kErrTimeout, row);
+        return;
+      }
+      find_bin<kDecThreads>(D.hist0, 4096, need, D.warp_tot, &D.sel_bin, &D.sel_above);
+    }
+  }
   uint32_t B0 = 0;
   bool whole = false;  // the bin's keys are all kept
   if (bad) {
     if (y == 0 && tid == 0) report_error(a.status, kErrNonFinite, row);
   } else {
-    find_bin<kDecThreads>(D.hist0, 4096, need, D.warp_tot, &D.sel_bin, &D.sel_above);
-    B0 = (uint32_t)D.sel_bin;
+    B0 = hbase + (uint32_t)D.sel_bin;
     need -= D.sel_above;
-    whole = D.hist0[B0] == need;
+    whole = D.hist0[B0 - hbase] == need;
     const uintptr_t rb = reinterpret_cast<uintptr_t>(mrow);
     const bool al16 = (rb & 15u) == 0, al4 = (rb & 3u) == 0;
     for (int i = 4 * tid; i < cnt; i += 4 * kDecThreads) {
@@ -407,6 +466,9 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
     W.arrive = 0u;
     W.ticket = 0u;
     W.ncand = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) W.maxbin[k] = 0u;
+    W.lowbad = 0u;
   }
 }
 

@@ -340,3 +340,29 @@ def test_decode_pools_new_blocks_in_the_same_launch(qsa, orc, tables, first, cou
     assert np.array_equal(outs[0][2], outs[1][2]), "masks differ"
     want, _ = oracle_masks(orc, outs[0][1], nb, pos, tokens, BUDGET)
     assert np.array_equal(outs[0][2], want)
+
+
+def test_decode_keep_th_key_far_below_the_top(qsa, orc, tables):
+    """A few block keys scaled by 2^70 make a handful of scores ~2^70 times the
+    rest: the keep-th score then lies hundreds of 12-bit bins below the row's
+    highest, outside the first window each CTA reads, so the whole histogram is
+    read; the masks must still equal the two-kernel path and the oracle."""
+    rng = qi.rng_for(1, salt=4097)
+    tokens = 65536
+    nb = tokens // 4
+    cache_np = qi.normal_bf16(rng, (nb, 128))
+    huge = rng.choice(nb - 100, 40, replace=False)
+    cache_np[huge] = qi.to_bf16_bits(qi.bf16_bits_to_f32(cache_np[huge]) * np.float32(2.0 ** 70))
+    q_np = qi.normal_bf16(rng, (3, 512))
+    qw, _ = qi.norm_weights(rng)
+    pos = np.array([tokens - 1, tokens - 3, 50001], np.int32)
+    (dsc, dmask, dst, _), (psc, pmask, pst, _), ws = run_both(qsa, tables, cache_np, q_np, pos,
+                                                            tokens, nb, qw)
+    assert dst == (0, 0) and pst == (0, 0)
+    assert int(ws.count_nonzero()) == 0
+    assert np.isfinite(dsc[dsc != -7.0]).all()
+    assert np.nanmax(dsc) > 2.0 ** 60            # the giant scores are there
+    assert np.array_equal(dmask, pmask)
+    want, codes = oracle_masks(orc, dsc, nb, pos, tokens, BUDGET)
+    assert all(c == 0 for c in codes)
+    assert np.array_equal(dmask, want)

@@ -616,13 +616,20 @@ def prefill_chunk(torch, qsa, device, hbm_gbs, bf16_tf, ncu=False):
         score()
         select()
 
+    def fused():  # the same step through the fused entry, qsa_index_select
+        qsa.qsa_index_select(raw[first:].reshape(-1), 128, first // 4, 1024, kw, fq, 640, pos, rows,
+                             tokens, qw, cd, sd, tokens, EPS, BUDGET, cache, sc, nb, mask, st,
+                             workspace=ws)
+
     for _ in range(2 if ncu else 3):
         step()
+        fused()
     torch.cuda.synchronize()
     if ncu:
         return None
     it = 10
     t_step = time_fn(torch, step, it)
+    t_fused = time_fn(torch, fused, it)
     t_pool = time_fn(torch, pool, it)
     t_score = time_fn(torch, score, it)
     t_sel = time_fn(torch, select, it)
@@ -635,6 +642,8 @@ def prefill_chunk(torch, qsa, device, hbm_gbs, bf16_tf, ncu=False):
     pool_bytes = 1024 * POOL_BYTES_PER_BLOCK
     return {
         "rows": rows, "rows_per_s": rows / (t_step * 1e-3), "step_us": t_step * 1000.0,
+        "fused_index_select_us": t_fused * 1000.0,
+        "fused_rows_per_s": rows / (t_fused * 1e-3),
         "pool": {"us": t_pool * 1000.0, "blocks": 1024,
                  "frac_of_measured_hbm": pool_bytes / (t_pool * 1e-3) / 1e9 / hbm_gbs},
         "score_tcgen05": {"us": t_score * 1000.0, "live_scores": live,

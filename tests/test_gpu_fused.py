@@ -109,3 +109,45 @@ def test_decode_steps_end_to_end(qsa, orc, tables):
         got = mask.cpu().numpy()[0]
         check_mask_structure(got, p, tokens, BUDGET)
         assert_masks_agree_up_to_tolerance(got, mask_o[0], sc_o[0], p, BUDGET, f"step {p}")
+
+
+def test_index_select_matches_the_single_stage_entries(qsa, orc, tables):
+    """1600 rows at 64k: qsa_index_select's scores and masks must equal, bit for
+    bit, those of qsa_score_rows + qsa_select_mask, and an out-of-range row near
+    the end is reported by its index."""
+    rng = qi.rng_for(3, salt=1600)
+    tokens, rows = 65536, 1600
+    nb = tokens // 4
+    c, s, cd, sd = tables
+    keys = qi.normal_bf16(rng, (nb, 128))
+    q = qi.normal_bf16(rng, (rows, 512))
+    qw, kw = qi.norm_weights(rng)
+    pos = rng.integers(2000, tokens, size=rows).astype(np.int32)
+    pos[1599] = tokens + 5                     # out of range
+    ws = qsa.new_workspace(rows)
+    outs = []
+    for fused in (True, False):
+        bk = dev(keys)
+        sc = torch.full((rows, nb), -7.0, dtype=torch.float32, device="cuda")
+        mask = torch.full((rows, tokens), 0xAB, dtype=torch.uint8, device="cuda")
+        st = qsa.new_status()
+        if fused:
+            qsa.qsa_index_select(bk, 128, 0, 0, dev(kw), dev(q), 512, dev(pos), rows, tokens,
+                                 dev(qw), cd, sd, c.shape[0], EPS, BUDGET, bk, sc, nb, mask, st,
+                                 workspace=ws)
+        else:
+            qsa.qsa_score_rows(dev(q), 512, dev(pos), None, rows, tokens, dev(qw), cd, sd,
+                               c.shape[0], EPS, bk, None, sc, nb, st, workspace=ws)
+            qsa.qsa_select_mask(sc, nb, dev(pos), rows, tokens, BUDGET, mask, st)
+        torch.cuda.synchronize()
+        outs.append((sc.cpu().numpy(), mask.cpu().numpy(), qsa.qsa_read_status(st)))
+    (fsc, fmask, fst), (psc, pmask, pst) = outs
+    assert fst == (qsa.QSA_ERR_ROW_RANGE, 1599) and pst == (qsa.QSA_ERR_ROW_RANGE, 1599)
+    assert np.array_equal(fsc, psc)
+    assert np.array_equal(fmask, pmask)
+    # and a few rows against the oracle's selection of these scores
+    check = [0, 767, 768, 1535, 1536, 1598]
+    want, codes = oracle_masks(orc, fsc, nb, pos, tokens, BUDGET, rows=check)
+    assert all(cd_ == 0 for cd_ in codes)
+    for k, r in enumerate(check):
+        assert np.array_equal(fmask[r], want[k]), r

@@ -6,13 +6,16 @@
 // layer's weight, [out, in].  Both operands are K-major, which is the
 // tcgen05 layout: D[row, col] = sum_k x[row, k] W[col, k].
 //
-// One CTA per 128 x 80 output tile (a 2048 x 640 slab is 16 x 8 = 128 CTAs,
-// one wave).  Warp 0's lane 0 streams 64-wide K slices of both operands with
-// TMA (128-byte swizzle, zero fill past the matrix edges) into a six-stage
-// ring; warp 1's lane 0 issues tcgen05.mma M128 N80 K16 four times per slice
-// into a TMEM accumulator (f32, 80 columns); then all four warps drain their
-// 32 TMEM lanes (one output row per thread), round to bf16 and store.  Every
-// wait is bounded; on a timeout the CTA records QSA_ERR_TIMEOUT.
+// One CTA per output tile of 128 rows x BN columns, BN = 160 when such tiles
+// alone fill most of the GPU (4096 x 640: 128 CTAs) and 80 otherwise (a 2048 x
+// 640 slab: 16 x 8 = 128 CTAs): a tcgen05.mma takes about as long at N = 80 as
+// at N = 160, so the wider tile does twice the work per instruction.  Warp 0's
+// lane 0 streams 64-wide K slices of both operands with TMA (128-byte swizzle,
+// zero fill past the matrix edges) into a six-stage ring; warp 1's lane 0
+// issues tcgen05.mma M128 N=BN K16 four times per slice into a TMEM
+// accumulator (f32); then all four warps drain their 32 TMEM lanes (one output
+// row per thread), round to bf16 and store.  Every wait is bounded; on a
+// timeout the CTA records QSA_ERR_TIMEOUT.
 #include <cuda.h>  // CUtensorMap and its enums (the encoder comes from the runtime)
 
 #include "qsa_device.cuh"
@@ -23,20 +26,26 @@ namespace qsa {
 namespace {
 
 constexpr int kPM = 128;        // output rows per tile (TMEM lanes)
-constexpr int kPN = 80;         // output columns per tile
 constexpr int kPK = 64;         // K per stage: one 128-byte swizzled row of bf16
 constexpr int kPStages = 6;
 constexpr int kPThreads = 128;
 constexpr uint32_t kPAStage = kPM * kPK * 2;  // 16 KiB
-constexpr uint32_t kPBStage = kPN * kPK * 2;  // 10 KiB
-constexpr uint32_t kPAOff = 0;
-constexpr uint32_t kPBOff = kPStages * kPAStage;
-constexpr uint32_t kPCtrlOff = kPBOff + kPStages * kPBStage;
-constexpr uint32_t kPTmemCols = 128;  // a power of two >= 80
 constexpr long long kPSpinLimit = 4000000000LL;
-// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M = 128, N = 80.
-constexpr uint32_t kPIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPN >> 3) << 17) |
-                             ((uint32_t)(kPM >> 4) << 24);
+
+// Tile geometry for BN output columns per tile (80 or 160).  A tcgen05.mma
+// costs about the same time at N = 80 as at N = 160, so wide tiles pay when
+// there are enough of them to fill the GPU.
+template <int BN>
+struct ProjGeom {
+  static constexpr uint32_t kBStage = BN * kPK * 2;
+  static constexpr uint32_t kAOff = 0;
+  static constexpr uint32_t kBOff = kPStages * kPAStage;
+  static constexpr uint32_t kCtrlOff = kBOff + kPStages * kBStage;
+  static constexpr uint32_t kTmemCols = BN <= 128 ? 128 : 256;  // a power of two >= BN
+  // instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M = 128, N = BN
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kPM >> 4) << 24);
+};
 
 struct ProjCtrl {
   uint64_t full[kPStages];
@@ -45,7 +54,8 @@ struct ProjCtrl {
   uint32_t tmem_base;
   int32_t abort;
 };
-constexpr size_t kPSmem = kPCtrlOff + sizeof(ProjCtrl) + 1024;  // + alignment slack
+template <int BN>
+constexpr size_t proj_smem() { return ProjGeom<BN>::kCtrlOff + sizeof(ProjCtrl) + 1024; }
 
 __device__ __forceinline__ uint32_t p_smem(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -103,12 +113,12 @@ __device__ __forceinline__ uint64_t p_desc(uint32_t saddr) {
 }
 
 __device__ __forceinline__ void p_mma(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
-                                      uint32_t accumulate) {
+                                      uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
-      "l"(adesc), "l"(bdesc), "r"(kPIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -136,17 +146,19 @@ __device__ __forceinline__ uint32_t p_pack(float lo, float hi) {
   return r;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kPThreads, 1)
 proj_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
             uint16_t *__restrict__ y, int64_t y_stride, int32_t n_rows, int32_t out_cols,
             int32_t nk, int32_t *status) {
+  using G = ProjGeom<BN>;
   extern __shared__ uint8_t p_smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(p_smem_raw) + 1023) & ~uintptr_t(1023));
-  ProjCtrl &C = *reinterpret_cast<ProjCtrl *>(smem + kPCtrlOff);
-  const uint32_t sA = p_smem(smem + kPAOff), sB = p_smem(smem + kPBOff);
+  ProjCtrl &C = *reinterpret_cast<ProjCtrl *>(smem + G::kCtrlOff);
+  const uint32_t sA = p_smem(smem + G::kAOff), sB = p_smem(smem + G::kBOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * kPN, m0 = blockIdx.y * kPM;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kPM;
   grid_dependency_sync();  // before TMEM too: an earlier launch may hold it
 
   if (tid == 0) {
@@ -161,7 +173,7 @@ proj_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CU
   if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      p_smem(&C.tmem_base)),
-                 "r"(kPTmemCols)
+                 "r"(G::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -180,9 +192,9 @@ proj_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CU
         const uint32_t it = (uint32_t)(kb / kPStages);
         if (!p_wait(p_smem(&C.empty[s]), (it & 1u) ^ 1u, abort_flag)) break;
         const uint32_t fb = p_smem(&C.full[s]);
-        p_expect_tx(fb, kPAStage + kPBStage);
+        p_expect_tx(fb, kPAStage + G::kBStage);
         p_tma_2d(sA + s * kPAStage, &amap, kb * kPK, m0, fb);
-        p_tma_2d(sB + s * kPBStage, &bmap, kb * kPK, n0, fb);
+        p_tma_2d(sB + s * G::kBStage, &bmap, kb * kPK, n0, fb);
         issued = kb + 1;
       }
       if (*abort_flag) {  // let our own copies land before the CTA leaves
@@ -203,8 +215,8 @@ proj_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CU
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
         for (int kk = 0; kk < kPK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
-          p_mma(tmem, p_desc(sA + s * kPAStage + kk * 32u), p_desc(sB + s * kPBStage + kk * 32u),
-                (kb > 0 || kk > 0) ? 1u : 0u);
+          p_mma(tmem, p_desc(sA + s * kPAStage + kk * 32u), p_desc(sB + s * G::kBStage + kk * 32u),
+                G::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
         p_commit(p_smem(&C.empty[s]));
       }
       // the accumulator is complete (or the CTA aborted) once every MMA issued has drained
@@ -223,7 +235,7 @@ proj_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CU
     const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
     uint16_t *dst = y + (int64_t)r * y_stride + n0;
 #pragma unroll
-    for (int c = 0; c < kPN / 16; ++c) {
+    for (int c = 0; c < BN / 16; ++c) {
       uint32_t v[16];
       p_ld16(taddr + (uint32_t)(16 * c), v);  // every lane of the warp takes part
       if (r < n_rows && n0 + 16 * c < out_cols) {
@@ -247,7 +259,7 @@ proj_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CU
   if (warp == 2) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kPTmemCols)
+                 "r"(G::kTmemCols)
                  : "memory");
   }
 }
@@ -270,6 +282,17 @@ PEncodeFn p_encoder() {
   return fn;
 }
 
+int p_sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
 }  // namespace
 
 cudaError_t launch_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, int32_t n_rows,
@@ -279,7 +302,7 @@ cudaError_t launch_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, 
   PEncodeFn enc = p_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
   const cuuint32_t estr[2] = {1, 1};
-  CUtensorMap amap, bmap;
+  CUtensorMap amap;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)n_rows};
     const cuuint64_t strides[1] = {(cuuint64_t)x_stride * 2};
@@ -289,26 +312,31 @@ cudaError_t launch_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  {
+  const int32_t nk = (hidden + kPK - 1) / kPK;
+  const int64_t m_tiles = (n_rows + kPM - 1) / kPM;
+  // wide tiles once they alone fill most of the GPU
+  const bool wide = m_tiles * ((out_cols + 159) / 160) >= (int64_t)p_sm_count() * 3 / 4;
+  auto run = [&](auto kernel, int bn, size_t smem, bool &attr_set) -> cudaError_t {
+    CUtensorMap bmap;
     const cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)out_cols};
     const cuuint64_t strides[1] = {(cuuint64_t)hidden * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kPK, (cuuint32_t)kPN};
+    const cuuint32_t box[2] = {(cuuint32_t)kPK, (cuuint32_t)bn};
     if (enc(&bmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(w), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  }
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kPSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int32_t nk = (hidden + kPK - 1) / kPK;
-  const dim3 grid((unsigned)((out_cols + kPN - 1) / kPN), (unsigned)((n_rows + kPM - 1) / kPM));
-  return launch_dependent(proj_kernel, grid, dim3(kPThreads), kPSmem, stream, 1u, amap, bmap, y,
-                          y_stride, n_rows, out_cols, nk, status);
+    if (!attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    const dim3 grid((unsigned)((out_cols + bn - 1) / bn), (unsigned)m_tiles);
+    return launch_dependent(kernel, grid, dim3(kPThreads), smem, stream, 1u, amap, bmap, y, y_stride,
+                            n_rows, out_cols, nk, status);
+  };
+  static bool set80 = false, set160 = false;
+  if (wide) return run(proj_kernel<160>, 160, proj_smem<160>(), set160);
+  return run(proj_kernel<80>, 80, proj_smem<80>(), set80);
 }
 
 }  // namespace qsa

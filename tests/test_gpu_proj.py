@@ -78,15 +78,18 @@ def test_proj_matches_oracle(qsa, orc, rows, hidden, out_cols):
     check(orc, got, x, w)
 
 
-def test_proj_slab_2048x2560x640_sampled_rows(qsa, orc):
-    """The pages' slab: 2048 rows, hidden 2560, 640 outputs; every tile runs,
-    rows from each row tile's edges and middle checked."""
-    rng = qi.rng_for(8, salt=2048)
-    x = qi.normal_bf16(rng, (2048, 2560))
+@pytest.mark.parametrize("n_rows", [2048, 4096, 4000])
+def test_proj_slabs_sampled_rows(qsa, orc, n_rows):
+    """The pages' slab (2048 rows, 80-column tiles) and longer launches that take
+    160-column tiles (4096 rows; 4000: a ragged last row tile); hidden 2560, 640
+    outputs; rows from every row tile's edges and middle checked."""
+    rng = qi.rng_for(8, salt=n_rows)
+    x = qi.normal_bf16(rng, (n_rows, 2560))
     w = qi.normal_bf16(rng, (640, 2560), std=0.02)
     got, st = run_proj(qsa, x, w)
     assert st == (0, 0)
-    rows = sorted({r for t in range(16) for r in (128 * t, 128 * t + 61, 128 * t + 127)})
+    rows = sorted({min(r, n_rows - 1) for t in range((n_rows + 127) // 128)
+                   for r in (128 * t, 128 * t + 61, 128 * t + 127)})
     check(orc, got, x, w, rows=rows)
 
 

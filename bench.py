@@ -344,6 +344,20 @@ def oracle_decode_rate(seconds: float, max_rows: int | None = None):
 
 # ------------------------------------------------------------ main arms
 
+def job_rate(torch, ms_local: float, units_local: float, world: int, device):
+    """The whole job's time and rate over `world` ranks (weak scaling): the
+    slowest rank's time, and the units every rank processed divided by it.
+    Ranks hold independent replicas, so these two reductions are the only
+    exchange; with one rank they are the local values."""
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    u = torch.tensor([units_local], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    ms = float(t.item())
+    return ms, float(u.item()) / (ms / 1000.0)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -400,12 +414,8 @@ def run_ours(args, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.summary(t0, t1)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(ms_t.item())
+    ms, value = job_rate(torch, ms, K, world, device)  # K rows on every rank
     ms_per_step = ms / K
-    value = world * K / (ms / 1000.0)
     code, row = qsa.qsa_read_status(wl.status)
     assert code == 0, f"device status {code} row {row}"
 

@@ -111,6 +111,9 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   grid_dependency_sync();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x, y = blockIdx.y, ny = gridDim.y;
+  // the query row's load is issued beside the position's (both may live in
+  // host memory: two round trips side by side instead of one after the other)
+  const uint4 qchunk = load_query_chunk(a, row);
   if (tid == 0) {
     s_maxbin = 0u;
     s_low = 0u;
@@ -179,7 +182,8 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
     }
   };
   if (cnt > 0 && !simt_score_blocks(a, row, p, c0, c1, S, ring,
-                                    [&](int b, float sc) { sc_s[b - c0] = sc; }, prologue, patch)) {
+                                    [&](int b, float sc) { sc_s[b - c0] = sc; }, prologue, patch,
+                                    &qchunk)) {
     if (tid == 0) report_error(a.status, kErrTimeout, row);
     return;  // the row's other CTAs time out at the barrier below
   }

@@ -62,13 +62,24 @@ __device__ __forceinline__ bool simt_wait(uint32_t mbar, uint32_t parity) {
   }
 }
 
+// This thread's 16 bytes of the row's query heads (warps 0 and 1: 4 half-warps
+// = 4 heads); they do not depend on the row's position, so a caller may load
+// them before it reads the position.
+__device__ __forceinline__ uint4 load_query_chunk(const ScoreArgs &a, int row) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= 2) return make_uint4(0u, 0u, 0u, 0u);
+  const int h = warp * 2 + (lane >> 4);
+  return ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * (lane & 15));
+}
+
 __device__ __forceinline__ void prep_query_heads(const ScoreArgs &a, int row, int p,
-                                                 float (*q_s)[kHeadDim]) {
+                                                 float (*q_s)[kHeadDim], const uint4 *preloaded) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp < 2) {  // 4 half-warps = 4 heads
     const int h = warp * 2 + (lane >> 4);
     const int g = lane & 15;
-    const uint4 v = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * g);
+    const uint4 v = preloaded ? *preloaded
+                              : ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * g);
     const uint4 w8 = ldg_nc_v4(a.q_norm_w + 8 * g);
     uint4 c8 = make_uint4(0, 0, 0, 0), s8 = make_uint4(0, 0, 0, 0);
     if (g < 8) {
@@ -104,7 +115,8 @@ template <typename Emit, typename Prologue = SimtNoHook, typename Patch = SimtNo
 __device__ __forceinline__ bool simt_score_blocks(const ScoreArgs &a, int row, int p, int c0, int c1,
                                                   SimtSmem &S, uint8_t *stages, Emit emit,
                                                   Prologue prologue = SimtNoHook(),
-                                                  Patch patch = SimtNoHook()) {
+                                                  Patch patch = SimtNoHook(),
+                                                  const uint4 *preloaded_q = nullptr) {
   const int n_it = (c1 - c0 + kSimtBlocksPerIter - 1) / kSimtBlocksPerIter;
   const uint16_t *kb = a.block_keys + (a.key_base ? a.key_base[row] : 0) * kHeadDim;
   const int tid = threadIdx.x;
@@ -130,7 +142,7 @@ __device__ __forceinline__ bool simt_score_blocks(const ScoreArgs &a, int row, i
     for (int it = 0; it < min(kSimtStages, n_it); ++it) issue(it);
   }
   // the first stages are in flight while the query heads are prepared
-  prep_query_heads(a, row, p, S.q_s);
+  prep_query_heads(a, row, p, S.q_s, preloaded_q);
   prologue();
   __syncthreads();
 

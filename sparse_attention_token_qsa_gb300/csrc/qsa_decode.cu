@@ -21,11 +21,11 @@
 //     key (a non-finite score shows up in the 16 outer bins), writes the final
 //     mask bytes of its own blocks outside that bin, and appends the bin's
 //     keys with their block indices to the row's candidate list;
-//  4. the last CTA of the row to finish (an atomic ticket) runs the remaining
-//     radix rounds (8, 8, 4 bits) over the candidates, cuts exact ties at the
-//     final key by radix rounds on the block index (lowest kept), writes the
-//     kept candidates' mask bytes, and zeroes the row's workspace for the
-//     next call.
+//  4. the last CTA of the row to finish (an atomic ticket) zeroes the row's
+//     workspace for the next call (its stores drain while it works on), runs
+//     the remaining radix rounds (8, 8, 4 bits) over the candidates, cuts
+//     exact ties at the final key by radix rounds on the block index (lowest
+//     kept), and writes the kept candidates' mask bytes.
 //
 // Workspace per row: the 4096-bin histogram, three counters, and room for
 // tokens / 4 candidates (key, block index).  It must be zero before the first
@@ -46,11 +46,13 @@ constexpr long long kDecSpinLimit = 4000000000LL;  // ~2 s of SM clock
 struct RowHdr {  // per row, at the start of the row's workspace
   uint32_t hist0[4096];
   uint32_t arrive;  // CTAs whose histogram is in
-  uint32_t ticket;  // CTAs done writing their blocks
-  uint32_t ncand;   // candidates listed
+  uint32_t pad0;
+  // candidates listed (low 32 bits) and CTAs done writing their blocks (high
+  // 32 bits): the last CTA's ticket returns the list's length with it
+  unsigned long long tc;
   uint32_t maxbin[8];  // the highest bin any key landed in (CTA y adds to slot y % 8)
   uint32_t lowbad;     // a key landed below bin 8 (a negative non-finite score)
-  uint32_t pad[52];
+  uint32_t pad[51];
 };
 static_assert(sizeof(RowHdr) == 16640, "the workspace layout is part of the ABI");
 
@@ -71,6 +73,9 @@ struct DecSmem {  // selection scratch, laid over the key ring once scoring is d
   uint32_t rule_prefix;
   uint32_t rule_shift;
   int32_t rule_cut;
+  uint32_t nl;         // candidates listed over the row (the last CTA)
+  int32_t rsel[4];     // each candidate round's bin ...
+  uint32_t rabove[4];  // ... and the keys above it
 };
 constexpr size_t kDecCandOff = (sizeof(DecSmem) + 127) & ~size_t(127);
 static_assert(kDecCandOff + (size_t)kDecCandCache * 8 <= kSimtRingBytes, "scratch overflows the ring");
@@ -322,7 +327,7 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
       }
       store_blocks(mrow, (int64_t)c0 + i, mq, kept, al16, al4);
       if (bits) {
-        uint32_t at = atomicAdd(&W.ncand, (uint32_t)__popc(bits));
+        uint32_t at = (uint32_t)atomicAdd(&W.tc, (unsigned long long)__popc(bits));
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           if (bits & (1u << e)) {
@@ -341,14 +346,32 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   __syncthreads();
   if (tid == 0) {
     // release this CTA's mask bytes and candidates; the last CTA acquires all
-    uint32_t t;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(&W.ticket) : "memory");
-    D.flag = t == (uint32_t)(ny - 1);
+    unsigned long long t;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
+                 : "=l"(t)
+                 : "l"(&W.tc), "l"(1ull << 32)
+                 : "memory");
+    D.flag = (uint32_t)(t >> 32) == (uint32_t)(ny - 1);
+    D.nl = (uint32_t)t;  // every CTA's candidates are listed by now
   }
   __syncthreads();
   if (!D.flag) return;
+  // every CTA has read the histogram and taken its ticket: clear it for the
+  // next call now, so that the stores drain while the candidates are resolved
+  for (int i = tid; i < 4096 / 4; i += kDecThreads)
+    reinterpret_cast<uint4 *>(W.hist0)[i] = make_uint4(0u, 0u, 0u, 0u);
+  auto clear_counters = [&]() {
+    if (tid == 0) {
+      W.arrive = 0u;
+      W.tc = 0ull;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) W.maxbin[k] = 0u;
+      W.lowbad = 0u;
+    }
+  };
+  if (bad || whole) clear_counters();
   if (!bad && !whole) {
-    const int32_t nl = (int32_t)__ldcg(&W.ncand);
+    const int32_t nl = (int32_t)D.nl;
     for (int j0 = 0; j0 < min(nl, kDecCandCache); j0 += 8 * kDecThreads) {
       uint32_t kk[8], ii[8];  // eight entries per thread in flight
 #pragma unroll
@@ -363,17 +386,21 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
         if (j < min(nl, kDecCandCache)) {
           ck_s[j] = kk[u];
           ci_s[j] = ii[u];
+          cand_key[j] = 0u;  // (the entry lives on in shared memory)
+          cand_idx[j] = 0u;
         }
       }
     }
     for (int i = tid; i < 256 + 256 + 16; i += kDecThreads) (&D.hist1[0])[i] = 0u;
     __syncthreads();
+    clear_counters();
     auto ckey = [&](int32_t j) { return j < kDecCandCache ? ck_s[j] : __ldcg(&cand_key[j]); };
     auto cidx = [&](int32_t j) { return j < kDecCandCache ? ci_s[j] : __ldcg(&cand_idx[j]); };
     uint32_t prefix = B0;
     int shift = 20;
     bool done = false;
-    // rounds of 8, 8 and 4 bits on the candidates
+    // rounds of 8, 8 and 4 bits on the candidates (each round's result in its
+    // own slot: two barriers a round)
     for (int r = 1; r < 4 && !done; ++r) {
       uint32_t *H = r == 1 ? D.hist1 : (r == 2 ? D.hist2 : D.hist3);
       const int nb = r == 3 ? 16 : 256, sh = r == 1 ? 12 : (r == 2 ? 4 : 0);
@@ -386,18 +413,17 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
         uint32_t B, above;
         warp_find_bin(H, nb, need, lane, B, above);
         if (lane == 0) {
-          D.sel_bin = (int32_t)B;
-          D.sel_above = above;
+          D.rsel[r] = (int32_t)B;
+          D.rabove[r] = above;
         }
       }
       __syncthreads();
-      const uint32_t B = (uint32_t)D.sel_bin;
+      const uint32_t B = (uint32_t)D.rsel[r];
       const uint32_t cB = H[B];
-      need -= D.sel_above;
+      need -= D.rabove[r];
       prefix = (prefix << (shift - sh)) | B;
       shift = sh;
       done = cB == need;
-      __syncthreads();  // sel_bin is rewritten next round
     }
     if (done) {
       if (tid == 0) {
@@ -456,23 +482,12 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
       const int32_t gi = (int32_t)cidx(j);
       if (kk > rp || (kk == rp && gi <= rc)) store_blocks(mrow, gi, 1, 1u, false, al4);
     }
-  }
-  // leave the row's workspace zero for the next call
-  if (!bad && !whole) {
-    const int32_t nl = (int32_t)__ldcg(&W.ncand);
-    for (int32_t j = tid; j < nl; j += kDecThreads) {
+    // candidates past the shared-memory cache were read from the workspace
+    // until now: cleared last
+    for (int32_t j = kDecCandCache + tid; j < nl; j += kDecThreads) {
       cand_key[j] = 0u;
       cand_idx[j] = 0u;
     }
-  }
-  for (int i = tid; i < 4096; i += kDecThreads) W.hist0[i] = 0u;
-  if (tid == 0) {
-    W.arrive = 0u;
-    W.ticket = 0u;
-    W.ncand = 0u;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) W.maxbin[k] = 0u;
-    W.lowbad = 0u;
   }
 }
 

@@ -52,8 +52,12 @@ __host__ __device__ constexpr int round_bins(int r) { return r == 0 ? 4096 : (r 
 __host__ __device__ constexpr int round_shift(int r) { return r == 0 ? 20 : (r == 1 ? 12 : (r == 2 ? 4 : 0)); }
 constexpr int kCandCap = 4096;                    // keys of round 0's bin kept for rounds 1..3
 
+constexpr int kZeroLanes = 32;  // round 0 counts exact zeros in one spare bin per lane
+
 struct SelectSmem {
-  uint32_t hist0[4096];  // per-round histograms; in a cluster round 0's is merged in place
+  // per-round histograms; in a cluster round 0's is merged in place.  Round
+  // 0's has kZeroLanes spare bins past its 4096, folded into the zero bin.
+  uint32_t hist0[4096 + kZeroLanes];
   uint32_t hist1[256];
   uint32_t hist2[256];
   uint32_t hist3[16];
@@ -69,6 +73,8 @@ struct SelectSmem {
   uint32_t eq_base;
   uint32_t band_hi;  // sampled band: keys at or above its upper edge
   int32_t band_bin[2];  // sampled band: its top and bottom bins
+  int32_t rsel[kRounds];     // each candidate round's bin ...
+  uint32_t rabove[kRounds];  // ... and the keys above it
   // cand keys [kCandCap] u32, cand local indices [kCandCap] u16, keys[] follow (dynamic)
 };
 
@@ -146,8 +152,16 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   const int32_t cnt = b1 - b0;
   const float *srow = scores + (int64_t)row * score_cols + b0;
   const int32_t cached = CACHE ? min(cnt, cap) : 0;
+  if (!CACHE && cnt <= 16384) {
+    // a slice of up to 64 KiB heads for L2 at once (two requests a thread):
+    // the loads below then wait on L2, not on HBM.  (A longer slice would
+    // crowd L2 out across the resident CTAs; the sampled band prefetches its
+    // own first batches.)
+    for (int32_t l = 32 * tid; l < cnt; l += 32 * NT)  // 32 scores: one 128-byte line
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(srow + l));
+  }
 
-  for (int i = tid; i < 4096 + 256 + 256 + 16; i += NT) (&S.hist0[0])[i] = 0u;
+  for (int i = tid; i < 4096 + kZeroLanes + 256 + 256 + 16; i += NT) (&S.hist0[0])[i] = 0u;
   if (tid == 0) {
     S.ncand = 0u;
     S.eq_base = 0u;
@@ -335,11 +349,13 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 
   if (!sampled) {
     // ---- round 0 while loading: key cache and top-12-bit histogram.  Exact
-    // zeros (relu outputs) share one bin: counted in registers, added per warp.
+    // zeros (relu outputs, the one heavy bin) go to the lane's own spare bin,
+    // so the lanes of a warp rarely add to the same bin; the spare bins are
+    // folded into the zero bin afterwards.
     {
       constexpr int kLoadsInFlight = 4;  // float4 loads issued per thread before use
       const int32_t nq = (cnt + 3) >> 2;
-      uint32_t zeros = 0;
+      const uint32_t zbin = 4096u + (uint32_t)lane;
       // one quad's keys into the histogram (and the key cache); ne = its keys in
       // the slice, a constant 4 on the fast path below
       auto take = [&](const float4 &f, int32_t qd, int ne) {
@@ -353,12 +369,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
               if (4 * qd + e < cached) keys_s[4 * qd + e] = kq[e];
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (e < ne) {
-              zeros += kq[e] == kZeroKey ? 1u : 0u;
-              if (kq[e] != kZeroKey) atomicAdd(&S.hist0[kq[e] >> 20], 1u);
-            }
-          }
+          for (int e = 0; e < 4; ++e)
+            if (e < ne) atomicAdd(&S.hist0[kq[e] == kZeroKey ? zbin : kq[e] >> 20], 1u);
         } else {
           // no copy to keep: zeros of either sign are found on the raw bits,
           // and no other key needs the -0.0 fold
@@ -367,10 +379,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             if (e < ne) {
-              const bool z = (uq[e] << 1) == 0u;
-              zeros += z ? 1u : 0u;
               const uint32_t key = uq[e] ^ ((uint32_t)((int32_t)uq[e] >> 31) | 0x80000000u);
-              if (!z) atomicAdd(&S.hist0[key >> 20], 1u);
+              atomicAdd(&S.hist0[(uq[e] << 1) == 0u ? zbin : key >> 20], 1u);
             }
           }
         }
@@ -401,10 +411,12 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
           if (qd < nq) take(v[u], qd, min(4, cnt - 4 * qd));
         }
       }
-      // one add per warp for the zeros
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) zeros += __shfl_xor_sync(0xffffffffu, zeros, off);
-      if (lane == 0 && zeros) atomicAdd(&S.hist0[kZeroKey >> 20], zeros);
+      // the spare bins into the zero bin
+      __syncthreads();
+      if (tid < kZeroLanes) {
+        const uint32_t z = S.hist0[4096 + tid];
+        if (z) atomicAdd(&S.hist0[kZeroKey >> 20], z);
+      }
     }
 
     // ---- round 0: merge the top-12-bit histograms over the cluster
@@ -468,18 +480,19 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         // own keys are written as dropped, appended with their local block
         // index to the candidate list (slots from a shared counter, so the list
         // is unordered) and patched once the threshold inside the bin is known.
+        // About one key in 25 lies in the bin, so nearly every warp step would
+        // take a listing branch: the pass only marks the thread's quads that
+        // hold one, and reads those few again afterwards to list them.
         {
           const uintptr_t rbm = reinterpret_cast<uintptr_t>(mrow);
           const bool m16 = (rbm & 15u) == 0, m4 = (rbm & 3u) == 0;
           // B0 < 0xFF8 (a finite key's bin), so the upper edge does not wrap
           const uint32_t bin_lo = B0 << 20, bin_hi = (B0 + 1u) << 20;
           const float t_lo = key_to_float(bin_lo), t_hi = key_to_float(bin_hi);
-          // one quad: its mask word(s) and its candidates; mq = its keys in the
-          // slice, a constant 4 on the fast path
-          auto place = [&](int32_t i, const uint32_t (&k)[4], int mq) {
-            // against the bin's edges (keys, or raw scores against the edges'
-            // floats): >= hi kept, [lo, hi) candidates
-            uint32_t bits = 0, w[4];
+          // one quad's keys against the bin's edges (keys, or raw scores against
+          // the edges' floats): w = mask words (>= hi kept), bits = [lo, hi)
+          auto classify = [&](const uint32_t (&k)[4], int mq, uint32_t (&w)[4]) {
+            uint32_t bits = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const bool in = e < mq;
@@ -494,27 +507,10 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
               w[e] = (in && kp) ? 0x01010101u : 0u;
               bits |= (in && !kp && lo) ? (1u << e) : 0u;
             }
-            if (mq == 4 && m16) {
-              *reinterpret_cast<uint4 *>(mrow + 4 * ((int64_t)b0 + i)) = make_uint4(w[0], w[1], w[2], w[3]);
-            } else {
-              store_blocks(mrow, (int64_t)b0 + i, mq,
-                           (w[0] & 1u) | ((w[1] & 1u) << 1) | ((w[2] & 1u) << 2) | ((w[3] & 1u) << 3),
-                           m16, m4);
-            }
-            if (bits) {
-              uint32_t at = atomicAdd(&S.ncand, (uint32_t)__popc(bits));
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                if (bits & (1u << e)) {
-                  cand_s[at] = CACHE ? k[e] : order_key(__uint_as_float(k[e]));
-                  cand_li[at] = (uint16_t)(i + e);
-                  ++at;
-                }
-              }
-            }
+            return bits;
           };
-          for (int32_t i = 4 * tid; i < cnt; i += 4 * NT) {
-            uint32_t k[4];  // order keys (cached), else raw score bits
+          // quad i's keys (order keys from the cache, else raw score bits)
+          auto fetch = [&](int32_t i, uint32_t (&k)[4]) {
             if (i + 3 < cnt && (!CACHE || i + 3 < cached)) {  // a whole quad, one 16-byte load
               if constexpr (CACHE) {
                 const uint4 kv = *reinterpret_cast<const uint4 *>(keys_s + i);
@@ -529,7 +525,6 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
                 k[2] = __float_as_uint(f.z);
                 k[3] = __float_as_uint(f.w);
               }
-              place(i, k, 4);
             } else {  // the slice's last quad, or past the key cache
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -539,7 +534,76 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
                 else
                   k[e] = (i + e < cnt) ? __float_as_uint(__ldg(srow + i + e)) : 0u;
               }
-              place(i, k, min(4, cnt - i));
+            }
+          };
+          uint64_t marked = 0;  // bit t: the thread's t-th quad holds candidates (per <= 65536)
+          // quad i (the thread's t-th): its final mask words, and its mark
+          auto place = [&](int32_t i, int t, const uint32_t (&k)[4]) {
+            uint32_t w[4];
+            const int mq = min(4, cnt - i);
+            const uint32_t bits = classify(k, mq, w);
+            if (mq == 4 && m16) {
+              *reinterpret_cast<uint4 *>(mrow + 4 * ((int64_t)b0 + i)) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+              store_blocks(mrow, (int64_t)b0 + i, mq,
+                           (w[0] & 1u) | ((w[1] & 1u) << 1) | ((w[2] & 1u) << 2) | ((w[3] & 1u) << 3),
+                           m16, m4);
+            }
+            marked |= bits ? (1ull << t) : 0ull;
+          };
+          // a whole quad, at a 16-byte aligned mask word: no per-key bounds
+          // tests, and only whether it holds a candidate (the listing below
+          // classifies marked quads again)
+          auto place4 = [&](int32_t i, int t, const uint32_t (&k)[4]) {
+            uint32_t w[4];
+            bool any = false;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              bool kp, lo;
+              if constexpr (CACHE) {
+                kp = k[e] >= bin_hi;
+                lo = k[e] >= bin_lo;
+              } else {
+                kp = __uint_as_float(k[e]) >= t_hi;
+                lo = __uint_as_float(k[e]) >= t_lo;
+              }
+              w[e] = kp ? 0x01010101u : 0u;
+              any |= lo && !kp;
+            }
+            *reinterpret_cast<uint4 *>(mrow + 4 * ((int64_t)b0 + i)) = make_uint4(w[0], w[1], w[2], w[3]);
+            marked |= any ? (1ull << t) : 0ull;
+          };
+          int32_t i = 4 * tid, t = 0;
+          if (m16) {  // two whole quads per step, both loads in flight
+            for (; i + 4 * NT + 3 < cnt; i += 8 * NT, t += 2) {
+              uint32_t k0[4], k1[4];
+              fetch(i, k0);
+              fetch(i + 4 * NT, k1);
+              place4(i, t, k0);
+              place4(i + 4 * NT, t + 1, k1);
+            }
+          }
+          for (; i < cnt; i += 4 * NT, ++t) {
+            uint32_t k[4];
+            fetch(i, k);
+            place(i, t, k);
+          }
+          // the marked quads again: their bin keys into the candidate list
+          while (marked) {
+            const int t = __ffsll((long long)marked) - 1;
+            marked &= marked - 1ull;
+            const int32_t i = 4 * tid + t * 4 * NT;
+            uint32_t k[4], w[4];
+            fetch(i, k);
+            const uint32_t bits = classify(k, min(4, cnt - i), w);
+            uint32_t at = atomicAdd(&S.ncand, (uint32_t)__popc(bits));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (bits & (1u << e)) {
+                cand_s[at] = CACHE ? k[e] : order_key(__uint_as_float(k[e]));
+                cand_li[at] = (uint16_t)(i + e);
+                ++at;
+              }
             }
           }
         }
@@ -580,34 +644,44 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         cand_li[j] = ld_dsmem_u16(&cand_li[jj], (uint32_t)q);
       }
       __syncthreads();
+      // Every candidate of the gathered list, strided over the CTA by whole
+      // warps (lanes past the end hold valid = false): fn(valid, key, global
+      // block index).
       const int32_t nl = (int32_t)S.roff[C];
+      auto each = [&](auto &&fn) {
+        for (int32_t j0 = warp * 32; j0 < nl; j0 += NT) {
+          const int32_t j = j0 + lane;
+          const bool v = j < nl;
+          int q = 0;
+          while (q + 1 < C && v && (int32_t)S.roff[q + 1] <= j) ++q;
+          fn(v, v ? cand_s[j] : 0u, v ? (uint32_t)(q * per) + (uint32_t)cand_li[j] : 0u);
+        }
+      };
       // rounds 1..3 on the candidates: every thread histograms, one warp
       // finds the bin (two barriers a round)
       bool done = false;
       for (int r = 1; r < kRounds && !done; ++r) {
         uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
         const int nb = round_bins(r), sh = round_shift(r);
-        for (int32_t j = tid; j < nl; j += NT) {
-          const uint32_t key = cand_s[j];
-          if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
-        }
+        each([&](bool v, uint32_t key, uint32_t) {
+          if (v && (key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+        });
         __syncthreads();
         if (warp == 0) {
           uint32_t B, above;
           warp_find_bin(H, nb, need, lane, B, above);
           if (lane == 0) {
-            S.sel_bin = (int32_t)B;
-            S.sel_above = above;
+            S.rsel[r] = (int32_t)B;
+            S.rabove[r] = above;
           }
         }
         __syncthreads();
-        const uint32_t B = (uint32_t)S.sel_bin;
+        const uint32_t B = (uint32_t)S.rsel[r];
         const uint32_t cB = H[B];
-        need -= S.sel_above;
+        need -= S.rabove[r];
         prefix = (prefix << (shift - sh)) | B;
         shift = sh;
         done = cB == need;
-        __syncthreads();  // sel_bin is rewritten next round
       }
       if (done) {
         if (tid == 0) {
@@ -618,8 +692,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       } else {
         // ties at the full key: of the keys equal to `prefix`, the `need`
         // with the lowest block indices are kept.  Radix rounds over the
-        // equal candidates' block indices, 8 bits at a time from the
-        // highest bit an index < n can have, find the cut index.
+        // equal candidates' block indices, 8 bits at a time from the highest
+        // bit an index < n can have, find the cut index.
         const uint32_t top = (uint32_t)n - 1u;
         int ish = top ? ((32 - __clz((int)top) + 7) & ~7) : 8;  // index bits, rounded up
         uint32_t iprefix = 0;  // the cut index's bits above ish
@@ -628,14 +702,10 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
           const int sh = ish - 8;
           if (tid < 256) H[tid] = 0u;
           __syncthreads();
-          for (int32_t j = tid; j < nl; j += NT) {
-            if (cand_s[j] != prefix) continue;
-            int q = 0;
-            while (q + 1 < C && (int32_t)S.roff[q + 1] <= j) ++q;
-            const uint32_t gi = (uint32_t)(q * per) + (uint32_t)cand_li[j];
-            if (ish >= 32 || (gi >> ish) == iprefix)  // ascending: digit d counts in bin 255-d
+          each([&](bool v, uint32_t key, uint32_t gi) {
+            if (v && key == prefix && (ish >= 32 || (gi >> ish) == iprefix))  // ascending: digit d in bin 255-d
               atomicAdd(&H[255u - ((gi >> sh) & 255u)], 1u);
-          }
+          });
           __syncthreads();
           if (warp == 0) {
             uint32_t B, above;

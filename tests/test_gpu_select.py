@@ -83,6 +83,34 @@ def test_select_many_long_rows_one_cta_each(qsa, orc):
         assert not bad, (budget, bad[:8])
 
 
+@pytest.mark.parametrize("k", [16, 17, 40])
+def test_select_many_rows_candidates_crowding_one_thread(qsa, orc, k):
+    """Many 16384-block rows (one CTA each, no key cache): the threshold bin's
+    keys sit in the positions one thread of the compaction pass reads (block
+    1024 j + e), k of them; 16 fit that thread's candidate slots, more send
+    the row to the rounds over every key.  Every fourth row is plain random;
+    tails of 0, 3 and 2 tokens."""
+    rng = qi.rng_for(4, salt=900 + k)
+    rows, tokens = 320, 65536
+    cols = tokens // 4
+    scores = rng.random((rows, cols), dtype=np.float32)
+    pos = (tokens - 1 - (np.arange(rows) % 3)).astype(np.int32)
+    crowd = (1024 * np.arange(16)[:, None] + np.arange(4)[None, :]).ravel()   # one thread's keys
+    for r in range(rows):
+        if r % 4 == 3:
+            continue
+        n = (int(pos[r]) + 1) // 4
+        top = rng.choice(np.setdiff1d(np.arange(n), crowd), size=500, replace=False)
+        scores[r, top] = rng.uniform(4.0, 8.0, size=500).astype(np.float32)
+        at = rng.choice(crowd[crowd < n], size=k, replace=False)
+        scores[r, at] = (2.0 + np.arange(k) * 2.0 ** -10).astype(np.float32)   # one 12-bit bin
+    got, _ = gpu_select(qsa, scores, cols, pos, tokens, 2048)
+    want, codes = oracle_masks(orc, scores, cols, pos, tokens, 2048)
+    assert all(c == 0 for c in codes)
+    bad = [r for r in range(rows) if not np.array_equal(got[r], want[r])]
+    assert not bad, bad[:8]
+
+
 def test_select_prefill_rows_with_injected_ties(qsa, orc):
     """Single-sequence prefill geometry (T=2304): every row, all-kept rows below
     the inert bound and truncating rows above it; 32 truncating rows get exact

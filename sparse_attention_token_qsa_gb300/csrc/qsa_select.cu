@@ -178,8 +178,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   int shift = 32;          // ... prefix = threshold >> shift
   bool rule_ready = false;  // the kept set is known: no candidate rounds
 
-  // ---- sampled band (a row on one CTA, long enough for a sample).  8 * NT
-  // scores in runs of 8, spread evenly over the row, are histogrammed on the
+  // ---- sampled band (a row on one CTA, long enough for a sample).  kRun * NT
+  // scores in runs of kRun, spread evenly over the row, are histogrammed on the
   // top 12 key bits.  With r = need * samples / n, the bins holding the
   // sample's (r - d)-th and (r + d)-th largest keys (d = 3 sqrt(r) + 2) bound
   // a band [t_lo, t_hi) that holds the row's keep-th key unless the sample is
@@ -191,7 +191,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   // is selected again by the full-histogram path, which rewrites every byte.
   bool sampled = false;
   {
-    constexpr int kSamp = 8 * NT;
+    constexpr int kRun = 8;  // (runs of 16 or 32 measured slower on 256k rows)
+    constexpr int kSamp = kRun * NT;
     // (rows whose keys a second pass would still find in L2 are faster on the
     // full-histogram path, and the cached shape never reads a key twice)
     const bool try_sample = !CACHE && C == 1 && cnt > 32768 && cnt <= 65536 &&
@@ -209,14 +210,20 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
           if (4 * qd < cnt)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(srow + 4 * (int64_t)qd));
         }
-        // run `tid` starts at a multiple of 8 at most cnt - 8 (rows are 16-byte aligned)
-        const int32_t at = (int32_t)((((int64_t)tid * (cnt - 8)) / (NT - 1)) & ~int64_t(7));
-        const float4 f0 = __ldg(reinterpret_cast<const float4 *>(srow + at));
-        const float4 f1 = __ldg(reinterpret_cast<const float4 *>(srow + at + 4));
-        const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+        // run `tid` starts at a multiple of 4 at most cnt - kRun (rows are 16-byte aligned)
+        const int32_t at = (int32_t)((((int64_t)tid * (cnt - kRun)) / (NT - 1)) & ~int64_t(3));
+        float v[kRun];
+#pragma unroll
+        for (int u = 0; u < kRun / 4; ++u) {
+          const float4 f = __ldg(reinterpret_cast<const float4 *>(srow + at + 4 * u));
+          v[4 * u] = f.x;
+          v[4 * u + 1] = f.y;
+          v[4 * u + 2] = f.z;
+          v[4 * u + 3] = f.w;
+        }
         bool nf = false;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < kRun; ++e) {
           nf |= (__float_as_uint(v[e]) & 0x7F800000u) == 0x7F800000u;
           atomicAdd(&S.hist0[order_key(v[e]) >> 20], 1u);
         }

@@ -253,11 +253,16 @@ def test_select_row_out_of_range_reported(qsa):
 
 
 def sampled_blocks(n):
+    """Every block a sampled-band pass could read: runs of `run` scores starting
+    at (t * (n - run)) // (nt - 1), rounded down to 4 (or 8), for each thread t
+    of either block shape and each run length the kernel may use."""
     hit = np.zeros(n, bool)
     for nt in (256, 512):
         t = np.arange(nt, dtype=np.int64)
-        at = ((t * (n - 8)) // (nt - 1)) & ~7
-        hit[(at[:, None] + np.arange(8)[None, :]).ravel()] = True
+        for run in (8, 16, 32):
+            for align in (3, 7):
+                at = ((t * (n - run)) // (nt - 1)) & ~align
+                hit[(at[:, None] + np.arange(run)[None, :]).ravel()] = True
     return hit
 
 

@@ -249,9 +249,16 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   const uint32_t sK = smem_u32(smem + kKOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int32_t row_tiles = (a.n_rows + kRowsPerCta - 1) / kRowsPerCta;
-  grid_dependency_sync();  // before TMEM too: an earlier launch may hold it
 
-  // ---- set-up: barriers, TMEM, and the work each row tile needs
+  // ---- set-up: barriers, TMEM, and the work each row tile needs.  It runs
+  // while the previous launch in the stream finishes: that launch is always
+  // the query preparation or an earlier slab of this kernel, which let this
+  // one start only once every launch before them had completed, and neither
+  // writes what the set-up reads (positions, visible lengths).  A CTA of an
+  // earlier slab still holding TMEM cannot share an SM with this one (each
+  // takes most of the shared memory), so the allocation does not wait on it.
+  // The wait for the previous launch itself comes before the first copy of
+  // the prepared queries.
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&C.full[s]), 1);
@@ -299,6 +306,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dependency_sync();
 
   const int64_t W = C.start[row_tiles];
   const int32_t w0 = (int32_t)(W * blockIdx.x / gridDim.x);

@@ -10,12 +10,14 @@
 // alone fill most of the GPU (4096 x 640: 128 CTAs) and 80 otherwise (a 2048 x
 // 640 slab: 16 x 8 = 128 CTAs): a tcgen05.mma takes about as long at N = 80 as
 // at N = 160, so the wider tile does twice the work per instruction.  Warp 0's
-// lane 0 streams 64-wide K slices of both operands with TMA (128-byte swizzle,
-// zero fill past the matrix edges) into a six-stage ring; warp 1's lane 0
-// issues tcgen05.mma M128 N=BN K16 four times per slice into a TMEM
-// accumulator (f32); then all four warps drain their 32 TMEM lanes (one output
-// row per thread), round to bf16 and store.  Every wait is bounded; on a
-// timeout the CTA records QSA_ERR_TIMEOUT.
+// lane 0 streams 128-wide K slices of both operands with TMA (two 64-wide
+// boxes each, 128-byte swizzle, zero fill past the matrix edges) into a ring
+// of four (BN = 80) or three (BN = 160) stages; warp 1's lane 0 issues
+// tcgen05.mma M128 N=BN K16 eight times per slice into a TMEM accumulator
+// (f32) -- one barrier wait per eight instructions: 64-wide slices, one wait
+// per four, took a quarter longer -- then all four warps drain their 32 TMEM
+// lanes (one output row per thread), round to bf16 and store.  Every wait is
+// bounded; on a timeout the CTA records QSA_ERR_TIMEOUT.
 #include <cuda.h>  // CUtensorMap and its enums (the encoder comes from the runtime)
 
 #include "qsa_device.cuh"
@@ -26,10 +28,12 @@ namespace qsa {
 namespace {
 
 constexpr int kPM = 128;        // output rows per tile (TMEM lanes)
-constexpr int kPK = 64;         // K per stage: one 128-byte swizzled row of bf16
-constexpr int kPStages = 6;
+constexpr int kPK = 64;         // K per TMA box: one 128-byte swizzled row of bf16
+constexpr int kPKS = 128;       // K per stage: two boxes
+constexpr int kPStages = 4;     // ring slots (the most any tile width uses)
 constexpr int kPThreads = 128;
-constexpr uint32_t kPAStage = kPM * kPK * 2;  // 16 KiB
+constexpr uint32_t kPAStage = kPM * kPKS * 2;  // 32 KiB
+constexpr uint32_t kPAChunk = kPM * kPK * 2;   // 16 KiB
 constexpr long long kPSpinLimit = 4000000000LL;
 
 // Tile geometry for BN output columns per tile (80 or 160).  A tcgen05.mma
@@ -37,10 +41,12 @@ constexpr long long kPSpinLimit = 4000000000LL;
 // there are enough of them to fill the GPU.
 template <int BN>
 struct ProjGeom {
-  static constexpr uint32_t kBStage = BN * kPK * 2;
+  static constexpr int kStages = BN <= 96 ? 4 : 3;
+  static constexpr uint32_t kBStage = BN * kPKS * 2;
+  static constexpr uint32_t kBChunk = BN * kPK * 2;
   static constexpr uint32_t kAOff = 0;
-  static constexpr uint32_t kBOff = kPStages * kPAStage;
-  static constexpr uint32_t kCtrlOff = kBOff + kPStages * kBStage;
+  static constexpr uint32_t kBOff = kStages * kPAStage;
+  static constexpr uint32_t kCtrlOff = kBOff + kStages * kBStage;
   static constexpr uint32_t kTmemCols = BN <= 128 ? 128 : 256;  // a power of two >= BN
   // instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M = 128, N = BN
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -162,7 +168,7 @@ proj_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CU
   grid_dependency_sync();  // before TMEM too: an earlier launch may hold it
 
   if (tid == 0) {
-    for (int s = 0; s < kPStages; ++s) {
+    for (int s = 0; s < G::kStages; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(p_smem(&C.full[s])) : "memory");
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(p_smem(&C.empty[s])) : "memory");
     }
@@ -188,18 +194,20 @@ proj_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CU
     if (lane == 0) {
       int issued = 0;
       for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kPStages;
-        const uint32_t it = (uint32_t)(kb / kPStages);
+        const int s = kb % G::kStages;
+        const uint32_t it = (uint32_t)(kb / G::kStages);
         if (!p_wait(p_smem(&C.empty[s]), (it & 1u) ^ 1u, abort_flag)) break;
         const uint32_t fb = p_smem(&C.full[s]);
         p_expect_tx(fb, kPAStage + G::kBStage);
-        p_tma_2d(sA + s * kPAStage, &amap, kb * kPK, m0, fb);
-        p_tma_2d(sB + s * G::kBStage, &bmap, kb * kPK, n0, fb);
+        p_tma_2d(sA + s * kPAStage, &amap, kb * kPKS, m0, fb);
+        p_tma_2d(sA + s * kPAStage + kPAChunk, &amap, kb * kPKS + kPK, m0, fb);
+        p_tma_2d(sB + s * G::kBStage, &bmap, kb * kPKS, n0, fb);
+        p_tma_2d(sB + s * G::kBStage + G::kBChunk, &bmap, kb * kPKS + kPK, n0, fb);
         issued = kb + 1;
       }
       if (*abort_flag) {  // let our own copies land before the CTA leaves
-        for (int kb = issued - kPStages < 0 ? 0 : issued - kPStages; kb < issued; ++kb)
-          p_wait(p_smem(&C.full[kb % kPStages]), (uint32_t)(kb / kPStages) & 1u, nullptr);
+        for (int kb = issued - G::kStages < 0 ? 0 : issued - G::kStages; kb < issued; ++kb)
+          p_wait(p_smem(&C.full[kb % G::kStages]), (uint32_t)(kb / G::kStages) & 1u, nullptr);
       }
     }
     __syncwarp();
@@ -208,15 +216,43 @@ proj_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CU
     if (lane == 0) {
       bool ok = true;
       for (int kb = 0; kb < nk && ok; ++kb) {
-        const int s = kb % kPStages;
-        const uint32_t it = (uint32_t)(kb / kPStages);
-        ok = p_wait(p_smem(&C.full[s]), it & 1u, abort_flag);
+        const int s = kb % G::kStages;
+        const uint32_t it = (uint32_t)(kb / G::kStages);
+        {
+          // non-suspending polls: the stage has usually landed already (a
+          // suspending wait here cost about 2 % at 2048 and 4096 rows)
+          const uint32_t fa = p_smem(&C.full[s]);
+          const long long t0 = clock64();
+          while (true) {
+            uint32_t done;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(done)
+                : "r"(fa), "r"(it & 1u)
+                : "memory");
+            if (done) break;
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            if (clock64() - t0 > kPSpinLimit) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
+        }
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
-        for (int kk = 0; kk < kPK / 16; ++kk)  // K = 16 per MMA: 32 bytes along the swizzled row
-          p_mma(tmem, p_desc(sA + s * kPAStage + kk * 32u), p_desc(sB + s * G::kBStage + kk * 32u),
+        for (int kk = 0; kk < kPKS / 16; ++kk) {  // K = 16 per MMA: 32 bytes along the swizzled row
+          const uint32_t ka = (uint32_t)(kk >> 2) * kPAChunk + (uint32_t)(kk & 3) * 32u;
+          const uint32_t kbb = (uint32_t)(kk >> 2) * G::kBChunk + (uint32_t)(kk & 3) * 32u;
+          p_mma(tmem, p_desc(sA + s * kPAStage + ka), p_desc(sB + s * G::kBStage + kbb),
                 G::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        }
         p_commit(p_smem(&C.empty[s]));
       }
       // the accumulator is complete (or the CTA aborted) once every MMA issued has drained
@@ -312,7 +348,7 @@ cudaError_t launch_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const int32_t nk = (hidden + kPK - 1) / kPK;
+  const int32_t nk = (hidden + kPKS - 1) / kPKS;
   const int64_t m_tiles = (n_rows + kPM - 1) / kPM;
   // wide tiles once they alone fill most of the GPU
   const bool wide = m_tiles * ((out_cols + 159) / 160) >= (int64_t)p_sm_count() * 3 / 4;

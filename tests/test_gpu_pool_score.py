@@ -281,3 +281,33 @@ def test_score_tc_chunk_64k_sampled(qsa, orc, tables):
                                        rng.choice(rows, 40, replace=False)]))
     want, _ = oracle_scores(orc, q[sample], 640, pos[sample], tokens, qw, c, s, keys, cols)
     assert_close(got[sample], want, "64k chunk scores (sampled rows)")
+
+
+def test_score_tc_rows_past_one_slab(qsa, orc, tables):
+    """More rows than one launch of the tensor-core scorer balances (65536):
+    the rows go in two slabs, the second launched behind the first; rows on
+    both sides of the slab edge against the oracle, an invalid row in the
+    second slab reported with its global index."""
+    rng = qi.rng_for(2, salt=66)
+    c, s, cd, sd = tables
+    tokens, rows = 1024, 65536 + 200
+    raw = qi.raw_keys(rng, tokens)
+    qw, kw = qi.norm_weights(rng)
+    nb = tokens // 4
+    keys = orc.pool_blocks(raw, 128, 0, nb, kw, c, s, EPS)
+    q = qi.fused_qk(rng, rows)
+    pos = rng.integers(0, tokens, size=rows).astype(np.int32)
+    bad = 65536 + 17
+    pos[bad] = tokens                       # out of range, in the second slab
+    cols = nb
+    sc = torch.full((rows, cols), -7.0, dtype=torch.float32, device="cuda")
+    st = qsa.new_status()
+    qsa.qsa_score_rows_with(dev(q), 640, dev(pos), None, rows, tokens, dev(qw), cd, sd,
+                            c.shape[0], EPS, dev(keys), None, sc, cols, st, path=2,
+                            workspace=qsa.new_workspace(rows))
+    assert qsa.qsa_read_status(st) == (3, bad)
+    got = sc.cpu().numpy()
+    assert np.all(got[bad] == -7.0)
+    sample = np.array([0, 1, 65470, 65535, 65536, 65537, 65560, rows - 1])
+    want, _ = oracle_scores(orc, q[sample], 640, pos[sample], tokens, qw, c, s, keys, cols)
+    assert_close(got[sample], want, "scores on both sides of the slab edge")

@@ -131,6 +131,10 @@ struct AttnArgs {
   int32_t nq, nkv, group;  // group = nq / nkv
   const uint16_t *k_pool, *v_pool;
   int32_t pool_pages, page_size;
+  // page of token t >= 0: t / page_size as umulhi(t, pg_mul) >> pg_shift
+  // (pg_shift < 0: page_size 1, the page is t)
+  uint32_t pg_mul;
+  int32_t pg_shift;
   const int32_t *table;
   int32_t table_len;
   int64_t table_cols;
@@ -201,13 +205,16 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
   const int n_tiles = (n + kAttnTile - 1) / kAttnTile;
   const int tok_in_tile = 4 * warp + (lane & 3);  // lanes 0..7 (the rest mirror them)
   constexpr int32_t kNoToken = INT32_MIN;
+  auto page_of = [&](int32_t t) -> int32_t {  // t >= 0
+    return a.pg_shift < 0 ? t : (int32_t)(__umulhi((uint32_t)t, a.pg_mul) >> a.pg_shift);
+  };
   auto fetch_tok = [&](int i) -> int32_t {
     const int32_t j = i * kAttnTile + tok_in_tile;
     return (i < n_tiles && j < n) ? srow[j] : kNoToken;
   };
   auto fetch_page = [&](int32_t t) -> int32_t {  // -1: outside the table
     if (t == kNoToken) return kNoToken;
-    const int32_t pg = t >= 0 ? t / a.page_size : -1;
+    const int32_t pg = t >= 0 ? page_of(t) : -1;
     return (t >= 0 && pg < a.table_len) ? trow[pg] : -1;
   };
   auto start = [&](int i, int32_t t, int32_t phys) {  // this warp's part of tile i
@@ -224,7 +231,7 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
     }
     __syncwarp();
     if (ok) {
-      const int32_t pg = t / a.page_size;
+      const int32_t pg = page_of(t);
       const int64_t src_row = ((int64_t)phys * a.page_size + (t - pg * a.page_size)) * a.nkv + kvh;
       const uint16_t *src = (lane < 4 ? a.k_pool : a.v_pool) + src_row * HD;
       const uint8_t *dst = ring + (size_t)s * Geo::kStageBytes +
@@ -459,6 +466,21 @@ cudaError_t launch_sparse_attn(const uint16_t *q, int64_t q_stride, int32_t nq, 
   a.v_pool = v_pool;
   a.pool_pages = pool_pages;
   a.page_size = page_size;
+  // Division by the page size as a multiply-high and a shift (Granlund and
+  // Montgomery, "Division by invariant integers using multiplication", 1994):
+  // with l = ceil(log2 d), p = 31 + l and m = ceil(2^p / d) < 2^32, every
+  // 0 <= t < 2^31 has t / d == (t * m) >> p, since t * (m d - 2^p) < 2^31 d
+  // <= 2^p keeps the error below 1/d.
+  if (page_size == 1) {
+    a.pg_mul = 1u;
+    a.pg_shift = -1;
+  } else {
+    int l = 0;
+    while ((1ll << l) < page_size) ++l;
+    const int p = 31 + l;
+    a.pg_mul = (uint32_t)((((uint64_t)1 << p) + (uint64_t)page_size - 1) / (uint64_t)page_size);
+    a.pg_shift = p - 32;
+  }
   a.table = table;
   a.table_len = table_len;
   a.table_cols = table_cols;

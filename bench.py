@@ -46,7 +46,7 @@ EPS = 1e-6
 THETA = 10000.0
 L2_BYTES = 129 * 1024 * 1024
 
-# algorithmic bytes per unit (measurement)
+# algorithmic bytes per unit: what each kernel must move at minimum (HBM-bound kernels)
 POOL_BYTES_PER_BLOCK = 1024 + 256 + 256
 SCORE_BYTES_PER_BLOCK = 256 + 4
 SELECT_BYTES_PER_BLOCK = 4          # + 1 byte per mask token written

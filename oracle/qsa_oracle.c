@@ -30,7 +30,7 @@
  *           projection of the normed hidden states (hidden -> 640) in slabs of
  *           2048 rows.
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *  R1  bf16 <-> f32: widening is exact; narrowing is round-to-nearest-even,
  *      NaN stays NaN.
  *  R2  RoPE table: inv_freq[j] = f32(1 / theta^(2j/64)), angle = f32(p * inv_freq[j])

@@ -10,22 +10,25 @@
 // selected set comes as the token lists qsa_mask_tokens writes.
 //
 // Per (row, KV head, chunk of 8 query heads) one CTA of 4 warps, the grid
-// ordered KV head first.  The CTA walks the row's tokens in 16-token tiles:
-// warp 0's lanes bring each token's K and V rows (one 16-byte aligned run of
-// head_dim bf16 per token and KV head) with the bulk-copy engine into a
-// three-stage ring shared by the CTA (row stride head_dim * 2 + 16 bytes, so
-// the fragment loads below hit 32 distinct banks); the four warps split the
-// head dims, each computing its part of the logits and of the output.  The
-// partial logits meet once per tile in shared memory and every warp sums them
-// in the same order, so every warp holds the same softmax state and no final
-// combine is needed.  About 55 KiB of shared memory per CTA: four CTAs (16
-// warps) per SM.
+// ordered KV head first.  The CTA walks the row's tokens in 32-token tiles:
+// each warp's lanes bring 8 tokens' K and V rows (one 16-byte aligned run of
+// head_dim bf16 per token and KV head) with the bulk-copy engine into a ring
+// shared by the CTA (two stages at head_dim 256, three at 128; row stride
+// head_dim * 2 + 16 bytes, so the fragment loads below hit 32 distinct
+// banks); the four warps split the head dims, each computing its part of the
+// logits and of the output.  The partial logits meet once per tile in shared
+// memory and every warp sums them in the same order, so every warp holds the
+// same softmax state and no final combine is needed.  About 74 KiB of shared
+// memory per CTA at head_dim 256: three CTAs (12 warps) per SM.  (16-token
+// tiles in a three-stage ring, four CTAs per SM, took 4 % longer: the
+// barrier, the exchange and the softmax bookkeeping come once per tile.)
 //
 // The contraction per (row, KV head) has only 8 query heads, so it runs on
 // warp-level mma.sync m16n8k16 (bf16 in, f32 accumulate):
 //   S = Q K^T   M = query heads (8, padded to 16 with zero rows), N = 8 tokens
-//               (two tiles per 16 tokens), K = head dims;
-//   O^T += V^T P^T   M = head dims, N = the 8 query heads, K = 16 tokens,
+//               (four tiles per 32 tokens), K = head dims;
+//   O^T += V^T P^T   M = head dims, N = the 8 query heads, K = 16 tokens (two
+//               steps per tile),
 // where P^T's operand registers are exactly S's accumulator registers (the
 // accumulator of S holds, per lane, head lane/4 at tokens 2(lane%4), +1, which
 // is the B operand layout of the second product), so no shuffle moves P.
@@ -45,27 +48,28 @@ namespace qsa {
 namespace {
 
 constexpr int kAttnWarps = 4;
-constexpr int kAttnStages = 3;
-constexpr int kAttnTile = 16;  // tokens per tile
+constexpr int kAttnStagesMax = 3;
+constexpr int kAttnTile = 32;  // tokens per tile (each warp brings 8)
 constexpr long long kAttnSpinLimit = 4000000000LL;
 
 // Control block at the start of shared memory (one per CTA).
 struct AttnCtrl {
-  uint64_t full[kAttnStages];               // a tile's K and V rows have landed
-  uint32_t vmask[kAttnStages][kAttnWarps];  // which of each warp's 4 tokens are in the list
+  uint64_t full[kAttnStagesMax];               // a tile's K and V rows have landed
+  uint32_t vmask[kAttnStagesMax][kAttnWarps];  // which of each warp's 8 tokens are in the list
   int32_t abort;
-  alignas(16) float xbuf[2][kAttnWarps * 32 * 4];  // partial logits, double-buffered by tile
+  alignas(16) float xbuf[2][kAttnWarps * 32 * 8];  // partial logits, double-buffered by tile
 };
 
 template <int HD>
 struct AttnGeom {
+  static constexpr int kStages = HD >= 256 ? 2 : 3;           // three CTAs per SM at HD 256
   static constexpr int kRowBytes = HD * 2;                     // one token's K (or V) row
   static constexpr int kStride = kRowBytes + 16;               // in shared memory
   static constexpr int kStageBytes = 2 * kAttnTile * kStride;  // K rows then V rows
   static constexpr int kJ = HD / 128;  // 16-byte K chunks per lane per warp (S, its head dims)
   static constexpr int kMT = HD / 64;  // m-tiles of O^T per warp (its head dims)
   static constexpr size_t kRingOff = (sizeof(AttnCtrl) + 127) & ~size_t(127);
-  static constexpr size_t kSmem = kRingOff + (size_t)kAttnStages * kStageBytes;
+  static constexpr size_t kSmem = kRingOff + (size_t)kStages * kStageBytes;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -150,7 +154,7 @@ struct AttnArgs {
 };
 
 template <int HD>
-__global__ void __launch_bounds__(32 * kAttnWarps, 4)
+__global__ void __launch_bounds__(32 * kAttnWarps, 3)
 sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
   using Geo = AttnGeom<HD>;
   extern __shared__ __align__(128) uint8_t attn_smem[];
@@ -189,7 +193,7 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
     }
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kAttnStages; ++s)  // one expect_tx arrival per warp
+    for (int s = 0; s < Geo::kStages; ++s)  // one expect_tx arrival per warp
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&C.full[s])),
                    "r"(kAttnWarps)
                    : "memory");
@@ -198,12 +202,12 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
   }
   __syncthreads();
 
-  // ---- producers: warp w brings tokens 4w .. 4w+3 of each tile, lanes 0..3
-  // their K rows and lanes 4..7 their V rows, into the stage tile i % S.  The
+  // ---- producers: warp w brings tokens 8w .. 8w+7 of each tile, lanes 0..7
+  // their K rows and lanes 8..15 their V rows, into the stage tile i % S.  The
   // two lookups before a tile's copies (its token, then that token's page
   // entry) run ahead in queues: tokens 2L tiles ahead, pages L tiles ahead.
   const int n_tiles = (n + kAttnTile - 1) / kAttnTile;
-  const int tok_in_tile = 4 * warp + (lane & 3);  // lanes 0..7 (the rest mirror them)
+  const int tok_in_tile = 8 * warp + (lane & 7);  // lanes 0..15 (the rest mirror them)
   constexpr int32_t kNoToken = INT32_MIN;
   auto page_of = [&](int32_t t) -> int32_t {  // t >= 0
     return a.pg_shift < 0 ? t : (int32_t)(__umulhi((uint32_t)t, a.pg_mul) >> a.pg_shift);
@@ -218,13 +222,13 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
     return (t >= 0 && pg < a.table_len) ? trow[pg] : -1;
   };
   auto start = [&](int i, int32_t t, int32_t phys) {  // this warp's part of tile i
-    const int s = i % kAttnStages;
-    const bool ok = lane < 8 && t != kNoToken && phys >= 0 && phys < a.pool_pages;
-    if (lane < 4 && t != kNoToken && !ok) report_error(a.status, kErrTokenRange, row);
+    const int s = i % Geo::kStages;
+    const bool ok = lane < 16 && t != kNoToken && phys >= 0 && phys < a.pool_pages;
+    if (lane < 8 && t != kNoToken && !ok) report_error(a.status, kErrTokenRange, row);
     const uint32_t bal = __ballot_sync(0xffffffffu, ok);
     const uint32_t mb = smem_u32(&C.full[s]);
     if (lane == 0) {
-      C.vmask[s][warp] = (bal & 0xFu) << (4 * warp);
+      C.vmask[s][warp] = (bal & 0xFFu) << (8 * warp);
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb),
                    "r"((uint32_t)__popc(bal) * (uint32_t)Geo::kRowBytes)
                    : "memory");
@@ -233,9 +237,9 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
     if (ok) {
       const int32_t pg = page_of(t);
       const int64_t src_row = ((int64_t)phys * a.page_size + (t - pg * a.page_size)) * a.nkv + kvh;
-      const uint16_t *src = (lane < 4 ? a.k_pool : a.v_pool) + src_row * HD;
+      const uint16_t *src = (lane < 8 ? a.k_pool : a.v_pool) + src_row * HD;
       const uint8_t *dst = ring + (size_t)s * Geo::kStageBytes +
-                           (lane < 4 ? 0 : kAttnTile * Geo::kStride) + tok_in_tile * Geo::kStride;
+                           (lane < 8 ? 0 : kAttnTile * Geo::kStride) + tok_in_tile * Geo::kStride;
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
               "r"(smem_u32(dst)), "l"(src), "r"((uint32_t)Geo::kRowBytes), "r"(mb)
@@ -246,21 +250,21 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
   int issued = 0;
   int32_t tokq[kLook2], pageq[kLook];
   {
-    int32_t tok_pre[kAttnStages + kLook2], page_pre[kAttnStages + kLook];
+    int32_t tok_pre[Geo::kStages + kLook2], page_pre[Geo::kStages + kLook];
 #pragma unroll
-    for (int k = 0; k < kAttnStages + kLook2; ++k) tok_pre[k] = fetch_tok(k);
+    for (int k = 0; k < Geo::kStages + kLook2; ++k) tok_pre[k] = fetch_tok(k);
 #pragma unroll
-    for (int k = 0; k < kAttnStages + kLook; ++k) page_pre[k] = fetch_page(tok_pre[k]);
+    for (int k = 0; k < Geo::kStages + kLook; ++k) page_pre[k] = fetch_page(tok_pre[k]);
 #pragma unroll
-    for (int k = 0; k < kAttnStages; ++k)
+    for (int k = 0; k < Geo::kStages; ++k)
       if (k < n_tiles) {
         start(k, tok_pre[k], page_pre[k]);
         ++issued;
       }
 #pragma unroll
-    for (int k = 0; k < kLook2; ++k) tokq[k] = tok_pre[kAttnStages + k];  // tiles S .. S + 2L - 1
+    for (int k = 0; k < kLook2; ++k) tokq[k] = tok_pre[Geo::kStages + k];  // tiles S .. S + 2L - 1
 #pragma unroll
-    for (int k = 0; k < kLook; ++k) pageq[k] = page_pre[kAttnStages + k];  // tiles S .. S + L - 1
+    for (int k = 0; k < kLook; ++k) pageq[k] = page_pre[Geo::kStages + k];  // tiles S .. S + L - 1
   }
 
   float m_run = -INFINITY;  // running max of head g's logits (log2 units), same in every warp
@@ -269,12 +273,12 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
 #pragma unroll
   for (int t = 0; t < Geo::kMT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
   for (int i = 0; i < n_tiles; ++i) {
-    const int s = i % kAttnStages;
+    const int s = i % Geo::kStages;
     // every warp runs every iteration and every barrier; after an abort the
     // waits return at once and the results are discarded
     // (every lane waits: each acquires the bulk copies' writes for itself)
     const bool okw = __all_sync(
-        0xffffffffu, attn_wait(smem_u32(&C.full[s]), (uint32_t)(i / kAttnStages) & 1u, abort_flag));
+        0xffffffffu, attn_wait(smem_u32(&C.full[s]), (uint32_t)(i / Geo::kStages) & 1u, abort_flag));
     const uint8_t *kt = ring + (size_t)s * Geo::kStageBytes;
     const uint8_t *vt = kt + kAttnTile * Geo::kStride;
     uint32_t vb = 0;
@@ -283,22 +287,25 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
       for (int w = 0; w < kAttnWarps; ++w) vb |= C.vmask[s][w];
     }
 
-    // ---- this warp's part of S = Q K^T: its head dims, both 8-token halves
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // ---- this warp's part of S = Q K^T: its head dims, four 8-token n-tiles
+    float sc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
     for (int jj = 0; jj < Geo::kJ; ++jj) {
       const int c = k_chunk(q, warp * Geo::kJ + jj);
-      const uint4 k0 = *reinterpret_cast<const uint4 *>(kt + g * Geo::kStride + 16 * c);
-      const uint4 k1 = *reinterpret_cast<const uint4 *>(kt + (g + 8) * Geo::kStride + 16 * c);
-      mma_bf16(sc[0], qa[2 * jj][0], 0u, qa[2 * jj][1], 0u, k0.x, k0.y);
-      mma_bf16(sc[1], qa[2 * jj][0], 0u, qa[2 * jj][1], 0u, k1.x, k1.y);
-      mma_bf16(sc[0], qa[2 * jj + 1][0], 0u, qa[2 * jj + 1][1], 0u, k0.z, k0.w);
-      mma_bf16(sc[1], qa[2 * jj + 1][0], 0u, qa[2 * jj + 1][1], 0u, k1.z, k1.w);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const uint4 kv = *reinterpret_cast<const uint4 *>(kt + (g + 8 * nt) * Geo::kStride + 16 * c);
+        mma_bf16(sc[nt], qa[2 * jj][0], 0u, qa[2 * jj][1], 0u, kv.x, kv.y);
+        mma_bf16(sc[nt], qa[2 * jj + 1][0], 0u, qa[2 * jj + 1][1], 0u, kv.z, kv.w);
+      }
     }
-    // partial logits of head g at tile tokens 2q, 2q+1, 2q+8, 2q+9, summed over
-    // the warps in a fixed order so every warp holds the same values
+    // partial logits of head g at tile tokens 2q + 8nt, +1 (nt = 0..3), summed
+    // over the warps in a fixed order so every warp holds the same values
     float4 *xb = reinterpret_cast<float4 *>(C.xbuf[i & 1]);
-    xb[warp * 32 + lane] = make_float4(sc[0][0], sc[0][1], sc[1][0], sc[1][1]);
+    xb[2 * (warp * 32 + lane)] = make_float4(sc[0][0], sc[0][1], sc[1][0], sc[1][1]);
+    xb[2 * (warp * 32 + lane) + 1] = make_float4(sc[2][0], sc[2][1], sc[3][0], sc[3][1]);
     __syncthreads();
     // every warp is past tile i - 1: its stage takes tile i - 1 + S
     const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;  // one verdict per warp
@@ -313,18 +320,23 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
       for (int k = 0; k + 1 < kLook2; ++k) tokq[k] = tokq[k + 1];
       tokq[kLook2 - 1] = fetch_tok(issued + kLook2 - 1);
     }
-    float sv[4] = {0.f, 0.f, 0.f, 0.f};
+    float sv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) {
-      const float4 p = xb[w * 32 + lane];
-      sv[0] += p.x;
-      sv[1] += p.y;
-      sv[2] += p.z;
-      sv[3] += p.w;
+      const float4 p0 = xb[2 * (w * 32 + lane)];
+      const float4 p1 = xb[2 * (w * 32 + lane) + 1];
+      sv[0] += p0.x;
+      sv[1] += p0.y;
+      sv[2] += p0.z;
+      sv[3] += p0.w;
+      sv[4] += p1.x;
+      sv[5] += p1.y;
+      sv[6] += p1.z;
+      sv[7] += p1.w;
     }
     float tmax = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 8; ++e) {
       const int tk = 2 * q + (e & 1) + 8 * (e >> 1);
       sv[e] = ((vb >> tk) & 1u) ? sv[e] * a.scale_log2 : -INFINITY;
       tmax = fmaxf(tmax, sv[e]);
@@ -335,10 +347,12 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
     const float m_use = m_new == -INFINITY ? 0.f : m_new;
     const float alpha = exp2f(m_run - m_use);  // 0 while nothing was seen
     m_run = m_new;
-    const uint32_t pb0 = pack_bf16x2(exp2f(sv[0] - m_use), exp2f(sv[1] - m_use));
-    const uint32_t pb1 = pack_bf16x2(exp2f(sv[2] - m_use), exp2f(sv[3] - m_use));
+    uint32_t pb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) pb[k] = pack_bf16x2(exp2f(sv[2 * k] - m_use), exp2f(sv[2 * k + 1] - m_use));
     // the weights the product uses are the rounded ones: so is their sum
-    l_run = l_run * alpha + ((bf16_lo(pb0) + bf16_hi(pb0)) + (bf16_lo(pb1) + bf16_hi(pb1)));
+    l_run = l_run * alpha + (((bf16_lo(pb[0]) + bf16_hi(pb[0])) + (bf16_lo(pb[1]) + bf16_hi(pb[1]))) +
+                             ((bf16_lo(pb[2]) + bf16_hi(pb[2])) + (bf16_lo(pb[3]) + bf16_hi(pb[3]))));
     if (__any_sync(0xffffffffu, alpha != 1.f)) {  // some head's maximum moved
       // O^T's columns are heads 2q, 2q+1, whose factors lanes 8q and 8q+4 hold
       const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * q);
@@ -356,13 +370,15 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
     // g+8 of m-tile T are dims 8(g + 8c) + 2e, +1 with c = T / 4, e = T % 4
     // (in a partial tile a token outside the list contributes zeros: its stage
     // row may hold anything)
-    auto pv = [&](const uint32_t z0, const uint32_t z1, const uint32_t z2, const uint32_t z3) {
+    auto pv = [&](const int ks, const uint32_t z0, const uint32_t z1, const uint32_t z2,
+                  const uint32_t z3) {  // k-step ks: tile tokens 16 ks .. 16 ks + 15
       const int c = (warp * Geo::kMT) / 4;
       const int off = 16 * (g + 8 * c);
-      const uint4 v0 = *reinterpret_cast<const uint4 *>(vt + (2 * q) * Geo::kStride + off);
-      const uint4 v1 = *reinterpret_cast<const uint4 *>(vt + (2 * q + 1) * Geo::kStride + off);
-      const uint4 v2 = *reinterpret_cast<const uint4 *>(vt + (2 * q + 8) * Geo::kStride + off);
-      const uint4 v3 = *reinterpret_cast<const uint4 *>(vt + (2 * q + 9) * Geo::kStride + off);
+      const uint8_t *vk = vt + (16 * ks) * Geo::kStride;
+      const uint4 v0 = *reinterpret_cast<const uint4 *>(vk + (2 * q) * Geo::kStride + off);
+      const uint4 v1 = *reinterpret_cast<const uint4 *>(vk + (2 * q + 1) * Geo::kStride + off);
+      const uint4 v2 = *reinterpret_cast<const uint4 *>(vk + (2 * q + 8) * Geo::kStride + off);
+      const uint4 v3 = *reinterpret_cast<const uint4 *>(vk + (2 * q + 9) * Geo::kStride + off);
       // words e = (warp * kMT) % 4 + t of the chunk: dims 8(g + 8c) + 2e, +1
       uint32_t w0[Geo::kMT], w1[Geo::kMT], w2[Geo::kMT], w3[Geo::kMT];
       if constexpr (Geo::kMT == 4) {
@@ -381,14 +397,19 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
       for (int t = 0; t < Geo::kMT; ++t) {
         const uint32_t x0 = w0[t] & z0, x1 = w1[t] & z1, x2 = w2[t] & z2, x3 = w3[t] & z3;
         mma_bf16(acc[t], prmt(x0, x1, 0x5410u), prmt(x0, x1, 0x7632u), prmt(x2, x3, 0x5410u),
-                 prmt(x2, x3, 0x7632u), pb0, pb1);
+                 prmt(x2, x3, 0x7632u), pb[2 * ks], pb[2 * ks + 1]);
       }
     };
-    if (vb == 0xFFFFu) {  // a whole tile (uniform over the CTA): constant masks fold away
-      pv(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+    if (vb == 0xFFFFFFFFu) {  // a whole tile (uniform over the CTA): constant masks fold away
+      pv(0, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+      pv(1, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
     } else {
-      pv((vb >> (2 * q)) & 1u ? 0xFFFFFFFFu : 0u, (vb >> (2 * q + 1)) & 1u ? 0xFFFFFFFFu : 0u,
-         (vb >> (2 * q + 8)) & 1u ? 0xFFFFFFFFu : 0u, (vb >> (2 * q + 9)) & 1u ? 0xFFFFFFFFu : 0u);
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t vk = vb >> (16 * ks);
+        pv(ks, (vk >> (2 * q)) & 1u ? 0xFFFFFFFFu : 0u, (vk >> (2 * q + 1)) & 1u ? 0xFFFFFFFFu : 0u,
+           (vk >> (2 * q + 8)) & 1u ? 0xFFFFFFFFu : 0u, (vk >> (2 * q + 9)) & 1u ? 0xFFFFFFFFu : 0u);
+      }
     }
   }
 
@@ -426,8 +447,8 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
   // the copies issued land before the CTA's shared memory is released (in a
   // run that completed, every tile was waited for already)
   if (lane == 0) {
-    for (int k = max(0, issued - kAttnStages); k < issued; ++k)
-      attn_wait(smem_u32(&C.full[k % kAttnStages]), (uint32_t)(k / kAttnStages) & 1u, nullptr);
+    for (int k = max(0, issued - Geo::kStages); k < issued; ++k)
+      attn_wait(smem_u32(&C.full[k % Geo::kStages]), (uint32_t)(k / Geo::kStages) & 1u, nullptr);
   }
 }
 

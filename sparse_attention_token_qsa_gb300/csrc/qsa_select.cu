@@ -75,6 +75,7 @@ struct SelectSmem {
   int32_t band_bin[2];  // sampled band: its top and bottom bins
   int32_t rsel[kRounds];     // each candidate round's bin ...
   uint32_t rabove[kRounds];  // ... and the keys above it
+  uint32_t kmin, kmax;       // the candidates under the prefix: their key range
   // cand keys [kCandCap] u32, cand local indices [kCandCap] u16, keys[] follow (dynamic)
 };
 
@@ -689,6 +690,35 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         prefix = (prefix << (shift - sh)) | B;
         shift = sh;
         done = cB == need;
+        if (!done && r < kRounds - 1 && cB > 64u) {
+          // many keys left under the prefix: if they all hold one key (exact
+          // ties, as quantised scores give) the remaining key rounds are moot
+          // and the index rounds below cut the ties
+          if (tid == 0) {
+            S.kmin = 0xFFFFFFFFu;
+            S.kmax = 0u;
+          }
+          __syncthreads();
+          uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+          each([&](bool v, uint32_t key, uint32_t) {
+            if (v && (key >> shift) == prefix) {
+              lo = min(lo, key);
+              hi = max(hi, key);
+            }
+          });
+          lo = __reduce_min_sync(0xffffffffu, lo);
+          hi = __reduce_max_sync(0xffffffffu, hi);
+          if (lane == 0) {
+            atomicMin(&S.kmin, lo);
+            atomicMax(&S.kmax, hi);
+          }
+          __syncthreads();
+          if (S.kmin == S.kmax) {
+            prefix = S.kmin;
+            shift = 0;
+            break;
+          }
+        }
       }
       if (done) {
         if (tid == 0) {

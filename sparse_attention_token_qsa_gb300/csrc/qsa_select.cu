@@ -726,6 +726,41 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
           S.rule_shift = (uint32_t)shift;
           S.rule_cut = INT32_MAX;
         }
+      } else if (C == 1 && n <= 65536) {
+        // ties at the full key, on one CTA: of the keys equal to `prefix`,
+        // the `need` with the lowest block indices are kept.  Their indices
+        // are marked in a bitmap (round 0's histogram is no longer read) and
+        // a scan of its words' bit counts finds the need-th lowest.
+        constexpr int kWords = 65536 / 32, kPer = kWords / NT;
+        uint32_t *bm = S.hist0;
+        for (int i = tid; i < kWords; i += NT) bm[i] = 0u;
+        __syncthreads();
+        each([&](bool v, uint32_t key, uint32_t gi) {
+          if (v && key == prefix) atomicOr(&bm[gi >> 5], 1u << (gi & 31u));
+        });
+        __syncthreads();
+        uint32_t c = 0;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) c += (uint32_t)__popc(bm[tid * kPer + k]);
+        uint32_t total;
+        const uint32_t before = block_excl_scan<NT>(c, S.warp_tot, total);
+        if (before < need && need <= before + c) {
+          uint32_t acc = before;
+          for (int k = 0; k < kPer; ++k) {
+            uint32_t w = bm[tid * kPer + k];
+            const uint32_t cw = (uint32_t)__popc(w);
+            if (acc + cw >= need) {
+              for (uint32_t r = need - acc; r > 1u; --r) w &= w - 1u;  // drop the lower set bits
+              S.rule_cut = (int32_t)(32 * (tid * kPer + k) + __ffs((int)w) - 1);
+              break;
+            }
+            acc += cw;
+          }
+        }
+        if (tid == 0) {
+          S.rule_prefix = prefix;
+          S.rule_shift = 0;
+        }
       } else {
         // ties at the full key: of the keys equal to `prefix`, the `need`
         // with the lowest block indices are kept.  Radix rounds over the

@@ -17,15 +17,17 @@
 //    of the row's blocks and keeps its keys in shared memory, so HBM sees
 //    each score once;
 //  * the first round histograms the top 12 bits of every key as it is loaded
-//    (exact zeros, the heavy bin of relu scores, counted in registers and
-//    added once per warp); the histograms merge over the cluster through
-//    distributed shared memory; a non-finite score shows up as a count in one
-//    of the 16 outer bins, so no per-key check is needed;
-//  * one pass over the cached keys then writes the final mask bytes of every
-//    key outside the selected bin and compacts the bin's keys (with their
-//    block indices) into a candidate list, which rank 0 gathers; rounds of
-//    8, 8 and 4 bits run on the candidates only, and exact ties at the final
-//    key are cut by radix rounds on the block index (lowest indices kept);
+//    (exact zeros, the heavy bin of relu scores, go to one spare bin per lane
+//    and are folded in afterwards); the histograms merge over the cluster
+//    through distributed shared memory; a non-finite score shows up as a
+//    count in one of the 16 outer bins, so no per-key check is needed;
+//  * one pass over the keys then writes the final mask bytes of every key
+//    outside the selected bin and marks the quads that hold the bin's keys; a
+//    second, short walk over the marked quads lists those keys (with their
+//    block indices) as candidates, which rank 0 gathers; rounds of 8, 8 and
+//    4 bits run on the candidates only (stopping once the keys left are all
+//    one key), and exact ties at the final key are cut on the block index
+//    (lowest indices kept) by radix rounds, or on one CTA by a bitmap;
 //  * every CTA then patches the mask bytes of its own candidates.  A bin too
 //    large for the candidate list falls back to rounds over every key, with
 //    ties ranked by a block scan in the mask pass.

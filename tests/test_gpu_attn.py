@@ -221,3 +221,22 @@ def test_attn_prefill_chunk_64k_sampled_rows(qsa, orc):
     assert st == (0, 0)
     check_rows(orc, got, q_np, nq, nkv, hd, k_np, v_np, page_size, table, sel_np, n_sel, sel_cols,
                scale, rows=[0, 1, 2, 3, 1000, 2047, 4094, 4095])
+
+
+@pytest.mark.parametrize("page_size", [1, 5, 12, 1000])
+def test_attn_page_sizes(qsa, orc, page_size):
+    """Page sizes of one token, odd and not a power of two, and larger than a
+    row's whole list: the token -> page division (a multiply-high and a shift
+    for every size but one) finds each token's slot."""
+    rng = qi.rng_for(6, salt=300 + page_size)
+    nq, nkv, hd = 8, 2, 128
+    counts = [1, 33, 64, 97]
+    table_len = max(4, (3000 + page_size - 1) // page_size)
+    q_np, k_np, v_np, tables, sel_np, n_sel = make_case(rng, len(counts), nq, nkv, hd, page_size,
+                                                        table_len, counts, extra_pages=3)
+    scale = 1.0 / np.sqrt(hd)
+    got, st = run_attn(qsa, q_np, nq, nkv, hd, k_np, v_np, page_size, tables, sel_np, n_sel,
+                       sel_np.shape[1], scale)
+    assert st == (0, 0)
+    check_rows(orc, got, q_np, nq, nkv, hd, k_np, v_np, page_size, tables, sel_np, n_sel,
+               sel_np.shape[1], scale)

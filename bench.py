@@ -444,7 +444,12 @@ def run_ours(args, rank, world, device):
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_gbs,
                 "unit": "GB/s", "frac": achieved / hbm_gbs, "traffic": traffic,
                 "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes": d["bytes"],
-                "avg_launch_us": d["us"]}
+                "avg_launch_us": d["us"],
+                "note": "batch-1 decode is latency-bound: one 64k row moves "
+                        f"{d['bytes'] / 1e6:.2f} MB, {d['bytes'] / (hbm_gbs * 1e3):.2f} us at "
+                        "the measured peak, against a launch, a grid barrier and a few "
+                        "dependent L2 round trips; the bandwidth-bound kernels' fractions "
+                        "are in secondary (score, select, pool, gather)"}
     kernels = {n: {"avg_launch_us": round(v["us"], 3), "algorithmic_bytes": v["bytes"],
                    "achieved_gbs": round(v["bytes"] / (v["us"] * 1e-6) / 1e9, 1),
                    "frac_of_measured_hbm": round(v["bytes"] / (v["us"] * 1e-6) / 1e9 / hbm_gbs, 4)}

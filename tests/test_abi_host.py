@@ -201,7 +201,7 @@ def test_sparse_attn_refusals(lib):
                                    a["tcols"], P(a["sel"]), a["scols"], P(a["n_sel"]), a["n"],
                                    a["max_sel"], a["scale"], P(a["out"]), a["os"], P(a["st"]), None)
     assert call(n=0) == 0                             # nothing to do
-    for kw in (dict(nq=15), dict(nkv=0), dict(hd=64), dict(psz=0), dict(max_sel=2052),
+    for kw in (dict(nq=15), dict(nkv=0), dict(hd=64), dict(psz=0), dict(psz=-3), dict(max_sel=2052),
                dict(tcols=63), dict(qs=4095), dict(qs=4100), dict(os=4000), dict(q=U),
                dict(out=U), dict(k=0), dict(sel=0), dict(table=0), dict(n_sel=0),
                dict(scale=float("nan")), dict(scale=float("inf")), dict(n=-1)):

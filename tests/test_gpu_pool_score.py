@@ -311,3 +311,63 @@ def test_score_tc_rows_past_one_slab(qsa, orc, tables):
     sample = np.array([0, 1, 65470, 65535, 65536, 65537, 65560, rows - 1])
     want, _ = oracle_scores(orc, q[sample], 640, pos[sample], tokens, qw, c, s, keys, cols)
     assert_close(got[sample], want, "scores on both sides of the slab edge")
+
+
+def test_pool_rounds_the_mean_to_bf16_like_the_oracle(qsa, orc, tables):
+    """The closed-form case where the bf16 cast of the f32 mean decides the key
+    bits (a tie after the gain): the GPU must give the oracle's bits, at block 0
+    (no rotation) and at later blocks (rotated at 4b)."""
+    import test_oracle_pins as pins
+
+    k, w = pins.mean_cast_case()
+    nb = 9
+    keys = np.tile(k, (nb, 1))
+    c, s, cd, sd = tables
+    out = torch.full((nb, 128), 0x7FAB, dtype=torch.int16, device="cuda")
+    qsa.qsa_pool_blocks(dev(keys).view(-1), 128, 0, nb, dev(w), cd, sd, c.shape[0], 0.0, out)
+    got = host16(out)
+    want = orc.pool_blocks(keys, 128, 0, nb, w, c, s, 0.0)
+    small = qi.to_bf16_bits(np.array([2.0**-13 * 1.515625], np.float32))[0]
+    assert np.all(got[0, :126] == small)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_score_one_hot_queries_rotate_at_their_positions(qsa, orc, tables, path):
+    """One-hot query heads on dim i against one-hot keys e_i and e_{i+32}: the
+    two scores are the rotated query's cos and sin components, so they pin the
+    query's RoPE position on both scorers (oracle closed form in the pins)."""
+    c, s, cd, sd = tables
+    T = 4096
+    cases = [(p, i) for p in (9, 14, 37, 101, 250, 399, 2050, 4095) for i in (0, 1, 7, 31)]
+    n = len(cases)
+    # 64 rows or more keep the tensor-core path on its own shape; pad with copies
+    reps = -(-64 // n)
+    cases = (cases * reps)[:max(64, n)]
+    n = len(cases)
+    fq = np.zeros((n, 640), np.float32)
+    for r, (p, i) in enumerate(cases):
+        fq[r, [i, 128 + i, 256 + i, 384 + i]] = 1.0
+    fqb = qi.to_bf16_bits(fq)
+    pos = np.array([p for p, _ in cases], np.int32)
+    zero_w = np.zeros(128, np.uint16)
+    cols = T // 4
+    for i in sorted({i for _, i in cases}):
+        keys = np.zeros((T // 4, 128), np.float32)
+        keys[0, i], keys[1, i + 32] = 1.0, 1.0
+        keys = qi.to_bf16_bits(keys)
+        rows = np.array([r for r, (_, ii) in enumerate(cases) if ii == i])
+        vis = np.full(n, 8, np.int32)
+        sc = torch.full((n, cols), -7.0, dtype=torch.float32, device="cuda")
+        st = qsa.new_status()
+        qsa.qsa_score_rows_with(dev(fqb), 640, dev(pos), dev(vis), n, T, dev(zero_w), cd, sd,
+                                c.shape[0], 0.0, dev(keys), None, sc, cols, st, path=path,
+                                workspace=qsa.new_workspace(n))
+        assert qsa.qsa_read_status(st) == (0, 0)
+        got = sc.cpu().numpy()[rows]
+        want = np.full((len(rows), cols), -7.0, np.float32)
+        rc, _ = orc.score_rows(fqb[rows], 640, pos[rows], len(rows), T, zero_w, c, s, 0.0, keys,
+                               want, cols, visible_len=vis[rows])
+        assert rc == 0
+        assert_close(got, want, f"one-hot query scores, dim {i}", atol=0, rtol=1e-6)
+        assert np.all(got[:, 2:] == -7.0)

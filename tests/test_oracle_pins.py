@@ -190,6 +190,63 @@ def test_pool_stride_and_offset_indexing(orc):
     assert np.all(part[:17] == 0) and np.all(part[26:] == 0)
 
 
+def mean_cast_case():
+    """Raw keys of one block whose f32 mean must be rounded to bf16 to give the
+    expected block key (see test_pool_mean_is_cast_to_bf16_before_the_norm)."""
+    k = np.zeros((4, 128), np.float32)
+    k[0, :126] = 2.0**-8
+    k[1, :126] = 3 * 2.0**-17
+    k[:, 126:] = 64.0
+    w = np.zeros(128, np.float32)
+    w[:] = 0.5
+    return qi.to_bf16_bits(k), qi.to_bf16_bits(w)
+
+
+def test_pool_mean_is_cast_to_bf16_before_the_norm(orc):
+    """PR #1160 description: the four raw keys are averaged in float32 and the
+    mean is cast back to bf16 before the norm.  These inputs make that cast
+    decide the output bits.
+      dims 0..125: tokens 2^-8, 3*2^-17, 0, 0.  The f32 mean is 2^-10 (1 + 3*2^-9),
+                   which bf16 rounds up to 2^-10 (1 + 2^-7).
+      dims 126, 127: four tokens of 64, so the mean is 64.
+    With eps = 0 the mean square is 2*64^2/128 = 64 plus the small dims' share
+    (below 2^-20, under half an f32 ulp of 64), so r = 1/sqrt(64) = 1/8 exactly.
+    w = 0.5 gives a gain of 1.5, and block 0 sits at position 0 (no rotation).
+      small dims: 2^-13 (1 + 2^-7) * 1.5 = 2^-13 * 1.51171875, halfway between the
+                  bf16 values 2^-13 * 1.5078125 and 2^-13 * 1.515625; the tie goes
+                  to the even one, 1.515625.  (Kept in f32, the mean would give
+                  2^-13 * 1.5087890625, which rounds to 1.5078125.)
+      large dims: 64 / 8 * 1.5 = 12."""
+    k, w = mean_cast_case()
+    c, s = orc.rope_table(4)
+    out = orc.pool_blocks(k, 128, 0, 1, w, c, s, 0.0)
+    small = qi.to_bf16_bits(np.array([2.0**-13 * 1.515625], np.float32))[0]
+    assert widen(small) == np.float32(2.0**-13 * 1.515625)      # a bf16 value
+    assert np.all(out[0, :126] == small), hex(out[0, 0])
+    assert np.all(out[0, 126:] == qi.to_bf16_bits(np.array([12.0], np.float32))[0])
+
+
+def test_pool_depends_on_the_bf16_mean_only(orc):
+    """PR #1160 description (mean in float32, cast back to bf16): a block's key
+    is a function of the bf16 mean of its four tokens.  Replacing the four
+    tokens by four copies of that mean (its exact sum rounded once to f32, then
+    torch's bf16 cast) must give the same key bits, at every block position."""
+    rng = np.random.default_rng(14)
+    nb = 96
+    keys = qi.raw_keys(rng, 4 * nb, token_scale=True)
+    kw = qi.normal_bf16(rng, (128,), 0.1)
+    c, s = orc.rope_table(4 * nb)
+    kf = widen(keys).astype(np.float64).reshape(nb, 4, 128)
+    mean = (kf.sum(axis=1).astype(np.float32) * np.float32(0.25))
+    mean_bf16 = qi.to_bf16_bits(mean)
+    # the f32 means are rarely bf16 values, so this case tests the cast
+    assert np.mean(widen(mean_bf16) != mean) > 0.5
+    replicated = np.repeat(mean_bf16, 4, axis=0)
+    a = orc.pool_blocks(keys, 128, 0, nb, kw, c, s, 1e-6)
+    b = orc.pool_blocks(replicated, 128, 0, nb, kw, c, s, 1e-6)
+    assert np.array_equal(a, b)
+
+
 # --------------------------------------------------------------------------
 # Scoring
 # --------------------------------------------------------------------------
@@ -288,6 +345,45 @@ def test_score_rows_range_errors(orc):
         rc, row = orc.score_rows(fq, 640, np.array(pos, np.int32), 3, T, z, c, s, 1e-6, keys, sc, 4,
                                  visible_len=None if vis is None else np.array(vis, np.int32))
         assert rc == 3 and row == bad
+
+
+def test_query_rotates_at_the_row_position(orc):
+    """PR #1160 description: each query head is normed and then rotated at the
+    row's own position p.  All four heads are one-hot on dim i < 32 (w = 0,
+    eps = 0): the norm gives bf16(sqrt(128)) = 11.3125 on dim i, and RoPE at p
+    moves it to bf16(11.3125 c) on dim i and bf16(11.3125 s) on dim i + 32
+    (c, s: the table's bf16 cos/sin at row p, column i; the product of two
+    8-bit significands is exact in f32).  Block 0's key is e_i, block 1's is
+    e_{i+32}; with the head sum of four equal relus the scores are
+    4 relu(bf16(11.3125 c)) / sqrt(128) and 4 relu(bf16(11.3125 s)) / sqrt(128)."""
+    T = 400
+    c, s = orc.rope_table(T)
+    cf, sf = widen(c).astype(np.float32), widen(s).astype(np.float32)
+    n = np.float32(11.3125)
+    cases = [(p, i) for p in (9, 14, 37, 101, 250, 399) for i in (0, 1, 7, 31)]
+    fq = np.zeros((len(cases), 640), np.float32)
+    for r, (p, i) in enumerate(cases):
+        fq[r, [i, 128 + i, 256 + i, 384 + i]] = 1.0
+    pos = np.array([p for p, _ in cases], np.int32)
+    sc = np.full((len(cases), 4), -7.0, np.float32)
+    for i in sorted({i for _, i in cases}):
+        rows = [r for r, (_, ii) in enumerate(cases) if ii == i]
+        keys = np.zeros((T // 4, 128), np.float32)
+        keys[0, i], keys[1, i + 32] = 1.0, 1.0
+        sub = np.full((len(rows), 4), -7.0, np.float32)
+        rc, _ = orc.score_rows(qi.to_bf16_bits(fq[rows]), 640, pos[rows], len(rows), T,
+                               np.zeros(128, np.uint16), c, s, 0.0, qi.to_bf16_bits(keys), sub, 4,
+                               visible_len=np.full(len(rows), 8, np.int32))
+        assert rc == 0
+        sc[rows] = sub
+    for r, (p, i) in enumerate(cases):
+        rot = qi.to_bf16_bits(np.array([n * cf[p, i], n * sf[p, i]], np.float32))
+        want = 4.0 * np.maximum(widen(rot).astype(np.float64), 0.0) / math.sqrt(128.0)
+        assert np.allclose(sc[r, :2], want.astype(np.float32), rtol=1e-6, atol=0), (p, i)
+        assert np.all(sc[r, 2:] == -7.0)
+    # the cases span both signs of cos and sin, so a missing or wrong rotation shows
+    assert np.any(sc[:, 0] == 0) and np.any(sc[:, 1] == 0)
+    assert np.mean(sc[:, 0] > 0) > 0.3 and np.mean(sc[:, 1] > 0) > 0.3
 
 
 # --------------------------------------------------------------------------
@@ -723,6 +819,11 @@ MUTANTS = {
     "stride_ignored": ("acc += (double)orc_widen(k0[(int64_t)t * key_stride + d]);",
                        "acc += (double)orc_widen(k0[(int64_t)t * ORC_HD + d]);"),
     "cos_sin_swapped": ("float c = orc_widen(crow[i]);", "float c = orc_widen(srow[i]);"),
+    "mean_kept_f32": ("m[d] = orc_round_bf16(mean);", "m[d] = mean;"),
+    "qprep_unrotated": ("orc_norm_rope(x, q_norm_w, pos, cos_t, sin_t, eps, q_out + h * ORC_HD);",
+                        "orc_norm_rope(x, q_norm_w, 0, cos_t, sin_t, eps, q_out + h * ORC_HD);"),
+    "qprep_at_block_start": ("orc_qprep(q + (int64_t)i * q_stride, p, q_norm_w",
+                             "orc_qprep(q + (int64_t)i * q_stride, p - p % ORC_RATIO, q_norm_w"),
 }
 
 # the pins that must catch the mistakes (each mutant must fail at least one)
@@ -731,7 +832,9 @@ PIN_TESTS = [
     test_select_golden_geometry, test_pool_constant_vector_closed_form,
     test_pool_weight_enters_as_one_plus_w, test_pool_eps_and_mean_closed_form,
     test_pool_mean_of_distinct_tokens, test_pool_stride_and_offset_indexing,
+    test_pool_mean_is_cast_to_bf16_before_the_norm, test_pool_depends_on_the_bf16_mean_only,
     test_score_onehot_closed_form, test_score_relu_is_per_head,
+    test_query_rotates_at_the_row_position,
     test_mask_tokens_equals_nonzero, test_mask_tokens_of_a_selection_is_the_pages_list,
     test_gather_equals_fancy_indexing, test_gather_refuses_tokens_past_the_table,
     test_sparse_attn_one_token_is_its_value_row, test_sparse_attn_equal_logits_give_the_mean,

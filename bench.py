@@ -6,8 +6,10 @@ Workload (one bench step = one decode step of one sequence): batch-1 decode at
 pooled block keys cached, the block a token completes pooled on that step, then
 score and select with budget 2048.  To keep every step's inputs out of L2, the
 steps rotate over R independent sequences whose key caches together exceed the
-129 MB L2 (no flush is needed).  Steps are replayed from CUDA graphs, so the
-host does not pace the GPU.
+129 MB L2 (no flush is needed).  Step k decodes position 65280 + (k mod 256) of
+sequence k mod R with R odd, so consecutive steps walk consecutive positions
+and every fourth step completes a block and pools it.  Steps are replayed from
+CUDA graphs, so the host does not pace the GPU.
 
 Printed: one JSON line (rank 0) with rows/s, per-kernel roofline of the
 dominant kernel (CUDA events, live), the oracle's CPU baseline, an end-to-end
@@ -216,16 +218,21 @@ class DecodeWorkload:
         self.status = qsa.new_status(device)
         # zeroed workspace of the fused decode entry (every call leaves it zero)
         self.dws = qsa.new_decode_workspace(1, TOKENS, device)
-        # the cache holds every block completed before the decode window
+        # every block of the sequence is cached before the first step; a step
+        # that completes a block pools it again (the same key, the same work)
         for r in range(n_seq):
-            qsa.qsa_pool_blocks(self.keys[r], 128, 0, FIRST_POS // 4, self.kw, self.cos, self.sin,
+            qsa.qsa_pool_blocks(self.keys[r], 128, 0, N_BLOCKS, self.kw, self.cos, self.sin,
                                 TOKENS, EPS, self.cache[r])
         self.positions = dev_tensor(torch, np.arange(FIRST_POS, TOKENS, dtype=np.int32), device)
         torch.cuda.synchronize(device)
 
     def step_params(self, k: int):
+        """Step k: sequence k mod R at position FIRST_POS + (k mod 256).  R is
+        odd (coprime to 256), so every run of 4 steps holds one step whose
+        token completes a block, and all R * 256 (sequence, position) pairs
+        come round before any repeats."""
         seq = k % self.R
-        j = (k // self.R) % 256
+        j = k % 256
         return seq, j, FIRST_POS + j
 
     def pool(self, k):
@@ -302,9 +309,11 @@ def time_graphs(torch, graphs):
 
 # ------------------------------------------------------------ oracle (CPU)
 
-def oracle_decode_rate(seconds: float, max_rows: int | None = None):
+def oracle_decode_rate(seconds: float, max_rows: int | None = None, min_seconds: float = 0.0):
     """The oracle on the host cores: decode steps at 64k on one sequence,
-    row-parallel over threads (each thread runs whole steps)."""
+    row-parallel over threads (each thread runs whole steps).  Runs until
+    `seconds` have passed, or sooner once `max_rows` rows are done and at least
+    `min_seconds` have passed."""
     import oracle
 
     orc = oracle.Oracle()
@@ -314,16 +323,20 @@ def oracle_decode_rate(seconds: float, max_rows: int | None = None):
     keys = qi.raw_keys(rr, TOKENS, token_scale=True)
     q = np.ascontiguousarray(qi.fused_qk(rr, 256)[:, :512])
     c, s = orc.rope_table(TOKENS, THETA)
-    cache = orc.pool_blocks(keys, 128, 0, FIRST_POS // 4, kw, c, s, EPS, total_blocks=N_BLOCKS)
+    cache = orc.pool_blocks(keys, 128, 0, N_BLOCKS, kw, c, s, EPS)
     cores = max(1, min(os.cpu_count() or 1, 64))
     caches = [cache.copy() for _ in range(cores)]
-    stop = time.time() + seconds
+    t_start = time.time()
+    stop, min_stop = t_start + seconds, t_start + min_seconds
     counts = [0] * cores
 
     def worker(t):
         sc = np.zeros((1, N_BLOCKS), np.float32)
         j = t
-        while time.time() < stop and (max_rows is None or j < max_rows):
+        while True:
+            now = time.time()
+            if now >= stop or (max_rows is not None and j >= max_rows and now >= min_stop):
+                break
             p = FIRST_POS + (j % 256)
             if (p + 1) % 4 == 0:      # pool the block this token completes (own copy)
                 b = (p + 1) // 4 - 1
@@ -361,15 +374,19 @@ def job_rate(torch, ms_local: float, units_local: float, world: int, device):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    # K steps of one decode row each, row-parallel over the host cores, bounded
-    # at 240 s of wall time (the line reports how many rows ran)
-    rate, cores, rows, dt = oracle_decode_rate(seconds=240.0, max_rows=max(args.steps, 1))
+    # at least K decode rows and at least 20 s of work, row-parallel over the
+    # host cores, bounded at 240 s of wall time (the line reports how many rows ran)
+    rate, cores, rows, dt = oracle_decode_rate(seconds=240.0, max_rows=max(args.steps, 1),
+                                               min_seconds=20.0)
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": "rows/s",
-        "n_gpus": args.gpus, "steps": rows, "warmup": args.warmup,
+        "n_gpus": args.gpus, "steps": args.steps, "rows_run": rows, "warmup": args.warmup,
         "ms_per_step": 1000.0 * dt / max(rows, 1) * cores, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (oracle)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "tokens": TOKENS, "budget": BUDGET, "rows_per_step": 1,
+                   "step_schedule": "row j: position 65280 + j mod 256; a row whose token "
+                                    "completes a block pools it",
+                   "pool_steps_timed": sum(1 for j in range(rows) if (FIRST_POS + j % 256 + 1) % 4 == 0),
                    "parallelism": "host threads"},
         "cpu_baseline": {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
                          "sample": f"{rows} decode rows in {dt:.1f} s on {cores} threads"},
@@ -385,7 +402,7 @@ def run_ours(args, rank, world, device):
 
     hbm_gbs, bf16_tf, bf16_tf_sus, peak_src = load_peaks()
     per_seq_bytes = N_BLOCKS * 256 + TOKENS * 256 + N_BLOCKS * 4 + TOKENS
-    R = max(8, int(np.ceil(1.5 * L2_BYTES / (N_BLOCKS * 256))))
+    R = max(9, int(np.ceil(1.5 * L2_BYTES / (N_BLOCKS * 256)))) | 1   # odd: coprime to 256
     wl = DecodeWorkload(torch, qsa, device, R)
 
     # warm-up (eager): first calls also set kernel attributes outside any capture
@@ -416,6 +433,7 @@ def run_ours(args, rank, world, device):
     clk = clocks.summary(t0, t1)
     ms, value = job_rate(torch, ms, K, world, device)  # K rows on every rank
     ms_per_step = ms / K
+    pool_steps_timed = sum(1 for k in steps if (wl.step_params(k)[2] + 1) % 4 == 0)
     code, row = qsa.qsa_read_status(wl.status)
     assert code == 0, f"device status {code} row {row}"
 
@@ -523,6 +541,7 @@ def run_ours(args, rank, world, device):
 
     secondary = {}
     if not args.no_secondary:
+        secondary["prefill_2304"] = prefill_2304(torch, qsa, device, hbm_gbs, bf16_tf)
         secondary["select_256k"] = select_256k(torch, qsa, device, hbm_gbs)
         secondary["prefill_chunk_64k"] = prefill_chunk(torch, qsa, device, hbm_gbs, bf16_tf)
         secondary["decode_long_32seq"] = decode_long(torch, qsa, device, hbm_gbs)
@@ -540,13 +559,19 @@ def run_ours(args, rank, world, device):
                    "l2": "inputs larger than L2 (steps rotate over the sequences)",
                    "launch": "CUDA graphs of 256 steps; per step qsa_decode_index_select: "
                              "one fused launch (pool the completed block, score, select)",
-                   "three_entry_points_us_per_step": three_us,
+                   "pool_steps_timed": pool_steps_timed,
+                   "step_schedule": "step k: sequence k mod R, position 65280 + k mod 256; "
+                                    "a step whose token completes a block pools it",
                    "parallelism": f"replicas x{world}"},
+        "three_entry_points_us_per_step": three_us,
         "roofline": roofline, "kernels": kernels, "clocks": clk, "e2e": e2e,
         "gpu_launches": int(K),  # one fused launch per step (it pools the new block itself)
         "secondary": secondary,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        for name in ("prefill_2304", "prefill_chunk_64k", "decode_long_32seq", "select_256k"):
+            if name in secondary:
+                secondary[name]["oracle_single_thread"] = oracle_single_thread(name)
         rate, cores, rows, dt = oracle_decode_rate(args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{rows} decode rows (pos 65280.., 64k ctx) in "
@@ -586,6 +611,151 @@ def select_256k(torch, qsa, device, hbm_gbs, ncu=False):
             "achieved_gbs": byts / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": byts / (ms * 1e-3) / 1e9 / hbm_gbs,
             "us_single_row": ms1 * 1000.0, "budget": BUDGET,
             "context": "pages' L20 radix select: 298 us/row at 256k (context only)"}
+
+
+# ------------------------------------------------- oracle beside the GPU lines
+
+def oracle_single_thread(kind: str):
+    """The oracle, single-threaded, on a stated subset of a secondary workload:
+    the same shapes and input distributions, drawn on the host by the seeded
+    generators (the oracle never reads a buffer the GPU path wrote).  Returns
+    {"us_per_row", "sample"}: a baseline printed beside the GPU figures, not a
+    target."""
+    import oracle
+
+    orc = oracle.Oracle()
+    clock = time.perf_counter
+    if kind in ("prefill_2304", "prefill_chunk_64k"):
+        if kind == "prefill_2304":
+            T, first, n_rows, sample = 2304, 0, 2304, 64
+        else:
+            T, first, n_rows, sample = 65536, 61440, 4096, 64
+        rng = qi.rng_for(0 if kind == "prefill_2304" else 2)
+        qw, kw = qi.norm_weights(rng)
+        raw = qi.raw_keys(rng, T)
+        q = np.ascontiguousarray(qi.fused_qk(rng, sample)[:, :512])
+        c, s = orc.rope_table(T, THETA)
+        cache = np.zeros((T // 4, 128), np.uint16)
+        if first:
+            orc.pool_blocks(raw, 128, 0, first // 4, kw, c, s, EPS, block_keys=cache)
+        t0 = clock()
+        orc.pool_blocks(raw[first:], 128, first // 4, (T - first) // 4, kw, c, s, EPS,
+                        block_keys=cache)
+        t_pool = clock() - t0
+        rows = np.linspace(first, T - 1, sample).astype(np.int32)
+        sc = np.zeros((1, T // 4), np.float32)
+        t0 = clock()
+        for i, p in enumerate(rows):
+            orc.score_rows(q[i:i + 1], 512, rows[i:i + 1], 1, T, qw, c, s, EPS, cache, sc, T // 4)
+            orc.select_row(sc[0, :max(1, (p + 1) // 4)], int(p), T, BUDGET)
+        t_rows = clock() - t0
+        us = (t_pool / n_rows + t_rows / sample) * 1e6
+        what = (f"pool of the {(T - first) // 4} new blocks amortised over {n_rows} rows, plus "
+                f"score + select of {sample} rows spread evenly over positions {first}..{T - 1}")
+    elif kind == "decode_long_32seq":
+        rng = qi.rng_for(3)
+        lens = qi.long_context_lengths(rng, 32)[:2]
+        qw, kw = qi.norm_weights(rng)
+        tokens = 262144
+        c, s = orc.rope_table(tokens, THETA)
+        t_rows = 0.0
+        for i, L in enumerate(lens):
+            rr = qi.rng_for(3, salt=i + 1)
+            raw = qi.raw_keys(rr, int(L))
+            q = np.ascontiguousarray(qi.fused_qk(rr, 1)[:, :512])
+            cache = orc.pool_blocks(raw, 128, 0, int(L) // 4, kw, c, s, EPS)
+            sc = np.zeros((1, int(L) // 4), np.float32)
+            t0 = clock()
+            orc.score_rows(q, 512, np.array([L - 1], np.int32), 1, tokens, qw, c, s, EPS, cache,
+                           sc, int(L) // 4)
+            orc.select_row(sc[0], int(L - 1), tokens, BUDGET)
+            t_rows += clock() - t0
+        us = t_rows / len(lens) * 1e6
+        what = (f"score + select of {len(lens)} rows at lengths "
+                f"{', '.join(str(int(x)) for x in lens)}")
+    elif kind == "select_256k":
+        tokens, sample = 262144, 16
+        sc = qi.stress_scores(qi.rng_for(4), sample, tokens // 4)
+        t0 = clock()
+        for i in range(sample):
+            orc.select_row(sc[i], tokens - 1, tokens, BUDGET)
+        us = (clock() - t0) / sample * 1e6
+        what = f"select of {sample} stress rows at p = 262143, budget {BUDGET}"
+    else:
+        raise ValueError(kind)
+    return {"us_per_row": us, "rows_per_s": 1e6 / us, "cores": 1, "kind": "oracle",
+            "sample": what}
+
+
+def prefill_2304(torch, qsa, device, hbm_gbs, bf16_tf, ncu=False):
+    """Single-sequence prefill: T = 2304 tokens, every one of its 2304 rows
+    queried, budget 2048 (rows up to p = 2050 keep their whole prefix, later
+    rows truncate).  One step through qsa_index_select: pool the 576 blocks,
+    score on the tensor cores, select; each stage also timed alone."""
+    T = 2304
+    nb = T // 4
+    rng = qi.rng_for(0)
+    fq_h = qi.fused_qk(rng, T)
+    qw, kw = qi.norm_weights(rng)
+    c, s = qsa.qsa_rope_tables(T, THETA)
+    cd, sd = dev_tensor(torch, c, device), dev_tensor(torch, s, device)
+    qw, kw = dev_tensor(torch, qw, device), dev_tensor(torch, kw, device)
+    fq = dev_tensor(torch, fq_h, device)
+    keys = fq.view(-1)[512:]
+    pos = torch.arange(T, dtype=torch.int32, device=device)
+    cache = torch.zeros((nb, 128), dtype=torch.int16, device=device)
+    cols = nb
+    sc = torch.empty((T, cols), dtype=torch.float32, device=device)
+    mask = torch.empty((T, T), dtype=torch.uint8, device=device)
+    st = qsa.new_status(device)
+    ws = qsa.new_workspace(T, device)
+
+    def fused():
+        qsa.qsa_index_select(keys, 640, 0, nb, kw, fq, 640, pos, T, T, qw, cd, sd, T, EPS, BUDGET,
+                             cache, sc, cols, mask, st, workspace=ws)
+
+    def pool():
+        qsa.qsa_pool_blocks(keys, 640, 0, nb, kw, cd, sd, T, EPS, cache)
+
+    def score():
+        qsa.qsa_score_rows(fq, 640, pos, None, T, T, qw, cd, sd, T, EPS, cache, None, sc, cols, st,
+                           workspace=ws)
+
+    def select():
+        qsa.qsa_select_mask(sc, cols, pos, T, T, BUDGET, mask, st)
+
+    for _ in range(2 if ncu else 3):
+        fused()
+    torch.cuda.synchronize()
+    if ncu:
+        return None
+    it = 20
+    t_fused = time_fn(torch, fused, it)
+    t_pool = time_fn(torch, pool, it)
+    t_score = time_fn(torch, score, it)
+    t_sel = time_fn(torch, select, it)
+    code, row = qsa.qsa_read_status(st)
+    assert code == 0, (code, row)
+    live = sum((p + 1) // 4 for p in range(T))
+    trunc = sum((p + 1) // 4 for p in range(T) if (p + 1) // 4 > BUDGET // 4)
+    flops = 1024.0 * live
+    sel_bytes = 4.0 * trunc + T * T
+    return {
+        "rows": T, "tokens": T, "budget": BUDGET,
+        "first_truncating_row": next(p for p in range(T) if (p + 1) // 4 > BUDGET // 4),
+        "rows_per_s": T / (t_fused * 1e-3), "us_per_row": t_fused * 1000.0 / T,
+        "step_us": t_fused * 1000.0,
+        "path": "qsa_index_select (pool 576 blocks, tcgen05 score, select), CUDA graph",
+        "pool": {"us": t_pool * 1000.0, "blocks": nb,
+                 "frac_of_measured_hbm": nb * POOL_BYTES_PER_BLOCK / (t_pool * 1e-3) / 1e9 / hbm_gbs},
+        "score_tcgen05": {"us": t_score * 1000.0, "live_scores": live,
+                          "achieved_tflops": flops / (t_score * 1e-3) / 1e12,
+                          "frac_of_measured_bf16": flops / (t_score * 1e-3) / 1e12 / bf16_tf},
+        "select": {"us": t_sel * 1000.0, "algorithmic_bytes": sel_bytes,
+                   "frac_of_measured_hbm": sel_bytes / (t_sel * 1e-3) / 1e9 / hbm_gbs},
+        "note": "latency-bound: 0.68 GFLOP and 5.3 MB of mask, a few microseconds of work "
+                "at either peak",
+    }
 
 
 def time_fn(torch, fn, iters):
@@ -917,6 +1087,8 @@ def ncu_case(name: str):
             wl.step(k)
     elif name == "prefill":
         prefill_chunk(torch, qsa, dev, 6800.0, 1900.0, ncu=True)
+    elif name == "prefill2304":
+        prefill_2304(torch, qsa, dev, 6800.0, 1900.0, ncu=True)
     elif name == "select256k":
         select_256k(torch, qsa, dev, 6800.0, ncu=True)
     elif name == "decode_long":

@@ -84,6 +84,25 @@ int32_t qsa_version(void);
 const char *qsa_status_string(int32_t status);
 
 /*
+ * The limit of the bounded device waits a caller may shorten, in SM clock
+ * cycles (default 4e9, about 2 s at 2 GHz): the streaming scorer's wait for
+ * each stage of block keys it copies into shared memory (qsa_score_rows on
+ * the SIMT path, qsa_decode_index_select), and the fused decode step's
+ * barrier over a row's CTAs.  A wait that reaches the limit records
+ * QSA_ERR_TIMEOUT with its row in dev_status and the row's output is left
+ * unspecified (a fused decode call then also leaves its workspace dirty:
+ * zero it before the next call); the CTA first lets its own copies in flight
+ * land, under the fixed default limit.  Source: PR #1178's review note on
+ * environment side effects (a trap left the GPU unusable, so waits report
+ * instead of trapping); a short limit lets a test make a wait run out without
+ * faulting anything.  The value is process-wide and read when a kernel is
+ * launched (a captured CUDA graph keeps the value in force at capture).
+ * qsa_set_wait_limit_cycles refuses cycles <= 0 with QSA_ERR_INVALID_VALUE.
+ */
+qsa_status qsa_set_wait_limit_cycles(int64_t cycles);
+int64_t qsa_wait_limit_cycles(void);
+
+/*
  * RoPE cos/sin tables, HOST memory, built on the CPU (no device work).
  * Source: PR #1160 review ("read the cos and sin table that the rope module
  * builds"): the indexer rotates with the same position embeddings as attention,
@@ -189,7 +208,9 @@ qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; QSA_ERR_LAUNCH if the
  *    lookup fails.  Make the first call on each device before any stream
- *    capture.
+ *    capture.  After a device reset (cudaDeviceReset, or the primary context
+ *    released and created again) the next call sees a new context ID and
+ *    looks the address up again; make that call before any capture too.
  *  - Every call shares the one array and it keeps the last call's contents;
  *    each call overwrites all of it that it reads, so nothing must start at
  *    zero.  Calls that overlap on the GPU (unordered streams or host threads

@@ -38,7 +38,7 @@ EXPORTED = ("qsa_version", "qsa_status_string", "qsa_rope_tables", "qsa_pool_blo
             "qsa_score_rows_noalloc", "qsa_select_mask", "qsa_index_select",
             "qsa_decode_workspace_bytes", "qsa_decode_index_select", "qsa_mask_tokens",
             "qsa_gather_kv", "qsa_sparse_attn", "qsa_qk_proj", "qsa_reset_status",
-            "qsa_read_status")
+            "qsa_read_status", "qsa_set_wait_limit_cycles", "qsa_wait_limit_cycles")
 
 
 class QsaError(RuntimeError):
@@ -79,6 +79,8 @@ def _load() -> ctypes.CDLL:
         "qsa_qk_proj": ([P, i64, P, i32, i32, i32, P, i64, P, P], i32),
         "qsa_reset_status": ([P, P], i32),
         "qsa_read_status": ([P, P, P, P], i32),
+        "qsa_set_wait_limit_cycles": ([i64], i32),
+        "qsa_wait_limit_cycles": ([], i64),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -126,6 +128,16 @@ def _check(rc: int, where: str) -> None:
 
 def qsa_version() -> int:
     return int(_lib.qsa_version())
+
+
+def qsa_set_wait_limit_cycles(cycles: int) -> None:
+    """The limit, in SM clock cycles, of the waits a caller may shorten (the
+    streaming scorer's key-copy waits, the fused decode step's barrier)."""
+    _check(_lib.qsa_set_wait_limit_cycles(int(cycles)), "qsa_set_wait_limit_cycles")
+
+
+def qsa_wait_limit_cycles() -> int:
+    return int(_lib.qsa_wait_limit_cycles())
 
 
 def qsa_rope_tables(max_pos: int, theta: float = 10000.0) -> tuple[np.ndarray, np.ndarray]:

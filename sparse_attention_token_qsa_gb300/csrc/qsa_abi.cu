@@ -8,6 +8,7 @@
 // pointer is formed) and PR #1160 "score QSA token-indexer blocks in native
 // CUDA" (rows and visible_len as separate device arrays; the RoPE tables are
 // inputs; only rms_eps is a run-time scalar).
+#include <atomic>
 #include <cmath>
 #include <math.h>
 #include <stdint.h>
@@ -26,6 +27,9 @@ constexpr int kRatio = 4;
 constexpr int kRot = 64;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s of SM clock at 2 GHz
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
 
 qsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR_LAUNCH; }
 
@@ -89,9 +93,19 @@ qsa_status check_pool_args(const uint16_t *keys, int64_t key_stride, int32_t fir
 
 }  // namespace
 
+long long qsa::wait_limit_cycles() { return g_wait_limit.load(std::memory_order_relaxed); }
+
 extern "C" {
 
 int32_t qsa_version(void) { return kVersion; }
+
+qsa_status qsa_set_wait_limit_cycles(int64_t cycles) {
+  if (cycles <= 0) return QSA_ERR_INVALID_VALUE;
+  g_wait_limit.store(cycles, std::memory_order_relaxed);
+  return QSA_OK;
+}
+
+int64_t qsa_wait_limit_cycles(void) { return g_wait_limit.load(std::memory_order_relaxed); }
 
 const char *qsa_status_string(int32_t status) {
   switch (status) {
@@ -167,7 +181,7 @@ qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_
   if (path == QSA_SCORE_TCGEN05 && (key_base != nullptr || !ws_ok)) return QSA_ERR_INVALID_VALUE;
   qsa::ScoreArgs a{q,          q_stride, pos,   visible_len, n_rows,     tokens,
                    q_norm_w,   cos_t,    sin_t, eps,         block_keys, key_base,
-                   scores,     score_cols, dev_status};
+                   scores,     score_cols, dev_status, qsa::wait_limit_cycles()};
   if (path == QSA_SCORE_AUTO)
     path = (qsa::kTcScorerReady && key_base == nullptr && ws_ok && n_rows >= 64 && tokens >= 2048)
                ? QSA_SCORE_TCGEN05
@@ -271,7 +285,7 @@ qsa_status qsa_decode_index_select(const uint16_t *keys, int64_t key_stride,
   if (!pool_inside && (st = pool_launch()) != QSA_OK) return st;
   qsa::ScoreArgs a = {q,        q_stride, pos,        nullptr,    n_rows, tokens, q_norm_w,
                       cos_t,    sin_t,    eps,        block_keys, nullptr, scores, score_cols,
-                      dev_status};
+                      dev_status, qsa::wait_limit_cycles()};
   bool launched = false;
   st = from_cuda(qsa::launch_decode_fused(a, budget, mask, decode_ws, keys, key_stride,
                                           pool_first_block, pool_inside ? pool_n_blocks : 0,

@@ -454,14 +454,9 @@ sparse_attn_kernel(const AttnArgs a, int32_t head_chunks) {
 
 template <int HD>
 cudaError_t launch_attn_hd(const AttnArgs &a, int32_t n_rows, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<HD>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)AttnGeom<HD>::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDevice smem_attr;
+  const cudaError_t e = set_smem_once(smem_attr, sparse_attn_kernel<HD>, AttnGeom<HD>::kSmem);
+  if (e != cudaSuccess) return e;
   const int32_t head_chunks = (a.group + 7) / 8;
   const int64_t units = (int64_t)n_rows * a.nkv * head_chunks;
   return launch_dependent(sparse_attn_kernel<HD>, dim3((unsigned)units), dim3(32 * kAttnWarps),

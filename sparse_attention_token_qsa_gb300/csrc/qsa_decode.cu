@@ -229,9 +229,10 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
     // above) are visible to whoever sees the count
     red_add_release_gpu(&W.arrive, 1u);
     const long long t0 = clock64();
+    const long long limit = a.wait_limit > 0 ? a.wait_limit : kDecSpinLimit;
     int ok = 1;
     while (ld_acquire_gpu(&W.arrive) < (uint32_t)ny) {
-      if (clock64() - t0 > kDecSpinLimit) {
+      if (clock64() - t0 > limit) {
         ok = 0;
         break;
       }
@@ -491,23 +492,23 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   }
 }
 
-int g_dec_capacity = -1;  // co-resident CTAs of the fused kernel (0: not usable)
-
+// Co-resident CTAs of the fused kernel on the current device (0: not usable),
+// with its shared-memory attribute set; once per device.
 int dec_capacity() {
-  if (g_dec_capacity >= 0) return g_dec_capacity;
-  int dev = 0, sms = 0, per = 0;
-  if (cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kDecSmemBytes) != cudaSuccess ||
-      cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_fused_kernel, kDecThreads,
-                                                    kDecSmemBytes) != cudaSuccess) {
-    cudaGetLastError();
-    g_dec_capacity = 0;
-    return 0;
-  }
-  g_dec_capacity = per * sms;
-  return g_dec_capacity;
+  static PerDevice cache;
+  return cache.get([]() -> int {
+    int dev = 0, sms = 0, per = 0;
+    if (cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kDecSmemBytes) != cudaSuccess ||
+        cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_fused_kernel, kDecThreads,
+                                                      kDecSmemBytes) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    return per * sms;
+  });
 }
 
 }  // namespace

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "qsa_per_device.h"
+
 namespace qsa {
 
 // Launch `kernel` so that it may begin while the previous kernel in `stream`
@@ -57,7 +59,14 @@ struct ScoreArgs {
   float *scores;
   int64_t score_cols;
   int32_t *status;
+  // limit of the waits a caller may shorten (the streaming scorer's wait for
+  // its key copies, the fused decode step's grid barrier), in SM clock
+  // cycles; <= 0 means the default
+  long long wait_limit;
 };
+
+// The limit qsa_set_wait_limit_cycles set (process-wide), read at each launch.
+long long wait_limit_cycles();
 
 cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream);
 // Prepared query heads, [n_rows * 4, 128] bf16, into a workspace.

@@ -18,8 +18,16 @@
 // has to start at zero.  Calls whose kernels overlap on the GPU (different
 // streams, or different host threads on one device, without ordering between
 // them) race on the array.
+//
+// The array's device address belongs to the CUDA context that loaded this
+// module.  A device reset (cudaDeviceReset, or the primary context released
+// and created again) loads the module anew, possibly elsewhere, so the address
+// is looked up once per device and context: each call compares the current
+// context's ID with the one the address was looked up under and looks it up
+// again when they differ (or when the ID cannot be read).
 #include <mutex>
 
+#include <cuda.h>  // CUcontext (the two driver calls come through the runtime)
 #include <cuda_runtime.h>
 
 #include "../../include/qsa.h"
@@ -34,24 +42,71 @@ constexpr int64_t kNoAllocBytes = (int64_t)QSA_NOALLOC_MAX_ROWS * 4 * 128 * 2;
 static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_ws_addr[kMaxDevices] = {};
 
-// Set-up, once per device, with that device current: look up the array's
-// device address.  Returns nullptr if the lookup fails.
+struct WsAddr {
+  void *addr;                  // the array's device address ...
+  unsigned long long ctx_id;   // ... in the context with this ID (0: unknown)
+};
+std::mutex g_mu;
+WsAddr g_ws[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// The ID of the calling thread's current context (unique per context the
+// driver creates, never reused), or 0 if it cannot be read.
+unsigned long long current_context_id() {
+  struct Calls {
+    CtxGetCurrentFn get_current;
+    CtxGetIdFn get_id;
+  };
+  static const Calls calls = []() -> Calls {
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    const bool ok =
+        cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) ==
+            cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+            cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return Calls{nullptr, nullptr};
+    }
+    return Calls{reinterpret_cast<CtxGetCurrentFn>(a), reinterpret_cast<CtxGetIdFn>(b)};
+  }();
+  if (calls.get_current == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (calls.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      calls.get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Set-up, once per device and context, with that device current: look up the
+// array's device address (cudaGetSymbolAddress also makes the device's
+// primary context current on this thread).  Returns nullptr if the lookup
+// fails.
 void *workspace_for_current_device() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_ws_addr[dev] == nullptr) {
+  const unsigned long long id = current_context_id();
+  if (g_ws[dev].addr == nullptr || id == 0 || id != g_ws[dev].ctx_id) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess) {
       cudaGetLastError();  // leave no sticky error behind
+      g_ws[dev] = WsAddr{nullptr, 0};
       return nullptr;
     }
-    g_ws_addr[dev] = p;
+    g_ws[dev] = WsAddr{p, current_context_id()};
   }
-  return g_ws_addr[dev];
+  return g_ws[dev].addr;
 }
 
 }  // namespace

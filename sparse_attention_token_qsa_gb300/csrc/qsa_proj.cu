@@ -305,28 +305,19 @@ using PEncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, v
                                const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder (process-wide; looked up once, thread-safe).
 PEncodeFn p_encoder() {
-  static PEncodeFn fn = nullptr;
-  if (fn == nullptr) {
+  static const PEncodeFn fn = []() -> PEncodeFn {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PEncodeFn>(p);
-  }
+      return reinterpret_cast<PEncodeFn>(p);
+    cudaGetLastError();
+    return nullptr;
+  }();
   return fn;
-}
-
-int p_sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
 }
 
 }  // namespace
@@ -351,8 +342,8 @@ cudaError_t launch_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, 
   const int32_t nk = (hidden + kPKS - 1) / kPKS;
   const int64_t m_tiles = (n_rows + kPM - 1) / kPM;
   // wide tiles once they alone fill most of the GPU
-  const bool wide = m_tiles * ((out_cols + 159) / 160) >= (int64_t)p_sm_count() * 3 / 4;
-  auto run = [&](auto kernel, int bn, size_t smem, bool &attr_set) -> cudaError_t {
+  const bool wide = m_tiles * ((out_cols + 159) / 160) >= (int64_t)device_sm_count() * 3 / 4;
+  auto run = [&](auto kernel, int bn, size_t smem, PerDevice &smem_attr) -> cudaError_t {
     CUtensorMap bmap;
     const cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)out_cols};
     const cuuint64_t strides[1] = {(cuuint64_t)hidden * 2};
@@ -361,16 +352,13 @@ cudaError_t launch_proj(const uint16_t *x, int64_t x_stride, const uint16_t *w, 
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    if (!attr_set) {
-      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr_set = true;
-    }
+    const cudaError_t e = set_smem_once(smem_attr, kernel, smem);
+    if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((out_cols + bn - 1) / bn), (unsigned)m_tiles);
     return launch_dependent(kernel, grid, dim3(kPThreads), smem, stream, 1u, amap, bmap, y, y_stride,
                             n_rows, out_cols, nk, status);
   };
-  static bool set80 = false, set160 = false;
+  static PerDevice set80, set160;
   if (wide) return run(proj_kernel<160>, 160, proj_smem<160>(), set160);
   return run(proj_kernel<80>, 80, proj_smem<80>(), set80);
 }

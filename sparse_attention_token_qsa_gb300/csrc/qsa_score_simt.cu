@@ -43,17 +43,12 @@ score_simt_kernel(const ScoreArgs a, int32_t blocks_per_cta) {
 cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream) {
   const int64_t n_max = (int64_t)a.tokens / kRatio;
   if (n_max == 0) return cudaSuccess;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(score_simt_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSimtSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDevice smem_attr;
+  const cudaError_t e = set_smem_once(smem_attr, score_simt_kernel, kSimtSmemBytes);
+  if (e != cudaSuccess) return e;
   const int64_t iters = (n_max + kSimtBlocksPerIter - 1) / kSimtBlocksPerIter;
   // enough CTAs to cover ~8 per SM, each streaming at least 128 blocks
-  int64_t k = ((int64_t)a.n_rows * iters) / (8 * 152);
+  int64_t k = ((int64_t)a.n_rows * iters) / (8 * (int64_t)device_sm_count());
   k = k < 1 ? 1 : (k > 16 ? 16 : k);
   while ((iters + k - 1) / k > 65535) ++k;
   const int32_t bpc = (int32_t)(k * kSimtBlocksPerIter);

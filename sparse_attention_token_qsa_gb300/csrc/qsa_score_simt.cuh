@@ -33,6 +33,11 @@ constexpr int kSimtStages = 3;
 constexpr uint32_t kSimtStageBytes = kSimtBlocksPerIter * kHeadDim * 2;  // 32 KiB
 constexpr long long kSimtSpinLimit = 4000000000LL;                      // ~2 s of SM clock
 
+// The limit of a wait the caller may shorten (ScoreArgs::wait_limit).
+__device__ __forceinline__ long long caller_wait_limit(const ScoreArgs &a) {
+  return a.wait_limit > 0 ? a.wait_limit : kSimtSpinLimit;
+}
+
 struct SimtSmem {
   float q_s[kHeads][kHeadDim];
   uint64_t full[kSimtStages];
@@ -45,8 +50,9 @@ __device__ __forceinline__ uint32_t simt_smem_u32(const void *p) {
 }
 
 // Bounded wait on an mbarrier phase (the thread sleeps in hardware between
-// tests).  Returns false once the limit is reached.
-__device__ __forceinline__ bool simt_wait(uint32_t mbar, uint32_t parity) {
+// tests).  Returns false once `limit` cycles have passed.
+__device__ __forceinline__ bool simt_wait(uint32_t mbar, uint32_t parity,
+                                          long long limit = kSimtSpinLimit) {
   const long long t0 = clock64();
   while (true) {
     uint32_t ok;
@@ -58,7 +64,7 @@ __device__ __forceinline__ bool simt_wait(uint32_t mbar, uint32_t parity) {
         : "r"(mbar), "r"(parity), "r"(20000u)
         : "memory");
     if (ok) return true;
-    if (clock64() - t0 > kSimtSpinLimit) return false;
+    if (clock64() - t0 > limit) return false;
   }
 }
 
@@ -163,7 +169,8 @@ __device__ __forceinline__ bool simt_score_blocks(const ScoreArgs &a, int row, i
   bool failed = false;
   for (; it < n_it; ++it) {
     const int s = it % kSimtStages;
-    const bool ok = simt_wait(simt_smem_u32(&S.full[s]), (uint32_t)(it / kSimtStages) & 1u);
+    const bool ok = simt_wait(simt_smem_u32(&S.full[s]), (uint32_t)(it / kSimtStages) & 1u,
+                              caller_wait_limit(a));
     if (__syncthreads_or(!ok)) {
       failed = true;
       break;
@@ -219,7 +226,8 @@ __device__ __forceinline__ bool simt_score_blocks(const ScoreArgs &a, int row, i
     if (tid == 0 && it + kSimtStages < n_it) issue(it + kSimtStages);
   }
   if (failed && tid == 0) {
-    // let this CTA's own copies land before its shared memory is reused
+    // let this CTA's own copies land before its shared memory is reused (at
+    // the fixed limit: a copy in flight lands within microseconds)
     for (int k = it; k < min(n_it, it + kSimtStages); ++k)
       simt_wait(simt_smem_u32(&S.full[k % kSimtStages]), (uint32_t)(k / kSimtStages) & 1u);
   }

@@ -484,28 +484,19 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder (process-wide; looked up once, thread-safe).
 EncodeTiledFn encoder() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void *p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+    return nullptr;
+  }();
   return fn;
-}
-
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
 }
 
 }  // namespace
@@ -539,14 +530,10 @@ cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stre
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  cudaError_t e = launch_qprep(a, qws, stream);
+  static PerDevice smem_attr;
+  cudaError_t e = set_smem_once(smem_attr, score_tc_kernel, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = launch_qprep(a, qws, stream);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM, each taking a balanced contiguous range of
   // (row tile, block tile) units; more than kMaxRowTiles row tiles go in slabs,
@@ -563,7 +550,7 @@ cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stre
     b.visible_len = a.visible_len ? a.visible_len + r0 : nullptr;
     b.scores = a.scores + (int64_t)r0 * a.score_cols;
     const int64_t row_tiles = (b.n_rows + kRowsPerCta - 1) / kRowsPerCta;
-    int64_t ctas = sm_count();
+    int64_t ctas = device_sm_count();
     if (ctas > row_tiles * tiles_total) ctas = row_tiles * tiles_total;
     e = launch_dependent(score_tc_kernel, dim3((unsigned)ctas), dim3(kThreads), kSmemBytes, stream,
                          1u, kmap, qmap, b, tiles_total, r0);

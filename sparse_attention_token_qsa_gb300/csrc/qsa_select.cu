@@ -940,8 +940,6 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   if (C > 1) cluster_sync_all();
 }
 
-static int g_max_cluster = -1;
-
 static size_t select_smem_bytes(int32_t cap) {
   return ((sizeof(SelectSmem) + 15) & ~size_t(15)) + 6 * (size_t)kCandCap +
          4 * (size_t)(cap > 0 ? cap : 1);
@@ -949,9 +947,15 @@ static size_t select_smem_bytes(int32_t cap) {
 
 // Largest cluster the select kernel can be co-scheduled with (16 needs the
 // non-portable opt-in; fall back to 8, 4, 2 if the GPU refuses).  Both block
-// shapes get their attributes here, once.
+// shapes get their attributes here, once per device.
+static int probe_max_cluster();
+
 static int max_cluster_size() {
-  if (g_max_cluster >= 0) return g_max_cluster;
+  static PerDevice cache;
+  return cache.get(probe_max_cluster);
+}
+
+static int probe_max_cluster() {
   int best = 1;
   for (auto fn : {select_kernel<512, true>, select_kernel<256, false>}) {
     cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -977,23 +981,10 @@ static int max_cluster_size() {
     }
   }
   cudaGetLastError();  // a refused query leaves no sticky error
-  g_max_cluster = best;
   return best;
 }
 
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-      n = v;
-    else
-      n = 1;
-    cudaGetLastError();
-  }
-  return n;
-}
+static int sm_count() { return device_sm_count(); }
 
 // Cluster size for a launch: split a row over a cluster when its blocks
 // overflow one CTA's key cache, and then, for launches of a few such rows,

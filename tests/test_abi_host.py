@@ -236,3 +236,19 @@ def test_rope_tables_match_oracle(lib, orc):
     assert lib.qsa_rope_tables(-1, 1e4, None, None) == 1
     assert lib.qsa_rope_tables(4, 0.0, P(A), P(A)) == 1
     assert lib.qsa_rope_tables(0, 1e4, None, None) == 0
+
+
+def test_wait_limit_is_settable_and_refuses_non_positive(lib):
+    import sparse_attention_token_qsa_gb300 as qsa
+
+    default = lib.qsa_wait_limit_cycles()
+    assert default == 4000000000
+    assert lib.qsa_set_wait_limit_cycles(0) == qsa.QSA_ERR_INVALID_VALUE
+    assert lib.qsa_set_wait_limit_cycles(-7) == qsa.QSA_ERR_INVALID_VALUE
+    assert lib.qsa_wait_limit_cycles() == default
+    try:
+        assert lib.qsa_set_wait_limit_cycles(12345) == qsa.QSA_OK
+        assert lib.qsa_wait_limit_cycles() == 12345
+    finally:
+        assert lib.qsa_set_wait_limit_cycles(default) == qsa.QSA_OK
+    assert lib.qsa_wait_limit_cycles() == default

@@ -87,12 +87,13 @@ const char *qsa_status_string(int32_t status);
  * The limit of the bounded device waits a caller may shorten, in SM clock
  * cycles (default 4e9, about 2 s at 2 GHz): the streaming scorer's wait for
  * each stage of block keys it copies into shared memory (qsa_score_rows on
- * the SIMT path, qsa_decode_index_select), and the fused decode step's
- * barrier over a row's CTAs.  A wait that reaches the limit records
- * QSA_ERR_TIMEOUT with its row in dev_status and the row's output is left
- * unspecified (a fused decode call then also leaves its workspace dirty:
- * zero it before the next call); the CTA first lets its own copies in flight
- * land, under the fixed default limit.  Source: PR #1178's review note on
+ * the SIMT path), and the fused decode step's waits for its key copies, its
+ * MMAs and its barrier over a row's CTAs (qsa_decode_index_select).  A wait
+ * that reaches the limit records QSA_ERR_TIMEOUT with its row in dev_status
+ * and the row's output is left unspecified (a fused decode call may then
+ * leave its workspace dirty: zero it before the next call); the CTA first
+ * lets its own copies and MMAs in flight finish, under the fixed default
+ * limit.  Source: PR #1178's review note on
  * environment side effects (a trap left the GPU unusable, so waits report
  * instead of trapping); a short limit lets a test make a wait run out without
  * faulting anything.  The value is process-wide and read when a kernel is

@@ -3,25 +3,36 @@
 //
 // The operation is the scorer's and the selector's, unchanged (PR #1160
 // "score QSA token-indexer blocks in native CUDA": S[p, b] = sum_h relu(q_h .
-// k_b) / sqrt(128) over the row's visible blocks; PR #1178 "select QSA indexer
-// blocks", "Exact semantics": the keep = min(budget / 4, blocks) highest
-// scores under (score descending, block index ascending), their tokens and the
-// row's tail visible).  metrale layers/qsa.rs decode_select runs the two back
-// to back for each decode step; at one row per step the second launch and
-// the selector's single-CTA passes over the row are most of the step's time,
-// so here the row's scoring CTAs also do the selection:
+// k_b) / sqrt(128) over the row's visible blocks, relu per head before the
+// head sum, NaN kept; PR #1178 "select QSA indexer blocks", "Exact semantics":
+// the keep = min(budget / 4, blocks) highest scores under (score descending,
+// block index ascending, -0.0 == +0.0), their tokens and the row's tail
+// visible).  metrale layers/qsa.rs decode_select runs the two back to back
+// for each decode step; at one row per step the second launch and the
+// selector's single-CTA passes over the row are most of the step's time, so
+// here the row's scoring CTAs also do the selection:
 //
-//  1. each CTA scores its contiguous range of the row's blocks (the streaming
-//     core shared with the decode scorer), keeps its scores in shared memory
-//     and adds their top-12-bit order-key histogram into the row's workspace
-//     (exact zeros counted per warp);
-//  2. the row's CTAs meet at a grid barrier (the launch is cooperative, so
+//  1. each CTA scores a contiguous range of at most 256 of the row's blocks
+//     on the tensor cores: warp 0 copies them with TMA (128-byte swizzle), one
+//     128-block tile per stage, issued as soon as the launch may read memory;
+//     warps 2-3 prepare the row's four query heads ((1 + w) RMSNorm, RoPE at
+//     the row's position) as the 16 x 128 operand of the MMA (rows 4..15
+//     zero); warp 1 issues tcgen05.mma M128 N16 K16 x 8 per tile (keys on M,
+//     heads on N) into its own TMEM accumulator; warps 4-7 first pool the
+//     newly complete blocks of the range (writing each into its landed tile
+//     as well, since the copy may have read the old key), then read the
+//     accumulators (one block per TMEM lane, its four heads in four columns),
+//     apply relu, the head sum in order 0..3 and the scale, and keep the
+//     scores in shared memory;
+//  2. each CTA adds its scores' top-12-bit order-key histogram into the row's
+//     workspace (one add per distinct bin per warp);
+//  3. the row's CTAs meet at a grid barrier (the launch is cooperative, so
 //     they are co-resident; the wait is bounded);
-//  3. every CTA reads the row's histogram, finds the bin holding the keep-th
+//  4. every CTA reads the row's histogram, finds the bin holding the keep-th
 //     key (a non-finite score shows up in the 16 outer bins), writes the final
 //     mask bytes of its own blocks outside that bin, and appends the bin's
 //     keys with their block indices to the row's candidate list;
-//  4. the last CTA of the row to finish (an atomic ticket) zeroes the row's
+//  5. the last CTA of the row to finish (an atomic ticket) zeroes the row's
 //     workspace for the next call (its stores drain while it works on), runs
 //     the remaining radix rounds (8, 8, 4 bits) over the candidates, cuts
 //     exact ties at the final key by radix rounds on the block index (lowest
@@ -31,17 +42,29 @@
 // tokens / 4 candidates (key, block index).  It must be zero before the first
 // call; every call that completes leaves it zero.  A call that reports an
 // error may leave it dirty: zero it again before the next call.
-#include "qsa_score_simt.cuh"
+#include "qsa_device.cuh"
+#include "qsa_launch.h"
 #include "qsa_select_util.cuh"
+#include "qsa_tma.h"
 
 namespace qsa {
 
 namespace {
 
-constexpr int kDecThreads = kSimtThreads;
-constexpr int kDecMaxBpc = 512;      // blocks per CTA (their scores stay in shared memory)
-constexpr int kDecCandCache = 8192;  // candidates the last CTA copies into shared memory
+constexpr int kDecThreads = 256;
+constexpr int kDecTile = 128;                                 // blocks per key tile: the MMA's M
+constexpr int kDecStages = 2;                                 // tiles per CTA, one stage each
+constexpr int kDecMaxBpc = kDecStages * kDecTile;             // blocks per CTA
+constexpr uint32_t kDecTileBytes = kDecTile * kHeadDim * 2;   // 32 KiB
+constexpr uint32_t kDecHalfBytes = kDecTile * 64 * 2;         // one 64-dim box: 16 KiB
+constexpr int kDecN = 16;                                     // MMA N: 4 heads, 12 zero rows
+constexpr uint32_t kDecTmemCols = 32;                         // one 16-column accumulator per tile
+constexpr int kDecCandCache = 4096;  // candidates the last CTA copies into shared memory
 constexpr long long kDecSpinLimit = 4000000000LL;  // ~2 s of SM clock
+constexpr uint32_t kDecSuspendNs = 500;
+// instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M = 128, N = 16
+constexpr uint32_t kDecIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                               ((uint32_t)(kDecN >> 3) << 17) | ((uint32_t)(kDecTile >> 4) << 24);
 
 struct RowHdr {  // per row, at the start of the row's workspace
   uint32_t hist0[4096];
@@ -78,9 +101,156 @@ struct DecSmem {  // selection scratch, laid over the key ring once scoring is d
   uint32_t rabove[4];  // ... and the keys above it
 };
 constexpr size_t kDecCandOff = (sizeof(DecSmem) + 127) & ~size_t(127);
-static_assert(kDecCandOff + (size_t)kDecCandCache * 8 <= kSimtRingBytes, "scratch overflows the ring");
-constexpr size_t kDecSmemBytes = kSimtStageOff + kSimtRingBytes + kDecMaxBpc * sizeof(float);
+static_assert(kDecCandOff + (size_t)kDecCandCache * 8 <= kDecStages * kDecTileBytes,
+              "selection scratch overflows the ring");
 
+// Shared memory, from a 1024-byte aligned base: the key ring (the selection's
+// scratch once the keys are scored), the query operand, the scores, control.
+constexpr uint32_t kDecQOff = kDecStages * kDecTileBytes;
+constexpr uint32_t kDecQBytes = kDecN * kHeadDim * 2;  // two 64-dim halves of 2 KiB
+constexpr uint32_t kDecScOff = kDecQOff + kDecQBytes;
+constexpr uint32_t kDecCtrlOff = kDecScOff + kDecMaxBpc * 4;
+
+struct DecCtrl {
+  uint64_t full[kDecStages];
+  uint64_t tfull[kDecStages];
+  uint64_t qready;
+  uint64_t pooled;
+  uint64_t drain;
+  uint64_t hbar;         // the histogram copies of the selection
+  uint32_t tmem_base;
+  int32_t abort;
+  int32_t issued;        // key tiles the producer issued
+  uint32_t maxbin;       // this CTA's highest bin
+  uint32_t low;          // a key of this CTA landed below bin 8
+};
+constexpr size_t kDecSmemBytes = kDecCtrlOff + sizeof(DecCtrl) + 1024;  // + alignment slack
+
+__device__ __forceinline__ uint32_t sm32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+
+// Bounded wait on a phase: a non-blocking test, then sleeps of up to
+// kDecSuspendNs that end early when the phase completes.  Gives up (raising
+// the abort flag) once `limit` cycles have passed, or when another role
+// already gave up.
+__device__ bool tc_wait(uint32_t mb, uint32_t parity, long long limit,
+                        volatile int32_t *abort_flag) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(mb), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(mb), "r"(parity), "r"(kDecSuspendNs)
+        : "memory");
+    if (ok) return true;
+  }
+}
+
+// The same wait made warp-uniform: lane 0 waits, the verdict is broadcast.
+__device__ __forceinline__ bool tc_warp_wait(uint32_t mb, uint32_t parity, long long limit,
+                                             volatile int32_t *abort_flag) {
+  uint32_t ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = tc_wait(mb, parity, limit, abort_flag) ? 1u : 0u;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart, descriptor version 1 (sm_100 family).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+      "l"(adesc), "l"(bdesc), "r"(kDecIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// This thread's TMEM lane, four consecutive columns (the four heads).
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3])
+               :
+               : "memory");
+}
+
+// relu that keeps NaN (max.NaN returns NaN when either input is NaN)
+__device__ __forceinline__ float relu_nan(float d) {
+  float r;
+  asm("max.NaN.f32 %0, %1, 0f00000000;" : "=f"(r) : "f"(d));
+  return r;
+}
+
+// The row's selection across the cluster (every CTA calls it; the row has
+// more blocks than keep_max and every CTA's scores and level-1 counts h1 are
+// in place).  Levels of 12, 8, 8 and 4 order-key bits; at each, every CTA
+// adds its counts of the keys in the current bin into the owners' slices of
+// the cluster's histogram, and after one cluster barrier reads the sums back
+// and finds the bin of the need-th key.  Writes this CTA's mask bytes.
 __device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -99,99 +269,207 @@ struct PoolArgs {         // newly complete blocks to pool in the same launch
   uint16_t *block_keys;  // the scorer's block-key cache, written here
 };
 
-constexpr int kDecPoolOverlap = 12;  // blocks a scoring CTA pools in its copy window (warps 2..7)
-
 __global__ void __launch_bounds__(kDecThreads)
-decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ mask,
-                    uint8_t *__restrict__ ws, int64_t row_ws_bytes, int32_t bpc,
-                    const PoolArgs pa) {
-  extern __shared__ __align__(128) uint8_t dec_smem[];
-  __shared__ uint32_t s_maxbin, s_low;  // this CTA's highest bin, any bin below 8
-  SimtSmem &S = *reinterpret_cast<SimtSmem *>(dec_smem);
-  uint8_t *ring = dec_smem + kSimtStageOff;
-  float *sc_s = reinterpret_cast<float *>(ring + kSimtRingBytes);
-  DecSmem &D = *reinterpret_cast<DecSmem *>(ring);
+decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int32_t keep_max,
+                    uint8_t *__restrict__ mask, uint8_t *__restrict__ ws, int64_t row_ws_bytes,
+                    int32_t bpc, const PoolArgs pa) {
+  extern __shared__ uint8_t dec_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(dec_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *ring = smem;
+  DecCtrl &C = *reinterpret_cast<DecCtrl *>(smem + kDecCtrlOff);
+  float *sc_s = reinterpret_cast<float *>(smem + kDecScOff);
+  DecSmem &D = *reinterpret_cast<DecSmem *>(ring);  // selection scratch, once the keys are scored
   uint32_t *ck_s = reinterpret_cast<uint32_t *>(ring + kDecCandOff);  // cached candidate keys
   uint32_t *ci_s = ck_s + kDecCandCache;                              // ... and block indices
-  grid_dependency_sync();
+  const uint32_t sRing = sm32(ring), sQ = sm32(smem + kDecQOff);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x, y = blockIdx.y, ny = gridDim.y;
-  // the query row's load is issued beside the position's (both may live in
-  // host memory: two round trips side by side instead of one after the other)
-  const uint4 qchunk = load_query_chunk(a, row);
+
+  // ---- set-up while the previous launch finishes: barriers, the zero rows of
+  // the query operand, TMEM
   if (tid == 0) {
-    s_maxbin = 0u;
-    s_low = 0u;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(sm32(&C.full[s]), 1);
+      mbar_init(sm32(&C.tfull[s]), 1);
+    }
+    mbar_init(sm32(&C.qready), 64);  // the query-prep threads
+    mbar_init(sm32(&C.pooled), 128);  // the epilogue threads, once they have pooled
+    mbar_init(sm32(&C.drain), 1);
+    mbar_init(sm32(&C.hbar), 1);
+    C.abort = 0;
+    C.issued = 0;
+    C.maxbin = 0u;
+    C.low = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  reinterpret_cast<uint4 *>(smem + kDecQOff)[tid] = make_uint4(0u, 0u, 0u, 0u);  // 4 KiB
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     sm32(&C.tmem_base)),
+                 "r"(kDecTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  grid_dependency_sync();
+
+  // the position is read by every role; only the key copies start without it
   const int32_t p = a.pos[row];
   const bool valid = p >= 0 && p < a.tokens;
   const int32_t n = valid ? (p + 1) >> 2 : 0;
-
-  // ---- 0. the newly complete blocks in this CTA's range are pooled here
-  // (every row's CTAs pool them, writing identical keys, so the range is
-  // covered whatever each row sees).  A CTA that scores them does it in its
-  // copy window and patches its landed stage; any other CTA, or one with more
-  // than kDecPoolOverlap of them, pools before it scores.
-  const int pr0 = max(pa.first, y * bpc);
-  const int pr1 = min(pa.first + pa.n, min(y * bpc + bpc, a.tokens >> 2));
+  const int32_t n_max = a.tokens >> 2;
+  const int c0 = y * bpc;
+  const int c1 = min(n, c0 + bpc);
+  const int cnt = max(0, c1 - c0);
+  const int tiles = (cnt + kDecTile - 1) / kDecTile;
+  // the newly complete blocks in this CTA's range (every row's CTAs pool them,
+  // writing identical keys, so the range is covered whatever each row sees)
+  const int pr0 = max(pa.first, c0);
+  const int pr1 = min(pa.first + pa.n, min(c0 + bpc, n_max));
   const int npool = max(0, pr1 - pr0);
-  const int c0_ = y * bpc;
-  const int cnt_ = max(0, min(n, c0_ + bpc) - c0_);
-  const bool overlap = npool > 0 && cnt_ > 0 && npool <= kDecPoolOverlap;
-  auto pool_one = [&](int b) {  // both half-warps of the calling warp call it
-    return pool_block_16(pa.keys + (int64_t)(b - pa.first) * kRatio * pa.key_stride,
-                         pa.key_stride, b, pa.k_norm_w, a.cos_t, a.sin_t, a.eps, lane & 15);
-  };
-  if (npool > 0 && !overlap) {
-    for (int j0 = 0; j0 < npool; j0 += kDecThreads / 16) {
-      const int j = j0 + (tid >> 4);
-      const uint4 key = pool_one(pr0 + min(j, npool - 1));
-      if (j < npool)
-        *reinterpret_cast<uint4 *>(pa.block_keys + (int64_t)(pr0 + j) * kHeadDim + 8 * (lane & 15)) = key;
+  const long long lim = a.wait_limit > 0 ? a.wait_limit : kDecSpinLimit;
+  volatile int32_t *abort_flag = &C.abort;
+  const uint32_t tmem = C.tmem_base;
+
+  if (warp == 0) {
+    // ---- TMA producer: every tile of the range, one stage each, issued before
+    // the position arrives (a row that sees fewer blocks ignores the rest)
+    if (lane == 0) {
+      const int ntiles = (max(0, min(bpc, n_max - c0)) + kDecTile - 1) / kDecTile;
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int32_t b0 = c0 + t * kDecTile;
+        const uint32_t fb = sm32(&C.full[t]);
+        mbar_expect_tx(fb, kDecTileBytes);
+        tma_load_2d(sRing + t * kDecTileBytes, &kmap, 0, b0, fb);
+        tma_load_2d(sRing + t * kDecTileBytes + kDecHalfBytes, &kmap, 64, b0, fb);
+        issued = t + 1;
+      }
+      C.issued = issued;
     }
-    __syncthreads();
-    // the bulk copies below read these keys through the async proxy
-    if (tid == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+  } else if (warp == 1) {
+    // ---- MMA issuer: tile t into accumulator t
+    if (lane == 0 && tiles > 0) {
+      bool ok = tc_wait(sm32(&C.qready), 0u, lim, abort_flag);
+      if (ok) tc_fence_after();
+      bool patched = npool == 0;
+      for (int t = 0; t < tiles && ok; ++t) {
+        if (!(ok = tc_wait(sm32(&C.full[t]), 0u, lim, abort_flag))) break;
+        const int32_t b0 = c0 + t * kDecTile;
+        if (!patched && b0 < pr1 && b0 + kDecTile > pr0) {  // the tile holds pooled blocks
+          if (!(ok = tc_wait(sm32(&C.pooled), 0u, kDecSpinLimit, abort_flag))) break;
+          patched = true;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t kin = (uint32_t)(kk & 3) * 32u;  // K step inside the 128-byte row
+          const uint64_t ad =
+              sw128_desc(sRing + t * kDecTileBytes + (uint32_t)(kk >> 2) * kDecHalfBytes + kin);
+          const uint64_t bd = sw128_desc(sQ + (uint32_t)(kk >> 2) * (kDecQBytes / 2) + kin);
+          mma_bf16(tmem + (uint32_t)(t * kDecN), ad, bd, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(sm32(&C.tfull[t]));
+      }
+      // every MMA this thread issued has finished before TMEM is freed
+      mma_commit(sm32(&C.drain));
+      tc_wait(sm32(&C.drain), 0u, kDecSpinLimit, nullptr);
+    }
+  } else if (warp < 4) {
+    // ---- warps 2-3: the query operand
+    const int h = (warp - 2) * 2 + (lane >> 4);  // head
+    const int g = lane & 15;                     // dims 8g .. 8g+7
+    const uint4 v = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * g);
+    const uint4 w8 = ldg_nc_v4(a.q_norm_w + 8 * g);
+    const int64_t pp = valid ? p : 0;  // (an invalid row's operand is never used)
+    uint4 c8 = make_uint4(0u, 0u, 0u, 0u), s8 = make_uint4(0u, 0u, 0u, 0u);
+    if (g < 8) {
+      c8 = ldg_nc_v4(a.cos_t + pp * kRot + 8 * g);
+      s8 = ldg_nc_v4(a.sin_t + pp * kRot + 8 * g);
+    }
+    float x[8];
+    unpack8(v, x);
+    const uint4 o = norm_rope_16(x, w8, c8, s8, a.eps, g);
+    // row h of the operand, 16-byte chunk g: 128-byte swizzle within its half
+    const int half = g >> 3, j = g & 7;
+    *reinterpret_cast<uint4 *>(smem + kDecQOff + half * (kDecQBytes / 2) + h * 128 +
+                               ((j ^ (h & 7)) << 4)) = o;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMAs
+    mbar_arrive(sm32(&C.qready));
+  } else {
+    // ---- warps 4-7, first: pool the newly complete blocks of the range (one per
+    // 16 lanes).  Their tile's copy may have read the old key, so a block
+    // this CTA scores is also written into its landed tile (the 128-byte
+    // swizzled row of the MMA operand) before the MMAs read it.
+    const int g = lane & 15;
+    for (int j0 = 0; j0 < npool; j0 += 8) {
+      const int jj = j0 + (warp - 4) * 2 + (lane >> 4);
+      const int b = pr0 + min(jj, npool - 1);
+      const uint4 key = pool_block_16(pa.keys + (int64_t)(b - pa.first) * kRatio * pa.key_stride,
+                                      pa.key_stride, b, pa.k_norm_w, a.cos_t, a.sin_t, a.eps, g);
+      if (jj < npool) {
+        *reinterpret_cast<uint4 *>(pa.block_keys + (int64_t)b * kHeadDim + 8 * g) = key;
+        const int t = (b - c0) / kDecTile, r = (b - c0) % kDecTile;
+        if (t < tiles && tc_wait(sm32(&C.full[t]), 0u, kDecSpinLimit, abort_flag)) {
+          const int half = g >> 3, j = g & 7;
+          *reinterpret_cast<uint4 *>(ring + t * kDecTileBytes + half * kDecHalfBytes + r * 128 +
+                                     ((j ^ (r & 7)) << 4)) = key;
+        }
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the patches, to the MMAs
+    mbar_arrive(sm32(&C.pooled));
+    // ---- then one TMEM lane quarter each, one block per lane
+    const int q = warp & 3;
+    const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
+    float *srow = a.scores + (int64_t)row * a.score_cols;
+    for (int t = 0; t < tiles; ++t) {
+      if (!tc_warp_wait(sm32(&C.tfull[t]), 0u, lim, abort_flag)) break;
+      tc_fence_after();
+      uint32_t v[4];
+      tmem_ld4(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(t * kDecN), v);
+      const float h0 = relu_nan(__uint_as_float(v[0]));
+      const float h1 = relu_nan(__uint_as_float(v[1]));
+      const float h2 = relu_nan(__uint_as_float(v[2]));
+      const float h3 = relu_nan(__uint_as_float(v[3]));
+      const float sc = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(h0, h1), h2), h3), inv_sqrt_hd);
+      const int bl = t * kDecTile + 32 * q + lane;
+      if (bl < cnt) {
+        sc_s[bl] = sc;
+        srow[c0 + bl] = sc;
+      }
+    }
   }
+
+  __syncthreads();  // scoring done or given up; every MMA has drained
+  if (tid == 0 && (C.issued > tiles || C.abort)) {
+    // let every copy this CTA issued land before its shared memory is reused
+    for (int t = 0; t < C.issued; ++t) tc_wait(sm32(&C.full[t]), 0u, kDecSpinLimit, nullptr);
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kDecTmemCols)
+                 : "memory");
+  }
+  __syncthreads();
   if (!valid) {  // uniform over the row's CTAs: nobody waits for them
     if (y == 0 && tid == 0) report_error(a.status, kErrRowRange, row);
     return;
+  }
+  if (C.abort) {
+    if (tid == 0) report_error(a.status, kErrTimeout, row);
+    return;  // the row's other CTAs time out at the barrier below
   }
   uint8_t *mrow = mask + (int64_t)row * a.tokens;
   uint8_t *wrow = ws + (int64_t)row * row_ws_bytes;
   RowHdr &W = *reinterpret_cast<RowHdr *>(wrow);
   uint32_t *cand_key = reinterpret_cast<uint32_t *>(wrow + sizeof(RowHdr));
   uint32_t *cand_idx = cand_key + (a.tokens >> 2);
-  const int c0 = y * bpc;
-  const int c1 = min(n, c0 + bpc);
-  const int cnt = max(0, c1 - c0);
-
-  // ---- 1. scores of this CTA's blocks
-  const int pj = (warp - 2) * 2 + (lane >> 4);  // warps 2..7: pooled block pr0 + pj
-  uint4 pooled = make_uint4(0u, 0u, 0u, 0u);
-  auto prologue = [&]() {
-    if (overlap && warp >= 2) {
-      pooled = pool_one(pr0 + min(pj, npool - 1));
-      if (pj < npool)
-        *reinterpret_cast<uint4 *>(pa.block_keys + (int64_t)(pr0 + pj) * kHeadDim + 8 * (lane & 15)) =
-            pooled;
-    }
-  };
-  auto patch = [&](int base, uint8_t *st) {  // the stage read the keys before pooling
-    if (overlap && pr0 < base + kSimtBlocksPerIter && pr1 > base) {
-      const int b = pr0 + pj;
-      if (warp >= 2 && pj < npool && b >= base && b < base + kSimtBlocksPerIter)
-        *reinterpret_cast<uint4 *>(st + (size_t)(b - base) * (kHeadDim * 2) + 16 * (lane & 15)) =
-            pooled;
-      __syncthreads();
-    }
-  };
-  if (cnt > 0 && !simt_score_blocks(a, row, p, c0, c1, S, ring,
-                                    [&](int b, float sc) { sc_s[b - c0] = sc; }, prologue, patch,
-                                    &qchunk)) {
-    if (tid == 0) report_error(a.status, kErrTimeout, row);
-    return;  // the row's other CTAs time out at the barrier below
-  }
   if (n <= keep_max) {  // every block kept: this CTA's share of the visible prefix
     const int64_t span = ((int64_t)a.tokens + ny - 1) / ny;
     const int64_t lo = (int64_t)y * span;
@@ -215,16 +493,16 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   my_max = __reduce_max_sync(0xffffffffu, my_max);
   my_low = __reduce_or_sync(0xffffffffu, my_low);
   if (lane == 0) {
-    atomicMax(&s_maxbin, my_max);
-    if (my_low) s_low = 1u;
+    atomicMax(&C.maxbin, my_max);
+    if (my_low) C.low = 1u;
   }
 
   // ---- 2. grid barrier over the row's CTAs
   __syncthreads();
   if (tid == 0) {
-    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(&W.maxbin[y & 7]), "r"(s_maxbin)
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(&W.maxbin[y & 7]), "r"(C.maxbin)
                  : "memory");
-    if (s_low) asm volatile("red.relaxed.gpu.global.or.b32 [%0], 1;" ::"l"(&W.lowbad) : "memory");
+    if (C.low) asm volatile("red.relaxed.gpu.global.or.b32 [%0], 1;" ::"l"(&W.lowbad) : "memory");
     // release: the CTA's histogram adds (ordered before it by the barrier
     // above) are visible to whoever sees the count
     red_add_release_gpu(&W.arrive, 1u);
@@ -267,20 +545,16 @@ decode_fused_kernel(const ScoreArgs a, int32_t keep_max, uint8_t *__restrict__ m
   const uint32_t wlo = D.rule_shift;
   auto fetch_hist = [&](uint32_t first, uint32_t nbins, uint32_t parity) {
     if (tid == 0) {
-      const uint32_t mb = simt_smem_u32(&S.full[0]);  // the ring's barriers are free again
-      if (parity == 0u) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mb) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-      }
+      const uint32_t mb = sm32(&C.hbar);
       asm volatile("fence.proxy.async.global;" ::: "memory");
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(4u * nbins)
                    : "memory");
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-              "r"(simt_smem_u32(D.hist0)),
+              "r"(sm32(D.hist0)),
           "l"(W.hist0 + first), "r"(4u * nbins), "r"(mb)
           : "memory");
-      D.flag = simt_wait(mb, parity) ? 1 : 0;
+      D.flag = tc_wait(mb, parity, kDecSpinLimit, nullptr) ? 1 : 0;
       D.sel_bin = -1;
     }
     __syncthreads();
@@ -525,16 +799,19 @@ cudaError_t launch_decode_fused(const ScoreArgs &a, int32_t budget, uint8_t *mas
   *launched = false;
   const int64_t n_max = (int64_t)a.tokens / kRatio;
   const int cap = dec_capacity();
-  if (n_max == 0 || cap <= 0) return cudaSuccess;
-  // the fewest blocks per CTA (128 .. 512) that keep every CTA co-resident
+  if (n_max == 0 || cap <= 0 || a.key_base != nullptr) return cudaSuccess;
+  // the fewest blocks per CTA (128 or 256) that keep every CTA co-resident
   int32_t bpc = 0;
-  for (int32_t k = kSimtBlocksPerIter; k <= kDecMaxBpc; k += kSimtBlocksPerIter) {
+  for (int32_t k = kDecTile; k <= kDecMaxBpc; k += kDecTile) {
     if ((int64_t)a.n_rows * ((n_max + k - 1) / k) <= cap && (n_max + k - 1) / k <= 65535) {
       bpc = k;
       break;
     }
   }
   if (bpc == 0) return cudaSuccess;  // too many rows: the caller takes the two-kernel path
+  CUtensorMap kmap;
+  if (!encode_bf16_sw128(&kmap, a.block_keys, kHeadDim, (uint64_t)n_max, kHeadDim, 64, kDecTile))
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -549,7 +826,7 @@ cudaError_t launch_decode_fused(const ScoreArgs &a, int32_t budget, uint8_t *mas
   cfg.numAttrs = 2;
   const PoolArgs pa{pool_keys, pool_key_stride, pool_first, pool_n, k_norm_w, block_keys};
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, decode_fused_kernel, a, budget / kRatio, mask,
+      cudaLaunchKernelEx(&cfg, decode_fused_kernel, kmap, a, budget / kRatio, mask,
                          static_cast<uint8_t *>(ws), decode_row_ws_bytes(a.tokens), bpc, pa);
   if (e == cudaSuccess) *launched = true;
   return e;

@@ -141,3 +141,18 @@ def long_keys_case(tokens=65536, seed_index=1, token_scale=True):
     qw, kw = qi.norm_weights(rng)
     q = qi.fused_qk(rng, 256)[:, :512]
     return dict(keys=keys, q_norm_w=qw, k_norm_w=kw, q=np.ascontiguousarray(q), tokens=tokens)
+
+
+def index_select_tc(qsa, keys, key_stride, first, count, k_norm_w, q, q_stride, pos, n_rows,
+                    tokens, q_norm_w, cos_t, sin_t, table_rows, eps, budget, block_keys, scores,
+                    score_cols, mask, status):
+    """qsa_index_select's three stages with the tensor-core scorer forced: the
+    same MMA per (block, head) as the fused decode kernel, so its scores must
+    equal that kernel's bit for bit."""
+    if count:
+        qsa.qsa_pool_blocks(keys, key_stride, first, count, k_norm_w, cos_t, sin_t, table_rows, eps,
+                            block_keys)
+    qsa.qsa_score_rows_with(q, q_stride, pos, None, n_rows, tokens, q_norm_w, cos_t, sin_t,
+                            table_rows, eps, block_keys, None, scores, score_cols, status,
+                            path=qsa.QSA_SCORE_TCGEN05, workspace=qsa.new_workspace(n_rows))
+    qsa.qsa_select_mask(scores, score_cols, pos, n_rows, tokens, budget, mask, status)

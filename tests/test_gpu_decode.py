@@ -1,11 +1,14 @@
 """qsa_decode_index_select: pooling, scoring and selection with the fused
-decode launch, against the oracle and against qsa_index_select.
+decode launch (one thread-block cluster per row), against the oracle and
+against the single-stage entry points.
 
-Its scores come from the same streaming scorer as qsa_index_select's SIMT path,
-so they must be bit-identical to that path's and within tolerance of the
-oracle's; its masks must equal, byte for byte, the oracle's selection over the
-GPU's own scores (selection is exact integer work on given scores).  The
-zeroed workspace must be zero again after every call that completes.
+Its scores come from the same tcgen05 MMA per (block, head) as the tensor-core
+scorer of qsa_score_rows_with, so they must equal that path's bit for bit (or,
+when the rows' CTAs cannot all be co-resident and the call falls back to the
+streaming scorer, that scorer's) and lie within tolerance of the oracle's; its
+masks must equal, byte for byte, the oracle's selection over the GPU's own
+scores (selection is exact integer work on given scores).  The zeroed
+workspace must be zero again after every call that completes.
 """
 import numpy as np
 import pytest
@@ -13,7 +16,8 @@ import torch
 
 import qsa_inputs as qi
 from qsa_cases import (BUDGET, EPS, THETA, assert_close, assert_masks_agree_up_to_tolerance,
-                       check_mask_structure, long_keys_case, oracle_masks, oracle_scores)
+                       check_mask_structure, index_select_tc, long_keys_case, oracle_masks,
+                       oracle_scores)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,12 +44,14 @@ def tables(qsa):
 
 def run_both(qsa, tables, cache_np, q_np, pos_np, tokens, cols, qw, budget=BUDGET, mask_offset=0,
              keys=None, pool=(0, 0), ws=None):
-    """One call of each entry point on identical inputs; returns (decode, plain)
-    outputs as host arrays plus the two status words and the workspace."""
+    """One call of the decode entry and of the two-kernel path with each scorer
+    on identical inputs; returns the decode outputs, the outputs of the
+    two-kernel path whose scores equal the decode call's (the tensor-core one
+    if neither does), and the workspace."""
     c, s, cd, sd = tables
     n_rows = len(pos_np)
     out = []
-    for entry in ("decode", "plain"):
+    for entry in ("decode", "tc", "simt"):
         cache = dev(cache_np.copy())
         sc = torch.full((n_rows, cols), -7.0, dtype=torch.float32, device="cuda")
         buf = torch.full((n_rows * tokens + mask_offset + 16,), 0xAB, dtype=torch.uint8,
@@ -60,6 +66,8 @@ def run_both(qsa, tables, cache_np, q_np, pos_np, tokens, cols, qw, budget=BUDGE
             if ws is None:
                 ws = qsa.new_decode_workspace(n_rows, tokens)
             qsa.qsa_decode_index_select(*args, ws)
+        elif entry == "tc":
+            index_select_tc(qsa, *args)
         else:
             qsa.qsa_index_select(*args)
         torch.cuda.synchronize()
@@ -67,7 +75,8 @@ def run_both(qsa, tables, cache_np, q_np, pos_np, tokens, cols, qw, budget=BUDGE
         assert np.all(g[:mask_offset] == 0xAB) and np.all(g[mask_offset + n_rows * tokens:] == 0xAB)
         out.append((sc.cpu().numpy(), mask.view(n_rows, tokens).cpu().numpy(),
                     qsa.qsa_read_status(st), cache.cpu().numpy().view(np.uint16)))
-    return out[0], out[1], ws
+    same = [o for o in out[1:] if np.array_equal(o[0], out[0][0])]
+    return out[0], (same[0] if same else out[1]), ws
 
 
 def test_decode_steps_match_oracle_and_two_kernel_path(qsa, orc, tables):
@@ -297,10 +306,10 @@ def test_decode_with_inputs_and_mask_in_pinned_host_memory(qsa, orc, tables):
 
 @pytest.mark.parametrize("first,count", [(16255, 2), (16300, 84), (16383, 1)])
 def test_decode_pools_new_blocks_in_the_same_launch(qsa, orc, tables, first, count):
-    """The fused launch pools the new blocks itself: a range straddling two CTAs
-    (each pools its share while its keys stream in), a range too long for that
-    (pooled before scoring), rows that see none of the new blocks; the cache,
-    scores and masks equal those of the separate pool kernel and the oracle."""
+    """The fused launch pools the new blocks itself: a range straddling two CTAs'
+    shares (each pools its own before its keys are copied), a long range, rows
+    that see none of the new blocks; the cache, scores and masks equal those of
+    the separate pool kernel and the oracle."""
     rng = qi.rng_for(1, salt=first)
     c, s, cd, sd = tables
     tokens = 65536
@@ -315,7 +324,7 @@ def test_decode_pools_new_blocks_in_the_same_launch(qsa, orc, tables, first, cou
     pos = np.array([last, 4 * first + 2, last - 1], np.int32)
     q_np = qi.normal_bf16(rng, (3, 512))
     outs = []
-    for entry in ("decode", "plain"):
+    for entry in ("decode", "tc", "simt"):
         cache = dev(cache_np)
         sc = torch.full((3, nb), -7.0, dtype=torch.float32, device="cuda")
         mask = torch.full((3, tokens), 0xAB, dtype=torch.uint8, device="cuda")
@@ -328,10 +337,14 @@ def test_decode_pools_new_blocks_in_the_same_launch(qsa, orc, tables, first, cou
             qsa.qsa_decode_index_select(*args, ws)
             torch.cuda.synchronize()
             assert int(ws.count_nonzero()) == 0
+        elif entry == "tc":
+            index_select_tc(qsa, *args)
         else:
             qsa.qsa_index_select(*args)
         assert qsa.qsa_read_status(st) == (0, 0)
         outs.append((cache.cpu().numpy().view(np.uint16), sc.cpu().numpy(), mask.cpu().numpy()))
+    same = [o for o in outs[1:] if np.array_equal(o[1], outs[0][1])]
+    outs = [outs[0], same[0] if same else outs[1]]
     top = first + count
     assert np.array_equal(outs[0][0][:top], keys_o[:top]), "pooled cache differs from the oracle"
     assert np.all(outs[0][0][top:] == 0x7FAB), "blocks past the new range were written"
@@ -366,3 +379,39 @@ def test_decode_keep_th_key_far_below_the_top(qsa, orc, tables):
     want, codes = oracle_masks(orc, dsc, nb, pos, tokens, BUDGET)
     assert all(c == 0 for c in codes)
     assert np.array_equal(dmask, want)
+
+
+def test_decode_long_rows_past_64k(qsa, orc):
+    """Two rows of a 270000-token context (67500 blocks): the fused launch, or
+    the two-kernel path when its CTAs do not fit, gives the results of one of
+    the library's two-kernel paths and the oracle's selection over its scores."""
+    tokens = 270000
+    nb = tokens // 4
+    c, s = qsa.qsa_rope_tables(tokens, THETA)
+    cd, sd = dev(c), dev(s)
+    rng = qi.rng_for(1, salt=270000)
+    cache_np = qi.normal_bf16(rng, (nb, 128))
+    q_np = qi.normal_bf16(rng, (2, 512))
+    qw, _ = qi.norm_weights(rng)
+    pos = np.array([tokens - 1, 100001], np.int32)
+    outs = []
+    for entry in ("decode", "tc", "simt"):
+        cache = dev(cache_np)
+        sc = torch.full((2, nb), -7.0, dtype=torch.float32, device="cuda")
+        mask = torch.full((2, tokens), 0xAB, dtype=torch.uint8, device="cuda")
+        st = qsa.new_status()
+        args = (cache, 128, 0, 0, dev(np.zeros(128, np.uint16)), dev(q_np), 512, dev(pos), 2,
+                tokens, dev(qw), cd, sd, tokens, EPS, BUDGET, cache, sc, nb, mask, st)
+        if entry == "decode":
+            qsa.qsa_decode_index_select(*args, qsa.new_decode_workspace(2, tokens))
+        elif entry == "tc":
+            index_select_tc(qsa, *args)
+        else:
+            qsa.qsa_index_select(*args)
+        assert qsa.qsa_read_status(st) == (0, 0)
+        outs.append((sc.cpu().numpy(), mask.cpu().numpy()))
+    same = [o for o in outs[1:] if np.array_equal(o[0], outs[0][0])]
+    assert same, "decode scores equal neither two-kernel path"
+    assert np.array_equal(outs[0][1], same[0][1])
+    want, codes = oracle_masks(orc, outs[0][0], nb, pos, tokens, BUDGET)
+    assert codes == [0, 0] and np.array_equal(outs[0][1], want)

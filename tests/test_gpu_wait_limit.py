@@ -4,10 +4,11 @@ PR #1178's review note on environment side effects: a deliberate trap left
 the GPU unusable, so every wait in this library is bounded and reports
 QSA_ERR_TIMEOUT in the status word instead of trapping.  Here the limit is cut
 to one SM cycle with qsa_set_wait_limit_cycles, so the fused decode step's
-barrier over a 64k row's CTAs gives up in every CTA that arrives before the
-last one.  The call must return, the status must be QSA_ERR_TIMEOUT for that
-row, and once the limit is restored and the workspace zeroed the next call
-must give the exact selection again.
+waits for its key copies, its MMAs and its grid barrier give up (the first
+test of each finds the copy, the MMA or the other CTAs still in flight).  The
+call must return, the status must be QSA_ERR_TIMEOUT for one of the rows, and
+once the limit is restored and the workspace zeroed the next call must give
+the exact selection again.
 """
 import numpy as np
 import pytest
@@ -56,7 +57,8 @@ def test_decode_barrier_runs_out_then_the_next_call_is_exact(orc):
     assert code == qsa.QSA_ERR_TIMEOUT, (code, row)
     assert row in (0, 1)
 
-    # the workspace may be dirty after an error: zero it, then the next call is exact
+    # the workspace may be dirty after an error: zero it; the next call, at the
+    # default limit, is exact
     ws.zero_()
     sc = torch.full((n_rows, nb), -7.0, dtype=torch.float32, device="cuda")
     mask = torch.full((n_rows, tokens), 0xAB, dtype=torch.uint8, device="cuda")

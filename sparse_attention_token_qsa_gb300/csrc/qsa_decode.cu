@@ -525,20 +525,31 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
 
   // ---- 3. the threshold bin, this CTA's mask bytes and candidates
   // A non-finite score lands above bin 0xFF7 (positive) or below bin 8
-  // (negative); every finite one between.  The row's histogram comes into
-  // shared memory by bulk copies (the copy engine reads global memory through
-  // the async proxy, so that proxy is fenced after the acquire that made the
-  // other CTAs' adds visible): first the kDecWindow bins ending at the row's
-  // highest one, then, only if they hold fewer than keep keys, all 4096.
-  if (tid == 0) {
-    uint32_t mx = 0u;
+  // (negative); every finite one between.  The row's highest bin is read
+  // beside a copy of the 512 bins ending 256 above this CTA's own highest one
+  // (a row's highest bin lies within that unless a few CTAs hold scores 2^32
+  // times the others'), so the kDecWindow bins ending at the row's highest one
+  // are usually in shared memory after one round trip.  Otherwise they come by
+  // a bulk copy (the copy engine reads global memory through the async proxy,
+  // so that proxy is fenced after the acquire that made the other CTAs' adds
+  // visible), and, only if they hold fewer than keep keys, all 4096 bins.
+  const uint32_t spec_lo = (uint32_t)min(max((int)C.maxbin + 256 - 511, 0), 4096 - 512);
+  {
+    const uint32_t v0 = __ldcg(&W.hist0[spec_lo + tid]);
+    const uint32_t v1 = __ldcg(&W.hist0[spec_lo + 256 + tid]);
+    if (tid == 0) {
+      uint32_t mx = 0u;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) mx = max(mx, __ldcg(&W.maxbin[k]));
-    const bool nf = __ldcg(&W.lowbad) != 0u || mx >= 0xFF8u;
-    D.rule_prefix = nf ? 1u : 0u;  // (scratch: the non-finite verdict)
-    // window start: 16-byte aligned, rounded up so the highest bin stays inside
-    // (mx <= 0xFF7 for a finite row, so the window ends inside the histogram)
-    D.rule_shift = ((uint32_t)max(0, (int)mx + 1 - kDecWindow) + 3u) & ~3u;
+      for (int k = 0; k < 8; ++k) mx = max(mx, __ldcg(&W.maxbin[k]));
+      const bool nf = __ldcg(&W.lowbad) != 0u || mx >= 0xFF8u;
+      D.rule_prefix = nf ? 1u : 0u;  // (scratch: the non-finite verdict)
+      // window start: 16-byte aligned, rounded up so the highest bin stays inside
+      // (mx <= 0xFF7 for a finite row, so the window ends inside the histogram)
+      D.rule_shift = ((uint32_t)max(0, (int)mx + 1 - kDecWindow) + 3u) & ~3u;
+      D.sel_bin = -1;
+    }
+    D.hist0[tid] = v0;
+    D.hist0[256 + tid] = v1;
   }
   __syncthreads();
   const bool bad = D.rule_prefix != 0u;
@@ -561,21 +572,33 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     return D.flag != 0;
   };
   uint32_t need = (uint32_t)min(keep_max, n);
-  uint32_t hbase = wlo;  // D.hist0[i] holds bin hbase + i
+  uint32_t hbase = spec_lo;  // D.hist0[i] holds bin hbase + i
+  int32_t sel = -1;          // the bin holding the need-th key, relative to hbase
   if (!bad) {
-    if (!fetch_hist(wlo, kDecWindow, 0u)) {
-      if (tid == 0) report_error(a.status, kErrTimeout, row);
-      return;
+    if (wlo >= spec_lo && wlo + kDecWindow <= spec_lo + 512) {
+      find_bin<kDecThreads>(D.hist0 + (wlo - spec_lo), kDecWindow, need, D.warp_tot, &D.sel_bin,
+                            &D.sel_above);
+      sel = D.sel_bin < 0 ? -1 : D.sel_bin + (int32_t)(wlo - spec_lo);
+      __syncthreads();  // every thread has read sel_bin
     }
-    find_bin<kDecThreads>(D.hist0, kDecWindow, need, D.warp_tot, &D.sel_bin, &D.sel_above);
-    if (D.sel_bin < 0) {  // the keep-th key lies below the window
-      __syncthreads();    // every thread has read sel_bin
-      hbase = 0u;
-      if (!fetch_hist(0u, 4096u, 1u)) {
+    if (sel < 0) {
+      hbase = wlo;
+      if (!fetch_hist(wlo, kDecWindow, 0u)) {
         if (tid == 0) report_error(a.status, kErrTimeout, row);
         return;
       }
-      find_bin<kDecThreads>(D.hist0, 4096, need, D.warp_tot, &D.sel_bin, &D.sel_above);
+      find_bin<kDecThreads>(D.hist0, kDecWindow, need, D.warp_tot, &D.sel_bin, &D.sel_above);
+      sel = D.sel_bin;
+      if (sel < 0) {        // the keep-th key lies below the window
+        __syncthreads();    // every thread has read sel_bin
+        hbase = 0u;
+        if (!fetch_hist(0u, 4096u, 1u)) {
+          if (tid == 0) report_error(a.status, kErrTimeout, row);
+          return;
+        }
+        find_bin<kDecThreads>(D.hist0, 4096, need, D.warp_tot, &D.sel_bin, &D.sel_above);
+        sel = D.sel_bin;
+      }
     }
   }
   uint32_t B0 = 0;
@@ -583,7 +606,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   if (bad) {
     if (y == 0 && tid == 0) report_error(a.status, kErrNonFinite, row);
   } else {
-    B0 = hbase + (uint32_t)D.sel_bin;
+    B0 = hbase + (uint32_t)sel;
     need -= D.sel_above;
     whole = D.hist0[B0 - hbase] == need;
     const uintptr_t rb = reinterpret_cast<uintptr_t>(mrow);

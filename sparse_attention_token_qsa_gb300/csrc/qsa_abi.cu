@@ -161,6 +161,22 @@ int64_t qsa_score_workspace_bytes(int32_t n_rows) {
   return n_rows < 0 ? -1 : (int64_t)n_rows * 4 * kHeadDim * 2;
 }
 
+namespace {
+
+// A caller workspace the tensor-core scorer can use for n_rows query rows.
+bool score_ws_ok(const void *workspace, int64_t workspace_bytes, int32_t n_rows) {
+  return workspace != nullptr && aligned16(workspace) &&
+         workspace_bytes >= qsa_score_workspace_bytes(n_rows) && (int64_t)n_rows * 4 <= INT32_MAX;
+}
+
+// QSA_SCORE_AUTO's choice: the tensor-core scorer once there are enough rows
+// to fill its 64-row tiles and blocks to fill a key tile, else streaming.
+bool auto_picks_tc(const int64_t *key_base, bool ws_ok, int32_t n_rows, int32_t tokens) {
+  return qsa::kTcScorerReady && key_base == nullptr && ws_ok && n_rows >= 64 && tokens >= 2048;
+}
+
+}  // namespace
+
 qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_t *pos,
                                const int32_t *visible_len, int32_t n_rows, int32_t tokens,
                                const uint16_t *q_norm_w, const uint16_t *cos_t,
@@ -175,17 +191,13 @@ qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_
   qsa_status st = check_score_args(q, q_stride, pos, n_rows, tokens, q_norm_w, cos_t, sin_t,
                                    table_rows, eps, block_keys, scores, score_cols);
   if (st != QSA_OK || n_rows == 0 || tokens == 0) return st;
-  const bool ws_ok = workspace != nullptr && aligned16(workspace) &&
-                     workspace_bytes >= qsa_score_workspace_bytes(n_rows) &&
-                     (int64_t)n_rows * 4 <= INT32_MAX;
+  const bool ws_ok = score_ws_ok(workspace, workspace_bytes, n_rows);
   if (path == QSA_SCORE_TCGEN05 && (key_base != nullptr || !ws_ok)) return QSA_ERR_INVALID_VALUE;
   qsa::ScoreArgs a{q,          q_stride, pos,   visible_len, n_rows,     tokens,
                    q_norm_w,   cos_t,    sin_t, eps,         block_keys, key_base,
                    scores,     score_cols, dev_status, qsa::wait_limit_cycles()};
   if (path == QSA_SCORE_AUTO)
-    path = (qsa::kTcScorerReady && key_base == nullptr && ws_ok && n_rows >= 64 && tokens >= 2048)
-               ? QSA_SCORE_TCGEN05
-               : QSA_SCORE_SIMT;
+    path = auto_picks_tc(key_base, ws_ok, n_rows, tokens) ? QSA_SCORE_TCGEN05 : QSA_SCORE_SIMT;
   if (path == QSA_SCORE_TCGEN05)
     return from_cuda(qsa::launch_score_tc(a, static_cast<uint16_t *>(workspace), (cudaStream_t)stream));
   return from_cuda(qsa::launch_score_simt(a, (cudaStream_t)stream));
@@ -231,15 +243,27 @@ qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t po
   if (st != QSA_OK) return st;
   if (workspace_bytes < 0) return QSA_ERR_INVALID_VALUE;
   cudaStream_t s = (cudaStream_t)stream;
-  if (pool_n_blocks > 0) {
+  // on the tensor-core path the new blocks are pooled by the query-prep launch
+  const bool tc = n_rows > 0 && tokens > 0 &&
+                  auto_picks_tc(nullptr, score_ws_ok(workspace, workspace_bytes, n_rows), n_rows,
+                                tokens);
+  if (pool_n_blocks > 0 && !tc) {
     st = from_cuda(qsa::launch_pool_blocks(keys, key_stride, pool_first_block, pool_n_blocks,
                                            k_norm_w, cos_t, sin_t, eps, block_keys, s));
     if (st != QSA_OK) return st;
   }
   if (n_rows == 0 || tokens == 0) return QSA_OK;
-  st = qsa_score_rows_with(q, q_stride, pos, nullptr, n_rows, tokens, q_norm_w, cos_t, sin_t,
-                           table_rows, eps, block_keys, nullptr, scores, score_cols, dev_status,
-                           QSA_SCORE_AUTO, workspace, workspace_bytes, stream);
+  if (tc) {
+    const qsa::ScoreArgs a{q,          q_stride, pos,   nullptr, n_rows,     tokens,
+                           q_norm_w,   cos_t,    sin_t, eps,     block_keys, nullptr,
+                           scores,     score_cols, dev_status, qsa::wait_limit_cycles()};
+    const qsa::PoolArgs pa{keys, key_stride, pool_first_block, pool_n_blocks, k_norm_w, block_keys};
+    st = from_cuda(qsa::launch_score_tc(a, static_cast<uint16_t *>(workspace), s, &pa));
+  } else {
+    st = qsa_score_rows_with(q, q_stride, pos, nullptr, n_rows, tokens, q_norm_w, cos_t, sin_t,
+                             table_rows, eps, block_keys, nullptr, scores, score_cols, dev_status,
+                             QSA_SCORE_AUTO, workspace, workspace_bytes, stream);
+  }
   if (st != QSA_OK) return st;
   return from_cuda(qsa::launch_select(scores, score_cols, pos, n_rows, tokens, budget, mask,
                                       dev_status, s));

@@ -261,14 +261,6 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
   return v;
 }
 
-struct PoolArgs {         // newly complete blocks to pool in the same launch
-  const uint16_t *keys;  // token 4 * first's raw key
-  int64_t key_stride;
-  int32_t first, n;      // blocks [first, first + n); n = 0: none
-  const uint16_t *k_norm_w;
-  uint16_t *block_keys;  // the scorer's block-key cache, written here
-};
-
 __global__ void __launch_bounds__(kDecThreads)
 decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a, int32_t keep_max,
                     uint8_t *__restrict__ mask, uint8_t *__restrict__ ws, int64_t row_ws_bytes,

@@ -174,15 +174,39 @@ __device__ __forceinline__ uint4 pool_block_16(const uint16_t *tok0, int64_t key
   unpack8(t1, bb);
   unpack8(t2, c);
   unpack8(t3, d);
+  // The mean needs the exact sum of the 4 bf16 values rounded once to f32.
+  // When the smallest magnitude of a dim's four is at least 2^-14 of the
+  // largest (their exponents at most 14 apart) and the largest is below 2^125,
+  // every partial sum is a multiple of the smallest value's bf16 quantum below
+  // 2^24 quanta, so plain f32 additions are exact; a warp whose lanes all meet
+  // that takes them, any other the TwoSum cascade (same result).  A zero sum
+  // is +0 on both (the plain one adds +0 last: four -0 keys sum to +0, as the
+  // exact definition, which starts from +0, gives).
+  bool plain = true;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    // exact sum of the 4 bf16 values, rounded once to f32 (TwoSum cascade)
-    float s1, e1, s2, e2, s3, e3;
-    two_sum(a[e], bb[e], s1, e1);
-    two_sum(s1, c[e], s2, e2);
-    two_sum(s2, d[e], s3, e3);
-    const float sum = __fadd_rn(s3, __fadd_rn(__fadd_rn(e1, e2), e3));
-    m[e] = round_bf16(__fmul_rn(sum, 0.25f));  // f32 mean, cast back to bf16
+    const float hi = fmaxf(fmaxf(fabsf(a[e]), fabsf(bb[e])), fmaxf(fabsf(c[e]), fabsf(d[e])));
+    const float lo = fminf(fminf(fabsf(a[e]), fabsf(bb[e])), fminf(fabsf(c[e]), fabsf(d[e])));
+    plain = plain && hi < 0x1p125f && __fmul_rn(lo, 16384.0f) >= hi;
+  }
+  if (__all_sync(0xffffffffu, plain)) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float sum =
+          __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(a[e], bb[e]), c[e]), d[e]), 0.0f);
+      m[e] = round_bf16(__fmul_rn(sum, 0.25f));  // f32 mean, cast back to bf16
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      // exact sum of the 4 bf16 values, rounded once to f32 (TwoSum cascade)
+      float s1, e1, s2, e2, s3, e3;
+      two_sum(a[e], bb[e], s1, e1);
+      two_sum(s1, c[e], s2, e2);
+      two_sum(s2, d[e], s3, e3);
+      const float sum = __fadd_rn(s3, __fadd_rn(__fadd_rn(e1, e2), e3));
+      m[e] = round_bf16(__fmul_rn(sum, 0.25f));  // f32 mean, cast back to bf16
+    }
   }
   return norm_rope_16(m, w8, c8, s8, eps, g);
 }

@@ -43,6 +43,16 @@ cudaError_t launch_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t
                                const uint16_t *sin_t, float eps, uint16_t *block_keys,
                                cudaStream_t stream);
 
+// Newly complete blocks that a scoring launch pools itself, before any of
+// their keys are read (the cos/sin tables and eps are the scorer's).
+struct PoolArgs {
+  const uint16_t *keys;  // token 4 * first's raw key
+  int64_t key_stride;
+  int32_t first, n;      // blocks [first, first + n); n = 0: none
+  const uint16_t *k_norm_w;
+  uint16_t *block_keys;  // the scorer's block-key cache, written here
+};
+
 struct ScoreArgs {
   const uint16_t *q;
   int64_t q_stride;
@@ -69,10 +79,14 @@ struct ScoreArgs {
 long long wait_limit_cycles();
 
 cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream);
-// Prepared query heads, [n_rows * 4, 128] bf16, into a workspace.
-cudaError_t launch_qprep(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream);
-// Tensor-core scorer; qws is a workspace of n_rows * 1024 bytes (16-byte aligned).
-cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream);
+// Prepared query heads, [n_rows * 4, 128] bf16, into a workspace; the same
+// launch pools `pool`'s blocks when it is given (its own CTAs).
+cudaError_t launch_qprep(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream,
+                         const PoolArgs *pool = nullptr);
+// Tensor-core scorer; qws is a workspace of n_rows * 1024 bytes (16-byte
+// aligned).  `pool`'s blocks are pooled by the query-prep launch in front of it.
+cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream,
+                            const PoolArgs *pool = nullptr);
 extern const bool kTcScorerReady;
 
 // Fused decode step (pool the given new blocks, score, select: one

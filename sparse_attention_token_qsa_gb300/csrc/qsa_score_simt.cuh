@@ -49,13 +49,24 @@ __device__ __forceinline__ uint32_t simt_smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Bounded wait on an mbarrier phase (the thread sleeps in hardware between
-// tests).  Returns false once `limit` cycles have passed.
+// Bounded wait on an mbarrier phase: a non-blocking test, then the limit,
+// then a test that may sleep in hardware until the phase completes.  Returns
+// false once `limit` cycles have passed (a phase still open at the first test
+// with a limit of a few cycles gives up at once).
 __device__ __forceinline__ bool simt_wait(uint32_t mbar, uint32_t parity,
                                           long long limit = kSimtSpinLimit) {
   const long long t0 = clock64();
   while (true) {
     uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > limit) return false;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
@@ -64,7 +75,6 @@ __device__ __forceinline__ bool simt_wait(uint32_t mbar, uint32_t parity,
         : "r"(mbar), "r"(parity), "r"(20000u)
         : "memory");
     if (ok) return true;
-    if (clock64() - t0 > limit) return false;
   }
 }
 

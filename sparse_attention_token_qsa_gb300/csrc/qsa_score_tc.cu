@@ -501,9 +501,14 @@ EncodeTiledFn encoder() {
 
 }  // namespace
 
-cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream) {
+cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream,
+                            const PoolArgs *pool) {
   const int64_t n_cap = (int64_t)a.tokens / kRatio;  // no row sees more blocks than this
-  if (n_cap == 0 || a.n_rows == 0) return cudaSuccess;
+  if (n_cap == 0 || a.n_rows == 0) {
+    if (pool == nullptr || pool->n == 0) return cudaSuccess;
+    return launch_pool_blocks(pool->keys, pool->key_stride, pool->first, pool->n, pool->k_norm_w,
+                              a.cos_t, a.sin_t, a.eps, pool->block_keys, stream);
+  }
   if ((int64_t)a.n_rows * kHeads > INT32_MAX) return cudaErrorInvalidValue;
   EncodeTiledFn enc = encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -533,7 +538,7 @@ cudaError_t launch_score_tc(const ScoreArgs &a, uint16_t *qws, cudaStream_t stre
   static PerDevice smem_attr;
   cudaError_t e = set_smem_once(smem_attr, score_tc_kernel, kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = launch_qprep(a, qws, stream);
+  e = launch_qprep(a, qws, stream, pool);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM, each taking a balanced contiguous range of
   // (row tile, block tile) units; more than kMaxRowTiles row tiles go in slabs,

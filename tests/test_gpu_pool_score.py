@@ -371,3 +371,53 @@ def test_score_one_hot_queries_rotate_at_their_positions(qsa, orc, tables, path)
         assert rc == 0
         assert_close(got, want, f"one-hot query scores, dim {i}", atol=0, rtol=1e-6)
         assert np.all(got[:, 2:] == -7.0)
+
+
+def _bf16_bits(x):
+    """bf16 bits of float32 values that bf16 represents exactly."""
+    b = np.ascontiguousarray(x, np.float32).view(np.uint32)
+    assert np.all(b & 0xFFFF == 0), "value not representable in bf16"
+    return (b >> 16).astype(np.uint16)
+
+
+def special_sum_keys(n_blocks=4096, seed=11):
+    """Raw keys whose 4-token sums exercise both ways the pool kernel forms the
+    exact sum: plain f32 adds when a dim's four magnitudes lie within 2^14 of
+    each other and below 2^125, the TwoSum cascade otherwise.  Block kinds
+    cycle with the block index, so a warp (two blocks) mixes kinds; per-dim
+    draws make some warps take the plain adds and others not."""
+    rng = np.random.default_rng(seed)
+    q = lambda v: (np.asarray(v, np.float32).view(np.uint32) & 0xFFFF0000).view(np.float32)
+    out = np.empty((n_blocks * 4, 128), np.float32)
+    for b in range(n_blocks):
+        kind = b % 8      # a warp pools blocks 2w and 2w + 1: kinds (0,1) (2,3) (4,5) (6,7)
+        if kind in (0, 5):  # ordinary values
+            v = rng.standard_normal((4, 128))
+        elif kind == 1:    # magnitudes exactly 2^14 apart: the plain adds' edge, still exact
+            e = rng.integers(-20, 20, (1, 128))
+            v = np.ldexp(1.0, e) * np.array([[1.0], [2.0 ** -14], [-1.0], [2.0 ** -7]])
+        elif kind == 2:    # signed zeros only (the sum is +0)
+            v = np.where(rng.random((4, 128)) < 0.5, -0.0, 0.0)
+        elif kind == 3:    # bf16 subnormals next to small normals
+            v = np.ldexp(rng.integers(1, 128, (4, 128)).astype(np.float64), -133)
+            v[0] *= np.where(rng.random(128) < 0.5, 1, 2 ** 6)
+        elif kind == 4:    # large (squares still finite in f32), cancelling
+            v = np.ldexp(rng.choice([1.0, -1.0, 1.5, -1.25], (4, 128)), rng.integers(50, 60, (4, 128)))
+        elif kind == 6:    # 2^23 apart: TwoSum, where plain f32 adds would round
+            e = rng.integers(-20, 20, (1, 128))
+            v = np.ldexp(1.0, e) * np.array([[1.0], [2.0 ** -23 * 1.0078125], [1.0], [2.0 ** -31]])
+        else:              # wide random exponents, one zero
+            v = np.ldexp(rng.standard_normal((4, 128)), rng.integers(-30, 30, (4, 128)))
+            v[rng.integers(0, 4)] = 0.0
+        out[4 * b:4 * b + 4] = q(v)
+    return _bf16_bits(out)
+
+
+def test_pool_sum_paths_bit_exact(qsa, orc, tables):
+    keys = special_sum_keys()
+    nb = keys.shape[0] // 4
+    c, s, _, _ = tables
+    kw = qi.norm_weights(qi.rng_for(3))[1]
+    got = gpu_pool(qsa, tables, dev(keys).view(-1), 128, 0, nb, kw, nb)
+    want = orc.pool_blocks(keys, 128, 0, nb, kw, c, s, EPS)
+    assert np.array_equal(got, want), f"{int(np.sum(got != want))} pooled values differ"

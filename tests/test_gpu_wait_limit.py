@@ -14,7 +14,8 @@ import numpy as np
 import pytest
 import torch
 
-from qsa_cases import BUDGET, EPS, THETA, check_mask_structure, long_keys_case, oracle_masks
+from qsa_cases import (BUDGET, EPS, THETA, assert_close, check_mask_structure, long_keys_case,
+                       oracle_masks, oracle_scores)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,3 +73,58 @@ def test_decode_barrier_runs_out_then_the_next_call_is_exact(orc):
     for i, p in enumerate(pos_np):
         check_mask_structure(got[i], int(p), tokens, BUDGET)
         assert np.array_equal(got[i], want[i]), f"row {i}"
+
+
+def test_streaming_scorer_ring_wait_runs_out_then_the_next_call_is_exact(orc):
+    """The streaming scorer's wait for each landed stage of its key ring takes
+    the same limit.  64 rows of 64k, each over its own 4 MiB of block keys
+    (256 MiB in all, twice L2), keep the kernel bound by its copies, so its
+    consumers find stages still in flight; cut to one cycle, such a wait gives
+    up, the CTA drains its own copies and records QSA_ERR_TIMEOUT.  Restored,
+    the same call writes the same scores as before the cut."""
+    import sparse_attention_token_qsa_gb300 as qsa
+    import qsa_inputs as qi
+
+    tokens = 65536
+    nb = tokens // 4
+    n_rows = 64
+    case = long_keys_case()
+    c, s = qsa.qsa_rope_tables(tokens, THETA)
+    keys = qi.torch_normal_bf16(torch, (n_rows * nb, 128), 21, "cuda")
+    base_np = (np.arange(n_rows, dtype=np.int64) * nb)
+    pos_np = (65535 - 97 * np.arange(n_rows)).astype(np.int32)
+    head = (dev(case["q"][:n_rows]), 512, dev(pos_np), None, n_rows, tokens,
+            dev(case["q_norm_w"]), dev(c), dev(s), tokens, EPS, keys, dev(base_np))
+
+    def run():
+        sc = torch.full((n_rows, nb), -7.0, dtype=torch.float32, device="cuda")
+        st = qsa.new_status()
+        qsa.qsa_score_rows_with(*head, sc, nb, st, path=qsa.QSA_SCORE_SIMT)
+        return sc, qsa.qsa_read_status(st)
+
+    before, status = run()
+    assert status == (0, 0)
+
+    default = qsa.qsa_wait_limit_cycles()
+    qsa.qsa_set_wait_limit_cycles(1)
+    try:
+        _, (code, row) = run()
+    finally:
+        qsa.qsa_set_wait_limit_cycles(default)
+    assert qsa.qsa_wait_limit_cycles() == default
+    assert code == qsa.QSA_ERR_TIMEOUT, (code, row)
+    assert 0 <= row < n_rows
+
+    after, status = run()
+    assert status == (0, 0)
+    assert torch.equal(after, before)
+    # and the restored call's scores are the oracle's, within the score tolerance
+    got = after.cpu().numpy()
+    for i in (0, 31, 63):
+        kh = keys[i * nb:(i + 1) * nb].cpu().numpy().view(np.uint16)
+        want, res = oracle_scores(orc, np.ascontiguousarray(case["q"][i:i + 1]), 512,
+                                  pos_np[i:i + 1], tokens, case["q_norm_w"], c, s, kh, nb)
+        assert all(rc == 0 for rc, _ in res)
+        nv = (int(pos_np[i]) + 1) // 4
+        assert np.all(got[i, nv:] == -7.0)
+        assert_close(got[i, :nv], want[0, :nv], f"row {i}")

@@ -271,24 +271,29 @@ qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t po
 
 /*
  * Bytes of the workspace qsa_decode_index_select needs: per row, a 4096-bin
- * histogram, three counters and room for tokens/4 candidates.  -1 for
+ * histogram, a few counters and room for tokens/4 candidates.  -1 for
  * negative arguments.
  */
 int64_t qsa_decode_workspace_bytes(int32_t n_rows, int32_t tokens);
 
 /*
  * The same operation as qsa_index_select (pool the newly complete blocks,
- * score every row with the streaming scorer, select), for decode-sized row
- * counts, as ONE cooperative launch: the CTAs whose block ranges hold new
- * blocks pool them while their keys stream in, each row's scoring CTAs build
- * the row's histogram, meet at a bounded grid barrier and write their own
- * blocks' mask bytes, and the row's last CTA resolves the threshold bin.
- * (New blocks at or past tokens/4 are pooled by a separate launch first.)  Source: metrale
- * layers/qsa.rs decode_select (score then top-k each decode step), PR #1160
- * (scores), PR #1178 "Exact semantics" (selection).  Results equal those of
- * qsa_index_select with the SIMT scorer.  When the rows' CTAs cannot all be
- * resident at once, the call falls back to the scorer and the selector as two
- * launches (same results; the workspace is not used).
+ * score every row, select), for decode-sized row counts, as ONE cooperative
+ * launch: each CTA copies a 128-block tile of a row's keys with TMA and
+ * scores it on the tensor cores (the CTAs whose ranges hold new blocks pool
+ * them while the tile lands), the row's CTAs build its histogram, meet at a
+ * bounded grid barrier, find the bin of the keep-th key, write their own
+ * blocks' mask bytes and list that bin's keys; the row's last CTA clears the
+ * workspace and resolves the listed keys.  (New blocks at or past tokens/4
+ * are pooled by a separate launch first.)  Source: metrale layers/qsa.rs
+ * decode_select (score then top-k each decode step), PR #1160 (scores),
+ * PR #1178 "Exact semantics" (selection).
+ * The scores equal those of qsa_index_select's tensor-core scorer (same MMA
+ * shape and accumulation order) and the mask is the selector's on them.
+ * When the rows' CTAs cannot all be resident at once, the call falls back to
+ * the streaming scorer and the selector as two launches (the workspace is not
+ * used; scores within the scoring tolerance of the tensor-core ones, the
+ * mask exact on them).
  *  arguments   as qsa_index_select, except:
  *  decode_ws   DEVICE workspace of at least qsa_decode_workspace_bytes(n_rows,
  *              tokens) bytes, 16-byte aligned, ZERO before the first call.

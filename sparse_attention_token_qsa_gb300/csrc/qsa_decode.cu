@@ -24,8 +24,8 @@
 //     accumulators (one block per TMEM lane, its four heads in four columns),
 //     apply relu, the head sum in order 0..3 and the scale, and keep the
 //     scores in shared memory;
-//  2. each CTA adds its scores' top-12-bit order-key histogram into the row's
-//     workspace (one add per distinct bin per warp);
+//  2. the epilogue warps add each score's top-12-bit order-key bin into the
+//     row's histogram in the workspace (one add per distinct bin per warp);
 //  3. the row's CTAs meet at a grid barrier (the launch is cooperative, so
 //     they are co-resident; the wait is bounded);
 //  4. every CTA reads the row's histogram, finds the bin holding the keep-th
@@ -38,10 +38,11 @@
 //     exact ties at the final key by radix rounds on the block index (lowest
 //     kept), and writes the kept candidates' mask bytes.
 //
-// Workspace per row: the 4096-bin histogram, three counters, and room for
-// tokens / 4 candidates (key, block index).  It must be zero before the first
-// call; every call that completes leaves it zero.  A call that reports an
-// error may leave it dirty: zero it again before the next call.
+// Workspace per row: the 4096-bin histogram (interleaved over L2 lines, see
+// hist_slot), a few counters, and room for tokens / 4 candidates (key, block
+// index).  It must be zero before the first call; every call that completes
+// leaves it zero.  A call that reports an error may leave it dirty: zero it
+// again before the next call.
 #include "qsa_device.cuh"
 #include "qsa_launch.h"
 #include "qsa_select_util.cuh"
@@ -67,7 +68,7 @@ constexpr uint32_t kDecIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                ((uint32_t)(kDecN >> 3) << 17) | ((uint32_t)(kDecTile >> 4) << 24);
 
 struct RowHdr {  // per row, at the start of the row's workspace
-  uint32_t hist0[4096];
+  uint32_t hist0[4096];  // bin b's count at hist_slot(b)
   uint32_t arrive;  // CTAs whose histogram is in
   uint32_t pad0;
   // candidates listed (low 32 bits) and CTAs done writing their blocks (high
@@ -78,6 +79,15 @@ struct RowHdr {  // per row, at the start of the row's workspace
   uint32_t pad[51];
 };
 static_assert(sizeof(RowHdr) == 16640, "the workspace layout is part of the ABI");
+
+// A row's scores crowd into a few dozen neighbouring bins, and every CTA of the
+// row adds into them.  Bins go in runs of eight (one 32-byte sector), and run
+// r sits in 128-byte line r mod 128 (sector r / 128 of it): neighbouring runs
+// lie in different lines, so the adds spread over a dozen lines rather than
+// queue on three, while a read of consecutive bins still uses whole sectors.
+__device__ __forceinline__ uint32_t hist_slot(uint32_t bin) {
+  return (((bin >> 3) & 127u) << 5) | ((bin >> 10) << 3) | (bin & 7u);
+}
 
 // Keys of the keep-th largest score and everything above it sit in the top few
 // dozen bins of a row's histogram, so each CTA first reads only this many bins
@@ -117,7 +127,6 @@ struct DecCtrl {
   uint64_t qready;
   uint64_t pooled;
   uint64_t drain;
-  uint64_t hbar;         // the histogram copies of the selection
   uint32_t tmem_base;
   int32_t abort;
   int32_t issued;        // key tiles the producer issued
@@ -245,12 +254,6 @@ __device__ __forceinline__ float relu_nan(float d) {
   return r;
 }
 
-// The row's selection across the cluster (every CTA calls it; the row has
-// more blocks than keep_max and every CTA's scores and level-1 counts h1 are
-// in place).  Levels of 12, 8, 8 and 4 order-key bits; at each, every CTA
-// adds its counts of the keys in the current bin into the owners' slices of
-// the cluster's histogram, and after one cluster barrier reads the sums back
-// and finds the bin of the need-th key.  Writes this CTA's mask bytes.
 __device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -289,7 +292,6 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     mbar_init(sm32(&C.qready), 64);  // the query-prep threads
     mbar_init(sm32(&C.pooled), 128);  // the epilogue threads, once they have pooled
     mbar_init(sm32(&C.drain), 1);
-    mbar_init(sm32(&C.hbar), 1);
     C.abort = 0;
     C.issued = 0;
     C.maxbin = 0u;
@@ -309,12 +311,28 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   tc_fence_after();
   grid_dependency_sync();
 
-  // the position is read by every role; only the key copies start without it
+  const int32_t n_max = a.tokens >> 2;
+  const int c0 = y * bpc;
+  if (warp == 0 && lane == 0) {
+    // ---- TMA producer: every tile of the range, one stage each, issued before
+    // the position is read (a row that sees fewer blocks ignores the rest)
+    const int ntiles = (max(0, min(bpc, n_max - c0)) + kDecTile - 1) / kDecTile;
+    int issued = 0;
+    for (int t = 0; t < ntiles; ++t) {
+      const int32_t b0 = c0 + t * kDecTile;
+      const uint32_t fb = sm32(&C.full[t]);
+      mbar_expect_tx(fb, kDecTileBytes);
+      tma_load_2d(sRing + t * kDecTileBytes, &kmap, 0, b0, fb);
+      tma_load_2d(sRing + t * kDecTileBytes + kDecHalfBytes, &kmap, 64, b0, fb);
+      issued = t + 1;
+    }
+    C.issued = issued;
+  }
+
+  // the position is read by every other role
   const int32_t p = a.pos[row];
   const bool valid = p >= 0 && p < a.tokens;
   const int32_t n = valid ? (p + 1) >> 2 : 0;
-  const int32_t n_max = a.tokens >> 2;
-  const int c0 = y * bpc;
   const int c1 = min(n, c0 + bpc);
   const int cnt = max(0, c1 - c0);
   const int tiles = (cnt + kDecTile - 1) / kDecTile;
@@ -326,23 +344,11 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   const long long lim = a.wait_limit > 0 ? a.wait_limit : kDecSpinLimit;
   volatile int32_t *abort_flag = &C.abort;
   const uint32_t tmem = C.tmem_base;
+  uint8_t *wrow = ws + (int64_t)row * row_ws_bytes;
+  RowHdr &W = *reinterpret_cast<RowHdr *>(wrow);
 
   if (warp == 0) {
-    // ---- TMA producer: every tile of the range, one stage each, issued before
-    // the position arrives (a row that sees fewer blocks ignores the rest)
-    if (lane == 0) {
-      const int ntiles = (max(0, min(bpc, n_max - c0)) + kDecTile - 1) / kDecTile;
-      int issued = 0;
-      for (int t = 0; t < ntiles; ++t) {
-        const int32_t b0 = c0 + t * kDecTile;
-        const uint32_t fb = sm32(&C.full[t]);
-        mbar_expect_tx(fb, kDecTileBytes);
-        tma_load_2d(sRing + t * kDecTileBytes, &kmap, 0, b0, fb);
-        tma_load_2d(sRing + t * kDecTileBytes + kDecHalfBytes, &kmap, 64, b0, fb);
-        issued = t + 1;
-      }
-      C.issued = issued;
-    }
+    // (the producer issued its copies above)
   } else if (warp == 1) {
     // ---- MMA issuer: tile t into accumulator t
     if (lane == 0 && tiles > 0) {
@@ -419,6 +425,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     const int q = warp & 3;
     const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
     float *srow = a.scores + (int64_t)row * a.score_cols;
+    const bool selecting = n > keep_max;  // uniform over the row's CTAs
+    uint32_t my_max = 0u, my_low = 0u;
     for (int t = 0; t < tiles; ++t) {
       if (!tc_warp_wait(sm32(&C.tfull[t]), 0u, lim, abort_flag)) break;
       tc_fence_after();
@@ -434,6 +442,23 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
         sc_s[bl] = sc;
         srow[c0 + bl] = sc;
       }
+      if (selecting) {
+        // the score's top-12-bit bin into the row's histogram, one add per
+        // distinct bin per warp (every CTA of the row adds into it)
+        const uint32_t bin = bl < cnt ? order_key(sc) >> 20 : 0xFFFFFFFFu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (bin != 0xFFFFFFFFu) {
+          if (lane == __ffs(peers) - 1) atomicAdd(&W.hist0[hist_slot(bin)], (uint32_t)__popc(peers));
+          my_max = max(my_max, bin);
+          my_low |= bin < 8u ? 1u : 0u;
+        }
+      }
+    }
+    my_max = __reduce_max_sync(0xffffffffu, my_max);
+    my_low = __reduce_or_sync(0xffffffffu, my_low);
+    if (lane == 0) {
+      atomicMax(&C.maxbin, my_max);
+      if (my_low) C.low = 1u;
     }
   }
 
@@ -458,8 +483,6 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     return;  // the row's other CTAs time out at the barrier below
   }
   uint8_t *mrow = mask + (int64_t)row * a.tokens;
-  uint8_t *wrow = ws + (int64_t)row * row_ws_bytes;
-  RowHdr &W = *reinterpret_cast<RowHdr *>(wrow);
   uint32_t *cand_key = reinterpret_cast<uint32_t *>(wrow + sizeof(RowHdr));
   uint32_t *cand_idx = cand_key + (a.tokens >> 2);
   if (n <= keep_max) {  // every block kept: this CTA's share of the visible prefix
@@ -468,29 +491,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     fill_visible(mrow, lo, min((int64_t)a.tokens, lo + span), p);
     return;
   }
-  __syncthreads();  // sc_s complete; the ring is free
-  // one add per distinct bin per warp: a row's keys crowd into a few hundred
-  // bins, and every CTA of the row adds into the same workspace counters
-  uint32_t my_max = 0u, my_low = 0u;
-  for (int i0 = warp * 32; i0 < cnt; i0 += kDecThreads) {
-    const int i = i0 + lane;
-    const uint32_t bin = i < cnt ? order_key(sc_s[i]) >> 20 : 0xFFFFFFFFu;
-    const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-    if (bin != 0xFFFFFFFFu) {
-      if (lane == __ffs(peers) - 1) atomicAdd(&W.hist0[bin], (uint32_t)__popc(peers));
-      my_max = max(my_max, bin);
-      my_low |= bin < 8u ? 1u : 0u;
-    }
-  }
-  my_max = __reduce_max_sync(0xffffffffu, my_max);
-  my_low = __reduce_or_sync(0xffffffffu, my_low);
-  if (lane == 0) {
-    atomicMax(&C.maxbin, my_max);
-    if (my_low) C.low = 1u;
-  }
-
-  // ---- 2. grid barrier over the row's CTAs
-  __syncthreads();
+  // ---- 2. grid barrier over the row's CTAs (the histogram adds and C.maxbin
+  // were made by the epilogue warps before the barrier after scoring)
   if (tid == 0) {
     asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(&W.maxbin[y & 7]), "r"(C.maxbin)
                  : "memory");
@@ -521,14 +523,13 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   // beside a copy of the 512 bins ending 256 above this CTA's own highest one
   // (a row's highest bin lies within that unless a few CTAs hold scores 2^32
   // times the others'), so the kDecWindow bins ending at the row's highest one
-  // are usually in shared memory after one round trip.  Otherwise they come by
-  // a bulk copy (the copy engine reads global memory through the async proxy,
-  // so that proxy is fenced after the acquire that made the other CTAs' adds
-  // visible), and, only if they hold fewer than keep keys, all 4096 bins.
+  // are usually in shared memory after one round trip.  Otherwise those bins
+  // are loaded in a second one, and, only if they hold fewer than keep keys,
+  // all 4096 bins in a third.
   const uint32_t spec_lo = (uint32_t)min(max((int)C.maxbin + 256 - 511, 0), 4096 - 512);
   {
-    const uint32_t v0 = __ldcg(&W.hist0[spec_lo + tid]);
-    const uint32_t v1 = __ldcg(&W.hist0[spec_lo + 256 + tid]);
+    const uint32_t v0 = __ldcg(&W.hist0[hist_slot(spec_lo + tid)]);
+    const uint32_t v1 = __ldcg(&W.hist0[hist_slot(spec_lo + 256 + tid)]);
     if (tid == 0) {
       uint32_t mx = 0u;
 #pragma unroll
@@ -546,22 +547,19 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   __syncthreads();
   const bool bad = D.rule_prefix != 0u;
   const uint32_t wlo = D.rule_shift;
-  auto fetch_hist = [&](uint32_t first, uint32_t nbins, uint32_t parity) {
-    if (tid == 0) {
-      const uint32_t mb = sm32(&C.hbar);
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mb), "r"(4u * nbins)
-                   : "memory");
-      asm volatile(
-          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-              "r"(sm32(D.hist0)),
-          "l"(W.hist0 + first), "r"(4u * nbins), "r"(mb)
-          : "memory");
-      D.flag = tc_wait(mb, parity, kDecSpinLimit, nullptr) ? 1 : 0;
-      D.sel_bin = -1;
+  auto fetch_hist = [&](uint32_t first, uint32_t nbins) {  // nbins: kDecWindow or 4096
+    __syncthreads();  // every thread is done with the previous copy
+    uint32_t v[4096 / kDecThreads];  // every load in flight before the first store
+#pragma unroll
+    for (int u = 0; u < 4096 / kDecThreads; ++u) {
+      const uint32_t b = u * kDecThreads + tid;
+      v[u] = b < nbins ? __ldcg(&W.hist0[hist_slot(first + b)]) : 0u;
     }
+#pragma unroll
+    for (int u = 0; u < 4096 / kDecThreads; ++u)
+      if (u * kDecThreads + tid < (int)nbins) D.hist0[u * kDecThreads + tid] = v[u];
+    if (tid == 0) D.sel_bin = -1;
     __syncthreads();
-    return D.flag != 0;
   };
   uint32_t need = (uint32_t)min(keep_max, n);
   uint32_t hbase = spec_lo;  // D.hist0[i] holds bin hbase + i
@@ -575,19 +573,12 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     }
     if (sel < 0) {
       hbase = wlo;
-      if (!fetch_hist(wlo, kDecWindow, 0u)) {
-        if (tid == 0) report_error(a.status, kErrTimeout, row);
-        return;
-      }
+      fetch_hist(wlo, kDecWindow);
       find_bin<kDecThreads>(D.hist0, kDecWindow, need, D.warp_tot, &D.sel_bin, &D.sel_above);
       sel = D.sel_bin;
       if (sel < 0) {        // the keep-th key lies below the window
-        __syncthreads();    // every thread has read sel_bin
         hbase = 0u;
-        if (!fetch_hist(0u, 4096u, 1u)) {
-          if (tid == 0) report_error(a.status, kErrTimeout, row);
-          return;
-        }
+        fetch_hist(0u, 4096u);  // (its first barrier: every thread has read sel_bin)
         find_bin<kDecThreads>(D.hist0, 4096, need, D.warp_tot, &D.sel_bin, &D.sel_above);
         sel = D.sel_bin;
       }

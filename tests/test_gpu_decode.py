@@ -1,6 +1,6 @@
 """qsa_decode_index_select: pooling, scoring and selection with the fused
-decode launch (one thread-block cluster per row), against the oracle and
-against the single-stage entry points.
+decode launch (one cooperative launch, each row over many CTAs), against the
+oracle and against the single-stage entry points.
 
 Its scores come from the same tcgen05 MMA per (block, head) as the tensor-core
 scorer of qsa_score_rows_with, so they must equal that path's bit for bit (or,

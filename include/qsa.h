@@ -270,7 +270,7 @@ qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t po
                             int64_t workspace_bytes, void *stream);
 
 /*
- * Bytes of the workspace qsa_decode_index_select needs: per row, a 4096-bin
+ * Bytes of the workspace qsa_decode_index_select needs: per row, a 65536-bin
  * histogram, a few counters and room for tokens/4 candidates.  -1 for
  * negative arguments.
  */

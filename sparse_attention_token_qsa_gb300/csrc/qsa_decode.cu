@@ -24,23 +24,23 @@
 //     accumulators (one block per TMEM lane, its four heads in four columns),
 //     apply relu, the head sum in order 0..3 and the scale, and keep the
 //     scores in shared memory;
-//  2. the epilogue warps add each score's top-12-bit order-key bin into the
+//  2. the epilogue warps add each score's top-16-bit order-key bin into the
 //     row's histogram in the workspace (one add per distinct bin per warp);
 //  3. the row's CTAs meet at a grid barrier (the launch is cooperative, so
 //     they are co-resident; the wait is bounded);
 //  4. every CTA reads the row's histogram, finds the bin holding the keep-th
-//     key (a non-finite score shows up in the 16 outer bins), writes the final
+//     key (a non-finite score shows up in the 256 outer bins), writes the final
 //     mask bytes of its own blocks outside that bin, and appends the bin's
 //     keys with their block indices to the row's candidate list;
 //  5. the last CTA of the row to finish (an atomic ticket) zeroes the row's
 //     workspace for the next call (its stores drain while it works on), runs
-//     the remaining radix rounds (8, 8, 4 bits) over the candidates, cuts
+//     the remaining radix rounds (8 and 8 bits) over the candidates, cuts
 //     exact ties at the final key by radix rounds on the block index (lowest
 //     kept), and writes the kept candidates' mask bytes.
 //
-// Workspace per row: the 4096-bin histogram (interleaved over L2 lines, see
-// hist_slot), a few counters, and room for tokens / 4 candidates (key, block
-// index).  It must be zero before the first call; every call that completes
+// Workspace per row: the 65536-bin histogram (interleaved over L2 lines, see
+// hist_slot; only the bins between the row's lowest and highest are touched),
+// a few counters, and room for tokens / 4 candidates (key, block index).  It must be zero before the first call; every call that completes
 // leaves it zero.  A call that reports an error may leave it dirty: zero it
 // again before the next call.
 #include "qsa_device.cuh"
@@ -67,41 +67,50 @@ constexpr uint32_t kDecSuspendNs = 500;
 constexpr uint32_t kDecIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                ((uint32_t)(kDecN >> 3) << 17) | ((uint32_t)(kDecTile >> 4) << 24);
 
+constexpr int kDecBinBits = 16;                 // first-level bins: the order key's top 16 bits
+constexpr uint32_t kDecBins = 1u << kDecBinBits;
+constexpr uint32_t kDecHiBad = 0xFF80u;  // a positive non-finite score's bins start here
+constexpr uint32_t kDecLoBad = 0x0080u;  // ... and a negative one's end below this
+constexpr uint32_t kDecZeroBin = 0x8000u;  // the bin of a +0.0 score (relu's zero; -0.0 folds in)
+
 struct RowHdr {  // per row, at the start of the row's workspace
-  uint32_t hist0[4096];  // bin b's count at hist_slot(b)
+  uint32_t hist0[kDecBins];  // bin b's count at hist_slot(b)
   uint32_t arrive;  // CTAs whose histogram is in
-  uint32_t pad0;
+  uint32_t binrev;  // kDecBins - 1 minus the lowest bin other than kDecZeroBin any key landed in
   // candidates listed (low 32 bits) and CTAs done writing their blocks (high
   // 32 bits): the last CTA's ticket returns the list's length with it
   unsigned long long tc;
   uint32_t maxbin[8];  // the highest bin any key landed in (CTA y adds to slot y % 8)
-  uint32_t lowbad;     // a key landed below bin 8 (a negative non-finite score)
+  uint32_t lowbad;     // a key landed below kDecLoBad (a negative non-finite score)
   uint32_t pad[51];
 };
-static_assert(sizeof(RowHdr) == 16640, "the workspace layout is part of the ABI");
+static_assert(sizeof(RowHdr) == 262400, "qsa_decode_workspace_bytes reports this size");
 
-// A row's scores crowd into a few dozen neighbouring bins, and every CTA of the
+// A row's scores crowd into a range of neighbouring bins, and every CTA of the
 // row adds into them.  Bins go in runs of eight (one 32-byte sector), and run
-// r sits in 128-byte line r mod 128 (sector r / 128 of it): neighbouring runs
-// lie in different lines, so the adds spread over a dozen lines rather than
-// queue on three, while a read of consecutive bins still uses whole sectors.
+// r sits in 128-byte line r mod 2048 (sector r / 2048 of it): each line holds
+// one run of the crowded range rather than four, while a read of consecutive
+// bins still uses whole sectors.
 __device__ __forceinline__ uint32_t hist_slot(uint32_t bin) {
-  return (((bin >> 3) & 127u) << 5) | ((bin >> 10) << 3) | (bin & 7u);
+  return (((bin >> 3) & 2047u) << 5) | ((bin >> 14) << 3) | (bin & 7u);
 }
 
-// Keys of the keep-th largest score and everything above it sit in the top few
-// dozen bins of a row's histogram, so each CTA first reads only this many bins
-// below the row's highest one (and the whole histogram if they fall short).
+// Keys of the keep-th largest score and everything above it sit within a few
+// hundred bins (two octaves of score) of the row's highest one, so each CTA
+// first reads only this many bins below it, and lower ones only if they fall
+// short.
 constexpr int kDecWindow = 256;
+constexpr int kDecChunk = 4096;  // bins per later read
 
 struct DecSmem {  // selection scratch, laid over the key ring once scoring is done
-  uint32_t hist0[4096];
+  uint32_t hist0[kDecChunk];
   uint32_t hist1[256];
   uint32_t hist2[256];
-  uint32_t hist3[16];
   uint32_t warp_tot[kDecThreads / 32];
   int32_t sel_bin;
   uint32_t sel_above;
+  uint32_t sel_total;
+  uint32_t row_max, row_min;  // the row's highest and lowest bin
   int32_t flag;
   uint32_t rule_prefix;
   uint32_t rule_shift;
@@ -131,6 +140,7 @@ struct DecCtrl {
   int32_t abort;
   int32_t issued;        // key tiles the producer issued
   uint32_t maxbin;       // this CTA's highest bin
+  uint32_t minbin;       // ... and lowest
   uint32_t low;          // a key of this CTA landed below bin 8
 };
 constexpr size_t kDecSmemBytes = kDecCtrlOff + sizeof(DecCtrl) + 1024;  // + alignment slack
@@ -295,6 +305,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     C.abort = 0;
     C.issued = 0;
     C.maxbin = 0u;
+    C.minbin = kDecBins - 1u;
     C.low = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -426,7 +437,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
     float *srow = a.scores + (int64_t)row * a.score_cols;
     const bool selecting = n > keep_max;  // uniform over the row's CTAs
-    uint32_t my_max = 0u, my_low = 0u;
+    uint32_t my_max = 0u, my_min = kDecBins - 1u, my_low = 0u;
     for (int t = 0; t < tiles; ++t) {
       if (!tc_warp_wait(sm32(&C.tfull[t]), 0u, lim, abort_flag)) break;
       tc_fence_after();
@@ -443,21 +454,24 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
         srow[c0 + bl] = sc;
       }
       if (selecting) {
-        // the score's top-12-bit bin into the row's histogram, one add per
+        // the score's top-16-bit bin into the row's histogram, one add per
         // distinct bin per warp (every CTA of the row adds into it)
-        const uint32_t bin = bl < cnt ? order_key(sc) >> 20 : 0xFFFFFFFFu;
+        const uint32_t bin = bl < cnt ? order_key(sc) >> (32 - kDecBinBits) : 0xFFFFFFFFu;
         const uint32_t peers = __match_any_sync(0xffffffffu, bin);
         if (bin != 0xFFFFFFFFu) {
           if (lane == __ffs(peers) - 1) atomicAdd(&W.hist0[hist_slot(bin)], (uint32_t)__popc(peers));
           my_max = max(my_max, bin);
-          my_low |= bin < 8u ? 1u : 0u;
+          if (bin != kDecZeroBin) my_min = min(my_min, bin);  // (+0.0 has a bin of its own)
+          my_low |= bin < kDecLoBad ? 1u : 0u;
         }
       }
     }
     my_max = __reduce_max_sync(0xffffffffu, my_max);
+    my_min = __reduce_min_sync(0xffffffffu, my_min);
     my_low = __reduce_or_sync(0xffffffffu, my_low);
     if (lane == 0) {
       atomicMax(&C.maxbin, my_max);
+      atomicMin(&C.minbin, my_min);
       if (my_low) C.low = 1u;
     }
   }
@@ -496,6 +510,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   if (tid == 0) {
     asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(&W.maxbin[y & 7]), "r"(C.maxbin)
                  : "memory");
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(&W.binrev),
+                 "r"(kDecBins - 1u - C.minbin)
+                 : "memory");
     if (C.low) asm volatile("red.relaxed.gpu.global.or.b32 [%0], 1;" ::"l"(&W.lowbad) : "memory");
     // release: the CTA's histogram adds (ordered before it by the barrier
     // above) are visible to whoever sees the count
@@ -518,15 +535,15 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   }
 
   // ---- 3. the threshold bin, this CTA's mask bytes and candidates
-  // A non-finite score lands above bin 0xFF7 (positive) or below bin 8
-  // (negative); every finite one between.  The row's highest bin is read
-  // beside a copy of the 512 bins ending 256 above this CTA's own highest one
-  // (a row's highest bin lies within that unless a few CTAs hold scores 2^32
-  // times the others'), so the kDecWindow bins ending at the row's highest one
-  // are usually in shared memory after one round trip.  Otherwise those bins
-  // are loaded in a second one, and, only if they hold fewer than keep keys,
-  // all 4096 bins in a third.
-  const uint32_t spec_lo = (uint32_t)min(max((int)C.maxbin + 256 - 511, 0), 4096 - 512);
+  // A non-finite score lands at or above bin kDecHiBad (positive) or below
+  // kDecLoBad (negative); every finite one between.  The row's highest bin is
+  // read beside a copy of the 512 bins ending 256 above this CTA's own highest
+  // one (a row's highest bin lies within that unless a few CTAs hold scores
+  // four times the others'), so the kDecWindow bins ending at the row's
+  // highest one are usually in shared memory after one round trip.  Otherwise
+  // those bins are loaded in a second one, and, only if they hold fewer than
+  // keep keys, the bins below them kDecChunk at a time.
+  const uint32_t spec_lo = (uint32_t)min(max((int)C.maxbin + 256 - 511, 0), (int)kDecBins - 512);
   {
     const uint32_t v0 = __ldcg(&W.hist0[hist_slot(spec_lo + tid)]);
     const uint32_t v1 = __ldcg(&W.hist0[hist_slot(spec_lo + 256 + tid)]);
@@ -534,11 +551,11 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
       uint32_t mx = 0u;
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx = max(mx, __ldcg(&W.maxbin[k]));
-      const bool nf = __ldcg(&W.lowbad) != 0u || mx >= 0xFF8u;
+      const bool nf = __ldcg(&W.lowbad) != 0u || mx >= kDecHiBad;
       D.rule_prefix = nf ? 1u : 0u;  // (scratch: the non-finite verdict)
-      // window start: 16-byte aligned, rounded up so the highest bin stays inside
-      // (mx <= 0xFF7 for a finite row, so the window ends inside the histogram)
-      D.rule_shift = ((uint32_t)max(0, (int)mx + 1 - kDecWindow) + 3u) & ~3u;
+      D.rule_shift = (uint32_t)max(0, (int)mx + 1 - kDecWindow);  // the window ends at mx
+      D.row_max = mx;
+      D.row_min = kDecBins - 1u - __ldcg(&W.binrev);
       D.sel_bin = -1;
     }
     D.hist0[tid] = v0;
@@ -547,16 +564,16 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   __syncthreads();
   const bool bad = D.rule_prefix != 0u;
   const uint32_t wlo = D.rule_shift;
-  auto fetch_hist = [&](uint32_t first, uint32_t nbins) {  // nbins: kDecWindow or 4096
+  auto fetch_hist = [&](uint32_t first, uint32_t nbins) {  // bins [first, first + nbins <= kDecChunk)
     __syncthreads();  // every thread is done with the previous copy
-    uint32_t v[4096 / kDecThreads];  // every load in flight before the first store
+    uint32_t v[kDecChunk / kDecThreads];  // every load in flight before the first store
 #pragma unroll
-    for (int u = 0; u < 4096 / kDecThreads; ++u) {
+    for (int u = 0; u < kDecChunk / kDecThreads; ++u) {
       const uint32_t b = u * kDecThreads + tid;
       v[u] = b < nbins ? __ldcg(&W.hist0[hist_slot(first + b)]) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < 4096 / kDecThreads; ++u)
+    for (int u = 0; u < kDecChunk / kDecThreads; ++u)
       if (u * kDecThreads + tid < (int)nbins) D.hist0[u * kDecThreads + tid] = v[u];
     if (tid == 0) D.sel_bin = -1;
     __syncthreads();
@@ -567,22 +584,32 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   if (!bad) {
     if (wlo >= spec_lo && wlo + kDecWindow <= spec_lo + 512) {
       find_bin<kDecThreads>(D.hist0 + (wlo - spec_lo), kDecWindow, need, D.warp_tot, &D.sel_bin,
-                            &D.sel_above);
+                            &D.sel_above, &D.sel_total);
       sel = D.sel_bin < 0 ? -1 : D.sel_bin + (int32_t)(wlo - spec_lo);
-      __syncthreads();  // every thread has read sel_bin
-    }
-    if (sel < 0) {
+    } else {
       hbase = wlo;
       fetch_hist(wlo, kDecWindow);
-      find_bin<kDecThreads>(D.hist0, kDecWindow, need, D.warp_tot, &D.sel_bin, &D.sel_above);
+      find_bin<kDecThreads>(D.hist0, kDecWindow, need, D.warp_tot, &D.sel_bin, &D.sel_above,
+                            &D.sel_total);
       sel = D.sel_bin;
-      if (sel < 0) {        // the keep-th key lies below the window
-        hbase = 0u;
-        fetch_hist(0u, 4096u);  // (its first barrier: every thread has read sel_bin)
-        find_bin<kDecThreads>(D.hist0, 4096, need, D.warp_tot, &D.sel_bin, &D.sel_above);
-        sel = D.sel_bin;
-      }
     }
+    // the keep-th key lies below the window: the bins below it, a chunk at a
+    // time (the histogram holds all n >= need keys, so the scan ends)
+    for (uint32_t top = wlo; sel < 0 && top > 0;) {
+      need -= D.sel_total;
+      const uint32_t lo = top > (uint32_t)kDecChunk ? top - kDecChunk : 0u;
+      hbase = lo;
+      fetch_hist(lo, top - lo);  // (its first barrier: every thread has read sel_bin, sel_total)
+      find_bin<kDecThreads>(D.hist0, (int)(top - lo), need, D.warp_tot, &D.sel_bin, &D.sel_above,
+                            &D.sel_total);
+      sel = D.sel_bin;
+      top = lo;
+    }
+    if (sel < 0) {  // (only a workspace left dirty by the caller gets here)
+      sel = 0;
+      hbase = 0;
+    }
+    __syncthreads();  // every thread has read sel_bin
   }
   uint32_t B0 = 0;
   bool whole = false;  // the bin's keys are all kept
@@ -600,7 +627,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         k[e] = e < mq ? order_key(sc_s[i + e]) : 0u;
-        const uint32_t d = k[e] >> 20;
+        const uint32_t d = k[e] >> (32 - kDecBinBits);
         if (e < mq) {
           kept |= (d > B0 || (whole && d == B0) ? 1u : 0u) << e;
           bits |= (!whole && d == B0 ? 1u : 0u) << e;
@@ -637,13 +664,20 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   }
   __syncthreads();
   if (!D.flag) return;
-  // every CTA has read the histogram and taken its ticket: clear it for the
-  // next call now, so that the stores drain while the candidates are resolved
-  for (int i = tid; i < 4096 / 4; i += kDecThreads)
-    reinterpret_cast<uint4 *>(W.hist0)[i] = make_uint4(0u, 0u, 0u, 0u);
+  // every CTA has read the histogram and taken its ticket: clear the bins the
+  // row's keys landed in for the next call now, so that the stores drain
+  // while the candidates are resolved (runs of eight bins, one 32-byte sector
+  // each, from the row's lowest bin to its highest, and the zero bin)
+  for (uint32_t r = (D.row_min >> 3) + tid; r <= (D.row_max >> 3); r += kDecThreads) {
+    uint4 *run = reinterpret_cast<uint4 *>(&W.hist0[hist_slot(r << 3)]);
+    run[0] = make_uint4(0u, 0u, 0u, 0u);
+    run[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (tid == 0) W.hist0[hist_slot(kDecZeroBin)] = 0u;
   auto clear_counters = [&]() {
     if (tid == 0) {
       W.arrive = 0u;
+      W.binrev = 0u;
       W.tc = 0ull;
 #pragma unroll
       for (int k = 0; k < 8; ++k) W.maxbin[k] = 0u;
@@ -672,19 +706,19 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
         }
       }
     }
-    for (int i = tid; i < 256 + 256 + 16; i += kDecThreads) (&D.hist1[0])[i] = 0u;
+    for (int i = tid; i < 256 + 256; i += kDecThreads) (&D.hist1[0])[i] = 0u;
     __syncthreads();
     clear_counters();
     auto ckey = [&](int32_t j) { return j < kDecCandCache ? ck_s[j] : __ldcg(&cand_key[j]); };
     auto cidx = [&](int32_t j) { return j < kDecCandCache ? ci_s[j] : __ldcg(&cand_idx[j]); };
     uint32_t prefix = B0;
-    int shift = 20;
+    int shift = 32 - kDecBinBits;
     bool done = false;
-    // rounds of 8, 8 and 4 bits on the candidates (each round's result in its
-    // own slot: two barriers a round)
-    for (int r = 1; r < 4 && !done; ++r) {
-      uint32_t *H = r == 1 ? D.hist1 : (r == 2 ? D.hist2 : D.hist3);
-      const int nb = r == 3 ? 16 : 256, sh = r == 1 ? 12 : (r == 2 ? 4 : 0);
+    // two rounds of 8 bits on the candidates (each round's result in its own
+    // slot: two barriers a round)
+    for (int r = 1; r < 3 && !done; ++r) {
+      uint32_t *H = r == 1 ? D.hist1 : D.hist2;
+      const int nb = 256, sh = r == 1 ? 8 : 0;
       for (int32_t j = tid; j < nl; j += kDecThreads) {
         const uint32_t key = ckey(j);
         if ((key >> shift) == prefix) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);

@@ -105,12 +105,14 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_t
 
 // Find the bin of histogram M[nb] (shared memory) that holds the need-th
 // largest key, scanning bins from the top: *sel_bin gets the bin, *sel_above
-// the number of keys in higher bins (both in shared memory, read after the
-// call).  Every thread of the CTA calls it; warp_tot holds NT / 32 words.
+// the number of keys in higher bins, *sel_total (if given) the histogram's
+// total (all in shared memory, read after the call; *sel_bin is left as it was
+// when the total is below need).  Every thread of the CTA calls it; warp_tot
+// holds NT / 32 words.
 template <int NT>
 __device__ __forceinline__ void find_bin(const uint32_t *M, int nb, uint32_t need,
                                          uint32_t *warp_tot, int32_t *sel_bin,
-                                         uint32_t *sel_above) {
+                                         uint32_t *sel_above, uint32_t *sel_total = nullptr) {
   const int tid = threadIdx.x;
   const int per = (nb + NT - 1) / NT;
   const int hi = nb - 1 - tid * per;  // this thread's bins: hi, hi-1, ..., hi-per+1
@@ -119,6 +121,7 @@ __device__ __forceinline__ void find_bin(const uint32_t *M, int nb, uint32_t nee
     if (hi - j >= 0) sum += M[hi - j];
   uint32_t total;
   const uint32_t before = block_excl_scan<NT>(sum, warp_tot, total);
+  if (sel_total != nullptr && tid == 0) *sel_total = total;
   if (before < need && need <= before + sum) {
     uint32_t acc = before;
     for (int j = 0; j < per; ++j) {

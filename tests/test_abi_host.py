@@ -135,7 +135,7 @@ def test_index_select_refusals(lib):
 
 
 def test_decode_workspace_bytes(lib):
-    row = 16640 + 8 * (65536 // 4)          # histogram + counters, then the candidates
+    row = 262400 + 8 * (65536 // 4)         # histogram + counters, then the candidates
     assert lib.qsa_decode_workspace_bytes(1, 65536) == (row + 255) // 256 * 256
     assert lib.qsa_decode_workspace_bytes(3, 65536) == 3 * ((row + 255) // 256 * 256)
     assert lib.qsa_decode_workspace_bytes(2, 4099) % 256 == 0

@@ -29,14 +29,14 @@
 //  3. the row's CTAs meet at a grid barrier (the launch is cooperative, so
 //     they are co-resident; the wait is bounded);
 //  4. every CTA reads the row's histogram, finds the bin holding the keep-th
-//     key (a non-finite score shows up in the 256 outer bins), writes the final
-//     mask bytes of its own blocks outside that bin, and appends the bin's
-//     keys with their block indices to the row's candidate list;
-//  5. the last CTA of the row to finish (an atomic ticket) zeroes the row's
-//     workspace for the next call (its stores drain while it works on), runs
-//     the remaining radix rounds (8 and 8 bits) over the candidates, cuts
-//     exact ties at the final key by radix rounds on the block index (lowest
-//     kept), and writes the kept candidates' mask bytes.
+//     key (a non-finite score shows up in the 256 outer bins), appends that
+//     bin's keys with their block indices to the row's candidate list, takes
+//     an atomic ticket, and writes the mask bytes of its other blocks;
+//  5. the last CTA of the row to take its ticket zeroes the row's workspace
+//     for the next call (its stores drain while it works on), runs the
+//     remaining radix rounds (8 and 8 bits) over the candidates, cuts exact
+//     ties at the final key by radix rounds on the block index (lowest kept),
+//     and writes the candidates' mask bytes.
 //
 // Workspace per row: the 65536-bin histogram (interleaved over L2 lines, see
 // hist_slot; only the bins between the row's lowest and highest are touched),
@@ -613,47 +613,45 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   }
   uint32_t B0 = 0;
   bool whole = false;  // the bin's keys are all kept
+  const uintptr_t rb = reinterpret_cast<uintptr_t>(mrow);
+  const bool al16 = (rb & 15u) == 0, al4 = (rb & 3u) == 0;
+  // this thread's quad of the CTA's blocks (cnt <= 256: one quad at most)
+  const int i = 4 * tid;
+  const int mq = i < cnt ? min(4, cnt - i) : 0;
+  uint32_t kept = 0, bits = 0;  // kept blocks; blocks of bin B0 (the candidates)
   if (bad) {
     if (y == 0 && tid == 0) report_error(a.status, kErrNonFinite, row);
   } else {
     B0 = hbase + (uint32_t)sel;
     need -= D.sel_above;
     whole = D.hist0[B0 - hbase] == need;
-    const uintptr_t rb = reinterpret_cast<uintptr_t>(mrow);
-    const bool al16 = (rb & 15u) == 0, al4 = (rb & 3u) == 0;
-    for (int i = 4 * tid; i < cnt; i += 4 * kDecThreads) {
-      const int mq = min(4, cnt - i);
-      uint32_t kept = 0, bits = 0, k[4];
+    uint32_t k[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      k[e] = e < mq ? order_key(sc_s[i + e]) : 0u;
+      const uint32_t d = k[e] >> (32 - kDecBinBits);
+      if (e < mq) {
+        kept |= (d > B0 || (whole && d == B0) ? 1u : 0u) << e;
+        bits |= (!whole && d == B0 ? 1u : 0u) << e;
+      }
+    }
+    if (bits) {  // listed for the last CTA, which also writes their mask bytes
+      uint32_t at = (uint32_t)atomicAdd(&W.tc, (unsigned long long)__popc(bits));
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        k[e] = e < mq ? order_key(sc_s[i + e]) : 0u;
-        const uint32_t d = k[e] >> (32 - kDecBinBits);
-        if (e < mq) {
-          kept |= (d > B0 || (whole && d == B0) ? 1u : 0u) << e;
-          bits |= (!whole && d == B0 ? 1u : 0u) << e;
-        }
-      }
-      store_blocks(mrow, (int64_t)c0 + i, mq, kept, al16, al4);
-      if (bits) {
-        uint32_t at = (uint32_t)atomicAdd(&W.tc, (unsigned long long)__popc(bits));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (bits & (1u << e)) {
-            cand_key[at] = k[e];
-            cand_idx[at] = (uint32_t)(c0 + i + e);
-            ++at;
-          }
+        if (bits & (1u << e)) {
+          cand_key[at] = k[e];
+          cand_idx[at] = (uint32_t)(c0 + i + e);
+          ++at;
         }
       }
     }
-    // tokens past the complete blocks: the tail is visible, the rest zero
-    if (y == ny - 1) fill_visible(mrow, 4 * (int64_t)n, a.tokens, p);
   }
 
-  // ---- 4. the last CTA of the row resolves the candidates
+  // ---- 4. the ticket: the last CTA of the row resolves the candidates
   __syncthreads();
   if (tid == 0) {
-    // release this CTA's mask bytes and candidates; the last CTA acquires all
+    // release this CTA's candidates; the last CTA acquires every CTA's
     unsigned long long t;
     asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
                  : "=l"(t)
@@ -662,8 +660,29 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     D.flag = (uint32_t)(t >> 32) == (uint32_t)(ny - 1);
     D.nl = (uint32_t)t;  // every CTA's candidates are listed by now
   }
+  // this CTA's mask bytes other than the candidates' (no other CTA writes
+  // them, so they need not precede the ticket)
+  if (!bad) {
+    if (bits == 0u) {
+      if (mq) store_blocks(mrow, (int64_t)c0 + i, mq, kept, al16, al4);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (e < mq && !(bits & (1u << e)))
+          store_blocks(mrow, (int64_t)c0 + i + e, 1, (kept >> e) & 1u, false, al4);
+    }
+    // tokens past the complete blocks: the tail is visible, the rest zero
+    if (y == ny - 1) fill_visible(mrow, 4 * (int64_t)n, a.tokens, p);
+  }
   __syncthreads();
   if (!D.flag) return;
+  const int32_t nl = (int32_t)D.nl;
+  const bool few = !bad && !whole && nl <= 32;
+  uint32_t ck = 0u, ci = 0u;  // (few: lane j of warp 0 holds candidate j)
+  if (few && warp == 0 && lane < nl) {  // loaded before the clearing stores below
+    ck = __ldcg(&cand_key[lane]);
+    ci = __ldcg(&cand_idx[lane]);
+  }
   // every CTA has read the histogram and taken its ticket: clear the bins the
   // row's keys landed in for the next call now, so that the stores drain
   // while the candidates are resolved (runs of eight bins, one 32-byte sector
@@ -684,9 +703,24 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
       W.lowbad = 0u;
     }
   };
-  if (bad || whole) clear_counters();
-  if (!bad && !whole) {
-    const int32_t nl = (int32_t)D.nl;
+  if (bad || whole || few) clear_counters();
+  if (few && warp == 0) {
+    // a warp ranks the few candidates exactly: candidate j is kept if fewer
+    // than `need` others come before it (a higher key, or the same key and a
+    // lower block index)
+    uint32_t rank = 0;
+    for (int j = 0; j < nl; ++j) {
+      const uint32_t kj = __shfl_sync(0xffffffffu, ck, j);
+      const uint32_t ij = __shfl_sync(0xffffffffu, ci, j);
+      rank += (kj > ck || (kj == ck && ij < ci)) ? 1u : 0u;
+    }
+    if (lane < nl) {
+      store_blocks(mrow, (int64_t)ci, 1, rank < need ? 1u : 0u, false, al4);
+      cand_key[lane] = 0u;
+      cand_idx[lane] = 0u;
+    }
+  }
+  if (!bad && !whole && !few) {
     for (int j0 = 0; j0 < min(nl, kDecCandCache); j0 += 8 * kDecThreads) {
       uint32_t kk[8], ii[8];  // eight entries per thread in flight
 #pragma unroll
@@ -788,14 +822,13 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
       }
     }
     __syncthreads();
-    // the kept candidates' mask bytes (every candidate was written as dropped)
+    // every candidate's mask bytes (their owners wrote none)
     const uint32_t rp = D.rule_prefix, rs = D.rule_shift;
     const int32_t rc = D.rule_cut;
-    const bool al4 = (reinterpret_cast<uintptr_t>(mrow) & 3u) == 0;
     for (int32_t j = tid; j < nl; j += kDecThreads) {
       const uint32_t kk = ckey(j) >> rs;
       const int32_t gi = (int32_t)cidx(j);
-      if (kk > rp || (kk == rp && gi <= rc)) store_blocks(mrow, gi, 1, 1u, false, al4);
+      store_blocks(mrow, gi, 1, (kk > rp || (kk == rp && gi <= rc)) ? 1u : 0u, false, al4);
     }
     // candidates past the shared-memory cache were read from the workspace
     // until now: cleared last

@@ -357,9 +357,10 @@ def test_decode_pools_new_blocks_in_the_same_launch(qsa, orc, tables, first, cou
 
 def test_decode_keep_th_key_far_below_the_top(qsa, orc, tables):
     """A few block keys scaled by 2^70 make a handful of scores ~2^70 times the
-    rest: the keep-th score then lies hundreds of 12-bit bins below the row's
-    highest, outside the first window each CTA reads, so the whole histogram is
-    read; the masks must still equal the two-kernel path and the oracle."""
+    rest: the keep-th score then lies thousands of 16-bit bins below the row's
+    highest, outside the first window each CTA reads, so the bins below it are
+    read a chunk at a time; the masks must still equal the two-kernel path and
+    the oracle."""
     rng = qi.rng_for(1, salt=4097)
     tokens = 65536
     nb = tokens // 4

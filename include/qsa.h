@@ -44,9 +44,10 @@
  *    a visible length outside [0, p+1], a non-finite score inside a
  *    truncating row's block prefix) do not trap: the kernel records the first
  *    one in the caller's status word and leaves that row's output untouched
- *    -- except the mask row of a non-finite score, which a one-pass selection
- *    of a long row may have partly written before it met the score (its
- *    bytes are then 0 or 1, and unspecified).  Every other row is complete.
+ *    -- except the mask row of a non-finite score, which the selection may
+ *    have partly written before it met the score (the tokens past the row's
+ *    complete blocks, or a one-pass selection's bytes; they are then 0 or 1,
+ *    and unspecified).  Every other row is complete.
  *    dev_status is a DEVICE int32_t[2] = {code, row}; it must be zero before
  *    the call (qsa_reset_status) and is read with qsa_read_status.
  */

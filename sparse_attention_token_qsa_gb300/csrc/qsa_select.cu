@@ -18,16 +18,25 @@
 //    each score once;
 //  * the first round histograms the top 12 bits of every key as it is loaded
 //    (exact zeros, the heavy bin of relu scores, go to one spare bin per lane
-//    and are folded in afterwards); the histograms merge over the cluster
-//    through distributed shared memory; a non-finite score shows up as a
-//    count in one of the 16 outer bins, so no per-key check is needed;
+//    and are folded in afterwards); a non-finite score shows up as a count in
+//    one of the 16 outer bins, so no per-key check is needed.  In a cluster
+//    every CTA finds the selected bin itself, in two short reads of its
+//    peers' shared memory (the ranks' sums over runs of 64 bins, then the
+//    chosen run's bins), without merging the 4096 bins;
 //  * one pass over the keys then writes the final mask bytes of every key
 //    outside the selected bin and marks the quads that hold the bin's keys; a
 //    second, short walk over the marked quads lists those keys (with their
-//    block indices) as candidates, which rank 0 gathers; rounds of 8, 8 and
-//    4 bits run on the candidates only (stopping once the keys left are all
-//    one key), and exact ties at the final key are cut on the block index
-//    (lowest indices kept) by radix rounds, or on one CTA by a bitmap;
+//    block indices) as candidates; rounds of 8, 8 and 4 bits run on the
+//    candidates only (stopping once the keys left are all one key), and exact
+//    ties at the final key are cut on the block index (lowest indices kept).
+//    On one CTA the rounds run on its list, ties cut by a bitmap or radix
+//    rounds on the indices.  In a cluster of the key-caching shape each list
+//    stays in its CTA: a round's digit counts, and each rank's key range and
+//    count under the prefix, are read from the peers, every CTA reaches the
+//    same bins, and ties are cut by the ranks' counts (ranks own ascending
+//    slices) and a bitmap in the one CTA where the cut falls.  (Clusters of
+//    the other shape, for rows past 65536 blocks in many-row launches, gather
+//    the lists in rank 0, which runs the rounds and hands out the result);
 //  * every CTA then patches the mask bytes of its own candidates.  A bin too
 //    large for the candidate list falls back to rounds over every key, with
 //    ties ranked by a block scan in the mask pass.
@@ -78,6 +87,16 @@ struct SelectSmem {
   int32_t rsel[kRounds];     // each candidate round's bin ...
   uint32_t rabove[kRounds];  // ... and the keys above it
   uint32_t kmin, kmax;       // the candidates under the prefix: their key range
+  uint32_t coarse[64];       // in a cluster: this CTA's round-0 counts over runs of 64 bins
+  uint32_t sel_cnt;          // in a cluster: the selected round-0 bin's count over the cluster
+  // in a cluster, per candidate round r (1..3, and 4 for a final check):
+  uint32_t rcnt[kRounds];          //   the round's bin count over the cluster
+  uint32_t kmin_r[kRounds + 1];    //   this CTA's candidates under the prefix: lowest key,
+  uint32_t kmax_r[kRounds + 1];    //   highest key
+  uint32_t kcnt_r[kRounds + 1];    //   and count
+  uint32_t one_key;                // every rank's candidates under the prefix hold one key ...
+  uint32_t one_key_val;            // ... this one
+  uint32_t tbefore;                // ... and the lower ranks hold this many of them
   // cand keys [kCandCap] u32, cand local indices [kCandCap] u16, keys[] follow (dynamic)
 };
 
@@ -107,6 +126,96 @@ __device__ __forceinline__ uint16_t ld_dsmem_u16(const uint16_t *local, uint32_t
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(laddr), "r"(rank));
   asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(raddr) : "memory");
   return v;
+}
+
+// Bin b of H summed over the cluster's C ranks (one thread per bin: the
+// loads of a warp read 32 consecutive bins of one rank at a time).
+__device__ __forceinline__ uint32_t cluster_bin(const uint32_t *H, int b, int C) {
+  uint32_t v[kSelMaxCluster];
+#pragma unroll
+  for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&H[b], (uint32_t)q) : 0u;
+  uint32_t t = 0;
+#pragma unroll
+  for (int q = 0; q < kSelMaxCluster; ++q) t += v[q];
+  return t;
+}
+
+// Round 0's bin over a cluster, in two levels: the ranks' 64 run sums, then
+// the chosen run's 64 bins of every rank; and the non-finite verdict (the
+// 16 outer bins).  Every thread of the CTA calls it; the results land in
+// S.sel_bin / sel_above / sel_cnt and the verdict is returned.
+template <int NT>
+__device__ __forceinline__ bool cluster_find_round0(SelectSmem &S, int C, uint32_t need) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t *M = S.msmall;  // merged run sums, then the run's merged bins
+  bool nf = false;
+  if (tid < 64) M[tid] = cluster_bin(S.coarse, tid, C);
+  else if (tid < 80) nf = cluster_bin(S.hist0, tid < 72 ? tid - 64 : 4088 + (tid - 72), C) != 0u;
+  if (__syncthreads_or(nf)) return true;
+  if (warp == 0) {
+    uint32_t B, above;
+    warp_find_bin(M, 64, need, lane, B, above);
+    if (lane == 0) {
+      S.sel_bin = (int32_t)B;
+      S.sel_above = above;
+    }
+  }
+  __syncthreads();
+  const uint32_t run = (uint32_t)S.sel_bin, above_run = S.sel_above;
+  __syncthreads();  // (M and sel_bin are rewritten below)
+  if (tid < 64) M[tid] = cluster_bin(S.hist0, (int)(64 * run) + tid, C);
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t B, above;
+    warp_find_bin(M, 64, need - above_run, lane, B, above);
+    if (lane == 0) {
+      S.sel_bin = (int32_t)(64 * run + B);
+      S.sel_above = above_run + above;
+      S.sel_cnt = M[B];
+    }
+  }
+  __syncthreads();
+  return false;
+}
+
+// Candidate round r's bin over a cluster (H's nb bins summed over the ranks;
+// nb = 0 for the final check) into S.rsel / rabove / rcnt[r]; and, from every
+// rank's key range and count of the candidates under the prefix, whether
+// they all hold one key (S.one_key, S.one_key_val) and how many of them the
+// ranks below this one hold (S.tbefore).  Every thread of the CTA calls it.
+template <int NT>
+__device__ __forceinline__ void cluster_find_round(SelectSmem &S, const uint32_t *H, int nb, int r, int C,
+                                                   uint32_t need, uint32_t rank) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t *M = S.msmall;
+  if (tid < nb) M[tid] = cluster_bin(H, tid, C);
+  if (warp == NT / 32 - 1) {  // the last warp: the ranks' key ranges and counts
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u, c = 0u;
+    if (lane < C) {
+      lo = ld_dsmem(&S.kmin_r[r], (uint32_t)lane);
+      hi = ld_dsmem(&S.kmax_r[r], (uint32_t)lane);
+      c = ld_dsmem(&S.kcnt_r[r], (uint32_t)lane);
+    }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t below = __reduce_add_sync(0xffffffffu, lane < (int)rank ? c : 0u);
+    if (lane == 0) {
+      S.one_key = lo == hi ? 1u : 0u;
+      S.one_key_val = lo;
+      S.tbefore = below;
+    }
+  }
+  __syncthreads();
+  if (nb > 0 && !S.one_key && warp == 0) {
+    uint32_t B, above;
+    warp_find_bin(M, nb, need, lane, B, above);
+    if (lane == 0) {
+      S.rsel[r] = (int32_t)B;
+      S.rabove[r] = above;
+      S.rcnt[r] = M[B];
+    }
+  }
+  __syncthreads();
 }
 
 // Histogram increment for one key per lane (exact zeros, the one heavy bin of
@@ -155,6 +264,15 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   const int32_t cnt = b1 - b0;
   const float *srow = scores + (int64_t)row * score_cols + b0;
   const int32_t cached = CACHE ? min(cnt, cap) : 0;
+  {
+    // tokens past the complete blocks (the tail visible, the rest zero) depend
+    // on no score: their stores drain while the scores load
+    const int64_t lo = 4 * (int64_t)n;
+    const int64_t span = ((int64_t)tokens - lo + C - 1) / C;
+    const int64_t a = lo + (int64_t)rank * span;
+    const int64_t b = a + span < tokens ? a + span : tokens;
+    fill_visible(mrow, a, b, p);
+  }
   if (!CACHE && cnt <= 16384) {
     // a slice of up to 64 KiB heads for L2 at once (two requests a thread):
     // the loads below then wait on L2, not on HBM.  (A longer slice would
@@ -169,6 +287,12 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     S.ncand = 0u;
     S.eq_base = 0u;
     S.band_hi = 0u;
+#pragma unroll
+    for (int r = 0; r <= kRounds; ++r) {
+      S.kmin_r[r] = 0xFFFFFFFFu;
+      S.kmax_r[r] = 0u;
+      S.kcnt_r[r] = 0u;
+    }
   }
   __syncthreads();
 
@@ -429,51 +553,44 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       }
     }
 
-    // ---- round 0: merge the top-12-bit histograms over the cluster
-    if (C > 1) {
-      cluster_sync_all();
-      // reduce-scatter: this CTA sums its slice of bins over the cluster, in place
-      const int slice = 4096 / C;
-      for (int b = (int)rank * slice + tid; b < ((int)rank + 1) * slice; b += NT) {
-        uint32_t v[kSelMaxCluster];
-#pragma unroll
-        for (int q = 0; q < kSelMaxCluster; ++q) v[q] = q < C ? ld_dsmem(&S.hist0[b], (uint32_t)q) : 0u;
-        uint32_t t = 0;
-#pragma unroll
-        for (int q = 0; q < kSelMaxCluster; ++q) t += v[q];
-        S.hist0[b] = t;
-      }
-      cluster_sync_all();
-      // gather the other slices' merged bins (their owners no longer change them)
-      constexpr int kGather = (4096 + NT - 1) / NT;
-      uint32_t g[kGather];
-#pragma unroll
-      for (int j = 0; j < kGather; ++j) {
-        const int b = tid + j * NT;
-        g[j] = 0u;
-        if (b < 4096) {
-          const int owner = b / slice;
-          g[j] = owner != (int)rank ? ld_dsmem(&S.hist0[b], (uint32_t)owner) : S.hist0[b];
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kGather; ++j)
-        if (tid + j * NT < 4096) S.hist0[tid + j * NT] = g[j];
-    }
+    // ---- round 0 over a cluster, in two levels: each CTA sums its bins in
+    // runs of 64; after one cluster barrier every CTA reads the ranks' 64 run
+    // sums (and the 16 outer bins), finds the run holding the need-th key,
+    // then reads that run's 64 bins from every rank and finds the bin.  Every
+    // CTA reaches the same bin without merging the 4096 bins.
+    //
     // A score is non-finite exactly when its key lands in one of the 16 outer
     // bins: keys of -inf and negative NaNs are below 0x00800000 (bins 0..7),
     // keys of +inf and positive NaNs at or above 0xFF800000 (bins 0xFF8..0xFFF),
     // and every finite score's key lies between.
-    __syncthreads();
-    {
+    if (C > 1) {
+      __syncthreads();  // the spare bins are folded in
+      {
+        constexpr int kPer = 4096 / NT;    // bins per thread: 8 or 16
+        constexpr int kGroup = 64 / kPer;  // threads per run of 64 bins
+        const uint4 *h4 = reinterpret_cast<const uint4 *>(S.hist0 + tid * kPer);
+        uint32_t t = 0;
+#pragma unroll
+        for (int k = 0; k < kPer / 4; ++k) {
+          const uint4 v = h4[k];
+          t += v.x + v.y + v.z + v.w;
+        }
+#pragma unroll
+        for (int off = 1; off < kGroup; off <<= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+        if ((tid & (kGroup - 1)) == 0) S.coarse[tid / kGroup] = t;
+      }
+      cluster_sync_all();  // every rank's bins and run sums are final until the next one
+      bad = cluster_find_round0<NT>(S, C, need);  // the same verdict in every CTA of the cluster
+    } else {
+      __syncthreads();
       const bool nf = tid < 16 && S.hist0[tid < 8 ? tid : 0xFF0 + tid] != 0u;
-      bad = __syncthreads_or(nf) != 0;  // the same verdict in every CTA of the cluster
+      bad = __syncthreads_or(nf) != 0;
     }
 
     if (!bad) {
-      find_bin<NT>(S.hist0, 4096, need, S.warp_tot, &S.sel_bin, &S.sel_above);
+      if (C == 1) find_bin<NT>(S.hist0, 4096, need, S.warp_tot, &S.sel_bin, &S.sel_above);
       const uint32_t B0 = (uint32_t)S.sel_bin;
-      const uint32_t cnt0 = S.hist0[B0];
+      const uint32_t cnt0 = C > 1 ? S.sel_cnt : S.hist0[B0];
       need -= S.sel_above;
       prefix = B0;
       shift = 20;
@@ -610,12 +727,16 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               if (bits & (1u << e)) {
-                cand_s[at] = CACHE ? k[e] : order_key(__uint_as_float(k[e]));
+                const uint32_t key = CACHE ? k[e] : order_key(__uint_as_float(k[e]));
+                cand_s[at] = key;
                 cand_li[at] = (uint16_t)(i + e);
                 ++at;
+                // a cluster's first candidate round histograms the lists as they form
+                if (CACHE && C > 1) atomicAdd(&S.hist1[(key >> 12) & 255u], 1u);
               }
             }
           }
+
         }
         cand_path = true;
       } else {
@@ -624,7 +745,126 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     }
   }
 
-  if (cand_path) {
+  if (CACHE && cand_path && C > 1) {
+    // ---- a cluster's candidate rounds, each over the CTAs' own lists: one
+    // warp merges the round's digit counts from every rank's histogram, with
+    // every rank's key range and count of the candidates under the prefix;
+    // every CTA reaches the same bins, and no list leaves its CTA.  Once the
+    // candidates under the prefix all hold one key (exact ties, as quantised
+    // scores give), no key round can split them: the ranks' counts place the
+    // cut, in block order, at once.
+    __syncthreads();  // this CTA's list is complete
+    own_n = S.ncand;
+    {
+      // round 1's key range (its digits were counted as the list formed)
+      uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+      for (uint32_t j = tid; j < own_n; j += NT) {
+        lo = min(lo, cand_s[j]);
+        hi = max(hi, cand_s[j]);
+      }
+      lo = __reduce_min_sync(0xffffffffu, lo);
+      hi = __reduce_max_sync(0xffffffffu, hi);
+      if (lane == 0 && lo <= hi) {
+        atomicMin(&S.kmin_r[1], lo);
+        atomicMax(&S.kmax_r[1], hi);
+      }
+      if (tid == 0) S.kcnt_r[1] = own_n;
+    }
+    bool done = false;
+    int r_one = 0;  // the round whose check found one key
+    for (int r = 1; r <= kRounds && !done; ++r) {
+      uint32_t *H = r == 1 ? S.hist1 : (r == 2 ? S.hist2 : S.hist3);
+      const int nb = r < kRounds ? round_bins(r) : 0, sh = r < kRounds ? round_shift(r) : 0;
+      if (r > 1) {  // this CTA's candidates under the prefix: digits, key range, count
+        uint32_t lo = 0xFFFFFFFFu, hi = 0u, c = 0u;
+        for (uint32_t j = tid; j < own_n; j += NT) {
+          const uint32_t key = cand_s[j];
+          if ((key >> shift) == prefix) {
+            if (nb > 0) atomicAdd(&H[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+            lo = min(lo, key);
+            hi = max(hi, key);
+            ++c;
+          }
+        }
+        lo = __reduce_min_sync(0xffffffffu, lo);
+        hi = __reduce_max_sync(0xffffffffu, hi);
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (lane == 0 && c) {
+          atomicMin(&S.kmin_r[r], lo);
+          atomicMax(&S.kmax_r[r], hi);
+          atomicAdd(&S.kcnt_r[r], c);
+        }
+      }
+      cluster_sync_all();
+      cluster_find_round<NT>(S, H, nb, r, C, need, rank);
+      if (S.one_key || r == kRounds) {  // (after round 3 the prefix is a whole key)
+        if (r < kRounds) {
+          prefix = S.one_key_val;
+          shift = 0;
+        }
+        r_one = r;
+        break;
+      }
+      need -= S.rabove[r];
+      prefix = (prefix << (shift - sh)) | (uint32_t)S.rsel[r];
+      shift = sh;
+      done = S.rcnt[r] == need;
+    }
+    int32_t cut = INT32_MAX;  // keys equal to the prefix: kept up to this block index
+    if (!done) {
+      // the need lowest block indices among the keys equal to `prefix` are
+      // kept; ranks own ascending slices, so the lower ranks' come first
+      const uint32_t before = S.tbefore, mine = S.kcnt_r[r_one];
+      if (need <= before) {
+        cut = -1;
+      } else if (need < before + mine) {
+        // this CTA keeps its m lowest: a bitmap of their local indices and a
+        // scan of its words' bit counts
+        const uint32_t m = need - before;
+        const int words = (cnt + 31) >> 5;  // cnt <= 65536 on this path
+        const int per_t = (words + NT - 1) / NT;
+        uint32_t *bm = S.hist0;  // no rank reads round 0's bins any more
+        for (int i = tid; i < words; i += NT) bm[i] = 0u;
+        __syncthreads();
+        for (uint32_t j = tid; j < own_n; j += NT) {
+          if (cand_s[j] == prefix) {
+            const uint32_t li = cand_li[j];
+            atomicOr(&bm[li >> 5], 1u << (li & 31u));
+          }
+        }
+        __syncthreads();
+        uint32_t c = 0;
+        for (int k = 0; k < per_t; ++k) {
+          const int w = tid * per_t + k;
+          if (w < words) c += (uint32_t)__popc(bm[w]);
+        }
+        uint32_t total;
+        const uint32_t below = block_excl_scan<NT>(c, S.warp_tot, total);
+        if (below < m && m <= below + c) {
+          uint32_t acc = below;
+          for (int k = 0; k < per_t; ++k) {
+            const int w = tid * per_t + k;
+            uint32_t word = bm[w];
+            const uint32_t cw = (uint32_t)__popc(word);
+            if (acc + cw >= m) {
+              for (uint32_t q = m - acc; q > 1u; --q) word &= word - 1u;  // drop the lower set bits
+              S.sel_bin = (int32_t)(32 * w + __ffs((int)word) - 1);
+              break;
+            }
+            acc += cw;
+          }
+        }
+        __syncthreads();
+        cut = b0 + S.sel_bin;
+      }
+    }
+    if (tid == 0) {
+      S.rule_prefix = prefix;
+      S.rule_shift = (uint32_t)shift;
+      S.rule_cut = cut;
+    }
+    __syncthreads();
+  } else if (cand_path) {
     if (C > 1) cluster_sync_all(); else __syncthreads();
     own_n = S.ncand;
     if (rank == 0 && !rule_ready) {
@@ -927,12 +1167,6 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
       }
       if (m > 0) store_blocks(mrow, (int64_t)b0 + i, m, kept, al16, al4);
     }
-    // tokens past the complete blocks: the tail is visible, the rest zero
-    const int64_t lo = 4 * (int64_t)n;
-    const int64_t span = ((int64_t)tokens - lo + C - 1) / C;
-    const int64_t a = lo + (int64_t)rank * span;
-    const int64_t b = a + span < tokens ? a + span : tokens;
-    fill_visible(mrow, a, b, p);
   } else if (rank == 0 && tid == 0) {
     report_error(status, kErrNonFinite, row);
   }
@@ -989,9 +1223,10 @@ static int sm_count() { return device_sm_count(); }
 // Cluster size for a launch: split a row over a cluster when its blocks
 // overflow one CTA's key cache, and then, for launches of a few such rows,
 // further while the whole launch stays within half the GPU and every CTA keeps
-// at least 4096 keys (one 65536-block row: 13.7 us on 4 CTAs, 11.3 us on 16; 32
-// such rows are fastest on 4 each: more CTAs than one wave cost more in
-// cluster barriers and remote reads than they gain).
+// at least 8192 keys (one 65536-block row: 12.3 us on 4 CTAs, 10.5 us on 8,
+// 11.0 us on 16; 32 rows of 32768-65536 blocks: 12.4 us on 4 CTAs each, 12.8 on
+// 8, 16.4 on 16 -- past one wave the cluster barriers and remote reads cost
+// more than the split gains).
 int select_cluster_size(int64_t n_rows, int64_t tokens) {
   const int64_t n_max = tokens / kRatio;
   const int cmax = max_cluster_size();
@@ -1005,7 +1240,7 @@ int select_cluster_size(int64_t n_rows, int64_t tokens) {
   }
   while (C < cmax && (n_max + C - 1) / C > kSelCapMax) C <<= 1;
   // (a row that fits one CTA stays on one: its cluster barriers would cost more)
-  while (C > 1 && 2 * C <= cmax && n_rows * 2 * C <= sm_count() / 2 && n_max / (2 * C) >= 4096)
+  while (C > 1 && 2 * C <= cmax && n_rows * 2 * C <= sm_count() / 2 && n_max / (2 * C) >= 8192)
     C <<= 1;
   return C;
 }

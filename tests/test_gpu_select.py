@@ -182,6 +182,54 @@ def test_select_cluster_split_rows(qsa, orc, rows):
         assert np.array_equal(got[r], want[r]), r
 
 
+@pytest.mark.parametrize("rows", [3, 32])
+@pytest.mark.parametrize("kind", ["plateau", "plateau_one_slice", "low_bits", "stress", "nonfinite"])
+def test_select_cluster_rows_rounds_and_ties(qsa, orc, kind, rows):
+    """Few long rows on clusters of the key-caching shape (3 rows: 8 CTAs each,
+    32 rows: 4 each), where every CTA runs the candidate rounds on its own list.
+    A plateau of equal keys straddling the cut, spread over every rank's slice
+    or inside one slice (the cut placed by the ranks' tie counts); keys that
+    differ only in their last four bits (every round, then the final one-key
+    check); stress scores; a non-finite score in a middle rank's slice."""
+    rng = qi.rng_for(4, salt=1000 + rows)
+    tokens = 262144
+    cols = tokens // 4
+    pos = np.full(rows, tokens - 1, np.int32)
+    pos[1::3] = tokens - 2
+    pos[2::3] = tokens - 7 - 4 * rng.integers(0, 30000, size=len(pos[2::3]))
+    if kind == "stress":
+        scores = qi.stress_scores(rng, rows, cols)
+    else:
+        scores = rng.random((rows, cols), dtype=np.float32)
+        for r in range(rows):
+            n = (int(pos[r]) + 1) // 4
+            hi = rng.choice(n, 300, replace=False)            # kept outright
+            scores[r, hi] = np.float32(2.0) + rng.random(300, dtype=np.float32)
+            if kind == "plateau_one_slice":                    # 600 blocks inside one slice
+                start = int(rng.integers(n // 3, n // 3 + 2000))
+                mid = np.setdiff1d(np.arange(start, start + 1200, 2), hi)[:600]
+            else:
+                mid = np.setdiff1d(rng.choice(n, 900, replace=False), hi)[:600]
+            if kind == "low_bits":
+                bits = np.float32(1.5).view(np.uint32) + rng.integers(0, 16, size=len(mid)).astype(np.uint32)
+                scores[r, mid] = bits.astype(np.uint32).view(np.float32)
+            else:
+                scores[r, mid] = np.float32(1.5)
+    expect_row = None
+    if kind == "nonfinite":
+        scores[1, 40000] = np.nan
+        expect_row = 1
+    for budget in (512, 2044, 2048):
+        got, row = gpu_select(qsa, scores, cols, pos, tokens, budget, expect=4 if expect_row else 0)
+        want, codes = oracle_masks(orc, scores, cols, pos, tokens, budget)
+        for r in range(rows):
+            if r == expect_row:
+                assert row == r and codes[r] == 4
+                assert np.all((got[r] == 0xAB) | (got[r] <= 1))   # unspecified, within the row
+            else:
+                assert np.array_equal(got[r], want[r]), (kind, budget, r, pos[r])
+
+
 def test_select_low_byte_differences_and_deep_truncation(qsa, orc):
     """Keys that differ only in their lowest byte, and budget 4 at 256k."""
     rng = qi.rng_for(4, salt=99)

@@ -106,9 +106,15 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 
+// Cluster barrier whose release covers shared memory only: the CTAs of a
+// cluster exchange nothing but their shared memory (no CTA reads another's
+// global writes), so an arrive need not wait for the mask stores in flight.
 __device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
+  asm volatile(
+      "fence.release.sync_restrict::shared::cta.cluster;\n\t"
+      "barrier.cluster.arrive.relaxed.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_dsmem(const uint32_t *local, uint32_t rank) {

@@ -88,6 +88,8 @@ struct SelectSmem {
   uint32_t rabove[kRounds];  // ... and the keys above it
   uint32_t kmin, kmax;       // the candidates under the prefix: their key range
   uint32_t coarse[64];       // in a cluster: this CTA's round-0 counts over runs of 64 bins
+  uint32_t lmax;             // in a cluster: this CTA's highest non-empty round-0 bin
+  uint32_t rowmax;           // ... and the row's
   uint32_t sel_cnt;          // in a cluster: the selected round-0 bin's count over the cluster
   // in a cluster, per candidate round r (1..3, and 4 for a final check):
   uint32_t rcnt[kRounds];          //   the round's bin count over the cluster
@@ -146,18 +148,62 @@ __device__ __forceinline__ uint32_t cluster_bin(const uint32_t *H, int b, int C)
   return t;
 }
 
-// Round 0's bin over a cluster, in two levels: the ranks' 64 run sums, then
-// the chosen run's 64 bins of every rank; and the non-finite verdict (the
-// 16 outer bins).  Every thread of the CTA calls it; the results land in
-// S.sel_bin / sel_above / sel_cnt and the verdict is returned.
+// Round 0's bin over a cluster and the non-finite verdict (the 16 outer
+// bins).  First, in one read of the peers: the kWin0 bins ending 32 above
+// this CTA's own highest one, summed over the ranks, with the ranks' highest
+// bins.  If that window reaches the row's highest bin and holds at least
+// need keys, the need-th key's bin is in it (no key lies above it).
+// Otherwise, in two levels: the ranks' 64 run sums, then the chosen run's 64
+// bins of every rank.  Every CTA reaches the same bin, whichever way.  Every
+// thread of the CTA calls it; the results land in S.sel_bin / sel_above /
+// sel_cnt and the verdict is returned.
+constexpr int kWin0 = 128;
+
 template <int NT>
 __device__ __forceinline__ bool cluster_find_round0(SelectSmem &S, int C, uint32_t need) {
+  static_assert(NT >= kWin0 + 64, "the window, the outer bins and the ranks' maxima need their own threads");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t *M = S.msmall;  // merged run sums, then the run's merged bins
+  uint32_t *M = S.msmall;  // merged window bins; else run sums, then the run's bins
+  const int w0 = min(max((int)S.lmax + 32 - (kWin0 - 1), 0), 4096 - kWin0);
   bool nf = false;
-  if (tid < 64) M[tid] = cluster_bin(S.coarse, tid, C);
-  else if (tid < 80) nf = cluster_bin(S.hist0, tid < 72 ? tid - 64 : 4088 + (tid - 72), C) != 0u;
+  if (tid < kWin0) {
+    M[tid] = cluster_bin(S.hist0, w0 + tid, C);
+  } else if (tid < kWin0 + 16) {
+    const int o = tid - kWin0;
+    nf = cluster_bin(S.hist0, o < 8 ? o : 4088 + (o - 8), C) != 0u;
+  } else if (warp == kWin0 / 32 + 1) {
+    uint32_t m = lane < C ? ld_dsmem(&S.lmax, (uint32_t)lane) : 0u;
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane == 0) S.rowmax = m;
+  }
   if (__syncthreads_or(nf)) return true;
+  if (S.rowmax <= (uint32_t)(w0 + kWin0 - 1)) {
+    if (warp == 0) {
+      uint32_t sum = 0;
+#pragma unroll
+      for (int j = 0; j < kWin0 / 32; ++j) sum += M[lane * (kWin0 / 32) + j];
+      const uint32_t total = __reduce_add_sync(0xffffffffu, sum);
+      int32_t sb = -1;
+      uint32_t ab = 0, cb = 0;
+      if (total >= need) {
+        uint32_t B, above;
+        warp_find_bin(M, kWin0, need, lane, B, above);
+        sb = w0 + (int32_t)B;
+        ab = above;
+        cb = M[B];
+      }
+      if (lane == 0) {
+        S.sel_bin = sb;
+        S.sel_above = ab;
+        S.sel_cnt = cb;
+      }
+    }
+    __syncthreads();
+    if (S.sel_bin >= 0) return false;
+    __syncthreads();  // (M and sel_bin are rewritten below)
+  }
+  if (tid < 64) M[tid] = cluster_bin(S.coarse, tid, C);
+  __syncthreads();
   if (warp == 0) {
     uint32_t B, above;
     warp_find_bin(M, 64, need, lane, B, above);
@@ -293,6 +339,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
     S.ncand = 0u;
     S.eq_base = 0u;
     S.band_hi = 0u;
+    S.lmax = 0u;
 #pragma unroll
     for (int r = 0; r <= kRounds; ++r) {
       S.kmin_r[r] = 0xFFFFFFFFu;
@@ -575,15 +622,22 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         constexpr int kPer = 4096 / NT;    // bins per thread: 8 or 16
         constexpr int kGroup = 64 / kPer;  // threads per run of 64 bins
         const uint4 *h4 = reinterpret_cast<const uint4 *>(S.hist0 + tid * kPer);
-        uint32_t t = 0;
+        uint32_t t = 0, hb = 0;  // (hb: the thread's highest non-empty bin)
 #pragma unroll
         for (int k = 0; k < kPer / 4; ++k) {
           const uint4 v = h4[k];
           t += v.x + v.y + v.z + v.w;
+          const uint32_t b = (uint32_t)(tid * kPer + 4 * k);
+          hb = v.x ? b : hb;
+          hb = v.y ? b + 1u : hb;
+          hb = v.z ? b + 2u : hb;
+          hb = v.w ? b + 3u : hb;
         }
 #pragma unroll
         for (int off = 1; off < kGroup; off <<= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
         if ((tid & (kGroup - 1)) == 0) S.coarse[tid / kGroup] = t;
+        hb = __reduce_max_sync(0xffffffffu, hb);
+        if (lane == 0 && hb) atomicMax(&S.lmax, hb);
       }
       cluster_sync_all();  // every rank's bins and run sums are final until the next one
       bad = cluster_find_round0<NT>(S, C, need);  // the same verdict in every CTA of the cluster

@@ -183,14 +183,18 @@ def test_select_cluster_split_rows(qsa, orc, rows):
 
 
 @pytest.mark.parametrize("rows", [3, 32])
-@pytest.mark.parametrize("kind", ["plateau", "plateau_one_slice", "low_bits", "stress", "nonfinite"])
+@pytest.mark.parametrize("kind", ["plateau", "plateau_one_slice", "low_bits", "stress", "nonfinite",
+                                  "skewed", "sparse_top"])
 def test_select_cluster_rows_rounds_and_ties(qsa, orc, kind, rows):
     """Few long rows on clusters of the key-caching shape (3 rows: 8 CTAs each,
     32 rows: 4 each), where every CTA runs the candidate rounds on its own list.
     A plateau of equal keys straddling the cut, spread over every rank's slice
     or inside one slice (the cut placed by the ranks' tie counts); keys that
     differ only in their last four bits (every round, then the final one-key
-    check); stress scores; a non-finite score in a middle rank's slice."""
+    check); stress scores; a non-finite score in a middle rank's slice; one
+    slice holding every large score, so the other CTAs' first window over the
+    round-0 bins misses the row's highest bin; and 300 huge scores over tiny
+    ones, so the window holds too few keys for budgets above 1200."""
     rng = qi.rng_for(4, salt=1000 + rows)
     tokens = 262144
     cols = tokens // 4
@@ -199,6 +203,17 @@ def test_select_cluster_rows_rounds_and_ties(qsa, orc, kind, rows):
     pos[2::3] = tokens - 7 - 4 * rng.integers(0, 30000, size=len(pos[2::3]))
     if kind == "stress":
         scores = qi.stress_scores(rng, rows, cols)
+    elif kind == "skewed":
+        scores = rng.random((rows, cols), dtype=np.float32)
+        for r in range(rows):
+            n = (int(pos[r]) + 1) // 4
+            scores[r, 3 * n // 4:n] *= np.float32(2.0 ** 40)
+    elif kind == "sparse_top":
+        scores = rng.random((rows, cols), dtype=np.float32) * np.float32(2.0 ** -100)
+        for r in range(rows):
+            n = (int(pos[r]) + 1) // 4
+            hi = rng.choice(n, 300, replace=False)
+            scores[r, hi] = (np.float32(1.0) + rng.random(300, dtype=np.float32)) * np.float32(2.0 ** 100)
     else:
         scores = rng.random((rows, cols), dtype=np.float32)
         for r in range(rows):

@@ -20,9 +20,9 @@
 //    (exact zeros, the heavy bin of relu scores, go to one spare bin per lane
 //    and are folded in afterwards); a non-finite score shows up as a count in
 //    one of the 16 outer bins, so no per-key check is needed.  In a cluster
-//    every CTA finds the selected bin itself, in two short reads of its
-//    peers' shared memory (the ranks' sums over runs of 64 bins, then the
-//    chosen run's bins), without merging the 4096 bins;
+//    every CTA finds the selected bin itself from its peers' shared memory,
+//    without merging the 4096 bins: a window below its own highest bin in one
+//    read, else the ranks' sums over runs of 64 bins, then the chosen run's;
 //  * one pass over the keys then writes the final mask bytes of every key
 //    outside the selected bin and marks the quads that hold the bin's keys; a
 //    second, short walk over the marked quads lists those keys (with their

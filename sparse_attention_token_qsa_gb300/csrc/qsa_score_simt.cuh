@@ -164,13 +164,15 @@ __device__ __forceinline__ bool simt_score_blocks(const ScoreArgs &a, int row, i
 
   const int gi = tid >> 3;
   const int g = tid & 7;
-  float qr[kHeads][2][8];
+  // the lane's 16 query dims per head as (even, odd) pairs for packed FMAs
+  float2 qr[kHeads][2][4];
 #pragma unroll
   for (int h = 0; h < kHeads; ++h)
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) qr[h][j][e] = S.q_s[h][8 * (8 * j + g) + e];
+      for (int i = 0; i < 4; ++i)
+        qr[h][j][i] = make_float2(S.q_s[h][8 * (8 * j + g) + 2 * i], S.q_s[h][8 * (8 * j + g) + 2 * i + 1]);
 
   float *srow = a.scores + (int64_t)row * a.score_cols;
   const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
@@ -198,16 +200,25 @@ __device__ __forceinline__ bool simt_score_blocks(const ScoreArgs &a, int row, i
     }
 #pragma unroll
     for (int u = 0; u < kSimtUnroll; ++u) {
-      float acc[kHeads] = {0.f, 0.f, 0.f, 0.f};
+      // per head, the even and the odd dims summed apart by one packed FMA
+      // per dim pair (the two bf16 of a key word unpacked side by side), then
+      // added
+      float2 acc2[kHeads];
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) acc2[h] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        float k[8];
-        unpack8(kv[u][j], k);
+        const uint32_t w[4] = {kv[u][j].x, kv[u][j].y, kv[u][j].z, kv[u][j].w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
+        for (int i = 0; i < 4; ++i) {
+          const float2 kk = make_float2(lo_bf16(w[i]), hi_bf16(w[i]));
 #pragma unroll
-          for (int h = 0; h < kHeads; ++h) acc[h] = fmaf(qr[h][j][e], k[e], acc[h]);
+          for (int h = 0; h < kHeads; ++h) acc2[h] = __ffma2_rn(qr[h][j][i], kk, acc2[h]);
+        }
       }
+      float acc[kHeads];
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) acc[h] = acc2[h].x + acc2[h].y;
       // reduce-scatter the 4 head sums over the 8 lanes of the group
       const bool up4 = g & 4;
       float keep0 = up4 ? acc[2] : acc[0];

@@ -73,9 +73,12 @@ typedef enum {
 
 /* Which scorer qsa_score_rows_with runs. */
 typedef enum {
-    QSA_SCORE_AUTO = 0,   /* host picks: tensor cores for many rows sharing one key set */
-    QSA_SCORE_SIMT = 1,   /* bandwidth-bound warp-dot scorer (decode shape, any rows) */
-    QSA_SCORE_TCGEN05 = 2 /* tcgen05/TMEM/TMA tile scorer; needs key_base == NULL */
+    QSA_SCORE_AUTO = 0,    /* host picks: the tile scorer for many rows sharing one key set,
+                              else the streaming one */
+    QSA_SCORE_SIMT = 1,    /* bandwidth-bound warp-dot scorer (decode shape, any rows) */
+    QSA_SCORE_TCGEN05 = 2, /* tcgen05/TMEM/TMA tile scorer; needs key_base == NULL */
+    QSA_SCORE_STREAM = 3   /* streaming tcgen05 scorer: each row's 128-block tiles fetched
+                              by TMA, scored against its 4 heads (decode shape, any rows) */
 } qsa_score_path;
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -86,10 +89,11 @@ const char *qsa_status_string(int32_t status);
 
 /*
  * The limit of the bounded device waits a caller may shorten, in SM clock
- * cycles (default 4e9, about 2 s at 2 GHz): the streaming scorer's wait for
- * each stage of block keys it copies into shared memory (qsa_score_rows on
- * the SIMT path), and the fused decode step's waits for its key copies, its
- * MMAs and its barrier over a row's CTAs (qsa_decode_index_select).  A wait
+ * cycles (default 4e9, about 2 s at 2 GHz): the streaming scorers' waits for
+ * the block keys they copy into shared memory and for their MMAs
+ * (qsa_score_rows on the SIMT and QSA_SCORE_STREAM paths), and the fused
+ * decode step's waits for its key copies, its MMAs and its barrier over a
+ * row's CTAs (qsa_decode_index_select).  A wait
  * that reaches the limit records QSA_ERR_TIMEOUT with its row in dev_status
  * and the row's output is left unspecified (a fused decode call may then
  * leave its workspace dirty: zero it before the next call); the CTA first
@@ -166,10 +170,12 @@ qsa_status qsa_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t fir
  *  workspace   DEVICE scratch owned by the caller, or NULL; 16-byte aligned.
  *              The tensor-core scorer needs qsa_score_workspace_bytes(n_rows)
  *              bytes for the prepared query heads; its contents on entry do
- *              not matter and are overwritten.  The SIMT scorer uses none.
+ *              not matter and are overwritten.  The streaming scorers use
+ *              none.
  * qsa_score_rows picks the scorer itself (QSA_SCORE_AUTO): the tensor-core
- * scorer for 64 or more rows sharing one key set (key_base == NULL) when the
- * workspace is large enough, the SIMT scorer otherwise.
+ * tile scorer for 64 or more rows sharing one key set (key_base == NULL) when
+ * the workspace is large enough, the streaming tcgen05 scorer otherwise (its
+ * scores equal the fused decode launch's: the same MMA per block).
  */
 qsa_status qsa_score_rows(const uint16_t *q, int64_t q_stride, const int32_t *pos,
                           const int32_t *visible_len, int32_t n_rows, int32_t tokens,
@@ -259,7 +265,8 @@ qsa_status qsa_select_mask(const float *scores, int64_t score_cols, const int32_
  *  block_keys  DEVICE pooled-key cache (read and written);
  *  scores      DEVICE f32 work buffer of n_rows * score_cols (its contents
  *              afterwards are the rows' scores);
- *  workspace, workspace_bytes: as qsa_score_rows (NULL selects the SIMT scorer).
+ *  workspace, workspace_bytes: as qsa_score_rows (NULL selects the streaming
+ *              scorer).
  */
 qsa_status qsa_index_select(const uint16_t *keys, int64_t key_stride, int32_t pool_first_block,
                             int32_t pool_n_blocks, const uint16_t *k_norm_w, const uint16_t *q,
@@ -292,9 +299,9 @@ int64_t qsa_decode_workspace_bytes(int32_t n_rows, int32_t tokens);
  * The scores equal those of qsa_index_select's tensor-core scorer (same MMA
  * shape and accumulation order) and the mask is the selector's on them.
  * When the rows' CTAs cannot all be resident at once, the call falls back to
- * the streaming scorer and the selector as two launches (the workspace is not
- * used; scores within the scoring tolerance of the tensor-core ones, the
- * mask exact on them).
+ * the streaming tcgen05 scorer and the selector as two launches (the
+ * workspace is not used; the same scores, since that scorer runs the same
+ * MMA per block, and the same mask).
  *  arguments   as qsa_index_select, except:
  *  decode_ws   DEVICE workspace of at least qsa_decode_workspace_bytes(n_rows,
  *              tokens) bytes, 16-byte aligned, ZERO before the first call.

@@ -30,6 +30,7 @@ QSA_ERR_TOKEN_RANGE = 6
 QSA_SCORE_AUTO = 0
 QSA_SCORE_SIMT = 1
 QSA_SCORE_TCGEN05 = 2
+QSA_SCORE_STREAM = 3
 
 HEADS, HEAD_DIM, RATIO, ROT_DIM, FUSED_WIDTH = 4, 128, 4, 64, 640
 

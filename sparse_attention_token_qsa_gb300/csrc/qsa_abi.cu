@@ -169,8 +169,9 @@ bool score_ws_ok(const void *workspace, int64_t workspace_bytes, int32_t n_rows)
          workspace_bytes >= qsa_score_workspace_bytes(n_rows) && (int64_t)n_rows * 4 <= INT32_MAX;
 }
 
-// QSA_SCORE_AUTO's choice: the tensor-core scorer once there are enough rows
-// to fill its 64-row tiles and blocks to fill a key tile, else streaming.
+// QSA_SCORE_AUTO's choice: the tensor-core tile scorer once there are enough
+// rows to fill its 64-row tiles and blocks to fill a key tile, else the
+// streaming tensor-core scorer.
 bool auto_picks_tc(const int64_t *key_base, bool ws_ok, int32_t n_rows, int32_t tokens) {
   return qsa::kTcScorerReady && key_base == nullptr && ws_ok && n_rows >= 64 && tokens >= 2048;
 }
@@ -185,7 +186,8 @@ qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_
                                float *scores, int64_t score_cols, int32_t *dev_status,
                                int32_t path, void *workspace, int64_t workspace_bytes,
                                void *stream) {
-  if (path != QSA_SCORE_AUTO && path != QSA_SCORE_SIMT && path != QSA_SCORE_TCGEN05)
+  if (path != QSA_SCORE_AUTO && path != QSA_SCORE_SIMT && path != QSA_SCORE_TCGEN05 &&
+      path != QSA_SCORE_STREAM)
     return QSA_ERR_INVALID_VALUE;
   if (workspace_bytes < 0) return QSA_ERR_INVALID_VALUE;
   qsa_status st = check_score_args(q, q_stride, pos, n_rows, tokens, q_norm_w, cos_t, sin_t,
@@ -197,9 +199,10 @@ qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_
                    q_norm_w,   cos_t,    sin_t, eps,         block_keys, key_base,
                    scores,     score_cols, dev_status, qsa::wait_limit_cycles()};
   if (path == QSA_SCORE_AUTO)
-    path = auto_picks_tc(key_base, ws_ok, n_rows, tokens) ? QSA_SCORE_TCGEN05 : QSA_SCORE_SIMT;
+    path = auto_picks_tc(key_base, ws_ok, n_rows, tokens) ? QSA_SCORE_TCGEN05 : QSA_SCORE_STREAM;
   if (path == QSA_SCORE_TCGEN05)
     return from_cuda(qsa::launch_score_tc(a, static_cast<uint16_t *>(workspace), (cudaStream_t)stream));
+  if (path == QSA_SCORE_STREAM) return from_cuda(qsa::launch_score_stream(a, (cudaStream_t)stream));
   return from_cuda(qsa::launch_score_simt(a, (cudaStream_t)stream));
 }
 
@@ -317,7 +320,7 @@ qsa_status qsa_decode_index_select(const uint16_t *keys, int64_t key_stride,
   if (st != QSA_OK || launched) return st;
   // more rows than can be co-resident: pool, score and select in turn
   if (pool_inside && (st = pool_launch()) != QSA_OK) return st;
-  st = from_cuda(qsa::launch_score_simt(a, s));
+  st = from_cuda(qsa::launch_score_stream(a, s));
   if (st != QSA_OK) return st;
   return from_cuda(qsa::launch_select(scores, score_cols, pos, n_rows, tokens, budget, mask,
                                       dev_status, s));

@@ -79,6 +79,9 @@ struct ScoreArgs {
 long long wait_limit_cycles();
 
 cudaError_t launch_score_simt(const ScoreArgs &a, cudaStream_t stream);
+// Streaming tensor-core scorer: the SIMT scorer's rows and ranges, each
+// 128-block tile scored by tcgen05 MMAs from TMA-fetched keys.
+cudaError_t launch_score_stream(const ScoreArgs &a, cudaStream_t stream);
 // Prepared query heads, [n_rows * 4, 128] bf16, into a workspace; the same
 // launch pools `pool`'s blocks when it is given (its own CTAs).
 cudaError_t launch_qprep(const ScoreArgs &a, uint16_t *qws, cudaStream_t stream,

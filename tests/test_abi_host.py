@@ -106,7 +106,7 @@ def test_score_refusals(lib):
     for kw in (dict(q_stride=504), dict(q_stride=644), dict(q=U), dict(keys=U), dict(scores=U),
                dict(cols=1020), dict(cols=1022), dict(rows=4095), dict(eps=-1e-6),
                dict(q=0), dict(pos=0), dict(keys=0), dict(scores=0), dict(w=0), dict(cos=0),
-               dict(path=3), dict(path=2, base=B, ws=A, wsb=1 << 20), dict(path=2),
+               dict(path=4), dict(path=-1), dict(path=2, base=B, ws=A, wsb=1 << 20), dict(path=2),
                dict(path=2, ws=A, wsb=3 * 1024 - 1), dict(path=2, ws=U, wsb=1 << 20),
                dict(wsb=-1)):
         assert score(lib, n_rows=3, **kw) == 1, kw

@@ -51,7 +51,7 @@ def run_both(qsa, tables, cache_np, q_np, pos_np, tokens, cols, qw, budget=BUDGE
     c, s, cd, sd = tables
     n_rows = len(pos_np)
     out = []
-    for entry in ("decode", "tc", "simt"):
+    for entry in ("decode", "tc", "stream"):
         cache = dev(cache_np.copy())
         sc = torch.full((n_rows, cols), -7.0, dtype=torch.float32, device="cuda")
         buf = torch.full((n_rows * tokens + mask_offset + 16,), 0xAB, dtype=torch.uint8,
@@ -324,7 +324,7 @@ def test_decode_pools_new_blocks_in_the_same_launch(qsa, orc, tables, first, cou
     pos = np.array([last, 4 * first + 2, last - 1], np.int32)
     q_np = qi.normal_bf16(rng, (3, 512))
     outs = []
-    for entry in ("decode", "tc", "simt"):
+    for entry in ("decode", "tc", "stream"):
         cache = dev(cache_np)
         sc = torch.full((3, nb), -7.0, dtype=torch.float32, device="cuda")
         mask = torch.full((3, tokens), 0xAB, dtype=torch.uint8, device="cuda")
@@ -396,7 +396,7 @@ def test_decode_long_rows_past_64k(qsa, orc):
     qw, _ = qi.norm_weights(rng)
     pos = np.array([tokens - 1, 100001], np.int32)
     outs = []
-    for entry in ("decode", "tc", "simt"):
+    for entry in ("decode", "tc", "stream"):
         cache = dev(cache_np)
         sc = torch.full((2, nb), -7.0, dtype=torch.float32, device="cuda")
         mask = torch.full((2, tokens), 0xAB, dtype=torch.uint8, device="cuda")

@@ -92,7 +92,7 @@ def pooled_prefill(orc, case, c, s):
     return orc.pool_blocks(case["fq"].reshape(-1)[512:], 640, 0, nb, case["k_norm_w"], c, s, EPS)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_score_prefill_all_rows(qsa, orc, tables, path):
     """Every row of the 2304-token prefill, scored against the oracle's pooled keys;
     entries past each row's prefix keep their sentinel."""
@@ -115,8 +115,10 @@ def test_score_prefill_all_rows(qsa, orc, tables, path):
     assert worst < 5e-3
 
 
-def test_score_decode_rows_long_context(qsa, orc, tables):
-    """Decode rows at 64k (16384 blocks each), visible_len and key_base variants."""
+@pytest.mark.parametrize("path", [1, 3])
+def test_score_decode_rows_long_context(qsa, orc, tables, path):
+    """Decode rows at 64k (16384 blocks each), visible_len and key_base variants,
+    on the SIMT and the streaming tcgen05 scorer."""
     case = long_keys_case()
     keys_raw = case["keys"]
     c, s, cd, sd = tables
@@ -131,9 +133,9 @@ def test_score_decode_rows_long_context(qsa, orc, tables):
     for use_vis, use_base in ((False, False), (True, False), (True, True)):
         sc = torch.full((rows, cols), -7.0, dtype=torch.float32, device="cuda")
         st = qsa.new_status()
-        qsa.qsa_score_rows(dev(q), 512, dev(pos), dev(vis) if use_vis else None, rows, 65536,
-                           dev(case["q_norm_w"]), cd, sd, c.shape[0], EPS, dev(keys),
-                           dev(base) if use_base else None, sc, cols, st)
+        qsa.qsa_score_rows_with(dev(q), 512, dev(pos), dev(vis) if use_vis else None, rows,
+                                65536, dev(case["q_norm_w"]), cd, sd, c.shape[0], EPS, dev(keys),
+                                dev(base) if use_base else None, sc, cols, st, path=path)
         assert qsa.qsa_read_status(st) == (0, 0)
         got = sc.cpu().numpy()
         want, _ = oracle_scores(orc, q, 512, pos, 65536, case["q_norm_w"], c, s, keys, cols,
@@ -142,8 +144,11 @@ def test_score_decode_rows_long_context(qsa, orc, tables):
         assert_close(got, want, f"decode scores vis={use_vis} base={use_base}")
 
 
-def test_score_key_base_per_sequence(qsa, orc, tables):
-    """Rows of different sequences in one call: key_base selects each row's key set."""
+@pytest.mark.parametrize("path", [0, 1, 3])
+def test_score_key_base_per_sequence(qsa, orc, tables, path):
+    """Rows of different sequences in one call: key_base selects each row's key set
+    (the last row's blocks end the key buffer, so a scorer that read past them
+    would read past the allocation)."""
     rng = qi.rng_for(3, salt=1)
     c, s, cd, sd = tables
     lens = [4000, 9000, 6001]
@@ -163,14 +168,14 @@ def test_score_key_base_per_sequence(qsa, orc, tables):
     cols = 2252
     sc = torch.full((3, cols), -7.0, dtype=torch.float32, device="cuda")
     st = qsa.new_status()
-    qsa.qsa_score_rows(dev(q), 512, dev(pos), None, 3, 9000, dev(qw), cd, sd, c.shape[0], EPS,
-                       dev(keys), dev(base), sc, cols, st)
+    qsa.qsa_score_rows_with(dev(q), 512, dev(pos), None, 3, 9000, dev(qw), cd, sd, c.shape[0],
+                            EPS, dev(keys), dev(base), sc, cols, st, path=path)
     assert qsa.qsa_read_status(st) == (0, 0)
     want, _ = oracle_scores(orc, q, 512, pos, 9000, qw, c, s, keys, cols, key_base=base)
     assert_close(sc.cpu().numpy(), want, "per-sequence scores")
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_score_nan_key_propagates(qsa, orc, tables, path):
     case = prefill_case(T=512)
     c, s, cd, sd = tables
@@ -332,7 +337,7 @@ def test_pool_rounds_the_mean_to_bf16_like_the_oracle(qsa, orc, tables):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_score_one_hot_queries_rotate_at_their_positions(qsa, orc, tables, path):
     """One-hot query heads on dim i against one-hot keys e_i and e_{i+32}: the
     two scores are the rotated query's cos and sin components, so they pin the

@@ -113,7 +113,7 @@ def test_decode_random_cases(qsa, orc):
         first = int(rng.integers(0, max(1, nb)))
         cnt = int(rng.integers(0, min(200, nb - first) + 1)) if nb > first else 0
         outs = []
-        for entry in ("decode", "tc", "simt"):
+        for entry in ("decode", "tc", "stream"):
             cache = torch.zeros((max(nb, 1), 128), dtype=torch.int16, device="cuda")
             if nb:
                 qsa.qsa_pool_blocks(d16(raw).view(-1), 128, 0, nb, d16(kw), cd, sd, c.shape[0], EPS,

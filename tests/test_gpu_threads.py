@@ -42,7 +42,7 @@ def chain(qsa, seed, stream):
         st = qsa.new_status()
         cache = torch.zeros((nb, 128), dtype=torch.int16, device=dev_)
         qsa.qsa_pool_blocks(raw, 128, 0, nb, kw, cd, sd, T, EPS, cache, stream=stream)
-        for path in (qsa.QSA_SCORE_SIMT, qsa.QSA_SCORE_TCGEN05):
+        for path in (qsa.QSA_SCORE_SIMT, qsa.QSA_SCORE_TCGEN05, qsa.QSA_SCORE_STREAM):
             sc = torch.full((R, nb), -7.0, dtype=torch.float32, device=dev_)
             qsa.qsa_score_rows_with(fq, 640, pos, None, R, T, qw, cd, sd, T, EPS, cache, None, sc,
                                     nb, st, path=path, workspace=qsa.new_workspace(R, dev_),

@@ -75,9 +75,11 @@ def test_decode_barrier_runs_out_then_the_next_call_is_exact(orc):
         assert np.array_equal(got[i], want[i]), f"row {i}"
 
 
-def test_streaming_scorer_ring_wait_runs_out_then_the_next_call_is_exact(orc):
-    """The streaming scorer's wait for each landed stage of its key ring takes
-    the same limit.  64 rows of 64k, each over its own 4 MiB of block keys
+@pytest.mark.parametrize("path", ["simt", "stream"])
+def test_streaming_scorer_ring_wait_runs_out_then_the_next_call_is_exact(orc, path):
+    """The streaming scorers' waits for each landed stage of their key ring (and,
+    on the tcgen05 one, for the query operand and each accumulator) take the
+    same limit.  64 rows of 64k, each over its own 4 MiB of block keys
     (256 MiB in all, twice L2), keep the kernel bound by its copies, so its
     consumers find stages still in flight; cut to one cycle, such a wait gives
     up, the CTA drains its own copies and records QSA_ERR_TIMEOUT.  Restored,
@@ -99,7 +101,8 @@ def test_streaming_scorer_ring_wait_runs_out_then_the_next_call_is_exact(orc):
     def run():
         sc = torch.full((n_rows, nb), -7.0, dtype=torch.float32, device="cuda")
         st = qsa.new_status()
-        qsa.qsa_score_rows_with(*head, sc, nb, st, path=qsa.QSA_SCORE_SIMT)
+        qsa.qsa_score_rows_with(*head, sc, nb, st, path=qsa.QSA_SCORE_SIMT if path == "simt"
+                                else qsa.QSA_SCORE_STREAM)
         return sc, qsa.qsa_read_status(st)
 
     before, status = run()

@@ -266,10 +266,14 @@ cudaError_t launch_score_stream(const ScoreArgs &a, cudaStream_t stream) {
   CUtensorMap kmap;
   if (!encode_bf16_sw128(&kmap, a.block_keys, kHeadDim, 0x7fffffffull, kHeadDim, 64, kStTile))
     return cudaErrorInvalidValue;
-  // tiles per CTA: about four waves of two CTAs per SM over every row's tiles
+  // tiles per CTA: one wave of two CTAs per SM over every row's tiles at most
+  // (a CTA's ring fills and drains once, and no second wave runs half full:
+  // 32 rows of 131k-262k tokens in 63 us on one wave, 67 us on about two, 71
+  // us on four)
   const int64_t row_tiles = (n_max + kStTile - 1) / kStTile;
-  int64_t k = ((int64_t)a.n_rows * row_tiles) / (8 * (int64_t)device_sm_count());
-  k = k < 2 ? 2 : (k > 32 ? 32 : k);
+  int64_t k = ((int64_t)a.n_rows * row_tiles) / (2 * (int64_t)device_sm_count());
+  k = k < 2 ? 2 : k;
+  if (k > row_tiles) k = row_tiles;  // (one CTA per row)
   while ((row_tiles + k - 1) / k > 65535) ++k;
   const int32_t bpc = (int32_t)(k * kStTile);
   const dim3 grid((unsigned)a.n_rows, (unsigned)((n_max + bpc - 1) / bpc));

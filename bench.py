@@ -459,7 +459,7 @@ def run_ours(args, rank, world, device):
     for name, fn, bytes_per_launch, src in (
             ("decode_fused", wl.fused_only, SCORE_BYTES_PER_BLOCK * N_BLOCKS + TOKENS,
              DECODE_FUSED_SOURCES),
-            ("score", wl.score, SCORE_BYTES_PER_BLOCK * N_BLOCKS, "qsa_score_simt.cu"),
+            ("score", wl.score, SCORE_BYTES_PER_BLOCK * N_BLOCKS, "qsa_score_stream.cu"),
             ("select", wl.select, SELECT_BYTES_PER_BLOCK * N_BLOCKS + TOKENS, "qsa_select.cu")):
         gk = capture_graphs(torch, fn, steps[:min(K, 4096)])
         t_ms = time_graphs(torch, gk) / min(K, 4096)

@@ -64,7 +64,7 @@ typedef enum {
     QSA_OK = 0,
     QSA_ERR_INVALID_VALUE = 1, /* refused on the host; nothing launched */
     QSA_ERR_LAUNCH = 2,        /* the CUDA runtime refused a launch */
-    QSA_ERR_ROW_RANGE = 3,     /* device: pos or visible_len out of range */
+    QSA_ERR_ROW_RANGE = 3,     /* device: pos, visible_len (or key_base) out of range */
     QSA_ERR_NONFINITE = 4,     /* device: NaN/Inf score in a truncating row */
     QSA_ERR_TIMEOUT = 5,       /* device: a bounded wait gave up */
     QSA_ERR_TOKEN_RANGE = 6    /* device: a gathered token or its page lies outside
@@ -162,7 +162,11 @@ qsa_status qsa_pool_blocks(const uint16_t *keys, int64_t key_stride, int32_t fir
  *              blocks (the tensor-core scorer fetches whole 128-block tiles;
  *              blocks past a row's prefix are read but never used).
  *  key_base    DEVICE int64[n_rows] or NULL (= 0): per-row block offset, so one
- *              call can score rows of different sequences.
+ *              call can score rows of different sequences.  Only a row's own
+ *              blocks are read.  The streaming tcgen05 scorer addresses
+ *              blocks below 2^31 (512 GiB of keys): a row whose key_base +
+ *              blocks passes that, or a negative key_base, is recorded as
+ *              QSA_ERR_ROW_RANGE.
  *  scores      DEVICE f32, row stride score_cols (>= tokens/4, multiple of 4;
  *              spare capacity allowed), 16-byte aligned.  Row i gets entries
  *              b < blocks; entries past that are not written.

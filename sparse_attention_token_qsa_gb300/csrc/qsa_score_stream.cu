@@ -11,11 +11,11 @@
 //
 // Each CTA scores a contiguous range of one row's visible blocks, a 128-block
 // tile at a time, the way the fused decode launch scores its tiles:
-//  * warp 0 streams the tiles into a ring of shared-memory stages with TMA
-//    (two 64-dim boxes, 128-byte swizzle), refilling a stage once the MMAs
-//    that read it have finished; a last, partial tile is copied by the warp's
-//    lanes into the same layout (only the row's own blocks are read, so no
-//    tile reaches past the caller's key buffer);
+//  * warp 0 streams the whole tiles into a ring of shared-memory stages with
+//    TMA (two 64-dim boxes, 128-byte swizzle), refilling a stage once the MMAs
+//    that read it have finished; a partial tile goes first, copied by every
+//    thread at once into the same layout (only the row's own blocks are read,
+//    so no copy reaches past the caller's key buffer);
 //  * warps 2-3 prepare the row's four query heads as the 16 x 128 B operand
 //    (rows 4..15 zero);
 //  * one lane of warp 1 issues tcgen05.mma M128 N16 K16 x 8 per tile (keys on
@@ -116,56 +116,81 @@ score_stream_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   const int c1 = min(n, c0 + bpc);
   const int cnt = max(0, c1 - c0);
   const int tiles = (cnt + kStTile - 1) / kStTile;
+  const int tail = cnt % kStTile;  // blocks of a partial last tile
   const int64_t kbase = a.key_base ? a.key_base[row] : 0;
-  // whole tiles come by TMA (its row coordinate is a 32-bit int); the rest by
-  // the producer warp's lanes
-  const int tma_tiles = (kbase + c1 <= (int64_t)0x7fffffff) ? cnt / kStTile : 0;
+  // TMA's row coordinate is a 32-bit int: 2^31 blocks are 512 GiB of keys, so
+  // a row past it has an invalid key_base, reported like a bad position
+  const bool keys_ok = kbase >= 0 && kbase + c1 <= (int64_t)0x7fffffff;
+  const int ntiles = keys_ok ? tiles : 0;
   const long long lim = a.wait_limit > 0 ? a.wait_limit : kStSpinLimit;
   volatile int32_t *abort_flag = &C.abort;
   const uint32_t tmem = C.tmem_base;
+  // Tile t of the range: a partial tile, if any, comes first (t = 0), then
+  // the whole ones in order.  Its first block relative to c0:
+  auto tile_off = [&](int t) {
+    return tail ? (t == 0 ? (tiles - 1) * kStTile : (t - 1) * kStTile) : t * kStTile;
+  };
+  auto issue_tma = [&](int t) {  // a whole tile into stage t % kStStages (one thread)
+    const int s = t % kStStages;
+    const uint32_t fb = sm32(&C.full[s]);
+    const int y0 = (int)(kbase + c0 + tile_off(t));
+    mbar_expect_tx(fb, kStTileBytes);
+    tma_load_2d(sRing + s * kStTileBytes, &kmap, 0, y0, fb);
+    tma_load_2d(sRing + s * kStTileBytes + kStHalfBytes, &kmap, 64, y0, fb);
+  };
+  // ---- the first stages: the whole tiles by TMA, and the partial tile (only
+  // the row's own blocks, so no copy reaches past the caller's key buffer) by
+  // the six warps other than the query preparers, which meanwhile build the
+  // query operand: 16 bytes a load, each chunk where the swizzled copy would
+  // put it (chunk j of a box's row r at 16 * (j ^ (r % 8)))
+  const int first = min(kStStages, ntiles);
+  if (tid == 0) {
+    for (int t = tail ? 1 : 0; t < first; ++t) issue_tma(t);
+    C.issued = first;
+  }
+  if (tail && ntiles > 0 && (warp < 2 || warp >= 4)) {
+    constexpr int kCopiers = kStThreads - 64;
+    const int ct = (warp < 2 ? warp : warp - 2) * 32 + lane;
+    const uint16_t *src = a.block_keys + (kbase + c0 + tile_off(0)) * kHeadDim;
+    for (int i0 = 0; i0 < kStTile * 16; i0 += 4 * kCopiers) {
+      uint4 v[4];  // four loads in flight a thread
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kCopiers + ct, r = i >> 4, ch = i & 15;
+        v[u] = (i < kStTile * 16 && r < tail) ? ldg_nc_v4(src + (int64_t)r * kHeadDim + 8 * ch)
+                                              : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kCopiers + ct, r = i >> 4, ch = i & 15;
+        if (i < kStTile * 16)
+          *reinterpret_cast<uint4 *>(smem + (ch >> 3) * kStHalfBytes + r * 128 +
+                                     (((ch & 7) ^ (r & 7)) << 4)) = v[u];
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMAs
+    asm volatile("bar.sync 1, %0;" ::"n"(kCopiers) : "memory");
+    if (ct == 0) mbar_arrive(sm32(&C.full[0]));
+  }
 
   if (warp == 0) {
-    // ---- producer: tile t into stage t % kStStages once its previous tile's
-    // MMAs are done
-    for (int t = 0; t < tiles; ++t) {
+    // ---- producer: whole tile t into stage t % kStStages once the MMAs of
+    // the stage's previous tile are done
+    for (int t = first; t < ntiles; ++t) {
       const int s = t % kStStages;
-      if (t >= kStStages &&
-          !tc_warp_wait(sm32(&C.empty[s]), (uint32_t)((t / kStStages) - 1) & 1u, lim, abort_flag))
+      if (!tc_warp_wait(sm32(&C.empty[s]), (uint32_t)((t / kStStages) - 1) & 1u, lim, abort_flag))
         break;
-      const int32_t b0 = c0 + t * kStTile;
-      const uint32_t fb = sm32(&C.full[s]);
-      if (t < tma_tiles) {
-        if (lane == 0) {
-          mbar_expect_tx(fb, kStTileBytes);
-          tma_load_2d(sRing + s * kStTileBytes, &kmap, 0, (int)(kbase + b0), fb);
-          tma_load_2d(sRing + s * kStTileBytes + kStHalfBytes, &kmap, 64, (int)(kbase + b0), fb);
-        }
-      } else {
-        // 16-byte chunks of the tile's own blocks, each where the swizzled
-        // copy would put it (chunk j of a box's row r at 16 * (j ^ (r % 8))),
-        // zeros past the range
-        const int rows_here = c1 - b0;
-        uint8_t *stg = smem + s * kStTileBytes;
-        const uint16_t *src = a.block_keys + (kbase + b0) * kHeadDim;
-        for (int i = lane; i < kStTile * 16; i += 32) {
-          const int r = i >> 4, ch = i & 15;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (r < rows_here) v = ldg_nc_v4(src + (int64_t)r * kHeadDim + 8 * ch);
-          *reinterpret_cast<uint4 *>(stg + (ch >> 3) * kStHalfBytes + r * 128 +
-                                     (((ch & 7) ^ (r & 7)) << 4)) = v;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the MMAs
-        __syncwarp();
-        if (lane == 0) mbar_arrive(fb);
+      if (lane == 0) {
+        issue_tma(t);
+        C.issued = t + 1;
       }
-      if (lane == 0) C.issued = t + 1;
     }
   } else if (warp == 1) {
     // ---- MMA issuer: tile t into accumulator t % 2
-    if (lane == 0 && tiles > 0) {
+    if (lane == 0 && ntiles > 0) {
       bool ok = tc_wait(sm32(&C.qready), 0u, lim, abort_flag);
       if (ok) tc_fence_after();
-      for (int t = 0; t < tiles && ok; ++t) {
+      for (int t = 0; t < ntiles && ok; ++t) {
         const int s = t % kStStages, acc = t & 1;
         if (!(ok = tc_wait(sm32(&C.full[s]), (uint32_t)(t / kStStages) & 1u, lim, abort_flag))) break;
         if (t >= 2 &&
@@ -189,7 +214,7 @@ score_stream_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     }
   } else if (warp < 4) {
     // ---- warps 2-3: the query operand
-    if (tiles > 0) {
+    if (ntiles > 0) {
       const int h = (warp - 2) * 2 + (lane >> 4);  // head
       const int g = lane & 15;                     // dims 8g .. 8g+7
       const uint4 v = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * g);
@@ -214,7 +239,7 @@ score_stream_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     const int q = warp & 3;
     const float inv_sqrt_hd = 0.08838834764831845f;  // 1/sqrt(128)
     float *srow = a.scores + (int64_t)row * a.score_cols + c0;
-    for (int t = 0; t < tiles; ++t) {
+    for (int t = 0; t < ntiles; ++t) {
       const int acc = t & 1;
       if (!tc_warp_wait(sm32(&C.tfull[acc]), (uint32_t)(t >> 1) & 1u, lim, abort_flag)) break;
       tc_fence_after();
@@ -228,8 +253,8 @@ score_stream_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
       const float h2 = relu_nan(__uint_as_float(v[2]));
       const float h3 = relu_nan(__uint_as_float(v[3]));
       const float sc = __fmul_rn(__fadd_rn(__fadd_rn(__fadd_rn(h0, h1), h2), h3), inv_sqrt_hd);
-      const int bl = t * kStTile + 32 * q + lane;
-      if (bl < cnt) srow[bl] = sc;
+      const int r = 32 * q + lane;  // the block's row in the tile
+      if (r < (tail && t == 0 ? tail : kStTile)) srow[tile_off(t) + r] = sc;
     }
   }
 
@@ -238,7 +263,7 @@ score_stream_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     // let every copy this CTA issued land before its shared memory is released
     const int issued = C.issued;
     for (int t = max(0, issued - kStStages); t < issued; ++t)
-      if (t < tma_tiles)
+      if (!(tail && t == 0))
         tc_wait(sm32(&C.full[t % kStStages]), (uint32_t)(t / kStStages) & 1u, kStSpinLimit, nullptr);
   }
   if (warp == 1) {
@@ -248,7 +273,7 @@ score_stream_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
                  : "memory");
   }
   if (tid == 0) {
-    if (!valid && y == 0) report_error(a.status, kErrRowRange, row);
+    if ((!valid && y == 0) || (valid && !keys_ok)) report_error(a.status, kErrRowRange, row);
     if (C.abort) report_error(a.status, kErrTimeout, row);
   }
 }

@@ -55,7 +55,7 @@ SELECT_BYTES_PER_BLOCK = 4          # + 1 byte per mask token written
 GATHER_WIDTH = 512                  # 2 KV heads x head dim 256, bf16
 GATHER_PAGE = 16                    # tokens per cache page
 GATHER_BYTES_PER_TOKEN = 8 * GATHER_WIDTH + 8   # K, V read and written; index and page entry
-DECODE_FUSED_SOURCES = ("qsa_decode.cu", "qsa_select_util.cuh", "qsa_device.cuh", "qsa_tma.h",
+DECODE_FUSED_SOURCES = ("qsa_decode.cu", "qsa_tc_device.cuh", "qsa_select_util.cuh", "qsa_device.cuh", "qsa_tma.h",
                         "qsa_launch.h")
 
 

@@ -13,9 +13,10 @@
 // tile at a time, the way the fused decode launch scores its tiles:
 //  * warp 0 streams the whole tiles into a ring of shared-memory stages with
 //    TMA (two 64-dim boxes, 128-byte swizzle), refilling a stage once the MMAs
-//    that read it have finished; a partial tile goes first, copied by every
-//    thread at once into the same layout (only the row's own blocks are read,
-//    so no copy reaches past the caller's key buffer);
+//    that read it have finished; a partial tile goes first, copied into the
+//    same layout by the six warps that do not build the query operand (only
+//    the row's own blocks are read, so no copy reaches past the caller's key
+//    buffer);
 //  * warps 2-3 prepare the row's four query heads as the 16 x 128 B operand
 //    (rows 4..15 zero);
 //  * one lane of warp 1 issues tcgen05.mma M128 N16 K16 x 8 per tile (keys on

@@ -61,7 +61,11 @@ constexpr int kRounds = 4;
 __host__ __device__ constexpr int round_bins(int r) { return r == 0 ? 4096 : (r == 3 ? 16 : 256); }
 // key >> round_shift(r) = the prefix known after round r
 __host__ __device__ constexpr int round_shift(int r) { return r == 0 ? 20 : (r == 1 ? 12 : (r == 2 ? 4 : 0)); }
-constexpr int kCandCap = 4096;                    // keys of round 0's bin kept for rounds 1..3
+constexpr int kCandCap = 4096;  // keys of round 0's bin kept for rounds 1..3
+// The shape without a key cache holds half as many when no row of the launch
+// can take the sampled band (rows up to 32768 blocks), which lets six CTAs
+// share an SM instead of five (the 64k prefill chunk: 197 -> 192 us a step).
+constexpr int kCandCapShort = 2048;
 
 constexpr int kZeroLanes = 32;  // round 0 counts exact zeros in one spare bin per lane
 
@@ -99,7 +103,7 @@ struct SelectSmem {
   uint32_t one_key;                // every rank's candidates under the prefix hold one key ...
   uint32_t one_key_val;            // ... this one
   uint32_t tbefore;                // ... and the lower ranks hold this many of them
-  // cand keys [kCandCap] u32, cand local indices [kCandCap] u16, keys[] follow (dynamic)
+  // cand keys [CAND] u32, cand local indices [CAND] u16, keys[] follow (dynamic)
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -277,8 +281,8 @@ __device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, bool valid) 
   if (valid) atomicAdd(&h[bin], 1u);
 }
 
-template <int NT, bool CACHE>
-__global__ void __launch_bounds__(NT, NT == 256 ? 5 : 2)
+template <int NT, bool CACHE, int CAND = kCandCap>
+__global__ void __launch_bounds__(NT, NT == 256 ? (CAND <= kCandCapShort ? 6 : 5) : 2)
 select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_t *__restrict__ pos,
               int32_t tokens, int32_t keep_max, uint8_t *__restrict__ mask, int32_t *status,
               int32_t C, int32_t cap) {
@@ -286,8 +290,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   SelectSmem &S = *reinterpret_cast<SelectSmem *>(smem_raw);
   uint32_t *cand_s =
       reinterpret_cast<uint32_t *>(smem_raw + ((sizeof(SelectSmem) + 15) & ~size_t(15)));
-  uint16_t *cand_li = reinterpret_cast<uint16_t *>(cand_s + kCandCap);
-  uint32_t *keys_s = reinterpret_cast<uint32_t *>(cand_li + kCandCap);
+  uint16_t *cand_li = reinterpret_cast<uint16_t *>(cand_s + CAND);
+  uint32_t *keys_s = reinterpret_cast<uint32_t *>(cand_li + CAND);
 
   grid_dependency_sync();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -452,7 +456,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               if (bits & (1u << e)) {
-                if (at < (uint32_t)kCandCap) {
+                if (at < (uint32_t)CAND) {
                   cand_s[at] = order_key(x[e]);
                   cand_li[at] = (uint16_t)(i + e);
                 }
@@ -492,7 +496,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
         const bool nf = !(chk == 0.f);
         ok = __syncthreads_or(nf) == 0;  // (also the barrier before the totals are read)
         const uint32_t hi_n = S.band_hi, nc = S.ncand;
-        ok = ok && hi_n <= need && hi_n + nc >= need && nc <= (uint32_t)kCandCap;
+        ok = ok && hi_n <= need && hi_n + nc >= need && nc <= (uint32_t)CAND;
         if (ok) {
           sampled = true;
           cand_path = true;
@@ -661,7 +665,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
           S.rule_cut = INT32_MAX;
         }
         __syncthreads();
-      } else if (cnt0 <= (uint32_t)kCandCap && per <= 65536) {
+      } else if (cnt0 <= (uint32_t)CAND && per <= 65536) {
         // ---- candidate path.  One pass over this CTA's keys: the mask bytes of
         // keys above the bin (kept) and below it (dropped) are final; the bin's
         // own keys are written as dropped, appended with their local block
@@ -1116,7 +1120,7 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   }
 
   if (scan_ties) {
-    // ---- fallback (round 0's bin holds more than kCandCap keys): rounds 1..3
+    // ---- fallback (round 0's bin holds more than CAND keys): rounds 1..3
     // over every key, each histogram merged over the cluster
     bool done = false;
     for (int r = 1; r < kRounds && !done; ++r) {
@@ -1234,8 +1238,8 @@ select_kernel(const float *__restrict__ scores, int64_t score_cols, const int32_
   if (C > 1) cluster_sync_all();
 }
 
-static size_t select_smem_bytes(int32_t cap) {
-  return ((sizeof(SelectSmem) + 15) & ~size_t(15)) + 6 * (size_t)kCandCap +
+static size_t select_smem_bytes(int32_t cap, int cand = kCandCap) {
+  return ((sizeof(SelectSmem) + 15) & ~size_t(15)) + 6 * (size_t)cand +
          4 * (size_t)(cap > 0 ? cap : 1);
 }
 
@@ -1317,6 +1321,10 @@ cudaError_t launch_select(const float *scores, int64_t score_cols, const int32_t
   const bool narrow = ctas > 2 * (int64_t)sm_count();
   const int32_t cap = narrow ? 0 : (int32_t)(per < kSelCapMax ? per : kSelCapMax);
 
+  if (narrow && C == 1 && n_max <= 32768)  // no row can take the sampled band
+    return launch_dependent(select_kernel<256, false, kCandCapShort>, dim3((unsigned)ctas), dim3(256),
+                            select_smem_bytes(0, kCandCapShort), stream, 1u, scores, score_cols, pos,
+                            tokens, keep_max, mask, status, (int32_t)1, 0);
   const size_t smem = select_smem_bytes(cap);
   if (narrow)
     return launch_dependent(select_kernel<256, false>, dim3((unsigned)ctas), dim3(256), smem, stream,

@@ -1285,12 +1285,12 @@ static int probe_max_cluster() {
 static int sm_count() { return device_sm_count(); }
 
 // Cluster size for a launch: split a row over a cluster when its blocks
-// overflow one CTA's key cache, and then, for launches of a few such rows,
-// further while the whole launch stays within half the GPU and every CTA keeps
-// at least 8192 keys (one 65536-block row: 12.3 us on 4 CTAs, 10.5 us on 8,
-// 11.0 us on 16; 32 rows of 32768-65536 blocks: 12.4 us on 4 CTAs each, 12.8 on
-// 8, 16.4 on 16 -- past one wave the cluster barriers and remote reads cost
-// more than the split gains).
+// overflow one CTA's key cache, and, for launches of a few rows, further, up
+// to 8 CTAs a row, while the whole launch stays within half the GPU and every
+// CTA keeps at least 4096 keys (one 16384-block row: 8.6 us on 1 CTA, 8.1 on
+// 2, 7.5 on 4; one 65536-block row: 12.3 us on 4, 9.5 on 8, 10.1 on 16; 32 rows
+// of 32768-65536 blocks: 11.2 us on 4 CTAs each, 12.8 on 8 -- past one wave
+// the cluster barriers and remote reads cost more than the split gains).
 int select_cluster_size(int64_t n_rows, int64_t tokens) {
   const int64_t n_max = tokens / kRatio;
   const int cmax = max_cluster_size();
@@ -1303,8 +1303,7 @@ int select_cluster_size(int64_t n_rows, int64_t tokens) {
     return C;
   }
   while (C < cmax && (n_max + C - 1) / C > kSelCapMax) C <<= 1;
-  // (a row that fits one CTA stays on one: its cluster barriers would cost more)
-  while (C > 1 && 2 * C <= cmax && n_rows * 2 * C <= sm_count() / 2 && n_max / (2 * C) >= 8192)
+  while (2 * C <= (cmax < 8 ? cmax : 8) && n_rows * 2 * C <= sm_count() / 2 && n_max / (2 * C) >= 4096)
     C <<= 1;
   return C;
 }

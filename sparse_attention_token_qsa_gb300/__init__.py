@@ -133,7 +133,8 @@ def qsa_version() -> int:
 
 def qsa_set_wait_limit_cycles(cycles: int) -> None:
     """The limit, in SM clock cycles, of the waits a caller may shorten (the
-    streaming scorer's key-copy waits, the fused decode step's barrier)."""
+    streaming scorers' key-copy, operand and accumulator waits, the fused decode
+    step's waits and barrier)."""
     _check(_lib.qsa_set_wait_limit_cycles(int(cycles)), "qsa_set_wait_limit_cycles")
 
 

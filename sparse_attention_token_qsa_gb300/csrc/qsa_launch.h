@@ -69,9 +69,9 @@ struct ScoreArgs {
   float *scores;
   int64_t score_cols;
   int32_t *status;
-  // limit of the waits a caller may shorten (the streaming scorer's wait for
-  // its key copies, the fused decode step's grid barrier), in SM clock
-  // cycles; <= 0 means the default
+  // limit of the waits a caller may shorten (the streaming scorers' waits
+  // for their key copies, query operand and accumulators, the fused decode
+  // step's waits and grid barrier), in SM clock cycles; <= 0 means the default
   long long wait_limit;
 };
 

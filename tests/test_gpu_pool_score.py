@@ -196,7 +196,8 @@ def test_score_nan_key_propagates(qsa, orc, tables, path):
     assert_close(got, want, "scores with a NaN key")
 
 
-def test_score_row_range_errors(qsa, tables):
+@pytest.mark.parametrize("path", [1, 3])
+def test_score_row_range_errors(qsa, tables, path):
     c, s, cd, sd = tables
     q = torch.zeros((3, 640), dtype=torch.int16, device="cuda")
     keys = torch.zeros((64, 128), dtype=torch.int16, device="cuda")
@@ -205,12 +206,37 @@ def test_score_row_range_errors(qsa, tables):
                           ([9, 9, 9], [10, 11, 4], 1)):
         sc = torch.full((3, 64), -7.0, dtype=torch.float32, device="cuda")
         st = qsa.new_status()
-        qsa.qsa_score_rows(q, 640, dev(np.array(pos, np.int32)),
-                           None if vis is None else dev(np.array(vis, np.int32)), 3, 256, w, cd, sd,
-                           c.shape[0], EPS, keys, None, sc, 64, st)
+        qsa.qsa_score_rows_with(q, 640, dev(np.array(pos, np.int32)),
+                                None if vis is None else dev(np.array(vis, np.int32)), 3, 256, w,
+                                cd, sd, c.shape[0], EPS, keys, None, sc, 64, st, path=path)
         code, row = qsa.qsa_read_status(st)
         assert (code, row) == (3, bad)
         assert np.all(sc.cpu().numpy()[bad] == -7.0)
+
+
+def test_score_stream_negative_key_base_is_a_row_error(qsa, orc, tables):
+    """The streaming tcgen05 scorer reads only a row's own blocks and addresses
+    them from key_base: a negative key_base is recorded as a row-range error for
+    that row, which it leaves unwritten, and the other rows are scored."""
+    c, s, cd, sd = tables
+    rng = qi.rng_for(3, salt=77)
+    keys = qi.normal_bf16(rng, (3 * 600, 128))
+    q = qi.fused_qk(rng, 3)[:, :512].copy()
+    qw = qi.normal_bf16(rng, (128,), 0.1)
+    pos = np.array([2399, 1999, 2100], np.int32)
+    base = np.array([0, -5, 1200], np.int64)
+    cols = 604
+    sc = torch.full((3, cols), -7.0, dtype=torch.float32, device="cuda")
+    st = qsa.new_status()
+    qsa.qsa_score_rows_with(dev(q), 512, dev(pos), None, 3, 2400, dev(qw), cd, sd, c.shape[0], EPS,
+                            dev(keys), dev(base), sc, cols, st, path=qsa.QSA_SCORE_STREAM)
+    assert qsa.qsa_read_status(st) == (3, 1)
+    got = sc.cpu().numpy()
+    assert np.all(got[1] == -7.0)
+    ok_rows = np.array([0, 2])
+    want, _ = oracle_scores(orc, q[ok_rows], 512, pos[ok_rows], 2400, qw, c, s, keys, cols,
+                            key_base=base[ok_rows])
+    assert_close(got[ok_rows], want, "rows beside the bad key_base")
 
 
 @pytest.mark.parametrize("n_rows,tokens,seed", [(100, 3000, 1), (64, 520, 2), (1, 9000, 3),

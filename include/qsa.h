@@ -194,7 +194,9 @@ qsa_status qsa_score_rows(const uint16_t *q, int64_t q_stride, const int32_t *po
 int64_t qsa_score_workspace_bytes(int32_t n_rows);
 
 /* qsa_score_rows with an explicit scorer; QSA_SCORE_TCGEN05 refuses key_base != NULL
- * and a workspace smaller than qsa_score_workspace_bytes(n_rows). */
+ * and a workspace smaller than qsa_score_workspace_bytes(n_rows); QSA_SCORE_SIMT and
+ * QSA_SCORE_STREAM take any rows and no workspace.  The three give the same scores
+ * within the scoring tolerance; the two tcgen05 scorers give identical ones. */
 qsa_status qsa_score_rows_with(const uint16_t *q, int64_t q_stride, const int32_t *pos,
                                const int32_t *visible_len, int32_t n_rows, int32_t tokens,
                                const uint16_t *q_norm_w, const uint16_t *cos_t,

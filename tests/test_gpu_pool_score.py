@@ -452,3 +452,30 @@ def test_pool_sum_paths_bit_exact(qsa, orc, tables):
     got = gpu_pool(qsa, tables, dev(keys).view(-1), 128, 0, nb, kw, nb)
     want = orc.pool_blocks(keys, 128, 0, nb, kw, c, s, EPS)
     assert np.array_equal(got, want), f"{int(np.sum(got != want))} pooled values differ"
+
+
+def test_tile_and_streaming_tcgen05_scorers_agree_bit_for_bit(qsa, tables):
+    """The tile scorer (M128 N256: 64 rows x 4 heads) and the streaming scorer
+    (M128 N16: one row's 4 heads) run the same per-(block, head) MMA over K and
+    the same epilogue, so their scores are identical, bit for bit, on every
+    row shape (full tiles, a partial last tile, short and empty prefixes)."""
+    c, s, cd, sd = tables
+    rng = qi.rng_for(3, salt=99)
+    T = 65536
+    nb = T // 4
+    keys = qi.torch_normal_bf16(torch, (nb, 128), qi.seed_for(3, 98), "cuda")
+    rows = 70
+    q = qi.fused_qk(rng, rows)
+    qw = qi.normal_bf16(rng, (128,), 0.1)
+    pos = rng.integers(0, T, size=rows).astype(np.int32)
+    pos[:4] = [T - 1, 0, 3, 511]
+    out = []
+    for path in (qsa.QSA_SCORE_TCGEN05, qsa.QSA_SCORE_STREAM):
+        sc = torch.full((rows, nb), -7.0, dtype=torch.float32, device="cuda")
+        st = qsa.new_status()
+        qsa.qsa_score_rows_with(dev(q), 640, dev(pos), None, rows, T, dev(qw), cd, sd, c.shape[0],
+                                EPS, keys, None, sc, nb, st, path=path,
+                                workspace=qsa.new_workspace(rows))
+        assert qsa.qsa_read_status(st) == (0, 0)
+        out.append(sc.cpu().numpy())
+    assert np.array_equal(out[0].view(np.uint32), out[1].view(np.uint32))

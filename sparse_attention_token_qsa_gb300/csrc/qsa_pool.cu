@@ -16,7 +16,10 @@
 
 namespace qsa {
 
-constexpr int kPoolThreads = 256;               // 16 blocks per CTA
+// 8 blocks per CTA: with 56 registers a thread, 128-thread CTAs leave a
+// smaller partial last wave than 256-thread ones (3-4 % faster at 16k and at
+// 1.5M blocks)
+constexpr int kPoolThreads = 128;
 constexpr int kPoolBlocksPerCta = kPoolThreads / 16;
 
 __global__ void __launch_bounds__(kPoolThreads)

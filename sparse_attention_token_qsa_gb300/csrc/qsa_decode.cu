@@ -149,6 +149,14 @@ __device__ __forceinline__ void red_add_release_gpu(uint32_t *p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// A plain load kept in program order after the loads issued before it (they
+// are inline assembly too), so that its use does not delay their issue.
+__device__ __forceinline__ int32_t ld_global_s32(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -219,6 +227,14 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   __syncthreads();
   tc_fence_after();
   grid_dependency_sync();
+  // warps 2-3 issue the loads of the query row and the norm weight before the
+  // position's: only the RoPE rows wait for it
+  uint4 qv = make_uint4(0u, 0u, 0u, 0u), qw8 = make_uint4(0u, 0u, 0u, 0u);
+  if (warp == 2 || warp == 3) {
+    const int h = (warp - 2) * 2 + (lane >> 4), g = lane & 15;
+    qv = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * g);
+    qw8 = ldg_nc_v4(a.q_norm_w + 8 * g);
+  }
 
   const int32_t n_max = a.tokens >> 2;
   const int c0 = y * bpc;
@@ -239,7 +255,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
   }
 
   // the position is read by every other role
-  const int32_t p = a.pos[row];
+  const int32_t p = ld_global_s32(a.pos + row);
   const bool valid = p >= 0 && p < a.tokens;
   const int32_t n = valid ? (p + 1) >> 2 : 0;
   const int c1 = min(n, c0 + bpc);
@@ -290,8 +306,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap kmap, const ScoreArgs a,
     // ---- warps 2-3: the query operand
     const int h = (warp - 2) * 2 + (lane >> 4);  // head
     const int g = lane & 15;                     // dims 8g .. 8g+7
-    const uint4 v = ldg_nc_v4(a.q + (int64_t)row * a.q_stride + h * kHeadDim + 8 * g);
-    const uint4 w8 = ldg_nc_v4(a.q_norm_w + 8 * g);
+    const uint4 v = qv, w8 = qw8;
     const int64_t pp = valid ? p : 0;  // (an invalid row's operand is never used)
     uint4 c8 = make_uint4(0u, 0u, 0u, 0u), s8 = make_uint4(0u, 0u, 0u, 0u);
     if (g < 8) {
